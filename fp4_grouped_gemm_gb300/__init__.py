@@ -1,0 +1,192 @@
+"""Block-scaled low-precision (MXFP8 / NVFP4) grouped GEMM for MoE on GB300.
+
+A thin Python binding over libhq.so's C ABI (include/hq.h).  Every function
+here only marshals arguments -- device pointers, sizes and the current CUDA
+stream -- and calls the entry point of the same name; all computation runs in
+the library's sm_103a kernels.  Outputs may be passed in (written in place) or
+are allocated here with torch, which serves only as the device-memory and
+stream provider.  A non-zero status from the library raises HQError.
+"""
+
+import ctypes
+
+import torch
+
+from . import _abi
+from ._abi import (HQ_MXFP8, HQ_NVFP4, HQ_STATUS_WAIT_TIMEOUT, HQ_STATUS_MASK_CLAMPED,  # noqa: F401
+                   HQ_STATUS_BAD_OFFSETS, HQ_STATUS_TOKENS_CLAMPED)
+
+__all__ = [
+    "HQError", "mode_id", "group_size", "sf_bytes", "capabilities", "get_device_status",
+    "set_wait_limit_ns", "selftest_wait_expiry", "set_gemm_tile_n", "hq_quant",
+    "hq_gemm_dense", "hq_gemm_grouped_contig", "hq_gemm_grouped_masked", "hq_swiglu_quant",
+    "hq_gemm_dswiglu", "hq_gemm_dswiglu_workspace_size", "swiglu_kb_dim",
+]
+
+_MODES = {"mxfp8": HQ_MXFP8, "w8a8-mxfp8": HQ_MXFP8, "nvfp4": HQ_NVFP4, "w4a4-nvfp4": HQ_NVFP4,
+          HQ_MXFP8: HQ_MXFP8, HQ_NVFP4: HQ_NVFP4}
+
+
+class HQError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        msg = _abi.load().hq_status_string(status).decode()
+        super().__init__(f"{where}: {msg}")
+
+
+def _check(status, where):
+    if status != 0:
+        raise HQError(status, where)
+
+
+def mode_id(mode):
+    try:
+        return _MODES[mode]
+    except KeyError:
+        raise ValueError(f"unknown mode {mode!r}") from None
+
+
+def group_size(mode):
+    return 32 if mode_id(mode) == HQ_MXFP8 else 16
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def sf_bytes(rows, k, mode):
+    return _abi.load().hq_sf_bytes(rows, k, mode_id(mode))
+
+
+def capabilities():
+    caps = _abi.Capabilities()
+    _check(_abi.load().hq_capabilities(ctypes.byref(caps)), "hq_capabilities")
+    return {name: getattr(caps, name) for name, _ in caps._fields_}
+
+
+def get_device_status(clear=True, stream=None):
+    """(status word, return code) after the stream's queued work completes."""
+    v = ctypes.c_uint32(0)
+    rc = _abi.load().hq_get_device_status(ctypes.byref(v), 1 if clear else 0, _stream(stream))
+    if rc not in (0, _abi.HQ_ERR_TIMEOUT):
+        raise HQError(rc, "hq_get_device_status")
+    return v.value, rc
+
+
+def set_wait_limit_ns(ns):
+    _check(_abi.load().hq_set_wait_limit_ns(int(ns)), "hq_set_wait_limit_ns")
+
+
+def selftest_wait_expiry(limit_ns, stream=None):
+    _check(_abi.load().hq_selftest_wait_expiry(int(limit_ns), _stream(stream)),
+           "hq_selftest_wait_expiry")
+
+
+def set_gemm_tile_n(tile_n):
+    _check(_abi.load().hq_set_gemm_tile_n(int(tile_n)), "hq_set_gemm_tile_n")
+
+
+def _q_shape(rows, k, mode):
+    return (rows, k) if mode_id(mode) == HQ_MXFP8 else (rows, k // 2)
+
+
+def hq_quant(x, mode, use_swizzle=True, global_scale=None, q_out=None, sf_out=None,
+             use_pdl=False, stream=None):
+    """Group-wise quantiser.  x: [m, k] BF16 CUDA tensor.  Returns (q, sf)."""
+    m, k = x.shape
+    if q_out is None:
+        q_out = torch.empty(_q_shape(m, k, mode), dtype=torch.uint8, device=x.device)
+    if sf_out is None:
+        sf_out = torch.empty(max(sf_bytes(m, k, mode), 1), dtype=torch.uint8, device=x.device)
+    rc = _abi.load().hq_quant(_ptr(x), m, k, mode_id(mode), 1 if use_swizzle else 0,
+                              _ptr(global_scale), _ptr(q_out), _ptr(sf_out), 1 if use_pdl else 0,
+                              _stream(stream))
+    _check(rc, "hq_quant")
+    return q_out, sf_out
+
+
+def hq_gemm_dense(a, sfa, b, sfb, m, n, k, mode, alpha=None, bias=None, out=None, sm_count=-1,
+                  use_pdl=False, stream=None):
+    if out is None:
+        out = torch.empty(m, n, dtype=torch.bfloat16, device=a.device)
+    rc = _abi.load().hq_gemm_dense(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(alpha),
+                                   _ptr(bias), _ptr(out), m, n, k, mode_id(mode), sm_count,
+                                   1 if use_pdl else 0, _stream(stream))
+    _check(rc, "hq_gemm_dense")
+    return out
+
+
+def hq_gemm_grouped_contig(a, sfa, b, sfb, padded_offsets, m_rows, n, k, mode, alpha=None,
+                           bias=None, out=None, sm_count=-1, stream=None):
+    if out is None:
+        out = torch.empty(m_rows, n, dtype=torch.bfloat16, device=a.device)
+    rc = _abi.load().hq_gemm_grouped_contig(
+        _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(padded_offsets), padded_offsets.numel(),
+        _ptr(alpha), _ptr(bias), _ptr(out), m_rows, n, k, mode_id(mode), sm_count,
+        _stream(stream))
+    _check(rc, "hq_gemm_grouped_contig")
+    return out
+
+
+def hq_gemm_grouped_masked(a, sfa, b, sfb, masked_m, max_m, n, k, mode, alpha=None, bias=None,
+                           out=None, sm_count=-1, stream=None):
+    E = masked_m.numel()
+    if out is None:
+        out = torch.empty(E * max_m, n, dtype=torch.bfloat16, device=a.device)
+    rc = _abi.load().hq_gemm_grouped_masked(
+        _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(masked_m), E, max_m, _ptr(alpha),
+        _ptr(bias), _ptr(out), n, k, mode_id(mode), sm_count, _stream(stream))
+    _check(rc, "hq_gemm_grouped_masked")
+    return out
+
+
+def swiglu_kb_dim(H, mode):
+    return -(-H // 512) * 16 if mode_id(mode) == HQ_MXFP8 else H // 16
+
+
+def hq_swiglu_quant(x, mode, token_nums=None, rows_per_expert=0, global_scale=None, q_out=None,
+                    sf_out=None, stream=None):
+    """Fused SwiGLU + requantisation.  x: [rows, 2H] BF16 ([gate | up])."""
+    rows, two_h = x.shape
+    H = two_h // 2
+    if q_out is None:
+        q_out = torch.empty(_q_shape(rows, H, mode), dtype=torch.uint8, device=x.device)
+    if sf_out is None:
+        nbytes = -(-rows // 128) * 128 * swiglu_kb_dim(H, mode)
+        sf_out = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=x.device)
+    E = token_nums.numel() if token_nums is not None else 0
+    rc = _abi.load().hq_swiglu_quant(_ptr(x), rows, H, _ptr(token_nums), E, rows_per_expert,
+                                     mode_id(mode), _ptr(global_scale), _ptr(q_out), _ptr(sf_out),
+                                     _stream(stream))
+    _check(rc, "hq_swiglu_quant")
+    return q_out, sf_out
+
+
+def hq_gemm_dswiglu_workspace_size(L, n):
+    return _abi.load().hq_gemm_dswiglu_workspace_size(L, n)
+
+
+def hq_gemm_dswiglu(a, b, c, padded_offsets, alpha, beta, prob, dprob, dbias=None, d_row=None,
+                    workspace=None, sm_count=-1, stream=None):
+    """BF16 grouped GEMM + dSwiGLU.  dprob (and dbias) accumulate (+=)."""
+    m, k = a.shape
+    L, n, _ = b.shape
+    if d_row is None:
+        d_row = torch.empty(m, 2 * n, dtype=torch.bfloat16, device=a.device)
+    ws_bytes = 0
+    if dbias is not None:
+        ws_bytes = hq_gemm_dswiglu_workspace_size(L, n)
+        if workspace is None:
+            workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=a.device)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    rc = _abi.load().hq_gemm_dswiglu(
+        _ptr(a), _ptr(b), _ptr(c), _ptr(padded_offsets), L, _ptr(alpha), _ptr(beta), _ptr(prob),
+        _ptr(d_row), _ptr(dprob), _ptr(dbias), m, n, k, _ptr(workspace), ws_bytes, sm_count,
+        _stream(stream))
+    _check(rc, "hq_gemm_dswiglu")
+    return d_row, dprob, dbias

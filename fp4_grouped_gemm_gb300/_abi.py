@@ -1,0 +1,86 @@
+"""ctypes declarations of libhq.so's C ABI (see include/hq.h).
+
+The library must have been built (``fp4_grouped_gemm_gb300.build.build()``);
+loading fails loudly otherwise -- there is no fallback implementation.
+"""
+
+import ctypes
+import os
+
+from . import build as _build
+
+c_i32 = ctypes.c_int32
+c_i64 = ctypes.c_int64
+c_u32 = ctypes.c_uint32
+c_u64 = ctypes.c_uint64
+c_sz = ctypes.c_size_t
+c_p = ctypes.c_void_p
+
+HQ_MXFP8 = 0
+HQ_NVFP4 = 2
+
+HQ_OK = 0
+HQ_ERR_INVALID = 1
+HQ_ERR_UNSUPPORTED = 2
+HQ_ERR_CUDA = 3
+HQ_ERR_TIMEOUT = 4
+
+HQ_STATUS_WAIT_TIMEOUT = 0x1
+HQ_STATUS_MASK_CLAMPED = 0x2
+HQ_STATUS_BAD_OFFSETS = 0x4
+HQ_STATUS_TOKENS_CLAMPED = 0x8
+
+
+class Capabilities(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int) for name in (
+        "abi_version", "sfatom_rows", "sfatom_cols", "sfatom_bytes", "group_mxfp8",
+        "group_nvfp4", "contig_row_align", "tile_m", "ptr_align_bytes", "max_groups",
+        "glu_block")]
+
+
+# name -> (restype, argtypes)
+SIGNATURES = {
+    "hq_capabilities": (c_i32, [ctypes.POINTER(Capabilities)]),
+    "hq_status_string": (ctypes.c_char_p, [c_i32]),
+    "hq_sf_bytes": (c_sz, [c_i64, c_i64, c_i32]),
+    "hq_get_device_status": (c_i32, [ctypes.POINTER(c_u32), c_i32, c_p]),
+    "hq_set_wait_limit_ns": (c_i32, [c_u64]),
+    "hq_selftest_wait_expiry": (c_i32, [c_u64, c_p]),
+    "hq_set_gemm_tile_n": (c_i32, [c_i32]),
+    "hq_quant": (c_i32, [c_p, c_i64, c_i64, c_i32, c_i32, c_p, c_p, c_p, c_i32, c_p]),
+    "hq_gemm_dense": (c_i32, [c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_i32,
+                              c_i32, c_i32, c_p]),
+    "hq_gemm_grouped_contig": (c_i32, [c_p, c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_p, c_i64,
+                                       c_i64, c_i64, c_i32, c_i32, c_p]),
+    "hq_gemm_grouped_masked": (c_i32, [c_p, c_p, c_p, c_p, c_p, c_i32, c_i64, c_p, c_p, c_p,
+                                       c_i64, c_i64, c_i32, c_i32, c_p]),
+    "hq_swiglu_quant": (c_i32, [c_p, c_i64, c_i64, c_p, c_i32, c_i64, c_i32, c_p, c_p, c_p, c_p]),
+    "hq_gemm_dswiglu": (c_i32, [c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_p, c_p, c_p, c_p, c_i64,
+                                c_i64, c_i64, c_p, c_sz, c_i32, c_p]),
+    "hq_gemm_dswiglu_workspace_size": (c_sz, [c_i32, c_i64]),
+}
+
+_LIB = None
+
+
+def lib_path():
+    return _build.LIB_PATH
+
+
+def load():
+    """Load libhq.so and declare its signatures (raises if it was not built)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build the CUDA library first "
+            "(python -c 'import fp4_grouped_gemm_gb300.build as b; b.build()')")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib

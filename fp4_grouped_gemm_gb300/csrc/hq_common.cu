@@ -1,0 +1,183 @@
+// hq_common.cu -- library-wide state and small entry points: the device status
+// word, capability constants, status strings, scale-buffer sizing, the
+// bounded-wait self-test, tensor-map encoding and per-device caches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "hq_internal.h"
+#include "hq_ptx.cuh"
+
+namespace hq {
+
+// One 32-bit status word per device that loads the library.  Kernels receive
+// its device address as an argument (resolved per device below).
+__device__ uint32_t g_status_word;
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+uint32_t* g_status_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+std::atomic<uint64_t> g_wait_limit_ns{1000000000ull};
+std::atomic<int> g_tile_n{0};
+using EncodeFn = decltype(&cuTensorMapEncodeTiled);
+EncodeFn g_encode = nullptr;
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+}  // namespace
+
+uint32_t* status_word_ptr() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(); }
+
+int forced_tile_n() { return g_tile_n.load(); }
+
+int num_sms() {
+  const int dev = current_device();
+  if (dev < 0) return 0;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sms[dev] = n;
+  }
+  return g_sms[dev];
+}
+
+int encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, void* base,
+                      const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                      CUtensorMapSwizzle swizzle) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return HQ_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeFn>(fn);
+    }
+  }
+  cuuint64_t gdim[5];
+  cuuint64_t gstride[4];
+  cuuint32_t bdim[5];
+  cuuint32_t estride[5];
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bdim[i] = box[i];
+    estride[i] = 1;
+    if (i > 0) gstride[i - 1] = strides_bytes[i - 1];
+  }
+  CUresult r = g_encode(map, dtype, rank, base, gdim, gstride, bdim, estride,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? HQ_OK : HQ_ERR_CUDA;
+}
+
+// Waits on an mbarrier that nothing arrives on; the bounded wait expires.
+__global__ void selftest_wait_kernel(uint32_t* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    WaitCtx w{status, &abort_flag, limit_ns};
+    wait_bounded(smem_u32(&bar), 0, w);
+  }
+  __syncthreads();
+}
+
+}  // namespace hq
+
+extern "C" {
+
+int hq_capabilities(hq_capabilities_t* out) {
+  if (!out) return HQ_ERR_INVALID;
+  out->abi_version = 1;
+  out->sfatom_rows = 128;
+  out->sfatom_cols = 4;
+  out->sfatom_bytes = 512;
+  out->group_mxfp8 = 32;
+  out->group_nvfp4 = 16;
+  out->contig_row_align = 256;
+  out->tile_m = 128;
+  out->ptr_align_bytes = 16;
+  out->max_groups = 1024;
+  out->glu_block = 32;
+  return HQ_OK;
+}
+
+const char* hq_status_string(int status) {
+  switch (status) {
+    case HQ_OK: return "HQ_OK";
+    case HQ_ERR_INVALID: return "HQ_ERR_INVALID: invalid argument (pointer, shape, stride or alignment)";
+    case HQ_ERR_UNSUPPORTED: return "HQ_ERR_UNSUPPORTED: valid request not supported by this library";
+    case HQ_ERR_CUDA: return "HQ_ERR_CUDA: a CUDA call failed";
+    case HQ_ERR_TIMEOUT: return "HQ_ERR_TIMEOUT: a bounded pipeline wait expired on the device";
+    default: return "unknown hq status";
+  }
+}
+
+size_t hq_sf_bytes(int64_t rows, int64_t k, hq_mode mode) {
+  int64_t gs = mode == HQ_MXFP8 ? 32 : (mode == HQ_NVFP4 ? 16 : 0);
+  if (gs == 0 || rows < 0 || k <= 0 || k % (4 * gs) != 0) return 0;
+  return static_cast<size_t>((rows + 127) / 128 * 128) * static_cast<size_t>(k / gs);
+}
+
+int hq_get_device_status(uint32_t* out, int clear, hq_stream_t s) {
+  if (!out) return HQ_ERR_INVALID;
+  uint32_t* p = hq::status_word_ptr();
+  if (!p) return HQ_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, p, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return HQ_ERR_CUDA;
+  if (clear && cudaMemsetAsync(p, 0, sizeof(uint32_t), st) != cudaSuccess) return HQ_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return HQ_ERR_CUDA;
+  *out = v;
+  return (v & HQ_STATUS_WAIT_TIMEOUT) ? HQ_ERR_TIMEOUT : HQ_OK;
+}
+
+int hq_set_wait_limit_ns(uint64_t ns) {
+  if (ns == 0) return HQ_ERR_INVALID;
+  hq::g_wait_limit_ns.store(ns);
+  return HQ_OK;
+}
+
+int hq_set_gemm_tile_n(int tile_n) {
+  if (tile_n != 0 && tile_n != 128 && tile_n != 256) return HQ_ERR_INVALID;
+  hq::g_tile_n.store(tile_n);
+  return HQ_OK;
+}
+
+int hq_selftest_wait_expiry(uint64_t limit_ns, hq_stream_t s) {
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return HQ_ERR_INVALID;
+  uint32_t* status = hq::status_word_ptr();
+  if (!status) return HQ_ERR_CUDA;
+  hq::selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(s)>>>(status, limit_ns);
+  return cudaGetLastError() == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,493 @@
+// hq_gemm_bs.cu -- block-scaled GEMMs (MXFP8 and NVFP4) on 5th-generation
+// tensor cores: out = alpha_g * (A . B_g^T) + bias_g, BF16 output.
+//
+// One persistent kernel serves the dense, grouped-contiguous and
+// grouped-masked problems (HALOps "GEMM" API dense_gemm / group_masked_gemm,
+// cuDNN frontend "Grouped GEMM + dGLU (SM100)" Step 1).  Per CTA:
+//   warp 0      TMA producer: A and B tiles (128-byte swizzled, K-major) and
+//               the matching 512-byte SfAtom scale atoms into a ring of
+//               shared-memory stages, completion tracked by mbarriers;
+//   warp 1      MMA issuer: copies each stage's scale atoms shared -> TMEM
+//               (tcgen05.cp 32x128b.warpx4) and issues block-scaled
+//               tcgen05.mma into a TMEM accumulator; owns the TMEM allocation;
+//   warps 2..5  epilogue: TMEM -> registers (tcgen05.ld), alpha/bias, BF16
+//               round-to-nearest-even, staged through shared memory and
+//               written as coalesced 16-byte row segments; rows outside the
+//               group's valid range are never written.
+// Tiles are 128 rows x BN columns; the tile sequence (n fastest inside each
+// 128-row block, so the CTAs of a wave share A rows and walk one expert's
+// weights together) is decoded identically by every role from device-resident
+// group information (padded_offsets or masked_m), validated on the device.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "hq_internal.h"
+#include "hq_ptx.cuh"
+#include "hq_sched.cuh"
+
+namespace hq {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kBKBytes = 128;   // bytes of K per stage and row (one 128B swizzle span)
+constexpr int kMmaKBytes = 32;  // bytes of K consumed by one MMA
+constexpr int kSmemLimit = 232448;
+
+struct GemmParams {
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  const float* alpha;        // [groups] or null
+  const uint16_t* bias;      // [groups, n] or null
+  uint16_t* out;             // [a_rows, n]
+  GroupSched gs;             // group layout (rows, offsets or masks, status word)
+  int64_t n, k;
+  int64_t S;                 // scale columns = k / group
+  int64_t sfb_group_bytes;   // ceil(n/128)*128*S
+  uint64_t wait_limit_ns;
+};
+
+template <int MODE, int BN, int STAGES, int ACC>
+struct Cfg {
+  static constexpr int GS = MODE == HQ_MXFP8 ? 32 : 16;
+  static constexpr int EPB = MODE == HQ_MXFP8 ? 1 : 2;            // elements per byte
+  static constexpr int BK = kBKBytes * EPB;                       // elements per stage
+  static constexpr int ATOMS = BK / GS / 4;                       // k-atoms per stage
+  static constexpr int RB = BN / 128;                             // 128-row blocks of B
+  static constexpr int A_BYTES = kBM * kBKBytes;
+  static constexpr int B_BYTES = BN * kBKBytes;
+  static constexpr int SFA_BYTES = ATOMS * 512;
+  static constexpr int SFB_BYTES = RB * ATOMS * 512;
+  static constexpr int SFA_COLS = (ATOMS * 4 + 7) / 8 * 8;         // padded to 8 columns
+  static constexpr int SFB_COLS = RB * ATOMS * 4;
+  static constexpr int SF_STAGE_COLS = (SFA_COLS + SFB_COLS + 15) / 16 * 16;
+  static constexpr int SF_BASE_COL = ACC * BN;
+  static constexpr int TMEM_USED = ACC * BN + STAGES * SF_STAGE_COLS;
+  static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64
+                                 : TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
+  static_assert(TMEM_USED <= 512, "TMEM budget");
+  // shared-memory layout (offsets from a 1024-aligned base)
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+  static constexpr int OFF_STAGE_OUT = OFF_SFB + STAGES * SFB_BYTES;  // 4 warps x 2 KB
+  static constexpr int OFF_TABLE = OFF_STAGE_OUT + 4 * 2048;          // 2 x (1024+1) int32
+  static constexpr int OFF_BAR = OFF_TABLE + 2 * (kMaxGroups + 1) * 4 + 8;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+  static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget");
+  static_assert(OFF_BAR % 8 == 0, "barrier alignment");
+  // instruction descriptor (block-scaled kinds): A/B K-major, M=128, N=BN
+  static constexpr uint32_t IDESC_BASE =
+      (MODE == HQ_MXFP8 ? ((0u << 7) | (0u << 10) | (1u << 23))   // E4M3 x E4M3, UE8M0
+                        : ((1u << 7) | (1u << 10) | (0u << 23)))  // E2M1 x E2M1, UE4M3
+      | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
+};
+
+template <int MODE, int BN, int STAGES, int ACC>
+__global__ void __launch_bounds__(kThreads, 1)
+    bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p) {
+  using C = Cfg<MODE, BN, STAGES, ACC>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  int32_t* tab0 = reinterpret_cast<int32_t*>(smem + C::OFF_TABLE);
+  int32_t* tab1 = tab0 + (kMaxGroups + 1);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + ACC + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * ACC);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  int64_t* total_mtiles_s = reinterpret_cast<int64_t*>(smem + C::OFF_MISC + 8);
+
+  if (warp == 0 && lane == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < ACC; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);
+    }
+    mbar_init(drain_bar, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  pdl_wait();  // inputs of a preceding kernel are visible after this point
+  if (warp == 2) build_table(p.gs, tab0, tab1, lane, total_mtiles_s);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  Schedule sch;
+  sch.n_tiles = static_cast<int>((p.n + BN - 1) / BN);
+  sch.total_tiles = *total_mtiles_s * sch.n_tiles;
+  sch.tab0 = tab0;
+  sch.tab1 = tab1;
+  const int num_kb = static_cast<int>((p.k + C::BK - 1) / C::BK);
+  const int atoms_total = static_cast<int>(p.S / 4);
+  const WaitCtx wctx{p.gs.status, abort_flag, p.wait_limit_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t filled_mask = 0, last_parity = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; ok && t < sch.total_tiles; t += gridDim.x) {
+        const TileInfo ti = decode_tile(p.gs, sch, t, BN);
+        const uint8_t* sfa_rows = p.sfa + (ti.row0 / kBM) * atoms_total * 512;
+        const uint8_t* sfb_grp = p.sfb + static_cast<int64_t>(ti.g) * p.sfb_group_bytes;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bounded(empty_bar(stage), phase ^ 1u, wctx)) { ok = false; break; }
+          int atoms = atoms_total - kb * C::ATOMS;
+          atoms = atoms < C::ATOMS ? atoms : C::ATOMS;
+          int rb_valid = static_cast<int>((p.n - ti.n0 + 127) / 128);
+          rb_valid = rb_valid < C::RB ? rb_valid : C::RB;
+          const uint32_t bytes = C::A_BYTES + C::B_BYTES + atoms * 512u * (1 + rb_valid);
+          mbar_arrive_expect_tx(full_bar(stage), bytes);
+          tma_load_2d(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, full_bar(stage),
+                      kb * kBKBytes, static_cast<int32_t>(ti.row0));
+          tma_load_3d(sbase + C::OFF_B + stage * C::B_BYTES, &tmB, full_bar(stage),
+                      kb * kBKBytes, ti.n0, ti.g);
+          bulk_load(sbase + C::OFF_SFA + stage * C::SFA_BYTES, sfa_rows + kb * C::ATOMS * 512,
+                    atoms * 512u, full_bar(stage));
+          for (int rb = 0; rb < rb_valid; ++rb) {
+            const uint8_t* src =
+                sfb_grp + ((ti.n0 / 128 + rb) * static_cast<int64_t>(atoms_total) + kb * C::ATOMS) * 512;
+            bulk_load(sbase + C::OFF_SFB + stage * C::SFB_BYTES + rb * C::ATOMS * 512, src,
+                      atoms * 512u, full_bar(stage));
+          }
+          filled_mask |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // every copy this thread issued has landed before the CTA may exit
+      for (int s = 0; s < STAGES; ++s)
+        if (filled_mask & (1u << s)) wait_drain(full_bar(s), (last_parity >> s) & 1u, p.wait_limit_ns);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; ok && t < sch.total_tiles; t += gridDim.x) {
+        const TileInfo ti = decode_tile(p.gs, sch, t, BN);
+        int rb_valid = static_cast<int>((p.n - ti.n0 + 127) / 128);
+        rb_valid = rb_valid < C::RB ? rb_valid : C::RB;
+        if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, wctx)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bounded(full_bar(stage), phase, wctx)) { ok = false; break; }
+          tc_fence_after();
+          int atoms = atoms_total - kb * C::ATOMS;
+          atoms = atoms < C::ATOMS ? atoms : C::ATOMS;
+          const uint32_t sfa_t = tmem_base + C::SF_BASE_COL + stage * C::SF_STAGE_COLS;
+          const uint32_t sfb_t = sfa_t + C::SFA_COLS;
+          const uint32_t sfa_s = sbase + C::OFF_SFA + stage * C::SFA_BYTES;
+          const uint32_t sfb_s = sbase + C::OFF_SFB + stage * C::SFB_BYTES;
+          for (int a = 0; a < atoms; ++a) {
+            tc_cp_32x128b_warpx4(sfa_t + a * 4, smem_desc_sfatom(sfa_s + a * 512));
+            for (int rb = 0; rb < rb_valid; ++rb)
+              tc_cp_32x128b_warpx4(sfb_t + (a * C::RB + rb) * 4,
+                                   smem_desc_sfatom(sfb_s + (rb * C::ATOMS + a) * 512));
+          }
+          const uint32_t a_s = sbase + C::OFF_A + stage * C::A_BYTES;
+          const uint32_t b_s = sbase + C::OFF_B + stage * C::B_BYTES;
+          const int n_mma = MODE == HQ_MXFP8 ? (kBKBytes / kMmaKBytes) : atoms;
+          for (int j = 0; j < n_mma; ++j) {
+            const uint64_t adesc = smem_desc_sw128(a_s + j * kMmaKBytes);
+            const uint64_t bdesc = smem_desc_sw128(b_s + j * kMmaKBytes);
+            const uint32_t acc_flag = (kb > 0 || j > 0) ? 1u : 0u;
+            if (MODE == HQ_MXFP8) {
+              // one scale per row per MMA: byte j of the atom's 32-bit columns
+              const uint32_t idesc = C::IDESC_BASE | (static_cast<uint32_t>(j) << 4) |
+                                     (static_cast<uint32_t>(j) << 29);
+              mma_mxf8(d_tmem, adesc, bdesc, idesc, sfa_t | (static_cast<uint32_t>(j) << 30),
+                       sfb_t | (static_cast<uint32_t>(j) << 30), acc_flag);
+            } else {
+              // four scales per row per MMA: one whole atom column group
+              mma_nvf4(d_tmem, adesc, bdesc, C::IDESC_BASE, sfa_t + j * 4,
+                       sfb_t + j * C::RB * 4, acc_flag);
+            }
+          }
+          tc_commit(empty_bar(stage));
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(tfull_bar(acc));
+        if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
+      }
+      // all tcgen05 work issued by this thread is complete before TMEM is freed
+      tc_commit(drain_bar);
+      wait_drain(drain_bar, 0, p.wait_limit_ns);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    uint8_t* stage_out = smem + C::OFF_STAGE_OUT + (warp - 2) * 2048;
+    const uint32_t stage_out_s = smem_u32(stage_out);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int64_t t = blockIdx.x; t < sch.total_tiles; t += gridDim.x) {
+      const TileInfo ti = decode_tile(p.gs, sch, t, BN);
+      // every lane waits; the warp proceeds only if all lanes saw completion
+      const bool ok = wait_bounded(tfull_bar(acc), acc_phase, wctx);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      tc_fence_after();
+      const float alpha = p.alpha ? __ldg(p.alpha + ti.g) : 1.0f;
+      const uint16_t* bias_row = p.bias ? p.bias + static_cast<int64_t>(ti.g) * p.n : nullptr;
+      const int rows_here = ti.rows_valid - q * 32;  // valid rows of this warp's quarter
+      for (int c = 0; c < BN / 32; ++c) {
+        const int col0 = ti.n0 + c * 32;
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c * 32, r);
+        tmem_ld_wait();
+        if (col0 >= p.n) continue;
+        float bias_v[32];
+        if (bias_row) {
+          const uint4* bp = reinterpret_cast<const uint4*>(bias_row + col0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 v = __ldg(bp + i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              bias_v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+              bias_v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) bias_v[i] = 0.0f;
+        }
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float v0 = __fadd_rn(__fmul_rn(alpha, __uint_as_float(r[2 * i])), bias_v[2 * i]);
+          const float v1 = __fadd_rn(__fmul_rn(alpha, __uint_as_float(r[2 * i + 1])), bias_v[2 * i + 1]);
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(v0, v1);
+          packed[i] = *reinterpret_cast<uint32_t*>(&b2);
+        }
+        // stage: row = lane, 4 x 16-byte chunks, chunk index xor-swizzled
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t off = lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage_out_s + off),
+                       "r"(packed[4 * j]), "r"(packed[4 * j + 1]), "r"(packed[4 * j + 2]),
+                       "r"(packed[4 * j + 3])
+                       : "memory");
+        }
+        __syncwarp();
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          const int rr = it * 8 + (lane >> 2);
+          const int j = lane & 3;
+          const uint32_t off = rr * 64 + ((j ^ ((rr >> 1) & 3)) * 16);
+          uint4 v;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                       : "r"(stage_out_s + off)
+                       : "memory");
+          if (rr < rows_here) {
+            uint16_t* dst = p.out + (ti.row0 + q * 32 + rr) * p.n + col0 + j * 8;
+            *reinterpret_cast<uint4*>(dst) = v;
+          }
+        }
+        __syncwarp();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  __syncthreads();
+  pdl_launch_dependents();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+template <int MODE, int BN, int STAGES, int ACC>
+int run_bs(const void* a, const void* b, const GemmParams& p0, int sm_count, bool pdl,
+           cudaStream_t st) {
+  using C = Cfg<MODE, BN, STAGES, ACC>;
+  GemmParams p = p0;
+  const uint64_t kbytes = static_cast<uint64_t>(p.k) / C::EPB;
+  CUtensorMap tmA, tmB;
+  {
+    const uint64_t dims[2] = {kbytes, static_cast<uint64_t>(p.gs.a_rows)};
+    const uint64_t strides[1] = {kbytes};
+    const uint32_t box[2] = {kBKBytes, kBM};
+    int rc = encode_tensor_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a), dims,
+                               strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != HQ_OK) return rc;
+  }
+  {
+    const uint64_t dims[3] = {kbytes, static_cast<uint64_t>(p.n), static_cast<uint64_t>(p.gs.groups)};
+    const uint64_t strides[2] = {kbytes, kbytes * static_cast<uint64_t>(p.n)};
+    const uint32_t box[3] = {kBKBytes, static_cast<uint32_t>(BN), 1};
+    int rc = encode_tensor_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(b), dims,
+                               strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != HQ_OK) return rc;
+  }
+  auto kern = bs_gemm_kernel<MODE, BN, STAGES, ACC>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+      cudaSuccess)
+    return HQ_ERR_CUDA;
+  const int sms = num_sms();
+  if (sms <= 0) return HQ_ERR_CUDA;
+  int64_t mtiles_bound;
+  if (p.gs.sched == kMasked)
+    mtiles_bound = static_cast<int64_t>(p.gs.groups) * ((p.gs.max_m + kBM - 1) / kBM);
+  else
+    mtiles_bound = (p.gs.a_rows + kBM - 1) / kBM;
+  const int64_t tiles_bound = mtiles_bound * ((p.n + BN - 1) / BN);
+  int64_t grid = sm_count > 0 ? sm_count : sms;
+  if (grid > sms) grid = sms;
+  if (grid > tiles_bound) grid = tiles_bound;
+  if (grid < 1) grid = 1;
+  cudaError_t e = launch(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), C::SMEM_BYTES, st,
+                         pdl, tmA, tmB, p);
+  return e == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
+}
+
+int run_gemm(hq_mode mode, const void* a, const void* b, const GemmParams& p, int sm_count,
+             bool pdl, cudaStream_t st) {
+  int bn = forced_tile_n();
+  if (bn == 0) bn = (p.n % 256 == 0) ? 256 : 128;
+  if (bn == 256 && p.n % 256 != 0 && p.n < 256) bn = 128;
+  if (mode == HQ_MXFP8) {
+    if (bn == 256) return run_bs<HQ_MXFP8, 256, 4, 1>(a, b, p, sm_count, pdl, st);
+    return run_bs<HQ_MXFP8, 128, 6, 2>(a, b, p, sm_count, pdl, st);
+  }
+  if (bn == 256) return run_bs<HQ_NVFP4, 256, 3, 1>(a, b, p, sm_count, pdl, st);
+  return run_bs<HQ_NVFP4, 128, 5, 2>(a, b, p, sm_count, pdl, st);
+}
+
+// Host-side checks shared by the three entry points.
+int check_common(const void* a, const uint8_t* sfa, const void* b, const uint8_t* sfb,
+                 const float* alpha, const hq_bf16* bias, const hq_bf16* out, int64_t n, int64_t k,
+                 hq_mode mode) {
+  if (mode != HQ_MXFP8 && mode != HQ_NVFP4) return HQ_ERR_INVALID;
+  const int64_t gs = mode == HQ_MXFP8 ? 32 : 16;
+  if (n <= 0 || k <= 0 || k % (4 * gs) != 0 || n % 128 != 0) return HQ_ERR_INVALID;
+  if (n > (1ll << 30) || k > (1ll << 30)) return HQ_ERR_INVALID;
+  if (!a || !sfa || !b || !sfb || !out) return HQ_ERR_INVALID;
+  if (!aligned16(a) || !aligned16(sfa) || !aligned16(b) || !aligned16(sfb) || !aligned16(out))
+    return HQ_ERR_INVALID;
+  if (bias && !aligned16(bias)) return HQ_ERR_INVALID;
+  if (alpha && (reinterpret_cast<uintptr_t>(alpha) & 3u)) return HQ_ERR_INVALID;
+  if (mode == HQ_NVFP4 && !alpha) return HQ_ERR_UNSUPPORTED;
+  if (mode == HQ_NVFP4 && bias) return HQ_ERR_UNSUPPORTED;
+  return HQ_OK;
+}
+
+GemmParams base_params(const uint8_t* sfa, const uint8_t* sfb, const float* alpha,
+                       const hq_bf16* bias, hq_bf16* out, int64_t n, int64_t k, hq_mode mode) {
+  GemmParams p{};
+  const int64_t gs = mode == HQ_MXFP8 ? 32 : 16;
+  p.sfa = sfa;
+  p.sfb = sfb;
+  p.alpha = alpha;
+  p.bias = bias;
+  p.out = out;
+  p.n = n;
+  p.k = k;
+  p.S = k / gs;
+  p.sfb_group_bytes = (n + 127) / 128 * 128 * (k / gs);
+  p.gs.status = status_word_ptr();
+  p.wait_limit_ns = wait_limit_ns();
+  return p;
+}
+
+}  // namespace
+}  // namespace hq
+
+extern "C" {
+
+int hq_gemm_dense(const void* a, const uint8_t* sfa, const void* b, const uint8_t* sfb,
+                  const float* alpha, const hq_bf16* bias, hq_bf16* out, int64_t m, int64_t n,
+                  int64_t k, hq_mode mode, int sm_count, int use_pdl, hq_stream_t s) {
+  int rc = hq::check_common(a, sfa, b, sfb, alpha, bias, out, n, k, mode);
+  if (rc != HQ_OK) return rc;
+  if (m < 0 || m > (1ll << 31) - 256) return HQ_ERR_INVALID;
+  if (m == 0) return HQ_OK;
+  hq::GemmParams p = hq::base_params(sfa, sfb, alpha, bias, out, n, k, mode);
+  if (!p.gs.status) return HQ_ERR_CUDA;
+  p.gs.a_rows = m;
+  p.gs.groups = 1;
+  p.gs.sched = hq::kDense;
+  return hq::run_gemm(mode, a, b, p, sm_count, use_pdl != 0, reinterpret_cast<cudaStream_t>(s));
+}
+
+int hq_gemm_grouped_contig(const void* a, const uint8_t* sfa, const void* b, const uint8_t* sfb,
+                           const int32_t* padded_offsets, int L, const float* alpha,
+                           const hq_bf16* bias, hq_bf16* out, int64_t m_rows, int64_t n,
+                           int64_t k, hq_mode mode, int sm_count, hq_stream_t s) {
+  int rc = hq::check_common(a, sfa, b, sfb, alpha, bias, out, n, k, mode);
+  if (rc != HQ_OK) return rc;
+  if (!padded_offsets || L < 1 || L > hq::kMaxGroups) return HQ_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(padded_offsets) & 3u) return HQ_ERR_INVALID;
+  if (m_rows < 0 || m_rows > (1ll << 31) - 256) return HQ_ERR_INVALID;
+  if (m_rows == 0) return HQ_OK;
+  hq::GemmParams p = hq::base_params(sfa, sfb, alpha, bias, out, n, k, mode);
+  if (!p.gs.status) return HQ_ERR_CUDA;
+  p.gs.a_rows = m_rows;
+  p.gs.groups = L;
+  p.gs.group_info = padded_offsets;
+  p.gs.sched = hq::kContig;
+  return hq::run_gemm(mode, a, b, p, sm_count, false, reinterpret_cast<cudaStream_t>(s));
+}
+
+int hq_gemm_grouped_masked(const void* a, const uint8_t* sfa, const void* b, const uint8_t* sfb,
+                           const int32_t* masked_m, int E, int64_t max_m, const float* alpha,
+                           const hq_bf16* bias, hq_bf16* out, int64_t n, int64_t k, hq_mode mode,
+                           int sm_count, hq_stream_t s) {
+  int rc = hq::check_common(a, sfa, b, sfb, alpha, bias, out, n, k, mode);
+  if (rc != HQ_OK) return rc;
+  if (!masked_m || E < 1 || E > hq::kMaxGroups) return HQ_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(masked_m) & 3u) return HQ_ERR_INVALID;
+  if (max_m <= 0 || max_m % 128 != 0) return HQ_ERR_INVALID;
+  if (static_cast<int64_t>(E) * max_m > (1ll << 31) - 256) return HQ_ERR_INVALID;
+  hq::GemmParams p = hq::base_params(sfa, sfb, alpha, bias, out, n, k, mode);
+  if (!p.gs.status) return HQ_ERR_CUDA;
+  p.gs.a_rows = static_cast<int64_t>(E) * max_m;
+  p.gs.groups = E;
+  p.gs.group_info = masked_m;
+  p.gs.max_m = max_m;
+  p.gs.sched = hq::kMasked;
+  return hq::run_gemm(mode, a, b, p, sm_count, false, reinterpret_cast<cudaStream_t>(s));
+}
+
+}  // extern "C"

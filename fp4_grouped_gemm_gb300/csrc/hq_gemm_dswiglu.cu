@@ -1,0 +1,392 @@
+// hq_gemm_dswiglu.cu -- BF16 grouped GEMM fused with the dSwiGLU backward
+// epilogue (cuDNN frontend "Grouped GEMM + dGLU (SM100)", BF16 contract,
+// act_func = "dswiglu", dense B).
+//
+//   R_g = alpha_g^2 A_g B_g^T  (tcgen05.mma kind::f16, BF16 x BF16 -> FP32 in TMEM)
+//   X_g = beta_g C_g, split into alternating 32-column gate / input blocks
+//   D_row[gate col]  = R prob input s (1 + gate (1 - s)),  s = sigmoid(gate)
+//   D_row[input col] = R prob gate s
+//   dprob[m]        += sum_j R gate s input
+//   dbias[g, c]     += sum_{m in g} D_row[m, c]
+//
+// Persistent warp-specialised kernel: warp 0 streams A / B tiles with TMA into
+// a ring of shared-memory stages, warp 1 issues the MMAs into one of two TMEM
+// accumulators (so the epilogue of tile i overlaps the main loop of tile i+1),
+// warps 2..5 run the epilogue.  A compact tile of 128 columns j maps to the
+// 256 C / D_row columns [2 j0, 2 j0 + 256).  Each epilogue thread owns one
+// row: it reads that row's C segment, writes its D_row segment, accumulates
+// its dprob partial (one float atomic per row and tile), and, when dbias is
+// requested, the warp transposes its fp32 D values through shared memory to
+// produce per-column partial sums that are added to a float32 workspace with
+// one atomic per column, warp and chunk.  A final pass adds the workspace
+// into the caller's BF16 dbias.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "hq_internal.h"
+#include "hq_ptx.cuh"
+#include "hq_sched.cuh"
+
+namespace hq {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kBN = 128;          // compact columns per tile
+constexpr int kBKElems = 64;      // BF16 elements of K per stage (128 bytes)
+constexpr int kStages = 5;
+constexpr int kAcc = 2;
+constexpr int kTmemCols = kAcc * kBN;
+constexpr int kABytes = kBM * kBKElems * 2;
+constexpr int kBBytes = kBN * kBKElems * 2;
+constexpr int kTransStride = 65;  // floats per row of the dbias transpose buffer
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + kStages * kABytes;
+constexpr int kOffTrans = kOffB + kStages * kBBytes;
+constexpr int kOffTable = kOffTrans + 4 * 32 * kTransStride * 4;
+constexpr int kOffBar = (kOffTable + 2 * (kMaxGroups + 1) * 4 + 15) / 16 * 16;
+constexpr int kNumBars = 2 * kStages + 2 * kAcc + 1;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+// kind::f16 instruction descriptor: D f32, A/B bf16, K-major, M=128, N=128
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                            (static_cast<uint32_t>(kBN >> 3) << 17) |
+                            (static_cast<uint32_t>(kBM >> 4) << 24);
+
+struct DsParams {
+  GroupSched gs;
+  const uint16_t* c;      // [m, 2n]
+  const float* alpha;     // [L]
+  const float* beta;      // [L]
+  const float* prob;      // [m]
+  uint16_t* d_row;        // [m, 2n]
+  float* dprob;           // [m]
+  float* dbias_ws;        // [L, 2n] float32 partial sums, or null
+  int64_t n, k;
+  uint64_t wait_limit_ns;
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    dswiglu_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const DsParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  int32_t* tab0 = reinterpret_cast<int32_t*>(smem + kOffTable);
+  int32_t* tab1 = tab0 + (kMaxGroups + 1);
+  const uint32_t bar0 = sbase + kOffBar;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + kAcc + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 2 * kAcc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  int64_t* total_mtiles_s = reinterpret_cast<int64_t*>(smem + kOffMisc + 8);
+
+  if (warp == 0 && lane == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < kAcc; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);
+    }
+    mbar_init(drain_bar, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 2) build_table(p.gs, tab0, tab1, lane, total_mtiles_s);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  Schedule sch;
+  sch.n_tiles = static_cast<int>((p.n + kBN - 1) / kBN);
+  sch.total_tiles = *total_mtiles_s * sch.n_tiles;
+  sch.tab0 = tab0;
+  sch.tab1 = tab1;
+  const int num_kb = static_cast<int>((p.k + kBKElems - 1) / kBKElems);
+  const WaitCtx wctx{p.gs.status, abort_flag, p.wait_limit_ns};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, filled_mask = 0, last_parity = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; ok && t < sch.total_tiles; t += gridDim.x) {
+        const TileInfo ti = decode_tile(p.gs, sch, t, kBN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bounded(empty_bar(stage), phase ^ 1u, wctx)) { ok = false; break; }
+          mbar_arrive_expect_tx(full_bar(stage), kABytes + kBBytes);
+          tma_load_2d(sbase + kOffA + stage * kABytes, &tmA, full_bar(stage), kb * kBKElems,
+                      static_cast<int32_t>(ti.row0));
+          tma_load_3d(sbase + kOffB + stage * kBBytes, &tmB, full_bar(stage), kb * kBKElems, ti.n0,
+                      ti.g);
+          filled_mask |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      for (int s = 0; s < kStages; ++s)
+        if (filled_mask & (1u << s)) wait_drain(full_bar(s), (last_parity >> s) & 1u, p.wait_limit_ns);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; ok && t < sch.total_tiles; t += gridDim.x) {
+        if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, wctx)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kBN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bounded(full_bar(stage), phase, wctx)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_s = sbase + kOffA + stage * kABytes;
+          const uint32_t b_s = sbase + kOffB + stage * kBBytes;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)  // 4 x K=16 per 128-byte swizzle row
+            mma_bf16(d_tmem, smem_desc_sw128(a_s + j * 32), smem_desc_sw128(b_s + j * 32), kIdesc,
+                     (kb > 0 || j > 0) ? 1u : 0u);
+          tc_commit(empty_bar(stage));
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(tfull_bar(acc));
+        if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
+      }
+      tc_commit(drain_bar);
+      wait_drain(drain_bar, 0, p.wait_limit_ns);
+    }
+  } else {
+    const int q = warp & 3;
+    float* trans = reinterpret_cast<float*>(smem + kOffTrans) + (warp - 2) * 32 * kTransStride;
+    const int64_t two_n = 2 * p.n;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int64_t t = blockIdx.x; t < sch.total_tiles; t += gridDim.x) {
+      const TileInfo ti = decode_tile(p.gs, sch, t, kBN);
+      const bool ok = wait_bounded(tfull_bar(acc), acc_phase, wctx);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      tc_fence_after();
+      const int r_local = q * 32 + lane;
+      const bool row_ok = r_local < ti.rows_valid;
+      const int64_t row = ti.row0 + r_local;
+      const float alpha = __ldg(p.alpha + ti.g);
+      const float a2 = __fmul_rn(alpha, alpha);
+      const float beta = __ldg(p.beta + ti.g);
+      const float prob = row_ok ? __ldg(p.prob + row) : 0.0f;
+      float dprob_part = 0.0f;
+      for (int c = 0; c < kBN / 32; ++c) {
+        const int64_t j0 = ti.n0 + c * 32;
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN + c * 32,
+                           r);
+        if (j0 >= p.n) {  // past the last compact column (n % 32 == 0: whole chunk)
+          tmem_ld_wait();
+          continue;
+        }
+        uint4 cv[8];
+        const int64_t cbase = row * two_n + 2 * j0;  // gate block start; input at +32
+        if (row_ok) {
+          const uint4* src = reinterpret_cast<const uint4*>(p.c + cbase);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) cv[i] = __ldcs(src + i);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) cv[i] = make_uint4(0, 0, 0, 0);
+        }
+        tmem_ld_wait();
+        uint32_t dg[16], di[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          // element pair (2i, 2i+1): gate words in cv[0..3], input words in cv[4..7]
+          const uint32_t gw = reinterpret_cast<const uint32_t*>(cv)[i];
+          const uint32_t iw = reinterpret_cast<const uint32_t*>(cv)[16 + i];
+          float outg[2], outi[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float gate = __fmul_rn(beta, h ? bf16_hi(gw) : bf16_lo(gw));
+            const float inp = __fmul_rn(beta, h ? bf16_hi(iw) : bf16_lo(iw));
+            const float R = __fmul_rn(a2, __uint_as_float(r[2 * i + h]));
+            const float s = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-gate)));
+            const float rp = __fmul_rn(R, prob);
+            outg[h] = rp * inp * s * (1.0f + gate * (1.0f - s));
+            outi[h] = rp * gate * s;
+            dprob_part += R * gate * s * inp;
+          }
+          __nv_bfloat162 bg = __floats2bfloat162_rn(outg[0], outg[1]);
+          __nv_bfloat162 bi = __floats2bfloat162_rn(outi[0], outi[1]);
+          dg[i] = *reinterpret_cast<uint32_t*>(&bg);
+          di[i] = *reinterpret_cast<uint32_t*>(&bi);
+          if (p.dbias_ws) {
+            float* tr = trans + lane * kTransStride;
+            tr[2 * i] = row_ok ? outg[0] : 0.0f;
+            tr[2 * i + 1] = row_ok ? outg[1] : 0.0f;
+            tr[32 + 2 * i] = row_ok ? outi[0] : 0.0f;
+            tr[32 + 2 * i + 1] = row_ok ? outi[1] : 0.0f;
+          }
+        }
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(p.d_row + cbase);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(dg[4 * i], dg[4 * i + 1], dg[4 * i + 2], dg[4 * i + 3]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[4 + i] = make_uint4(di[4 * i], di[4 * i + 1], di[4 * i + 2], di[4 * i + 3]);
+        }
+        if (p.dbias_ws) {
+          __syncwarp();
+          float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll 8
+          for (int rr = 0; rr < 32; ++rr) {
+            s0 += trans[rr * kTransStride + lane];
+            s1 += trans[rr * kTransStride + 32 + lane];
+          }
+          float* ws = p.dbias_ws + static_cast<int64_t>(ti.g) * two_n + 2 * j0;
+          atomicAdd(ws + lane, s0);
+          atomicAdd(ws + 32 + lane, s1);
+          __syncwarp();
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (row_ok) atomicAdd(p.dprob + row, dprob_part);
+      if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// dbias[i] = bf16(float(dbias[i]) + ws[i])
+__global__ void dbias_finalize_kernel(uint16_t* dbias, const float* ws, int64_t count) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float v = __fadd_rn(__uint_as_float(static_cast<uint32_t>(dbias[i]) << 16), ws[i]);
+    __nv_bfloat16 b = __float2bfloat16_rn(v);
+    dbias[i] = *reinterpret_cast<uint16_t*>(&b);
+  }
+}
+
+}  // namespace
+}  // namespace hq
+
+extern "C" {
+
+size_t hq_gemm_dswiglu_workspace_size(int L, int64_t n) {
+  if (L < 1 || n <= 0) return 0;
+  const size_t bytes = static_cast<size_t>(L) * static_cast<size_t>(2 * n) * sizeof(float);
+  return (bytes + 255) / 256 * 256;
+}
+
+int hq_gemm_dswiglu(const hq_bf16* a, const hq_bf16* b, const hq_bf16* c,
+                    const int32_t* padded_offsets, int L, const float* alpha, const float* beta,
+                    const float* prob, hq_bf16* d_row, float* dprob, hq_bf16* dbias, int64_t m,
+                    int64_t n, int64_t k, void* workspace, size_t ws_bytes, int sm_count,
+                    hq_stream_t s) {
+  using namespace hq;
+  if (L < 1 || L > kMaxGroups) return HQ_ERR_INVALID;
+  if (m < 0 || n <= 0 || k <= 0 || n % 32 != 0 || k % 8 != 0) return HQ_ERR_INVALID;
+  if (m > (1ll << 31) - 256 || n > (1ll << 28) || k > (1ll << 30)) return HQ_ERR_INVALID;
+  if (!a || !b || !c || !padded_offsets || !alpha || !beta || !prob || !d_row || !dprob)
+    return HQ_ERR_INVALID;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(c) || !aligned16(d_row)) return HQ_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(padded_offsets) | reinterpret_cast<uintptr_t>(alpha) |
+       reinterpret_cast<uintptr_t>(beta) | reinterpret_cast<uintptr_t>(prob) |
+       reinterpret_cast<uintptr_t>(dprob)) & 3u)
+    return HQ_ERR_INVALID;
+  if (dbias) {
+    if (reinterpret_cast<uintptr_t>(dbias) & 1u) return HQ_ERR_INVALID;
+    if (!workspace || ws_bytes < hq_gemm_dswiglu_workspace_size(L, n)) return HQ_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return HQ_ERR_INVALID;
+  }
+  if (m == 0) return HQ_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  DsParams p{};
+  p.gs.group_info = padded_offsets;
+  p.gs.a_rows = m;
+  p.gs.groups = L;
+  p.gs.sched = kContig;
+  p.gs.status = status_word_ptr();
+  if (!p.gs.status) return HQ_ERR_CUDA;
+  p.c = c;
+  p.alpha = alpha;
+  p.beta = beta;
+  p.prob = prob;
+  p.d_row = d_row;
+  p.dprob = dprob;
+  p.dbias_ws = dbias ? static_cast<float*>(workspace) : nullptr;
+  p.n = n;
+  p.k = k;
+  p.wait_limit_ns = wait_limit_ns();
+
+  CUtensorMap tmA, tmB;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(k), static_cast<uint64_t>(m)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(k) * 2};
+    const uint32_t box[2] = {kBKElems, kBM};
+    int rc = encode_tensor_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<hq_bf16*>(a),
+                               dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != HQ_OK) return rc;
+  }
+  {
+    const uint64_t dims[3] = {static_cast<uint64_t>(k), static_cast<uint64_t>(n),
+                              static_cast<uint64_t>(L)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(k) * 2, static_cast<uint64_t>(k) * 2 * n};
+    const uint32_t box[3] = {kBKElems, kBN, 1};
+    int rc = encode_tensor_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<hq_bf16*>(b),
+                               dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != HQ_OK) return rc;
+  }
+  if (dbias) {
+    const size_t bytes = static_cast<size_t>(L) * static_cast<size_t>(2 * n) * sizeof(float);
+    if (cudaMemsetAsync(workspace, 0, bytes, st) != cudaSuccess) return HQ_ERR_CUDA;
+  }
+  if (cudaFuncSetAttribute(dswiglu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes) != cudaSuccess)
+    return HQ_ERR_CUDA;
+  const int sms = num_sms();
+  if (sms <= 0) return HQ_ERR_CUDA;
+  const int64_t tiles_bound = ((m + kBM - 1) / kBM) * ((n + kBN - 1) / kBN);
+  int64_t grid = sm_count > 0 ? sm_count : sms;
+  if (grid > sms) grid = sms;
+  if (grid > tiles_bound) grid = tiles_bound;
+  if (grid < 1) grid = 1;
+  if (launch(dswiglu_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, st,
+             false, tmA, tmB, p) != cudaSuccess)
+    return HQ_ERR_CUDA;
+  if (dbias) {
+    const int64_t count = static_cast<int64_t>(L) * 2 * n;
+    int64_t blocks = (count + 255) / 256;
+    if (blocks > 4 * sms) blocks = 4 * sms;
+    dbias_finalize_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+        reinterpret_cast<uint16_t*>(dbias), static_cast<const float*>(workspace), count);
+    if (cudaGetLastError() != cudaSuccess) return HQ_ERR_CUDA;
+  }
+  return HQ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,52 @@
+// hq_internal.h -- host-side helpers shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <utility>
+
+#include "../../include/hq.h"
+
+namespace hq {
+
+// Device address of the status word on the current device (resolved once per
+// device with cudaGetSymbolAddress); nullptr on failure.
+uint32_t* status_word_ptr();
+
+// Current limit for bounded pipeline waits, in nanoseconds.
+uint64_t wait_limit_ns();
+
+// Number of SMs of the current device (cached per device); 0 on failure.
+int num_sms();
+
+// Forced GEMM tile width (0 = automatic).
+int forced_tile_n();
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point.
+// Returns HQ_OK or HQ_ERR_CUDA.
+int encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, void* base,
+                      const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                      CUtensorMapSwizzle swizzle);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launch with optional programmatic-dependent-launch attribute.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+}  // namespace hq

@@ -1,0 +1,268 @@
+/*
+ * hq.h -- C ABI of the block-scaled low-precision MoE GEMM library (libhq.so).
+ *
+ * One GB300 (sm_103a) hot path: a group-wise quantiser (BF16 -> MXFP8 / NVFP4
+ * with scales in the 128x4 SfAtom layout), dense / grouped-contiguous /
+ * grouped-masked block-scaled GEMMs with BF16 output, a fused SwiGLU +
+ * requantisation pass, and a BF16 grouped GEMM fused with the dSwiGLU
+ * backward (per-row dprob, per-expert dbias).
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ *  - Every tensor argument is a DEVICE pointer into memory the caller owns and
+ *    has allocated (outputs are pre-allocated and written in place, as the
+ *    HALOps "GEMM" API does for every op: "Written in-place").  The library
+ *    allocates no memory; where a call needs scratch space the caller passes
+ *    it (sized by a *_workspace_size query), so it can be allocated before a
+ *    CUDA-graph capture (FlashRT fp4-gemm notes, large-M tier workspace).
+ *  - Every call is asynchronous on the given stream (NULL = legacy default
+ *    stream).  The library keeps no pointer after it returns, but every
+ *    buffer must stay alive and unchanged until the stream reaches the work.
+ *  - Every call validates its arguments on the host and returns a status
+ *    BEFORE launching anything ("Unsupported calls raise before launch" --
+ *    FlashRT fp4-gemm notes; "rejected before allocation or compilation" --
+ *    cuDNN "Grouped GEMM + dGLU (SM100)", Backend dispatch).  On a non-zero
+ *    status nothing was launched and no output was touched.
+ *  - Values the host cannot see (device-resident offsets, masks, counts) are
+ *    checked on the device: a violation is clamped to a safe value, the
+ *    affected rows are skipped, and a bit is set in the device status word
+ *    (read with hq_get_device_status).  A pipeline wait that exceeds the
+ *    wait limit sets HQ_STATUS_WAIT_TIMEOUT and the kernel returns early
+ *    instead of hanging.
+ *  - Matrices are row-major.  A and B are K-major (the contiguous dimension is
+ *    K); outputs are N-major.  FP8 data is one byte per element
+ *    (float8_e4m3fn); FP4 data is packed E2M1, two elements per byte with the
+ *    even element index in the low nibble, so an [r, k] FP4 matrix occupies
+ *    r * k / 2 bytes.  BF16 values are passed as raw 16-bit patterns.
+ *  - Scale factors: one byte per group of 32 (MXFP8, UE8M0 = power-of-two
+ *    biased exponent) or 16 (NVFP4, UE4M3 = float8_e4m3fn bit pattern with a
+ *    clear sign bit) consecutive K elements.  The swizzled layout is the
+ *    "SfAtom 128x4" of the HALOps API (cuDNN shape (32, 4, ceil(R/128), 4,
+ *    ceil(S/4), L)): for R rows and S = K / group scale columns the byte of
+ *    (row r, column s) is at
+ *        ((r / 128) * (S / 4) + s / 4) * 512
+ *          + (r % 32) * 16 + ((r % 128) / 32) * 4 + (s % 4),
+ *    the buffer holds ceil(R / 128) * 128 * S bytes, and expert-stacked weight
+ *    scales place expert e at e * ceil(N / 128) * 128 * S.
+ */
+#ifndef HQ_H_
+#define HQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same handle type as cudaStream_t / CUstream (NULL = legacy default stream). */
+typedef struct CUstream_st *hq_stream_t;
+
+/* A BF16 value as its raw bit pattern. */
+typedef uint16_t hq_bf16;
+
+/* Quantisation recipe ("mode" string of the HALOps API). */
+typedef enum {
+  HQ_MXFP8 = 0, /* "w8a8-mxfp8": E4M3 elements, UE8M0 scale per 32          */
+  HQ_NVFP4 = 2  /* "w4a4-nvfp4": packed E2M1, UE4M3 scale per 16, FP32 alpha */
+} hq_mode;
+
+/* Return codes. */
+enum {
+  HQ_OK = 0,
+  HQ_ERR_INVALID = 1,     /* null pointer, bad shape, stride or alignment      */
+  HQ_ERR_UNSUPPORTED = 2, /* valid request this library does not implement    */
+  HQ_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed                 */
+  HQ_ERR_TIMEOUT = 4      /* device status reports an expired pipeline wait    */
+};
+
+/* Bits of the device status word. */
+#define HQ_STATUS_WAIT_TIMEOUT 0x1u   /* a bounded mbarrier wait expired           */
+#define HQ_STATUS_MASK_CLAMPED 0x2u   /* masked_m[e] outside [0, max_m]: clamped    */
+#define HQ_STATUS_BAD_OFFSETS 0x4u    /* padded_offsets not monotone / 128-aligned /
+                                         beyond the row count: rows skipped      */
+#define HQ_STATUS_TOKENS_CLAMPED 0x8u /* token_nums[e] outside [0, rows/expert]    */
+
+/* Layout and alignment constants, so integrations need not copy them
+ * (FlashRT fp4-gemm notes: "Read capabilities() instead of duplicating
+ * scale-factor layout or alignment constants"). */
+typedef struct {
+  int abi_version;       /* 1                                               */
+  int sfatom_rows;       /* 128 rows per atom                               */
+  int sfatom_cols;       /* 4 scale columns per atom                        */
+  int sfatom_bytes;      /* 512                                             */
+  int group_mxfp8;       /* 32                                              */
+  int group_nvfp4;       /* 16                                              */
+  int contig_row_align;  /* 256: padded_offsets alignment the pages fix     */
+  int tile_m;            /* 128: rows per GEMM tile (offsets must be multiples) */
+  int ptr_align_bytes;   /* 16: every tensor base pointer                   */
+  int max_groups;        /* 1024 experts at most                            */
+  int glu_block;         /* 32: dGLU gate/input interleave width            */
+} hq_capabilities_t;
+
+/* Fills *out.  Returns HQ_ERR_INVALID if out is NULL. */
+int hq_capabilities(hq_capabilities_t *out);
+
+/* Human-readable name of a return code (static string, never NULL). */
+const char *hq_status_string(int status);
+
+/* Bytes of a scale buffer for `rows` rows of K = k elements in `mode`:
+ * ceil(rows / 128) * 128 * (k / group).  Returns 0 if k is not a multiple of
+ * 4 * group or mode is unknown. */
+size_t hq_sf_bytes(int64_t rows, int64_t k, hq_mode mode);
+
+/* Reads the device status word of the current device (after the work queued
+ * on `s` completes: this call synchronises `s`) into *out; if clear != 0 the
+ * word is reset to 0.  Returns HQ_ERR_TIMEOUT if HQ_STATUS_WAIT_TIMEOUT is
+ * set, HQ_ERR_CUDA on a CUDA failure, else HQ_OK. */
+int hq_get_device_status(uint32_t *out, int clear, hq_stream_t s);
+
+/* Limit of every bounded pipeline wait inside the kernels, in nanoseconds
+ * (default 1e9).  Applies to launches made after the call. */
+int hq_set_wait_limit_ns(uint64_t ns);
+
+/* Self-test of the bounded wait: launches one CTA that waits on a pipeline
+ * barrier nothing ever arrives on, with the given limit.  The wait expires,
+ * HQ_STATUS_WAIT_TIMEOUT is set in the device status word and the kernel
+ * returns; the context stays usable.  No GPU fault is involved. */
+int hq_selftest_wait_expiry(uint64_t limit_ns, hq_stream_t s);
+
+/* Tuning knob: GEMM tile width in N for the block-scaled GEMMs (0 = choose
+ * automatically, 128 or 256 = force).  Applies to later calls. */
+int hq_set_gemm_tile_n(int tile_n);
+
+/* ------------------------------------------------------------------------- *
+ * Group-wise quantiser
+ *
+ * HALOps "GEMM" API, group_wise_quant: quantises a 2-D BF16 tensor per group
+ * along K and returns the data and the block scales (SfAtom layout when
+ * use_swizzle, plain row-major otherwise).  Scale rule (cuDNN "Grouped GEMM +
+ * dGLU (SM100)", Step 3): SF = norm_const * amax(group) * rcp_max,
+ * q = x * norm_const / SF, with norm_const = *global_scale (NVFP4; 1 when
+ * NULL) or 1 (MXFP8), rcp_max = 1/448 (E4M3) or 1/6 (E2M1), evaluated in
+ * IEEE float32 in that order.  MXFP8 rounds SF up to a power of two
+ * (UE8M0 = clamp(ceil(log2 SF) + 127, 0, 254), 0 for an all-zero group) and
+ * stores E4M3(x * 2^(127 - UE8M0)); NVFP4 stores UE4M3 = E4M3(SF) and
+ * E2M1(x * (g / SF_decoded)).  Element encodes round to nearest even and
+ * saturate.
+ *
+ *   x            [m, k] BF16, 16-byte aligned
+ *   mode         HQ_MXFP8 or HQ_NVFP4
+ *   use_swizzle  1: SfAtom layout; 0: row-major [ceil(m/128)*128, k/group]
+ *   global_scale NVFP4 only: device float [1] or NULL (=1); must be NULL for
+ *                MXFP8 (HQ_ERR_UNSUPPORTED otherwise)
+ *   q_out        MXFP8 [m, k] bytes; NVFP4 [m, k/2] bytes; 16-byte aligned
+ *   sf_out       hq_sf_bytes(m, k, mode) bytes; padding rows written as 0
+ *   use_pdl      1: launch with programmatic dependent launch
+ * Requires k % (4 * group) == 0 (HQ_ERR_INVALID otherwise).  m == 0 is a
+ * no-op. */
+int hq_quant(const hq_bf16 *x, int64_t m, int64_t k, hq_mode mode, int use_swizzle,
+             const float *global_scale, void *q_out, uint8_t *sf_out, int use_pdl,
+             hq_stream_t s);
+
+/* ------------------------------------------------------------------------- *
+ * Block-scaled GEMMs: out = alpha * (A . B^T) + bias, BF16 output (RNE).
+ *
+ * Common arguments:
+ *   a, sfa   quantised A and its SfAtom scales (as hq_quant writes them)
+ *   b, sfb   quantised B (one [n, k] matrix per group, stacked) and its
+ *            SfAtom scales (per group ceil(n/128)*128*(k/group) bytes)
+ *   alpha    device float per group, or NULL (= 1).  Required for HQ_NVFP4
+ *            (HQ_ERR_UNSUPPORTED if NULL), optional for HQ_MXFP8
+ *   bias     device BF16 [groups, n] or NULL.  HQ_MXFP8 only
+ *            (HQ_ERR_UNSUPPORTED with HQ_NVFP4), as the HALOps API states
+ *   sm_count number of persistent CTAs (<= 0: all SMs)
+ * Shape rules: k % (4 * group) == 0; n % 128 == 0; all pointers 16-byte
+ * aligned.  Each tile is 128 rows by 128 or 256 columns.
+ * ------------------------------------------------------------------------- */
+
+/* HALOps "GEMM" API, dense_gemm: out[m, n] = alpha * a[m, k] . b[n, k]^T + bias.
+ * sfa holds ceil(m/128)*128 rows.  A batched GEMM (batch_gemm) is
+ * hq_gemm_grouped_masked with masked_m[e] = max_m, or hq_gemm_grouped_contig
+ * with padded_offsets[e] = (e + 1) * M. */
+int hq_gemm_dense(const void *a, const uint8_t *sfa, const void *b, const uint8_t *sfb,
+                  const float *alpha, const hq_bf16 *bias, hq_bf16 *out, int64_t m, int64_t n,
+                  int64_t k, hq_mode mode, int sm_count, int use_pdl, hq_stream_t s);
+
+/* cuDNN "Grouped GEMM + dGLU (SM100)", Step 1 with groups "contiguous in the M
+ * dimension and described by padded_offsets (cumulative aligned end
+ * offsets)"; HALOps group_contiguous_gemm with per-expert weights.
+ *   a [m_rows, k], out [m_rows, n]; b [L, n, k]; sfb per expert as above
+ *   padded_offsets  device int32 [L], non-decreasing group ends, each a
+ *                   multiple of 128 (the pages use 256), last <= m_rows
+ *   L               1..1024
+ * Rows in [off[g-1], off[g]) use expert g; rows >= off[L-1] are not written.
+ * Offset violations set HQ_STATUS_BAD_OFFSETS and the affected rows are
+ * skipped. */
+int hq_gemm_grouped_contig(const void *a, const uint8_t *sfa, const void *b, const uint8_t *sfb,
+                           const int32_t *padded_offsets, int L, const float *alpha,
+                           const hq_bf16 *bias, hq_bf16 *out, int64_t m_rows, int64_t n,
+                           int64_t k, hq_mode mode, int sm_count, hq_stream_t s);
+
+/* HALOps "GEMM" API, group_masked_gemm: a [E * max_m, k] with expert e's rows
+ * at e * max_m; masked_m (device int32 [E]) valid rows per expert; only rows
+ * e * max_m + i, i < masked_m[e], are computed and written -- every other
+ * output row is left untouched.  max_m > 0 and max_m % 128 == 0;
+ * masked_m[e] outside [0, max_m] is clamped (HQ_STATUS_MASK_CLAMPED). */
+int hq_gemm_grouped_masked(const void *a, const uint8_t *sfa, const void *b, const uint8_t *sfb,
+                           const int32_t *masked_m, int E, int64_t max_m, const float *alpha,
+                           const hq_bf16 *bias, hq_bf16 *out, int64_t n, int64_t k, hq_mode mode,
+                           int sm_count, hq_stream_t s);
+
+/* ------------------------------------------------------------------------- *
+ * HALOps "GEMM" API, fused_swiglu_quant: y = up * silu(gate) over input =
+ * [gate | up] (gate = columns [0, H), up = [H, 2H)), then y (float32) is
+ * quantised exactly as hq_quant does (MXFP8: group 32, UE8M0; NVFP4: group
+ * 16, UE4M3, norm_const = *global_scale or 1).
+ *   in          [rows, 2H] BF16
+ *   token_nums  device int32 [E] valid rows per expert, or NULL (all rows).
+ *               With token_nums, row r belongs to expert r / rows_per_expert
+ *               and is written only if r % rows_per_expert < token_nums[e]
+ *               (nothing of an invalid row is written, not even its scales).
+ *   q_out       MXFP8 [rows, H] bytes; NVFP4 [rows, H/2] bytes
+ *   sf_out      SfAtom scales of kb_dim columns over ceil(rows/128)*128 rows:
+ *               MXFP8 kb_dim = ceil(H / 512) * 16, NVFP4 kb_dim = H / 16;
+ *               MXFP8 columns [H/32, kb_dim) of written rows hold 0; with
+ *               token_nums == NULL the padding rows hold 0.
+ * Requires H % 128 == 0 (MXFP8) or H % 64 == 0 (NVFP4), rows_per_expert > 0
+ * and E * rows_per_expert == rows when token_nums is given. */
+int hq_swiglu_quant(const hq_bf16 *in, int64_t rows, int64_t H, const int32_t *token_nums, int E,
+                    int64_t rows_per_expert, hq_mode mode, const float *global_scale,
+                    void *q_out, uint8_t *sf_out, hq_stream_t s);
+
+/* ------------------------------------------------------------------------- *
+ * cuDNN "Grouped GEMM + dGLU (SM100)", BF16 contract, act_func = "dswiglu",
+ * dense B:  R_g = alpha_g^2 A_g B_g^T,  X_g = beta_g C_g; X is split into
+ * alternating 32-column gate / input blocks (within each 64 columns: 32 gate
+ * then 32 input); with s = sigmoid(gate):
+ *     D_row[gate col]  = dgate  = R prob input s (1 + gate (1 - s))
+ *     D_row[input col] = dinput = R prob gate s
+ *     dprob[m]        += sum_j R gate s input           (no prob factor)
+ *     dbias[g, c]     += sum over rows m of group g of D_row[m, c]
+ *   a        [m, k] BF16                  b  [L, n, k] BF16 (K-major)
+ *   c        [m, 2n] BF16 (saved forward) d_row [m, 2n] BF16 output
+ *   padded_offsets device int32 [L] (rules as hq_gemm_grouped_contig)
+ *   alpha, beta    device float [L];  prob device float [m]
+ *   dprob    device float [m], caller-zeroed, accumulated (+=)
+ *   dbias    device BF16 [L, 2n] or NULL; caller-zeroed, accumulated (+=) from
+ *            float32 partial sums of the unrounded D values
+ *   workspace      device scratch of hq_gemm_dswiglu_workspace_size(L, n)
+ *                  bytes (may be NULL when dbias is NULL); contents need not
+ *                  be initialised; 256-byte aligned
+ * Rows >= padded_offsets[L-1] are not written.  Requires n % 32 == 0,
+ * k % 8 == 0, 1 <= L <= 1024. */
+int hq_gemm_dswiglu(const hq_bf16 *a, const hq_bf16 *b, const hq_bf16 *c,
+                    const int32_t *padded_offsets, int L, const float *alpha, const float *beta,
+                    const float *prob, hq_bf16 *d_row, float *dprob, hq_bf16 *dbias, int64_t m,
+                    int64_t n, int64_t k, void *workspace, size_t ws_bytes, int sm_count,
+                    hq_stream_t s);
+
+/* Bytes of scratch hq_gemm_dswiglu needs for dbias: L * 2n float32, rounded
+ * up to 256 bytes. */
+size_t hq_gemm_dswiglu_workspace_size(int L, int64_t n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HQ_H_ */

@@ -1,0 +1,118 @@
+"""Host-side checks of the C ABI: libhq.so loads, exports every function that
+include/hq.h declares, and rejects invalid calls before touching a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp4_grouped_gemm_gb300 as hq
+from fp4_grouped_gemm_gb300 import _abi, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _abi.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "hq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported_and_bound(lib):
+    names = declared_functions()
+    assert len(names) >= 14
+    for name in names:
+        assert hasattr(lib, name), name
+        assert name in _abi.SIGNATURES, f"{name} has no ctypes signature"
+
+
+def test_capabilities_and_sizes(lib):
+    caps = hq.capabilities()
+    assert caps["sfatom_bytes"] == 512 and caps["group_mxfp8"] == 32 and caps["group_nvfp4"] == 16
+    assert hq.sf_bytes(200, 256, "mxfp8") == 256 * 8
+    assert hq.sf_bytes(128, 5120, "nvfp4") == 128 * 320
+    assert hq.sf_bytes(10, 100, "mxfp8") == 0          # k not a multiple of 128
+    assert hq.hq_gemm_dswiglu_workspace_size(16, 1408) == 16 * 2816 * 4
+    assert hq.swiglu_kb_dim(1536, "mxfp8") == 48 and hq.swiglu_kb_dim(640, "mxfp8") == 32
+
+
+def test_status_strings(lib):
+    for rc in range(5):
+        assert lib.hq_status_string(rc)
+    assert b"unknown" in lib.hq_status_string(99)
+
+
+FAKE = ctypes.c_void_p(0x10000)  # aligned, never dereferenced: validation fails first
+
+
+def test_quant_rejects_bad_arguments(lib):
+    # k not a multiple of 4 * group
+    assert lib.hq_quant(FAKE, 4, 96, 0, 1, None, FAKE, FAKE, 0, None) == _abi.HQ_ERR_INVALID
+    # unknown mode
+    assert lib.hq_quant(FAKE, 4, 128, 7, 1, None, FAKE, FAKE, 0, None) == _abi.HQ_ERR_INVALID
+    # null input
+    assert lib.hq_quant(None, 4, 128, 0, 1, None, FAKE, FAKE, 0, None) == _abi.HQ_ERR_INVALID
+    # misaligned input
+    assert lib.hq_quant(ctypes.c_void_p(0x10002), 4, 128, 0, 1, None, FAKE, FAKE, 0, None) == \
+        _abi.HQ_ERR_INVALID
+    # a global scale is an NVFP4 feature
+    assert lib.hq_quant(FAKE, 4, 128, 0, 1, FAKE, FAKE, FAKE, 0, None) == _abi.HQ_ERR_UNSUPPORTED
+    # m == 0 is a no-op
+    assert lib.hq_quant(FAKE, 0, 128, 0, 1, None, FAKE, FAKE, 0, None) == _abi.HQ_OK
+
+
+def test_gemm_rejects_bad_arguments(lib):
+    f = lib.hq_gemm_dense
+    # n not a multiple of 128
+    assert f(FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 128, 100, 256, 0, -1, 0, None) == _abi.HQ_ERR_INVALID
+    # NVFP4 needs alpha
+    assert f(FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 128, 128, 256, 2, -1, 0, None) == _abi.HQ_ERR_UNSUPPORTED
+    # NVFP4 takes no bias
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 128, 256, 2, -1, 0, None) == _abi.HQ_ERR_UNSUPPORTED
+    # k not a multiple of 4 * group
+    assert f(FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 128, 128, 96, 0, -1, 0, None) == _abi.HQ_ERR_INVALID
+    g = lib.hq_gemm_grouped_masked
+    # max_m not a multiple of 128
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 100, None, None, FAKE, 128, 128, 0, -1, None) == _abi.HQ_ERR_INVALID
+    # too many experts
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 1025, 128, None, None, FAKE, 128, 128, 0, -1, None) == _abi.HQ_ERR_INVALID
+    c = lib.hq_gemm_grouped_contig
+    assert c(FAKE, FAKE, FAKE, FAKE, None, 4, None, None, FAKE, 1024, 128, 128, 0, -1, None) == _abi.HQ_ERR_INVALID
+    assert c(FAKE, FAKE, FAKE, FAKE, FAKE, 0, None, None, FAKE, 1024, 128, 128, 0, -1, None) == _abi.HQ_ERR_INVALID
+
+
+def test_swiglu_and_dswiglu_reject_bad_arguments(lib):
+    s = lib.hq_swiglu_quant
+    assert s(FAKE, 10, 100, None, 0, 0, 0, None, FAKE, FAKE, None) == _abi.HQ_ERR_INVALID   # H % 128
+    assert s(FAKE, 10, 128, FAKE, 3, 4, 0, None, FAKE, FAKE, None) == _abi.HQ_ERR_INVALID   # E*rpe != rows
+    assert s(FAKE, 10, 128, None, 0, 0, 0, FAKE, FAKE, FAKE, None) == _abi.HQ_ERR_UNSUPPORTED
+    d = lib.hq_gemm_dswiglu
+    args = [FAKE, FAKE, FAKE, FAKE, 2, FAKE, FAKE, FAKE, FAKE, FAKE, None, 512, 48, 64, None, 0, -1, None]
+    assert d(*args) == _abi.HQ_ERR_INVALID                       # n % 32
+    args[12] = 64
+    args[10] = FAKE                                               # dbias without workspace
+    assert d(*args) == _abi.HQ_ERR_INVALID
+    args[14] = ctypes.c_void_p(0x10000)
+    args[15] = 100                                                # workspace too small
+    assert d(*args) == _abi.HQ_ERR_INVALID
+
+
+def test_knobs_validate(lib):
+    assert lib.hq_set_gemm_tile_n(96) == _abi.HQ_ERR_INVALID
+    assert lib.hq_set_gemm_tile_n(0) == _abi.HQ_OK
+    assert lib.hq_set_wait_limit_ns(0) == _abi.HQ_ERR_INVALID
+    assert lib.hq_selftest_wait_expiry(0, None) == _abi.HQ_ERR_INVALID
+
+
+def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(_abi, "_LIB", None)
+    monkeypatch.setattr(_abi, "lib_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        _abi.load()

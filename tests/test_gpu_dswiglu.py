@@ -1,0 +1,133 @@
+"""GPU parity of the BF16 grouped GEMM + dSwiGLU backward against the oracle.
+
+D_row: |gpu - ref| <= 2^-8 |ref| + 2^-20 (alpha^2 sum|a b|) |activation factor|
+dprob: |gpu - ref| <= 1e-3 sum_j |R swish input|
+dbias: |gpu - ref| <= 1e-3 sum_m |D| + one BF16 ulp of ref
+Rows at and past padded_offsets[L-1] keep their sentinel (D_row) / zero (dprob).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import fp4_grouped_gemm_gb300 as hq
+import synth
+from oracle import glu
+
+from gpu_util import assert_rows_untouched, bf16_rows, np_f32, sentinel_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def bf16_ulp(x):
+    a = np.abs(x)
+    e = np.floor(np.log2(np.where(a > 0, a, 1e-300)))
+    return np.where(a > 0, 2.0 ** (e - 7), 2.0 ** -133)
+
+
+def run_case(offsets, m, n, k, seed, with_dbias=True):
+    L = len(offsets)
+    a = bf16_rows(m, k, seed)
+    b = torch.stack([bf16_rows(n, k, seed + 1 + e, std=0.05) for e in range(L)])
+    c = bf16_rows(m, 2 * n, seed + 40, std=2.0)
+    gen = torch.Generator().manual_seed(seed)
+    prob = 1.0 - torch.rand(m, generator=gen)
+    alpha = 0.8 + 0.4 * torch.rand(L, generator=gen)
+    beta = 0.8 + 0.4 * torch.rand(L, generator=gen)
+    dev = torch.device("cuda")
+    dprob = torch.zeros(m, dtype=torch.float32, device=dev)
+    dbias = torch.zeros(L, 2 * n, dtype=torch.bfloat16, device=dev) if with_dbias else None
+    d_row = sentinel_bf16((m, 2 * n))
+    hq.hq_gemm_dswiglu(a.to(dev), b.to(dev), c.to(dev), torch.tensor(offsets, dtype=torch.int32, device=dev),
+                       alpha.to(dev), beta.to(dev), prob.to(dev), dprob, dbias=dbias, d_row=d_row)
+    torch.cuda.synchronize()
+    ref = glu.dswiglu(np_f32(a), np_f32(b), np_f32(c), offsets, alpha.numpy(), beta.numpy(), prob.numpy())
+    return ref, d_row, dprob, dbias
+
+
+def check(ref, d_row, dprob, dbias):
+    w = ref["written"]
+    D = d_row.float().cpu().numpy().astype(np.float64)
+    tol = 2.0 ** -8 * np.abs(ref["D"]) + 2.0 ** -20 * ref["D_mag"] + 1e-30
+    err = np.abs(D - ref["D"])
+    bad = (err > tol) & w[:, None]
+    assert not bad.any(), f"D_row: {int(bad.sum())} bad; first {np.argwhere(bad)[0]}"
+    assert_rows_untouched(d_row, w, "D_row")
+    dp = dprob.cpu().numpy().astype(np.float64)
+    dp_tol = 1e-3 * ref["dprob_mag"] + 1e-30
+    assert (np.abs(dp - ref["dprob"]) <= dp_tol)[w].all(), "dprob outside 1e-3 relative"
+    assert not dp[~w].any(), "dprob written past the last group"
+    if dbias is not None:
+        db = dbias.float().cpu().numpy().astype(np.float64)
+        db_tol = 1e-3 * ref["dbias_mag"] + bf16_ulp(ref["dbias"])
+        assert (np.abs(db - ref["dbias"]) <= db_tol).all(), "dbias outside tolerance"
+
+
+@pytest.mark.parametrize("n", [64, 128, 160])
+def test_dswiglu_small(cuda_dev, n):
+    offsets = [256, 256, 768, 1024]       # empty group 1; rows >= 1024 not written
+    check(*run_case(offsets, 1152, n, 192, seed=n))
+
+
+def test_dswiglu_no_dbias(cuda_dev):
+    check(*run_case([512], 640, 96, 64, seed=3, with_dbias=False))
+
+
+def test_dswiglu_accumulates_into_dprob_and_dbias(cuda_dev):
+    """dprob and dbias are += outputs: two calls give twice one call."""
+    m, n, k = 512, 64, 128
+    a = bf16_rows(m, k, 1).cuda()
+    b = bf16_rows(n, k, 2, std=0.05).view(1, n, k).cuda()
+    c = bf16_rows(m, 2 * n, 3).cuda()
+    off = torch.tensor([m], dtype=torch.int32, device="cuda")
+    ones = torch.ones(1, device="cuda")
+    prob = torch.full((m,), 0.5, device="cuda")
+    dprob = torch.zeros(m, device="cuda")
+    dbias = torch.zeros(1, 2 * n, dtype=torch.bfloat16, device="cuda")
+    hq.hq_gemm_dswiglu(a, b, c, off, ones, ones, prob, dprob, dbias=dbias)
+    d1, b1 = dprob.clone(), dbias.float().clone()
+    hq.hq_gemm_dswiglu(a, b, c, off, ones, ones, prob, dprob, dbias=dbias)
+    torch.cuda.synchronize()
+    assert torch.allclose(dprob, 2 * d1, rtol=1e-5, atol=1e-6)
+    assert torch.allclose(dbias.float(), 2 * b1, rtol=2 ** -7, atol=1e-3)
+
+
+def test_dswiglu_full_size_sampled(cuda_dev):
+    cfg = synth.dswiglu_bwd(device="cuda")
+    m, n, k, L = cfg["m"], cfg["n"], cfg["k"], cfg["L"]
+    dprob = torch.zeros(m, dtype=torch.float32, device="cuda")
+    dbias = torch.zeros(L, 2 * n, dtype=torch.bfloat16, device="cuda")
+    off = torch.from_numpy(cfg["padded_offsets"]).cuda()
+    d_row, _, _ = hq.hq_gemm_dswiglu(cfg["a"], cfg["b"], cfg["c"], off, cfg["alpha"], cfg["beta"],
+                                     cfg["prob"], dprob, dbias=dbias)
+    torch.cuda.synchronize()
+    rows = np.sort(np.random.default_rng(5).choice(m, 48, replace=False))
+    ri = torch.from_numpy(rows).cuda()
+    grp = np.searchsorted(cfg["padded_offsets"], rows, side="right")
+    a_s, c_s = np_f32(cfg["a"][ri]), np_f32(cfg["c"][ri])
+    p_s = cfg["prob"][ri].cpu().numpy()
+    alpha, beta = cfg["alpha"].cpu().numpy(), cfg["beta"].cpu().numpy()
+    for g in np.unique(grp):
+        sel = grp == g
+        b_g = np_f32(cfg["b"][g]).astype(np.float64)
+        R, magR, _ = glu.grouped_R(a_s[sel], b_g[None], [int(sel.sum())], [alpha[g]])
+        D, dp, dp_mag, mult = glu.dswiglu_epilogue(R, c_s[sel], p_s[sel], np.full(int(sel.sum()), beta[g]))
+        gc, ic = glu.interleave_columns(n)
+        magD = np.zeros_like(D)
+        magD[:, gc] = magR * mult[:, gc]
+        magD[:, ic] = magR * mult[:, ic]
+        got = d_row[ri[torch.from_numpy(np.nonzero(sel)[0]).cuda()]].float().cpu().numpy()
+        assert (np.abs(got - D) <= 2.0 ** -8 * np.abs(D) + 2.0 ** -20 * magD + 1e-30).all()
+        got_p = dprob[ri[torch.from_numpy(np.nonzero(sel)[0]).cuda()]].cpu().numpy()
+        assert (np.abs(got_p - dp) <= 1e-3 * dp_mag + 1e-30).all()
+    # dbias equals the per-group column sums of the GPU's own D_row (any size)
+    D_all = d_row.double()
+    starts = np.concatenate([[0], cfg["padded_offsets"][:-1]])
+    for g in range(L):
+        s, e = int(starts[g]), int(cfg["padded_offsets"][g])
+        colsum = D_all[s:e].sum(dim=0) if e > s else torch.zeros(2 * n, dtype=torch.float64, device="cuda")
+        absum = D_all[s:e].abs().sum(dim=0) if e > s else torch.zeros(2 * n, dtype=torch.float64, device="cuda")
+        got = dbias[g].double()
+        # bf16 rounding of each D element (2^-9 relative) bounds the difference
+        tol = 2.0 ** -8 * absum + 2.0 ** -7 * got.abs() + 1e-6
+        assert bool(((got - colsum).abs() <= tol).all()), f"dbias group {g}"

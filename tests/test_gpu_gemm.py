@@ -1,0 +1,283 @@
+"""GPU parity of the block-scaled GEMMs against the oracle.
+
+Per element |gpu - ref| <= 2^-8 |ref| + 2^-20 |alpha| sum_k |a_k b_k| (ref in
+float64 from the oracle's dequantised operands).  Rows the GEMM must not write
+are pre-filled with a sentinel and checked bit for bit afterwards.
+
+Two kinds of inputs: operands quantised by the oracle and handed to the GEMM
+(isolates the GEMM kernel), and the hot path end to end (hq_quant on the GPU
+followed by the GEMM; the oracle quantises the same BF16 inputs itself).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import fp4_grouped_gemm_gb300 as hq
+import synth
+from oracle import gemm as ogemm
+from oracle import quant as oquant
+
+from gpu_util import (assert_gemm_close, assert_rows_untouched, bf16_rows, np_f32,
+                      oracle_quant_to_device, sentinel_bf16, stacked_weights_to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _reset_knobs():
+    yield
+    hq.set_gemm_tile_n(0)
+
+
+def dense_case(m, n, k, mode, tile_n=0, alpha=None, bias=False, seed=0, g_a=None, g_b=None):
+    hq.set_gemm_tile_n(tile_n)
+    a = bf16_rows(m, k, seed, spread=2)
+    b = bf16_rows(n, k, seed + 1, std=0.05, spread=2)
+    qa, sfa, qa_np, sfa_np = oracle_quant_to_device(a, mode, g_a)
+    qb, sfb, qb_np, sfb_np = oracle_quant_to_device(b, mode, g_b)
+    al = torch.tensor([alpha], dtype=torch.float32, device="cuda") if alpha is not None else None
+    bi = bf16_rows(1, n, seed + 2).cuda().view(n) if bias else None
+    out = sentinel_bf16((m, n))
+    hq.hq_gemm_dense(qa, sfa, qb, sfb, m, n, k, mode, alpha=al, bias=bi, out=out)
+    torch.cuda.synchronize()
+    ref, mag = ogemm.dense(oquant.dequantize(qa_np, sfa_np, mode), oquant.dequantize(qb_np, sfb_np, mode),
+                           alpha=None if alpha is None else [alpha],
+                           bias=None if bi is None else np_f32(bi)[None, :])
+    return assert_gemm_close(out, ref, mag, f"dense {mode} {m}x{n}x{k} tile_n={tile_n}")
+
+
+@pytest.mark.parametrize("tile_n", [0, 128, 256])
+def test_dense_mxfp8_256(cuda_dev, tile_n):
+    dense_case(256, 256, 256, "mxfp8", tile_n)
+
+
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("m,n,k", [(200, 384, 256), (129, 256, 1024), (1, 128, 128), (515, 768, 640)])
+def test_dense_mxfp8_shapes_alpha_bias(cuda_dev, tile_n, m, n, k):
+    if tile_n == 256 and n % 256:
+        pytest.skip("tile 256 needs n % 256 == 0 for full tiles; covered by the partial-tile case")
+    dense_case(m, n, k, "mxfp8", tile_n, alpha=0.75, bias=True, seed=m + n + k)
+
+
+def test_dense_mxfp8_forced_256_partial_n_tile(cuda_dev):
+    dense_case(130, 384, 256, "mxfp8", 256, alpha=1.5, bias=True, seed=3)
+
+
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("m,n,k", [(256, 256, 256), (300, 512, 512), (77, 256, 320), (130, 384, 1088)])
+def test_dense_nvfp4_shapes(cuda_dev, tile_n, m, n, k):
+    if tile_n == 256 and n % 256:
+        pytest.skip("partial n tile with 256 covered separately")
+    dense_case(m, n, k, "nvfp4", tile_n, alpha=0.5, seed=m * 3 + k, g_a=4.0, g_b=100.0)
+
+
+def test_dense_nvfp4_forced_256_partial_n_tile(cuda_dev):
+    dense_case(200, 384, 512, "nvfp4", 256, alpha=2.0, seed=11)
+
+
+def test_dense_end_to_end_quant_then_gemm(cuda_dev):
+    """The hot path: BF16 -> hq_quant (GPU) -> hq_gemm_dense, vs the oracle."""
+    m, n, k = 384, 512, 1024
+    a = bf16_rows(m, k, 21)
+    b = bf16_rows(n, k, 22, std=0.02)
+    ga, gb = synth.global_scale_nvfp4(a), synth.global_scale_nvfp4(b)
+    alpha = float(np.float32(1.0 / (np.float64(ga) * np.float64(gb))))
+    dev = torch.device("cuda")
+    ga_t = torch.tensor([ga], dtype=torch.float32, device=dev)
+    gb_t = torch.tensor([gb], dtype=torch.float32, device=dev)
+    qa, sfa = hq.hq_quant(a.cuda(), "nvfp4", global_scale=ga_t)
+    qb, sfb = hq.hq_quant(b.cuda(), "nvfp4", global_scale=gb_t)
+    out = hq.hq_gemm_dense(qa, sfa, qb, sfb, m, n, k, "nvfp4",
+                           alpha=torch.tensor([alpha], dtype=torch.float32, device=dev))
+    torch.cuda.synchronize()
+    qa_np, sa_np = oquant.quantize(np_f32(a), "nvfp4", ga)
+    qb_np, sb_np = oquant.quantize(np_f32(b), "nvfp4", gb)
+    ref, mag = ogemm.dense(oquant.dequantize(qa_np, sa_np, "nvfp4"),
+                           oquant.dequantize(qb_np, sb_np, "nvfp4"), alpha=[alpha])
+    assert_gemm_close(out, ref, mag, "end-to-end nvfp4")
+    # and the result approximates the unquantised BF16 product
+    exact = np_f32(a).astype(np.float64) @ np_f32(b).astype(np.float64).T
+    rel = np.linalg.norm(out.float().cpu().numpy() - exact) / np.linalg.norm(exact)
+    assert rel < 0.2
+
+
+# ----------------------------------------------------------------------------- grouped
+
+
+def contig_case(offsets, m_rows, n, k, mode, tile_n=0, alpha=None, bias=False, seed=0):
+    hq.set_gemm_tile_n(tile_n)
+    L = len(offsets)
+    a = bf16_rows(m_rows, k, seed, spread=1)
+    w = torch.stack([bf16_rows(n, k, seed + 10 + e, std=0.03) for e in range(L)])
+    qa, sfa, qa_np, sfa_np = oracle_quant_to_device(a, mode)
+    qb, sfb, b_deq = stacked_weights_to_device(w, mode)
+    off = torch.tensor(offsets, dtype=torch.int32, device="cuda")
+    al = torch.tensor(alpha, dtype=torch.float32, device="cuda") if alpha is not None else None
+    bi = torch.stack([bf16_rows(1, n, seed + 50 + e).view(n) for e in range(L)]).cuda() if bias else None
+    out = sentinel_bf16((m_rows, n))
+    hq.hq_gemm_grouped_contig(qa, sfa, qb, sfb, off, m_rows, n, k, mode, alpha=al, bias=bi, out=out)
+    torch.cuda.synchronize()
+    ref, mag, written = ogemm.grouped_contig(oquant.dequantize(qa_np, sfa_np, mode), b_deq, offsets,
+                                             alpha=alpha, bias=None if bi is None else np_f32(bi))
+    w_rows = np.nonzero(written)[0]
+    assert_gemm_close(out[torch.from_numpy(w_rows).cuda()], ref[w_rows], mag[w_rows], f"contig {mode}")
+    assert_rows_untouched(out, written, "contig")
+
+
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4"])
+def test_grouped_contig_small(cuda_dev, tile_n, mode):
+    offsets = [256, 256, 768, 1024]            # empty group 1; rows >= 1024 untouched
+    alpha = [0.5, 1.0, 2.0, 1.25]
+    contig_case(offsets, 1152, 256, 256, mode, tile_n, alpha=alpha, bias=(mode == "mxfp8"), seed=3)
+
+
+def test_grouped_contig_batch_equivalence(cuda_dev):
+    """batch_gemm == grouped contiguous with equal offsets == grouped masked with full masks."""
+    B, M, n, k = 3, 256, 256, 256
+    a = bf16_rows(B * M, k, 7)
+    w = torch.stack([bf16_rows(n, k, 70 + e, std=0.05) for e in range(B)])
+    qa, sfa, _, _ = oracle_quant_to_device(a, "mxfp8")
+    qb, sfb, _ = stacked_weights_to_device(w, "mxfp8")
+    off = torch.tensor([M, 2 * M, 3 * M], dtype=torch.int32, device="cuda")
+    o1 = hq.hq_gemm_grouped_contig(qa, sfa, qb, sfb, off, B * M, n, k, "mxfp8")
+    o2 = hq.hq_gemm_grouped_masked(qa, sfa, qb, sfb, torch.full((B,), M, dtype=torch.int32, device="cuda"),
+                                   M, n, k, "mxfp8")
+    o3 = torch.cat([hq.hq_gemm_dense(qa[i * M:(i + 1) * M], sfa[i * M * (k // 32):(i + 1) * M * (k // 32)],
+                                     qb[i], sfb[i * n * (k // 32):(i + 1) * n * (k // 32)], M, n, k, "mxfp8")
+                    for i in range(B)])
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(o1, o3)
+
+
+def masked_case(masked, max_m, n, k, mode, tile_n=0, alpha=None, seed=0):
+    hq.set_gemm_tile_n(tile_n)
+    E = len(masked)
+    a = bf16_rows(E * max_m, k, seed, spread=1)
+    w = torch.stack([bf16_rows(n, k, seed + 10 + e, std=0.03) for e in range(E)])
+    qa, sfa, qa_np, sfa_np = oracle_quant_to_device(a, mode)
+    qb, sfb, b_deq = stacked_weights_to_device(w, mode)
+    mm = torch.tensor(masked, dtype=torch.int32, device="cuda")
+    al = torch.tensor(alpha, dtype=torch.float32, device="cuda") if alpha is not None else None
+    out = sentinel_bf16((E * max_m, n))
+    hq.get_device_status(clear=True)
+    hq.hq_gemm_grouped_masked(qa, sfa, qb, sfb, mm, max_m, n, k, mode, alpha=al, out=out)
+    torch.cuda.synchronize()
+    status, _ = hq.get_device_status(clear=True)
+    ref, mag, written = ogemm.grouped_masked(oquant.dequantize(qa_np, sfa_np, mode), b_deq, masked, max_m,
+                                             alpha=alpha)
+    w_rows = np.nonzero(written)[0]
+    assert_gemm_close(out[torch.from_numpy(w_rows).cuda()], ref[w_rows], mag[w_rows], f"masked {mode}")
+    assert_rows_untouched(out, written, "masked")
+    return status
+
+
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4"])
+def test_grouped_masked_small(cuda_dev, tile_n, mode):
+    status = masked_case([256, 64, 0, 129, 1], 256, 256, 256, mode, tile_n,
+                         alpha=[1.0, 0.5, 2.0, 0.75, 1.5], seed=5)
+    assert status == 0
+
+
+def test_grouped_masked_clamps_and_flags(cuda_dev):
+    status = masked_case([300, -4, 128], 128, 256, 128, "mxfp8", seed=8)
+    assert status & hq.HQ_STATUS_MASK_CLAMPED
+
+
+def test_grouped_contig_flags_bad_offsets(cuda_dev):
+    hq.get_device_status(clear=True)
+    a = bf16_rows(512, 128, 1)
+    w = torch.stack([bf16_rows(128, 128, 2)])
+    qa, sfa, _, _ = oracle_quant_to_device(a, "mxfp8")
+    qb, sfb, _ = stacked_weights_to_device(w, "mxfp8")
+    off = torch.tensor([1000], dtype=torch.int32, device="cuda")   # beyond m_rows = 512
+    out = sentinel_bf16((512, 128))
+    hq.hq_gemm_grouped_contig(qa, sfa, qb, sfb, off, 512, 128, 128, "mxfp8", out=out)
+    status, _ = hq.get_device_status(clear=True)
+    assert status & hq.HQ_STATUS_BAD_OFFSETS
+
+
+# ----------------------------------------------------------------------------- full-size workloads
+
+
+def _sample(n, count, seed):
+    return np.sort(np.random.default_rng(seed).choice(n, min(count, n), replace=False))
+
+
+def test_full_dense_nvfp4_4096x12288x5120_sampled(cuda_dev):
+    cfg = synth.dense_nvfp4(device="cuda")
+    m, n, k = cfg["m"], cfg["n"], cfg["k"]
+    dev = torch.device("cuda")
+    qa, sfa = hq.hq_quant(cfg["a"], "nvfp4", global_scale=torch.tensor([cfg["g_a"]], device=dev))
+    qb, sfb = hq.hq_quant(cfg["b"], "nvfp4", global_scale=torch.tensor([cfg["g_b"]], device=dev))
+    out = hq.hq_gemm_dense(qa, sfa, qb, sfb, m, n, k, "nvfp4",
+                           alpha=torch.tensor([cfg["alpha"]], dtype=torch.float32, device=dev))
+    torch.cuda.synchronize()
+    rows, cols = _sample(m, 48, 1), _sample(n, 512, 2)
+    a_s = np_f32(cfg["a"][torch.from_numpy(rows).cuda()])
+    b_s = np_f32(cfg["b"][torch.from_numpy(cols).cuda()])
+    qa_np, sa_np = oquant.quantize(a_s, "nvfp4", cfg["g_a"])
+    qb_np, sb_np = oquant.quantize(b_s, "nvfp4", cfg["g_b"])
+    ref, mag = ogemm.dense(oquant.dequantize(qa_np, sa_np, "nvfp4"), oquant.dequantize(qb_np, sb_np, "nvfp4"),
+                           alpha=[cfg["alpha"]])
+    got = out[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()]
+    assert_gemm_close(got, ref, mag, "dense nvfp4 full size")
+
+
+def test_full_moe_contig_mxfp8_sampled(cuda_dev):
+    cfg = synth.moe_contig(device="cuda")
+    M, n, k, L = cfg["m"], cfg["n"], cfg["k"], cfg["L"]
+    off = torch.from_numpy(cfg["padded_offsets"]).cuda()
+    qa, sfa = hq.hq_quant(cfg["a"], "mxfp8")
+    qb, sfb = hq.hq_quant(cfg["b"].view(L * n, k), "mxfp8")
+    out = hq.hq_gemm_grouped_contig(qa, sfa, qb.view(L, n, k), sfb, off, M, n, k, "mxfp8")
+    torch.cuda.synchronize()
+    rows, cols = _sample(M, 64, 3), _sample(n, 384, 4)
+    grp = ogemm.group_of_rows_contig(cfg["padded_offsets"], M)
+    a_s = np_f32(cfg["a"][torch.from_numpy(rows).cuda()])
+    qa_np, sa_np = oquant.quantize(a_s, "mxfp8")
+    a_deq = oquant.dequantize(qa_np, sa_np, "mxfp8")
+    got = out[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()]
+    ref = np.zeros((len(rows), len(cols)))
+    mag = np.zeros_like(ref)
+    for g in np.unique(grp[rows]):
+        sel = grp[rows] == g
+        qb_np, sb_np = oquant.quantize(np_f32(cfg["b"][g][torch.from_numpy(cols).cuda()]), "mxfp8")
+        r, mg = ogemm.dense(a_deq[sel], oquant.dequantize(qb_np, sb_np, "mxfp8"))
+        ref[sel], mag[sel] = r, mg
+    assert_gemm_close(got, ref, mag, "moe contig full size")
+
+
+def test_full_moe_masked_nvfp4_sampled_and_untouched(cuda_dev):
+    cfg = synth.moe_masked(device="cuda")
+    E, max_m, n, k = cfg["E"], cfg["max_m"], cfg["n"], cfg["k"]
+    qa, sfa = hq.hq_quant(cfg["a"], "nvfp4")
+    qb, sfb = hq.hq_quant(cfg["b"].view(E * n, k), "nvfp4")
+    mm = torch.from_numpy(cfg["masked_m"]).cuda()
+    out = sentinel_bf16((E * max_m, n))
+    hq.hq_gemm_grouped_masked(qa, sfa, qb.view(E, n, k), sfb, mm, max_m, n, k, "nvfp4",
+                              alpha=cfg["alpha"], out=out)
+    torch.cuda.synchronize()
+    written = np.zeros(E * max_m, bool)
+    for e, c in enumerate(cfg["masked_m"]):
+        written[e * max_m: e * max_m + c] = True
+    # untouched rows, checked on the device over the whole output
+    unw = torch.from_numpy(~written).cuda()
+    assert bool((out.view(torch.int16)[unw] == -21846).all())
+    rows = _sample(E * max_m, 400, 5)
+    rows = rows[written[rows]][:64]
+    cols = _sample(n, 256, 6)
+    alpha = cfg["alpha"].cpu().numpy().astype(np.float64)
+    got = out[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()]
+    ref = np.zeros((len(rows), len(cols)))
+    mag = np.zeros_like(ref)
+    qa_np, sa_np = oquant.quantize(np_f32(cfg["a"][torch.from_numpy(rows).cuda()]), "nvfp4")
+    a_deq = oquant.dequantize(qa_np, sa_np, "nvfp4")
+    for i, r in enumerate(rows):
+        e = r // max_m
+        qb_np, sb_np = oquant.quantize(np_f32(cfg["b"][e][torch.from_numpy(cols).cuda()]), "nvfp4")
+        rr, mg = ogemm.dense(a_deq[i:i + 1], oquant.dequantize(qb_np, sb_np, "nvfp4"), alpha=[alpha[e]])
+        ref[i], mag[i] = rr[0], mg[0]
+    assert_gemm_close(got, ref, mag, "moe masked full size")

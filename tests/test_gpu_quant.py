@@ -1,0 +1,92 @@
+"""GPU parity of hq_quant against the oracle: quantised bytes and scale bytes
+must match bit for bit (SfAtom and row-major layouts, padding rows included)."""
+
+import numpy as np
+import pytest
+import torch
+
+import fp4_grouped_gemm_gb300 as hq
+import synth
+from oracle import quant as oquant
+
+from gpu_util import bf16_rows, np_f32
+
+pytestmark = pytest.mark.gpu
+
+
+def run_and_compare(x_cpu, mode, swizzle=True, g=None, rows_check=None):
+    dev = torch.device("cuda")
+    x = x_cpu.to(dev)
+    gs_t = torch.tensor([g], dtype=torch.float32, device=dev) if g is not None else None
+    m, k = x.shape
+    q_out = torch.full(((m, k) if mode == "mxfp8" else (m, k // 2)), 0xAA, dtype=torch.uint8, device=dev)
+    sf_out = torch.full((hq.sf_bytes(m, k, mode),), 0xAA, dtype=torch.uint8, device=dev)
+    hq.hq_quant(x, mode, use_swizzle=swizzle, global_scale=gs_t, q_out=q_out, sf_out=sf_out)
+    torch.cuda.synchronize()
+    if rows_check is None:
+        q_ref, sf_ref = oquant.group_wise_quant(np_f32(x_cpu), mode, swizzle, g)
+        q_gpu = q_out.cpu().numpy()
+        assert np.array_equal(q_gpu, q_ref), f"{mode} data bytes differ at {np.argwhere(q_gpu != q_ref)[:5]}"
+        sf_gpu = sf_out.cpu().numpy()
+        assert np.array_equal(sf_gpu, sf_ref), f"{mode} scale bytes differ at {np.argwhere(sf_gpu != sf_ref)[:5]}"
+    else:
+        # sampled rows of a large tensor: compare those rows' data and scales
+        rows = np.asarray(rows_check)
+        q_ref, sf_ref = oquant.quantize(np_f32(x_cpu[torch.from_numpy(rows)]), mode, g)
+        q_gpu = q_out[torch.from_numpy(rows).to(dev)].cpu().numpy()
+        assert np.array_equal(q_gpu, q_ref)
+        S = k // oquant.GROUP_SIZE[mode]
+        rr, ss = np.meshgrid(rows, np.arange(S), indexing="ij")
+        off = oquant.sfatom_offset(rr, ss, S) if swizzle else rr * S + ss
+        sf_gpu = sf_out.cpu().numpy()[off]
+        assert np.array_equal(sf_gpu, sf_ref)
+
+
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("swizzle", [True, False])
+@pytest.mark.parametrize("m,k", [(1, 128), (130, 256), (257, 512), (64, 1152)])
+def test_quant_small_bit_exact(cuda_dev, mode, swizzle, m, k):
+    x = bf16_rows(m, k, seed=m * 7 + k, spread=20)
+    run_and_compare(x, mode, swizzle)
+
+
+@pytest.mark.parametrize("g", [0.5, 3.0, 2688.0 / 7.5])
+def test_quant_nvfp4_global_scale(cuda_dev, g):
+    x = bf16_rows(200, 256, seed=5, spread=4)
+    run_and_compare(x, "nvfp4", True, g=float(np.float32(g)))
+
+
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4"])
+def test_quant_special_values(cuda_dev, mode):
+    k = 256
+    x = torch.zeros(8, k)
+    x[1] = 448.0                       # exact top of E4M3
+    x[2, :16] = -0.0
+    x[2, 16:] = 2.0 ** -133            # BF16 subnormal: tiny scales
+    x[3] = torch.linspace(-3e38, 3e38, k)  # near the BF16 maximum
+    x[4, ::2] = 6.0
+    x[4, 1::2] = -0.25                 # E2M1 ties
+    x[5] = torch.exp2(torch.arange(k) % 40 - 20.0)
+    x[6, 0] = 1.0                      # a lone value per row
+    x[7] = -x[5]
+    run_and_compare(x.to(torch.bfloat16), mode, True)
+
+
+def test_quant_dense_nvfp4_activation_full_size(cuda_dev):
+    cfg = synth.dense_nvfp4(device="cuda")
+    rows = np.random.default_rng(0).choice(cfg["m"], 96, replace=False)
+    run_and_compare(cfg["a"].cpu(), "nvfp4", True, g=cfg["g_a"], rows_check=np.sort(rows))
+
+
+def test_quant_moe_contig_activation_full_size(cuda_dev):
+    cfg = synth.moe_contig(device="cuda")
+    rows = np.random.default_rng(1).choice(cfg["m"], 96, replace=False)
+    run_and_compare(cfg["a"].cpu(), "mxfp8", True, rows_check=np.sort(rows))
+
+
+def test_quant_pdl_launch_matches(cuda_dev):
+    x = bf16_rows(300, 512, seed=9, spread=3).cuda()
+    q1, s1 = hq.hq_quant(x, "mxfp8", use_pdl=False)
+    q2, s2 = hq.hq_quant(x, "mxfp8", use_pdl=True)
+    torch.cuda.synchronize()
+    assert torch.equal(q1, q2) and torch.equal(s1, s2)

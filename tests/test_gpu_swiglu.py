@@ -1,0 +1,118 @@
+"""GPU parity of the fused SwiGLU + requantisation against the oracle.
+
+The GPU evaluates silu with CUDA's expf and the oracle with a correctly rounded
+exp, so the float32 activation may differ by an ulp.  Bytes must match except
+where the oracle's float64 value lies within a relative 2^-20 of the rounding
+boundary that separates the two codes; such boundary cases are counted and
+must stay rare.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import fp4_grouped_gemm_gb300 as hq
+from oracle import formats, glu, quant as oquant
+
+from gpu_util import bf16_rows, np_f32
+
+pytestmark = pytest.mark.gpu
+
+REL = 2.0 ** -20
+
+
+def unpack_q(q, mode, H):
+    return q if mode == "mxfp8" else formats.unpack_e2m1(q)
+
+
+def check_swiglu(x_cpu, mode, q_gpu, sf_gpu_flat, token_nums=None, rpe=None, g=None):
+    rows, two_h = x_cpu.shape
+    H = two_h // 2
+    ref = glu.swiglu_quant(np_f32(x_cpu), mode, token_nums, rpe, g)
+    kb = glu.swiglu_kb_dim(H, mode)
+    gs = oquant.GROUP_SIZE[mode]
+    written = ref["written"]
+    sf_gpu = oquant.from_sfatom(sf_gpu_flat, rows, kb)
+    # scale bytes: exact, or a one-step difference justified by a near-boundary amax
+    y64 = ref["y64"]
+    amax64 = np.abs(y64).reshape(rows, H // gs, gs).max(axis=2)
+    lo_b = oquant.quantize(np.repeat((amax64 * (1 - REL)).astype(np.float32), gs, axis=1), mode, g)[1]
+    hi_b = oquant.quantize(np.repeat((amax64 * (1 + REL)).astype(np.float32), gs, axis=1), mode, g)[1]
+    sf_ref = ref["sf_plain"][:, : H // gs]
+    sf_g = sf_gpu[:, : H // gs]
+    sf_ok = (sf_g == sf_ref) | (sf_g == lo_b) | (sf_g == hi_b)
+    assert sf_ok[written].all(), "scale bytes outside the boundary band"
+    assert not sf_gpu[written, H // gs:].any(), "padding scale columns must be zero"
+    n_sf_boundary = int(((sf_g != sf_ref) & written[:, None]).sum())
+    # element codes under the GPU's own scale bytes, with the same boundary band
+    codes_gpu = unpack_q(q_gpu, mode, H)
+    c_lo = glu.codes_with_scale(y64 * (1 - REL), mode, sf_g, g)
+    c_hi = glu.codes_with_scale(y64 * (1 + REL), mode, sf_g, g)
+    c_mid = glu.codes_with_scale(ref["y32"].astype(np.float64), mode, sf_g, g)
+    ok = (codes_gpu == c_mid) | (codes_gpu == c_lo) | (codes_gpu == c_hi)
+    assert ok[written].all(), f"element codes outside the boundary band at {np.argwhere(~ok & written[:, None])[:5]}"
+    n_el_boundary = int(((codes_gpu != c_mid) & written[:, None]).sum())
+    assert n_el_boundary <= max(2, 1e-4 * codes_gpu[written].size)
+    assert n_sf_boundary <= max(2, 1e-3 * sf_g[written].size)
+    return n_el_boundary, n_sf_boundary
+
+
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("rows,H", [(1, 128), (300, 256), (129, 1536)])
+def test_swiglu_quant_all_rows(cuda_dev, mode, rows, H):
+    x = bf16_rows(rows, 2 * H, seed=rows + H, std=2.0, spread=3)
+    q, sf = hq.hq_swiglu_quant(x.cuda(), mode)
+    torch.cuda.synchronize()
+    check_swiglu(x, mode, q.cpu().numpy(), sf.cpu().numpy())
+
+
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4"])
+def test_swiglu_quant_token_nums_untouched_rows(cuda_dev, mode):
+    E, rpe, H = 3, 100, 256
+    x = bf16_rows(E * rpe, 2 * H, seed=4, std=1.5)
+    tn = [100, 37, 0]
+    q = torch.full(((E * rpe, H) if mode == "mxfp8" else (E * rpe, H // 2)), 0xAA, dtype=torch.uint8, device="cuda")
+    kb = hq.swiglu_kb_dim(H, mode)
+    sf = torch.full((384 * kb,), 0xAA, dtype=torch.uint8, device="cuda")
+    hq.hq_swiglu_quant(x.cuda(), mode, token_nums=torch.tensor(tn, dtype=torch.int32, device="cuda"),
+                       rows_per_expert=rpe, q_out=q, sf_out=sf)
+    torch.cuda.synchronize()
+    qn, sfn = q.cpu().numpy(), sf.cpu().numpy()
+    written = np.zeros(E * rpe, bool)
+    written[0:100] = True
+    written[100:137] = True
+    assert (qn[~written] == 0xAA).all()
+    plain = oquant.from_sfatom(sfn, E * rpe, kb)
+    assert (plain[~written] == 0xAA).all()
+    check_swiglu(x, mode, qn, sfn, token_nums=tn, rpe=rpe)
+
+
+def test_swiglu_quant_mxfp8_kb_dim_padding(cuda_dev):
+    # H = 640: kb_dim = ceil(640/512)*16 = 32 > 640/32 = 20 -> columns 20..31 zero
+    x = bf16_rows(130, 1280, seed=6)
+    q, sf = hq.hq_swiglu_quant(x.cuda(), "mxfp8")
+    torch.cuda.synchronize()
+    check_swiglu(x, "mxfp8", q.cpu().numpy(), sf.cpu().numpy())
+
+
+def test_swiglu_nvfp4_global_scale(cuda_dev):
+    x = bf16_rows(256, 512, seed=7, std=3.0)
+    g = float(np.float32(37.5))
+    q, sf = hq.hq_swiglu_quant(x.cuda(), "nvfp4", global_scale=torch.tensor([g], device="cuda"))
+    torch.cuda.synchronize()
+    check_swiglu(x, "nvfp4", q.cpu().numpy(), sf.cpu().numpy(), g=g)
+
+
+def test_swiglu_moe_contig_output_full_size_sampled(cuda_dev):
+    rows, H = 17408, 1536
+    x = bf16_rows(rows, 2 * H, seed=8, std=1.0)
+    q, sf = hq.hq_swiglu_quant(x.cuda(), "mxfp8")
+    torch.cuda.synchronize()
+    pick = np.sort(np.random.default_rng(0).choice(rows // 128, 3, replace=False))
+    sfn = sf.cpu().numpy()
+    qn = q.cpu().numpy()
+    kb = hq.swiglu_kb_dim(H, "mxfp8")
+    for blk in pick:  # whole 128-row SfAtom blocks
+        r0 = int(blk) * 128
+        sub_sf = sfn[r0 * kb:(r0 + 128) * kb]
+        check_swiglu(x[r0:r0 + 128], "mxfp8", qn[r0:r0 + 128], sub_sf)
