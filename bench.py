@@ -1,0 +1,480 @@
+#!/usr/bin/env python
+"""Benchmark of the block-scaled MoE GEMM hot path on GB300.
+
+Headline workload (one step = one pass of the hot path over one batch):
+  dense NVFP4 W4A4 GEMM, M=4096 N=12288 K=5120: quantise A (BF16 -> NVFP4 with
+  its per-tensor global scale), quantise B (same), block-scaled GEMM with
+  alpha = 1/(g_A g_B), BF16 out.  value = 2 M N K / step time, in TFLOP/s.
+  Inputs are resident in HBM; L2 is flushed (256 MiB write) before every timed
+  step and the flush is outside the timed interval.
+
+Extra keys report, on one GPU, each kernel of the other workloads (dense MXFP8
+256^3 latency, grouped-contiguous MXFP8 + SwiGLU requant, grouped-masked NVFP4,
+BF16 grouped GEMM + dSwiGLU, and the quantiser's GB/s) against its roofline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl hq|reference]
+
+--impl reference times the CPU oracle (the only other implementation of this
+path) on a bounded sample of the same workload.  Under torchrun each rank runs
+an independent replica (the path has no exchange step); the time is the
+maximum over ranks and value sums the work of all ranks.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# nominal dense tensor-core ratios to BF16 (2.25 PFLOP/s): FP8 x2, FP4 x6
+RATIO = {"bf16": 1.0, "fp8": 2.0, "fp4": 6.0}
+
+
+def load_peaks():
+    if os.path.exists(PEAKS_FILE):
+        with open(PEAKS_FILE) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK, "fallback"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", default="hq", choices=["hq", "reference"])
+    p.add_argument("--main-only", action="store_true", help="skip the per-workload extras")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# --------------------------------------------------------------------------- distributed
+
+
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "hq" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws, device):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- clocks
+
+
+class Clocks:
+    """nvidia-smi sampling (200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [s.strip() for s in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        return rows
+
+    @staticmethod
+    def summarize(rows):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------- helpers
+
+
+class L2Flush:
+    def __init__(self, device, mib=256):
+        self.buf = torch.empty(mib * (1 << 20) // 4, dtype=torch.int32, device=device)
+
+    def __call__(self):
+        self.buf.add_(1)
+
+
+def time_kernel(fn, iters, flush=None, warmup=3):
+    """Average device time (s) of fn() over iters launches, L2 flushed before each."""
+    for _ in range(warmup):
+        fn()
+    st = torch.cuda.current_stream()
+    evs = []
+    for _ in range(iters):
+        if flush:
+            flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        fn()
+        b.record(st)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / iters / 1e3
+
+
+def oracle_cpu_baseline(budget_s=10.0, ms=64, ns=512):
+    """The CPU oracle on a bounded sample of the headline workload."""
+    from oracle import gemm as ogemm, quant as oquant
+    gen = torch.Generator().manual_seed(2)
+    k = 5120
+    a = torch.randn(ms, k, generator=gen).to(torch.bfloat16).float().numpy()
+    b = (torch.randn(ns, k, generator=gen) * 0.02).to(torch.bfloat16).float().numpy()
+    flops, t0, reps = 0.0, time.time(), 0
+    while True:
+        qa, sa = oquant.quantize(a, "nvfp4", 37.0)
+        qb, sb = oquant.quantize(b, "nvfp4", 1.0e4)
+        ogemm.dense(oquant.dequantize(qa, sa, "nvfp4"), oquant.dequantize(qb, sb, "nvfp4"), alpha=[1e-6])
+        flops += 2.0 * ms * ns * k
+        reps += 1
+        if time.time() - t0 >= budget_s:
+            break
+    dt = time.time() - t0
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        threads = len(os.sched_getaffinity(0))
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": int(threads), "kind": "oracle",
+            "sample": f"{reps} x (quantise A[{ms},{k}] and B[{ns},{k}] to NVFP4, dequantise, "
+                      f"float64 GEMM) in {dt:.1f} s, from the {4096}x{12288}x{5120} workload"}
+
+
+# --------------------------------------------------------------------------- reference arm
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    cfg_name = "dense_nvfp4_4096x12288x5120"
+    for _ in range(max(args.warmup, 0)):
+        oracle_cpu_baseline(budget_s=0.0, ms=16, ns=256)
+    vals = []
+    for _ in range(args.steps):
+        r = oracle_cpu_baseline(budget_s=0.0, ms=16, ns=256)
+        vals.append(r["value"])
+    base = dict(r) if args.steps else oracle_cpu_baseline(budget_s=0.0, ms=16, ns=256)
+    v = statistics.median(vals) if vals else base["value"]
+    base["value"] = v
+    base["sample"] = f"per step: {base['sample']}"
+    line = {"metric": "block-scaled GEMM TFLOP/s (hot-path step: quantise A and B, GEMM)",
+            "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference", "config": {"workload": cfg_name, "sample": base["sample"]},
+            "cpu_baseline": base,
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- workloads
+
+
+def headline(hq, dev, args, ws, peaks, pk_src):
+    cfg = synth.dense_nvfp4(device=dev)
+    m, n, k = cfg["m"], cfg["n"], cfg["k"]
+    flops = 2.0 * m * n * k
+    ga = torch.tensor([cfg["g_a"]], dtype=torch.float32, device=dev)
+    gb = torch.tensor([cfg["g_b"]], dtype=torch.float32, device=dev)
+    alpha = torch.tensor([cfg["alpha"]], dtype=torch.float32, device=dev)
+    qa = torch.empty(m, k // 2, dtype=torch.uint8, device=dev)
+    qb = torch.empty(n, k // 2, dtype=torch.uint8, device=dev)
+    sfa = torch.empty(hq.sf_bytes(m, k, "nvfp4"), dtype=torch.uint8, device=dev)
+    sfb = torch.empty(hq.sf_bytes(n, k, "nvfp4"), dtype=torch.uint8, device=dev)
+    out = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+    a, b = cfg["a"], cfg["b"]
+    st = torch.cuda.current_stream()
+
+    def step(gemm_events=None):
+        hq.hq_quant(a, "nvfp4", global_scale=ga, q_out=qa, sf_out=sfa)
+        hq.hq_quant(b, "nvfp4", global_scale=gb, q_out=qb, sf_out=sfb)
+        if gemm_events:
+            gemm_events[0].record(st)
+        hq.hq_gemm_dense(qa, sfa, qb, sfb, m, n, k, "nvfp4", alpha=alpha, out=out)
+        if gemm_events:
+            gemm_events[1].record(st)
+
+    flush = L2Flush(dev)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = Clocks(torch.cuda.current_device())
+    clocks.start()
+    barrier(ws)
+    torch.cuda.synchronize()
+    steps, gemms = [], []
+    for _ in range(args.steps):
+        flush()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        s0.record(st)
+        step(g)
+        s1.record(st)
+        steps.append((s0, s1))
+        gemms.append(g)
+    torch.cuda.synchronize()
+    barrier(ws)
+    rows = clocks.stop()
+    if len(rows) < 3:  # timed region shorter than the sampling period: continue the same step
+        clocks.start()
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            for _ in range(20):
+                step()
+            torch.cuda.synchronize()
+        rows += clocks.stop()
+    total = sum(a.elapsed_time(b) for a, b in steps) / 1e3
+    gemm_avg = sum(a.elapsed_time(b) for a, b in gemms) / len(gemms) / 1e3
+    total_max = max_over_ranks(total, ws, dev)
+    value = ws * args.steps * flops / total_max / 1e12
+    peak_fp4 = peaks["bf16_tflops"] * RATIO["fp4"]
+    achieved = flops / gemm_avg / 1e12
+
+    # end to end through the public API from pinned host buffers
+    a_h = a.cpu().pin_memory()
+    b_h = b.cpu().pin_memory()
+    out_h = torch.empty(m, n, dtype=torch.bfloat16).pin_memory()
+    a_d = torch.empty_like(a)
+    b_d = torch.empty_like(b)
+    e2e_steps = max(3, min(args.steps, 20))
+    evs = []
+    for i in range(e2e_steps + 2):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        a_d.copy_(a_h, non_blocking=True)
+        b_d.copy_(b_h, non_blocking=True)
+        hq.hq_quant(a_d, "nvfp4", global_scale=ga, q_out=qa, sf_out=sfa)
+        hq.hq_quant(b_d, "nvfp4", global_scale=gb, q_out=qb, sf_out=sfb)
+        hq.hq_gemm_dense(qa, sfa, qb, sfb, m, n, k, "nvfp4", alpha=alpha, out=out)
+        out_h.copy_(out, non_blocking=True)
+        e1.record(st)
+        if i >= 2:
+            evs.append((e0, e1))
+    torch.cuda.synchronize()
+    e2e_t = sum(x.elapsed_time(y) for x, y in evs) / len(evs) / 1e3
+    e2e_t = max_over_ranks(e2e_t, ws, dev)
+    h2d = (a.numel() + b.numel()) * 2
+    d2h = out.numel() * 2
+    return {
+        "value": value, "ms_per_step": total_max / args.steps * 1e3,
+        "config": {"workload": cfg["name"], "M": m, "N": n, "K": k, "mode": "nvfp4",
+                   "step": "hq_quant(A) + hq_quant(B) + hq_gemm_dense",
+                   "l2": "flushed (256 MiB write) before every timed step",
+                   "inputs": "A ~ N(0,1), B ~ N(0,0.02) BF16, seeded; g = 2688/amax per tensor"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_fp4, "unit": "TFLOP/s",
+                     "frac": achieved / peak_fp4, "traffic": None,
+                     "kernel": "bs_gemm_kernel<NVFP4,256>",
+                     "peak_source": f"{pk_src} bf16 burst {peaks['bf16_tflops']} x 6 (nominal FP4/BF16)"},
+        "e2e": {"value": ws * flops / e2e_t / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": Clocks.summarize(rows),
+        "gemm_ms": gemm_avg * 1e3,
+    }
+
+
+def extras(hq, dev, peaks):
+    """Kernel-level numbers for the other workloads (one GPU)."""
+    res = {}
+    flush = L2Flush(dev)
+    hbm = peaks["hbm_gbs"]
+    p_fp8 = peaks["bf16_tflops"] * RATIO["fp8"]
+    p_fp4 = peaks["bf16_tflops"] * RATIO["fp4"]
+    p_bf16 = peaks["bf16_tflops"]
+
+    # dense MXFP8 256^3: latency
+    c1 = synth.dense_small(device=dev)
+    qa, sfa = hq.hq_quant(c1["a"], "mxfp8")
+    qb, sfb = hq.hq_quant(c1["b"], "mxfp8")
+    out1 = torch.empty(256, 256, dtype=torch.bfloat16, device=dev)
+    t = time_kernel(lambda: hq.hq_gemm_dense(qa, sfa, qb, sfb, 256, 256, 256, "mxfp8", out=out1), 200)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(100):
+            hq.hq_gemm_dense(qa, sfa, qb, sfb, 256, 256, 256, "mxfp8", out=out1)
+    g.replay()
+    torch.cuda.synchronize()
+    tg = time_kernel(lambda: g.replay(), 10) / 100
+    res["dense_mxfp8_256"] = {"us_per_call": t * 1e6, "us_per_call_graph": tg * 1e6,
+                              "tflops": 2 * 256 ** 3 / t / 1e12}
+    del c1
+
+    # quantiser on the headline activation / weight shapes
+    c2 = synth.dense_nvfp4(device=dev)
+    for name, x in (("A", c2["a"]), ("B", c2["b"])):
+        m, k = x.shape
+        q = torch.empty(m, k // 2, dtype=torch.uint8, device=dev)
+        sf = torch.empty(hq.sf_bytes(m, k, "nvfp4"), dtype=torch.uint8, device=dev)
+        gsc = torch.tensor([1.0], device=dev)
+        t = time_kernel(lambda: hq.hq_quant(x, "nvfp4", global_scale=gsc, q_out=q, sf_out=sf), 20, flush)
+        byts = 2 * m * k + m * k // 2 + sf.numel()
+        res[f"quant_nvfp4_{name}_{m}x{k}"] = {"us": t * 1e6, "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / hbm}
+    del c2
+
+    # grouped contiguous MXFP8 + SwiGLU requant
+    c3 = synth.moe_contig(device=dev)
+    M, n, k, L = c3["m"], c3["n"], c3["k"], c3["L"]
+    qa, sfa = hq.hq_quant(c3["a"], "mxfp8")
+    qb, sfb = hq.hq_quant(c3["b"].view(L * n, k), "mxfp8")
+    t = time_kernel(lambda: hq.hq_quant(c3["a"], "mxfp8", q_out=qa, sf_out=sfa), 10, flush)
+    byts = 3 * M * k + sfa.numel()
+    res["quant_mxfp8_A_17408x4096"] = {"us": t * 1e6, "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / hbm}
+    off = torch.from_numpy(c3["padded_offsets"]).to(dev)
+    out3 = torch.empty(M, n, dtype=torch.bfloat16, device=dev)
+    qbv = qb.view(L, n, k)
+    t = time_kernel(lambda: hq.hq_gemm_grouped_contig(qa, sfa, qbv, sfb, off, M, n, k, "mxfp8", out=out3), 20, flush)
+    fl = 2.0 * M * n * k
+    res["moe_contig_mxfp8_L8"] = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_fp8": fl / t / 1e12 / p_fp8,
+                                 "tflops_routed_rows": 2.0 * 16384 * n * k / t / 1e12}
+    H = n // 2
+    qs = torch.empty(M, H, dtype=torch.uint8, device=dev)
+    sfs = torch.empty(M * hq.swiglu_kb_dim(H, "mxfp8"), dtype=torch.uint8, device=dev)
+    t = time_kernel(lambda: hq.hq_swiglu_quant(out3, "mxfp8", q_out=qs, sf_out=sfs), 20, flush)
+    byts = M * n * 2 + M * H + sfs.numel()
+    res["swiglu_quant_mxfp8_17408x3072"] = {"us": t * 1e6, "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / hbm}
+    del c3, qa, qb, out3, qs
+
+    # grouped masked NVFP4
+    c4 = synth.moe_masked(device=dev)
+    E, max_m, n, k = c4["E"], c4["max_m"], c4["n"], c4["k"]
+    qa, sfa = hq.hq_quant(c4["a"], "nvfp4")
+    qb, sfb = hq.hq_quant(c4["b"].view(E * n, k), "nvfp4")
+    mm = torch.from_numpy(c4["masked_m"]).to(dev)
+    out4 = torch.empty(E * max_m, n, dtype=torch.bfloat16, device=dev)
+    qbv = qb.view(E, n, k // 2)
+    t = time_kernel(lambda: hq.hq_gemm_grouped_masked(qa, sfa, qbv, sfb, mm, max_m, n, k, "nvfp4",
+                                                      alpha=c4["alpha"], out=out4), 20, flush)
+    valid = int(c4["masked_m"].sum())
+    tiles = int(sum(-(-int(c) // 128) for c in c4["masked_m"]))
+    fl = 2.0 * valid * n * k
+    byts = E * n * k // 2 + sfb.numel() + tiles * 128 * (k // 2 + k // 16) + valid * n * 2
+    res["moe_masked_nvfp4_E32"] = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_fp4": fl / t / 1e12 / p_fp4,
+                                  "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / hbm}
+    t = time_kernel(lambda: hq.hq_quant(c4["b"].view(E * n, k), "nvfp4", q_out=qb, sf_out=sfb), 5, flush)
+    byts = 2 * E * n * k + E * n * k // 2 + sfb.numel()
+    res["quant_nvfp4_W_131072x7168"] = {"us": t * 1e6, "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / hbm}
+    del c4, qa, qb, out4
+
+    # BF16 grouped GEMM + dSwiGLU
+    c5 = synth.dswiglu_bwd(device=dev)
+    M, n, k, L = c5["m"], c5["n"], c5["k"], c5["L"]
+    off = torch.from_numpy(c5["padded_offsets"]).to(dev)
+    dprob = torch.zeros(M, device=dev)
+    dbias = torch.zeros(L, 2 * n, dtype=torch.bfloat16, device=dev)
+    d_row = torch.empty(M, 2 * n, dtype=torch.bfloat16, device=dev)
+    ws_t = torch.empty(hq.hq_gemm_dswiglu_workspace_size(L, n), dtype=torch.uint8, device=dev)
+    t = time_kernel(lambda: hq.hq_gemm_dswiglu(c5["a"], c5["b"], c5["c"], off, c5["alpha"], c5["beta"],
+                                               c5["prob"], dprob, dbias=dbias, d_row=d_row, workspace=ws_t),
+                    20, flush)
+    fl = 2.0 * M * n * k
+    byts = M * k * 2 + L * n * k * 2 + 2 * M * 2 * n * 2 + M * 8
+    res["dswiglu_bwd_L16"] = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_bf16": fl / t / 1e12 / p_bf16,
+                             "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / hbm}
+    return res
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+    import __graft_entry__
+    __graft_entry__.build()
+    import fp4_grouped_gemm_gb300 as hq
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    peaks, pk_src = load_peaks()
+    h = headline(hq, dev, args, ws, peaks, pk_src)
+    line = {"metric": "block-scaled GEMM TFLOP/s (hot-path step: quantise A and B, GEMM)",
+            "value": h["value"], "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": h["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e2m1 (fp32 accumulate)",
+            "data": "synthetic", "config": h["config"], "roofline": h["roofline"], "e2e": h["e2e"],
+            "gpu_launches": h["gpu_launches"], "clocks": h["clocks"], "gemm_ms": h["gemm_ms"]}
+    if rank == 0 and ws == 1 and not args.main_only:
+        line["workloads"] = extras(hq, dev, peaks)
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

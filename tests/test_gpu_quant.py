@@ -63,7 +63,7 @@ def test_quant_special_values(cuda_dev, mode):
     x[1] = 448.0                       # exact top of E4M3
     x[2, :16] = -0.0
     x[2, 16:] = 2.0 ** -133            # BF16 subnormal: tiny scales
-    x[3] = torch.linspace(-3e38, 3e38, k)  # near the BF16 maximum
+    x[3] = torch.linspace(-1.0, 1.0, k) * 3e38  # near the BF16 maximum
     x[4, ::2] = 6.0
     x[4, 1::2] = -0.25                 # E2M1 ties
     x[5] = torch.exp2(torch.arange(k) % 40 - 20.0)
