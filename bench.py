@@ -41,6 +41,7 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # nominal dense tensor-core ratios to BF16 (2.25 PFLOP/s): FP8 x2, FP4 x6
 RATIO = {"bf16": 1.0, "fp8": 2.0, "fp4": 6.0}
+SECTIONS = ("dense_mxfp8_256", "quant_nvfp4", "moe_contig", "moe_masked", "dswiglu")
 
 
 def load_peaks():
@@ -59,6 +60,8 @@ def parse():
     p.add_argument("--impl", default="hq", choices=["hq", "reference"])
     p.add_argument("--main-only", action="store_true", help="skip the per-workload extras")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--only", choices=list(SECTIONS), default=None,
+                   help="run only one per-workload section (for profiling) and print its numbers")
     return p.parse_args()
 
 
@@ -346,104 +349,125 @@ def headline(hq, dev, args, ws, peaks, pk_src):
     }
 
 
-def extras(hq, dev, peaks):
-    """Kernel-level numbers for the other workloads (one GPU)."""
-    res = {}
-    flush = L2Flush(dev)
-    hbm = peaks["hbm_gbs"]
-    p_fp8 = peaks["bf16_tflops"] * RATIO["fp8"]
-    p_fp4 = peaks["bf16_tflops"] * RATIO["fp4"]
-    p_bf16 = peaks["bf16_tflops"]
+class Extras:
+    """Kernel-level numbers for the other workloads (one GPU), one method each."""
 
-    # dense MXFP8 256^3: latency
-    c1 = synth.dense_small(device=dev)
-    qa, sfa = hq.hq_quant(c1["a"], "mxfp8")
-    qb, sfb = hq.hq_quant(c1["b"], "mxfp8")
-    out1 = torch.empty(256, 256, dtype=torch.bfloat16, device=dev)
-    t = time_kernel(lambda: hq.hq_gemm_dense(qa, sfa, qb, sfb, 256, 256, 256, "mxfp8", out=out1), 200)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        for _ in range(100):
-            hq.hq_gemm_dense(qa, sfa, qb, sfb, 256, 256, 256, "mxfp8", out=out1)
-    g.replay()
-    torch.cuda.synchronize()
-    tg = time_kernel(lambda: g.replay(), 10) / 100
-    res["dense_mxfp8_256"] = {"us_per_call": t * 1e6, "us_per_call_graph": tg * 1e6,
-                              "tflops": 2 * 256 ** 3 / t / 1e12}
-    del c1
+    NAMES = SECTIONS
 
-    # quantiser on the headline activation / weight shapes
-    c2 = synth.dense_nvfp4(device=dev)
-    for name, x in (("A", c2["a"]), ("B", c2["b"])):
-        m, k = x.shape
-        q = torch.empty(m, k // 2, dtype=torch.uint8, device=dev)
-        sf = torch.empty(hq.sf_bytes(m, k, "nvfp4"), dtype=torch.uint8, device=dev)
-        gsc = torch.tensor([1.0], device=dev)
-        t = time_kernel(lambda: hq.hq_quant(x, "nvfp4", global_scale=gsc, q_out=q, sf_out=sf), 20, flush)
-        byts = 2 * m * k + m * k // 2 + sf.numel()
-        res[f"quant_nvfp4_{name}_{m}x{k}"] = {"us": t * 1e6, "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / hbm}
-    del c2
+    def __init__(self, hq, dev, peaks):
+        self.hq, self.dev = hq, dev
+        self.flush = L2Flush(dev)
+        self.hbm = peaks["hbm_gbs"]
+        self.p_fp8 = peaks["bf16_tflops"] * RATIO["fp8"]
+        self.p_fp4 = peaks["bf16_tflops"] * RATIO["fp4"]
+        self.p_bf16 = peaks["bf16_tflops"]
 
-    # grouped contiguous MXFP8 + SwiGLU requant
-    c3 = synth.moe_contig(device=dev)
-    M, n, k, L = c3["m"], c3["n"], c3["k"], c3["L"]
-    qa, sfa = hq.hq_quant(c3["a"], "mxfp8")
-    qb, sfb = hq.hq_quant(c3["b"].view(L * n, k), "mxfp8")
-    t = time_kernel(lambda: hq.hq_quant(c3["a"], "mxfp8", q_out=qa, sf_out=sfa), 10, flush)
-    byts = 3 * M * k + sfa.numel()
-    res["quant_mxfp8_A_17408x4096"] = {"us": t * 1e6, "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / hbm}
-    off = torch.from_numpy(c3["padded_offsets"]).to(dev)
-    out3 = torch.empty(M, n, dtype=torch.bfloat16, device=dev)
-    qbv = qb.view(L, n, k)
-    t = time_kernel(lambda: hq.hq_gemm_grouped_contig(qa, sfa, qbv, sfb, off, M, n, k, "mxfp8", out=out3), 20, flush)
-    fl = 2.0 * M * n * k
-    res["moe_contig_mxfp8_L8"] = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_fp8": fl / t / 1e12 / p_fp8,
-                                 "tflops_routed_rows": 2.0 * 16384 * n * k / t / 1e12}
-    H = n // 2
-    qs = torch.empty(M, H, dtype=torch.uint8, device=dev)
-    sfs = torch.empty(M * hq.swiglu_kb_dim(H, "mxfp8"), dtype=torch.uint8, device=dev)
-    t = time_kernel(lambda: hq.hq_swiglu_quant(out3, "mxfp8", q_out=qs, sf_out=sfs), 20, flush)
-    byts = M * n * 2 + M * H + sfs.numel()
-    res["swiglu_quant_mxfp8_17408x3072"] = {"us": t * 1e6, "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / hbm}
-    del c3, qa, qb, out3, qs
+    def run(self, names):
+        res = {}
+        for name in names:
+            res.update(getattr(self, name)())
+            torch.cuda.empty_cache()
+        return res
 
-    # grouped masked NVFP4
-    c4 = synth.moe_masked(device=dev)
-    E, max_m, n, k = c4["E"], c4["max_m"], c4["n"], c4["k"]
-    qa, sfa = hq.hq_quant(c4["a"], "nvfp4")
-    qb, sfb = hq.hq_quant(c4["b"].view(E * n, k), "nvfp4")
-    mm = torch.from_numpy(c4["masked_m"]).to(dev)
-    out4 = torch.empty(E * max_m, n, dtype=torch.bfloat16, device=dev)
-    qbv = qb.view(E, n, k // 2)
-    t = time_kernel(lambda: hq.hq_gemm_grouped_masked(qa, sfa, qbv, sfb, mm, max_m, n, k, "nvfp4",
-                                                      alpha=c4["alpha"], out=out4), 20, flush)
-    valid = int(c4["masked_m"].sum())
-    tiles = int(sum(-(-int(c) // 128) for c in c4["masked_m"]))
-    fl = 2.0 * valid * n * k
-    byts = E * n * k // 2 + sfb.numel() + tiles * 128 * (k // 2 + k // 16) + valid * n * 2
-    res["moe_masked_nvfp4_E32"] = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_fp4": fl / t / 1e12 / p_fp4,
-                                  "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / hbm}
-    t = time_kernel(lambda: hq.hq_quant(c4["b"].view(E * n, k), "nvfp4", q_out=qb, sf_out=sfb), 5, flush)
-    byts = 2 * E * n * k + E * n * k // 2 + sfb.numel()
-    res["quant_nvfp4_W_131072x7168"] = {"us": t * 1e6, "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / hbm}
-    del c4, qa, qb, out4
+    def dense_mxfp8_256(self):
+        hq, dev = self.hq, self.dev
+        c1 = synth.dense_small(device=dev)
+        qa, sfa = hq.hq_quant(c1["a"], "mxfp8")
+        qb, sfb = hq.hq_quant(c1["b"], "mxfp8")
+        out1 = torch.empty(256, 256, dtype=torch.bfloat16, device=dev)
+        t = time_kernel(lambda: hq.hq_gemm_dense(qa, sfa, qb, sfb, 256, 256, 256, "mxfp8", out=out1), 200)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(100):
+                hq.hq_gemm_dense(qa, sfa, qb, sfb, 256, 256, 256, "mxfp8", out=out1)
+        g.replay()
+        torch.cuda.synchronize()
+        tg = time_kernel(lambda: g.replay(), 10) / 100
+        return {"dense_mxfp8_256": {"us_per_call": t * 1e6, "us_per_call_graph": tg * 1e6,
+                                    "tflops": 2 * 256 ** 3 / t / 1e12}}
 
-    # BF16 grouped GEMM + dSwiGLU
-    c5 = synth.dswiglu_bwd(device=dev)
-    M, n, k, L = c5["m"], c5["n"], c5["k"], c5["L"]
-    off = torch.from_numpy(c5["padded_offsets"]).to(dev)
-    dprob = torch.zeros(M, device=dev)
-    dbias = torch.zeros(L, 2 * n, dtype=torch.bfloat16, device=dev)
-    d_row = torch.empty(M, 2 * n, dtype=torch.bfloat16, device=dev)
-    ws_t = torch.empty(hq.hq_gemm_dswiglu_workspace_size(L, n), dtype=torch.uint8, device=dev)
-    t = time_kernel(lambda: hq.hq_gemm_dswiglu(c5["a"], c5["b"], c5["c"], off, c5["alpha"], c5["beta"],
-                                               c5["prob"], dprob, dbias=dbias, d_row=d_row, workspace=ws_t),
-                    20, flush)
-    fl = 2.0 * M * n * k
-    byts = M * k * 2 + L * n * k * 2 + 2 * M * 2 * n * 2 + M * 8
-    res["dswiglu_bwd_L16"] = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_bf16": fl / t / 1e12 / p_bf16,
-                             "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / hbm}
-    return res
+    def quant_nvfp4(self):
+        hq, dev = self.hq, self.dev
+        res = {}
+        c2 = synth.dense_nvfp4(device=dev)
+        for name, x in (("A", c2["a"]), ("B", c2["b"])):
+            m, k = x.shape
+            q = torch.empty(m, k // 2, dtype=torch.uint8, device=dev)
+            sf = torch.empty(hq.sf_bytes(m, k, "nvfp4"), dtype=torch.uint8, device=dev)
+            gsc = torch.tensor([1.0], device=dev)
+            t = time_kernel(lambda: hq.hq_quant(x, "nvfp4", global_scale=gsc, q_out=q, sf_out=sf), 20, self.flush)
+            byts = 2 * m * k + m * k // 2 + sf.numel()
+            res[f"quant_nvfp4_{name}_{m}x{k}"] = {"us": t * 1e6, "gbs": byts / t / 1e9,
+                                                  "frac_hbm": byts / t / 1e9 / self.hbm}
+        return res
+
+    def moe_contig(self):
+        hq, dev = self.hq, self.dev
+        res = {}
+        c3 = synth.moe_contig(device=dev)
+        M, n, k, L = c3["m"], c3["n"], c3["k"], c3["L"]
+        qa, sfa = hq.hq_quant(c3["a"], "mxfp8")
+        qb, sfb = hq.hq_quant(c3["b"].view(L * n, k), "mxfp8")
+        t = time_kernel(lambda: hq.hq_quant(c3["a"], "mxfp8", q_out=qa, sf_out=sfa), 10, self.flush)
+        byts = 3 * M * k + sfa.numel()
+        res["quant_mxfp8_A_17408x4096"] = {"us": t * 1e6, "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / self.hbm}
+        off = torch.from_numpy(c3["padded_offsets"]).to(dev)
+        out3 = torch.empty(M, n, dtype=torch.bfloat16, device=dev)
+        qbv = qb.view(L, n, k)
+        t = time_kernel(lambda: hq.hq_gemm_grouped_contig(qa, sfa, qbv, sfb, off, M, n, k, "mxfp8", out=out3),
+                        20, self.flush)
+        fl = 2.0 * M * n * k
+        res["moe_contig_mxfp8_L8"] = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_fp8": fl / t / 1e12 / self.p_fp8,
+                                     "tflops_routed_rows": 2.0 * 16384 * n * k / t / 1e12}
+        H = n // 2
+        qs = torch.empty(M, H, dtype=torch.uint8, device=dev)
+        sfs = torch.empty(M * hq.swiglu_kb_dim(H, "mxfp8"), dtype=torch.uint8, device=dev)
+        t = time_kernel(lambda: hq.hq_swiglu_quant(out3, "mxfp8", q_out=qs, sf_out=sfs), 20, self.flush)
+        byts = M * n * 2 + M * H + sfs.numel()
+        res["swiglu_quant_mxfp8_17408x3072"] = {"us": t * 1e6, "gbs": byts / t / 1e9,
+                                                "frac_hbm": byts / t / 1e9 / self.hbm}
+        return res
+
+    def moe_masked(self):
+        hq, dev = self.hq, self.dev
+        res = {}
+        c4 = synth.moe_masked(device=dev)
+        E, max_m, n, k = c4["E"], c4["max_m"], c4["n"], c4["k"]
+        qa, sfa = hq.hq_quant(c4["a"], "nvfp4")
+        qb, sfb = hq.hq_quant(c4["b"].view(E * n, k), "nvfp4")
+        mm = torch.from_numpy(c4["masked_m"]).to(dev)
+        out4 = torch.empty(E * max_m, n, dtype=torch.bfloat16, device=dev)
+        qbv = qb.view(E, n, k // 2)
+        t = time_kernel(lambda: hq.hq_gemm_grouped_masked(qa, sfa, qbv, sfb, mm, max_m, n, k, "nvfp4",
+                                                          alpha=c4["alpha"], out=out4), 20, self.flush)
+        valid = int(c4["masked_m"].sum())
+        tiles = int(sum(-(-int(c) // 128) for c in c4["masked_m"]))
+        fl = 2.0 * valid * n * k
+        byts = E * n * k // 2 + sfb.numel() + tiles * 128 * (k // 2 + k // 16) + valid * n * 2
+        res["moe_masked_nvfp4_E32"] = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_fp4": fl / t / 1e12 / self.p_fp4,
+                                      "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / self.hbm}
+        t = time_kernel(lambda: hq.hq_quant(c4["b"].view(E * n, k), "nvfp4", q_out=qb, sf_out=sfb), 5, self.flush)
+        byts = 2 * E * n * k + E * n * k // 2 + sfb.numel()
+        res["quant_nvfp4_W_131072x7168"] = {"us": t * 1e6, "gbs": byts / t / 1e9,
+                                            "frac_hbm": byts / t / 1e9 / self.hbm}
+        return res
+
+    def dswiglu(self):
+        hq, dev = self.hq, self.dev
+        c5 = synth.dswiglu_bwd(device=dev)
+        M, n, k, L = c5["m"], c5["n"], c5["k"], c5["L"]
+        off = torch.from_numpy(c5["padded_offsets"]).to(dev)
+        dprob = torch.zeros(M, device=dev)
+        dbias = torch.zeros(L, 2 * n, dtype=torch.bfloat16, device=dev)
+        d_row = torch.empty(M, 2 * n, dtype=torch.bfloat16, device=dev)
+        ws_t = torch.empty(hq.hq_gemm_dswiglu_workspace_size(L, n), dtype=torch.uint8, device=dev)
+        t = time_kernel(lambda: hq.hq_gemm_dswiglu(c5["a"], c5["b"], c5["c"], off, c5["alpha"], c5["beta"],
+                                                   c5["prob"], dprob, dbias=dbias, d_row=d_row, workspace=ws_t),
+                        20, self.flush)
+        fl = 2.0 * M * n * k
+        byts = M * k * 2 + L * n * k * 2 + 2 * M * 2 * n * 2 + M * 8
+        return {"dswiglu_bwd_L16": {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_bf16": fl / t / 1e12 / self.p_bf16,
+                                    "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / self.hbm}}
 
 
 def main():
@@ -458,6 +482,9 @@ def main():
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     peaks, pk_src = load_peaks()
+    if args.only:
+        print(json.dumps({"only": args.only, "workloads": Extras(hq, dev, peaks).run([args.only])}), flush=True)
+        return
     h = headline(hq, dev, args, ws, peaks, pk_src)
     line = {"metric": "block-scaled GEMM TFLOP/s (hot-path step: quantise A and B, GEMM)",
             "value": h["value"], "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
@@ -466,7 +493,7 @@ def main():
             "data": "synthetic", "config": h["config"], "roofline": h["roofline"], "e2e": h["e2e"],
             "gpu_launches": h["gpu_launches"], "clocks": h["clocks"], "gemm_ms": h["gemm_ms"]}
     if rank == 0 and ws == 1 and not args.main_only:
-        line["workloads"] = extras(hq, dev, peaks)
+        line["workloads"] = Extras(hq, dev, peaks).run(Extras.NAMES)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_cpu_baseline()
     if rank == 0:
