@@ -29,7 +29,15 @@
 namespace hq {
 namespace {
 
-constexpr int kThreads = 192;
+// How scale atoms reach TMEM:
+//   0  the MMA thread issues tcgen05.cp (32x128b.warpx4) before its MMAs;
+//   1  a dedicated warp issues the tcgen05.cp and signals the MMA thread;
+//   2  four scale warps (one per TMEM lane quarter) read the atoms from shared
+//      memory and write them with tcgen05.st, replicated into every quarter
+//      exactly as the warpx4 copy would, then signal the MMA thread.
+constexpr int kSfPath = 2;
+constexpr int kSfWarps = kSfPath == 1 ? 1 : (kSfPath == 2 ? 4 : 0);
+constexpr int kThreads = 192 + 32 * kSfWarps;
 constexpr int kBKBytes = 128;   // bytes of K per stage and row (one 128B swizzle span)
 constexpr int kMmaKBytes = 32;  // bytes of K consumed by one MMA
 constexpr int kSmemLimit = 232448;
@@ -47,7 +55,9 @@ struct GemmParams {
   uint64_t wait_limit_ns;
 };
 
-template <int MODE, int BN, int STAGES, int ACC>
+// TABLE: entries of the per-CTA group table (0 for the dense GEMM, which
+// needs none and spends the shared memory on a deeper pipeline instead).
+template <int MODE, int BN, int STAGES, int ACC, int TABLE>
 struct Cfg {
   static constexpr int GS = MODE == HQ_MXFP8 ? 32 : 16;
   static constexpr int EPB = MODE == HQ_MXFP8 ? 1 : 2;            // elements per byte
@@ -72,9 +82,9 @@ struct Cfg {
   static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
   static constexpr int OFF_STAGE_OUT = OFF_SFB + STAGES * SFB_BYTES;  // 4 warps x 2 KB
-  static constexpr int OFF_TABLE = OFF_STAGE_OUT + 4 * 2048;          // 2 x (1024+1) int32
-  static constexpr int OFF_BAR = OFF_TABLE + 2 * (kMaxGroups + 1) * 4 + 8;
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC + 1;
+  static constexpr int OFF_TABLE = OFF_STAGE_OUT + 4 * 2048;          // 2 x TABLE int32
+  static constexpr int OFF_BAR = OFF_TABLE + 2 * TABLE * 4 + 8;
+  static constexpr int NUM_BARS = 3 * STAGES + 2 * ACC + 2;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget");
@@ -86,11 +96,11 @@ struct Cfg {
       | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
 };
 
-template <int MODE, int BN, int STAGES, int ACC>
+template <int MODE, int BN, int STAGES, int ACC, int TABLE>
 __global__ void __launch_bounds__(kThreads, 1)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
-  using C = Cfg<MODE, BN, STAGES, ACC>;
+  using C = Cfg<MODE, BN, STAGES, ACC, TABLE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -99,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   int32_t* tab0 = reinterpret_cast<int32_t*>(smem + C::OFF_TABLE);
-  int32_t* tab1 = tab0 + (kMaxGroups + 1);
+  int32_t* tab1 = tab0 + TABLE;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -107,6 +117,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + ACC + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * ACC);
+  const uint32_t drain_sf_bar = drain_bar + 8u;
+  auto sfready_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * ACC + 2 + s); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   int64_t* total_mtiles_s = reinterpret_cast<int64_t*>(smem + C::OFF_MISC + 8);
@@ -122,6 +134,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tempty_bar(a), 4);
     }
     mbar_init(drain_bar, 1);
+    mbar_init(drain_sf_bar, 1);
+    for (int s = 0; s < STAGES; ++s) mbar_init(sfready_bar(s), kSfPath == 2 ? 4 : 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -201,19 +215,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!wait_bounded(full_bar(stage), phase, wctx)) { ok = false; break; }
+          // kSfPath 0: this thread stages the scales; otherwise the scale
+          // warp(s) signal sfready after the stage's scales are in TMEM
+          const uint32_t ready = kSfPath == 0 ? full_bar(stage) : sfready_bar(stage);
+          if (!wait_bounded(ready, phase, wctx)) { ok = false; break; }
           tc_fence_after();
           int atoms = atoms_total - kb * C::ATOMS;
           atoms = atoms < C::ATOMS ? atoms : C::ATOMS;
           const uint32_t sfa_t = tmem_base + C::SF_BASE_COL + stage * C::SF_STAGE_COLS;
           const uint32_t sfb_t = sfa_t + C::SFA_COLS;
-          const uint32_t sfa_s = sbase + C::OFF_SFA + stage * C::SFA_BYTES;
-          const uint32_t sfb_s = sbase + C::OFF_SFB + stage * C::SFB_BYTES;
-          for (int a = 0; a < atoms; ++a) {
-            tc_cp_32x128b_warpx4(sfa_t + a * 4, smem_desc_sfatom(sfa_s + a * 512));
-            for (int rb = 0; rb < rb_valid; ++rb)
-              tc_cp_32x128b_warpx4(sfb_t + (a * C::RB + rb) * 4,
-                                   smem_desc_sfatom(sfb_s + (rb * C::ATOMS + a) * 512));
+          if (kSfPath == 0) {
+            const uint32_t sfa_s = sbase + C::OFF_SFA + stage * C::SFA_BYTES;
+            const uint32_t sfb_s = sbase + C::OFF_SFB + stage * C::SFB_BYTES;
+            for (int a = 0; a < atoms; ++a) {
+              tc_cp_32x128b_warpx4(sfa_t + a * 4, smem_desc_sfatom(sfa_s + a * 512));
+              for (int rb = 0; rb < rb_valid; ++rb)
+                tc_cp_32x128b_warpx4(sfb_t + (a * C::RB + rb) * 4,
+                                     smem_desc_sfatom(sfb_s + (rb * C::ATOMS + a) * 512));
+            }
           }
           const uint32_t a_s = sbase + C::OFF_A + stage * C::A_BYTES;
           const uint32_t b_s = sbase + C::OFF_B + stage * C::B_BYTES;
@@ -244,6 +263,86 @@ __global__ void __launch_bounds__(kThreads, 1)
       // all tcgen05 work issued by this thread is complete before TMEM is freed
       tc_commit(drain_bar);
       wait_drain(drain_bar, 0, p.wait_limit_ns);
+    }
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ scale staging
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; ok && t < sch.total_tiles; t += gridDim.x) {
+      const TileInfo ti = decode_tile(p.gs, sch, t, BN);
+      int rb_valid = static_cast<int>((p.n - ti.n0 + 127) / 128);
+      rb_valid = rb_valid < C::RB ? rb_valid : C::RB;
+      for (int kb = 0; kb < num_kb; ++kb) {
+        int atoms = atoms_total - kb * C::ATOMS;
+        atoms = atoms < C::ATOMS ? atoms : C::ATOMS;
+        const uint32_t sfa_t = tmem_base + C::SF_BASE_COL + stage * C::SF_STAGE_COLS;
+        const uint32_t sfb_t = sfa_t + C::SFA_COLS;
+        const uint32_t sfa_s = sbase + C::OFF_SFA + stage * C::SFA_BYTES;
+        const uint32_t sfb_s = sbase + C::OFF_SFB + stage * C::SFB_BYTES;
+        if (kSfPath == 1) {
+          if (lane == 0) {
+            ok = wait_bounded(full_bar(stage), phase, wctx);
+            if (ok) {
+              tc_fence_after();
+              for (int a = 0; a < atoms; ++a) {
+                tc_cp_32x128b_warpx4(sfa_t + a * 4, smem_desc_sfatom(sfa_s + a * 512));
+                for (int rb = 0; rb < rb_valid; ++rb)
+                  tc_cp_32x128b_warpx4(sfb_t + (a * C::RB + rb) * 4,
+                                       smem_desc_sfatom(sfb_s + (rb * C::ATOMS + a) * 512));
+              }
+              tc_commit(sfready_bar(stage));
+            }
+          }
+          ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        } else {
+          const bool w = wait_bounded(full_bar(stage), phase, wctx);
+          ok = __all_sync(0xFFFFFFFFu, w);
+          if (!ok) break;
+          // lane i carries row i of each 512-byte atom: 16 bytes = 4 columns
+          const uint32_t lq = static_cast<uint32_t>(q * 32) << 16;
+          if (atoms == C::ATOMS && rb_valid == C::RB) {
+            // whole k-block: all loads first, then one wide store per operand
+            constexpr int NA = 4 * C::ATOMS;
+            constexpr int NB = 4 * C::ATOMS * C::RB;
+            uint32_t va[NA], vb[NB];
+#pragma unroll
+            for (int a = 0; a < C::ATOMS; ++a) {
+              lds128(sfa_s + a * 512 + lane * 16, va + 4 * a);
+#pragma unroll
+              for (int rb = 0; rb < C::RB; ++rb)
+                lds128(sfb_s + (rb * C::ATOMS + a) * 512 + lane * 16, vb + 4 * (a * C::RB + rb));
+            }
+            tmem_st_32x32b<NA>(lq + sfa_t, va);
+            tmem_st_32x32b<NB>(lq + sfb_t, vb);
+          } else {
+          for (int a = 0; a < atoms; ++a) {
+            uint32_t v0, v1, v2, v3;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+                         : "r"(sfa_s + a * 512 + lane * 16));
+            tmem_st_32x32b_x4(lq + sfa_t + a * 4, v0, v1, v2, v3);
+            for (int rb = 0; rb < rb_valid; ++rb) {
+              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+                           : "r"(sfb_s + (rb * C::ATOMS + a) * 512 + lane * 16));
+              tmem_st_32x32b_x4(lq + sfb_t + (a * C::RB + rb) * 4, v0, v1, v2, v3);
+            }
+          }
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sfready_bar(stage));
+        }
+        if (!ok) break;
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (kSfPath == 1 && lane == 0) {
+      tc_commit(drain_sf_bar);
+      wait_drain(drain_sf_bar, 0, p.wait_limit_ns);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -338,10 +437,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // host side
 // ---------------------------------------------------------------------------
 
-template <int MODE, int BN, int STAGES, int ACC>
+template <int MODE, int BN, int STAGES, int ACC, int TABLE>
 int run_bs(const void* a, const void* b, const GemmParams& p0, int sm_count, bool pdl,
            cudaStream_t st) {
-  using C = Cfg<MODE, BN, STAGES, ACC>;
+  using C = Cfg<MODE, BN, STAGES, ACC, TABLE>;
   GemmParams p = p0;
   const uint64_t kbytes = static_cast<uint64_t>(p.k) / C::EPB;
   CUtensorMap tmA, tmB;
@@ -361,7 +460,7 @@ int run_bs(const void* a, const void* b, const GemmParams& p0, int sm_count, boo
                                strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != HQ_OK) return rc;
   }
-  auto kern = bs_gemm_kernel<MODE, BN, STAGES, ACC>;
+  auto kern = bs_gemm_kernel<MODE, BN, STAGES, ACC, TABLE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
       cudaSuccess)
     return HQ_ERR_CUDA;
@@ -387,12 +486,18 @@ int run_gemm(hq_mode mode, const void* a, const void* b, const GemmParams& p, in
   int bn = forced_tile_n();
   if (bn == 0) bn = (p.n % 256 == 0) ? 256 : 128;
   if (bn == 256 && p.n % 256 != 0 && p.n < 256) bn = 128;
+  constexpr int T = kMaxGroups + 1;
+  const bool dense = p.gs.sched == kDense;
   if (mode == HQ_MXFP8) {
-    if (bn == 256) return run_bs<HQ_MXFP8, 256, 4, 1>(a, b, p, sm_count, pdl, st);
-    return run_bs<HQ_MXFP8, 128, 6, 2>(a, b, p, sm_count, pdl, st);
+    if (bn == 256) return dense ? run_bs<HQ_MXFP8, 256, 4, 1, 0>(a, b, p, sm_count, pdl, st)
+                                : run_bs<HQ_MXFP8, 256, 4, 1, T>(a, b, p, sm_count, pdl, st);
+    return dense ? run_bs<HQ_MXFP8, 128, 6, 2, 0>(a, b, p, sm_count, pdl, st)
+                 : run_bs<HQ_MXFP8, 128, 6, 2, T>(a, b, p, sm_count, pdl, st);
   }
-  if (bn == 256) return run_bs<HQ_NVFP4, 256, 3, 1>(a, b, p, sm_count, pdl, st);
-  return run_bs<HQ_NVFP4, 128, 5, 2>(a, b, p, sm_count, pdl, st);
+  if (bn == 256) return dense ? run_bs<HQ_NVFP4, 256, 4, 1, 0>(a, b, p, sm_count, pdl, st)
+                              : run_bs<HQ_NVFP4, 256, 3, 1, T>(a, b, p, sm_count, pdl, st);
+  return dense ? run_bs<HQ_NVFP4, 128, 5, 2, 0>(a, b, p, sm_count, pdl, st)
+               : run_bs<HQ_NVFP4, 128, 5, 2, T>(a, b, p, sm_count, pdl, st);
 }
 
 // Host-side checks shared by the three entry points.
