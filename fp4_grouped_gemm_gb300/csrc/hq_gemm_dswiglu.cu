@@ -24,6 +24,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "hq_internal.h"
 #include "hq_ptx.cuh"
 #include "hq_sched.cuh"
@@ -390,3 +392,62 @@ int hq_gemm_dswiglu(const hq_bf16* a, const hq_bf16* b, const hq_bf16* c,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of hq_gemm_dswiglu.
+//
+// The dbias partial sums need float32 scratch.  hq_gemm_dswiglu takes it from
+// the caller; this variant instead uses one fixed array in device global
+// memory that belongs to the library, so a caller that cannot allocate device
+// memory can still get dbias.  Every GPU that loads the library holds this
+// array (1 MiB) until the process exits.
+// ---------------------------------------------------------------------------
+namespace hq {
+namespace {
+
+constexpr size_t kNoAllocScratchFloats = 262144;  // 1 MiB: L * 2n <= 262144
+
+static __device__ __align__(256) float g_dswiglu_scratch[kNoAllocScratchFloats];
+
+constexpr int kMaxDev = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDev] = {};
+
+// Device address of g_dswiglu_scratch on the current device.  Host code must
+// not use the symbol itself (on the host it names a stand-in, not device
+// memory); the address is resolved once per device, with that device current.
+void* scratch_address() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_dswiglu_scratch) != cudaSuccess || !ptr) return nullptr;
+    g_scratch_addr[dev] = ptr;
+  }
+  return g_scratch_addr[dev];
+}
+
+}  // namespace
+}  // namespace hq
+
+extern "C" int hq_gemm_dswiglu_noalloc(const hq_bf16* a, const hq_bf16* b, const hq_bf16* c,
+                                       const int32_t* padded_offsets, int L, const float* alpha,
+                                       const float* beta, const float* prob, hq_bf16* d_row,
+                                       float* dprob, hq_bf16* dbias, int64_t m, int64_t n,
+                                       int64_t k, int sm_count, hq_stream_t s) {
+  if (L < 1 || n <= 0) return HQ_ERR_INVALID;
+  if (dbias && static_cast<uint64_t>(L) * static_cast<uint64_t>(2 * n) > hq::kNoAllocScratchFloats)
+    return HQ_ERR_UNSUPPORTED;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  if (dbias) {
+    ws = hq::scratch_address();
+    if (!ws) return HQ_ERR_CUDA;
+    ws_bytes = sizeof(float) * hq::kNoAllocScratchFloats;
+  }
+  // hq_gemm_dswiglu validates the rest and clears the used part of the
+  // scratch on the stream before the GEMM accumulates into it.
+  return hq_gemm_dswiglu(a, b, c, padded_offsets, L, alpha, beta, prob, d_row, dprob, dbias, m, n, k,
+                         ws, ws_bytes, sm_count, s);
+}

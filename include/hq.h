@@ -261,6 +261,36 @@ int hq_gemm_dswiglu(const hq_bf16 *a, const hq_bf16 *b, const hq_bf16 *c,
  * up to 256 bytes. */
 size_t hq_gemm_dswiglu_workspace_size(int L, int64_t n);
 
+/* ------------------------------------------------------------------------- *
+ * hq_gemm_dswiglu without caller-provided scratch.  The paper has no
+ * counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory -- for example a plugin or custom op loaded into a
+ * host framework that owns every device allocation and hands it only its
+ * inputs and outputs, or code that must not call cudaMalloc because that can
+ * synchronise the device and stall other work already running on it.
+ *
+ * Same arguments and results as hq_gemm_dswiglu, minus workspace/ws_bytes.
+ * The dbias partial sums go to a fixed scratch array inside the library:
+ * 1 MiB of device memory (262144 floats) that every GPU which loads
+ * libhq.so holds until the process exits.  dbias therefore needs
+ * L * 2n <= 262144; larger requests return HQ_ERR_UNSUPPORTED before
+ * anything is launched (dbias == NULL has no limit).  The call allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * The first call on a device resolves the scratch array's device address
+ * (once per device, with that device current); make that first call before
+ * any stream capture.  Every call clears the part of the scratch it uses
+ * before accumulating into it, because the array keeps the previous call's
+ * contents.  All calls share the one array, so two calls whose work overlaps
+ * on the GPU (different streams, no ordering between them) race on it and
+ * their dbias results are undefined; order such calls on one stream or with
+ * events. */
+int hq_gemm_dswiglu_noalloc(const hq_bf16 *a, const hq_bf16 *b, const hq_bf16 *c,
+                            const int32_t *padded_offsets, int L, const float *alpha,
+                            const float *beta, const float *prob, hq_bf16 *d_row, float *dprob,
+                            hq_bf16 *dbias, int64_t m, int64_t n, int64_t k, int sm_count,
+                            hq_stream_t s);
+
 #ifdef __cplusplus
 }
 #endif
