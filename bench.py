@@ -5,8 +5,9 @@ Headline workload (one step = one pass of the hot path over one batch):
   dense NVFP4 W4A4 GEMM, M=4096 N=12288 K=5120: quantise A (BF16 -> NVFP4 with
   its per-tensor global scale), quantise B (same), block-scaled GEMM with
   alpha = 1/(g_A g_B), BF16 out.  value = 2 M N K / step time, in TFLOP/s.
-  Inputs are resident in HBM; L2 is flushed (256 MiB write) before every timed
-  step and the flush is outside the timed interval.
+  Inputs are resident in HBM; L2 is flushed (256 MiB written, then another
+  256 MiB read, so no dirty lines remain) before every timed step, outside the
+  timed interval.
 
 Extra keys report, on one GPU, each kernel of the other workloads (dense MXFP8
 256^3 latency, grouped-contiguous MXFP8 + SwiGLU requant, grouped-masked NVFP4,
@@ -163,11 +164,19 @@ class Clocks:
 
 
 class L2Flush:
+    """Evicts L2 before a timed launch: writes one 256 MiB buffer, then reads
+    another, so the timed kernel starts with a cold cache holding only clean
+    lines (no write-backs of the flush itself land inside the timed region)."""
+
     def __init__(self, device, mib=256):
-        self.buf = torch.empty(mib * (1 << 20) // 4, dtype=torch.int32, device=device)
+        n = mib * (1 << 20) // 4
+        self.buf = torch.empty(n, dtype=torch.int32, device=device)
+        self.buf2 = torch.ones(n, dtype=torch.int32, device=device)
+        self.sink = torch.empty((), dtype=torch.int64, device=device)
 
     def __call__(self):
         self.buf.add_(1)
+        torch.sum(self.buf2, dim=0, out=self.sink)
 
 
 def time_kernel(fn, iters, flush=None, warmup=3):
@@ -335,7 +344,7 @@ def headline(hq, dev, args, ws, peaks, pk_src):
         "value": value, "ms_per_step": total_max / args.steps * 1e3,
         "config": {"workload": cfg["name"], "M": m, "N": n, "K": k, "mode": "nvfp4",
                    "step": "hq_quant(A) + hq_quant(B) + hq_gemm_dense",
-                   "l2": "flushed (256 MiB write) before every timed step",
+                   "l2": "flushed before every timed step (256 MiB written, then 256 MiB read)",
                    "inputs": "A ~ N(0,1), B ~ N(0,0.02) BF16, seeded; g = 2688/amax per tensor"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_fp4, "unit": "TFLOP/s",
                      "frac": achieved / peak_fp4, "traffic": None,

@@ -12,7 +12,8 @@
 // Persistent warp-specialised kernel: warp 0 streams A / B tiles with TMA into
 // a ring of shared-memory stages, warp 1 issues the MMAs into one of two TMEM
 // accumulators (so the epilogue of tile i overlaps the main loop of tile i+1),
-// warps 2..5 run the epilogue.  A compact tile of 128 columns j maps to the
+// warps 2..9 run the epilogue (two per TMEM lane quarter, each owning two of
+// the tile's four 32-column chunks).  A compact tile of 128 columns j maps to the
 // 256 C / D_row columns [2 j0, 2 j0 + 256).  Each epilogue thread owns one
 // row: it reads that row's C segment, writes its D_row segment, accumulates
 // its dprob partial (one float atomic per row and tile), and, when dbias is
@@ -33,10 +34,11 @@
 namespace hq {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;      // two per TMEM lane quarter, each owning half the columns
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kBN = 128;          // compact columns per tile
 constexpr int kBKElems = 64;      // BF16 elements of K per stage (128 bytes)
-constexpr int kStages = 5;
+constexpr int kStages = 4;
 constexpr int kAcc = 2;
 constexpr int kTmemCols = kAcc * kBN;
 constexpr int kABytes = kBM * kBKElems * 2;
@@ -45,7 +47,7 @@ constexpr int kTransStride = 65;  // floats per row of the dbias transpose buffe
 constexpr int kOffA = 0;
 constexpr int kOffB = kOffA + kStages * kABytes;
 constexpr int kOffTrans = kOffB + kStages * kBBytes;
-constexpr int kOffTable = kOffTrans + 4 * 32 * kTransStride * 4;
+constexpr int kOffTable = kOffTrans + kEpiWarps * 32 * kTransStride * 4;
 constexpr int kOffBar = (kOffTable + 2 * (kMaxGroups + 1) * 4 + 15) / 16 * 16;
 constexpr int kNumBars = 2 * kStages + 2 * kAcc + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -69,6 +71,11 @@ struct DsParams {
   uint64_t wait_limit_ns;
 };
 
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
@@ -102,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < kAcc; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4);
+      mbar_init(tempty_bar(a), kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     fence_mbar_init();
@@ -177,57 +184,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_drain(drain_bar, 0, p.wait_limit_ns);
     }
   } else {
-    const int q = warp & 3;
+    const int q = warp & 3;                  // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;        // which two of the four 32-column chunks
     float* trans = reinterpret_cast<float*>(smem + kOffTrans) + (warp - 2) * 32 * kTransStride;
     const int64_t two_n = 2 * p.n;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int64_t t = blockIdx.x; t < sch.total_tiles; t += gridDim.x) {
       const TileInfo ti = decode_tile(p.gs, sch, t, kBN);
-      const bool ok = wait_bounded(tfull_bar(acc), acc_phase, wctx);
-      if (!__all_sync(0xFFFFFFFFu, ok)) break;
-      tc_fence_after();
       const int r_local = q * 32 + lane;
       const bool row_ok = r_local < ti.rows_valid;
       const int64_t row = ti.row0 + r_local;
+      // this warp's C segments (2 chunks x 64 columns of the row) are loaded
+      // before the accumulator is ready, so their latency overlaps the wait
+      uint4 cv[2][8];
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int64_t j0 = ti.n0 + (2 * half + cc) * 32;
+        const bool ld = row_ok && j0 < p.n;
+        const uint4* src = reinterpret_cast<const uint4*>(p.c + row * two_n + 2 * j0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cv[cc][i] = ld ? __ldcs(src + i) : make_uint4(0, 0, 0, 0);
+      }
       const float alpha = __ldg(p.alpha + ti.g);
       const float a2 = __fmul_rn(alpha, alpha);
       const float beta = __ldg(p.beta + ti.g);
       const float prob = row_ok ? __ldg(p.prob + row) : 0.0f;
+      const bool ok = wait_bounded(tfull_bar(acc), acc_phase, wctx);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      tc_fence_after();
       float dprob_part = 0.0f;
-      for (int c = 0; c < kBN / 32; ++c) {
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * half + cc;
         const int64_t j0 = ti.n0 + c * 32;
         uint32_t r[32];
         tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN + c * 32,
                            r);
-        if (j0 >= p.n) {  // past the last compact column (n % 32 == 0: whole chunk)
-          tmem_ld_wait();
-          continue;
-        }
-        uint4 cv[8];
-        const int64_t cbase = row * two_n + 2 * j0;  // gate block start; input at +32
-        if (row_ok) {
-          const uint4* src = reinterpret_cast<const uint4*>(p.c + cbase);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) cv[i] = __ldcs(src + i);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) cv[i] = make_uint4(0, 0, 0, 0);
-        }
         tmem_ld_wait();
+        if (j0 >= p.n) continue;  // past the last compact column (n % 32 == 0: whole chunk)
+        const int64_t cbase = row * two_n + 2 * j0;  // gate block start; input at +32
         uint32_t dg[16], di[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          // element pair (2i, 2i+1): gate words in cv[0..3], input words in cv[4..7]
-          const uint32_t gw = reinterpret_cast<const uint32_t*>(cv)[i];
-          const uint32_t iw = reinterpret_cast<const uint32_t*>(cv)[16 + i];
+          // element pair (2i, 2i+1): gate words in cv[cc][0..3], input words in cv[cc][4..7]
+          const uint32_t gw = reinterpret_cast<const uint32_t*>(cv[cc])[i];
+          const uint32_t iw = reinterpret_cast<const uint32_t*>(cv[cc])[16 + i];
           float outg[2], outi[2];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const float gate = __fmul_rn(beta, h ? bf16_hi(gw) : bf16_lo(gw));
             const float inp = __fmul_rn(beta, h ? bf16_hi(iw) : bf16_lo(iw));
             const float R = __fmul_rn(a2, __uint_as_float(r[2 * i + h]));
-            const float s = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-gate)));
+            const float s = rcp_approx(__fadd_rn(1.0f, expf(-gate)));  // sigmoid(gate)
             const float rp = __fmul_rn(R, prob);
             outg[h] = rp * inp * s * (1.0f + gate * (1.0f - s));
             outi[h] = rp * gate * s;

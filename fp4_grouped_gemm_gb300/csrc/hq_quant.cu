@@ -1,14 +1,15 @@
 // hq_quant.cu -- the group-wise quantiser (hq_quant) and the fused SwiGLU +
 // requantisation pass (hq_swiglu_quant).
 //
-// Both are HBM-bound streaming passes.  A warp handles a 256-element segment of
-// one row per step: every lane loads 16 bytes (8 BF16 values; the SwiGLU pass
-// loads 8 gate and 8 up values), the lanes of one scale group (4 lanes for a
-// 32-element MXFP8 group, 2 for a 16-element NVFP4 group) reduce |x| with
-// shuffles, derive the scale byte, encode their 8 elements and store them with
-// one 8-byte (E4M3) or 4-byte (packed E2M1) store, so each warp writes a
-// contiguous 256- or 128-byte run.  The first lane of a group writes its
-// scale byte at the SfAtom (or row-major) position.
+// Both are HBM-bound streaming passes.  Each lane owns whole scale groups
+// (32 values for MXFP8, 16 for NVFP4): it loads the group with 16-byte loads
+// (the SwiGLU pass also loads the matching up values), takes |x|max locally,
+// derives the scale byte, encodes the group and stores it with 16-byte (E4M3)
+// or 8-byte (packed E2M1) stores; a warp step covers 32 consecutive groups of
+// one row.  Four consecutive groups share one 32-bit word of the SfAtom (and
+// row-major) scale layout; their bytes are gathered by shuffles and written
+// with one 4-byte store.  NVFP4's per-group multiplier g / value(UE4M3) comes
+// from a 128-entry table each CTA builds once with IEEE division.
 //
 // Scale rule (cuDNN frontend "Grouped GEMM + dGLU (SM100)", Step 3, with the
 // HALOps group_wise_quant encodings), evaluated in IEEE float32:
@@ -27,7 +28,7 @@ namespace hq {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kSegElems = 256;  // elements per warp step (32 lanes x 8)
+constexpr int kGroupsPerWarpStep = 32;  // one scale group per lane
 
 struct QuantParams {
   const uint16_t* in;        // BF16 rows (quant: [rows, k]; swiglu: [rows, 2k])
@@ -51,6 +52,12 @@ struct QuantParams {
 __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t s, int64_t S, int swizzle) {
   if (!swizzle) return r * S + s;
   return ((r >> 7) * (S >> 2) + (s >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (s & 3);
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
 }
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&x)[8]) {
@@ -80,94 +87,160 @@ __device__ __forceinline__ float pow2_neg_unbiased(uint32_t byte) {  // 2^(127 -
   return byte <= 253u ? __uint_as_float((254u - byte) << 23) : __uint_as_float(0x00400000u);
 }
 
-template <int MODE>
-__device__ __forceinline__ void encode_group_lane(const float (&x)[8], float amax, float g,
-                                                  uint32_t& scale_byte, uint2& packed) {
+// One lane quantises one whole scale group of GS values x[0..GS).
+// MXFP8 writes GS E4M3 bytes to q[0..GS) words; NVFP4 writes GS/2 packed bytes.
+template <int MODE, int GS>
+__device__ __forceinline__ uint32_t encode_group(const float (&x)[GS], float g,
+                                                 const float* r_table, uint32_t (&qw)[GS / 4]) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < GS; ++i) amax = fmaxf(amax, fabsf(x[i]));
   if (MODE == HQ_MXFP8) {
     const float s = __fmul_rn(__fmul_rn(g, amax), 1.0f / 448.0f);
-    scale_byte = ue8m0_ceil(s);
-    const float mult = pow2_neg_unbiased(scale_byte);
-    uint32_t c[4];
+    const uint32_t byte = ue8m0_ceil(s);
+    const float mult = pow2_neg_unbiased(byte);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      c[i] = cvt_e4m3x2(__fmul_rn(x[2 * i + 1], mult), __fmul_rn(x[2 * i], mult));
-    packed.x = c[0] | (c[1] << 16);
-    packed.y = c[2] | (c[3] << 16);
+    for (int i = 0; i < GS / 4; ++i) {
+      const uint32_t lo = cvt_e4m3x2(__fmul_rn(x[4 * i + 1], mult), __fmul_rn(x[4 * i], mult));
+      const uint32_t hi = cvt_e4m3x2(__fmul_rn(x[4 * i + 3], mult), __fmul_rn(x[4 * i + 2], mult));
+      qw[i] = lo | (hi << 16);
+    }
+    return byte;
   } else {
     const float s = __fmul_rn(__fmul_rn(g, amax), 1.0f / 6.0f);
-    scale_byte = cvt_e4m3x2(0.0f, s) & 0xFFu;
-    const float sd = ue4m3_value(scale_byte);
-    const float r = sd == 0.0f ? 0.0f : __fdiv_rn(g, sd);
-    uint32_t w = 0;
+    const uint32_t byte = cvt_e4m3x2(0.0f, s) & 0x7Fu;
+    const float r = r_table[byte];  // g / value(byte), 0 for a zero scale
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      w |= cvt_e2m1x2(__fmul_rn(x[2 * i + 1], r), __fmul_rn(x[2 * i], r)) << (8 * i);
-    packed.x = w;
-    packed.y = 0;
+    for (int i = 0; i < GS / 8; ++i) {
+      uint32_t w = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        w |= cvt_e2m1x2(__fmul_rn(x[8 * i + 2 * j + 1], r), __fmul_rn(x[8 * i + 2 * j], r)) << (8 * j);
+      qw[i] = w;
+    }
+    return byte;
   }
 }
 
 template <int MODE, bool SWIGLU>
 __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
-  pdl_wait();
   constexpr int GS = MODE == HQ_MXFP8 ? 32 : 16;
-  constexpr int LPG = GS / 8;  // lanes per scale group
+  constexpr int NV = GS / 8;          // 16-byte loads per operand and group
+  constexpr int U = MODE == HQ_MXFP8 ? 1 : 2;  // groups a lane holds in flight
+  __shared__ float r_table[128];
+  const float g = (MODE == HQ_NVFP4 && p.global_scale) ? __ldg(p.global_scale) : 1.0f;
+  if (MODE == HQ_NVFP4) {
+    // g / value(UE4M3 code) for every positive code, IEEE division
+    if (threadIdx.x < 128) {
+      const float sd = ue4m3_value(threadIdx.x);
+      r_table[threadIdx.x] = sd == 0.0f ? 0.0f : __fdiv_rn(g, sd);
+    }
+    __syncthreads();
+  }
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
-  const int64_t segs = (p.k + kSegElems - 1) / kSegElems;
-  const int64_t items = p.rows * segs;
-  const float g = (MODE == HQ_NVFP4 && p.global_scale) ? __ldg(p.global_scale) : 1.0f;
+  // an item is 32 * U consecutive groups of one row; lane l owns groups l, l+32, ...
+  const int64_t groups_row = p.S_real;
+  const int64_t chunks = (groups_row + 32 * U - 1) / (32 * U);
+  const int64_t items = p.rows * chunks;
+  const bool small = items < (1ll << 31);
 
+  // Software pipeline: the loads of a warp's next item are issued before the
+  // current item is encoded, so load latency overlaps the arithmetic.
+  auto row_of = [&](int64_t item) -> int64_t {
+    return small ? static_cast<int64_t>(static_cast<uint32_t>(item) / static_cast<uint32_t>(chunks))
+                 : item / chunks;
+  };
+  // token_nums: rows past an expert's count are skipped (data and scales)
+  auto row_valid = [&](int64_t row) -> bool {
+    if (!(SWIGLU && p.token_nums)) return true;
+    const int64_t e = row / p.rows_per_expert;
+    const int64_t local = row - e * p.rows_per_expert;
+    int tn = __ldg(p.token_nums + e);
+    if (tn < 0 || tn > p.rows_per_expert) {
+      if (lane == 0 && local == 0) atomicOr(p.status, HQ_STATUS_TOKENS_CLAMPED);
+      tn = tn < 0 ? 0 : static_cast<int>(p.rows_per_expert);
+    }
+    return local < tn;
+  };
+  uint4 v0[U][NV], v1[U][NV];
+  auto load_item = [&](int64_t item) {
+    const int64_t row = row_of(item);
+    const int64_t s0 = (item - row * chunks) * (32 * U);
+    const bool rv = row_valid(row);
+    const uint16_t* src_row = p.in + row * p.in_stride;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t s = s0 + u * 32 + lane;
+      const bool ok = rv && s < groups_row;
+      const uint4* src = reinterpret_cast<const uint4*>(src_row + s * GS);
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        v0[u][i] = ok ? __ldcs(src + i) : make_uint4(0, 0, 0, 0);
+        if (SWIGLU) v1[u][i] = ok ? __ldcs(src + i + p.k / 8) : make_uint4(0, 0, 0, 0);
+      }
+    }
+  };
+  if (warp < items) load_item(warp);
   for (int64_t item = warp; item < items; item += nwarps) {
-    const int64_t row = item / segs;
-    const int64_t col = (item - row * segs) * kSegElems + lane * 8;
-    if (SWIGLU && p.token_nums) {
-      const int64_t e = row / p.rows_per_expert;
-      const int64_t local = row - e * p.rows_per_expert;
-      int tn = __ldg(p.token_nums + e);
-      if (tn < 0 || tn > p.rows_per_expert) {
-        if (lane == 0 && local == 0) atomicOr(p.status, HQ_STATUS_TOKENS_CLAMPED);
-        tn = tn < 0 ? 0 : static_cast<int>(p.rows_per_expert);
-      }
-      if (local >= tn) continue;  // warp-uniform: the whole row is skipped
-    }
-    const bool in_range = col < p.k;
-    float x[8];
-    if (in_range) {
-      const uint16_t* src = p.in + row * p.in_stride + col;
-      if (SWIGLU) {
-        float gt[8], up[8];
-        bf16x8_to_f32(__ldcs(reinterpret_cast<const uint4*>(src)), gt);
-        bf16x8_to_f32(__ldcs(reinterpret_cast<const uint4*>(src + p.k)), up);
+    uint4 c0[U][NV], c1[U][NV];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float e = expf(-gt[i]);
-          const float t = __fdiv_rn(gt[i], __fadd_rn(1.0f, e));
-          x[i] = __fmul_rn(up[i], t);
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        c0[u][i] = v0[u][i];
+        if (SWIGLU) c1[u][i] = v1[u][i];
+      }
+    if (item + nwarps < items) load_item(item + nwarps);
+    const int64_t row = row_of(item);
+    const int64_t s0 = (item - row * chunks) * (32 * U);
+    if (!row_valid(row)) continue;  // warp-uniform
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t s = s0 + u * 32 + lane;
+      if (s0 + u * 32 >= groups_row) break;  // warp-uniform
+      float x[GS];
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        float a[8];
+        bf16x8_to_f32(c0[u][i], a);
+        if (SWIGLU) {
+          float b[8];
+          bf16x8_to_f32(c1[u][i], b);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            // silu(gate) = gate / (1 + exp(-gate)); the reciprocal is the
+            // hardware approximation (within 1 ulp)
+            const float e = expf(-a[j]);
+            const float t = __fmul_rn(a[j], rcp_approx(__fadd_rn(1.0f, e)));
+            x[8 * i + j] = __fmul_rn(b[j], t);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) x[8 * i + j] = a[j];
         }
-      } else {
-        bf16x8_to_f32(__ldcs(reinterpret_cast<const uint4*>(src)), x);
       }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) x[i] = 0.0f;
+      uint32_t qw[GS / 4];
+      const uint32_t byte = encode_group<MODE, GS>(x, g, r_table, qw);
+      // four consecutive groups (lanes 4j..4j+3) share one 32-bit scale word
+      const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, byte, 1);
+      const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, byte, 2);
+      const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, byte, 3);
+      if (s >= groups_row) continue;
+      if (MODE == HQ_MXFP8) {
+        uint4* dst = reinterpret_cast<uint4*>(p.q + row * p.k + s * GS);
+        dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+        dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+      } else {
+        *reinterpret_cast<uint2*>(p.q + (row * p.k + s * GS) / 2) = make_uint2(qw[0], qw[1]);
+      }
+      if ((lane & 3) == 0) {
+        const uint32_t word = byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
+        *reinterpret_cast<uint32_t*>(p.sf + sf_offset(row, s, p.S, p.swizzle)) = word;
+      }
     }
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
-#pragma unroll
-    for (int o = 1; o < LPG; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-    if (!in_range) continue;
-    uint32_t sbyte;
-    uint2 packed;
-    encode_group_lane<MODE>(x, amax, g, sbyte, packed);
-    if (MODE == HQ_MXFP8) {
-      *reinterpret_cast<uint2*>(p.q + row * p.k + col) = packed;
-    } else {
-      *reinterpret_cast<uint32_t*>(p.q + (row * p.k + col) / 2) = packed.x;
-    }
-    if ((lane % LPG) == 0) p.sf[sf_offset(row, col / GS, p.S, p.swizzle)] = static_cast<uint8_t>(sbyte);
   }
 
   // Scale bytes that hold 0: padding rows, and (swiglu, MXFP8) the columns
@@ -207,8 +280,7 @@ int launch_quant(const QuantParams& p, cudaStream_t st, bool pdl) {
                                                     0) != cudaSuccess)
     return HQ_ERR_CUDA;
   if (per_sm < 1) per_sm = 1;
-  const int64_t segs = (p.k + kSegElems - 1) / kSegElems;
-  const int64_t warps_needed = p.rows * segs + 1;
+  const int64_t warps_needed = p.rows * ((p.S_real + kGroupsPerWarpStep - 1) / kGroupsPerWarpStep) + 1;
   int64_t blocks = (warps_needed + (kThreads / 32) - 1) / (kThreads / 32);
   const int64_t cap = static_cast<int64_t>(sms) * per_sm;
   if (blocks > cap) blocks = cap;
