@@ -12,14 +12,13 @@
 // Persistent warp-specialised kernel: warp 0 streams A / B tiles with TMA into
 // a ring of shared-memory stages, warp 1 issues the MMAs into one of two TMEM
 // accumulators (so the epilogue of tile i overlaps the main loop of tile i+1),
-// warps 2..9 run the epilogue (two per TMEM lane quarter, each owning two of
+// warps 2..17 run the epilogue (four per TMEM lane quarter, each owning one of
 // the tile's four 32-column chunks).  A compact tile of 128 columns j maps to the
 // 256 C / D_row columns [2 j0, 2 j0 + 256).  Each epilogue thread owns one
-// row: it reads that row's C segment, writes its D_row segment, accumulates
-// its dprob partial (one float atomic per row and tile), and, when dbias is
-// requested, the warp transposes its fp32 D values through shared memory to
-// produce per-column partial sums that are added to a float32 workspace with
-// one atomic per column, warp and chunk.  A final pass adds the workspace
+// row: it reads that row's C segment, writes its D_row segment, adds its
+// dprob partial with one float atomic, and, when dbias is requested, the warp
+// reduces its fp32 D values over its 32 rows with a butterfly of shuffles and
+// adds the column sums to a float32 workspace with one atomic per column.  A final pass adds the workspace
 // into the caller's BF16 dbias.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -34,7 +33,7 @@
 namespace hq {
 namespace {
 
-constexpr int kEpiWarps = 8;      // two per TMEM lane quarter, each owning half the columns
+constexpr int kEpiWarps = 16;     // four per TMEM lane quarter, one 32-column chunk each
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kBN = 128;          // compact columns per tile
 constexpr int kBKElems = 64;      // BF16 elements of K per stage (128 bytes)
@@ -43,11 +42,9 @@ constexpr int kAcc = 2;
 constexpr int kTmemCols = kAcc * kBN;
 constexpr int kABytes = kBM * kBKElems * 2;
 constexpr int kBBytes = kBN * kBKElems * 2;
-constexpr int kTransStride = 65;  // floats per row of the dbias transpose buffer
 constexpr int kOffA = 0;
 constexpr int kOffB = kOffA + kStages * kABytes;
-constexpr int kOffTrans = kOffB + kStages * kBBytes;
-constexpr int kOffTable = kOffTrans + kEpiWarps * 32 * kTransStride * 4;
+constexpr int kOffTable = kOffB + kStages * kBBytes;
 constexpr int kOffBar = (kOffTable + 2 * (kMaxGroups + 1) * 4 + 15) / 16 * 16;
 constexpr int kNumBars = 2 * kStages + 2 * kAcc + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -79,7 +76,9 @@ __device__ __forceinline__ float rcp_approx(float x) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// 18 warps share four 16K-register sub-partitions (up to 5 warps on one):
+// 96 registers per thread is the most that lets the block launch.
+__global__ void __maxnreg__(96)
     dswiglu_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const DsParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -184,9 +183,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_drain(drain_bar, 0, p.wait_limit_ns);
     }
   } else {
-    const int q = warp & 3;                  // TMEM lane quarter this warp may access
-    const int half = (warp - 2) >> 2;        // which two of the four 32-column chunks
-    float* trans = reinterpret_cast<float*>(smem + kOffTrans) + (warp - 2) * 32 * kTransStride;
+    const int q = warp & 3;         // TMEM lane quarter this warp may access
+    const int c = (warp - 2) >> 2;  // the tile's 32-column chunk this warp owns
     const int64_t two_n = 2 * p.n;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -195,16 +193,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r_local = q * 32 + lane;
       const bool row_ok = r_local < ti.rows_valid;
       const int64_t row = ti.row0 + r_local;
-      // this warp's C segments (2 chunks x 64 columns of the row) are loaded
-      // before the accumulator is ready, so their latency overlaps the wait
-      uint4 cv[2][8];
+      const int64_t j0 = ti.n0 + c * 32;
+      const bool chunk_ok = j0 < p.n;  // n % 32 == 0: a chunk is all in or all out
+      // this row's C segment (32 gate then 32 input values) is loaded before
+      // the accumulator is ready, so its latency overlaps the wait
+      const int64_t cbase = row * two_n + 2 * j0;
+      uint4 cv[8];
+      {
+        const bool ld = row_ok && chunk_ok;
+        const uint4* src = reinterpret_cast<const uint4*>(p.c + cbase);
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int64_t j0 = ti.n0 + (2 * half + cc) * 32;
-        const bool ld = row_ok && j0 < p.n;
-        const uint4* src = reinterpret_cast<const uint4*>(p.c + row * two_n + 2 * j0);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) cv[cc][i] = ld ? __ldcs(src + i) : make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < 8; ++i) cv[i] = ld ? __ldcs(src + i) : make_uint4(0, 0, 0, 0);
       }
       const float alpha = __ldg(p.alpha + ti.g);
       const float a2 = __fmul_rn(alpha, alpha);
@@ -213,75 +212,73 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ok = wait_bounded(tfull_bar(acc), acc_phase, wctx);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       tc_fence_after();
-      float dprob_part = 0.0f;
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c = 2 * half + cc;
-        const int64_t j0 = ti.n0 + c * 32;
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN + c * 32,
-                           r);
-        tmem_ld_wait();
-        if (j0 >= p.n) continue;  // past the last compact column (n % 32 == 0: whole chunk)
-        const int64_t cbase = row * two_n + 2 * j0;  // gate block start; input at +32
-        uint32_t dg[16], di[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          // element pair (2i, 2i+1): gate words in cv[cc][0..3], input words in cv[cc][4..7]
-          const uint32_t gw = reinterpret_cast<const uint32_t*>(cv[cc])[i];
-          const uint32_t iw = reinterpret_cast<const uint32_t*>(cv[cc])[16 + i];
-          float outg[2], outi[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float gate = __fmul_rn(beta, h ? bf16_hi(gw) : bf16_lo(gw));
-            const float inp = __fmul_rn(beta, h ? bf16_hi(iw) : bf16_lo(iw));
-            const float R = __fmul_rn(a2, __uint_as_float(r[2 * i + h]));
-            const float s = rcp_approx(__fadd_rn(1.0f, expf(-gate)));  // sigmoid(gate)
-            const float rp = __fmul_rn(R, prob);
-            outg[h] = rp * inp * s * (1.0f + gate * (1.0f - s));
-            outi[h] = rp * gate * s;
-            dprob_part += R * gate * s * inp;
-          }
-          __nv_bfloat162 bg = __floats2bfloat162_rn(outg[0], outg[1]);
-          __nv_bfloat162 bi = __floats2bfloat162_rn(outi[0], outi[1]);
-          dg[i] = *reinterpret_cast<uint32_t*>(&bg);
-          di[i] = *reinterpret_cast<uint32_t*>(&bi);
-          if (p.dbias_ws) {
-            float* tr = trans + lane * kTransStride;
-            tr[2 * i] = row_ok ? outg[0] : 0.0f;
-            tr[2 * i + 1] = row_ok ? outg[1] : 0.0f;
-            tr[32 + 2 * i] = row_ok ? outi[0] : 0.0f;
-            tr[32 + 2 * i + 1] = row_ok ? outi[1] : 0.0f;
-          }
-        }
-        if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(p.d_row + cbase);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(dg[4 * i], dg[4 * i + 1], dg[4 * i + 2], dg[4 * i + 3]);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[4 + i] = make_uint4(di[4 * i], di[4 * i + 1], di[4 * i + 2], di[4 * i + 3]);
-        }
-        if (p.dbias_ws) {
-          __syncwarp();
-          float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll 8
-          for (int rr = 0; rr < 32; ++rr) {
-            s0 += trans[rr * kTransStride + lane];
-            s1 += trans[rr * kTransStride + 32 + lane];
-          }
-          float* ws = p.dbias_ws + static_cast<int64_t>(ti.g) * two_n + 2 * j0;
-          atomicAdd(ws + lane, s0);
-          atomicAdd(ws + 32 + lane, s1);
-          __syncwarp();
-        }
-      }
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN + c * 32, r);
+      tmem_ld_wait();
+      // the accumulator chunk is in registers: release it to the MMA issuer
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
-      if (row_ok) atomicAdd(p.dprob + row, dprob_part);
       if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
+      if (!chunk_ok) continue;
+      float dg[32], di[32];
+      float dprob_part = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        // element pair (2i, 2i+1): gate words in cv[0..3], input words in cv[4..7]
+        const uint32_t gw = reinterpret_cast<const uint32_t*>(cv)[i];
+        const uint32_t iw = reinterpret_cast<const uint32_t*>(cv)[16 + i];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float gate = __fmul_rn(beta, h ? bf16_hi(gw) : bf16_lo(gw));
+          const float inp = __fmul_rn(beta, h ? bf16_hi(iw) : bf16_lo(iw));
+          const float R = __fmul_rn(a2, __uint_as_float(r[2 * i + h]));
+          const float s = rcp_approx(__fadd_rn(1.0f, expf(-gate)));  // sigmoid(gate)
+          const float rp = __fmul_rn(R, prob);
+          dg[2 * i + h] = rp * inp * s * (1.0f + gate * (1.0f - s));
+          di[2 * i + h] = rp * gate * s;
+          dprob_part += R * gate * s * inp;
+        }
+      }
+      if (row_ok) {
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          __nv_bfloat162 bg = __floats2bfloat162_rn(dg[2 * i], dg[2 * i + 1]);
+          __nv_bfloat162 bi = __floats2bfloat162_rn(di[2 * i], di[2 * i + 1]);
+          w[i] = *reinterpret_cast<uint32_t*>(&bg);
+          w[16 + i] = *reinterpret_cast<uint32_t*>(&bi);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(p.d_row + cbase);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        atomicAdd(p.dprob + row, dprob_part);
+      }
+      if (p.dbias_ws) {
+        // column sums over the warp's 32 rows by a butterfly reduce-scatter:
+        // afterwards lane l holds the sums of gate column l and input column l
+        if (!row_ok) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) { dg[i] = 0.0f; di[i] = 0.0f; }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+          const bool upper = (lane & o) != 0;
+#pragma unroll
+          for (int i = 0; i < o; ++i) {
+            const float sg = upper ? dg[i] : dg[i + o];
+            const float si = upper ? di[i] : di[i + o];
+            const float kg = upper ? dg[i + o] : dg[i];
+            const float ki = upper ? di[i + o] : di[i];
+            dg[i] = kg + __shfl_xor_sync(0xFFFFFFFFu, sg, o);
+            di[i] = ki + __shfl_xor_sync(0xFFFFFFFFu, si, o);
+          }
+        }
+        float* ws = p.dbias_ws + static_cast<int64_t>(ti.g) * two_n + 2 * j0;
+        atomicAdd(ws + lane, dg[0]);
+        atomicAdd(ws + 32 + lane, di[0]);
+      }
     }
   }
 
