@@ -45,6 +45,29 @@ RATIO = {"bf16": 1.0, "fp8": 2.0, "fp4": 6.0}
 SECTIONS = ("dense_mxfp8_256", "quant_nvfp4", "moe_contig", "moe_masked", "dswiglu")
 
 
+GEMM_PROFILE = os.path.join(ROOT, "profiles", "bs_gemm_kernel_dense_nvfp4_4096x12288x5120.md")
+GEMM_SOURCES = ("hq_gemm_bs.cu", "hq_ptx.cuh", "hq_sched.cuh", "hq_internal.h")
+
+
+def profiled_traffic():
+    """DRAM bytes per GEMM launch from the committed ncu summary, or None when
+    the kernel's sources changed after the counters were taken."""
+    import hashlib
+    import re
+    if not os.path.exists(GEMM_PROFILE):
+        return None
+    text = open(GEMM_PROFILE).read()
+    mb = re.search(r"dram_bytes_per_launch \| (\d+)", text)
+    mh = re.search(r"source_sha256_16: ([0-9a-f]{16})", text)
+    if not (mb and mh):
+        return None
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "fp4_grouped_gemm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return int(mb.group(1)) if h.hexdigest()[:16] == mh.group(1) else None
+
+
 def load_peaks():
     if os.path.exists(PEAKS_FILE):
         with open(PEAKS_FILE) as f:
@@ -347,7 +370,8 @@ def headline(hq, dev, args, ws, peaks, pk_src):
                    "l2": "flushed before every timed step (256 MiB written, then 256 MiB read)",
                    "inputs": "A ~ N(0,1), B ~ N(0,0.02) BF16, seeded; g = 2688/amax per tensor"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_fp4, "unit": "TFLOP/s",
-                     "frac": achieved / peak_fp4, "traffic": None,
+                     "frac": achieved / peak_fp4, "traffic": profiled_traffic(),
+                     "traffic_unit": "bytes per launch (ncu dram read + write)",
                      "kernel": "bs_gemm_kernel<NVFP4,256>",
                      "peak_source": f"{pk_src} bf16 burst {peaks['bf16_tflops']} x 6 (nominal FP4/BF16)"},
         "e2e": {"value": ws * flops / e2e_t / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
