@@ -18,7 +18,7 @@ from ._abi import (HQ_MXFP8, HQ_NVFP4, HQ_STATUS_WAIT_TIMEOUT, HQ_STATUS_MASK_CL
 
 __all__ = [
     "HQError", "mode_id", "group_size", "sf_bytes", "capabilities", "get_device_status",
-    "set_wait_limit_ns", "selftest_wait_expiry", "set_gemm_tile_n", "hq_quant",
+    "set_wait_limit_ns", "selftest_wait_expiry", "set_gemm_tile_n", "set_gemm_2sm", "hq_quant",
     "hq_gemm_dense", "hq_gemm_grouped_contig", "hq_gemm_grouped_masked", "hq_swiglu_quant",
     "hq_gemm_dswiglu", "hq_gemm_dswiglu_workspace_size", "swiglu_kb_dim",
 ]
@@ -89,6 +89,10 @@ def selftest_wait_expiry(limit_ns, stream=None):
 
 def set_gemm_tile_n(tile_n):
     _check(_abi.load().hq_set_gemm_tile_n(int(tile_n)), "hq_set_gemm_tile_n")
+
+
+def set_gemm_2sm(enable):
+    _check(_abi.load().hq_set_gemm_2sm(1 if enable else 0), "hq_set_gemm_2sm")
 
 
 def _q_shape(rows, k, mode):

@@ -23,6 +23,7 @@ uint32_t* g_status_ptr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 std::atomic<uint64_t> g_wait_limit_ns{1000000000ull};
 std::atomic<int> g_tile_n{0};
+std::atomic<int> g_use_2sm{0};
 using EncodeFn = decltype(&cuTensorMapEncodeTiled);
 EncodeFn g_encode = nullptr;
 
@@ -48,6 +49,8 @@ uint32_t* status_word_ptr() {
 uint64_t wait_limit_ns() { return g_wait_limit_ns.load(); }
 
 int forced_tile_n() { return g_tile_n.load(); }
+
+bool use_2sm() { return g_use_2sm.load() != 0; }
 
 int num_sms() {
   const int dev = current_device();
@@ -169,6 +172,11 @@ int hq_set_wait_limit_ns(uint64_t ns) {
 int hq_set_gemm_tile_n(int tile_n) {
   if (tile_n != 0 && tile_n != 128 && tile_n != 256) return HQ_ERR_INVALID;
   hq::g_tile_n.store(tile_n);
+  return HQ_OK;
+}
+
+int hq_set_gemm_2sm(int enable) {
+  hq::g_use_2sm.store(enable ? 1 : 0);
   return HQ_OK;
 }
 

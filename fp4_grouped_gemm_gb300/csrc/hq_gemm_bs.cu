@@ -433,6 +433,379 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// 2-SM variant of the dense GEMM (cta_group::2): a cluster of two CTAs on two
+// SMs computes a 256 x 256 tile.  CTA r loads rows [128 r, 128 r + 128) of the
+// A tile and rows [128 r, 128 r + 128) of the B tile into its own shared
+// memory; the even CTA issues MMAs of M = 256, N = 256 that
+// read both CTAs' operands and write each CTA's 128 x 256 accumulator half in
+// its own TMEM.  Per SM this halves the B operand bytes fetched for the same
+// work compared with the 128 x 256 single-SM tile.
+//
+// Completion never crosses CTAs through TMA: each CTA's copies complete on its
+// own barriers; each CTA's scale warps wait for their CTA's stage, stage its
+// scales into their TMEM and arrive on their CTA's "ready" barrier; in the odd
+// CTA a relay thread forwards each completed phase to the even CTA's "ready"
+// barrier, which therefore also certifies the odd CTA's operands.  The even
+// CTA's commits are multicast to both CTAs' "empty" and "accumulator full"
+// barriers; epilogue warps arrive on their CTA's "accumulator empty" barrier
+// and the odd CTA's is relayed to the even CTA the same way.  Scale factors: each CTA holds the A scales of
+// its own 128 rows and the B scales of all 256 tile columns in its TMEM, in
+// the same layout as the single-SM N = 256 tile.
+// ---------------------------------------------------------------------------
+template <int MODE, int STAGES>
+struct Cfg2 {
+  static constexpr int GS = MODE == HQ_MXFP8 ? 32 : 16;
+  static constexpr int EPB = MODE == HQ_MXFP8 ? 1 : 2;
+  static constexpr int BK = kBKBytes * EPB;
+  static constexpr int ATOMS = BK / GS / 4;
+  static constexpr int BN = 256;                       // tile columns (both CTAs)
+  static constexpr int A_BYTES = kBM * kBKBytes;       // this CTA's 128 rows of A
+  static constexpr int B_BYTES = 128 * kBKBytes;       // this CTA's 128 rows of B
+  static constexpr int SFA_BYTES = ATOMS * 512;        // this CTA's 128 A rows
+  static constexpr int SFB_BYTES = 2 * ATOMS * 512;    // all 256 B rows of the tile
+  static constexpr int SFA_COLS = (ATOMS * 4 + 7) / 8 * 8;
+  static constexpr int SFB_COLS = 2 * ATOMS * 4;
+  static constexpr int SF_STAGE_COLS = (SFA_COLS + SFB_COLS + 15) / 16 * 16;
+  static constexpr int SF_BASE_COL = BN;
+  static constexpr int TMEM_USED = BN + STAGES * SF_STAGE_COLS;
+  static constexpr int TMEM_COLS = 512;
+  static_assert(TMEM_USED <= 512, "TMEM budget");
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+  static constexpr int OFF_STAGE_OUT = OFF_SFB + STAGES * SFB_BYTES;
+  static constexpr int OFF_BAR = OFF_STAGE_OUT + 4 * 2048;
+  static constexpr int NUM_BARS = 4 * STAGES + 3;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget");
+  // M = 256 across the pair, N = 256
+  static constexpr uint32_t IDESC_BASE =
+      (MODE == HQ_MXFP8 ? ((0u << 7) | (0u << 10) | (1u << 23))
+                        : ((1u << 7) | (1u << 10) | (0u << 23)))
+      | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(256 >> 4) << 24);
+};
+
+template <int MODE, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    bs_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const GemmParams p) {
+  using C = Cfg2<MODE, STAGES>;
+  static_assert(kSfPath == 2, "the 2-SM kernel stages scales with tcgen05.st");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs
+  const bool leader = rank == 0;
+
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };                 // this CTA's A, B
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };     // leader's commit
+  auto sffull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); }; // this CTA's scales
+  auto ready_bar = [&](int s) { return bar0 + 8u * (3 * STAGES + s); };  // used in the leader
+  const uint32_t tfull_bar = bar0 + 8u * (4 * STAGES);
+  const uint32_t tempty_bar = tfull_bar + 8u;  // used in the leader
+  const uint32_t drain_bar = tfull_bar + 16u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  if (warp == 0 && lane == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+      mbar_init(sffull_bar(s), 1);
+      // 4 local scale warps, plus (even CTA) one arrival relayed from the odd CTA
+      mbar_init(ready_bar(s), leader ? 5 : 4);
+    }
+    mbar_init(tfull_bar, 1);
+    mbar_init(tempty_bar, leader ? 5 : 4);  // 4 epilogue warps (+ relay in the even CTA)
+    mbar_init(drain_bar, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {  // one warp in each CTA allocates, collectively for the pair
+    tmem_alloc_2sm(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish_2sm();
+  }
+  pdl_wait();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers and TMEM exist before any cross-CTA use
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int n_tiles = static_cast<int>((p.n + C::BN - 1) / C::BN);
+  const int64_t m_pairs = (p.gs.a_rows + 255) / 256;
+  const int64_t total = m_pairs * n_tiles;
+  const int64_t cluster_id = blockIdx.x >> 1;
+  const int64_t num_clusters = gridDim.x >> 1;
+  const int64_t rows_pad = (p.gs.a_rows + kBM - 1) / kBM * kBM;  // rows the scale buffer holds
+  const int num_kb = static_cast<int>((p.k + C::BK - 1) / C::BK);
+  const int atoms_total = static_cast<int>(p.S / 4);
+  const WaitCtx wctx{p.gs.status, abort_flag, p.wait_limit_ns};
+  auto tile_rows = [&](int64_t t, int64_t& row0, int& n0) {
+    const int64_t mt = t / n_tiles;
+    n0 = static_cast<int>(t - mt * n_tiles) * C::BN;
+    row0 = mt * 256 + rank * kBM;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, filled_a = 0, filled_s = 0, par_a = 0, par_s = 0;
+      bool ok = true;
+      for (int64_t t = cluster_id; ok && t < total; t += num_clusters) {
+        int64_t row0;
+        int n0;
+        tile_rows(t, row0, n0);
+        const int nh0 = n0 + static_cast<int>(rank) * 128;  // this CTA's B rows
+        const bool has_sfa = row0 < rows_pad;
+        const uint8_t* sfa_rows = p.sfa + (row0 / kBM) * atoms_total * 512;
+        const uint8_t* sfb_rows = p.sfb + (n0 / 128) * static_cast<int64_t>(atoms_total) * 512;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bounded(empty_bar(stage), phase ^ 1u, wctx)) { ok = false; break; }
+          int atoms = atoms_total - kb * C::ATOMS;
+          atoms = atoms < C::ATOMS ? atoms : C::ATOMS;
+          mbar_arrive_expect_tx(full_bar(stage), C::A_BYTES + C::B_BYTES);
+          tma_load_2d(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, full_bar(stage), kb * kBKBytes,
+                      static_cast<int32_t>(row0));
+          tma_load_3d(sbase + C::OFF_B + stage * C::B_BYTES, &tmB, full_bar(stage), kb * kBKBytes,
+                      nh0, 0);
+          mbar_arrive_expect_tx(sffull_bar(stage), atoms * 512u * (has_sfa ? 3u : 2u));
+          if (has_sfa)
+            bulk_load(sbase + C::OFF_SFA + stage * C::SFA_BYTES, sfa_rows + kb * C::ATOMS * 512,
+                      atoms * 512u, sffull_bar(stage));
+          for (int rb = 0; rb < 2; ++rb)
+            bulk_load(sbase + C::OFF_SFB + stage * C::SFB_BYTES + rb * C::ATOMS * 512,
+                      sfb_rows + (rb * static_cast<int64_t>(atoms_total) + kb * C::ATOMS) * 512,
+                      atoms * 512u, sffull_bar(stage));
+          filled_a |= 1u << stage;
+          filled_s |= 1u << stage;
+          par_a = (par_a & ~(1u << stage)) | (phase << stage);
+          par_s = par_a;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      for (int s = 0; s < STAGES; ++s) {
+        if (filled_a & (1u << s)) wait_drain(full_bar(s), (par_a >> s) & 1u, p.wait_limit_ns);
+        if (filled_s & (1u << s)) wait_drain(sffull_bar(s), (par_s >> s) & 1u, p.wait_limit_ns);
+      }
+    }
+  } else if (warp == 1 && !leader) {
+    // ------------------------------------------------------------ relays (odd CTA)
+    // A warp's cluster-scope release arrive would first wait for all its
+    // earlier global stores to be acknowledged; so every warp arrives on its
+    // own CTA's barrier and one otherwise idle thread here forwards a single
+    // cluster-scope arrival per phase to the even CTA.
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int64_t t = cluster_id; ok && t < total; t += num_clusters)
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bounded(ready_bar(stage), phase, wctx)) { ok = false; break; }
+          mbar_arrive_cluster(mapa_shared(ready_bar(stage), 0));
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+    } else if (lane == 1) {
+      uint32_t acc_phase = 0;
+      for (int64_t t = cluster_id; t < total; t += num_clusters) {
+        if (!wait_bounded(tempty_bar, acc_phase, wctx)) break;
+        mbar_arrive_cluster(mapa_shared(tempty_bar, 0));
+        acc_phase ^= 1u;
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int64_t t = cluster_id; ok && t < total; t += num_clusters) {
+        if (!wait_bounded(tempty_bar, acc_phase ^ 1u, wctx)) break;
+        tc_fence_after();
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bounded(full_bar(stage), phase, wctx) ||
+              !wait_bounded(ready_bar(stage), phase, wctx)) { ok = false; break; }
+          tc_fence_after();
+          int atoms = atoms_total - kb * C::ATOMS;
+          atoms = atoms < C::ATOMS ? atoms : C::ATOMS;
+          const uint32_t sfa_t = tmem_base + C::SF_BASE_COL + stage * C::SF_STAGE_COLS;
+          const uint32_t sfb_t = sfa_t + C::SFA_COLS;
+          const uint32_t a_s = sbase + C::OFF_A + stage * C::A_BYTES;
+          const uint32_t b_s = sbase + C::OFF_B + stage * C::B_BYTES;
+          const int n_mma = MODE == HQ_MXFP8 ? (kBKBytes / kMmaKBytes) : atoms;
+          for (int j = 0; j < n_mma; ++j) {
+            const uint64_t adesc = smem_desc_sw128(a_s + j * kMmaKBytes);
+            const uint64_t bdesc = smem_desc_sw128(b_s + j * kMmaKBytes);
+            const uint32_t acc_flag = (kb > 0 || j > 0) ? 1u : 0u;
+            if (MODE == HQ_MXFP8) {
+              const uint32_t idesc = C::IDESC_BASE | (static_cast<uint32_t>(j) << 4) |
+                                     (static_cast<uint32_t>(j) << 29);
+              mma_mxf8_2sm(tmem_base, adesc, bdesc, idesc, sfa_t | (static_cast<uint32_t>(j) << 30),
+                           sfb_t | (static_cast<uint32_t>(j) << 30), acc_flag);
+            } else {
+              mma_nvf4_2sm(tmem_base, adesc, bdesc, C::IDESC_BASE, sfa_t + j * 4, sfb_t + j * 8,
+                           acc_flag);
+            }
+          }
+          tc_commit_2sm_mc(empty_bar(stage), 0x3);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit_2sm_mc(tfull_bar, 0x3);
+        acc_phase ^= 1u;
+      }
+      tc_commit_2sm_mc(drain_bar, 0x1);
+      wait_drain(drain_bar, 0, p.wait_limit_ns);
+    }
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ scale staging (both CTAs)
+    const int q = warp & 3;
+    const uint32_t lq = static_cast<uint32_t>(q * 32) << 16;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int64_t t = cluster_id; ok && t < total; t += num_clusters) {
+      for (int kb = 0; kb < num_kb; ++kb) {
+        int atoms = atoms_total - kb * C::ATOMS;
+        atoms = atoms < C::ATOMS ? atoms : C::ATOMS;
+        // the odd CTA's arrival also certifies its A and B tiles for this stage
+        const bool w = wait_bounded(sffull_bar(stage), phase, wctx) &&
+                       (leader || wait_bounded(full_bar(stage), phase, wctx));
+        ok = __all_sync(0xFFFFFFFFu, w);
+        if (!ok) break;
+        const uint32_t sfa_t = tmem_base + C::SF_BASE_COL + stage * C::SF_STAGE_COLS;
+        const uint32_t sfb_t = sfa_t + C::SFA_COLS;
+        const uint32_t sfa_s = sbase + C::OFF_SFA + stage * C::SFA_BYTES;
+        const uint32_t sfb_s = sbase + C::OFF_SFB + stage * C::SFB_BYTES;
+        // B scales at columns sfb_t + (a * 2 + rb) * 4: k-atom a, 128-row block rb
+        if (atoms == C::ATOMS) {
+          constexpr int NA = 4 * C::ATOMS;
+          uint32_t va[NA], vb[2 * NA];
+#pragma unroll
+          for (int a = 0; a < C::ATOMS; ++a) {
+            lds128(sfa_s + a * 512 + lane * 16, va + 4 * a);
+#pragma unroll
+            for (int rb = 0; rb < 2; ++rb)
+              lds128(sfb_s + (rb * C::ATOMS + a) * 512 + lane * 16, vb + 4 * (a * 2 + rb));
+          }
+          tmem_st_32x32b<NA>(lq + sfa_t, va);
+          tmem_st_32x32b<2 * NA>(lq + sfb_t, vb);
+        } else {
+          for (int a = 0; a < atoms; ++a) {
+            uint32_t v[4];
+            lds128(sfa_s + a * 512 + lane * 16, v);
+            tmem_st_32x32b<4>(lq + sfa_t + a * 4, v);
+            for (int rb = 0; rb < 2; ++rb) {
+              lds128(sfb_s + (rb * C::ATOMS + a) * 512 + lane * 16, v);
+              tmem_st_32x32b<4>(lq + sfb_t + (a * 2 + rb) * 4, v);
+            }
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ready_bar(stage));
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const uint32_t stage_out_s = sbase + C::OFF_STAGE_OUT + (warp - 2) * 2048;
+    uint32_t acc_phase = 0;
+    for (int64_t t = cluster_id; t < total; t += num_clusters) {
+      int64_t row0;
+      int n0;
+      tile_rows(t, row0, n0);
+      const bool okw = wait_bounded(tfull_bar, acc_phase, wctx);
+      if (!__all_sync(0xFFFFFFFFu, okw)) break;
+      tc_fence_after();
+      const float alpha = p.alpha ? __ldg(p.alpha) : 1.0f;
+      const int64_t rem = p.gs.a_rows - row0 - q * 32;
+      const int rows_here = rem < 0 ? 0 : (rem > 32 ? 32 : static_cast<int>(rem));
+      for (int c = 0; c < C::BN / 32; ++c) {
+        const int col0 = n0 + c * 32;
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + c * 32, r);
+        tmem_ld_wait();
+        if (col0 >= p.n) continue;
+        float bias_v[32];
+        if (p.bias) {
+          const uint4* bp = reinterpret_cast<const uint4*>(p.bias + col0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 v = __ldg(bp + i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              bias_v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+              bias_v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) bias_v[i] = 0.0f;
+        }
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float v0 = __fadd_rn(__fmul_rn(alpha, __uint_as_float(r[2 * i])), bias_v[2 * i]);
+          const float v1 = __fadd_rn(__fmul_rn(alpha, __uint_as_float(r[2 * i + 1])), bias_v[2 * i + 1]);
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(v0, v1);
+          packed[i] = *reinterpret_cast<uint32_t*>(&b2);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t off = lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage_out_s + off),
+                       "r"(packed[4 * j]), "r"(packed[4 * j + 1]), "r"(packed[4 * j + 2]),
+                       "r"(packed[4 * j + 3])
+                       : "memory");
+        }
+        __syncwarp();
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          const int rr = it * 8 + (lane >> 2);
+          const int j = lane & 3;
+          const uint32_t off = rr * 64 + ((j ^ ((rr >> 1) & 3)) * 16);
+          uint4 v;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                       : "r"(stage_out_s + off)
+                       : "memory");
+          if (rr < rows_here) {
+            uint16_t* dst = p.out + (row0 + q * 32 + rr) * p.n + col0 + j * 8;
+            *reinterpret_cast<uint4*>(dst) = v;
+          }
+        }
+        __syncwarp();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar);
+      acc_phase ^= 1u;
+    }
+  }
+
+  __syncthreads();
+  pdl_launch_dependents();
+  cluster_sync();  // the peer may still read this CTA's shared memory and TMEM until here
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_2sm(tmem_base, C::TMEM_COLS);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -481,9 +854,66 @@ int run_bs(const void* a, const void* b, const GemmParams& p0, int sm_count, boo
   return e == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
 }
 
+template <int MODE, int STAGES>
+int run_bs_2sm(const void* a, const void* b, const GemmParams& p, int sm_count, bool pdl,
+               cudaStream_t st) {
+  using C = Cfg2<MODE, STAGES>;
+  const uint64_t kbytes = static_cast<uint64_t>(p.k) / C::EPB;
+  CUtensorMap tmA, tmB;
+  {
+    const uint64_t dims[2] = {kbytes, static_cast<uint64_t>(p.gs.a_rows)};
+    const uint64_t strides[1] = {kbytes};
+    const uint32_t box[2] = {kBKBytes, kBM};
+    int rc = encode_tensor_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a), dims,
+                               strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != HQ_OK) return rc;
+  }
+  {
+    const uint64_t dims[3] = {kbytes, static_cast<uint64_t>(p.n), 1};
+    const uint64_t strides[2] = {kbytes, kbytes * static_cast<uint64_t>(p.n)};
+    const uint32_t box[3] = {kBKBytes, 128, 1};
+    int rc = encode_tensor_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(b), dims,
+                               strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != HQ_OK) return rc;
+  }
+  auto kern = bs_gemm_2sm_kernel<MODE, STAGES>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+      cudaSuccess)
+    return HQ_ERR_CUDA;
+  const int sms = num_sms();
+  if (sms < 2) return HQ_ERR_CUDA;
+  const int64_t pairs_needed = ((p.gs.a_rows + 255) / 256) * ((p.n + 255) / 256);
+  int64_t pairs = (sm_count > 0 ? sm_count : sms) / 2;
+  if (pairs > sms / 2) pairs = sms / 2;
+  if (pairs > pairs_needed) pairs = pairs_needed;
+  if (pairs < 1) pairs = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
+  return e == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
+}
+
 int run_gemm(hq_mode mode, const void* a, const void* b, const GemmParams& p, int sm_count,
              bool pdl, cudaStream_t st) {
   int bn = forced_tile_n();
+  // dense problems with whole 256-column tiles use the 2-SM kernel unless a
+  // single-SM tile width is forced
+  if (bn == 0 && p.gs.sched == kDense && p.n % 256 == 0 && use_2sm()) {
+    return mode == HQ_MXFP8 ? run_bs_2sm<HQ_MXFP8, 6>(a, b, p, sm_count, pdl, st)
+                            : run_bs_2sm<HQ_NVFP4, 5>(a, b, p, sm_count, pdl, st);
+  }
   if (bn == 0) bn = (p.n % 256 == 0) ? 256 : 128;
   if (bn == 256 && p.n % 256 != 0 && p.n < 256) bn = 128;
   constexpr int T = kMaxGroups + 1;

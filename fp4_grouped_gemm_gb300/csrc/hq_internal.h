@@ -24,6 +24,9 @@ int num_sms();
 // Forced GEMM tile width (0 = automatic).
 int forced_tile_n();
 
+// Whether dense GEMMs may use the 2-SM (cluster pair) kernel.
+bool use_2sm();
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point.
 // Returns HQ_OK or HQ_ERR_CUDA.
 int encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, void* base,

@@ -128,8 +128,15 @@ int hq_set_wait_limit_ns(uint64_t ns);
 int hq_selftest_wait_expiry(uint64_t limit_ns, hq_stream_t s);
 
 /* Tuning knob: GEMM tile width in N for the block-scaled GEMMs (0 = choose
- * automatically, 128 or 256 = force).  Applies to later calls. */
+ * automatically, 128 or 256 = force a single-SM tile).  Applies to later
+ * calls. */
 int hq_set_gemm_tile_n(int tile_n);
+
+/* Tuning knob: 1 lets dense block-scaled GEMMs whose n is a multiple of 256
+ * run on pairs of SMs (a two-CTA cluster computing 256 x 256 tiles with
+ * cta_group::2 MMAs); 0 (default, currently the faster choice on GB300) keeps
+ * every GEMM on single-SM tiles.  Applies to later calls. */
+int hq_set_gemm_2sm(int enable);
 
 /* ------------------------------------------------------------------------- *
  * Group-wise quantiser

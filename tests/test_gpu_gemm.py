@@ -28,6 +28,7 @@ pytestmark = pytest.mark.gpu
 def _reset_knobs():
     yield
     hq.set_gemm_tile_n(0)
+    hq.set_gemm_2sm(0)
 
 
 def dense_case(m, n, k, mode, tile_n=0, alpha=None, bias=False, seed=0, g_a=None, g_b=None):
@@ -74,6 +75,18 @@ def test_dense_nvfp4_shapes(cuda_dev, tile_n, m, n, k):
 
 def test_dense_nvfp4_forced_256_partial_n_tile(cuda_dev):
     dense_case(200, 384, 512, "nvfp4", 256, alpha=2.0, seed=11)
+
+
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("m,n,k", [(256, 256, 256), (300, 512, 1024), (129, 768, 640), (640, 256, 320)])
+def test_dense_two_sm_tiles(cuda_dev, mode, m, n, k):
+    """The 2-SM (cluster pair, cta_group::2) kernel: 256 x 256 tiles, ragged M and K."""
+    if mode == "mxfp8" and k % 128:
+        pytest.skip("MXFP8 needs k % 128 == 0")
+    hq.set_gemm_2sm(1)
+    dense_case(m, n, k, mode, 0, alpha=0.5 if mode == "nvfp4" else 1.25,
+               bias=(mode == "mxfp8"), seed=m + k + (7 if mode == "nvfp4" else 0),
+               g_a=2.0 if mode == "nvfp4" else None, g_b=64.0 if mode == "nvfp4" else None)
 
 
 def test_dense_end_to_end_quant_then_gemm(cuda_dev):
