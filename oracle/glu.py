@@ -202,6 +202,21 @@ def dgeglu_epilogue(R, C, prob, geglu_alpha=1.702, clamp_max=7.0, clamp_min=-7.0
     return D, dprob
 
 
+def dgeglu_mult_mag(C, prob, geglu_alpha=1.702, clamp_max=7.0, clamp_min=-7.0, linear_offset=1.0):
+    """Magnitude of the activation factor multiplying R at each D column (dGeGLU)."""
+    X = np.asarray(C, dtype=np.float64)
+    N = X.shape[1] // 2
+    p = np.abs(np.asarray(prob, dtype=np.float64))[:, None]
+    gc, ic = interleave_columns(N)
+    gate_c = np.minimum(X[:, gc], clamp_max)
+    up_c = np.clip(X[:, ic], clamp_min, clamp_max)
+    s = sigmoid(geglu_alpha * gate_c)
+    mult = np.zeros_like(X)
+    mult[:, gc] = p * np.abs(up_c + linear_offset) * (s + geglu_alpha * np.abs(gate_c) * s * (1.0 - s))
+    mult[:, ic] = p * np.abs(gate_c) * s
+    return mult
+
+
 def dbias_from_D(D, group, L):
     """dbias[g, c] = sum over rows of group g of D[row, c] (D2)."""
     D = np.asarray(D, dtype=np.float64)
@@ -211,6 +226,33 @@ def dbias_from_D(D, group, L):
         if np.any(rows):
             out[g] = D[rows].sum(axis=0)
     return out
+
+
+def dgeglu(a, b, c, padded_offsets, alpha, prob):
+    """Full BF16 grouped GEMM + dGeGLU oracle (the BF16 backend's fixed
+    constants: geglu_alpha 1.702, clamp [-7, 7] on up and <= 7 on gate, linear
+    offset 1; C used without beta).  Same dict layout as dswiglu()."""
+    R, magR, grp = grouped_R(a, b, padded_offsets, alpha)
+    L = len(padded_offsets)
+    D, dprob = dgeglu_epilogue(R, c, prob)
+    written = grp >= 0
+    D[~written] = 0.0
+    dprob[~written] = 0.0
+    N = R.shape[1]
+    gc, ic = interleave_columns(N)
+    X = np.asarray(c, dtype=np.float64)
+    gate_c = np.minimum(X[:, gc], 7.0)
+    up_c = np.clip(X[:, ic], -7.0, 7.0)
+    s = sigmoid(1.702 * gate_c)
+    dprob_mag = np.sum(np.abs(R * gate_c * s * (up_c + 1.0)), axis=1)
+    magR2 = np.zeros_like(D)
+    magR2[:, gc] = magR
+    magR2[:, ic] = magR
+    return {
+        "D": D, "dprob": dprob, "dprob_mag": dprob_mag,
+        "dbias": dbias_from_D(D, grp, L), "dbias_mag": dbias_from_D(np.abs(D), grp, L),
+        "D_mag": magR2 * dgeglu_mult_mag(c, prob), "written": written, "group": grp,
+    }
 
 
 def dswiglu(a, b, c, padded_offsets, alpha, beta, prob):

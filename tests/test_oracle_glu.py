@@ -195,3 +195,24 @@ def test_dgeglu_clamp_masks():
     # the gate gradient at column 2 uses the clamped up (7) + offset
     s = scipy.special.expit(1.702 * 1.0)
     assert D[0, 2] == pytest.approx((7.0 + 1.0) * s * (1 + 1.702 * 1.0 * (1 - s)), rel=1e-14)
+
+
+def test_dgeglu_full_groups_match_epilogue_and_tail():
+    r = rng_(10)
+    M, N, K = 768, 32, 8
+    a = r.standard_normal((M, K))
+    b = r.standard_normal((2, N, K))
+    c = r.uniform(-9, 9, (M, 2 * N))            # exercises both clamps
+    prob = r.uniform(0, 1, M)
+    out = glu.dgeglu(a, b, c, [256, 512], [1.0, 0.5], prob)
+    assert out["written"][:512].all() and not out["written"][512:].any()
+    R1 = 0.25 * (a[256:512] @ b[1].T)
+    D1, p1 = glu.dgeglu_epilogue(R1, c[256:512], prob[256:512])
+    assert np.allclose(out["D"][256:512], D1, rtol=1e-13)
+    assert np.allclose(out["dprob"][256:512], p1, rtol=1e-13)
+    assert not out["D"][512:].any()
+    # the magnitude bound dominates |D| / |R| elementwise
+    R, _, _ = glu.grouped_R(a, b, [256, 512], [1.0, 0.5])
+    gc, ic = glu.interleave_columns(N)
+    ratio_g = np.abs(out["D"][:512, gc]) - np.abs(R[:512]) * glu.dgeglu_mult_mag(c, prob)[:512, gc]
+    assert (ratio_g <= 1e-12).all()
