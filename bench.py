@@ -499,8 +499,13 @@ class Extras:
                         20, self.flush)
         fl = 2.0 * M * n * k
         byts = M * k * 2 + L * n * k * 2 + 2 * M * 2 * n * 2 + M * 8
-        return {"dswiglu_bwd_L16": {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_bf16": fl / t / 1e12 / self.p_bf16,
-                                    "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / self.hbm}}
+        res = {"dswiglu_bwd_L16": {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_bf16": fl / t / 1e12 / self.p_bf16,
+                                   "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / self.hbm}}
+        t = time_kernel(lambda: hq.hq_gemm_dgeglu(c5["a"], c5["b"], c5["c"], off, c5["alpha"], c5["prob"], dprob,
+                                                  dbias=dbias, d_row=d_row, workspace=ws_t), 20, self.flush)
+        res["dgeglu_bwd_L16"] = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_bf16": fl / t / 1e12 / self.p_bf16,
+                                 "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / self.hbm}
+        return res
 
 
 def main():

@@ -20,7 +20,7 @@ __all__ = [
     "HQError", "mode_id", "group_size", "sf_bytes", "capabilities", "get_device_status",
     "set_wait_limit_ns", "selftest_wait_expiry", "set_gemm_tile_n", "set_gemm_2sm", "hq_quant",
     "hq_gemm_dense", "hq_gemm_grouped_contig", "hq_gemm_grouped_masked", "hq_swiglu_quant",
-    "hq_gemm_dswiglu", "hq_gemm_dswiglu_workspace_size", "swiglu_kb_dim",
+    "hq_gemm_dswiglu", "hq_gemm_dswiglu_workspace_size", "hq_gemm_dgeglu", "swiglu_kb_dim",
 ]
 
 _MODES = {"mxfp8": HQ_MXFP8, "w8a8-mxfp8": HQ_MXFP8, "nvfp4": HQ_NVFP4, "w4a4-nvfp4": HQ_NVFP4,
@@ -193,4 +193,24 @@ def hq_gemm_dswiglu(a, b, c, padded_offsets, alpha, beta, prob, dprob, dbias=Non
         _ptr(d_row), _ptr(dprob), _ptr(dbias), m, n, k, _ptr(workspace), ws_bytes, sm_count,
         _stream(stream))
     _check(rc, "hq_gemm_dswiglu")
+    return d_row, dprob, dbias
+
+
+def hq_gemm_dgeglu(a, b, c, padded_offsets, alpha, prob, dprob, dbias=None, d_row=None,
+                   workspace=None, sm_count=-1, stream=None):
+    """BF16 grouped GEMM + clamped-GeGLU backward.  dprob (and dbias) accumulate (+=)."""
+    m, k = a.shape
+    L, n, _ = b.shape
+    if d_row is None:
+        d_row = torch.empty(m, 2 * n, dtype=torch.bfloat16, device=a.device)
+    ws_bytes = 0
+    if dbias is not None:
+        ws_bytes = hq_gemm_dswiglu_workspace_size(L, n)
+        if workspace is None:
+            workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=a.device)
+        ws_bytes = workspace.numel() * workspace.element_size()
+    rc = _abi.load().hq_gemm_dgeglu(
+        _ptr(a), _ptr(b), _ptr(c), _ptr(padded_offsets), L, _ptr(alpha), _ptr(prob), _ptr(d_row),
+        _ptr(dprob), _ptr(dbias), m, n, k, _ptr(workspace), ws_bytes, sm_count, _stream(stream))
+    _check(rc, "hq_gemm_dgeglu")
     return d_row, dprob, dbias

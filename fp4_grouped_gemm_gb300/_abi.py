@@ -59,6 +59,8 @@ SIGNATURES = {
     "hq_gemm_dswiglu": (c_i32, [c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_p, c_p, c_p, c_p, c_i64,
                                 c_i64, c_i64, c_p, c_sz, c_i32, c_p]),
     "hq_gemm_dswiglu_workspace_size": (c_sz, [c_i32, c_i64]),
+    "hq_gemm_dgeglu": (c_i32, [c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_p, c_p, c_p, c_i64, c_i64,
+                               c_i64, c_p, c_sz, c_i32, c_p]),
     "hq_gemm_dswiglu_noalloc": (c_i32, [c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_p, c_p, c_p, c_p,
                                         c_i64, c_i64, c_i64, c_i32, c_p]),
 }

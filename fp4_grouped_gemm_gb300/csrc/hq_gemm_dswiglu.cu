@@ -78,9 +78,12 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 
 // 18 warps share four 16K-register sub-partitions (up to 5 warps on one):
 // 96 registers per thread is the most that lets the block launch.
+enum Act : int { kSwiGLU = 0, kGeGLU = 1 };
+
+template <int ACT>
 __global__ void __maxnreg__(96)
-    dswiglu_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const DsParams p) {
+    dglu_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const DsParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -207,7 +210,7 @@ __global__ void __maxnreg__(96)
       }
       const float alpha = __ldg(p.alpha + ti.g);
       const float a2 = __fmul_rn(alpha, alpha);
-      const float beta = __ldg(p.beta + ti.g);
+      const float beta = ACT == kSwiGLU ? __ldg(p.beta + ti.g) : 1.0f;
       const float prob = row_ok ? __ldg(p.prob + row) : 0.0f;
       const bool ok = wait_bounded(tfull_bar(acc), acc_phase, wctx);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
@@ -230,14 +233,27 @@ __global__ void __maxnreg__(96)
         const uint32_t iw = reinterpret_cast<const uint32_t*>(cv)[16 + i];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const float gate = __fmul_rn(beta, h ? bf16_hi(gw) : bf16_lo(gw));
-          const float inp = __fmul_rn(beta, h ? bf16_hi(iw) : bf16_lo(iw));
           const float R = __fmul_rn(a2, __uint_as_float(r[2 * i + h]));
-          const float s = rcp_approx(__fadd_rn(1.0f, expf(-gate)));  // sigmoid(gate)
           const float rp = __fmul_rn(R, prob);
-          dg[2 * i + h] = rp * inp * s * (1.0f + gate * (1.0f - s));
-          di[2 * i + h] = rp * gate * s;
-          dprob_part += R * gate * s * inp;
+          if (ACT == kSwiGLU) {
+            const float gate = __fmul_rn(beta, h ? bf16_hi(gw) : bf16_lo(gw));
+            const float inp = __fmul_rn(beta, h ? bf16_hi(iw) : bf16_lo(iw));
+            const float s = rcp_approx(__fadd_rn(1.0f, expf(-gate)));  // sigmoid(gate)
+            dg[2 * i + h] = rp * inp * s * (1.0f + gate * (1.0f - s));
+            di[2 * i + h] = rp * gate * s;
+            dprob_part += R * gate * s * inp;
+          } else {
+            // clamped GeGLU: gate <= 7, up in [-7, 7], s = sigmoid(1.702 gate_c),
+            // gradients kept at equality with the bounds, linear offset 1
+            const float gate = h ? bf16_hi(gw) : bf16_lo(gw);
+            const float up = h ? bf16_hi(iw) : bf16_lo(iw);
+            const float gc = fminf(gate, 7.0f);
+            const float uc = fminf(fmaxf(up, -7.0f), 7.0f);
+            const float s = rcp_approx(__fadd_rn(1.0f, expf(-1.702f * gc)));
+            dg[2 * i + h] = gate <= 7.0f ? rp * (uc + 1.0f) * s * (1.0f + 1.702f * gc * (1.0f - s)) : 0.0f;
+            di[2 * i + h] = (up >= -7.0f && up <= 7.0f) ? rp * gc * s : 0.0f;
+            dprob_part += R * gc * s * (uc + 1.0f);
+          }
         }
       }
       if (row_ok) {
@@ -310,20 +326,25 @@ size_t hq_gemm_dswiglu_workspace_size(int L, int64_t n) {
   return (bytes + 255) / 256 * 256;
 }
 
-int hq_gemm_dswiglu(const hq_bf16* a, const hq_bf16* b, const hq_bf16* c,
-                    const int32_t* padded_offsets, int L, const float* alpha, const float* beta,
-                    const float* prob, hq_bf16* d_row, float* dprob, hq_bf16* dbias, int64_t m,
-                    int64_t n, int64_t k, void* workspace, size_t ws_bytes, int sm_count,
-                    hq_stream_t s) {
-  using namespace hq;
+}  // extern "C"
+
+namespace hq {
+namespace {
+
+template <int ACT>
+int run_dglu(const hq_bf16* a, const hq_bf16* b, const hq_bf16* c, const int32_t* padded_offsets,
+             int L, const float* alpha, const float* beta, const float* prob, hq_bf16* d_row,
+             float* dprob, hq_bf16* dbias, int64_t m, int64_t n, int64_t k, void* workspace,
+             size_t ws_bytes, int sm_count, hq_stream_t s) {
   if (L < 1 || L > kMaxGroups) return HQ_ERR_INVALID;
   if (m < 0 || n <= 0 || k <= 0 || n % 32 != 0 || k % 8 != 0) return HQ_ERR_INVALID;
   if (m > (1ll << 31) - 256 || n > (1ll << 28) || k > (1ll << 30)) return HQ_ERR_INVALID;
-  if (!a || !b || !c || !padded_offsets || !alpha || !beta || !prob || !d_row || !dprob)
+  if (!a || !b || !c || !padded_offsets || !alpha || !prob || !d_row || !dprob)
     return HQ_ERR_INVALID;
+  if (ACT == kSwiGLU && !beta) return HQ_ERR_INVALID;
   if (!aligned16(a) || !aligned16(b) || !aligned16(c) || !aligned16(d_row)) return HQ_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(padded_offsets) | reinterpret_cast<uintptr_t>(alpha) |
-       reinterpret_cast<uintptr_t>(beta) | reinterpret_cast<uintptr_t>(prob) |
+       reinterpret_cast<uintptr_t>(beta ? beta : alpha) | reinterpret_cast<uintptr_t>(prob) |
        reinterpret_cast<uintptr_t>(dprob)) & 3u)
     return HQ_ERR_INVALID;
   if (dbias) {
@@ -373,7 +394,7 @@ int hq_gemm_dswiglu(const hq_bf16* a, const hq_bf16* b, const hq_bf16* c,
     const size_t bytes = static_cast<size_t>(L) * static_cast<size_t>(2 * n) * sizeof(float);
     if (cudaMemsetAsync(workspace, 0, bytes, st) != cudaSuccess) return HQ_ERR_CUDA;
   }
-  if (cudaFuncSetAttribute(dswiglu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(dglu_kernel<ACT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemBytes) != cudaSuccess)
     return HQ_ERR_CUDA;
   const int sms = num_sms();
@@ -383,7 +404,7 @@ int hq_gemm_dswiglu(const hq_bf16* a, const hq_bf16* b, const hq_bf16* c,
   if (grid > sms) grid = sms;
   if (grid > tiles_bound) grid = tiles_bound;
   if (grid < 1) grid = 1;
-  if (launch(dswiglu_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, st,
+  if (launch(dglu_kernel<ACT>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, st,
              false, tmA, tmB, p) != cudaSuccess)
     return HQ_ERR_CUDA;
   if (dbias) {
@@ -395,6 +416,28 @@ int hq_gemm_dswiglu(const hq_bf16* a, const hq_bf16* b, const hq_bf16* c,
     if (cudaGetLastError() != cudaSuccess) return HQ_ERR_CUDA;
   }
   return HQ_OK;
+}
+
+}  // namespace
+}  // namespace hq
+
+extern "C" {
+
+int hq_gemm_dswiglu(const hq_bf16* a, const hq_bf16* b, const hq_bf16* c,
+                    const int32_t* padded_offsets, int L, const float* alpha, const float* beta,
+                    const float* prob, hq_bf16* d_row, float* dprob, hq_bf16* dbias, int64_t m,
+                    int64_t n, int64_t k, void* workspace, size_t ws_bytes, int sm_count,
+                    hq_stream_t s) {
+  return hq::run_dglu<hq::kSwiGLU>(a, b, c, padded_offsets, L, alpha, beta, prob, d_row, dprob,
+                                   dbias, m, n, k, workspace, ws_bytes, sm_count, s);
+}
+
+int hq_gemm_dgeglu(const hq_bf16* a, const hq_bf16* b, const hq_bf16* c,
+                   const int32_t* padded_offsets, int L, const float* alpha, const float* prob,
+                   hq_bf16* d_row, float* dprob, hq_bf16* dbias, int64_t m, int64_t n, int64_t k,
+                   void* workspace, size_t ws_bytes, int sm_count, hq_stream_t s) {
+  return hq::run_dglu<hq::kGeGLU>(a, b, c, padded_offsets, L, alpha, nullptr, prob, d_row, dprob,
+                                  dbias, m, n, k, workspace, ws_bytes, sm_count, s);
 }
 
 }  // extern "C"

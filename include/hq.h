@@ -269,6 +269,25 @@ int hq_gemm_dswiglu(const hq_bf16 *a, const hq_bf16 *b, const hq_bf16 *c,
 size_t hq_gemm_dswiglu_workspace_size(int L, int64_t n);
 
 /* ------------------------------------------------------------------------- *
+ * cuDNN "Grouped GEMM + dGLU (SM100)", BF16 contract, act_func = "dgeglu":
+ * the same grouped GEMM R_g = alpha_g^2 A_g B_g^T, and a clamped-GeGLU
+ * backward over the saved C used as stored (no beta), with the BF16
+ * backend's fixed constants geglu_alpha = 1.702, glu_clamp_max = 7,
+ * glu_clamp_min = -7, linear_offset = 1.  Within every 64 columns of C the
+ * first 32 are gate and the next 32 are up:
+ *     gate_c = min(gate, 7),  up_c = clamp(up, -7, 7),  s = sigmoid(1.702 gate_c)
+ *     D_row[gate col] = R prob (up_c + 1) s (1 + 1.702 gate_c (1 - s))  if gate <= 7, else 0
+ *     D_row[up col]   = R prob gate_c s                                 if -7 <= up <= 7, else 0
+ *     dprob[m]       += sum_j R gate_c s (up_c + 1)
+ *     dbias[g, c]    += sum over rows m of group g of D_row[m, c]
+ * Arguments, layouts, accumulation, workspace and errors as hq_gemm_dswiglu
+ * (there is no beta). */
+int hq_gemm_dgeglu(const hq_bf16 *a, const hq_bf16 *b, const hq_bf16 *c,
+                   const int32_t *padded_offsets, int L, const float *alpha, const float *prob,
+                   hq_bf16 *d_row, float *dprob, hq_bf16 *dbias, int64_t m, int64_t n, int64_t k,
+                   void *workspace, size_t ws_bytes, int sm_count, hq_stream_t s);
+
+/* ------------------------------------------------------------------------- *
  * hq_gemm_dswiglu without caller-provided scratch.  The paper has no
  * counterpart to this entry point; it exists for callers that cannot
  * allocate device memory -- for example a plugin or custom op loaded into a

@@ -25,11 +25,11 @@ def bf16_ulp(x):
     return np.where(a > 0, 2.0 ** (e - 7), 2.0 ** -133)
 
 
-def run_case(offsets, m, n, k, seed, with_dbias=True):
+def run_case(offsets, m, n, k, seed, with_dbias=True, act="dswiglu", c_std=2.0):
     L = len(offsets)
     a = bf16_rows(m, k, seed)
     b = torch.stack([bf16_rows(n, k, seed + 1 + e, std=0.05) for e in range(L)])
-    c = bf16_rows(m, 2 * n, seed + 40, std=2.0)
+    c = bf16_rows(m, 2 * n, seed + 40, std=c_std)
     gen = torch.Generator().manual_seed(seed)
     prob = 1.0 - torch.rand(m, generator=gen)
     alpha = 0.8 + 0.4 * torch.rand(L, generator=gen)
@@ -38,10 +38,18 @@ def run_case(offsets, m, n, k, seed, with_dbias=True):
     dprob = torch.zeros(m, dtype=torch.float32, device=dev)
     dbias = torch.zeros(L, 2 * n, dtype=torch.bfloat16, device=dev) if with_dbias else None
     d_row = sentinel_bf16((m, 2 * n))
-    hq.hq_gemm_dswiglu(a.to(dev), b.to(dev), c.to(dev), torch.tensor(offsets, dtype=torch.int32, device=dev),
-                       alpha.to(dev), beta.to(dev), prob.to(dev), dprob, dbias=dbias, d_row=d_row)
+    off_t = torch.tensor(offsets, dtype=torch.int32, device=dev)
+    if act == "dswiglu":
+        hq.hq_gemm_dswiglu(a.to(dev), b.to(dev), c.to(dev), off_t, alpha.to(dev), beta.to(dev), prob.to(dev),
+                           dprob, dbias=dbias, d_row=d_row)
+    else:
+        hq.hq_gemm_dgeglu(a.to(dev), b.to(dev), c.to(dev), off_t, alpha.to(dev), prob.to(dev), dprob,
+                          dbias=dbias, d_row=d_row)
     torch.cuda.synchronize()
-    ref = glu.dswiglu(np_f32(a), np_f32(b), np_f32(c), offsets, alpha.numpy(), beta.numpy(), prob.numpy())
+    if act == "dswiglu":
+        ref = glu.dswiglu(np_f32(a), np_f32(b), np_f32(c), offsets, alpha.numpy(), beta.numpy(), prob.numpy())
+    else:
+        ref = glu.dgeglu(np_f32(a), np_f32(b), np_f32(c), offsets, alpha.numpy(), prob.numpy())
     return ref, d_row, dprob, dbias
 
 
@@ -67,6 +75,40 @@ def check(ref, d_row, dprob, dbias):
 def test_dswiglu_small(cuda_dev, n):
     offsets = [256, 256, 768, 1024]       # empty group 1; rows >= 1024 not written
     check(*run_case(offsets, 1152, n, 192, seed=n))
+
+
+@pytest.mark.parametrize("n", [64, 160])
+def test_dgeglu_small(cuda_dev, n):
+    """dGeGLU (fixed 1.702 / +-7 / +1 constants); C spread wide enough to hit both clamps."""
+    offsets = [256, 256, 768, 1024]
+    check(*run_case(offsets, 1152, n, 192, seed=100 + n, act="dgeglu", c_std=5.0))
+
+
+def test_dgeglu_clamp_boundaries_exact(cuda_dev):
+    """Gate and up values exactly at the clamp bounds keep their gradients."""
+    m, n, k = 256, 32, 64
+    g = torch.Generator().manual_seed(3)
+    a = torch.randn(m, k, generator=g).to(torch.bfloat16)
+    b = (torch.randn(1, n, k, generator=g) * 0.05).to(torch.bfloat16)
+    c = torch.randn(m, 2 * n, generator=g) * 3
+    c[:, 0] = 7.0
+    c[:, 1] = 7.5
+    c[:, 32] = 7.0
+    c[:, 33] = -7.0
+    c[:, 34] = -7.5
+    c = c.to(torch.bfloat16)
+    prob = 1.0 - torch.rand(m, generator=g)
+    alpha = torch.tensor([1.1])
+    dev = torch.device("cuda")
+    dprob = torch.zeros(m, device=dev)
+    d_row, _, _ = hq.hq_gemm_dgeglu(a.to(dev), b.to(dev), c.to(dev), torch.tensor([m], dtype=torch.int32, device=dev),
+                                    alpha.to(dev), prob.to(dev), dprob)
+    torch.cuda.synchronize()
+    ref = glu.dgeglu(np_f32(a), np_f32(b), np_f32(c), [m], alpha.numpy(), prob.numpy())
+    check(ref, d_row, dprob, None)
+    D = d_row.float().cpu().numpy()
+    assert (D[:, 1] == 0).all() and (D[:, 34] == 0).all()       # masked beyond the bounds
+    assert (D[:, 0] != 0).any() and (D[:, 32] != 0).any() and (D[:, 33] != 0).any()
 
 
 def test_dswiglu_no_dbias(cuda_dev):
