@@ -444,13 +444,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // work compared with the 128 x 256 single-SM tile.
 //
 // Completion never crosses CTAs through TMA: each CTA's copies complete on its
-// own barriers; each CTA's scale warps wait for their CTA's stage, stage its
-// scales into their TMEM and arrive on their CTA's "ready" barrier; in the odd
-// CTA a relay thread forwards each completed phase to the even CTA's "ready"
-// barrier, which therefore also certifies the odd CTA's operands.  The even
-// CTA's commits are multicast to both CTAs' "empty" and "accumulator full"
-// barriers; epilogue warps arrive on their CTA's "accumulator empty" barrier
-// and the odd CTA's is relayed to the even CTA the same way.  Scale factors: each CTA holds the A scales of
+// own barriers.  Each CTA's scale warps stage its scales into their TMEM and
+// arrive on the even CTA's "ready" barrier; one thread of the odd CTA forwards
+// each completed phase of its A/B barrier to the even CTA's "peer full"
+// barrier.  The even CTA's commits are multicast to both CTAs' "empty" and
+// "accumulator full" barriers; all epilogue warps arrive on the even CTA's
+// "accumulator empty" barrier.  Those cross-CTA arrivals are relaxed: what
+// they order is tcgen05 work already completed with tcgen05.wait, and a
+// release would first wait for the warp's earlier global stores.  Scale factors: each CTA holds the A scales of
 // its own 128 rows and the B scales of all 256 tile columns in its TMEM, in
 // the same layout as the single-SM N = 256 tile.
 // ---------------------------------------------------------------------------
@@ -478,7 +479,7 @@ struct Cfg2 {
   static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
   static constexpr int OFF_STAGE_OUT = OFF_SFB + STAGES * SFB_BYTES;
   static constexpr int OFF_BAR = OFF_STAGE_OUT + 4 * 2048;
-  static constexpr int NUM_BARS = 4 * STAGES + 3;
+  static constexpr int NUM_BARS = 5 * STAGES + 3;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget");
@@ -509,7 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };     // leader's commit
   auto sffull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); }; // this CTA's scales
   auto ready_bar = [&](int s) { return bar0 + 8u * (3 * STAGES + s); };  // used in the leader
-  const uint32_t tfull_bar = bar0 + 8u * (4 * STAGES);
+  auto peerfull_bar = [&](int s) { return bar0 + 8u * (4 * STAGES + s); };  // used in the leader
+  const uint32_t tfull_bar = bar0 + 8u * (5 * STAGES);
   const uint32_t tempty_bar = tfull_bar + 8u;  // used in the leader
   const uint32_t drain_bar = tfull_bar + 16u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
@@ -521,11 +523,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
       mbar_init(sffull_bar(s), 1);
-      // 4 local scale warps, plus (even CTA) one arrival relayed from the odd CTA
-      mbar_init(ready_bar(s), leader ? 5 : 4);
+      mbar_init(ready_bar(s), 8);     // 4 scale warps in each CTA
+      mbar_init(peerfull_bar(s), 1);  // the odd CTA's A and B tiles landed
     }
     mbar_init(tfull_bar, 1);
-    mbar_init(tempty_bar, leader ? 5 : 4);  // 4 epilogue warps (+ relay in the even CTA)
+    mbar_init(tempty_bar, 8);  // 4 epilogue warps in each CTA
     mbar_init(drain_bar, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -600,28 +602,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1 && !leader) {
-    // ------------------------------------------------------------ relays (odd CTA)
-    // A warp's cluster-scope release arrive would first wait for all its
-    // earlier global stores to be acknowledged; so every warp arrives on its
-    // own CTA's barrier and one otherwise idle thread here forwards a single
-    // cluster-scope arrival per phase to the even CTA.
+    // ------------------------------------------------------------ odd CTA: operands landed
+    // Forwards each completed phase of this CTA's A/B barrier to the even
+    // CTA, whose MMAs read these tiles.
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       for (int64_t t = cluster_id; ok && t < total; t += num_clusters)
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!wait_bounded(ready_bar(stage), phase, wctx)) { ok = false; break; }
-          mbar_arrive_cluster(mapa_shared(ready_bar(stage), 0));
+          if (!wait_bounded(full_bar(stage), phase, wctx)) { ok = false; break; }
+          mbar_arrive_cluster(mapa_shared(peerfull_bar(stage), 0));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-    } else if (lane == 1) {
-      uint32_t acc_phase = 0;
-      for (int64_t t = cluster_id; t < total; t += num_clusters) {
-        if (!wait_bounded(tempty_bar, acc_phase, wctx)) break;
-        mbar_arrive_cluster(mapa_shared(tempty_bar, 0));
-        acc_phase ^= 1u;
-      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
@@ -634,6 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!wait_bounded(full_bar(stage), phase, wctx) ||
+              !wait_bounded(peerfull_bar(stage), phase, wctx) ||
               !wait_bounded(ready_bar(stage), phase, wctx)) { ok = false; break; }
           tc_fence_after();
           int atoms = atoms_total - kb * C::ATOMS;
@@ -678,9 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < num_kb; ++kb) {
         int atoms = atoms_total - kb * C::ATOMS;
         atoms = atoms < C::ATOMS ? atoms : C::ATOMS;
-        // the odd CTA's arrival also certifies its A and B tiles for this stage
-        const bool w = wait_bounded(sffull_bar(stage), phase, wctx) &&
-                       (leader || wait_bounded(full_bar(stage), phase, wctx));
+        const bool w = wait_bounded(sffull_bar(stage), phase, wctx);
         ok = __all_sync(0xFFFFFFFFu, w);
         if (!ok) break;
         const uint32_t sfa_t = tmem_base + C::SF_BASE_COL + stage * C::SF_STAGE_COLS;
@@ -714,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(ready_bar(stage));
+        if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(ready_bar(stage), 0));
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }
@@ -792,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar);
+      if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(tempty_bar, 0));
       acc_phase ^= 1u;
     }
   }
