@@ -45,7 +45,7 @@ RATIO = {"bf16": 1.0, "fp8": 2.0, "fp4": 6.0}
 SECTIONS = ("dense_mxfp8_256", "quant_nvfp4", "moe_contig", "moe_masked", "dswiglu")
 
 
-GEMM_PROFILE = os.path.join(ROOT, "profiles", "bs_gemm_kernel_dense_nvfp4_4096x12288x5120.md")
+GEMM_PROFILE = os.path.join(ROOT, "profiles", "bs_gemm_2sm_kernel_dense_nvfp4_4096x12288x5120.md")
 GEMM_SOURCES = ("hq_gemm_bs.cu", "hq_ptx.cuh", "hq_sched.cuh", "hq_internal.h")
 
 
@@ -372,7 +372,7 @@ def headline(hq, dev, args, ws, peaks, pk_src):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_fp4, "unit": "TFLOP/s",
                      "frac": achieved / peak_fp4, "traffic": profiled_traffic(),
                      "traffic_unit": "bytes per launch (ncu dram read + write)",
-                     "kernel": "bs_gemm_kernel<NVFP4,256>",
+                     "kernel": "bs_gemm_2sm_kernel<NVFP4,5> (cluster pair, 256x256 tiles)",
                      "peak_source": f"{pk_src} bf16 burst {peaks['bf16_tflops']} x 6 (nominal FP4/BF16)"},
         "e2e": {"value": ws * flops / e2e_t / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

@@ -23,7 +23,7 @@ uint32_t* g_status_ptr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 std::atomic<uint64_t> g_wait_limit_ns{1000000000ull};
 std::atomic<int> g_tile_n{0};
-std::atomic<int> g_use_2sm{0};
+std::atomic<int> g_use_2sm{1};
 using EncodeFn = decltype(&cuTensorMapEncodeTiled);
 EncodeFn g_encode = nullptr;
 

@@ -37,7 +37,9 @@ namespace {
 //      exactly as the warpx4 copy would, then signal the MMA thread.
 constexpr int kSfPath = 2;
 constexpr int kSfWarps = kSfPath == 1 ? 1 : (kSfPath == 2 ? 4 : 0);
-constexpr int kThreads = 192 + 32 * kSfWarps;
+constexpr int kEpiWarps = 8;             // warps 2..9: two per TMEM lane quarter
+constexpr int kSfWarp0 = 2 + kEpiWarps;  // first scale-staging warp
+constexpr int kThreads = 32 * (kSfWarp0 + kSfWarps);
 constexpr int kBKBytes = 128;   // bytes of K per stage and row (one 128B swizzle span)
 constexpr int kMmaKBytes = 32;  // bytes of K consumed by one MMA
 constexpr int kSmemLimit = 232448;
@@ -81,8 +83,8 @@ struct Cfg {
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-  static constexpr int OFF_STAGE_OUT = OFF_SFB + STAGES * SFB_BYTES;  // 4 warps x 2 KB
-  static constexpr int OFF_TABLE = OFF_STAGE_OUT + 4 * 2048;          // 2 x TABLE int32
+  static constexpr int OFF_STAGE_OUT = OFF_SFB + STAGES * SFB_BYTES;  // 1 KB per epilogue warp
+  static constexpr int OFF_TABLE = OFF_STAGE_OUT + kEpiWarps * 1024;  // 2 x TABLE int32
   static constexpr int OFF_BAR = OFF_TABLE + 2 * TABLE * 4 + 8;
   static constexpr int NUM_BARS = 3 * STAGES + 2 * ACC + 2;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
@@ -95,6 +97,124 @@ struct Cfg {
                         : ((1u << 7) | (1u << 10) | (0u << 23)))  // E2M1 x E2M1, UE4M3
       | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
 };
+
+// ---------------------------------------------------------------------------
+// Epilogue of one accumulator tile for one warp: TMEM lane quarter q holds
+// rows row0 + 32 q + lane; the warp owns tile columns [cw, cw + BN / 2).
+//   out[row, n0 + j] = bf16_rne(alpha * acc[row, j] + bias[n0 + j])
+// DRAIN: the warp first moves its whole share out of TMEM (as BF16 pairs in
+// registers) and calls release() before any global store, so the MMAs of the
+// next tile can start while the stores drain; otherwise release() follows the
+// stores.  Stores go through the warp's 1 KB staging buffer, 16 columns at a
+// time, so that two lanes write each row's 32 contiguous bytes.
+// ---------------------------------------------------------------------------
+struct EpiArgs {
+  uint32_t acc_t;        // TMEM address of (lane quarter, tile column 0)
+  int cw;                // first tile column of this warp
+  int64_t n0, n;         // tile's first output column, output width
+  float alpha;
+  const uint16_t* bias;  // bias row of the group (column 0) or null
+  uint16_t* out;         // output row of lane 0 of this quarter (column 0)
+  int rows_here;         // valid rows of this quarter (may be <= 0 or > 32)
+  uint32_t stage_s;      // this warp's staging buffer (shared address)
+  int lane;
+};
+
+__device__ __forceinline__ void epi_convert16(const EpiArgs& e, int64_t col0, const uint32_t (&r)[16],
+                                              uint32_t* packed) {
+  if (e.bias) {
+    const uint4* bp = reinterpret_cast<const uint4*>(e.bias + col0);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint4 v = __ldg(bp + i);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float v0, v1;
+        mul_f32x2(v0, v1, __uint_as_float(r[8 * i + 2 * j]), __uint_as_float(r[8 * i + 2 * j + 1]),
+                  e.alpha);
+        add_f32x2(v0, v1, v0, v1, __uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u));
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(v0, v1);
+        packed[4 * i + j] = *reinterpret_cast<uint32_t*>(&b2);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float v0, v1;
+      mul_f32x2(v0, v1, __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), e.alpha);
+      __nv_bfloat162 b2 = __floats2bfloat162_rn(v0, v1);
+      packed[i] = *reinterpret_cast<uint32_t*>(&b2);
+    }
+  }
+}
+
+__device__ __forceinline__ void epi_store16(const EpiArgs& e, int64_t col0, const uint32_t* packed) {
+  const int lane = e.lane;
+  // stage: row = lane, two 16-byte units, unit index xor-swizzled by row bit 2
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const uint32_t off = lane * 32 + ((u ^ ((lane >> 2) & 1)) * 16);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(e.stage_s + off),
+                 "r"(packed[4 * u]), "r"(packed[4 * u + 1]), "r"(packed[4 * u + 2]),
+                 "r"(packed[4 * u + 3])
+                 : "memory");
+  }
+  __syncwarp();
+#pragma unroll
+  for (int it = 0; it < 2; ++it) {
+    const int rr = it * 16 + (lane >> 1);
+    const int u = lane & 1;
+    const uint32_t off = rr * 32 + ((u ^ ((rr >> 2) & 1)) * 16);
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(e.stage_s + off)
+                 : "memory");
+    if (rr < e.rows_here) *reinterpret_cast<uint4*>(e.out + rr * e.n + col0 + u * 8) = v;
+  }
+  __syncwarp();
+}
+
+template <int BN, bool DRAIN, typename Release>
+__device__ __forceinline__ void epilogue_tile(const EpiArgs& e, Release release) {
+  constexpr int kPieces = BN / 2 / 16;  // 16-column pieces per warp
+  if (DRAIN) {
+    // piece s + 1 is read from TMEM while piece s is converted
+    uint32_t packed[kPieces * 8];
+    uint32_t r[2][16];
+    tmem_ld_32x32b_x16(e.acc_t + e.cw, r[0]);
+    tmem_ld_wait(r[0]);
+#pragma unroll
+    for (int s = 0; s < kPieces; ++s) {
+      if (s + 1 < kPieces) tmem_ld_32x32b_x16(e.acc_t + e.cw + (s + 1) * 16, r[(s + 1) & 1]);
+      const int64_t col0 = e.n0 + e.cw + s * 16;
+      if (col0 < e.n) epi_convert16(e, col0, r[s & 1], packed + 8 * s);
+      if (s + 1 < kPieces) tmem_ld_wait(r[(s + 1) & 1]);
+    }
+    tc_fence_before();
+    __syncwarp();
+    release();
+#pragma unroll
+    for (int s = 0; s < kPieces; ++s) {
+      const int64_t col0 = e.n0 + e.cw + s * 16;
+      if (col0 < e.n) epi_store16(e, col0, packed + 8 * s);
+    }
+  } else {
+    for (int s = 0; s < kPieces; ++s) {
+      uint32_t r[16], packed[8];
+      tmem_ld_32x32b_x16(e.acc_t + e.cw + s * 16, r);
+      tmem_ld_wait(r);
+      const int64_t col0 = e.n0 + e.cw + s * 16;
+      if (col0 >= e.n) continue;
+      epi_convert16(e, col0, r, packed);
+      epi_store16(e, col0, packed);
+    }
+    tc_fence_before();
+    __syncwarp();
+    release();
+  }
+}
 
 template <int MODE, int BN, int STAGES, int ACC, int TABLE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -131,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < ACC; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4);
+      mbar_init(tempty_bar(a), kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     mbar_init(drain_sf_bar, 1);
@@ -207,6 +327,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
+      // The tensor pipe keeps only about one MMA queued behind the executing
+      // one, so every instruction this thread runs between MMAs can leave it
+      // idle: descriptors are formed once and advanced by constants, and a
+      // whole k-block's MMAs are issued unrolled.
+      const uint64_t adesc0 = smem_desc_sw128(sbase + C::OFF_A);
+      const uint64_t bdesc0 = smem_desc_sw128(sbase + C::OFF_B);
+      constexpr int kFullMma = MODE == HQ_MXFP8 ? kBKBytes / kMmaKBytes : C::ATOMS;
       for (int64_t t = blockIdx.x; ok && t < sch.total_tiles; t += gridDim.x) {
         const TileInfo ti = decode_tile(p.gs, sch, t, BN);
         int rb_valid = static_cast<int>((p.n - ti.n0 + 127) / 128);
@@ -234,24 +361,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      smem_desc_sfatom(sfb_s + (rb * C::ATOMS + a) * 512));
             }
           }
-          const uint32_t a_s = sbase + C::OFF_A + stage * C::A_BYTES;
-          const uint32_t b_s = sbase + C::OFF_B + stage * C::B_BYTES;
-          const int n_mma = MODE == HQ_MXFP8 ? (kBKBytes / kMmaKBytes) : atoms;
-          for (int j = 0; j < n_mma; ++j) {
-            const uint64_t adesc = smem_desc_sw128(a_s + j * kMmaKBytes);
-            const uint64_t bdesc = smem_desc_sw128(b_s + j * kMmaKBytes);
-            const uint32_t acc_flag = (kb > 0 || j > 0) ? 1u : 0u;
+          // descriptor start addresses are in 16-byte units; one MMA consumes
+          // 32 bytes of K
+          const uint64_t ad = adesc0 + static_cast<uint64_t>((stage * C::A_BYTES) >> 4);
+          const uint64_t bd = bdesc0 + static_cast<uint64_t>((stage * C::B_BYTES) >> 4);
+          const uint32_t acc0 = kb > 0 ? 1u : 0u;
+          auto issue = [&](int j, uint32_t acc_flag) {
             if (MODE == HQ_MXFP8) {
               // one scale per row per MMA: byte j of the atom's 32-bit columns
               const uint32_t idesc = C::IDESC_BASE | (static_cast<uint32_t>(j) << 4) |
                                      (static_cast<uint32_t>(j) << 29);
-              mma_mxf8(d_tmem, adesc, bdesc, idesc, sfa_t | (static_cast<uint32_t>(j) << 30),
+              mma_mxf8(d_tmem, ad + 2 * j, bd + 2 * j, idesc,
+                       sfa_t | (static_cast<uint32_t>(j) << 30),
                        sfb_t | (static_cast<uint32_t>(j) << 30), acc_flag);
             } else {
               // four scales per row per MMA: one whole atom column group
-              mma_nvf4(d_tmem, adesc, bdesc, C::IDESC_BASE, sfa_t + j * 4,
+              mma_nvf4(d_tmem, ad + 2 * j, bd + 2 * j, C::IDESC_BASE, sfa_t + j * 4,
                        sfb_t + j * C::RB * 4, acc_flag);
             }
+          };
+          if (MODE == HQ_MXFP8 || atoms == C::ATOMS) {
+#pragma unroll
+            for (int j = 0; j < kFullMma; ++j) issue(j, j > 0 ? 1u : acc0);
+          } else {
+            for (int j = 0; j < atoms; ++j) issue(j, j > 0 ? 1u : acc0);
           }
           tc_commit(empty_bar(stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -264,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit(drain_bar);
       wait_drain(drain_bar, 0, p.wait_limit_ns);
     }
-  } else if (warp >= 6) {
+  } else if (warp >= kSfWarp0) {
     // ------------------------------------------------------------ scale staging
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int stage = 0;
@@ -347,80 +480,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    uint8_t* stage_out = smem + C::OFF_STAGE_OUT + (warp - 2) * 2048;
-    const uint32_t stage_out_s = smem_u32(stage_out);
+    const int ew = warp - 2;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int64_t t = blockIdx.x; t < sch.total_tiles; t += gridDim.x) {
       const TileInfo ti = decode_tile(p.gs, sch, t, BN);
+      const float alpha = p.alpha ? __ldg(p.alpha + ti.g) : 1.0f;  // loaded before the wait
       // every lane waits; the warp proceeds only if all lanes saw completion
       const bool ok = wait_bounded(tfull_bar(acc), acc_phase, wctx);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       tc_fence_after();
-      const float alpha = p.alpha ? __ldg(p.alpha + ti.g) : 1.0f;
-      const uint16_t* bias_row = p.bias ? p.bias + static_cast<int64_t>(ti.g) * p.n : nullptr;
-      const int rows_here = ti.rows_valid - q * 32;  // valid rows of this warp's quarter
-      for (int c = 0; c < BN / 32; ++c) {
-        const int col0 = ti.n0 + c * 32;
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c * 32, r);
-        tmem_ld_wait();
-        if (col0 >= p.n) continue;
-        float bias_v[32];
-        if (bias_row) {
-          const uint4* bp = reinterpret_cast<const uint4*>(bias_row + col0);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint4 v = __ldg(bp + i);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              bias_v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
-              bias_v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) bias_v[i] = 0.0f;
-        }
-        uint32_t packed[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float v0 = __fadd_rn(__fmul_rn(alpha, __uint_as_float(r[2 * i])), bias_v[2 * i]);
-          const float v1 = __fadd_rn(__fmul_rn(alpha, __uint_as_float(r[2 * i + 1])), bias_v[2 * i + 1]);
-          __nv_bfloat162 b2 = __floats2bfloat162_rn(v0, v1);
-          packed[i] = *reinterpret_cast<uint32_t*>(&b2);
-        }
-        // stage: row = lane, 4 x 16-byte chunks, chunk index xor-swizzled
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t off = lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage_out_s + off),
-                       "r"(packed[4 * j]), "r"(packed[4 * j + 1]), "r"(packed[4 * j + 2]),
-                       "r"(packed[4 * j + 3])
-                       : "memory");
-        }
-        __syncwarp();
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-          const int rr = it * 8 + (lane >> 2);
-          const int j = lane & 3;
-          const uint32_t off = rr * 64 + ((j ^ ((rr >> 1) & 3)) * 16);
-          uint4 v;
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                       : "r"(stage_out_s + off)
-                       : "memory");
-          if (rr < rows_here) {
-            uint16_t* dst = p.out + (ti.row0 + q * 32 + rr) * p.n + col0 + j * 8;
-            *reinterpret_cast<uint4*>(dst) = v;
-          }
-        }
-        __syncwarp();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      EpiArgs e;
+      e.acc_t = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      e.cw = (ew >> 2) * (BN / 2);
+      e.n0 = ti.n0;
+      e.n = p.n;
+      e.alpha = alpha;
+      e.bias = p.bias ? p.bias + static_cast<int64_t>(ti.g) * p.n : nullptr;
+      e.out = p.out + (ti.row0 + q * 32) * p.n;
+      e.rows_here = ti.rows_valid - q * 32;
+      e.stage_s = sbase + C::OFF_STAGE_OUT + ew * 1024;
+      e.lane = lane;
+      const uint32_t tempty = tempty_bar(acc);
+      // with one accumulator the next tile's MMAs wait for this epilogue:
+      // release TMEM before storing
+      epilogue_tile<BN, ACC == 1>(e, [&] { if (lane == 0) mbar_arrive(tempty); });
       if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
     }
   }
@@ -443,14 +527,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 // its own TMEM.  Per SM this halves the B operand bytes fetched for the same
 // work compared with the 128 x 256 single-SM tile.
 //
-// Completion never crosses CTAs through TMA: each CTA's copies complete on its
-// own barriers.  Each CTA's scale warps stage its scales into their TMEM and
-// arrive on the even CTA's "ready" barrier; one thread of the odd CTA forwards
-// each completed phase of its A/B barrier to the even CTA's "peer full"
-// barrier.  The even CTA's commits are multicast to both CTAs' "empty" and
-// "accumulator full" barriers; all epilogue warps arrive on the even CTA's
-// "accumulator empty" barrier.  Those cross-CTA arrivals are relaxed: what
-// they order is tcgen05 work already completed with tcgen05.wait, and a
+// Both CTAs' A / B copies complete on the even CTA's "full" barrier (the
+// cta_group::2 form of the TMA load), which expects the bytes of the pair; the
+// scale copies complete on each CTA's own barrier.  Each CTA's scale warps
+// stage its scales into its TMEM and arrive on the even CTA's "ready" barrier;
+// the even CTA's scale warps arrive only once the pair's A / B tiles landed, so
+// the MMA issuer waits on that single barrier per stage.
+// The even CTA's commits are multicast to both CTAs' "empty" and "accumulator
+// full" barriers; all epilogue warps arrive on the even CTA's "accumulator
+// empty" barrier.  Those cross-CTA arrivals are relaxed: what they order is
+// tcgen05 work already completed with tcgen05.wait, and a
 // release would first wait for the warp's earlier global stores.  Scale factors: each CTA holds the A scales of
 // its own 128 rows and the B scales of all 256 tile columns in its TMEM, in
 // the same layout as the single-SM N = 256 tile.
@@ -478,8 +564,8 @@ struct Cfg2 {
   static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
   static constexpr int OFF_STAGE_OUT = OFF_SFB + STAGES * SFB_BYTES;
-  static constexpr int OFF_BAR = OFF_STAGE_OUT + 4 * 2048;
-  static constexpr int NUM_BARS = 5 * STAGES + 3;
+  static constexpr int OFF_BAR = OFF_STAGE_OUT + kEpiWarps * 1024;
+  static constexpr int NUM_BARS = 4 * STAGES + 3;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget");
@@ -506,12 +592,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool leader = rank == 0;
 
   const uint32_t bar0 = sbase + C::OFF_BAR;
-  auto full_bar = [&](int s) { return bar0 + 8u * s; };                 // this CTA's A, B
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };                 // the pair's A, B (leader)
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };     // leader's commit
   auto sffull_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + s); }; // this CTA's scales
   auto ready_bar = [&](int s) { return bar0 + 8u * (3 * STAGES + s); };  // used in the leader
-  auto peerfull_bar = [&](int s) { return bar0 + 8u * (4 * STAGES + s); };  // used in the leader
-  const uint32_t tfull_bar = bar0 + 8u * (5 * STAGES);
+  const uint32_t tfull_bar = bar0 + 8u * (4 * STAGES);
   const uint32_t tempty_bar = tfull_bar + 8u;  // used in the leader
   const uint32_t drain_bar = tfull_bar + 16u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
@@ -524,10 +609,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(empty_bar(s), 1);
       mbar_init(sffull_bar(s), 1);
       mbar_init(ready_bar(s), 8);     // 4 scale warps in each CTA
-      mbar_init(peerfull_bar(s), 1);  // the odd CTA's A and B tiles landed
     }
     mbar_init(tfull_bar, 1);
-    mbar_init(tempty_bar, 8);  // 4 epilogue warps in each CTA
+    mbar_init(tempty_bar, 2 * kEpiWarps);  // every epilogue warp of both CTAs
     mbar_init(drain_bar, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -576,11 +660,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, wctx)) { ok = false; break; }
           int atoms = atoms_total - kb * C::ATOMS;
           atoms = atoms < C::ATOMS ? atoms : C::ATOMS;
-          mbar_arrive_expect_tx(full_bar(stage), C::A_BYTES + C::B_BYTES);
-          tma_load_2d(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, full_bar(stage), kb * kBKBytes,
-                      static_cast<int32_t>(row0));
-          tma_load_3d(sbase + C::OFF_B + stage * C::B_BYTES, &tmB, full_bar(stage), kb * kBKBytes,
-                      nh0, 0);
+          // both CTAs' A / B tiles complete on the even CTA's full barrier,
+          // which expects the bytes of the pair
+          if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * (C::A_BYTES + C::B_BYTES));
+          const uint32_t fb = mapa_shared(full_bar(stage), 0);
+          tma_load_2d_pair(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, fb, kb * kBKBytes,
+                           static_cast<int32_t>(row0));
+          tma_load_3d_pair(sbase + C::OFF_B + stage * C::B_BYTES, &tmB, fb, kb * kBKBytes, nh0, 0);
           mbar_arrive_expect_tx(sffull_bar(stage), atoms * 512u * (has_sfa ? 3u : 2u));
           if (has_sfa)
             bulk_load(sbase + C::OFF_SFA + stage * C::SFA_BYTES, sfa_rows + kb * C::ATOMS * 512,
@@ -596,60 +682,60 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
+      // the even CTA's full barriers count both CTAs' A / B bytes, so its
+      // drain covers the odd CTA's copies too (the odd CTA stays resident
+      // until the final cluster barrier)
       for (int s = 0; s < STAGES; ++s) {
-        if (filled_a & (1u << s)) wait_drain(full_bar(s), (par_a >> s) & 1u, p.wait_limit_ns);
+        if (leader && (filled_a & (1u << s)))
+          wait_drain(full_bar(s), (par_a >> s) & 1u, p.wait_limit_ns);
         if (filled_s & (1u << s)) wait_drain(sffull_bar(s), (par_s >> s) & 1u, p.wait_limit_ns);
       }
     }
   } else if (warp == 1 && !leader) {
-    // ------------------------------------------------------------ odd CTA: operands landed
-    // Forwards each completed phase of this CTA's A/B barrier to the even
-    // CTA, whose MMAs read these tiles.
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int64_t t = cluster_id; ok && t < total; t += num_clusters)
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!wait_bounded(full_bar(stage), phase, wctx)) { ok = false; break; }
-          mbar_arrive_cluster(mapa_shared(peerfull_bar(stage), 0));
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        }
-    }
+    // odd CTA: no MMA issuer
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
+      // as in the single-SM kernel: constant descriptor advances, unrolled
+      // MMAs, one wait per stage
+      const uint64_t adesc0 = smem_desc_sw128(sbase + C::OFF_A);
+      const uint64_t bdesc0 = smem_desc_sw128(sbase + C::OFF_B);
+      constexpr int kFullMma = MODE == HQ_MXFP8 ? kBKBytes / kMmaKBytes : C::ATOMS;
       for (int64_t t = cluster_id; ok && t < total; t += num_clusters) {
         if (!wait_bounded(tempty_bar, acc_phase ^ 1u, wctx)) break;
         tc_fence_after();
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!wait_bounded(full_bar(stage), phase, wctx) ||
-              !wait_bounded(peerfull_bar(stage), phase, wctx) ||
-              !wait_bounded(ready_bar(stage), phase, wctx)) { ok = false; break; }
+          // "ready" completes after the pair's A / B tiles landed and both
+          // CTAs' scales for the stage are in TMEM
+          if (!wait_bounded(ready_bar(stage), phase, wctx)) { ok = false; break; }
           tc_fence_after();
           int atoms = atoms_total - kb * C::ATOMS;
           atoms = atoms < C::ATOMS ? atoms : C::ATOMS;
           const uint32_t sfa_t = tmem_base + C::SF_BASE_COL + stage * C::SF_STAGE_COLS;
           const uint32_t sfb_t = sfa_t + C::SFA_COLS;
-          const uint32_t a_s = sbase + C::OFF_A + stage * C::A_BYTES;
-          const uint32_t b_s = sbase + C::OFF_B + stage * C::B_BYTES;
-          const int n_mma = MODE == HQ_MXFP8 ? (kBKBytes / kMmaKBytes) : atoms;
-          for (int j = 0; j < n_mma; ++j) {
-            const uint64_t adesc = smem_desc_sw128(a_s + j * kMmaKBytes);
-            const uint64_t bdesc = smem_desc_sw128(b_s + j * kMmaKBytes);
-            const uint32_t acc_flag = (kb > 0 || j > 0) ? 1u : 0u;
+          const uint64_t ad = adesc0 + static_cast<uint64_t>((stage * C::A_BYTES) >> 4);
+          const uint64_t bd = bdesc0 + static_cast<uint64_t>((stage * C::B_BYTES) >> 4);
+          const uint32_t acc0 = kb > 0 ? 1u : 0u;
+          auto issue = [&](int j, uint32_t acc_flag) {
             if (MODE == HQ_MXFP8) {
               const uint32_t idesc = C::IDESC_BASE | (static_cast<uint32_t>(j) << 4) |
                                      (static_cast<uint32_t>(j) << 29);
-              mma_mxf8_2sm(tmem_base, adesc, bdesc, idesc, sfa_t | (static_cast<uint32_t>(j) << 30),
+              mma_mxf8_2sm(tmem_base, ad + 2 * j, bd + 2 * j, idesc,
+                           sfa_t | (static_cast<uint32_t>(j) << 30),
                            sfb_t | (static_cast<uint32_t>(j) << 30), acc_flag);
             } else {
-              mma_nvf4_2sm(tmem_base, adesc, bdesc, C::IDESC_BASE, sfa_t + j * 4, sfb_t + j * 8,
-                           acc_flag);
+              mma_nvf4_2sm(tmem_base, ad + 2 * j, bd + 2 * j, C::IDESC_BASE, sfa_t + j * 4,
+                           sfb_t + j * 8, acc_flag);
             }
+          };
+          if (MODE == HQ_MXFP8 || atoms == C::ATOMS) {
+#pragma unroll
+            for (int j = 0; j < kFullMma; ++j) issue(j, j > 0 ? 1u : acc0);
+          } else {
+            for (int j = 0; j < atoms; ++j) issue(j, j > 0 ? 1u : acc0);
           }
           tc_commit_2sm_mc(empty_bar(stage), 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -661,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit_2sm_mc(drain_bar, 0x1);
       wait_drain(drain_bar, 0, p.wait_limit_ns);
     }
-  } else if (warp >= 6) {
+  } else if (warp >= kSfWarp0) {
     // ------------------------------------------------------------ scale staging (both CTAs)
     const int q = warp & 3;
     const uint32_t lq = static_cast<uint32_t>(q * 32) << 16;
@@ -706,6 +792,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
+        if (leader) {
+          // the pair's A / B tiles of this stage landed (counted on this CTA's
+          // full barrier) before the MMA issuer is released
+          const bool wf = wait_bounded(full_bar(stage), phase, wctx);
+          ok = __all_sync(0xFFFFFFFFu, wf);
+          if (!ok) break;
+        }
         if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(ready_bar(stage), 0));
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
@@ -713,78 +806,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int q = warp & 3;
-    const uint32_t stage_out_s = sbase + C::OFF_STAGE_OUT + (warp - 2) * 2048;
+    const int ew = warp - 2;
+    const uint32_t tempty_leader = mapa_shared(tempty_bar, 0);
     uint32_t acc_phase = 0;
     for (int64_t t = cluster_id; t < total; t += num_clusters) {
       int64_t row0;
       int n0;
       tile_rows(t, row0, n0);
+      const float alpha = p.alpha ? __ldg(p.alpha) : 1.0f;  // loaded before the wait
       const bool okw = wait_bounded(tfull_bar, acc_phase, wctx);
       if (!__all_sync(0xFFFFFFFFu, okw)) break;
       tc_fence_after();
-      const float alpha = p.alpha ? __ldg(p.alpha) : 1.0f;
       const int64_t rem = p.gs.a_rows - row0 - q * 32;
-      const int rows_here = rem < 0 ? 0 : (rem > 32 ? 32 : static_cast<int>(rem));
-      for (int c = 0; c < C::BN / 32; ++c) {
-        const int col0 = n0 + c * 32;
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + c * 32, r);
-        tmem_ld_wait();
-        if (col0 >= p.n) continue;
-        float bias_v[32];
-        if (p.bias) {
-          const uint4* bp = reinterpret_cast<const uint4*>(p.bias + col0);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint4 v = __ldg(bp + i);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              bias_v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
-              bias_v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) bias_v[i] = 0.0f;
-        }
-        uint32_t packed[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float v0 = __fadd_rn(__fmul_rn(alpha, __uint_as_float(r[2 * i])), bias_v[2 * i]);
-          const float v1 = __fadd_rn(__fmul_rn(alpha, __uint_as_float(r[2 * i + 1])), bias_v[2 * i + 1]);
-          __nv_bfloat162 b2 = __floats2bfloat162_rn(v0, v1);
-          packed[i] = *reinterpret_cast<uint32_t*>(&b2);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t off = lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage_out_s + off),
-                       "r"(packed[4 * j]), "r"(packed[4 * j + 1]), "r"(packed[4 * j + 2]),
-                       "r"(packed[4 * j + 3])
-                       : "memory");
-        }
-        __syncwarp();
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-          const int rr = it * 8 + (lane >> 2);
-          const int j = lane & 3;
-          const uint32_t off = rr * 64 + ((j ^ ((rr >> 1) & 3)) * 16);
-          uint4 v;
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                       : "r"(stage_out_s + off)
-                       : "memory");
-          if (rr < rows_here) {
-            uint16_t* dst = p.out + (row0 + q * 32 + rr) * p.n + col0 + j * 8;
-            *reinterpret_cast<uint4*>(dst) = v;
-          }
-        }
-        __syncwarp();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(tempty_bar, 0));
+      EpiArgs e;
+      e.acc_t = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      e.cw = (ew >> 2) * (C::BN / 2);
+      e.n0 = n0;
+      e.n = p.n;
+      e.alpha = alpha;
+      e.bias = p.bias;
+      e.out = p.out + (row0 + q * 32) * p.n;
+      e.rows_here = rem < 0 ? 0 : (rem > 32 ? 32 : static_cast<int>(rem));
+      e.stage_s = sbase + C::OFF_STAGE_OUT + ew * 1024;
+      e.lane = lane;
+      epilogue_tile<C::BN, true>(e, [&] { if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader); });
       acc_phase ^= 1u;
     }
   }

@@ -132,10 +132,11 @@ int hq_selftest_wait_expiry(uint64_t limit_ns, hq_stream_t s);
  * calls. */
 int hq_set_gemm_tile_n(int tile_n);
 
-/* Tuning knob: 1 lets dense block-scaled GEMMs whose n is a multiple of 256
- * run on pairs of SMs (a two-CTA cluster computing 256 x 256 tiles with
- * cta_group::2 MMAs); 0 (default, currently the faster choice on GB300) keeps
- * every GEMM on single-SM tiles.  Applies to later calls. */
+/* Tuning knob: 1 (default, the faster choice on GB300) runs dense
+ * block-scaled GEMMs whose n is a multiple of 256 on pairs of SMs (a two-CTA
+ * cluster computing 256 x 256 tiles with cta_group::2 MMAs, which halves the
+ * B bytes each SM loads); 0 keeps every GEMM on single-SM tiles.  Applies to
+ * later calls. */
 int hq_set_gemm_2sm(int enable);
 
 /* ------------------------------------------------------------------------- *

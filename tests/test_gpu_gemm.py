@@ -28,7 +28,7 @@ pytestmark = pytest.mark.gpu
 def _reset_knobs():
     yield
     hq.set_gemm_tile_n(0)
-    hq.set_gemm_2sm(0)
+    hq.set_gemm_2sm(1)
 
 
 def dense_case(m, n, k, mode, tile_n=0, alpha=None, bias=False, seed=0, g_a=None, g_b=None):
@@ -77,13 +77,15 @@ def test_dense_nvfp4_forced_256_partial_n_tile(cuda_dev):
     dense_case(200, 384, 512, "nvfp4", 256, alpha=2.0, seed=11)
 
 
+@pytest.mark.parametrize("two_sm", [1, 0])
 @pytest.mark.parametrize("mode", ["mxfp8", "nvfp4"])
 @pytest.mark.parametrize("m,n,k", [(256, 256, 256), (300, 512, 1024), (129, 768, 640), (640, 256, 320)])
-def test_dense_two_sm_tiles(cuda_dev, mode, m, n, k):
-    """The 2-SM (cluster pair, cta_group::2) kernel: 256 x 256 tiles, ragged M and K."""
+def test_dense_256_column_tiles(cuda_dev, mode, m, n, k, two_sm):
+    """n % 256 == 0: the 2-SM kernel (cluster pair, cta_group::2, 256 x 256
+    tiles) and the single-SM 128 x 256 kernel, ragged M and K."""
     if mode == "mxfp8" and k % 128:
         pytest.skip("MXFP8 needs k % 128 == 0")
-    hq.set_gemm_2sm(1)
+    hq.set_gemm_2sm(two_sm)
     dense_case(m, n, k, mode, 0, alpha=0.5 if mode == "nvfp4" else 1.25,
                bias=(mode == "mxfp8"), seed=m + k + (7 if mode == "nvfp4" else 0),
                g_a=2.0 if mode == "nvfp4" else None, g_b=64.0 if mode == "nvfp4" else None)
