@@ -2,8 +2,8 @@
 
 Sources (page titles and sections):
   * HALOps "GEMM" API, ``group_wise_quant``: BF16 [m, k] -> quantised data and
-    one scale per group along k (32 elements for w8a8-mxfp8, 16 for
-    w4a4-nvfp4); scales are [ceil(m/128)*128, k/group_size] uint8, either in the
+    one scale per group along k (32 elements for w8a8-mxfp8 and w4a4-mxfp4, 16
+    for w4a4-nvfp4); scales are [ceil(m/128)*128, k/group_size] uint8, either in the
     "CUTLASS SfAtom 128x4" interleaved layout (use_swizzle=True) or plain
     row-major (use_swizzle=False).
   * cuDNN frontend "Grouped GEMM + dGLU (SM100)", Step 3 (optional output
@@ -23,6 +23,11 @@ design notes):
   R3  UE4M3 (NVFP4): byte = E4M3(s) (RNE, satfinite); sd = its value;
       r = fp32(g / sd) once per group (0 when sd == 0); elements are
       E2M1(fp32(x * r)).
+  R6  UE8M0 with E2M1 elements (MXFP4): R1 with g = 1 (the page gives MXFP4
+      no global scale and no alpha) and rcp_max = fp32(1/6); the byte is
+      R2's power-of-two round-up, byte = clamp(ceil(log2 s) + 127, 0, 254);
+      elements are E2M1(x * 2^(127 - byte)) (an exact product), packed two
+      per byte as NVFP4's.
   R4  SfAtom byte offset of scale (row r, scale column s), S columns:
         ((r // 128) * (S // 4) + s // 4) * 512
         + (r % 32) * 16 + ((r % 128) // 32) * 4 + (s % 4)
@@ -38,8 +43,9 @@ from . import formats
 
 MODE_MXFP8 = "mxfp8"
 MODE_NVFP4 = "nvfp4"
+MODE_MXFP4 = "mxfp4"
 
-GROUP_SIZE = {MODE_MXFP8: 32, MODE_NVFP4: 16}
+GROUP_SIZE = {MODE_MXFP8: 32, MODE_NVFP4: 16, MODE_MXFP4: 32}
 
 RCP_E4M3_MAX = np.float32(1.0) / np.float32(448.0)
 RCP_E2M1_MAX = np.float32(1.0) / np.float32(6.0)
@@ -50,14 +56,24 @@ RCP_E2M1_MAX = np.float32(1.0) / np.float32(6.0)
 # --------------------------------------------------------------------------- #
 
 
-def scale_byte_mxfp8(amax, g=np.float32(1.0)):
-    """UE8M0 scale byte for groups with absolute maximum ``amax`` (R1, R2)."""
+def _ue8m0_round_up(amax, rcp_max, g=np.float32(1.0)):
+    """UE8M0 byte of s = fp32(fp32(g * amax) * rcp_max) rounded up to 2^e (R2)."""
     amax = np.asarray(amax, dtype=np.float32)
-    s = (np.float32(g) * amax) * RCP_E4M3_MAX           # float32 ops
+    s = (np.float32(g) * amax) * rcp_max                # float32 ops
     f, e = np.frexp(s.astype(np.float64))               # s = f * 2^e exactly
     clog2 = np.where(f == 0.5, e - 1, e)                # ceil(log2 s), s > 0
     byte = np.clip(clog2 + 127, 0, 254)
     return np.where(s == 0, 0, byte).astype(np.uint8)
+
+
+def scale_byte_mxfp8(amax, g=np.float32(1.0)):
+    """UE8M0 scale byte for groups with absolute maximum ``amax`` (R1, R2)."""
+    return _ue8m0_round_up(amax, RCP_E4M3_MAX, g)
+
+
+def scale_byte_mxfp4(amax):
+    """UE8M0 scale byte for E2M1 elements (R6)."""
+    return _ue8m0_round_up(amax, RCP_E2M1_MAX)
 
 
 def scale_byte_nvfp4(amax, g=np.float32(1.0)):
@@ -80,7 +96,7 @@ def quantize(x, mode, global_scale=None):
     """Quantise rows of ``x`` ([m, k], values exactly representable in BF16).
 
     Returns (q, sf_plain):
-      q        MXFP8: [m, k] uint8 E4M3 codes; NVFP4: [m, k/2] packed E2M1
+      q        MXFP8: [m, k] uint8 E4M3 codes; NVFP4 / MXFP4: [m, k/2] packed E2M1
       sf_plain [m, k/gs] uint8 scale bytes in natural (row, group) order
     """
     x = np.asarray(x, dtype=np.float32)
@@ -98,6 +114,14 @@ def quantize(x, mode, global_scale=None):
         y = xg.astype(np.float64) * mult[..., None]       # exact power-of-two scaling
         q = formats.encode_e4m3(y).reshape(m, k)
         return q, sf
+    if mode == MODE_MXFP4:
+        if global_scale is not None:
+            raise ValueError("MXFP4 uses no global scale")
+        sf = scale_byte_mxfp4(amax)
+        mult = np.ldexp(1.0, 127 - sf.astype(np.int64))  # 2^(127 - byte)
+        y = xg.astype(np.float64) * mult[..., None]       # exact power-of-two scaling
+        codes = formats.encode_e2m1(y).reshape(m, k)
+        return formats.pack_e2m1(codes), sf
     if mode == MODE_NVFP4:
         g = np.float32(1.0) if global_scale is None else np.float32(global_scale)
         sf, r = scale_byte_nvfp4(amax, g)
@@ -116,6 +140,9 @@ def dequantize(q, sf_plain, mode):
     elif mode == MODE_NVFP4:
         vals = formats.decode_e2m1(formats.unpack_e2m1(q))
         scl = formats.decode_ue4m3(sf_plain)
+    elif mode == MODE_MXFP4:
+        vals = formats.decode_e2m1(formats.unpack_e2m1(q))
+        scl = formats.decode_ue8m0(sf_plain)
     else:
         raise ValueError(mode)
     m, k = vals.shape

@@ -83,6 +83,30 @@ def test_dense_nvfp4_exact_brute_force():
     assert np.allclose(ref, exact_gemm(ad, bd, 1 / 3), rtol=1e-13)
 
 
+def torch_deq_mxfp4(qp, sf):
+    """Independent MXFP4 dequantisation: magnitude table for the nibbles,
+    PyTorch's float8_e8m0fnu decoder for the scales."""
+    lo = qp & 0xF
+    hi = qp >> 4
+    codes = np.stack([lo, hi], axis=-1).reshape(qp.shape[0], -1)
+    mag = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])[codes & 7]
+    v = np.where(codes & 8, -mag, mag)
+    s = torch.from_numpy(sf.copy()).view(torch.float8_e8m0fnu).double().numpy()
+    m, k = v.shape
+    return (v.reshape(m, k // 32, 32) * s[..., None]).reshape(m, k)
+
+
+def test_dense_mxfp4_exact_brute_force():
+    a = rand_bf16((3, 128), 25)
+    b = rand_bf16((5, 128), 26, 0.03)
+    qa, sa = quant.quantize(a, "mxfp4")
+    qb, sb = quant.quantize(b, "mxfp4")
+    ad, bd = torch_deq_mxfp4(qa, sa), torch_deq_mxfp4(qb, sb)
+    ref, _ = gemm.dense(quant.dequantize(qa, sa, "mxfp4"), quant.dequantize(qb, sb, "mxfp4"))
+    assert ref.shape == (3, 5)
+    assert np.allclose(ref, exact_gemm(ad, bd), rtol=1e-13, atol=1e-300)
+
+
 def test_closed_form_all_ones():
     K = 256
     q = np.full((2, K), 0x38, np.uint8)            # E4M3 1.0
@@ -151,7 +175,7 @@ def test_bound_check_rejects_a_wrong_result():
 def test_formats_used_by_gemm_decode_consistently():
     # the oracle's dequantisation equals the torch-decoder dequantisation
     a = rand_bf16((8, 128), 70)
-    for mode, deq in (("mxfp8", torch_deq_mxfp8), ("nvfp4", torch_deq_nvfp4)):
+    for mode, deq in (("mxfp8", torch_deq_mxfp8), ("nvfp4", torch_deq_nvfp4), ("mxfp4", torch_deq_mxfp4)):
         q, sf = quant.quantize(a, mode)
         assert np.array_equal(quant.dequantize(q, sf, mode), deq(q, sf))
     assert formats.decode_e4m3(0x38) == 1.0

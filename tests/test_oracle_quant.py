@@ -24,7 +24,7 @@ def group(vals, gs):
 # ----------------------------------------------------------------------------
 
 
-@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4", "mxfp4"])
 def test_all_zero_group(mode):
     gs = quant.GROUP_SIZE[mode]
     q, sf = quant.quantize(np.zeros((2, 4 * gs), np.float32), mode)
@@ -90,6 +90,51 @@ def test_nvfp4_global_scale_multiplies_scale():
     assert c[0] == 7 and c[1] == 4             # 6 and 2
 
 
+def test_mxfp4_amax_6_gives_unit_scale():
+    # 6 * fp32(1/6) rounds to exactly 1.0 in float32 -> byte 127 (2^0)
+    assert np.float32(6.0) * (np.float32(1.0) / np.float32(6.0)) == np.float32(1.0)
+    q, sf = quant.quantize(group([6.0, -3.0, 0.5, 0.25, 1.25, -1.75], 32), "mxfp4")
+    assert sf[0, 0] == 127
+    codes = formats.unpack_e2m1(q)[0]
+    # 6, -3, 0.5, 0.25 (tie -> 0), 1.25 (tie 1 / 1.5 -> even code 2 = 1.0),
+    # -1.75 (tie 1.5 / 2 -> even code 4 = 2, negative)
+    assert codes[:6].tolist() == [7, 13, 1, 0, 2, 12]
+
+
+def test_mxfp4_amax_1():
+    # s = fp32(1/6) ~ 2^-2.585 -> ceil(log2 s) = -2 -> byte 125, scale 1/4
+    q, sf = quant.quantize(group([1.0, 0.5, -0.25, 0.3], 32), "mxfp4")
+    assert sf[0, 0] == 125
+    codes = formats.unpack_e2m1(q)[0]
+    assert codes[:4].tolist() == [6, 4, 10, 2]  # 4, 2, -1, 1.2 -> 1
+
+
+def test_mxfp4_power_of_two_boundary():
+    # amax = 6 * 2^k gives s = 2^k exactly -> byte 127 + k; a hair above rounds up
+    for k in (-20, -3, 0, 5, 30):
+        amax = np.float32(6.0 * 2.0 ** k)
+        _, sf = quant.quantize(group([amax], 32), "mxfp4")
+        assert sf[0, 0] == 127 + k
+        _, sf = quant.quantize(group([np.nextafter(amax, np.float32(np.inf))], 32), "mxfp4")
+        assert sf[0, 0] == 128 + k
+
+
+def test_mxfp4_grid_values_round_trip_exactly():
+    # every E2M1 magnitude times a power-of-two scale decodes back to itself,
+    # with the group's largest element 6 * 2^k pinning the scale byte to 127 + k
+    mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float32)
+    for k in (-6, 0, 9):
+        vals = np.concatenate([mags, -mags[1:], np.zeros(17, np.float32)]) * np.float32(2.0 ** k)
+        q, sf = quant.quantize(vals[None, :32], "mxfp4")
+        assert sf[0, 0] == 127 + k
+        assert np.array_equal(quant.dequantize(q, sf, "mxfp4")[0], vals[:32].astype(np.float64))
+
+
+def test_mxfp4_rejects_global_scale():
+    with pytest.raises(ValueError):
+        quant.quantize(np.ones((1, 32), np.float32), "mxfp4", global_scale=2.0)
+
+
 # ----------------------------------------------------------------------------
 # library cross-check and round-trip bounds
 # ----------------------------------------------------------------------------
@@ -108,14 +153,14 @@ def test_mxfp8_elements_match_torch_cast():
     assert np.array_equal(ref, q)
 
 
-@pytest.mark.parametrize("mode,rel", [("mxfp8", 2.0 ** -4), ("nvfp4", 2.0 ** -2)])
+@pytest.mark.parametrize("mode,rel", [("mxfp8", 2.0 ** -4), ("nvfp4", 2.0 ** -2), ("mxfp4", 2.0 ** -2)])
 def test_round_trip_error_bound(mode, rel):
     rng = np.random.default_rng(2)
     x = torch.from_numpy(rng.standard_normal((32, 512)).astype(np.float32)).to(torch.bfloat16).float().numpy()
     q, sf = quant.quantize(x, mode)
     d = quant.dequantize(q, sf, mode)
     gs = quant.GROUP_SIZE[mode]
-    scale = np.repeat((formats.decode_ue8m0(sf) if mode == "mxfp8" else formats.decode_ue4m3(sf)), gs, axis=1)
+    scale = np.repeat((formats.decode_ue4m3(sf) if mode == "nvfp4" else formats.decode_ue8m0(sf)), gs, axis=1)
     # element relative rounding plus one subnormal step of the element grid
     sub = 2.0 ** -9 if mode == "mxfp8" else 0.5
     assert np.all(np.abs(d - x) <= rel * np.abs(x) + scale * sub / 2 * 1.0000001 + 1e-30)
