@@ -1,4 +1,4 @@
-"""Block-scaled low-precision (MXFP8 / NVFP4) grouped GEMM for MoE on GB300.
+"""Block-scaled low-precision (MXFP8 / MXFP4 / NVFP4) grouped GEMM for MoE on GB300.
 
 A thin Python binding over libhq.so's C ABI (include/hq.h).  Every function
 here only marshals arguments -- device pointers, sizes and the current CUDA
@@ -13,7 +13,7 @@ import ctypes
 import torch
 
 from . import _abi
-from ._abi import (HQ_MXFP8, HQ_NVFP4, HQ_STATUS_WAIT_TIMEOUT, HQ_STATUS_MASK_CLAMPED,  # noqa: F401
+from ._abi import (HQ_MXFP8, HQ_MXFP4, HQ_NVFP4, HQ_STATUS_WAIT_TIMEOUT, HQ_STATUS_MASK_CLAMPED,  # noqa: F401
                    HQ_STATUS_BAD_OFFSETS, HQ_STATUS_TOKENS_CLAMPED)
 
 __all__ = [
@@ -23,8 +23,9 @@ __all__ = [
     "hq_gemm_dswiglu", "hq_gemm_dswiglu_workspace_size", "hq_gemm_dgeglu", "swiglu_kb_dim",
 ]
 
-_MODES = {"mxfp8": HQ_MXFP8, "w8a8-mxfp8": HQ_MXFP8, "nvfp4": HQ_NVFP4, "w4a4-nvfp4": HQ_NVFP4,
-          HQ_MXFP8: HQ_MXFP8, HQ_NVFP4: HQ_NVFP4}
+_MODES = {"mxfp8": HQ_MXFP8, "w8a8-mxfp8": HQ_MXFP8, "mxfp4": HQ_MXFP4, "w4a4-mxfp4": HQ_MXFP4,
+          "nvfp4": HQ_NVFP4, "w4a4-nvfp4": HQ_NVFP4, HQ_MXFP8: HQ_MXFP8, HQ_MXFP4: HQ_MXFP4,
+          HQ_NVFP4: HQ_NVFP4}
 
 
 class HQError(RuntimeError):
@@ -47,7 +48,7 @@ def mode_id(mode):
 
 
 def group_size(mode):
-    return 32 if mode_id(mode) == HQ_MXFP8 else 16
+    return 16 if mode_id(mode) == HQ_NVFP4 else 32
 
 
 def _ptr(t):

@@ -17,6 +17,7 @@ c_sz = ctypes.c_size_t
 c_p = ctypes.c_void_p
 
 HQ_MXFP8 = 0
+HQ_MXFP4 = 1
 HQ_NVFP4 = 2
 
 HQ_OK = 0
@@ -35,7 +36,7 @@ class Capabilities(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int) for name in (
         "abi_version", "sfatom_rows", "sfatom_cols", "sfatom_bytes", "group_mxfp8",
         "group_nvfp4", "contig_row_align", "tile_m", "ptr_align_bytes", "max_groups",
-        "glu_block")]
+        "glu_block", "group_mxfp4")]
 
 
 # name -> (restype, argtypes)

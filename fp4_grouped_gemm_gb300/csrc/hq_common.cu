@@ -118,7 +118,7 @@ extern "C" {
 
 int hq_capabilities(hq_capabilities_t* out) {
   if (!out) return HQ_ERR_INVALID;
-  out->abi_version = 1;
+  out->abi_version = 2;
   out->sfatom_rows = 128;
   out->sfatom_cols = 4;
   out->sfatom_bytes = 512;
@@ -129,6 +129,7 @@ int hq_capabilities(hq_capabilities_t* out) {
   out->ptr_align_bytes = 16;
   out->max_groups = 1024;
   out->glu_block = 32;
+  out->group_mxfp4 = 32;
   return HQ_OK;
 }
 
@@ -144,7 +145,7 @@ const char* hq_status_string(int status) {
 }
 
 size_t hq_sf_bytes(int64_t rows, int64_t k, hq_mode mode) {
-  int64_t gs = mode == HQ_MXFP8 ? 32 : (mode == HQ_NVFP4 ? 16 : 0);
+  int64_t gs = (mode == HQ_MXFP8 || mode == HQ_MXFP4) ? 32 : (mode == HQ_NVFP4 ? 16 : 0);
   if (gs == 0 || rows < 0 || k <= 0 || k % (4 * gs) != 0) return 0;
   return static_cast<size_t>((rows + 127) / 128 * 128) * static_cast<size_t>(k / gs);
 }

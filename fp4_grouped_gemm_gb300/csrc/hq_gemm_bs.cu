@@ -61,7 +61,7 @@ struct GemmParams {
 // needs none and spends the shared memory on a deeper pipeline instead).
 template <int MODE, int BN, int STAGES, int ACC, int TABLE>
 struct Cfg {
-  static constexpr int GS = MODE == HQ_MXFP8 ? 32 : 16;
+  static constexpr int GS = MODE == HQ_NVFP4 ? 16 : 32;
   static constexpr int EPB = MODE == HQ_MXFP8 ? 1 : 2;            // elements per byte
   static constexpr int BK = kBKBytes * EPB;                       // elements per stage
   static constexpr int ATOMS = BK / GS / 4;                       // k-atoms per stage
@@ -94,7 +94,8 @@ struct Cfg {
   // instruction descriptor (block-scaled kinds): A/B K-major, M=128, N=BN
   static constexpr uint32_t IDESC_BASE =
       (MODE == HQ_MXFP8 ? ((0u << 7) | (0u << 10) | (1u << 23))   // E4M3 x E4M3, UE8M0
-                        : ((1u << 7) | (1u << 10) | (0u << 23)))  // E2M1 x E2M1, UE4M3
+       : MODE == HQ_MXFP4 ? ((1u << 7) | (1u << 10) | (1u << 23))  // E2M1 x E2M1, UE8M0
+                          : ((1u << 7) | (1u << 10) | (0u << 23)))  // E2M1 x E2M1, UE4M3
       | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
 };
 
@@ -333,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // whole k-block's MMAs are issued unrolled.
       const uint64_t adesc0 = smem_desc_sw128(sbase + C::OFF_A);
       const uint64_t bdesc0 = smem_desc_sw128(sbase + C::OFF_B);
-      constexpr int kFullMma = MODE == HQ_MXFP8 ? kBKBytes / kMmaKBytes : C::ATOMS;
+      constexpr int kFullMma = MODE == HQ_NVFP4 ? C::ATOMS : kBKBytes / kMmaKBytes;
       for (int64_t t = blockIdx.x; ok && t < sch.total_tiles; t += gridDim.x) {
         const TileInfo ti = decode_tile(p.gs, sch, t, BN);
         int rb_valid = static_cast<int>((p.n - ti.n0 + 127) / 128);
@@ -374,6 +375,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_mxf8(d_tmem, ad + 2 * j, bd + 2 * j, idesc,
                        sfa_t | (static_cast<uint32_t>(j) << 30),
                        sfb_t | (static_cast<uint32_t>(j) << 30), acc_flag);
+            } else if (MODE == HQ_MXFP4) {
+              // two scales per row per MMA: bytes 2 (j % 2), +1 of atom j / 2
+              const uint32_t sf = static_cast<uint32_t>(j & 1) * 2u;
+              const uint32_t idesc = C::IDESC_BASE | (sf << 4) | (sf << 29);
+              mma_mxf4(d_tmem, ad + 2 * j, bd + 2 * j, idesc, (sfa_t + (j >> 1) * 4) | (sf << 30),
+                       (sfb_t + (j >> 1) * C::RB * 4) | (sf << 30), acc_flag);
             } else {
               // four scales per row per MMA: one whole atom column group
               mma_nvf4(d_tmem, ad + 2 * j, bd + 2 * j, C::IDESC_BASE, sfa_t + j * 4,
@@ -384,7 +391,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < kFullMma; ++j) issue(j, j > 0 ? 1u : acc0);
           } else {
-            for (int j = 0; j < atoms; ++j) issue(j, j > 0 ? 1u : acc0);
+            // a partial last k-block: one MMA per atom (NVFP4), two (MXFP4)
+            const int n_mma = MODE == HQ_MXFP4 ? 2 * atoms : atoms;
+            for (int j = 0; j < n_mma; ++j) issue(j, j > 0 ? 1u : acc0);
           }
           tc_commit(empty_bar(stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -543,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 template <int MODE, int STAGES>
 struct Cfg2 {
-  static constexpr int GS = MODE == HQ_MXFP8 ? 32 : 16;
+  static constexpr int GS = MODE == HQ_NVFP4 ? 16 : 32;
   static constexpr int EPB = MODE == HQ_MXFP8 ? 1 : 2;
   static constexpr int BK = kBKBytes * EPB;
   static constexpr int ATOMS = BK / GS / 4;
@@ -572,7 +581,8 @@ struct Cfg2 {
   // M = 256 across the pair, N = 256
   static constexpr uint32_t IDESC_BASE =
       (MODE == HQ_MXFP8 ? ((0u << 7) | (0u << 10) | (1u << 23))
-                        : ((1u << 7) | (1u << 10) | (0u << 23)))
+       : MODE == HQ_MXFP4 ? ((1u << 7) | (1u << 10) | (1u << 23))
+                          : ((1u << 7) | (1u << 10) | (0u << 23)))
       | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(256 >> 4) << 24);
 };
 
@@ -703,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // MMAs, one wait per stage
       const uint64_t adesc0 = smem_desc_sw128(sbase + C::OFF_A);
       const uint64_t bdesc0 = smem_desc_sw128(sbase + C::OFF_B);
-      constexpr int kFullMma = MODE == HQ_MXFP8 ? kBKBytes / kMmaKBytes : C::ATOMS;
+      constexpr int kFullMma = MODE == HQ_NVFP4 ? C::ATOMS : kBKBytes / kMmaKBytes;
       for (int64_t t = cluster_id; ok && t < total; t += num_clusters) {
         if (!wait_bounded(tempty_bar, acc_phase ^ 1u, wctx)) break;
         tc_fence_after();
@@ -726,6 +736,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_mxf8_2sm(tmem_base, ad + 2 * j, bd + 2 * j, idesc,
                            sfa_t | (static_cast<uint32_t>(j) << 30),
                            sfb_t | (static_cast<uint32_t>(j) << 30), acc_flag);
+            } else if (MODE == HQ_MXFP4) {
+              const uint32_t sf = static_cast<uint32_t>(j & 1) * 2u;
+              const uint32_t idesc = C::IDESC_BASE | (sf << 4) | (sf << 29);
+              mma_mxf4_2sm(tmem_base, ad + 2 * j, bd + 2 * j, idesc,
+                           (sfa_t + (j >> 1) * 4) | (sf << 30), (sfb_t + (j >> 1) * 8) | (sf << 30),
+                           acc_flag);
             } else {
               mma_nvf4_2sm(tmem_base, ad + 2 * j, bd + 2 * j, C::IDESC_BASE, sfa_t + j * 4,
                            sfb_t + j * 8, acc_flag);
@@ -735,7 +751,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int j = 0; j < kFullMma; ++j) issue(j, j > 0 ? 1u : acc0);
           } else {
-            for (int j = 0; j < atoms; ++j) issue(j, j > 0 ? 1u : acc0);
+            const int n_mma = MODE == HQ_MXFP4 ? 2 * atoms : atoms;
+            for (int j = 0; j < n_mma; ++j) issue(j, j > 0 ? 1u : acc0);
           }
           tc_commit_2sm_mc(empty_bar(stage), 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -948,8 +965,9 @@ int run_gemm(hq_mode mode, const void* a, const void* b, const GemmParams& p, in
   // dense problems with whole 256-column tiles use the 2-SM kernel unless a
   // single-SM tile width is forced
   if (bn == 0 && p.gs.sched == kDense && p.n % 256 == 0 && use_2sm()) {
-    return mode == HQ_MXFP8 ? run_bs_2sm<HQ_MXFP8, 6>(a, b, p, sm_count, pdl, st)
-                            : run_bs_2sm<HQ_NVFP4, 5>(a, b, p, sm_count, pdl, st);
+    if (mode == HQ_MXFP8) return run_bs_2sm<HQ_MXFP8, 6>(a, b, p, sm_count, pdl, st);
+    if (mode == HQ_MXFP4) return run_bs_2sm<HQ_MXFP4, 5>(a, b, p, sm_count, pdl, st);
+    return run_bs_2sm<HQ_NVFP4, 5>(a, b, p, sm_count, pdl, st);
   }
   if (bn == 0) bn = (p.n % 256 == 0) ? 256 : 128;
   if (bn == 256 && p.n % 256 != 0 && p.n < 256) bn = 128;
@@ -961,6 +979,12 @@ int run_gemm(hq_mode mode, const void* a, const void* b, const GemmParams& p, in
     return dense ? run_bs<HQ_MXFP8, 128, 6, 2, 0>(a, b, p, sm_count, pdl, st)
                  : run_bs<HQ_MXFP8, 128, 6, 2, T>(a, b, p, sm_count, pdl, st);
   }
+  if (mode == HQ_MXFP4) {
+    if (bn == 256) return dense ? run_bs<HQ_MXFP4, 256, 4, 1, 0>(a, b, p, sm_count, pdl, st)
+                                : run_bs<HQ_MXFP4, 256, 3, 1, T>(a, b, p, sm_count, pdl, st);
+    return dense ? run_bs<HQ_MXFP4, 128, 5, 2, 0>(a, b, p, sm_count, pdl, st)
+                 : run_bs<HQ_MXFP4, 128, 5, 2, T>(a, b, p, sm_count, pdl, st);
+  }
   if (bn == 256) return dense ? run_bs<HQ_NVFP4, 256, 4, 1, 0>(a, b, p, sm_count, pdl, st)
                               : run_bs<HQ_NVFP4, 256, 3, 1, T>(a, b, p, sm_count, pdl, st);
   return dense ? run_bs<HQ_NVFP4, 128, 5, 2, 0>(a, b, p, sm_count, pdl, st)
@@ -971,8 +995,8 @@ int run_gemm(hq_mode mode, const void* a, const void* b, const GemmParams& p, in
 int check_common(const void* a, const uint8_t* sfa, const void* b, const uint8_t* sfb,
                  const float* alpha, const hq_bf16* bias, const hq_bf16* out, int64_t n, int64_t k,
                  hq_mode mode) {
-  if (mode != HQ_MXFP8 && mode != HQ_NVFP4) return HQ_ERR_INVALID;
-  const int64_t gs = mode == HQ_MXFP8 ? 32 : 16;
+  if (mode != HQ_MXFP8 && mode != HQ_MXFP4 && mode != HQ_NVFP4) return HQ_ERR_INVALID;
+  const int64_t gs = mode == HQ_NVFP4 ? 16 : 32;
   if (n <= 0 || k <= 0 || k % (4 * gs) != 0 || n % 128 != 0) return HQ_ERR_INVALID;
   if (n > (1ll << 30) || k > (1ll << 30)) return HQ_ERR_INVALID;
   if (!a || !sfa || !b || !sfb || !out) return HQ_ERR_INVALID;
@@ -980,15 +1004,18 @@ int check_common(const void* a, const uint8_t* sfa, const void* b, const uint8_t
     return HQ_ERR_INVALID;
   if (bias && !aligned16(bias)) return HQ_ERR_INVALID;
   if (alpha && (reinterpret_cast<uintptr_t>(alpha) & 3u)) return HQ_ERR_INVALID;
+  // HALOps "GEMM" API: alpha required for w4a4-nvfp4, not accepted for
+  // w4a4-mxfp4; bias only in w8a8-mxfp8 mode
   if (mode == HQ_NVFP4 && !alpha) return HQ_ERR_UNSUPPORTED;
-  if (mode == HQ_NVFP4 && bias) return HQ_ERR_UNSUPPORTED;
+  if (mode == HQ_MXFP4 && alpha) return HQ_ERR_UNSUPPORTED;
+  if (mode != HQ_MXFP8 && bias) return HQ_ERR_UNSUPPORTED;
   return HQ_OK;
 }
 
 GemmParams base_params(const uint8_t* sfa, const uint8_t* sfb, const float* alpha,
                        const hq_bf16* bias, hq_bf16* out, int64_t n, int64_t k, hq_mode mode) {
   GemmParams p{};
-  const int64_t gs = mode == HQ_MXFP8 ? 32 : 16;
+  const int64_t gs = mode == HQ_NVFP4 ? 16 : 32;
   p.sfa = sfa;
   p.sfb = sfb;
   p.alpha = alpha;

@@ -88,7 +88,8 @@ __device__ __forceinline__ float pow2_neg_unbiased(uint32_t byte) {  // 2^(127 -
 }
 
 // One lane quantises one whole scale group of GS values x[0..GS).
-// MXFP8 writes GS E4M3 bytes to q[0..GS) words; NVFP4 writes GS/2 packed bytes.
+// MXFP8 writes GS E4M3 bytes to qw[0..GS/4); NVFP4 and MXFP4 write GS/2 packed
+// bytes to qw[0..GS/8).
 template <int MODE, int GS>
 __device__ __forceinline__ uint32_t encode_group(const float (&x)[GS], float g,
                                                  const float* r_table, uint32_t (&qw)[GS / 4]) {
@@ -104,6 +105,22 @@ __device__ __forceinline__ uint32_t encode_group(const float (&x)[GS], float g,
       const uint32_t lo = cvt_e4m3x2(__fmul_rn(x[4 * i + 1], mult), __fmul_rn(x[4 * i], mult));
       const uint32_t hi = cvt_e4m3x2(__fmul_rn(x[4 * i + 3], mult), __fmul_rn(x[4 * i + 2], mult));
       qw[i] = lo | (hi << 16);
+    }
+    return byte;
+  } else if (MODE == HQ_MXFP4) {
+    // UE8M0 as for MXFP8, with the E2M1 range: s = amax * fp32(1/6), rounded up
+    // to a power of two; the products x * 2^(127 - byte) are exact
+    const float s = __fmul_rn(amax, 1.0f / 6.0f);
+    const uint32_t byte = ue8m0_ceil(s);
+    const float mult = pow2_neg_unbiased(byte);
+#pragma unroll
+    for (int i = 0; i < GS / 8; ++i) {
+      uint32_t w = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        w |= cvt_e2m1x2(__fmul_rn(x[8 * i + 2 * j + 1], mult), __fmul_rn(x[8 * i + 2 * j], mult))
+             << (8 * j);
+      qw[i] = w;
     }
     return byte;
   } else {
@@ -124,9 +141,9 @@ __device__ __forceinline__ uint32_t encode_group(const float (&x)[GS], float g,
 
 template <int MODE, bool SWIGLU>
 __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
-  constexpr int GS = MODE == HQ_MXFP8 ? 32 : 16;
+  constexpr int GS = MODE == HQ_NVFP4 ? 16 : 32;
   constexpr int NV = GS / 8;          // 16-byte loads per operand and group
-  constexpr int U = MODE == HQ_MXFP8 ? 1 : 2;  // groups a lane holds in flight
+  constexpr int U = MODE == HQ_NVFP4 ? 2 : 1;  // groups a lane holds in flight
   __shared__ float r_table[128];
   const float g = (MODE == HQ_NVFP4 && p.global_scale) ? __ldg(p.global_scale) : 1.0f;
   if (MODE == HQ_NVFP4) {
@@ -233,6 +250,8 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
         uint4* dst = reinterpret_cast<uint4*>(p.q + row * p.k + s * GS);
         dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
         dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+      } else if (MODE == HQ_MXFP4) {
+        *reinterpret_cast<uint4*>(p.q + (row * p.k + s * GS) / 2) = make_uint4(qw[0], qw[1], qw[2], qw[3]);
       } else {
         *reinterpret_cast<uint2*>(p.q + (row * p.k + s * GS) / 2) = make_uint2(qw[0], qw[1]);
       }
@@ -293,6 +312,7 @@ int launch_quant(const QuantParams& p, cudaStream_t st, bool pdl) {
 int dispatch(hq_mode mode, bool swiglu, const QuantParams& p, cudaStream_t st, bool pdl) {
   if (mode == HQ_MXFP8)
     return swiglu ? launch_quant<HQ_MXFP8, true>(p, st, pdl) : launch_quant<HQ_MXFP8, false>(p, st, pdl);
+  if (mode == HQ_MXFP4) return swiglu ? HQ_ERR_INVALID : launch_quant<HQ_MXFP4, false>(p, st, pdl);
   return swiglu ? launch_quant<HQ_NVFP4, true>(p, st, pdl) : launch_quant<HQ_NVFP4, false>(p, st, pdl);
 }
 
@@ -304,10 +324,10 @@ extern "C" {
 int hq_quant(const hq_bf16* x, int64_t m, int64_t k, hq_mode mode, int use_swizzle,
              const float* global_scale, void* q_out, uint8_t* sf_out, int use_pdl,
              hq_stream_t s) {
-  if (mode != HQ_MXFP8 && mode != HQ_NVFP4) return HQ_ERR_INVALID;
-  const int64_t gs = mode == HQ_MXFP8 ? 32 : 16;
+  if (mode != HQ_MXFP8 && mode != HQ_MXFP4 && mode != HQ_NVFP4) return HQ_ERR_INVALID;
+  const int64_t gs = mode == HQ_NVFP4 ? 16 : 32;
   if (m < 0 || k <= 0 || k % (4 * gs) != 0) return HQ_ERR_INVALID;
-  if (mode == HQ_MXFP8 && global_scale) return HQ_ERR_UNSUPPORTED;
+  if (mode != HQ_NVFP4 && global_scale) return HQ_ERR_UNSUPPORTED;
   if (m == 0) return HQ_OK;
   if (!x || !q_out || !sf_out) return HQ_ERR_INVALID;
   if (!hq::aligned16(x) || !hq::aligned16(q_out) || !hq::aligned16(sf_out)) return HQ_ERR_INVALID;

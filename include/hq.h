@@ -64,6 +64,7 @@ typedef uint16_t hq_bf16;
 /* Quantisation recipe ("mode" string of the HALOps API). */
 typedef enum {
   HQ_MXFP8 = 0, /* "w8a8-mxfp8": E4M3 elements, UE8M0 scale per 32          */
+  HQ_MXFP4 = 1, /* "w4a4-mxfp4": packed E2M1, UE8M0 scale per 32, no alpha  */
   HQ_NVFP4 = 2  /* "w4a4-nvfp4": packed E2M1, UE4M3 scale per 16, FP32 alpha */
 } hq_mode;
 
@@ -87,7 +88,7 @@ enum {
  * (FlashRT fp4-gemm notes: "Read capabilities() instead of duplicating
  * scale-factor layout or alignment constants"). */
 typedef struct {
-  int abi_version;       /* 1                                               */
+  int abi_version;       /* 2                                               */
   int sfatom_rows;       /* 128 rows per atom                               */
   int sfatom_cols;       /* 4 scale columns per atom                        */
   int sfatom_bytes;      /* 512                                             */
@@ -98,6 +99,7 @@ typedef struct {
   int ptr_align_bytes;   /* 16: every tensor base pointer                   */
   int max_groups;        /* 1024 experts at most                            */
   int glu_block;         /* 32: dGLU gate/input interleave width            */
+  int group_mxfp4;       /* 32                                              */
 } hq_capabilities_t;
 
 /* Fills *out.  Returns HQ_ERR_INVALID if out is NULL. */
@@ -147,19 +149,21 @@ int hq_set_gemm_2sm(int enable);
  * use_swizzle, plain row-major otherwise).  Scale rule (cuDNN "Grouped GEMM +
  * dGLU (SM100)", Step 3): SF = norm_const * amax(group) * rcp_max,
  * q = x * norm_const / SF, with norm_const = *global_scale (NVFP4; 1 when
- * NULL) or 1 (MXFP8), rcp_max = 1/448 (E4M3) or 1/6 (E2M1), evaluated in
- * IEEE float32 in that order.  MXFP8 rounds SF up to a power of two
- * (UE8M0 = clamp(ceil(log2 SF) + 127, 0, 254), 0 for an all-zero group) and
- * stores E4M3(x * 2^(127 - UE8M0)); NVFP4 stores UE4M3 = E4M3(SF) and
- * E2M1(x * (g / SF_decoded)).  Element encodes round to nearest even and
- * saturate.
+ * NULL) or 1 (MXFP8, MXFP4), rcp_max = 1/448 (E4M3) or 1/6 (E2M1), evaluated
+ * in IEEE float32 in that order.  MXFP8 and MXFP4 round SF up to a power of
+ * two (UE8M0 = clamp(ceil(log2 SF) + 127, 0, 254), 0 for an all-zero group)
+ * and store E4M3 or E2M1 of x * 2^(127 - UE8M0); NVFP4 stores
+ * UE4M3 = E4M3(SF) and E2M1(x * (g / SF_decoded)).  Element encodes round to
+ * nearest even and saturate; E2M1 codes are packed two per byte, the even
+ * element in the low nibble.
  *
  *   x            [m, k] BF16, 16-byte aligned
- *   mode         HQ_MXFP8 or HQ_NVFP4
+ *   mode         HQ_MXFP8, HQ_MXFP4 or HQ_NVFP4
  *   use_swizzle  1: SfAtom layout; 0: row-major [ceil(m/128)*128, k/group]
  *   global_scale NVFP4 only: device float [1] or NULL (=1); must be NULL for
- *                MXFP8 (HQ_ERR_UNSUPPORTED otherwise)
- *   q_out        MXFP8 [m, k] bytes; NVFP4 [m, k/2] bytes; 16-byte aligned
+ *                MXFP8 and MXFP4 (HQ_ERR_UNSUPPORTED otherwise)
+ *   q_out        MXFP8 [m, k] bytes; MXFP4 / NVFP4 [m, k/2] bytes; 16-byte
+ *                aligned
  *   sf_out       hq_sf_bytes(m, k, mode) bytes; padding rows written as 0
  *   use_pdl      1: launch with programmatic dependent launch
  * Requires k % (4 * group) == 0 (HQ_ERR_INVALID otherwise).  m == 0 is a
@@ -176,9 +180,10 @@ int hq_quant(const hq_bf16 *x, int64_t m, int64_t k, hq_mode mode, int use_swizz
  *   b, sfb   quantised B (one [n, k] matrix per group, stacked) and its
  *            SfAtom scales (per group ceil(n/128)*128*(k/group) bytes)
  *   alpha    device float per group, or NULL (= 1).  Required for HQ_NVFP4
- *            (HQ_ERR_UNSUPPORTED if NULL), optional for HQ_MXFP8
+ *            (HQ_ERR_UNSUPPORTED if NULL), optional for HQ_MXFP8, not
+ *            accepted for HQ_MXFP4 (HQ_ERR_UNSUPPORTED if given)
  *   bias     device BF16 [groups, n] or NULL.  HQ_MXFP8 only
- *            (HQ_ERR_UNSUPPORTED with HQ_NVFP4), as the HALOps API states
+ *            (HQ_ERR_UNSUPPORTED with the FP4 modes), as the HALOps API states
  *   sm_count number of persistent CTAs (<= 0: all SMs)
  * Shape rules: k % (4 * group) == 0; n % 128 == 0; all pointers 16-byte
  * aligned.  Each tile is 128 rows by 128 or 256 columns.

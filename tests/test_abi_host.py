@@ -36,9 +36,12 @@ def test_every_declared_function_is_exported_and_bound(lib):
 def test_capabilities_and_sizes(lib):
     caps = hq.capabilities()
     assert caps["sfatom_bytes"] == 512 and caps["group_mxfp8"] == 32 and caps["group_nvfp4"] == 16
+    assert caps["abi_version"] == 2 and caps["group_mxfp4"] == 32
     assert hq.sf_bytes(200, 256, "mxfp8") == 256 * 8
     assert hq.sf_bytes(128, 5120, "nvfp4") == 128 * 320
     assert hq.sf_bytes(10, 100, "mxfp8") == 0          # k not a multiple of 128
+    assert hq.sf_bytes(200, 256, "mxfp4") == 256 * 8   # one UE8M0 byte per 32
+    assert hq.sf_bytes(10, 192, "mxfp4") == 0          # k not a multiple of 128
     assert hq.hq_gemm_dswiglu_workspace_size(16, 1408) == 16 * 2816 * 4
     assert hq.swiglu_kb_dim(1536, "mxfp8") == 48 and hq.swiglu_kb_dim(640, "mxfp8") == 32
 
@@ -64,6 +67,9 @@ def test_quant_rejects_bad_arguments(lib):
         _abi.HQ_ERR_INVALID
     # a global scale is an NVFP4 feature
     assert lib.hq_quant(FAKE, 4, 128, 0, 1, FAKE, FAKE, FAKE, 0, None) == _abi.HQ_ERR_UNSUPPORTED
+    assert lib.hq_quant(FAKE, 4, 128, 1, 1, FAKE, FAKE, FAKE, 0, None) == _abi.HQ_ERR_UNSUPPORTED
+    # MXFP4 groups are 32 wide: k must be a multiple of 128
+    assert lib.hq_quant(FAKE, 4, 64, 1, 1, None, FAKE, FAKE, 0, None) == _abi.HQ_ERR_INVALID
     # m == 0 is a no-op
     assert lib.hq_quant(FAKE, 0, 128, 0, 1, None, FAKE, FAKE, 0, None) == _abi.HQ_OK
 
@@ -78,6 +84,10 @@ def test_gemm_rejects_bad_arguments(lib):
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 128, 256, 2, -1, 0, None) == _abi.HQ_ERR_UNSUPPORTED
     # k not a multiple of 4 * group
     assert f(FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 128, 128, 96, 0, -1, 0, None) == _abi.HQ_ERR_INVALID
+    # MXFP4 accepts neither alpha nor bias
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 128, 128, 256, 1, -1, 0, None) == _abi.HQ_ERR_UNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, 128, 128, 256, 1, -1, 0, None) == _abi.HQ_ERR_UNSUPPORTED
+    assert f(FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 128, 128, 192, 1, -1, 0, None) == _abi.HQ_ERR_INVALID
     g = lib.hq_gemm_grouped_masked
     # max_m not a multiple of 128
     assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 100, None, None, FAKE, 128, 128, 0, -1, None) == _abi.HQ_ERR_INVALID
@@ -93,6 +103,7 @@ def test_swiglu_and_dswiglu_reject_bad_arguments(lib):
     assert s(FAKE, 10, 100, None, 0, 0, 0, None, FAKE, FAKE, None) == _abi.HQ_ERR_INVALID   # H % 128
     assert s(FAKE, 10, 128, FAKE, 3, 4, 0, None, FAKE, FAKE, None) == _abi.HQ_ERR_INVALID   # E*rpe != rows
     assert s(FAKE, 10, 128, None, 0, 0, 0, FAKE, FAKE, FAKE, None) == _abi.HQ_ERR_UNSUPPORTED
+    assert s(FAKE, 10, 128, None, 0, 0, 1, None, FAKE, FAKE, None) == _abi.HQ_ERR_INVALID  # no MXFP4
     d = lib.hq_gemm_dswiglu
     args = [FAKE, FAKE, FAKE, FAKE, 2, FAKE, FAKE, FAKE, FAKE, FAKE, None, 512, 48, 64, None, 0, -1, None]
     assert d(*args) == _abi.HQ_ERR_INVALID                       # n % 32

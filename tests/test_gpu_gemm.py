@@ -77,17 +77,31 @@ def test_dense_nvfp4_forced_256_partial_n_tile(cuda_dev):
     dense_case(200, 384, 512, "nvfp4", 256, alpha=2.0, seed=11)
 
 
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("m,n,k", [(256, 256, 256), (300, 512, 512), (77, 256, 384), (130, 384, 1152)])
+def test_dense_mxfp4_shapes(cuda_dev, tile_n, m, n, k):
+    """MXFP4: E2M1 data, UE8M0 scales per 32, no alpha, no bias; k % 256 == 128
+    exercises the half k-block at the end."""
+    if tile_n == 256 and n % 256:
+        pytest.skip("partial n tile with 256 covered separately")
+    dense_case(m, n, k, "mxfp4", tile_n, seed=m * 5 + k)
+
+
+def test_dense_mxfp4_forced_256_partial_n_tile(cuda_dev):
+    dense_case(140, 384, 640, "mxfp4", 256, seed=13)
+
+
 @pytest.mark.parametrize("two_sm", [1, 0])
-@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4", "mxfp4"])
 @pytest.mark.parametrize("m,n,k", [(256, 256, 256), (300, 512, 1024), (129, 768, 640), (640, 256, 320)])
 def test_dense_256_column_tiles(cuda_dev, mode, m, n, k, two_sm):
     """n % 256 == 0: the 2-SM kernel (cluster pair, cta_group::2, 256 x 256
     tiles) and the single-SM 128 x 256 kernel, ragged M and K."""
-    if mode == "mxfp8" and k % 128:
-        pytest.skip("MXFP8 needs k % 128 == 0")
+    if mode != "nvfp4" and k % 128:
+        pytest.skip("MXFP8 and MXFP4 need k % 128 == 0")
     hq.set_gemm_2sm(two_sm)
-    dense_case(m, n, k, mode, 0, alpha=0.5 if mode == "nvfp4" else 1.25,
-               bias=(mode == "mxfp8"), seed=m + k + (7 if mode == "nvfp4" else 0),
+    dense_case(m, n, k, mode, 0, alpha={"nvfp4": 0.5, "mxfp8": 1.25, "mxfp4": None}[mode],
+               bias=(mode == "mxfp8"), seed=m + k + {"nvfp4": 7, "mxfp8": 0, "mxfp4": 3}[mode],
                g_a=2.0 if mode == "nvfp4" else None, g_b=64.0 if mode == "nvfp4" else None)
 
 
@@ -141,10 +155,10 @@ def contig_case(offsets, m_rows, n, k, mode, tile_n=0, alpha=None, bias=False, s
 
 
 @pytest.mark.parametrize("tile_n", [128, 256])
-@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4", "mxfp4"])
 def test_grouped_contig_small(cuda_dev, tile_n, mode):
     offsets = [256, 256, 768, 1024]            # empty group 1; rows >= 1024 untouched
-    alpha = [0.5, 1.0, 2.0, 1.25]
+    alpha = None if mode == "mxfp4" else [0.5, 1.0, 2.0, 1.25]
     contig_case(offsets, 1152, 256, 256, mode, tile_n, alpha=alpha, bias=(mode == "mxfp8"), seed=3)
 
 
@@ -189,10 +203,10 @@ def masked_case(masked, max_m, n, k, mode, tile_n=0, alpha=None, seed=0):
 
 
 @pytest.mark.parametrize("tile_n", [128, 256])
-@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4", "mxfp4"])
 def test_grouped_masked_small(cuda_dev, tile_n, mode):
     status = masked_case([256, 64, 0, 129, 1], 256, 256, 256, mode, tile_n,
-                         alpha=[1.0, 0.5, 2.0, 0.75, 1.5], seed=5)
+                         alpha=None if mode == "mxfp4" else [1.0, 0.5, 2.0, 0.75, 1.5], seed=5)
     assert status == 0
 
 

@@ -19,7 +19,7 @@ def run_and_compare(x_cpu, mode, swizzle=True, g=None, rows_check=None):
     x = x_cpu.to(dev)
     gs_t = torch.tensor([g], dtype=torch.float32, device=dev) if g is not None else None
     m, k = x.shape
-    q_out = torch.full(((m, k) if mode == "mxfp8" else (m, k // 2)), 0xAA, dtype=torch.uint8, device=dev)
+    q_out = torch.full(((m, k) if mode == "mxfp8" else (m, k // 2)), 0xAA, dtype=torch.uint8, device=dev)  # FP4 packed
     sf_out = torch.full((hq.sf_bytes(m, k, mode),), 0xAA, dtype=torch.uint8, device=dev)
     hq.hq_quant(x, mode, use_swizzle=swizzle, global_scale=gs_t, q_out=q_out, sf_out=sf_out)
     torch.cuda.synchronize()
@@ -42,7 +42,7 @@ def run_and_compare(x_cpu, mode, swizzle=True, g=None, rows_check=None):
         assert np.array_equal(sf_gpu, sf_ref)
 
 
-@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4", "mxfp4"])
 @pytest.mark.parametrize("swizzle", [True, False])
 @pytest.mark.parametrize("m,k", [(1, 128), (130, 256), (257, 512), (64, 1152)])
 def test_quant_small_bit_exact(cuda_dev, mode, swizzle, m, k):
@@ -56,7 +56,7 @@ def test_quant_nvfp4_global_scale(cuda_dev, g):
     run_and_compare(x, "nvfp4", True, g=float(np.float32(g)))
 
 
-@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4", "mxfp4"])
 def test_quant_special_values(cuda_dev, mode):
     k = 256
     x = torch.zeros(8, k)
