@@ -42,7 +42,7 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # nominal dense tensor-core ratios to BF16 (2.25 PFLOP/s): FP8 x2, FP4 x6
 RATIO = {"bf16": 1.0, "fp8": 2.0, "fp4": 6.0}
-SECTIONS = ("dense_mxfp8_256", "quant_nvfp4", "moe_contig", "moe_masked", "dswiglu")
+SECTIONS = ("dense_mxfp8_256", "quant_nvfp4", "moe_contig", "moe_masked", "dswiglu", "dense_mxfp4")
 
 
 GEMM_PROFILE = os.path.join(ROOT, "profiles", "bs_gemm_2sm_kernel_dense_nvfp4_4096x12288x5120.md")
@@ -432,6 +432,26 @@ class Extras:
             byts = 2 * m * k + m * k // 2 + sf.numel()
             res[f"quant_nvfp4_{name}_{m}x{k}"] = {"us": t * 1e6, "gbs": byts / t / 1e9,
                                                   "frac_hbm": byts / t / 1e9 / self.hbm}
+        return res
+
+    def dense_mxfp4(self):
+        """MXFP4 (w4a4-mxfp4, UE8M0 per 32, no alpha) on the headline shapes, and
+        its quantiser from a float16 copy of A."""
+        hq, dev = self.hq, self.dev
+        c2 = synth.dense_nvfp4(device=dev)
+        m, n, k = c2["m"], c2["n"], c2["k"]
+        qa, sfa = hq.hq_quant(c2["a"], "mxfp4")
+        qb, sfb = hq.hq_quant(c2["b"], "mxfp4")
+        out = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+        t = time_kernel(lambda: hq.hq_gemm_dense(qa, sfa, qb, sfb, m, n, k, "mxfp4", out=out), 20, self.flush)
+        fl = 2.0 * m * n * k
+        res = {"dense_mxfp4_4096x12288x5120": {"us": t * 1e6, "tflops": fl / t / 1e12,
+                                                "frac_fp4": fl / t / 1e12 / self.p_fp4}}
+        a16 = c2["a"].to(torch.float16)
+        t = time_kernel(lambda: hq.hq_quant(a16, "mxfp4", q_out=qa, sf_out=sfa), 20, self.flush)
+        byts = 2 * m * k + m * k // 2 + sfa.numel()
+        res["quant_mxfp4_A_fp16_4096x5120"] = {"us": t * 1e6, "gbs": byts / t / 1e9,
+                                               "frac_hbm": byts / t / 1e9 / self.hbm}
         return res
 
     def moe_contig(self):

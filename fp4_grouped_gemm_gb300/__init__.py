@@ -102,16 +102,20 @@ def _q_shape(rows, k, mode):
 
 def hq_quant(x, mode, use_swizzle=True, global_scale=None, q_out=None, sf_out=None,
              use_pdl=False, stream=None):
-    """Group-wise quantiser.  x: [m, k] BF16 CUDA tensor.  Returns (q, sf)."""
+    """Group-wise quantiser.  x: [m, k] BF16 or FP16 CUDA tensor (FP16 goes
+    to hq_quant_f16).  Returns (q, sf)."""
     m, k = x.shape
+    if x.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("hq_quant takes bfloat16 or float16 input")
     if q_out is None:
         q_out = torch.empty(_q_shape(m, k, mode), dtype=torch.uint8, device=x.device)
     if sf_out is None:
         sf_out = torch.empty(max(sf_bytes(m, k, mode), 1), dtype=torch.uint8, device=x.device)
-    rc = _abi.load().hq_quant(_ptr(x), m, k, mode_id(mode), 1 if use_swizzle else 0,
-                              _ptr(global_scale), _ptr(q_out), _ptr(sf_out), 1 if use_pdl else 0,
-                              _stream(stream))
-    _check(rc, "hq_quant")
+    lib = _abi.load()
+    fn, name = (lib.hq_quant_f16, "hq_quant_f16") if x.dtype == torch.float16 else (lib.hq_quant, "hq_quant")
+    rc = fn(_ptr(x), m, k, mode_id(mode), 1 if use_swizzle else 0, _ptr(global_scale), _ptr(q_out),
+            _ptr(sf_out), 1 if use_pdl else 0, _stream(stream))
+    _check(rc, name)
     return q_out, sf_out
 
 

@@ -19,6 +19,7 @@
 //   NVFP4: UE4M3 = E4M3(s), q = E2M1(x * (g / value(UE4M3))) (0 if value 0)
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "hq_internal.h"
@@ -31,7 +32,7 @@ constexpr int kThreads = 256;
 constexpr int kGroupsPerWarpStep = 32;  // one scale group per lane
 
 struct QuantParams {
-  const uint16_t* in;        // BF16 rows (quant: [rows, k]; swiglu: [rows, 2k])
+  const uint16_t* in;        // BF16 (or FP16) rows (quant: [rows, k]; swiglu: [rows, 2k])
   int64_t rows;
   int64_t k;                 // output elements per row (swiglu: H)
   int64_t in_stride;         // input row stride in elements
@@ -66,6 +67,17 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&x)[8]) {
   for (int i = 0; i < 4; ++i) {
     x[2 * i] = __uint_as_float(w[i] << 16);
     x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// eight FP16 values (exact conversion to float32)
+__device__ __forceinline__ void f16x8_to_f32(const uint4& v, float (&x)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
   }
 }
 
@@ -139,7 +151,8 @@ __device__ __forceinline__ uint32_t encode_group(const float (&x)[GS], float g,
   }
 }
 
-template <int MODE, bool SWIGLU>
+// F16IN: the input rows hold IEEE binary16 values instead of BF16
+template <int MODE, bool SWIGLU, bool F16IN = false>
 __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
   constexpr int GS = MODE == HQ_NVFP4 ? 16 : 32;
   constexpr int NV = GS / 8;          // 16-byte loads per operand and group
@@ -222,7 +235,8 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
         float a[8];
-        bf16x8_to_f32(c0[u][i], a);
+        if (F16IN) f16x8_to_f32(c0[u][i], a);
+        else bf16x8_to_f32(c0[u][i], a);
         if (SWIGLU) {
           float b[8];
           bf16x8_to_f32(c1[u][i], b);
@@ -290,13 +304,13 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
   pdl_launch_dependents();
 }
 
-template <int MODE, bool SWIGLU>
+template <int MODE, bool SWIGLU, bool F16IN = false>
 int launch_quant(const QuantParams& p, cudaStream_t st, bool pdl) {
   const int sms = num_sms();
   if (sms <= 0) return HQ_ERR_CUDA;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_kernel<MODE, SWIGLU>, kThreads,
-                                                    0) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_kernel<MODE, SWIGLU, F16IN>,
+                                                    kThreads, 0) != cudaSuccess)
     return HQ_ERR_CUDA;
   if (per_sm < 1) per_sm = 1;
   const int64_t warps_needed = p.rows * ((p.S_real + kGroupsPerWarpStep - 1) / kGroupsPerWarpStep) + 1;
@@ -304,9 +318,15 @@ int launch_quant(const QuantParams& p, cudaStream_t st, bool pdl) {
   const int64_t cap = static_cast<int64_t>(sms) * per_sm;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  cudaError_t e = launch(quant_kernel<MODE, SWIGLU>, dim3(static_cast<unsigned>(blocks)),
+  cudaError_t e = launch(quant_kernel<MODE, SWIGLU, F16IN>, dim3(static_cast<unsigned>(blocks)),
                          dim3(kThreads), 0, st, pdl, p);
   return e == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
+}
+
+int dispatch_f16(hq_mode mode, const QuantParams& p, cudaStream_t st, bool pdl) {
+  if (mode == HQ_MXFP8) return launch_quant<HQ_MXFP8, false, true>(p, st, pdl);
+  if (mode == HQ_MXFP4) return launch_quant<HQ_MXFP4, false, true>(p, st, pdl);
+  return launch_quant<HQ_NVFP4, false, true>(p, st, pdl);
 }
 
 int dispatch(hq_mode mode, bool swiglu, const QuantParams& p, cudaStream_t st, bool pdl) {
@@ -316,23 +336,19 @@ int dispatch(hq_mode mode, bool swiglu, const QuantParams& p, cudaStream_t st, b
   return swiglu ? launch_quant<HQ_NVFP4, true>(p, st, pdl) : launch_quant<HQ_NVFP4, false>(p, st, pdl);
 }
 
-}  // namespace
-}  // namespace hq
-
-extern "C" {
-
-int hq_quant(const hq_bf16* x, int64_t m, int64_t k, hq_mode mode, int use_swizzle,
-             const float* global_scale, void* q_out, uint8_t* sf_out, int use_pdl,
-             hq_stream_t s) {
+// Shared host side of hq_quant / hq_quant_f16: validation, then the launch.
+int quant_entry(const uint16_t* x, bool f16, int64_t m, int64_t k, hq_mode mode, int use_swizzle,
+                const float* global_scale, void* q_out, uint8_t* sf_out, int use_pdl,
+                hq_stream_t s) {
   if (mode != HQ_MXFP8 && mode != HQ_MXFP4 && mode != HQ_NVFP4) return HQ_ERR_INVALID;
   const int64_t gs = mode == HQ_NVFP4 ? 16 : 32;
   if (m < 0 || k <= 0 || k % (4 * gs) != 0) return HQ_ERR_INVALID;
   if (mode != HQ_NVFP4 && global_scale) return HQ_ERR_UNSUPPORTED;
   if (m == 0) return HQ_OK;
   if (!x || !q_out || !sf_out) return HQ_ERR_INVALID;
-  if (!hq::aligned16(x) || !hq::aligned16(q_out) || !hq::aligned16(sf_out)) return HQ_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(q_out) || !aligned16(sf_out)) return HQ_ERR_INVALID;
   if (global_scale && (reinterpret_cast<uintptr_t>(global_scale) & 3u)) return HQ_ERR_INVALID;
-  hq::QuantParams p{};
+  QuantParams p{};
   p.in = x;
   p.rows = m;
   p.k = k;
@@ -345,9 +361,27 @@ int hq_quant(const hq_bf16* x, int64_t m, int64_t k, hq_mode mode, int use_swizz
   p.q = static_cast<uint8_t*>(q_out);
   p.sf = sf_out;
   p.zero_pad_rows = 1;
-  p.status = hq::status_word_ptr();
+  p.status = status_word_ptr();
   if (!p.status) return HQ_ERR_CUDA;
-  return hq::dispatch(mode, false, p, reinterpret_cast<cudaStream_t>(s), use_pdl != 0);
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  return f16 ? dispatch_f16(mode, p, st, use_pdl != 0) : dispatch(mode, false, p, st, use_pdl != 0);
+}
+
+}  // namespace
+}  // namespace hq
+
+extern "C" {
+
+int hq_quant(const hq_bf16* x, int64_t m, int64_t k, hq_mode mode, int use_swizzle,
+             const float* global_scale, void* q_out, uint8_t* sf_out, int use_pdl,
+             hq_stream_t s) {
+  return hq::quant_entry(x, false, m, k, mode, use_swizzle, global_scale, q_out, sf_out, use_pdl, s);
+}
+
+int hq_quant_f16(const uint16_t* x, int64_t m, int64_t k, hq_mode mode, int use_swizzle,
+                 const float* global_scale, void* q_out, uint8_t* sf_out, int use_pdl,
+                 hq_stream_t s) {
+  return hq::quant_entry(x, true, m, k, mode, use_swizzle, global_scale, q_out, sf_out, use_pdl, s);
 }
 
 int hq_swiglu_quant(const hq_bf16* in, int64_t rows, int64_t H, const int32_t* token_nums, int E,

@@ -172,6 +172,13 @@ int hq_quant(const hq_bf16 *x, int64_t m, int64_t k, hq_mode mode, int use_swizz
              const float *global_scale, void *q_out, uint8_t *sf_out, int use_pdl,
              hq_stream_t s);
 
+/* HALOps group_wise_quant with a float16 input (the page accepts BF16 or
+ * FP16): identical to hq_quant except that x holds IEEE binary16 bit
+ * patterns, each converted exactly to float32 before the scale rule. */
+int hq_quant_f16(const uint16_t *x, int64_t m, int64_t k, hq_mode mode, int use_swizzle,
+                 const float *global_scale, void *q_out, uint8_t *sf_out, int use_pdl,
+                 hq_stream_t s);
+
 /* ------------------------------------------------------------------------- *
  * Block-scaled GEMMs: out = alpha * (A . B^T) + bias, BF16 output (RNE).
  *

@@ -72,6 +72,10 @@ def test_quant_rejects_bad_arguments(lib):
     assert lib.hq_quant(FAKE, 4, 64, 1, 1, None, FAKE, FAKE, 0, None) == _abi.HQ_ERR_INVALID
     # m == 0 is a no-op
     assert lib.hq_quant(FAKE, 0, 128, 0, 1, None, FAKE, FAKE, 0, None) == _abi.HQ_OK
+    # the float16-input entry point validates the same way
+    assert lib.hq_quant_f16(FAKE, 4, 96, 0, 1, None, FAKE, FAKE, 0, None) == _abi.HQ_ERR_INVALID
+    assert lib.hq_quant_f16(FAKE, 4, 128, 1, 1, FAKE, FAKE, FAKE, 0, None) == _abi.HQ_ERR_UNSUPPORTED
+    assert lib.hq_quant_f16(FAKE, 0, 128, 2, 1, None, FAKE, FAKE, 0, None) == _abi.HQ_OK
 
 
 def test_gemm_rejects_bad_arguments(lib):

@@ -72,6 +72,25 @@ def test_quant_special_values(cuda_dev, mode):
     run_and_compare(x.to(torch.bfloat16), mode, True)
 
 
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4", "mxfp4"])
+def test_quant_fp16_input_bit_exact(cuda_dev, mode):
+    """float16 input (hq_quant_f16): values BF16 cannot hold (11-bit
+    significands, FP16 subnormals, the FP16 maximum) quantise exactly as the
+    oracle quantises the same float values."""
+    g = torch.Generator().manual_seed(17)
+    x = (torch.randn(130, 512, generator=g) * 3).to(torch.float16)
+    x[0, :64] = torch.tensor(1.0 + 2.0 ** -10, dtype=torch.float16)   # not a BF16 value
+    x[1, :32] = torch.tensor(2.0 ** -24, dtype=torch.float16)         # smallest FP16 subnormal
+    x[2, :32] = 65504.0                                               # FP16 maximum
+    x[3] = torch.linspace(-1.0, 1.0, 512).to(torch.float16) * 2.0 ** -14
+    dev = torch.device("cuda")
+    q, sf = hq.hq_quant(x.to(dev), mode)
+    torch.cuda.synchronize()
+    q_ref, sf_ref = oquant.group_wise_quant(x.float().numpy(), mode, True, None)
+    assert np.array_equal(q.cpu().numpy(), q_ref)
+    assert np.array_equal(sf.cpu().numpy(), sf_ref)
+
+
 def test_quant_dense_nvfp4_activation_full_size(cuda_dev):
     cfg = synth.dense_nvfp4(device="cuda")
     rows = np.random.default_rng(0).choice(cfg["m"], 96, replace=False)
