@@ -15,12 +15,13 @@ formats  element and scale codecs (E4M3, E2M1, UE8M0, UE4M3) by value table
 quant    scale derivation, group-wise quantisation, the 128x4 SfAtom layout
 gemm     dequantise-then-float64 GEMM: dense, grouped contiguous, grouped masked
 glu      SwiGLU forward + requantisation, dSwiGLU and dGeGLU backward closed forms
+permute  routing permute of tokens and scales into the masked-GEMM layout
 
 Every function is pinned by ``tests/test_oracle_*.py`` against something other
 than itself (library decoders, hand-worked values, exact rational brute force,
 finite differences, invariants).
 """
 
-from . import formats, quant, gemm, glu  # noqa: F401
+from . import formats, quant, gemm, glu, permute  # noqa: F401
 
-__all__ = ["formats", "quant", "gemm", "glu"]
+__all__ = ["formats", "quant", "gemm", "glu", "permute"]
