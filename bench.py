@@ -42,7 +42,8 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # nominal dense tensor-core ratios to BF16 (2.25 PFLOP/s): FP8 x2, FP4 x6
 RATIO = {"bf16": 1.0, "fp8": 2.0, "fp4": 6.0}
-SECTIONS = ("dense_mxfp8_256", "quant_nvfp4", "moe_contig", "moe_masked", "dswiglu", "dense_mxfp4")
+SECTIONS = ("dense_mxfp8_256", "quant_nvfp4", "moe_contig", "moe_masked", "dswiglu", "dense_mxfp4",
+            "permute")
 
 
 GEMM_PROFILE = os.path.join(ROOT, "profiles", "bs_gemm_2sm_kernel_dense_nvfp4_4096x12288x5120.md")
@@ -453,6 +454,31 @@ class Extras:
         res["quant_mxfp4_A_fp16_4096x5120"] = {"us": t * 1e6, "gbs": byts / t / 1e9,
                                                "frac_hbm": byts / t / 1e9 / self.hbm}
         return res
+
+    def permute(self):
+        """Routing permute of 8192 FP8 tokens (hidden 7168, top-8 of 32 experts,
+        uniform routing, per-32 scales in direct mode) into the masked layout."""
+        hq, dev = self.hq, self.dev
+        T, hidden, topk, E = 8192, 7168, 8, 32
+        cap = 4096                                   # twice the mean load per expert
+        g = torch.Generator(device=dev).manual_seed(6)
+        x = torch.randint(0, 256, (T, hidden), generator=g, device=dev, dtype=torch.uint8)
+        sc = torch.randint(0, 256, (T, hidden // 32), generator=g, device=dev, dtype=torch.uint8)
+        ids = torch.argsort(torch.rand(T, E, generator=g, device=dev), dim=1)[:, :topk].contiguous()
+        xf = x.view(torch.float8_e4m3fn)
+        px = torch.empty(E * cap, hidden, dtype=torch.float8_e4m3fn, device=dev)
+        osf = torch.empty(E * cap * hidden // 32, dtype=torch.uint8, device=dev)
+        imap = torch.empty(T, topk, dtype=torch.int32, device=dev)
+        tn = torch.empty(E, dtype=torch.int32, device=dev)
+        ws = torch.empty(hq.hq_prefill_permute_workspace_size(T, E), dtype=torch.uint8, device=dev)
+        fn = lambda: hq.hq_prefill_permute(xf, sc, ids, E, cap, permute_x=px, out_scale=osf,  # noqa: E731
+                                           indice_map=imap, token_nums=tn, workspace=ws)
+        t = time_kernel(fn, 20, self.flush)
+        # algorithmic bytes: each routed row read once per slot and written once,
+        # scales likewise, ids read, map written
+        byts = T * topk * (2 * hidden + 2 * hidden // 32) + T * topk * (8 + 4)
+        return {"permute_fp8_T8192_top8_E32_h7168": {"us": t * 1e6, "gbs": byts / t / 1e9,
+                                                     "frac_hbm": byts / t / 1e9 / self.hbm}}
 
     def moe_contig(self):
         hq, dev = self.hq, self.dev

@@ -14,13 +14,14 @@ import torch
 
 from . import _abi
 from ._abi import (HQ_MXFP8, HQ_MXFP4, HQ_NVFP4, HQ_STATUS_WAIT_TIMEOUT, HQ_STATUS_MASK_CLAMPED,  # noqa: F401
-                   HQ_STATUS_BAD_OFFSETS, HQ_STATUS_TOKENS_CLAMPED)
+                   HQ_STATUS_BAD_OFFSETS, HQ_STATUS_TOKENS_CLAMPED, HQ_STATUS_ROUTING_DROPPED)
 
 __all__ = [
     "HQError", "mode_id", "group_size", "sf_bytes", "capabilities", "get_device_status",
     "set_wait_limit_ns", "selftest_wait_expiry", "set_gemm_tile_n", "set_gemm_2sm", "hq_quant",
     "hq_gemm_dense", "hq_gemm_grouped_contig", "hq_gemm_grouped_masked", "hq_swiglu_quant",
     "hq_gemm_dswiglu", "hq_gemm_dswiglu_workspace_size", "hq_gemm_dgeglu", "swiglu_kb_dim",
+    "hq_prefill_permute", "hq_prefill_permute_workspace_size",
 ]
 
 _MODES = {"mxfp8": HQ_MXFP8, "w8a8-mxfp8": HQ_MXFP8, "mxfp4": HQ_MXFP4, "w4a4-mxfp4": HQ_MXFP4,
@@ -219,3 +220,49 @@ def hq_gemm_dgeglu(a, b, c, padded_offsets, alpha, prob, dprob, dbias=None, d_ro
         _ptr(dprob), _ptr(dbias), m, n, k, _ptr(workspace), ws_bytes, sm_count, _stream(stream))
     _check(rc, "hq_gemm_dgeglu")
     return d_row, dprob, dbias
+
+
+def hq_prefill_permute_workspace_size(num_tokens, num_experts):
+    return _abi.load().hq_prefill_permute_workspace_size(num_tokens, num_experts)
+
+
+def hq_prefill_permute(x, scale, topk_ids, num_experts, max_token_num, permute_x=None,
+                       out_scale=None, indice_map=None, token_nums=None, workspace=None,
+                       stream=None):
+    """Routing permute into the masked-GEMM layout.  x: [T, hidden] bfloat16 or
+    float8_e4m3fn; scale: int32 [T, hidden/512] (broadcast) or uint8
+    [T, hidden/32] (direct); topk_ids: int64 [T, topk].  Returns (permute_x,
+    out_scale, indice_map, token_nums)."""
+    T, hidden = x.shape
+    topk = topk_ids.shape[1]
+    if x.dtype == torch.bfloat16:
+        elem = 2
+    elif x.dtype == torch.float8_e4m3fn:
+        elem = 1
+    else:
+        raise ValueError("x must be bfloat16 or float8_e4m3fn")
+    if scale.dtype == torch.int32:
+        mode = 0
+    elif scale.dtype == torch.uint8:
+        mode = 1
+    else:
+        raise ValueError("scale must be int32 (broadcast) or uint8 (direct)")
+    dev = x.device
+    rows = num_experts * max_token_num
+    if permute_x is None:
+        permute_x = torch.empty(rows, hidden, dtype=x.dtype, device=dev)
+    if out_scale is None:
+        out_scale = torch.empty(rows * (hidden // 32), dtype=torch.uint8, device=dev)
+    if indice_map is None:
+        indice_map = torch.empty(T, topk, dtype=torch.int32, device=dev)
+    if token_nums is None:
+        token_nums = torch.empty(num_experts, dtype=torch.int32, device=dev)
+    ws_bytes = hq_prefill_permute_workspace_size(T, num_experts)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    rc = _abi.load().hq_prefill_permute(_ptr(x), elem, _ptr(scale), mode, _ptr(topk_ids), T, hidden,
+                                        topk, num_experts, max_token_num, _ptr(permute_x),
+                                        _ptr(out_scale), _ptr(indice_map), _ptr(token_nums),
+                                        _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "hq_prefill_permute")
+    return permute_x, out_scale, indice_map, token_nums

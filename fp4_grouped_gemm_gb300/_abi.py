@@ -30,6 +30,7 @@ HQ_STATUS_WAIT_TIMEOUT = 0x1
 HQ_STATUS_MASK_CLAMPED = 0x2
 HQ_STATUS_BAD_OFFSETS = 0x4
 HQ_STATUS_TOKENS_CLAMPED = 0x8
+HQ_STATUS_ROUTING_DROPPED = 0x10
 
 
 class Capabilities(ctypes.Structure):
@@ -61,6 +62,9 @@ SIGNATURES = {
     "hq_gemm_dswiglu": (c_i32, [c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_p, c_p, c_p, c_p, c_i64,
                                 c_i64, c_i64, c_p, c_sz, c_i32, c_p]),
     "hq_gemm_dswiglu_workspace_size": (c_sz, [c_i32, c_i64]),
+    "hq_prefill_permute": (c_i32, [c_p, c_i32, c_p, c_i32, c_p, c_i64, c_i64, c_i32, c_i32, c_i64,
+                                   c_p, c_p, c_p, c_p, c_p, c_sz, c_p]),
+    "hq_prefill_permute_workspace_size": (c_sz, [c_i64, c_i32]),
     "hq_gemm_dgeglu": (c_i32, [c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_p, c_p, c_p, c_i64, c_i64,
                                c_i64, c_p, c_sz, c_i32, c_p]),
     "hq_gemm_dswiglu_noalloc": (c_i32, [c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_p, c_p, c_p, c_p,

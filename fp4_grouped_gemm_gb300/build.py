@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libhq.so")
 STAMP = os.path.join(BUILD_DIR, "libhq.stamp")
 
-SOURCES = ["hq_common.cu", "hq_quant.cu", "hq_gemm_bs.cu", "hq_gemm_dswiglu.cu"]
+SOURCES = ["hq_common.cu", "hq_quant.cu", "hq_gemm_bs.cu", "hq_gemm_dswiglu.cu", "hq_permute.cu"]
 HEADERS = ["hq_ptx.cuh", "hq_internal.h", "hq_sched.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

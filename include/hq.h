@@ -83,6 +83,7 @@ enum {
 #define HQ_STATUS_BAD_OFFSETS 0x4u    /* padded_offsets not monotone / 128-aligned /
                                          beyond the row count: rows skipped      */
 #define HQ_STATUS_TOKENS_CLAMPED 0x8u /* token_nums[e] outside [0, rows/expert]    */
+#define HQ_STATUS_ROUTING_DROPPED 0x10u /* permute: a bad expert id or a full expert */
 
 /* Layout and alignment constants, so integrations need not copy them
  * (FlashRT fp4-gemm notes: "Read capabilities() instead of duplicating
@@ -329,6 +330,42 @@ int hq_gemm_dswiglu_noalloc(const hq_bf16 *a, const hq_bf16 *b, const hq_bf16 *c
                             const float *beta, const float *prob, hq_bf16 *d_row, float *dprob,
                             hq_bf16 *dbias, int64_t m, int64_t n, int64_t k, int sm_count,
                             hq_stream_t s);
+
+/* ------------------------------------------------------------------------- *
+ * HALOps "GEMM" API, prefill_permute_to_masked_gemm: rearranges tokens into
+ * the padded expert layout [E * max_token_num, hidden] of
+ * hq_gemm_grouped_masked and converts their scale factors into the SfAtom
+ * layout of [E * max_token_num, hidden / 32] bytes.
+ *   x            [num_tokens, hidden] elements of elem_bytes bytes (1: E4M3,
+ *                2: BF16); 16-byte aligned
+ *   scale        scale_mode 0 ("broadcast"): int32 [num_tokens, hidden / 512],
+ *                byte b of word i is the scale of elements [128 (4i + b),
+ *                +128) and is repeated for its four 32-element groups;
+ *                scale_mode 1 ("direct"): uint8 [num_tokens, hidden / 32];
+ *                4-byte aligned
+ *   topk_ids     int64 [num_tokens, topk] expert per (token, slot); -1 means
+ *                unassigned
+ *   permute_x    [E * max_token_num, hidden] output (same element type)
+ *   out_scale    SfAtom output, E * max_token_num * hidden / 32 bytes
+ *   indice_map   int32 [num_tokens, topk]: the expert-local row of each
+ *                (token, slot), -1 if unassigned or dropped
+ *   token_nums   int32 [E]: rows written per expert (the masked_m of the
+ *                following hq_gemm_grouped_masked)
+ *   workspace    hq_prefill_permute_workspace_size(num_tokens, E) bytes,
+ *                256-byte aligned, caller-owned
+ * Each expert's rows are filled in increasing (token, slot) order.  An id
+ * outside [0, E) other than -1, or an entry whose expert already holds
+ * max_token_num rows, is dropped (map -1) and sets HQ_STATUS_ROUTING_DROPPED;
+ * nothing is written out of bounds.  Rows past token_nums[e] and their scale
+ * bytes are not written.  Requires 1 <= topk <= 32, 1 <= E <= 1024,
+ * max_token_num a positive multiple of 128, hidden a multiple of 512
+ * (broadcast) or 128 (direct). */
+int hq_prefill_permute(const void *x, int elem_bytes, const void *scale, int scale_mode,
+                       const int64_t *topk_ids, int64_t num_tokens, int64_t hidden, int topk,
+                       int num_experts, int64_t max_token_num, void *permute_x, uint8_t *out_scale,
+                       int32_t *indice_map, int32_t *token_nums, void *workspace, size_t ws_bytes,
+                       hq_stream_t s);
+size_t hq_prefill_permute_workspace_size(int64_t num_tokens, int num_experts);
 
 #ifdef __cplusplus
 }

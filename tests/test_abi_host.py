@@ -119,6 +119,30 @@ def test_swiglu_and_dswiglu_reject_bad_arguments(lib):
     assert d(*args) == _abi.HQ_ERR_INVALID
 
 
+def test_permute_rejects_bad_arguments(lib):
+    f = lib.hq_prefill_permute
+    ws = hq.hq_prefill_permute_workspace_size(300, 8)
+    assert ws >= 2 * 3 * 8 * 4 and ws % 256 == 0
+    good = [FAKE, 2, FAKE, 0, ctypes.c_void_p(0x10000), 300, 1024, 4, 8, 256, FAKE, FAKE, FAKE, FAKE,
+            ctypes.c_void_p(0x10000), ws, None]
+
+    def call(**over):
+        a = list(good)
+        for i, v in over.items():
+            a[int(i[1:])] = v
+        return f(*a)
+
+    assert call(a1=3) == _abi.HQ_ERR_INVALID                       # element size
+    assert call(a3=2) == _abi.HQ_ERR_INVALID                       # scale mode
+    assert call(a6=1000) == _abi.HQ_ERR_INVALID                    # hidden % 512 (broadcast)
+    assert call(a7=0) == _abi.HQ_ERR_INVALID and call(a7=33) == _abi.HQ_ERR_INVALID   # topk
+    assert call(a8=0) == _abi.HQ_ERR_INVALID and call(a8=1025) == _abi.HQ_ERR_INVALID  # experts
+    assert call(a9=200) == _abi.HQ_ERR_INVALID                     # max_token_num % 128
+    assert call(a15=ws - 256) == _abi.HQ_ERR_INVALID               # workspace too small
+    assert call(a0=ctypes.c_void_p(0x10008)) == _abi.HQ_ERR_INVALID  # x not 16-byte aligned
+    assert call(a13=None) == _abi.HQ_ERR_INVALID                   # token_nums
+
+
 def test_knobs_validate(lib):
     assert lib.hq_set_gemm_tile_n(96) == _abi.HQ_ERR_INVALID
     assert lib.hq_set_gemm_tile_n(0) == _abi.HQ_OK
