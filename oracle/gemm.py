@@ -82,6 +82,34 @@ def grouped_contig(a_deq, b_deq, padded_offsets, alpha=None, bias=None):
     return ref, mag, grp >= 0
 
 
+def grouped_rows(a_deq, b_deq, expert_ids, alpha=None, bias=None):
+    """Contiguous grouped GEMM with a per-row expert index (HALOps
+    group_contiguous_gemm: "expert_ids maps each token row to its expert",
+    groups packed without per-expert padding).
+
+    Reading G6: a row whose id lies outside [0, L), or that breaks the
+    non-decreasing order the page requires (id below the previous row's), is
+    not written.  Returns (ref [M, N], mag [M, N], written [M]).
+    """
+    a_deq = np.asarray(a_deq, dtype=np.float64)
+    b_deq = np.asarray(b_deq, dtype=np.float64)
+    L, N, _ = b_deq.shape
+    ids = np.asarray(expert_ids, dtype=np.int64)
+    M = a_deq.shape[0]
+    al, bi = _alpha_bias(alpha, bias, L, N)
+    ref = np.zeros((M, N))
+    mag = np.zeros((M, N))
+    written = np.zeros(M, dtype=bool)
+    for m in range(M):
+        g = int(ids[m])
+        if g < 0 or g >= L or (m > 0 and g < ids[m - 1]):
+            continue
+        ref[m] = al[g] * (b_deq[g] @ a_deq[m]) + bi[g]
+        mag[m] = abs(al[g]) * (np.abs(b_deq[g]) @ np.abs(a_deq[m]))
+        written[m] = True
+    return ref, mag, written
+
+
 def grouped_masked(a_deq, b_deq, masked_m, max_m, alpha=None, bias=None):
     """Masked grouped GEMM under G4.
 

@@ -148,6 +148,31 @@ def test_grouped_contig_groups_rows_and_skips_tail():
     assert not ref[768:].any()
 
 
+def test_grouped_rows_by_hand_and_against_contig():
+    K, N = 32, 4
+    a = rand_bf16((10, K), 80)
+    b = rand_bf16((3, N, K), 81)
+    ids = np.array([0, 0, 0, 2, 2, 2, 2, 2, 2, 2])     # expert 1 empty, no padding
+    ref, _, written = gemm.grouped_rows(a, b, ids, alpha=[1.0, 9.0, 0.5])
+    assert written.all()
+    assert np.allclose(ref[:3], a[:3] @ b[0].T, rtol=1e-14)
+    assert np.allclose(ref[3:], 0.5 * (a[3:] @ b[2].T), rtol=1e-14)
+    # a padded layout through expert ids equals the padded-offsets form
+    A = rand_bf16((768, K), 82)
+    ids2 = np.repeat([0, 2, 2], 256)
+    r1, m1, w1 = gemm.grouped_rows(A, b, ids2)
+    r2, m2, w2 = gemm.grouped_contig(A, b, [256, 256, 768])
+    assert np.array_equal(r1, r2) and np.array_equal(m1, m2) and np.array_equal(w1, w2)
+
+
+def test_grouped_rows_skips_bad_ids():
+    a = rand_bf16((6, 32), 83)
+    b = rand_bf16((2, 4, 32), 84)
+    _, _, written = gemm.grouped_rows(a, b, np.array([0, 5, 1, 0, 1, -1]))
+    # 5 out of range, 0 after 1 breaks the order, -1 out of range
+    assert written.tolist() == [True, False, True, False, True, False]
+
+
 def test_grouped_masked_rows():
     K, N, max_m = 32, 4, 128
     masked = [128, 64, 0, 200]                     # 200 is clamped to max_m
