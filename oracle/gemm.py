@@ -88,8 +88,8 @@ def grouped_rows(a_deq, b_deq, expert_ids, alpha=None, bias=None):
     groups packed without per-expert padding).
 
     Reading G6: a row whose id lies outside [0, L), or that breaks the
-    non-decreasing order the page requires (id below the previous row's), is
-    not written.  Returns (ref [M, N], mag [M, N], written [M]).
+    non-decreasing order the page requires (its id is below the id of the row
+    before it, whatever that id is), is not written.  Returns (ref [M, N], mag [M, N], written [M]).
     """
     a_deq = np.asarray(a_deq, dtype=np.float64)
     b_deq = np.asarray(b_deq, dtype=np.float64)

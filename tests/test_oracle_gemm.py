@@ -169,8 +169,9 @@ def test_grouped_rows_skips_bad_ids():
     a = rand_bf16((6, 32), 83)
     b = rand_bf16((2, 4, 32), 84)
     _, _, written = gemm.grouped_rows(a, b, np.array([0, 5, 1, 0, 1, -1]))
-    # 5 out of range, 0 after 1 breaks the order, -1 out of range
-    assert written.tolist() == [True, False, True, False, True, False]
+    # 5 is out of range; 1 after 5 and 0 after 1 break the order (each row is
+    # compared with the id of the row before it); -1 is out of range
+    assert written.tolist() == [True, False, False, False, True, False]
 
 
 def test_grouped_masked_rows():
