@@ -21,7 +21,8 @@ __all__ = [
     "set_wait_limit_ns", "selftest_wait_expiry", "set_gemm_tile_n", "set_gemm_2sm", "hq_quant",
     "hq_gemm_dense", "hq_gemm_grouped_contig", "hq_gemm_grouped_masked", "hq_swiglu_quant",
     "hq_gemm_dswiglu", "hq_gemm_dswiglu_workspace_size", "hq_gemm_dgeglu", "swiglu_kb_dim",
-    "hq_prefill_permute", "hq_prefill_permute_workspace_size",
+    "hq_prefill_permute", "hq_prefill_permute_workspace_size", "hq_gemm_grouped_rows",
+    "hq_gemm_grouped_rows_workspace_size",
 ]
 
 _MODES = {"mxfp8": HQ_MXFP8, "w8a8-mxfp8": HQ_MXFP8, "mxfp4": HQ_MXFP4, "w4a4-mxfp4": HQ_MXFP4,
@@ -140,6 +141,27 @@ def hq_gemm_grouped_contig(a, sfa, b, sfb, padded_offsets, m_rows, n, k, mode, a
         _ptr(alpha), _ptr(bias), _ptr(out), m_rows, n, k, mode_id(mode), sm_count,
         _stream(stream))
     _check(rc, "hq_gemm_grouped_contig")
+    return out
+
+
+def hq_gemm_grouped_rows_workspace_size(m_rows, L):
+    return _abi.load().hq_gemm_grouped_rows_workspace_size(m_rows, L)
+
+
+def hq_gemm_grouped_rows(a, sfa, b, sfb, expert_ids, L, m_rows, n, k, mode, alpha=None, bias=None,
+                         out=None, workspace=None, sm_count=-1, stream=None):
+    """HALOps group_contiguous_gemm with per-row expert ids (int32 [m_rows],
+    non-decreasing); groups need no padding."""
+    if out is None:
+        out = torch.empty(m_rows, n, dtype=torch.bfloat16, device=a.device)
+    ws_bytes = hq_gemm_grouped_rows_workspace_size(m_rows, L)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=a.device)
+    rc = _abi.load().hq_gemm_grouped_rows(
+        _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(expert_ids), L, _ptr(alpha), _ptr(bias),
+        _ptr(out), m_rows, n, k, mode_id(mode), _ptr(workspace), workspace.numel(), sm_count,
+        _stream(stream))
+    _check(rc, "hq_gemm_grouped_rows")
     return out
 
 

@@ -116,7 +116,8 @@ struct EpiArgs {
   float alpha;
   const uint16_t* bias;  // bias row of the group (column 0) or null
   uint16_t* out;         // output row of lane 0 of this quarter (column 0)
-  int rows_here;         // valid rows of this quarter (may be <= 0 or > 32)
+  int rows_here;         // valid rows of this quarter (may be <= 0 or > 32) ...
+  int rows_lo;           // ... from this row of the quarter on (may be <= 0)
   uint32_t stage_s;      // this warp's staging buffer (shared address)
   int lane;
 };
@@ -172,7 +173,8 @@ __device__ __forceinline__ void epi_store16(const EpiArgs& e, int64_t col0, cons
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(e.stage_s + off)
                  : "memory");
-    if (rr < e.rows_here) *reinterpret_cast<uint4*>(e.out + rr * e.n + col0 + u * 8) = v;
+    if (rr >= e.rows_lo && rr < e.rows_here)
+      *reinterpret_cast<uint4*>(e.out + rr * e.n + col0 + u * 8) = v;
   }
   __syncwarp();
 }
@@ -508,6 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       e.bias = p.bias ? p.bias + static_cast<int64_t>(ti.g) * p.n : nullptr;
       e.out = p.out + (ti.row0 + q * 32) * p.n;
       e.rows_here = ti.rows_valid - q * 32;
+      e.rows_lo = ti.row_lo - q * 32;
       e.stage_s = sbase + C::OFF_STAGE_OUT + ew * 1024;
       e.lane = lane;
       const uint32_t tempty = tempty_bar(acc);
@@ -844,6 +847,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       e.bias = p.bias;
       e.out = p.out + (row0 + q * 32) * p.n;
       e.rows_here = rem < 0 ? 0 : (rem > 32 ? 32 : static_cast<int>(rem));
+      e.rows_lo = 0;
       e.stage_s = sbase + C::OFF_STAGE_OUT + ew * 1024;
       e.lane = lane;
       epilogue_tile<C::BN, true>(e, [&] { if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader); });
@@ -1012,6 +1016,132 @@ int check_common(const void* a, const uint8_t* sfa, const void* b, const uint8_t
   return HQ_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Segment list for the per-row expert-id form of the contiguous GEMM (HALOps
+// group_contiguous_gemm).  Row r is valid if 0 <= id[r] < L and (r == 0 or
+// id[r] >= id[r - 1]); a segment is a maximal run of valid rows with one id
+// inside one 128-row block.  One warp per block: lane l holds rows l + 32 j
+// (j = 0..3); boundaries and starts come from ballots over the block's 128
+// rows.  Pass 0 counts a block's segments, pass 1 writes them at the block's
+// exclusive prefix (computed in between by seg_scan).
+// Workspace: int32 [0] = segment count, [1..3] unused, then int4
+// {row0, expert, first row - row0, end row - row0} per segment, then the
+// per-block counts and prefixes.
+// ---------------------------------------------------------------------------
+struct SegParams {
+  const int32_t* ids;
+  int64_t M;
+  int L;
+  int64_t nblocks;
+  int64_t cap;          // segment capacity of the list
+  int32_t* ws;          // header + list
+  int32_t* blk_count;   // [nblocks]
+  int32_t* blk_base;    // [nblocks]
+  uint32_t* status;
+};
+
+template <int PASS>
+__global__ void __launch_bounds__(256) seg_build(const SegParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (b >= p.nblocks) return;
+  const int64_t r0 = b * kBM;
+  uint32_t valid_m[4], start_m[4];
+  int id_of[4], prev_of[4];
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int64_t r = r0 + lane + 32 * j;
+    const bool in = r < p.M;
+    const int id = in ? __ldg(p.ids + r) : -1;
+    const int prev = (in && r > 0) ? __ldg(p.ids + r - 1) : -1;
+    const bool v = in && id >= 0 && id < p.L && (r == 0 || id >= prev);
+    if (in && !v) bad = true;
+    valid_m[j] = __ballot_sync(0xFFFFFFFFu, v);
+    id_of[j] = id;
+    prev_of[j] = prev;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    // a valid row starts a segment unless the row before it, in this block,
+    // is valid with the same id
+    const bool v = (valid_m[j] >> lane) & 1u;
+    const bool prev_valid = lane > 0 ? ((valid_m[j] >> (lane - 1)) & 1u)
+                                     : (j > 0 ? ((valid_m[j - 1] >> 31) & 1u) : false);
+    const bool st = v && (!prev_valid || prev_of[j] != id_of[j]);
+    start_m[j] = __ballot_sync(0xFFFFFFFFu, st);
+  }
+  if (__any_sync(0xFFFFFFFFu, bad) && lane == 0 && PASS == 0) atomicOr(p.status, HQ_STATUS_BAD_OFFSETS);
+  const int count = __popc(start_m[0]) + __popc(start_m[1]) + __popc(start_m[2]) + __popc(start_m[3]);
+  if (PASS == 0) {
+    if (lane == 0) p.blk_count[b] = count;
+    return;
+  }
+  // boundary = a start or an invalid row: a segment ends at the next boundary
+  uint32_t bnd[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) bnd[j] = start_m[j] | ~valid_m[j];
+  int k = p.blk_base[b];
+  int4* list = reinterpret_cast<int4*>(p.ws) + 1;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const bool st = (start_m[j] >> lane) & 1u;
+    // rank of this start within the block
+    int rank = __popc(start_m[j] & ((1u << lane) - 1u));
+    for (int jj = 0; jj < j; ++jj) rank += __popc(start_m[jj]);
+    if (st) {
+      const int s = lane + 32 * j;
+      int e = kBM;  // first boundary row after s
+      for (int w = s + 1; w < kBM; ++w)
+        if ((bnd[w >> 5] >> (w & 31)) & 1u) { e = w; break; }
+      const int64_t slot = static_cast<int64_t>(k) + rank;
+      if (slot < p.cap)
+        list[slot] = make_int4(static_cast<int>(r0), id_of[j], s, e);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(1024) seg_scan(const SegParams p) {
+  // single CTA: exclusive prefix of the per-block counts, in chunks of 1024
+  __shared__ int32_t part[32];
+  int64_t carry = 0;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int64_t base = 0; base < p.nblocks; base += 1024) {
+    const int64_t b = base + threadIdx.x;
+    const int32_t c = b < p.nblocks ? p.blk_count[b] : 0;
+    int32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (lane == 31) part[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int32_t v = part[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t u = __shfl_up_sync(0xFFFFFFFFu, v, o);
+        if (lane >= o) v += u;
+      }
+      part[lane] = v;  // inclusive prefix of warp totals
+    }
+    __syncthreads();
+    const int32_t warp_off = warp > 0 ? part[warp - 1] : 0;
+    if (b < p.nblocks) p.blk_base[b] = static_cast<int32_t>(carry + warp_off + incl - c);
+    carry += part[31];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    int64_t total = carry;
+    if (total > p.cap) {
+      atomicOr(p.status, HQ_STATUS_BAD_OFFSETS);
+      total = p.cap;
+    }
+    p.ws[0] = static_cast<int32_t>(total);
+  }
+}
+
 GemmParams base_params(const uint8_t* sfa, const uint8_t* sfb, const float* alpha,
                        const hq_bf16* bias, hq_bf16* out, int64_t n, int64_t k, hq_mode mode) {
   GemmParams p{};
@@ -1067,6 +1197,52 @@ int hq_gemm_grouped_contig(const void* a, const uint8_t* sfa, const void* b, con
   p.gs.group_info = padded_offsets;
   p.gs.sched = hq::kContig;
   return hq::run_gemm(mode, a, b, p, sm_count, false, reinterpret_cast<cudaStream_t>(s));
+}
+
+size_t hq_gemm_grouped_rows_workspace_size(int64_t m_rows, int L) {
+  if (m_rows < 0 || L < 1) return 0;
+  const size_t nblocks = static_cast<size_t>((m_rows + hq::kBM - 1) / hq::kBM);
+  const size_t cap = 2 * nblocks + static_cast<size_t>(L);
+  const size_t bytes = 16 + 16 * cap + 8 * nblocks;
+  return (bytes + 255) / 256 * 256;
+}
+
+int hq_gemm_grouped_rows(const void* a, const uint8_t* sfa, const void* b, const uint8_t* sfb,
+                         const int32_t* expert_ids, int L, const float* alpha, const hq_bf16* bias,
+                         hq_bf16* out, int64_t m_rows, int64_t n, int64_t k, hq_mode mode,
+                         void* workspace, size_t ws_bytes, int sm_count, hq_stream_t s) {
+  int rc = hq::check_common(a, sfa, b, sfb, alpha, bias, out, n, k, mode);
+  if (rc != HQ_OK) return rc;
+  if (!expert_ids || L < 1 || L > hq::kMaxGroups) return HQ_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(expert_ids) & 3u) return HQ_ERR_INVALID;
+  if (m_rows < 0 || m_rows > (1ll << 31) - 256) return HQ_ERR_INVALID;
+  if (m_rows == 0) return HQ_OK;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+      ws_bytes < hq_gemm_grouped_rows_workspace_size(m_rows, L))
+    return HQ_ERR_INVALID;
+  hq::GemmParams p = hq::base_params(sfa, sfb, alpha, bias, out, n, k, mode);
+  if (!p.gs.status) return HQ_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  hq::SegParams sp{};
+  sp.ids = expert_ids;
+  sp.M = m_rows;
+  sp.L = L;
+  sp.nblocks = (m_rows + hq::kBM - 1) / hq::kBM;
+  sp.cap = 2 * sp.nblocks + L;
+  sp.ws = static_cast<int32_t*>(workspace);
+  sp.blk_count = sp.ws + 4 + 4 * sp.cap;
+  sp.blk_base = sp.blk_count + sp.nblocks;
+  sp.status = p.gs.status;
+  const unsigned grid = static_cast<unsigned>((sp.nblocks * 32 + 255) / 256);
+  hq::seg_build<0><<<grid, 256, 0, st>>>(sp);
+  hq::seg_scan<<<1, 1024, 0, st>>>(sp);
+  hq::seg_build<1><<<grid, 256, 0, st>>>(sp);
+  if (cudaGetLastError() != cudaSuccess) return HQ_ERR_CUDA;
+  p.gs.a_rows = m_rows;
+  p.gs.groups = L;
+  p.gs.group_info = sp.ws;
+  p.gs.sched = hq::kSegments;
+  return hq::run_gemm(mode, a, b, p, sm_count, false, st);
 }
 
 int hq_gemm_grouped_masked(const void* a, const uint8_t* sfa, const void* b, const uint8_t* sfb,

@@ -8,6 +8,11 @@
 //               a [E * max_m, K] layout): per-expert clamped counts and an
 //               exclusive prefix of their 128-row tile counts, so only tiles
 //               that hold valid rows are ever scheduled.
+//   segments    (HALOps group_contiguous_gemm: a per-row expert index, groups
+//               packed without padding): a list, built by a preparatory
+//               kernel, of (128-row block, expert, first row, end row) runs;
+//               a block that holds rows of several experts is computed once
+//               per expert and each pass writes only that expert's rows.
 // Tile t covers rows [row0, row0 + 128) of one group and columns
 // [n0, n0 + BN); n varies fastest.
 #pragma once
@@ -18,13 +23,14 @@
 
 namespace hq {
 
-enum Sched : int { kDense = 0, kContig = 1, kMasked = 2 };
+enum Sched : int { kDense = 0, kContig = 1, kMasked = 2, kSegments = 3 };
 
 constexpr int kBM = 128;
 constexpr int kMaxGroups = 1024;
 
 struct GroupSched {
-  const int32_t* group_info;  // contig: padded_offsets[L]; masked: masked_m[E]
+  const int32_t* group_info;  // contig: padded_offsets[L]; masked: masked_m[E];
+                              // segments: [count, pad x3, {row0, g, lo, hi} x count]
   int64_t a_rows;             // rows of A / out
   int64_t max_m;              // masked only
   int groups;
@@ -35,7 +41,8 @@ struct GroupSched {
 struct TileInfo {
   int g;
   int64_t row0;
-  int rows_valid;
+  int rows_valid;  // rows [row0, row0 + rows_valid) may be written ...
+  int row_lo;      // ... from row0 + row_lo on (segments only; 0 otherwise)
   int n0;
 };
 
@@ -52,7 +59,14 @@ __device__ __forceinline__ TileInfo decode_tile(const GroupSched& p, const Sched
   TileInfo ti;
   const int64_t mt = t / s.n_tiles;
   ti.n0 = static_cast<int>(t - mt * s.n_tiles) * BN;
-  if (p.sched == kDense) {
+  ti.row_lo = 0;
+  if (p.sched == kSegments) {
+    const int4 sg = __ldg(reinterpret_cast<const int4*>(p.group_info) + 1 + mt);
+    ti.row0 = sg.x;
+    ti.g = sg.y;
+    ti.row_lo = sg.z;
+    ti.rows_valid = sg.w;
+  } else if (p.sched == kDense) {
     ti.g = 0;
     ti.row0 = mt * kBM;
     const int64_t rem = p.a_rows - ti.row0;
@@ -88,6 +102,10 @@ __device__ inline void build_table(const GroupSched& p, int32_t* tab0, int32_t* 
                             int64_t* total_mtiles) {
   if (p.sched == kDense) {
     if (lane == 0) *total_mtiles = (p.a_rows + kBM - 1) / kBM;
+    return;
+  }
+  if (p.sched == kSegments) {
+    if (lane == 0) *total_mtiles = __ldg(p.group_info);
     return;
   }
   bool bad = false;

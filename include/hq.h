@@ -220,6 +220,24 @@ int hq_gemm_grouped_contig(const void *a, const uint8_t *sfa, const void *b, con
                            const hq_bf16 *bias, hq_bf16 *out, int64_t m_rows, int64_t n,
                            int64_t k, hq_mode mode, int sm_count, hq_stream_t s);
 
+/* HALOps "GEMM" API, group_contiguous_gemm in its own form: rows of all
+ * experts packed contiguously without per-expert padding, expert_ids[m]
+ * (device int32 [m_rows], non-decreasing) naming the expert of row m.  A
+ * 128-row tile that holds rows of several experts is computed once per
+ * expert, each pass writing only that expert's rows.  A row whose id is
+ * outside [0, L), or below the id of the row before it, is not written and
+ * sets HQ_STATUS_BAD_OFFSETS.  workspace: caller-owned device memory of
+ * hq_gemm_grouped_rows_workspace_size(m_rows, L) bytes, 256-byte aligned (it
+ * holds the list of (tile, expert, row range) segments a preparatory kernel
+ * builds; at most 2 * ceil(m_rows / 128) + L segments, beyond which - only
+ * with ids that break the order on many rows - later rows are not written).
+ * Other arguments as hq_gemm_grouped_contig. */
+int hq_gemm_grouped_rows(const void *a, const uint8_t *sfa, const void *b, const uint8_t *sfb,
+                         const int32_t *expert_ids, int L, const float *alpha, const hq_bf16 *bias,
+                         hq_bf16 *out, int64_t m_rows, int64_t n, int64_t k, hq_mode mode,
+                         void *workspace, size_t ws_bytes, int sm_count, hq_stream_t s);
+size_t hq_gemm_grouped_rows_workspace_size(int64_t m_rows, int L);
+
 /* HALOps "GEMM" API, group_masked_gemm: a [E * max_m, k] with expert e's rows
  * at e * max_m; masked_m (device int32 [E]) valid rows per expert; only rows
  * e * max_m + i, i < masked_m[e], are computed and written -- every other

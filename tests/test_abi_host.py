@@ -119,6 +119,21 @@ def test_swiglu_and_dswiglu_reject_bad_arguments(lib):
     assert d(*args) == _abi.HQ_ERR_INVALID
 
 
+def test_grouped_rows_rejects_bad_arguments(lib):
+    f = lib.hq_gemm_grouped_rows
+    ws = hq.hq_gemm_grouped_rows_workspace_size(1000, 8)
+    assert ws % 256 == 0 and ws >= 16 + 16 * (2 * 8 + 8)
+    W = ctypes.c_void_p(0x10000)
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 8, None, None, FAKE, 1000, 128, 128, 0, W, ws, -1, None) == \
+        _abi.HQ_ERR_INVALID                                              # no ids
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 8, None, None, FAKE, 1000, 128, 128, 0, W, ws - 256, -1, None) == \
+        _abi.HQ_ERR_INVALID                                              # workspace too small
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 8, FAKE, None, FAKE, 1000, 128, 256, 1, W, ws, -1, None) == \
+        _abi.HQ_ERR_UNSUPPORTED                                          # alpha with MXFP4
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, 8, None, None, FAKE, 0, 128, 128, 0, None, 0, -1, None) == \
+        _abi.HQ_OK                                                       # no rows
+
+
 def test_permute_rejects_bad_arguments(lib):
     f = lib.hq_prefill_permute
     ws = hq.hq_prefill_permute_workspace_size(300, 8)

@@ -180,6 +180,59 @@ def test_grouped_contig_batch_equivalence(cuda_dev):
     assert torch.equal(o1, o2) and torch.equal(o1, o3)
 
 
+def rows_case(ids, n, k, mode, L, tile_n=0, alpha=None, bias=False, seed=0, expect_bad=False):
+    """Per-row expert ids (HALOps group_contiguous_gemm form) vs the oracle."""
+    hq.set_gemm_tile_n(tile_n)
+    ids = np.asarray(ids, dtype=np.int32)
+    M = len(ids)
+    a = bf16_rows(M, k, seed, spread=1)
+    w = torch.stack([bf16_rows(n, k, seed + 10 + e, std=0.03) for e in range(L)])
+    qa, sfa, qa_np, sfa_np = oracle_quant_to_device(a, mode)
+    qb, sfb, b_deq = stacked_weights_to_device(w, mode)
+    al = torch.tensor(alpha, dtype=torch.float32, device="cuda") if alpha is not None else None
+    bi = torch.stack([bf16_rows(1, n, seed + 50 + e).view(n) for e in range(L)]).cuda() if bias else None
+    out = sentinel_bf16((M, n))
+    hq.get_device_status(clear=True)
+    hq.hq_gemm_grouped_rows(qa, sfa, qb, sfb, torch.from_numpy(ids).cuda(), L, M, n, k, mode,
+                            alpha=al, bias=bi, out=out)
+    torch.cuda.synchronize()
+    status, _ = hq.get_device_status(clear=True)
+    ref, mag, written = ogemm.grouped_rows(oquant.dequantize(qa_np, sfa_np, mode), b_deq, ids,
+                                           alpha=alpha, bias=None if bi is None else np_f32(bi))
+    w_rows = np.nonzero(written)[0]
+    assert_gemm_close(out[torch.from_numpy(w_rows).cuda()], ref[w_rows], mag[w_rows], f"rows {mode}")
+    assert_rows_untouched(out, written, "rows")
+    assert bool(status & hq.HQ_STATUS_BAD_OFFSETS) == expect_bad
+
+
+@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4", "mxfp4"])
+def test_grouped_rows_unpadded_groups(cuda_dev, tile_n, mode):
+    # groups of 100, 0, 37, 300 and 3 rows: boundaries fall inside 128-row tiles
+    ids = np.repeat([0, 2, 3, 4], [100, 37, 300, 3])
+    L = 5
+    alpha = None if mode == "mxfp4" else [0.5, 3.0, 1.0, 2.0, 0.75]
+    rows_case(ids, 256, 256, mode, L, tile_n, alpha=alpha, bias=(mode == "mxfp8"), seed=21)
+
+
+def test_grouped_rows_many_experts_in_one_tile(cuda_dev):
+    ids = np.repeat(np.arange(40), 3)                 # 120 rows, 40 experts in one tile
+    rows_case(ids, 128, 128, "mxfp8", 40, 128, seed=22)
+
+
+def test_grouped_rows_padded_layout_matches_contig(cuda_dev):
+    """A padded layout given as per-row ids equals the padded-offsets form."""
+    ids = np.repeat([0, 1, 1, 2], 256)
+    rows_case(ids, 256, 256, "nvfp4", 3, 0, alpha=[1.0, 0.5, 2.0], seed=23)
+
+
+def test_grouped_rows_bad_ids_flagged_and_skipped(cuda_dev):
+    ids = np.repeat([0, 1, 2], [130, 130, 130])
+    ids[5] = 7                                        # out of range
+    ids[200] = 0                                      # below the previous id
+    rows_case(ids, 128, 128, "mxfp8", 3, 128, seed=24, expect_bad=True)
+
+
 def masked_case(masked, max_m, n, k, mode, tile_n=0, alpha=None, seed=0):
     hq.set_gemm_tile_n(tile_n)
     E = len(masked)
