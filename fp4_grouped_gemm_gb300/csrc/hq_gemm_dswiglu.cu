@@ -229,37 +229,64 @@ __global__ void __maxnreg__(96)
       if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
       if (!chunk_ok) continue;
       float dg[32], di[32];
-      float dprob_part = 0.0f;
+      // per element pair (2i, 2i+1), in packed f32x2 arithmetic; dprob is
+      // accumulated pairwise and the two halves added at the end
+      float dp0 = 0.0f, dp1 = 0.0f;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        // element pair (2i, 2i+1): gate words in cv[0..3], input words in cv[4..7]
+        // gate words cv[0..15], input words cv[16..31] (as 32-bit words)
         const uint32_t gw = reinterpret_cast<const uint32_t*>(cv)[i];
         const uint32_t iw = reinterpret_cast<const uint32_t*>(cv)[16 + i];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float R = __fmul_rn(a2, __uint_as_float(r[2 * i + h]));
-          const float rp = __fmul_rn(R, prob);
-          if (ACT == kSwiGLU) {
-            const float gate = __fmul_rn(beta, h ? bf16_hi(gw) : bf16_lo(gw));
-            const float inp = __fmul_rn(beta, h ? bf16_hi(iw) : bf16_lo(iw));
-            const float s = rcp_approx(__fadd_rn(1.0f, expf(-gate)));  // sigmoid(gate)
-            dg[2 * i + h] = rp * inp * s * (1.0f + gate * (1.0f - s));
-            di[2 * i + h] = rp * gate * s;
-            dprob_part += R * gate * s * inp;
-          } else {
-            // clamped GeGLU: gate <= 7, up in [-7, 7], s = sigmoid(1.702 gate_c),
-            // gradients kept at equality with the bounds, linear offset 1
-            const float gate = h ? bf16_hi(gw) : bf16_lo(gw);
-            const float up = h ? bf16_hi(iw) : bf16_lo(iw);
-            const float gc = fminf(gate, 7.0f);
-            const float uc = fminf(fmaxf(up, -7.0f), 7.0f);
-            const float s = rcp_approx(__fadd_rn(1.0f, expf(-1.702f * gc)));
-            dg[2 * i + h] = gate <= 7.0f ? rp * (uc + 1.0f) * s * (1.0f + 1.702f * gc * (1.0f - s)) : 0.0f;
-            di[2 * i + h] = (up >= -7.0f && up <= 7.0f) ? rp * gc * s : 0.0f;
-            dprob_part += R * gc * s * (uc + 1.0f);
-          }
+        float R0, R1, rp0, rp1;
+        mul_f32x2(R0, R1, __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), a2);
+        mul_f32x2(rp0, rp1, R0, R1, prob);
+        if (ACT == kSwiGLU) {
+          float g0, g1, x0, x1;
+          mul_f32x2(g0, g1, bf16_lo(gw), bf16_hi(gw), beta);
+          mul_f32x2(x0, x1, bf16_lo(iw), bf16_hi(iw), beta);
+          const float s0 = rcp_approx(__fadd_rn(1.0f, __expf(-g0)));  // sigmoid(gate)
+          const float s1 = rcp_approx(__fadd_rn(1.0f, __expf(-g1)));
+          float om0, om1, t0, t1, gs0, gs1, u0, u1;
+          fma_f32x2(om0, om1, s0, s1, -1.0f, -1.0f, 1.0f, 1.0f);      // 1 - s
+          fma_f32x2(t0, t1, g0, g1, om0, om1, 1.0f, 1.0f);            // 1 + gate (1 - s)
+          mul2_f32x2(gs0, gs1, g0, g1, s0, s1);                       // gate s
+          mul2_f32x2(u0, u1, rp0, rp1, x0, x1);                       // R prob input
+          mul2_f32x2(u0, u1, u0, u1, s0, s1);
+          mul2_f32x2(dg[2 * i], dg[2 * i + 1], u0, u1, t0, t1);
+          mul2_f32x2(di[2 * i], di[2 * i + 1], rp0, rp1, gs0, gs1);
+          float q0, q1;
+          mul2_f32x2(q0, q1, R0, R1, gs0, gs1);
+          fma_f32x2(dp0, dp1, q0, q1, x0, x1, dp0, dp1);             // += R gate s input
+        } else {
+          // clamped GeGLU: gate <= 7, up in [-7, 7], s = sigmoid(1.702 gate_c),
+          // gradients kept at equality with the bounds, linear offset 1
+          const float g0 = bf16_lo(gw), g1 = bf16_hi(gw);
+          const float x0 = bf16_lo(iw), x1 = bf16_hi(iw);
+          const float gc0 = fminf(g0, 7.0f), gc1 = fminf(g1, 7.0f);
+          const float uc0 = fminf(fmaxf(x0, -7.0f), 7.0f), uc1 = fminf(fmaxf(x1, -7.0f), 7.0f);
+          float kg0, kg1;
+          mul_f32x2(kg0, kg1, gc0, gc1, 1.702f);
+          const float s0 = rcp_approx(__fadd_rn(1.0f, __expf(-kg0)));
+          const float s1 = rcp_approx(__fadd_rn(1.0f, __expf(-kg1)));
+          float om0, om1, t0, t1, up0, up1, gs0, gs1, w0, w1, a0, a1, b0, b1;
+          fma_f32x2(om0, om1, s0, s1, -1.0f, -1.0f, 1.0f, 1.0f);      // 1 - s
+          fma_f32x2(t0, t1, kg0, kg1, om0, om1, 1.0f, 1.0f);          // 1 + 1.702 gate_c (1 - s)
+          add_f32x2(up0, up1, uc0, uc1, 1.0f, 1.0f);                  // up_c + 1
+          mul2_f32x2(gs0, gs1, gc0, gc1, s0, s1);                     // gate_c s
+          mul2_f32x2(w0, w1, rp0, rp1, up0, up1);
+          mul2_f32x2(w0, w1, w0, w1, s0, s1);
+          mul2_f32x2(a0, a1, w0, w1, t0, t1);
+          mul2_f32x2(b0, b1, rp0, rp1, gs0, gs1);
+          dg[2 * i] = g0 <= 7.0f ? a0 : 0.0f;
+          dg[2 * i + 1] = g1 <= 7.0f ? a1 : 0.0f;
+          di[2 * i] = (x0 >= -7.0f && x0 <= 7.0f) ? b0 : 0.0f;
+          di[2 * i + 1] = (x1 >= -7.0f && x1 <= 7.0f) ? b1 : 0.0f;
+          float q0, q1;
+          mul2_f32x2(q0, q1, R0, R1, gs0, gs1);
+          fma_f32x2(dp0, dp1, q0, q1, up0, up1, dp0, dp1);           // += R gate_c s (up_c + 1)
         }
       }
+      const float dprob_part = dp0 + dp1;
       if (row_ok) {
         uint32_t w[32];
 #pragma unroll

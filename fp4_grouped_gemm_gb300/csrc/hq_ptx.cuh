@@ -360,6 +360,23 @@ __device__ __forceinline__ void add_f32x2(float& o0, float& o1, float x0, float 
       : "f"(x0), "f"(x1), "f"(y0), "f"(y1));
 }
 
+// General pair forms: (o0, o1) = (a0 * b0, a1 * b1) and
+// (o0, o1) = (a0 * b0 + c0, a1 * b1 + c1) (one rounding, as fmaf).
+__device__ __forceinline__ void mul2_f32x2(float& o0, float& o1, float a0, float a1, float b0,
+                                           float b1) {
+  asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(o0), "=f"(o1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void fma_f32x2(float& o0, float& o1, float a0, float a1, float b0,
+                                          float b1, float c0, float c1) {
+  asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "mov.b64 c, {%6, %7};\n\tfma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(o0), "=f"(o1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
 // Two floats -> two E4M3 bytes: `hi` in bits 15..8, `lo` in bits 7..0.
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
   uint16_t r;
