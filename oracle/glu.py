@@ -34,6 +34,12 @@ Readings (also listed in the design notes):
   D2  dbias sums the float values of D_row before their BF16 rounding.
   D3  dGeGLU masks multiply by 0/1 (the value-bearing "filter" of the first
       formula listing is read as the mask of the second).
+  Q1  Block-scaled contract, Step 3 (FP8 D_row): per row and 32 consecutive
+      D_row columns, s = fp32(fp32(norm_const * amax) * fp32(1/448)),
+      SFD_row = UE8M0 s rounded up to a power of two (R2 of oracle.quant),
+      D_q = E4M3(fp32(D * norm_const) * 2^(127 - SFD_row)).  The D values are
+      the float32 values the epilogue computed (each a correctly rounded
+      restatement of the closed form here).
 """
 
 import numpy as np
@@ -278,3 +284,19 @@ def dswiglu(a, b, c, padded_offsets, alpha, beta, prob):
         "dbias": dbias_from_D(D, grp, L), "dbias_mag": dbias_from_D(np.abs(D), grp, L),
         "D_mag": magR2 * mult, "written": written, "group": grp,
     }
+
+
+def quantize_rows_fp8(D, norm_const=1.0):
+    """Step-3 row quantisation of D [rows, cols] (cols % 32 == 0) under Q1.
+
+    Returns (codes uint8 [rows, cols] E4M3, sf uint8 [rows, cols / 32]).
+    """
+    D = np.asarray(D, dtype=np.float32)
+    rows, cols = D.shape
+    g = np.float32(norm_const)
+    amax = np.max(np.abs(D.reshape(rows, cols // 32, 32)), axis=2)
+    sf = quant.scale_byte_mxfp8(amax, g)
+    y = (D * g).astype(np.float32).astype(np.float64)          # fp32 product
+    mult = np.ldexp(1.0, 127 - sf.astype(np.int64))
+    codes = formats.encode_e4m3(y.reshape(rows, cols // 32, 32) * mult[..., None])
+    return codes.reshape(rows, cols), sf

@@ -216,3 +216,26 @@ def test_dgeglu_full_groups_match_epilogue_and_tail():
     gc, ic = glu.interleave_columns(N)
     ratio_g = np.abs(out["D"][:512, gc]) - np.abs(R[:512]) * glu.dgeglu_mult_mag(c, prob)[:512, gc]
     assert (ratio_g <= 1e-12).all()
+
+
+def test_row_quantiser_unit_norm_equals_the_mxfp8_quantiser():
+    # norm_const = 1 is exactly the group-wise MXFP8 quantiser on float32 rows
+    r = rng_(11)
+    D = (r.standard_normal((6, 128)) * np.exp2(r.integers(-20, 20, (6, 1)))).astype(np.float32)
+    codes, sf = glu.quantize_rows_fp8(D, 1.0)
+    q_ref, sf_ref = quant.quantize(D, "mxfp8")
+    assert np.array_equal(codes, q_ref) and np.array_equal(sf, sf_ref)
+
+
+def test_row_quantiser_norm_const_by_hand():
+    # norm_const 4, amax 112: s = 4 * 112 / 448 = 1 exactly -> byte 127;
+    # D * 4 = 448 -> E4M3 0x7E; -28 * 4 = -112 = -1.75 * 2^6 -> sign | exponent 13 | mantissa 6 = 0xEE
+    D = np.zeros((1, 32), np.float32)
+    D[0, 0], D[0, 1] = 112.0, -28.0
+    codes, sf = glu.quantize_rows_fp8(D, 4.0)
+    assert sf[0, 0] == 127
+    assert codes[0, 0] == 0x7E and codes[0, 1] == 0xEE
+    # one ulp above the power of two rounds the scale up
+    D[0, 0] = np.nextafter(np.float32(112.0), np.float32(200.0))
+    _, sf = glu.quantize_rows_fp8(D, 4.0)
+    assert sf[0, 0] == 128
