@@ -551,6 +551,19 @@ class Extras:
                                                   dbias=dbias, d_row=d_row, workspace=ws_t), 20, self.flush)
         res["dgeglu_bwd_L16"] = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_bf16": fl / t / 1e12 / self.p_bf16,
                                  "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / self.hbm}
+        # block-scaled contract on the same shapes: MXFP8 operands, FP8 D_row + SFD_row
+        qa, sfa = hq.hq_quant(c5["a"], "mxfp8")
+        qb, sfb = hq.hq_quant(c5["b"].view(L * n, k), "mxfp8")
+        qb = qb.view(L, n, k)
+        d8 = torch.empty(M, 2 * n, dtype=torch.uint8, device=dev)
+        sfd = torch.empty(hq.sf_bytes(M, 2 * n, "mxfp8"), dtype=torch.uint8, device=dev)
+        t = time_kernel(lambda: hq.hq_gemm_dglu_bs(qa, sfa, qb, sfb, c5["c"], off, c5["alpha"], c5["prob"], dprob,
+                                                   k, "mxfp8", beta=c5["beta"], dbias=dbias, d_row=d8,
+                                                   fp8_out=True, sfd_row=sfd, workspace=ws_t), 20, self.flush)
+        byts8 = M * k + L * n * k + M * 2 * n * 2 + M * 2 * n + sfd.numel() + M * 8
+        res["dswiglu_bwd_mxfp8_fp8out_L16"] = {"us": t * 1e6, "tflops": fl / t / 1e12,
+                                               "frac_fp8": fl / t / 1e12 / self.p_fp8,
+                                               "gbs": byts8 / t / 1e9, "frac_hbm": byts8 / t / 1e9 / self.hbm}
         return res
 
 

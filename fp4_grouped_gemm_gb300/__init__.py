@@ -22,7 +22,7 @@ __all__ = [
     "hq_gemm_dense", "hq_gemm_grouped_contig", "hq_gemm_grouped_masked", "hq_swiglu_quant",
     "hq_gemm_dswiglu", "hq_gemm_dswiglu_workspace_size", "hq_gemm_dgeglu", "swiglu_kb_dim",
     "hq_prefill_permute", "hq_prefill_permute_workspace_size", "hq_gemm_grouped_rows",
-    "hq_gemm_grouped_rows_workspace_size",
+    "hq_gemm_grouped_rows_workspace_size", "hq_gemm_dglu_bs",
 ]
 
 _MODES = {"mxfp8": HQ_MXFP8, "w8a8-mxfp8": HQ_MXFP8, "mxfp4": HQ_MXFP4, "w4a4-mxfp4": HQ_MXFP4,
@@ -288,3 +288,31 @@ def hq_prefill_permute(x, scale, topk_ids, num_experts, max_token_num, permute_x
                                         _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "hq_prefill_permute")
     return permute_x, out_scale, indice_map, token_nums
+
+
+def hq_gemm_dglu_bs(a, sfa, b, sfb, c, padded_offsets, alpha, prob, dprob, k, mode, act="dswiglu",
+                    beta=None, dbias=None, d_row=None, fp8_out=False, sfd_row=None, norm_const=None,
+                    workspace=None, sm_count=-1, stream=None):
+    """Block-scaled grouped GEMM + dSwiGLU / dGeGLU backward (cuDNN block-scaled
+    contract).  a, b quantised as hq_quant writes them (b stacked [L, n, k]);
+    c [m, 2n] BF16.  With fp8_out the D_row is E4M3 with UE8M0 SfAtom scales
+    (sfd_row) and optional norm_const.  Returns (d_row, sfd_row, dprob, dbias)."""
+    m, two_n = c.shape
+    n = two_n // 2
+    L = padded_offsets.numel()
+    dev = c.device
+    if d_row is None:
+        d_row = torch.empty(m, two_n, dtype=torch.uint8 if fp8_out else torch.bfloat16, device=dev)
+    if fp8_out and sfd_row is None:
+        sfd_row = torch.empty(max(sf_bytes(m, two_n, "mxfp8"), 1), dtype=torch.uint8, device=dev)
+    ws_bytes = hq_gemm_dswiglu_workspace_size(L, n)
+    if dbias is not None and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    acts = {"dswiglu": 0, "dgeglu": 1}
+    rc = _abi.load().hq_gemm_dglu_bs(
+        _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(padded_offsets), L, _ptr(alpha),
+        _ptr(beta), _ptr(prob), acts[act], _ptr(d_row), _ptr(sfd_row if fp8_out else None),
+        _ptr(norm_const), _ptr(dprob), _ptr(dbias), m, n, k, mode_id(mode), _ptr(workspace),
+        0 if workspace is None else workspace.numel(), sm_count, _stream(stream))
+    _check(rc, "hq_gemm_dglu_bs")
+    return d_row, (sfd_row if fp8_out else None), dprob, dbias

@@ -55,7 +55,19 @@ struct GemmParams {
   int64_t S;                 // scale columns = k / group
   int64_t sfb_group_bytes;   // ceil(n/128)*128*S
   uint64_t wait_limit_ns;
+  // dGLU epilogues only (cuDNN "Grouped GEMM + dGLU (SM100)", block-scaled
+  // contract): out is not used; D_row = dGLU(alpha_g^2 acc, C) instead
+  const uint16_t* c;         // [a_rows, 2n] BF16 forward intermediate
+  const float* beta;         // [groups] (dSwiGLU)
+  const float* prob;         // [a_rows]
+  float* dprob;              // [a_rows], accumulated
+  float* dbias_ws;           // [groups, 2n] float32 partial sums, or null
+  uint8_t* d_row;            // [a_rows, 2n]: BF16, or E4M3 when sfd_row is set
+  uint8_t* sfd_row;          // SfAtom UE8M0 scales of D_row, [ceil(a_rows/128)*128, 2n/32], or null
+  const float* norm_const;   // FP8 D_row norm_const (device [1]) or null (= 1)
 };
+
+enum Epi : int { kEpiGemm = 0, kEpiDSwiGLU = 1, kEpiDGeGLU = 2 };
 
 // TABLE: entries of the per-CTA group table (0 for the dense GEMM, which
 // needs none and spends the shared memory on a deeper pipeline instead).
@@ -219,7 +231,155 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& e, Release release)
   }
 }
 
-template <int MODE, int BN, int STAGES, int ACC, int TABLE>
+// ---------------------------------------------------------------------------
+// dGLU epilogue of one 32-column chunk (compact columns [j0, j0 + 32)) for the
+// calling thread's row: R = a2 * acc, C's 32 gate and 32 input values of the
+// row, D_row written at the same 64 columns (BF16, or E4M3 with two UE8M0
+// scale bytes), the row's dprob partial added, and, when requested, the
+// warp's column sums of D added to the dbias workspace.
+//   dSwiGLU: X = beta C, s = sigmoid(gate)
+//     dgate = R prob input s (1 + gate (1 - s)),  dinput = R prob gate s,
+//     dprob += R gate s input
+//   dGeGLU:  gate_c = min(gate, 7), up_c = clamp(up, -7, 7), s = sigmoid(1.702 gate_c)
+//     dgate = R prob (up_c + 1) s (1 + 1.702 gate_c (1 - s)) [gate <= 7]
+//     dup   = R prob gate_c s [-7 <= up <= 7],  dprob += R gate_c s (up_c + 1)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float dglu_bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float dglu_bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float dglu_rcp(float x) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+template <int EPI>
+__device__ __forceinline__ void dglu_chunk(const GemmParams& p, const uint32_t (&r)[32],
+                                           const uint4 (&cv)[8], bool row_ok, int64_t row,
+                                           int64_t j0, int g, float a2, float beta, float prob,
+                                           float norm, int lane) {
+  float dg[32], di[32];
+  float dp0 = 0.0f, dp1 = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t gw = reinterpret_cast<const uint32_t*>(cv)[i];
+    const uint32_t iw = reinterpret_cast<const uint32_t*>(cv)[16 + i];
+    float R0, R1, rp0, rp1;
+    mul_f32x2(R0, R1, __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), a2);
+    mul_f32x2(rp0, rp1, R0, R1, prob);
+    if (EPI == kEpiDSwiGLU) {
+      float g0, g1, x0, x1;
+      mul_f32x2(g0, g1, dglu_bf16_lo(gw), dglu_bf16_hi(gw), beta);
+      mul_f32x2(x0, x1, dglu_bf16_lo(iw), dglu_bf16_hi(iw), beta);
+      const float s0 = dglu_rcp(__fadd_rn(1.0f, __expf(-g0)));
+      const float s1 = dglu_rcp(__fadd_rn(1.0f, __expf(-g1)));
+      float om0, om1, t0, t1, gs0, gs1, u0, u1, q0, q1;
+      fma_f32x2(om0, om1, s0, s1, -1.0f, -1.0f, 1.0f, 1.0f);
+      fma_f32x2(t0, t1, g0, g1, om0, om1, 1.0f, 1.0f);
+      mul2_f32x2(gs0, gs1, g0, g1, s0, s1);
+      mul2_f32x2(u0, u1, rp0, rp1, x0, x1);
+      mul2_f32x2(u0, u1, u0, u1, s0, s1);
+      mul2_f32x2(dg[2 * i], dg[2 * i + 1], u0, u1, t0, t1);
+      mul2_f32x2(di[2 * i], di[2 * i + 1], rp0, rp1, gs0, gs1);
+      mul2_f32x2(q0, q1, R0, R1, gs0, gs1);
+      fma_f32x2(dp0, dp1, q0, q1, x0, x1, dp0, dp1);
+    } else {
+      const float g0 = dglu_bf16_lo(gw), g1 = dglu_bf16_hi(gw);
+      const float x0 = dglu_bf16_lo(iw), x1 = dglu_bf16_hi(iw);
+      const float gc0 = fminf(g0, 7.0f), gc1 = fminf(g1, 7.0f);
+      const float uc0 = fminf(fmaxf(x0, -7.0f), 7.0f), uc1 = fminf(fmaxf(x1, -7.0f), 7.0f);
+      float kg0, kg1;
+      mul_f32x2(kg0, kg1, gc0, gc1, 1.702f);
+      const float s0 = dglu_rcp(__fadd_rn(1.0f, __expf(-kg0)));
+      const float s1 = dglu_rcp(__fadd_rn(1.0f, __expf(-kg1)));
+      float om0, om1, t0, t1, up0, up1, gs0, gs1, w0, w1, a0, a1, b0, b1, q0, q1;
+      fma_f32x2(om0, om1, s0, s1, -1.0f, -1.0f, 1.0f, 1.0f);
+      fma_f32x2(t0, t1, kg0, kg1, om0, om1, 1.0f, 1.0f);
+      add_f32x2(up0, up1, uc0, uc1, 1.0f, 1.0f);
+      mul2_f32x2(gs0, gs1, gc0, gc1, s0, s1);
+      mul2_f32x2(w0, w1, rp0, rp1, up0, up1);
+      mul2_f32x2(w0, w1, w0, w1, s0, s1);
+      mul2_f32x2(a0, a1, w0, w1, t0, t1);
+      mul2_f32x2(b0, b1, rp0, rp1, gs0, gs1);
+      dg[2 * i] = g0 <= 7.0f ? a0 : 0.0f;
+      dg[2 * i + 1] = g1 <= 7.0f ? a1 : 0.0f;
+      di[2 * i] = (x0 >= -7.0f && x0 <= 7.0f) ? b0 : 0.0f;
+      di[2 * i + 1] = (x1 >= -7.0f && x1 <= 7.0f) ? b1 : 0.0f;
+      mul2_f32x2(q0, q1, R0, R1, gs0, gs1);
+      fma_f32x2(dp0, dp1, q0, q1, up0, up1, dp0, dp1);
+    }
+  }
+  const int64_t two_n = 2 * p.n;
+  if (row_ok) {
+    if (!p.sfd_row) {
+      uint4* dst = reinterpret_cast<uint4*>(p.d_row + (row * two_n + 2 * j0) * 2);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float* v = u < 4 ? dg + 8 * u : di + 8 * (u - 4);
+        __nv_bfloat162 b0 = __floats2bfloat162_rn(v[0], v[1]), b1 = __floats2bfloat162_rn(v[2], v[3]),
+                       b2 = __floats2bfloat162_rn(v[4], v[5]), b3 = __floats2bfloat162_rn(v[6], v[7]);
+        dst[u] = make_uint4(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1),
+                            *reinterpret_cast<uint32_t*>(&b2), *reinterpret_cast<uint32_t*>(&b3));
+      }
+    } else {
+      // Step 3: per 32 D_row values, s = (norm * amax) / 448 rounded up to a
+      // power of two, codes E4M3((D * norm) * 2^(127 - byte))
+      uint32_t bytes2 = 0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float* v = h == 0 ? dg : di;
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        const uint32_t byte = ue8m0_ceil(__fmul_rn(__fmul_rn(norm, amax), 1.0f / 448.0f));
+        const float mult = pow2_neg_unbiased(byte);
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t lo = cvt_e4m3x2(__fmul_rn(__fmul_rn(v[4 * i + 1], norm), mult),
+                                         __fmul_rn(__fmul_rn(v[4 * i], norm), mult));
+          const uint32_t hi = cvt_e4m3x2(__fmul_rn(__fmul_rn(v[4 * i + 3], norm), mult),
+                                         __fmul_rn(__fmul_rn(v[4 * i + 2], norm), mult));
+          w[i] = lo | (hi << 16);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(p.d_row + row * two_n + 2 * j0 + 32 * h);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        bytes2 |= byte << (8 * h);
+      }
+      // the chunk's two scale columns s, s + 1 (s even) are adjacent in the atom row
+      const int64_t S = two_n / 32, s = 2 * j0 / 32;
+      const int64_t off = ((row >> 7) * (S >> 2) + (s >> 2)) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4 + (s & 3);
+      *reinterpret_cast<uint16_t*>(p.sfd_row + off) = static_cast<uint16_t>(bytes2);
+    }
+    atomicAdd(p.dprob + row, dp0 + dp1);
+  }
+  if (p.dbias_ws) {
+    // column sums over the warp's 32 rows (butterfly reduce-scatter): lane l
+    // ends with the sums of gate column l and input column l
+    if (!row_ok) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) { dg[i] = 0.0f; di[i] = 0.0f; }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const bool upper = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < o; ++i) {
+        const float sg = upper ? dg[i] : dg[i + o];
+        const float si = upper ? di[i] : di[i + o];
+        const float kg = upper ? dg[i + o] : dg[i];
+        const float ki = upper ? di[i + o] : di[i];
+        dg[i] = kg + __shfl_xor_sync(0xFFFFFFFFu, sg, o);
+        di[i] = ki + __shfl_xor_sync(0xFFFFFFFFu, si, o);
+      }
+    }
+    float* ws = p.dbias_ws + static_cast<int64_t>(g) * two_n + 2 * j0;
+    atomicAdd(ws + lane, dg[0]);
+    atomicAdd(ws + 32 + lane, di[0]);
+  }
+}
+
+template <int MODE, int BN, int STAGES, int ACC, int TABLE, int EPI = kEpiGemm>
 __global__ void __launch_bounds__(kThreads, 1)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
@@ -494,7 +654,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - 2;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int64_t t = blockIdx.x; t < sch.total_tiles; t += gridDim.x) {
+    if (EPI != kEpiGemm) {
+      // dGLU: the warp owns two 32-column chunks of its lane quarter; C of a
+      // chunk is loaded before its accumulator columns are read
+      static_assert(EPI == kEpiGemm || (BN == 128 && ACC == 2), "dGLU tiles are 128 wide");
+      const float norm = p.norm_const ? __ldg(p.norm_const) : 1.0f;
+      const int64_t two_n = 2 * p.n;
+      for (int64_t t = blockIdx.x; t < sch.total_tiles; t += gridDim.x) {
+        const TileInfo ti = decode_tile(p.gs, sch, t, BN);
+        const int r_local = q * 32 + lane;
+        const bool row_ok = r_local < ti.rows_valid;
+        const int64_t row = ti.row0 + r_local;
+        const float alpha = __ldg(p.alpha + ti.g);
+        const float a2 = __fmul_rn(alpha, alpha);
+        const float beta = EPI == kEpiDSwiGLU ? __ldg(p.beta + ti.g) : 1.0f;
+        const float prob = row_ok ? __ldg(p.prob + row) : 0.0f;
+        bool ok = true;
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = (ew >> 2) * 2 + cc;
+          const int64_t j0 = ti.n0 + c * 32;
+          const bool chunk_ok = j0 < p.n;
+          uint4 cv[8];
+          {
+            const bool ld = row_ok && chunk_ok;
+            const uint4* src = reinterpret_cast<const uint4*>(p.c + row * two_n + 2 * j0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) cv[i] = ld ? __ldcs(src + i) : make_uint4(0, 0, 0, 0);
+          }
+          if (cc == 0) {
+            const bool w = wait_bounded(tfull_bar(acc), acc_phase, wctx);
+            if (!__all_sync(0xFFFFFFFFu, w)) { ok = false; break; }
+            tc_fence_after();
+          }
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c * 32, r);
+          tmem_ld_wait();
+          if (cc == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+          }
+          if (chunk_ok) dglu_chunk<EPI>(p, r, cv, row_ok, row, j0, ti.g, a2, beta, prob, norm, lane);
+        }
+        if (!ok) break;
+        if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
+      }
+    }
+    for (int64_t t = blockIdx.x; EPI == kEpiGemm && t < sch.total_tiles; t += gridDim.x) {
       const TileInfo ti = decode_tile(p.gs, sch, t, BN);
       const float alpha = p.alpha ? __ldg(p.alpha + ti.g) : 1.0f;  // loaded before the wait
       // every lane waits; the warp proceeds only if all lanes saw completion
@@ -868,7 +1074,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // host side
 // ---------------------------------------------------------------------------
 
-template <int MODE, int BN, int STAGES, int ACC, int TABLE>
+template <int MODE, int BN, int STAGES, int ACC, int TABLE, int EPI = kEpiGemm>
 int run_bs(const void* a, const void* b, const GemmParams& p0, int sm_count, bool pdl,
            cudaStream_t st) {
   using C = Cfg<MODE, BN, STAGES, ACC, TABLE>;
@@ -891,7 +1097,7 @@ int run_bs(const void* a, const void* b, const GemmParams& p0, int sm_count, boo
                                strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != HQ_OK) return rc;
   }
-  auto kern = bs_gemm_kernel<MODE, BN, STAGES, ACC, TABLE>;
+  auto kern = bs_gemm_kernel<MODE, BN, STAGES, ACC, TABLE, EPI>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
       cudaSuccess)
     return HQ_ERR_CUDA;
@@ -1197,6 +1403,73 @@ int hq_gemm_grouped_contig(const void* a, const uint8_t* sfa, const void* b, con
   p.gs.group_info = padded_offsets;
   p.gs.sched = hq::kContig;
   return hq::run_gemm(mode, a, b, p, sm_count, false, reinterpret_cast<cudaStream_t>(s));
+}
+
+int hq_gemm_dglu_bs(const void* a, const uint8_t* sfa, const void* b, const uint8_t* sfb,
+                    const hq_bf16* c, const int32_t* padded_offsets, int L, const float* alpha,
+                    const float* beta, const float* prob, int act, void* d_row, uint8_t* sfd_row,
+                    const float* norm_const, float* dprob, hq_bf16* dbias, int64_t m, int64_t n,
+                    int64_t k, hq_mode mode, void* workspace, size_t ws_bytes, int sm_count,
+                    hq_stream_t s) {
+  if (act != 0 && act != 1) return HQ_ERR_INVALID;
+  if (mode != HQ_MXFP8 && mode != HQ_MXFP4 && mode != HQ_NVFP4) return HQ_ERR_INVALID;
+  const int64_t gs = mode == HQ_NVFP4 ? 16 : 32;
+  if (n <= 0 || k <= 0 || k % (4 * gs) != 0 || n % 128 != 0) return HQ_ERR_INVALID;
+  if (n > (1ll << 28) || k > (1ll << 30)) return HQ_ERR_INVALID;
+  if (m < 0 || m > (1ll << 31) - 256) return HQ_ERR_INVALID;
+  if (L < 1 || L > hq::kMaxGroups) return HQ_ERR_INVALID;
+  if (!a || !sfa || !b || !sfb || !c || !padded_offsets || !alpha || !prob || !d_row || !dprob)
+    return HQ_ERR_INVALID;
+  if (act == 0 && !beta) return HQ_ERR_INVALID;
+  if (!hq::aligned16(a) || !hq::aligned16(sfa) || !hq::aligned16(b) || !hq::aligned16(sfb) ||
+      !hq::aligned16(c) || !hq::aligned16(d_row) || (sfd_row && !hq::aligned16(sfd_row)))
+    return HQ_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(padded_offsets) | reinterpret_cast<uintptr_t>(alpha) |
+       reinterpret_cast<uintptr_t>(beta ? beta : alpha) | reinterpret_cast<uintptr_t>(prob) |
+       reinterpret_cast<uintptr_t>(dprob) |
+       reinterpret_cast<uintptr_t>(norm_const ? norm_const : alpha)) & 3u)
+    return HQ_ERR_INVALID;
+  if (norm_const && !sfd_row) return HQ_ERR_INVALID;  // norm_const belongs to the FP8 output
+  if (dbias) {
+    if (reinterpret_cast<uintptr_t>(dbias) & 1u) return HQ_ERR_INVALID;
+    if (!workspace || ws_bytes < hq_gemm_dswiglu_workspace_size(L, n)) return HQ_ERR_INVALID;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return HQ_ERR_INVALID;
+  }
+  if (m == 0) return HQ_OK;
+  hq::GemmParams p = hq::base_params(sfa, sfb, alpha, nullptr, nullptr, n, k, mode);
+  if (!p.gs.status) return HQ_ERR_CUDA;
+  p.gs.a_rows = m;
+  p.gs.groups = L;
+  p.gs.group_info = padded_offsets;
+  p.gs.sched = hq::kContig;
+  p.c = c;
+  p.beta = beta;
+  p.prob = prob;
+  p.dprob = dprob;
+  p.dbias_ws = dbias ? static_cast<float*>(workspace) : nullptr;
+  p.d_row = static_cast<uint8_t*>(d_row);
+  p.sfd_row = sfd_row;
+  p.norm_const = norm_const;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  const int64_t ws_count = static_cast<int64_t>(L) * 2 * n;
+  if (dbias && cudaMemsetAsync(workspace, 0, ws_count * sizeof(float), st) != cudaSuccess)
+    return HQ_ERR_CUDA;
+  constexpr int T = hq::kMaxGroups + 1;
+  int rc;
+  if (mode == HQ_MXFP8)
+    rc = act == 0 ? hq::run_bs<HQ_MXFP8, 128, 6, 2, T, hq::kEpiDSwiGLU>(a, b, p, sm_count, false, st)
+                  : hq::run_bs<HQ_MXFP8, 128, 6, 2, T, hq::kEpiDGeGLU>(a, b, p, sm_count, false, st);
+  else if (mode == HQ_MXFP4)
+    rc = act == 0 ? hq::run_bs<HQ_MXFP4, 128, 5, 2, T, hq::kEpiDSwiGLU>(a, b, p, sm_count, false, st)
+                  : hq::run_bs<HQ_MXFP4, 128, 5, 2, T, hq::kEpiDGeGLU>(a, b, p, sm_count, false, st);
+  else
+    rc = act == 0 ? hq::run_bs<HQ_NVFP4, 128, 5, 2, T, hq::kEpiDSwiGLU>(a, b, p, sm_count, false, st)
+                  : hq::run_bs<HQ_NVFP4, 128, 5, 2, T, hq::kEpiDGeGLU>(a, b, p, sm_count, false, st);
+  if (rc != HQ_OK) return rc;
+  if (dbias)
+    return hq::dbias_finalize(reinterpret_cast<uint16_t*>(dbias), static_cast<const float*>(workspace),
+                              ws_count, st);
+  return HQ_OK;
 }
 
 size_t hq_gemm_grouped_rows_workspace_size(int64_t m_rows, int L) {

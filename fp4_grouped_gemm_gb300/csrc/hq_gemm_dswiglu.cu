@@ -347,6 +347,17 @@ __global__ void dbias_finalize_kernel(uint16_t* dbias, const float* ws, int64_t 
 }
 
 }  // namespace
+
+int dbias_finalize(uint16_t* dbias, const float* ws, int64_t count, cudaStream_t st) {
+  const int sms = num_sms();
+  if (sms <= 0) return HQ_ERR_CUDA;
+  int64_t blocks = (count + 255) / 256;
+  if (blocks > 4 * sms) blocks = 4 * sms;
+  if (blocks < 1) blocks = 1;
+  dbias_finalize_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(dbias, ws, count);
+  return cudaGetLastError() == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
+}
+
 }  // namespace hq
 
 extern "C" {
@@ -439,12 +450,10 @@ int run_dglu(const hq_bf16* a, const hq_bf16* b, const hq_bf16* c, const int32_t
              false, tmA, tmB, p) != cudaSuccess)
     return HQ_ERR_CUDA;
   if (dbias) {
-    const int64_t count = static_cast<int64_t>(L) * 2 * n;
-    int64_t blocks = (count + 255) / 256;
-    if (blocks > 4 * sms) blocks = 4 * sms;
-    dbias_finalize_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-        reinterpret_cast<uint16_t*>(dbias), static_cast<const float*>(workspace), count);
-    if (cudaGetLastError() != cudaSuccess) return HQ_ERR_CUDA;
+    const int rc = dbias_finalize(reinterpret_cast<uint16_t*>(dbias),
+                                  static_cast<const float*>(workspace),
+                                  static_cast<int64_t>(L) * 2 * n, st);
+    if (rc != HQ_OK) return rc;
   }
   return HQ_OK;
 }

@@ -33,6 +33,10 @@ int encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, voi
                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
                       CUtensorMapSwizzle swizzle);
 
+// dbias[i] = bf16(float(dbias[i]) + ws[i]) for i < count, on stream st (the
+// final pass of the dGLU GEMMs' dbias reduction).  Returns HQ_OK or HQ_ERR_CUDA.
+int dbias_finalize(uint16_t* dbias, const float* ws, int64_t count, cudaStream_t st);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Launch with optional programmatic-dependent-launch attribute.

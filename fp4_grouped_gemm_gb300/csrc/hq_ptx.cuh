@@ -391,6 +391,24 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float hi, float lo) {
       : "f"(hi), "f"(lo));
   return r;
 }
+// UE8M0 byte: ceil(log2 s) + 127 clamped to [0, 254] for s >= 0 (0 for s == 0), from the
+// float32 bit pattern.
+__device__ __forceinline__ uint32_t ue8m0_ceil(float s) {
+  const uint32_t bits = __float_as_uint(s);
+  if (bits == 0) return 0;
+  const uint32_t e = bits >> 23, man = bits & 0x7FFFFFu;
+  if (e == 0) {  // subnormal: s = man * 2^-149
+    const int b = (32 - __clz(static_cast<int>(man - 1))) - 22;
+    return b > 0 ? static_cast<uint32_t>(b) : 0u;
+  }
+  const uint32_t b = e + (man != 0 ? 1u : 0u);
+  return b > 254u ? 254u : b;
+}
+
+__device__ __forceinline__ float pow2_neg_unbiased(uint32_t byte) {  // 2^(127 - byte)
+  return byte <= 253u ? __uint_as_float((254u - byte) << 23) : __uint_as_float(0x00400000u);
+}
+
 // Exact value of a UE4M3 scale byte (E4M3 bit pattern, sign bit ignored):
 // exponent field e, mantissa m: e == 0 -> m * 2^-9, else (1 + m/8) * 2^(e-7).
 __device__ __forceinline__ float ue4m3_value(uint32_t b) {

@@ -81,23 +81,6 @@ __device__ __forceinline__ void f16x8_to_f32(const uint4& v, float (&x)[8]) {
   }
 }
 
-// ceil(log2 s) + 127 clamped to [0, 254] for s >= 0 (0 for s == 0), from the
-// float32 bit pattern.
-__device__ __forceinline__ uint32_t ue8m0_ceil(float s) {
-  const uint32_t bits = __float_as_uint(s);
-  if (bits == 0) return 0;
-  const uint32_t e = bits >> 23, man = bits & 0x7FFFFFu;
-  if (e == 0) {  // subnormal: s = man * 2^-149
-    const int b = (32 - __clz(static_cast<int>(man - 1))) - 22;
-    return b > 0 ? static_cast<uint32_t>(b) : 0u;
-  }
-  const uint32_t b = e + (man != 0 ? 1u : 0u);
-  return b > 254u ? 254u : b;
-}
-
-__device__ __forceinline__ float pow2_neg_unbiased(uint32_t byte) {  // 2^(127 - byte)
-  return byte <= 253u ? __uint_as_float((254u - byte) << 23) : __uint_as_float(0x00400000u);
-}
 
 // One lane quantises one whole scale group of GS values x[0..GS).
 // MXFP8 writes GS E4M3 bytes to qw[0..GS/4); NVFP4 and MXFP4 write GS/2 packed

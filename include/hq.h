@@ -319,6 +319,30 @@ int hq_gemm_dgeglu(const hq_bf16 *a, const hq_bf16 *b, const hq_bf16 *c,
                    hq_bf16 *d_row, float *dprob, hq_bf16 *dbias, int64_t m, int64_t n, int64_t k,
                    void *workspace, size_t ws_bytes, int sm_count, hq_stream_t s);
 
+/* cuDNN frontend "Grouped GEMM + dGLU (SM100)", block-scaled contract:
+ * Step 1 R = alpha_g^2 * (dequantised A . dequantised B_g^T) with A, B and
+ * their SfAtom scales as hq_quant writes them (mode HQ_MXFP8, HQ_MXFP4 or
+ * HQ_NVFP4), groups contiguous in M by padded_offsets (as
+ * hq_gemm_grouped_contig); Step 2 the dGLU epilogue of hq_gemm_dswiglu
+ * (act 0) or hq_gemm_dgeglu (act 1) on the BF16 C [m, 2n]; Step 3 optional
+ * FP8 output.
+ *   d_row      sfd_row == NULL: BF16 [m, 2n].  Otherwise E4M3 [m, 2n] bytes
+ *              with sfd_row the UE8M0 scales of every 32 consecutive D_row
+ *              values of a row (SfAtom layout, ceil(m/128)*128 rows, 2n/32
+ *              columns): SF = norm_const * amax * (1/448) rounded up to a
+ *              power of two, D_q = E4M3(D * norm_const / SF)
+ *   norm_const device float [1] or NULL (= 1); only with sfd_row
+ *   alpha, beta, prob, dprob, dbias, workspace as hq_gemm_dswiglu (beta
+ *              ignored and may be NULL for act 1)
+ * Requires n % 128 == 0 and k % (4 * group) == 0.  The column-quantised
+ * D_col / SFD_col outputs of the page are not produced. */
+int hq_gemm_dglu_bs(const void *a, const uint8_t *sfa, const void *b, const uint8_t *sfb,
+                    const hq_bf16 *c, const int32_t *padded_offsets, int L, const float *alpha,
+                    const float *beta, const float *prob, int act, void *d_row, uint8_t *sfd_row,
+                    const float *norm_const, float *dprob, hq_bf16 *dbias, int64_t m, int64_t n,
+                    int64_t k, hq_mode mode, void *workspace, size_t ws_bytes, int sm_count,
+                    hq_stream_t s);
+
 /* ------------------------------------------------------------------------- *
  * hq_gemm_dswiglu without caller-provided scratch.  The paper has no
  * counterpart to this entry point; it exists for callers that cannot

@@ -1,0 +1,107 @@
+"""GPU parity of the block-scaled grouped GEMM + dGLU backward (cuDNN
+block-scaled contract) against the oracle: Step 1 on the oracle's dequantised
+operands, Step 2 the dSwiGLU / dGeGLU closed forms, Step 3 the FP8 row
+quantisation (reading Q1).
+
+BF16 D_row, dprob and dbias use the BF16 dGLU tolerances.  FP8 D_row: every
+scale byte within one step of the oracle's byte for the exact D (equal except
+where the group maximum sits at a power-of-two boundary), and the dequantised
+values within an E4M3 half-step of D plus the D tolerance.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import fp4_grouped_gemm_gb300 as hq
+from oracle import formats, glu
+from oracle import quant as oquant
+
+from gpu_util import (assert_rows_untouched, bf16_rows, np_f32, oracle_quant_to_device,
+                      sentinel_bf16, stacked_weights_to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+def bf16_ulp(x):
+    a = np.abs(x)
+    e = np.floor(np.log2(np.where(a > 0, a, 1e-300)))
+    return np.where(a > 0, 2.0 ** (e - 7), 2.0 ** -133)
+
+
+def run(mode, act, offsets, m, n, k, seed, fp8=False, norm=None, with_dbias=True):
+    L = len(offsets)
+    dev = torch.device("cuda")
+    a = bf16_rows(m, k, seed)
+    w = torch.stack([bf16_rows(n, k, seed + 1 + e, std=0.05) for e in range(L)])
+    c = bf16_rows(m, 2 * n, seed + 40, std=2.0 if act == "dswiglu" else 5.0)
+    gen = torch.Generator().manual_seed(seed)
+    prob = 1.0 - torch.rand(m, generator=gen)
+    alpha = 0.8 + 0.4 * torch.rand(L, generator=gen)
+    beta = 0.8 + 0.4 * torch.rand(L, generator=gen)
+    qa, sfa, qa_np, sfa_np = oracle_quant_to_device(a, mode)
+    qb, sfb, b_deq = stacked_weights_to_device(w, mode)
+    a_deq = oquant.dequantize(qa_np, sfa_np, mode)
+    dprob = torch.zeros(m, dtype=torch.float32, device=dev)
+    dbias = torch.zeros(L, 2 * n, dtype=torch.bfloat16, device=dev) if with_dbias else None
+    d_row = (torch.full((m, 2 * n), 0x5A, dtype=torch.uint8, device=dev) if fp8 else sentinel_bf16((m, 2 * n)))
+    nc = torch.tensor([norm], dtype=torch.float32, device=dev) if norm is not None else None
+    off = torch.tensor(offsets, dtype=torch.int32, device=dev)
+    d_row, sfd, dprob, dbias = hq.hq_gemm_dglu_bs(
+        qa, sfa, qb, sfb, c.to(dev), off, alpha.to(dev), prob.to(dev), dprob, k, mode, act=act,
+        beta=beta.to(dev) if act == "dswiglu" else None, dbias=dbias, d_row=d_row, fp8_out=fp8,
+        norm_const=nc)
+    torch.cuda.synchronize()
+    if act == "dswiglu":
+        ref = glu.dswiglu(a_deq, b_deq, np_f32(c), offsets, alpha.numpy(), beta.numpy(), prob.numpy())
+    else:
+        ref = glu.dgeglu(a_deq, b_deq, np_f32(c), offsets, alpha.numpy(), prob.numpy())
+    return ref, d_row, sfd, dprob, dbias
+
+
+def check_common(ref, dprob, dbias):
+    w = ref["written"]
+    dp = dprob.cpu().numpy().astype(np.float64)
+    assert (np.abs(dp - ref["dprob"]) <= 1e-3 * ref["dprob_mag"] + 1e-30)[w].all(), "dprob"
+    assert not dp[~w].any()
+    if dbias is not None:
+        db = dbias.float().cpu().numpy().astype(np.float64)
+        assert (np.abs(db - ref["dbias"]) <= 1e-3 * ref["dbias_mag"] + bf16_ulp(ref["dbias"])).all(), "dbias"
+
+
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4", "mxfp4"])
+@pytest.mark.parametrize("act", ["dswiglu", "dgeglu"])
+def test_dglu_bs_bf16_out(cuda_dev, mode, act):
+    offsets = [256, 256, 768, 1024]          # empty group 1; rows >= 1024 untouched
+    ref, d_row, _, dprob, dbias = run(mode, act, offsets, 1152, 256, 256, seed=7)
+    w = ref["written"]
+    D = d_row.float().cpu().numpy().astype(np.float64)
+    tol = 2.0 ** -8 * np.abs(ref["D"]) + 2.0 ** -20 * ref["D_mag"] + 1e-30
+    bad = (np.abs(D - ref["D"]) > tol) & w[:, None]
+    assert not bad.any(), f"{int(bad.sum())} bad D_row values"
+    assert_rows_untouched(d_row, w, "D_row")
+    check_common(ref, dprob, dbias)
+
+
+@pytest.mark.parametrize("mode,act,norm", [("mxfp8", "dswiglu", None), ("nvfp4", "dgeglu", 16.0),
+                                           ("mxfp4", "dswiglu", 0.25)])
+def test_dglu_bs_fp8_out(cuda_dev, mode, act, norm):
+    offsets = [256, 512]
+    m, n = 640, 128
+    ref, d_row, sfd, dprob, dbias = run(mode, act, offsets, m, n, 256, seed=9, fp8=True, norm=norm)
+    g = 1.0 if norm is None else norm
+    w = ref["written"]
+    codes = d_row.cpu().numpy()
+    S = 2 * n // 32
+    sf_plain = oquant.from_sfatom(sfd.cpu().numpy(), m, S)
+    _, sf_ref = glu.quantize_rows_fp8(ref["D"].astype(np.float32), g)
+    diff = np.abs(sf_plain.astype(np.int64) - sf_ref.astype(np.int64))[w]
+    assert diff.max() <= 1 and (diff == 0).mean() > 0.98, "scale bytes"
+    scale = np.repeat(formats.decode_ue8m0(sf_plain), 32, axis=1)
+    deq = formats.decode_e4m3(codes) * scale / g
+    D = ref["D"]
+    tol = 2.0 ** -4 * np.abs(D) + scale / g * 2.0 ** -10 + 2.0 ** -8 * np.abs(D) + 2.0 ** -20 * ref["D_mag"]
+    bad = (np.abs(deq - D) > tol) & w[:, None]
+    assert not bad.any(), f"{int(bad.sum())} bad FP8 D_row values"
+    assert (codes[~w] == 0x5A).all(), "rows past the last group written"
+    check_common(ref, dprob, dbias)
