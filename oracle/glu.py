@@ -40,6 +40,11 @@ Readings (also listed in the design notes):
       D_q = E4M3(fp32(D * norm_const) * 2^(127 - SFD_row)).  The D values are
       the float32 values the epilogue computed (each a correctly rounded
       restatement of the closed form here).
+  Q2  D_col (column quantisation): the same rule over every 32 consecutive
+      rows of one D column (rows 32 b .. 32 b + 31, b counted from row 0):
+      SFD_col[column, b] and D_col[m, column] = E4M3(fp32(D * norm_const) *
+      2^(127 - SFD_col[column, m // 32])); D_col is stored [rows, 2N] like
+      D_row, SFD_col in the SfAtom layout of a [2N, ceil(rows/128) * 4] matrix.
 """
 
 import numpy as np
@@ -300,3 +305,19 @@ def quantize_rows_fp8(D, norm_const=1.0):
     mult = np.ldexp(1.0, 127 - sf.astype(np.int64))
     codes = formats.encode_e4m3(y.reshape(rows, cols // 32, 32) * mult[..., None])
     return codes.reshape(rows, cols), sf
+
+
+def quantize_cols_fp8(D, norm_const=1.0):
+    """Step-3 column quantisation of D [rows, cols] (rows % 32 == 0) under Q2.
+
+    Returns (codes uint8 [rows, cols] E4M3, sf uint8 [cols, rows / 32]).
+    """
+    D = np.asarray(D, dtype=np.float32)
+    rows, cols = D.shape
+    g = np.float32(norm_const)
+    amax = np.max(np.abs(D.reshape(rows // 32, 32, cols)), axis=1)   # [rows/32, cols]
+    sf = quant.scale_byte_mxfp8(amax, g)                              # [rows/32, cols]
+    y = (D * g).astype(np.float32).astype(np.float64)
+    mult = np.ldexp(1.0, 127 - sf.astype(np.int64))
+    codes = formats.encode_e4m3(y.reshape(rows // 32, 32, cols) * mult[:, None, :])
+    return codes.reshape(rows, cols), np.ascontiguousarray(sf.T)

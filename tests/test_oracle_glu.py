@@ -239,3 +239,24 @@ def test_row_quantiser_norm_const_by_hand():
     D[0, 0] = np.nextafter(np.float32(112.0), np.float32(200.0))
     _, sf = glu.quantize_rows_fp8(D, 4.0)
     assert sf[0, 0] == 128
+
+
+def test_column_quantiser_by_hand():
+    # column 3: rows 0..31 hold 112 at row 5 and -28 at row 9 (norm 4 -> byte 127,
+    # codes 0x7E and 0xEE); rows 32..63 hold only 1.0 at row 40 (s = 4/448,
+    # ceil(log2) = -6 -> byte 121; 4 * 2^6 = 256 -> 0x78); every other value is 0
+    D = np.zeros((64, 32), np.float32)
+    D[5, 3], D[9, 3], D[40, 3] = 112.0, -28.0, 1.0
+    codes, sf = glu.quantize_cols_fp8(D, 4.0)
+    assert sf.shape == (32, 2)
+    assert sf[3].tolist() == [127, 121] and not sf[[0, 1, 2, 4]].any()
+    assert codes[5, 3] == 0x7E and codes[9, 3] == 0xEE and codes[40, 3] == 0x78
+    assert codes[:, [0, 1, 2]].sum() == 0
+
+
+def test_column_quantiser_is_the_row_quantiser_of_the_transpose():
+    r = rng_(12)
+    D = (r.standard_normal((64, 96)) * 3).astype(np.float32)
+    c1, s1 = glu.quantize_cols_fp8(D, 0.5)
+    c2, s2 = glu.quantize_rows_fp8(D.T.copy(), 0.5)
+    assert np.array_equal(c1, c2.T) and np.array_equal(s1, s2)
