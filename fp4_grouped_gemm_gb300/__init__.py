@@ -292,11 +292,13 @@ def hq_prefill_permute(x, scale, topk_ids, num_experts, max_token_num, permute_x
 
 def hq_gemm_dglu_bs(a, sfa, b, sfb, c, padded_offsets, alpha, prob, dprob, k, mode, act="dswiglu",
                     beta=None, dbias=None, d_row=None, fp8_out=False, sfd_row=None, norm_const=None,
-                    workspace=None, sm_count=-1, stream=None):
+                    col_out=False, d_col=None, sfd_col=None, workspace=None, sm_count=-1, stream=None):
     """Block-scaled grouped GEMM + dSwiGLU / dGeGLU backward (cuDNN block-scaled
     contract).  a, b quantised as hq_quant writes them (b stacked [L, n, k]);
     c [m, 2n] BF16.  With fp8_out the D_row is E4M3 with UE8M0 SfAtom scales
-    (sfd_row) and optional norm_const.  Returns (d_row, sfd_row, dprob, dbias)."""
+    (sfd_row) and optional norm_const; col_out (with fp8_out) also produces the
+    column-quantised D_col / SFD_col.  Returns (d_row, sfd_row, dprob, dbias)
+    or, with col_out, (d_row, sfd_row, d_col, sfd_col, dprob, dbias)."""
     m, two_n = c.shape
     n = two_n // 2
     L = padded_offsets.numel()
@@ -305,6 +307,14 @@ def hq_gemm_dglu_bs(a, sfa, b, sfb, c, padded_offsets, alpha, prob, dprob, k, mo
         d_row = torch.empty(m, two_n, dtype=torch.uint8 if fp8_out else torch.bfloat16, device=dev)
     if fp8_out and sfd_row is None:
         sfd_row = torch.empty(max(sf_bytes(m, two_n, "mxfp8"), 1), dtype=torch.uint8, device=dev)
+    if col_out:
+        if not fp8_out:
+            raise ValueError("col_out needs fp8_out")
+        if d_col is None:
+            d_col = torch.empty(m, two_n, dtype=torch.uint8, device=dev)
+        if sfd_col is None:
+            sfd_col = torch.empty(sf_bytes(two_n, (m + 127) // 128 * 128, "mxfp8"), dtype=torch.uint8,
+                                  device=dev)
     ws_bytes = hq_gemm_dswiglu_workspace_size(L, n)
     if dbias is not None and workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
@@ -312,7 +322,10 @@ def hq_gemm_dglu_bs(a, sfa, b, sfb, c, padded_offsets, alpha, prob, dprob, k, mo
     rc = _abi.load().hq_gemm_dglu_bs(
         _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(padded_offsets), L, _ptr(alpha),
         _ptr(beta), _ptr(prob), acts[act], _ptr(d_row), _ptr(sfd_row if fp8_out else None),
-        _ptr(norm_const), _ptr(dprob), _ptr(dbias), m, n, k, mode_id(mode), _ptr(workspace),
+        _ptr(d_col if col_out else None), _ptr(sfd_col if col_out else None), _ptr(norm_const),
+        _ptr(dprob), _ptr(dbias), m, n, k, mode_id(mode), _ptr(workspace),
         0 if workspace is None else workspace.numel(), sm_count, _stream(stream))
     _check(rc, "hq_gemm_dglu_bs")
+    if col_out:
+        return d_row, sfd_row, d_col, sfd_col, dprob, dbias
     return d_row, (sfd_row if fp8_out else None), dprob, dbias

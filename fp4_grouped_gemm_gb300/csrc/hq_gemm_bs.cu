@@ -65,6 +65,9 @@ struct GemmParams {
   uint8_t* d_row;            // [a_rows, 2n]: BF16, or E4M3 when sfd_row is set
   uint8_t* sfd_row;          // SfAtom UE8M0 scales of D_row, [ceil(a_rows/128)*128, 2n/32], or null
   const float* norm_const;   // FP8 D_row norm_const (device [1]) or null (= 1)
+  uint8_t* d_col;            // [a_rows, 2n] E4M3 column-quantised D, or null
+  uint8_t* sfd_col;          // SfAtom UE8M0 of [2n rows, ceil(a_rows/128)*4 cols], or null
+  int64_t sfd_col_s;         // scale columns of sfd_col (ceil(a_rows / 128) * 4)
 };
 
 enum Epi : int { kEpiGemm = 0, kEpiDSwiGLU = 1, kEpiDGeGLU = 2 };
@@ -352,6 +355,48 @@ __device__ __forceinline__ void dglu_chunk(const GemmParams& p, const uint32_t (
       *reinterpret_cast<uint16_t*>(p.sfd_row + off) = static_cast<uint16_t>(bytes2);
     }
     atomicAdd(p.dprob + row, dp0 + dp1);
+  }
+  if (p.d_col) {
+    // Step 3 along M: each D column's scale over the warp's 32 rows (one
+    // 32-row block), from a max all-reduce across the lanes; lane l keeps the
+    // bytes of gate column l and input column l
+    const int64_t blk = (row - lane) >> 5;
+    uint32_t my_byte[2] = {0u, 0u};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float* v = h == 0 ? dg : di;
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float y[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const float x = row_ok ? v[2 * i + u] : 0.0f;
+          float mx = fabsf(x);
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+          const uint32_t byte = ue8m0_ceil(__fmul_rn(__fmul_rn(norm, mx), 1.0f / 448.0f));
+          if (lane == 2 * i + u) my_byte[h] = byte;
+          y[u] = __fmul_rn(__fmul_rn(x, norm), pow2_neg_unbiased(byte));
+        }
+        const uint32_t pair = cvt_e4m3x2(y[1], y[0]);
+        if ((i & 1) == 0) w[i >> 1] = pair;
+        else w[i >> 1] |= pair << 16;
+      }
+      if (row_ok) {
+        uint4* dst = reinterpret_cast<uint4*>(p.d_col + row * two_n + 2 * j0 + 32 * h);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+    }
+    const int64_t S = p.sfd_col_s;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int64_t col = 2 * j0 + 32 * h + lane;
+      const int64_t off = ((col >> 7) * (S >> 2) + (blk >> 2)) * 512 + (col & 31) * 16 +
+                          ((col >> 5) & 3) * 4 + (blk & 3);
+      p.sfd_col[off] = static_cast<uint8_t>(my_byte[h]);
+    }
   }
   if (p.dbias_ws) {
     // column sums over the warp's 32 rows (butterfly reduce-scatter): lane l
@@ -1408,9 +1453,9 @@ int hq_gemm_grouped_contig(const void* a, const uint8_t* sfa, const void* b, con
 int hq_gemm_dglu_bs(const void* a, const uint8_t* sfa, const void* b, const uint8_t* sfb,
                     const hq_bf16* c, const int32_t* padded_offsets, int L, const float* alpha,
                     const float* beta, const float* prob, int act, void* d_row, uint8_t* sfd_row,
-                    const float* norm_const, float* dprob, hq_bf16* dbias, int64_t m, int64_t n,
-                    int64_t k, hq_mode mode, void* workspace, size_t ws_bytes, int sm_count,
-                    hq_stream_t s) {
+                    void* d_col, uint8_t* sfd_col, const float* norm_const, float* dprob,
+                    hq_bf16* dbias, int64_t m, int64_t n, int64_t k, hq_mode mode, void* workspace,
+                    size_t ws_bytes, int sm_count, hq_stream_t s) {
   if (act != 0 && act != 1) return HQ_ERR_INVALID;
   if (mode != HQ_MXFP8 && mode != HQ_MXFP4 && mode != HQ_NVFP4) return HQ_ERR_INVALID;
   const int64_t gs = mode == HQ_NVFP4 ? 16 : 32;
@@ -1430,6 +1475,8 @@ int hq_gemm_dglu_bs(const void* a, const uint8_t* sfa, const void* b, const uint
        reinterpret_cast<uintptr_t>(norm_const ? norm_const : alpha)) & 3u)
     return HQ_ERR_INVALID;
   if (norm_const && !sfd_row) return HQ_ERR_INVALID;  // norm_const belongs to the FP8 output
+  if ((d_col != nullptr) != (sfd_col != nullptr) || (d_col && !sfd_row)) return HQ_ERR_INVALID;
+  if (d_col && (!hq::aligned16(d_col) || !hq::aligned16(sfd_col))) return HQ_ERR_INVALID;
   if (dbias) {
     if (reinterpret_cast<uintptr_t>(dbias) & 1u) return HQ_ERR_INVALID;
     if (!workspace || ws_bytes < hq_gemm_dswiglu_workspace_size(L, n)) return HQ_ERR_INVALID;
@@ -1450,6 +1497,9 @@ int hq_gemm_dglu_bs(const void* a, const uint8_t* sfa, const void* b, const uint
   p.d_row = static_cast<uint8_t*>(d_row);
   p.sfd_row = sfd_row;
   p.norm_const = norm_const;
+  p.d_col = static_cast<uint8_t*>(d_col);
+  p.sfd_col = sfd_col;
+  p.sfd_col_s = (m + 127) / 128 * 4;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
   const int64_t ws_count = static_cast<int64_t>(L) * 2 * n;
   if (dbias && cudaMemsetAsync(workspace, 0, ws_count * sizeof(float), st) != cudaSuccess)

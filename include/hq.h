@@ -331,17 +331,20 @@ int hq_gemm_dgeglu(const hq_bf16 *a, const hq_bf16 *b, const hq_bf16 *c,
  *              values of a row (SfAtom layout, ceil(m/128)*128 rows, 2n/32
  *              columns): SF = norm_const * amax * (1/448) rounded up to a
  *              power of two, D_q = E4M3(D * norm_const / SF)
+ *   d_col      NULL, or (with sfd_row) E4M3 [m, 2n]: D quantised along M,
+ *              one UE8M0 scale per column and 32 consecutive rows in sfd_col
+ *              (SfAtom layout of a [2n, ceil(m/128)*4] matrix:
+ *              ceil(2n/128)*128 * ceil(m/128)*4 bytes), same rule
  *   norm_const device float [1] or NULL (= 1); only with sfd_row
  *   alpha, beta, prob, dprob, dbias, workspace as hq_gemm_dswiglu (beta
  *              ignored and may be NULL for act 1)
- * Requires n % 128 == 0 and k % (4 * group) == 0.  The column-quantised
- * D_col / SFD_col outputs of the page are not produced. */
+ * Requires n % 128 == 0 and k % (4 * group) == 0. */
 int hq_gemm_dglu_bs(const void *a, const uint8_t *sfa, const void *b, const uint8_t *sfb,
                     const hq_bf16 *c, const int32_t *padded_offsets, int L, const float *alpha,
                     const float *beta, const float *prob, int act, void *d_row, uint8_t *sfd_row,
-                    const float *norm_const, float *dprob, hq_bf16 *dbias, int64_t m, int64_t n,
-                    int64_t k, hq_mode mode, void *workspace, size_t ws_bytes, int sm_count,
-                    hq_stream_t s);
+                    void *d_col, uint8_t *sfd_col, const float *norm_const, float *dprob,
+                    hq_bf16 *dbias, int64_t m, int64_t n, int64_t k, hq_mode mode, void *workspace,
+                    size_t ws_bytes, int sm_count, hq_stream_t s);
 
 /* ------------------------------------------------------------------------- *
  * hq_gemm_dswiglu without caller-provided scratch.  The paper has no

@@ -29,7 +29,7 @@ def bf16_ulp(x):
     return np.where(a > 0, 2.0 ** (e - 7), 2.0 ** -133)
 
 
-def run(mode, act, offsets, m, n, k, seed, fp8=False, norm=None, with_dbias=True):
+def run(mode, act, offsets, m, n, k, seed, fp8=False, norm=None, with_dbias=True, col=False):
     L = len(offsets)
     dev = torch.device("cuda")
     a = bf16_rows(m, k, seed)
@@ -47,15 +47,22 @@ def run(mode, act, offsets, m, n, k, seed, fp8=False, norm=None, with_dbias=True
     d_row = (torch.full((m, 2 * n), 0x5A, dtype=torch.uint8, device=dev) if fp8 else sentinel_bf16((m, 2 * n)))
     nc = torch.tensor([norm], dtype=torch.float32, device=dev) if norm is not None else None
     off = torch.tensor(offsets, dtype=torch.int32, device=dev)
-    d_row, sfd, dprob, dbias = hq.hq_gemm_dglu_bs(
+    d_col = torch.full((m, 2 * n), 0x5A, dtype=torch.uint8, device=dev) if col else None
+    outs = hq.hq_gemm_dglu_bs(
         qa, sfa, qb, sfb, c.to(dev), off, alpha.to(dev), prob.to(dev), dprob, k, mode, act=act,
         beta=beta.to(dev) if act == "dswiglu" else None, dbias=dbias, d_row=d_row, fp8_out=fp8,
-        norm_const=nc)
+        norm_const=nc, col_out=col, d_col=d_col)
     torch.cuda.synchronize()
+    if col:
+        d_row, sfd, d_col, sfd_col, dprob, dbias = outs
+    else:
+        d_row, sfd, dprob, dbias = outs
     if act == "dswiglu":
         ref = glu.dswiglu(a_deq, b_deq, np_f32(c), offsets, alpha.numpy(), beta.numpy(), prob.numpy())
     else:
         ref = glu.dgeglu(a_deq, b_deq, np_f32(c), offsets, alpha.numpy(), prob.numpy())
+    if col:
+        return ref, d_row, sfd, dprob, dbias, d_col, sfd_col
     return ref, d_row, sfd, dprob, dbias
 
 
@@ -104,4 +111,30 @@ def test_dglu_bs_fp8_out(cuda_dev, mode, act, norm):
     bad = (np.abs(deq - D) > tol) & w[:, None]
     assert not bad.any(), f"{int(bad.sum())} bad FP8 D_row values"
     assert (codes[~w] == 0x5A).all(), "rows past the last group written"
+    check_common(ref, dprob, dbias)
+
+
+@pytest.mark.parametrize("mode,act,norm", [("mxfp8", "dswiglu", 2.0), ("nvfp4", "dgeglu", None)])
+def test_dglu_bs_column_quantised_output(cuda_dev, mode, act, norm):
+    """D_col / SFD_col (reading Q2): each column's scale over 32 consecutive rows."""
+    offsets = [256, 512]
+    m, n = 640, 128
+    ref, d_row, sfd, dprob, dbias, d_col, sfd_col = run(mode, act, offsets, m, n, 256, seed=13, fp8=True,
+                                                        norm=norm, col=True)
+    g = 1.0 if norm is None else norm
+    w = ref["written"]
+    rows_w = int(w.sum())                     # written rows form a prefix (offsets end at 512)
+    S = (m + 127) // 128 * 4
+    sf_plain = oquant.from_sfatom(sfd_col.cpu().numpy(), 2 * n, S)[:, : rows_w // 32]
+    _, sf_ref = glu.quantize_cols_fp8(ref["D"][:rows_w].astype(np.float32), g)
+    diff = np.abs(sf_plain.astype(np.int64) - sf_ref.astype(np.int64))
+    assert diff.max() <= 1 and (diff == 0).mean() > 0.98, "column scale bytes"
+    codes = d_col.cpu().numpy()[:rows_w]
+    scale = np.repeat(formats.decode_ue8m0(sf_plain).T, 32, axis=0)        # [rows_w, 2n]
+    deq = formats.decode_e4m3(codes) * scale / g
+    D = ref["D"][:rows_w]
+    tol = 2.0 ** -4 * np.abs(D) + scale / g * 2.0 ** -10 + 2.0 ** -8 * np.abs(D) + 2.0 ** -20 * ref["D_mag"][:rows_w]
+    bad = np.abs(deq - D) > tol
+    assert not bad.any(), f"{int(bad.sum())} bad D_col values"
+    assert (d_col.cpu().numpy()[rows_w:] == 0x5A).all()
     check_common(ref, dprob, dbias)
