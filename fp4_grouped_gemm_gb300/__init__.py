@@ -292,7 +292,8 @@ def hq_prefill_permute(x, scale, topk_ids, num_experts, max_token_num, permute_x
 
 def hq_gemm_dglu_bs(a, sfa, b, sfb, c, padded_offsets, alpha, prob, dprob, k, mode, act="dswiglu",
                     beta=None, dbias=None, d_row=None, fp8_out=False, sfd_row=None, norm_const=None,
-                    col_out=False, d_col=None, sfd_col=None, workspace=None, sm_count=-1, stream=None):
+                    col_out=False, d_col=None, sfd_col=None, amax=None, workspace=None, sm_count=-1,
+                    stream=None):
     """Block-scaled grouped GEMM + dSwiGLU / dGeGLU backward (cuDNN block-scaled
     contract).  a, b quantised as hq_quant writes them (b stacked [L, n, k]);
     c [m, 2n] BF16.  With fp8_out the D_row is E4M3 with UE8M0 SfAtom scales
@@ -323,7 +324,7 @@ def hq_gemm_dglu_bs(a, sfa, b, sfb, c, padded_offsets, alpha, prob, dprob, k, mo
         _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(padded_offsets), L, _ptr(alpha),
         _ptr(beta), _ptr(prob), acts[act], _ptr(d_row), _ptr(sfd_row if fp8_out else None),
         _ptr(d_col if col_out else None), _ptr(sfd_col if col_out else None), _ptr(norm_const),
-        _ptr(dprob), _ptr(dbias), m, n, k, mode_id(mode), _ptr(workspace),
+        _ptr(dprob), _ptr(dbias), _ptr(amax), m, n, k, mode_id(mode), _ptr(workspace),
         0 if workspace is None else workspace.numel(), sm_count, _stream(stream))
     _check(rc, "hq_gemm_dglu_bs")
     if col_out:

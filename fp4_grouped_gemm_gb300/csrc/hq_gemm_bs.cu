@@ -68,6 +68,7 @@ struct GemmParams {
   uint8_t* d_col;            // [a_rows, 2n] E4M3 column-quantised D, or null
   uint8_t* sfd_col;          // SfAtom UE8M0 of [2n rows, ceil(a_rows/128)*4 cols], or null
   int64_t sfd_col_s;         // scale columns of sfd_col (ceil(a_rows / 128) * 4)
+  float* amax;               // [groups, 2]: max |D| over gate / input columns, or null
 };
 
 enum Epi : int { kEpiGemm = 0, kEpiDSwiGLU = 1, kEpiDGeGLU = 2 };
@@ -355,6 +356,28 @@ __device__ __forceinline__ void dglu_chunk(const GemmParams& p, const uint32_t (
       *reinterpret_cast<uint16_t*>(p.sfd_row + off) = static_cast<uint16_t>(bytes2);
     }
     atomicAdd(p.dprob + row, dp0 + dp1);
+  }
+  if (p.amax) {
+    // per-group max |D| over the gate and the input columns: a max all-reduce
+    // over the warp, then one integer atomic max per value (|D| >= 0, so the
+    // float order is the order of the bit patterns)
+    float mg = 0.0f, mi = 0.0f;
+    if (row_ok) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        mg = fmaxf(mg, fabsf(dg[i]));
+        mi = fmaxf(mi, fabsf(di[i]));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      mg = fmaxf(mg, __shfl_xor_sync(0xFFFFFFFFu, mg, o));
+      mi = fmaxf(mi, __shfl_xor_sync(0xFFFFFFFFu, mi, o));
+    }
+    if (lane == 0) {
+      atomicMax(reinterpret_cast<int*>(p.amax + 2 * g), __float_as_int(mg));
+      atomicMax(reinterpret_cast<int*>(p.amax + 2 * g + 1), __float_as_int(mi));
+    }
   }
   if (p.d_col) {
     // Step 3 along M: each D column's scale over the warp's 32 rows (one
@@ -1454,8 +1477,8 @@ int hq_gemm_dglu_bs(const void* a, const uint8_t* sfa, const void* b, const uint
                     const hq_bf16* c, const int32_t* padded_offsets, int L, const float* alpha,
                     const float* beta, const float* prob, int act, void* d_row, uint8_t* sfd_row,
                     void* d_col, uint8_t* sfd_col, const float* norm_const, float* dprob,
-                    hq_bf16* dbias, int64_t m, int64_t n, int64_t k, hq_mode mode, void* workspace,
-                    size_t ws_bytes, int sm_count, hq_stream_t s) {
+                    hq_bf16* dbias, float* amax, int64_t m, int64_t n, int64_t k, hq_mode mode,
+                    void* workspace, size_t ws_bytes, int sm_count, hq_stream_t s) {
   if (act != 0 && act != 1) return HQ_ERR_INVALID;
   if (mode != HQ_MXFP8 && mode != HQ_MXFP4 && mode != HQ_NVFP4) return HQ_ERR_INVALID;
   const int64_t gs = mode == HQ_NVFP4 ? 16 : 32;
@@ -1477,6 +1500,7 @@ int hq_gemm_dglu_bs(const void* a, const uint8_t* sfa, const void* b, const uint
   if (norm_const && !sfd_row) return HQ_ERR_INVALID;  // norm_const belongs to the FP8 output
   if ((d_col != nullptr) != (sfd_col != nullptr) || (d_col && !sfd_row)) return HQ_ERR_INVALID;
   if (d_col && (!hq::aligned16(d_col) || !hq::aligned16(sfd_col))) return HQ_ERR_INVALID;
+  if (amax && (reinterpret_cast<uintptr_t>(amax) & 3u)) return HQ_ERR_INVALID;
   if (dbias) {
     if (reinterpret_cast<uintptr_t>(dbias) & 1u) return HQ_ERR_INVALID;
     if (!workspace || ws_bytes < hq_gemm_dswiglu_workspace_size(L, n)) return HQ_ERR_INVALID;
@@ -1500,7 +1524,10 @@ int hq_gemm_dglu_bs(const void* a, const uint8_t* sfa, const void* b, const uint
   p.d_col = static_cast<uint8_t*>(d_col);
   p.sfd_col = sfd_col;
   p.sfd_col_s = (m + 127) / 128 * 4;
+  p.amax = amax;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  if (amax && cudaMemsetAsync(amax, 0, static_cast<size_t>(L) * 2 * sizeof(float), st) != cudaSuccess)
+    return HQ_ERR_CUDA;
   const int64_t ws_count = static_cast<int64_t>(L) * 2 * n;
   if (dbias && cudaMemsetAsync(workspace, 0, ws_count * sizeof(float), st) != cudaSuccess)
     return HQ_ERR_CUDA;

@@ -336,6 +336,9 @@ int hq_gemm_dgeglu(const hq_bf16 *a, const hq_bf16 *b, const hq_bf16 *c,
  *              (SfAtom layout of a [2n, ceil(m/128)*4] matrix:
  *              ceil(2n/128)*128 * ceil(m/128)*4 bytes), same rule
  *   norm_const device float [1] or NULL (= 1); only with sfd_row
+ *   amax       NULL, or device float [L, 2], overwritten: max |D| over each
+ *              group's rows and its gate columns ([g, 0]) / input columns
+ *              ([g, 1]) (0 for an empty group; m == 0 leaves it untouched)
  *   alpha, beta, prob, dprob, dbias, workspace as hq_gemm_dswiglu (beta
  *              ignored and may be NULL for act 1)
  * Requires n % 128 == 0 and k % (4 * group) == 0. */
@@ -343,8 +346,8 @@ int hq_gemm_dglu_bs(const void *a, const uint8_t *sfa, const void *b, const uint
                     const hq_bf16 *c, const int32_t *padded_offsets, int L, const float *alpha,
                     const float *beta, const float *prob, int act, void *d_row, uint8_t *sfd_row,
                     void *d_col, uint8_t *sfd_col, const float *norm_const, float *dprob,
-                    hq_bf16 *dbias, int64_t m, int64_t n, int64_t k, hq_mode mode, void *workspace,
-                    size_t ws_bytes, int sm_count, hq_stream_t s);
+                    hq_bf16 *dbias, float *amax, int64_t m, int64_t n, int64_t k, hq_mode mode,
+                    void *workspace, size_t ws_bytes, int sm_count, hq_stream_t s);
 
 /* ------------------------------------------------------------------------- *
  * hq_gemm_dswiglu without caller-provided scratch.  The paper has no

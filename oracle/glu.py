@@ -45,6 +45,9 @@ Readings (also listed in the design notes):
       SFD_col[column, b] and D_col[m, column] = E4M3(fp32(D * norm_const) *
       2^(127 - SFD_col[column, m // 32])); D_col is stored [rows, 2N] like
       D_row, SFD_col in the SfAtom layout of a [2N, ceil(rows/128) * 4] matrix.
+  Q3  amax (BF16 D output, shape (L, 2)): amax[g, 0] = max |D| over group g's
+      rows and the gate columns, amax[g, 1] over the input (up) columns; 0 for
+      an empty group.
 """
 
 import numpy as np
@@ -321,3 +324,16 @@ def quantize_cols_fp8(D, norm_const=1.0):
     mult = np.ldexp(1.0, 127 - sf.astype(np.int64))
     codes = formats.encode_e4m3(y.reshape(rows // 32, 32, cols) * mult[:, None, :])
     return codes.reshape(rows, cols), np.ascontiguousarray(sf.T)
+
+
+def group_amax(D, group, L):
+    """Q3: per-group max |D| over the gate and the input columns -> [L, 2]."""
+    D = np.asarray(D, dtype=np.float64)
+    gc, ic = interleave_columns(D.shape[1] // 2)
+    out = np.zeros((L, 2))
+    for g in range(L):
+        rows = np.nonzero(np.asarray(group) == g)[0]
+        if rows.size:
+            out[g, 0] = np.abs(D[np.ix_(rows, gc)]).max()
+            out[g, 1] = np.abs(D[np.ix_(rows, ic)]).max()
+    return out

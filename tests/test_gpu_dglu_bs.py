@@ -29,7 +29,7 @@ def bf16_ulp(x):
     return np.where(a > 0, 2.0 ** (e - 7), 2.0 ** -133)
 
 
-def run(mode, act, offsets, m, n, k, seed, fp8=False, norm=None, with_dbias=True, col=False):
+def run(mode, act, offsets, m, n, k, seed, fp8=False, norm=None, with_dbias=True, col=False, amax=False):
     L = len(offsets)
     dev = torch.device("cuda")
     a = bf16_rows(m, k, seed)
@@ -48,10 +48,12 @@ def run(mode, act, offsets, m, n, k, seed, fp8=False, norm=None, with_dbias=True
     nc = torch.tensor([norm], dtype=torch.float32, device=dev) if norm is not None else None
     off = torch.tensor(offsets, dtype=torch.int32, device=dev)
     d_col = torch.full((m, 2 * n), 0x5A, dtype=torch.uint8, device=dev) if col else None
+    am = torch.full((L, 2), -1.0, dtype=torch.float32, device=dev) if amax else None
+    run.last_amax = am
     outs = hq.hq_gemm_dglu_bs(
         qa, sfa, qb, sfb, c.to(dev), off, alpha.to(dev), prob.to(dev), dprob, k, mode, act=act,
         beta=beta.to(dev) if act == "dswiglu" else None, dbias=dbias, d_row=d_row, fp8_out=fp8,
-        norm_const=nc, col_out=col, d_col=d_col)
+        norm_const=nc, col_out=col, d_col=d_col, amax=am)
     torch.cuda.synchronize()
     if col:
         d_row, sfd, d_col, sfd_col, dprob, dbias = outs
@@ -80,7 +82,11 @@ def check_common(ref, dprob, dbias):
 @pytest.mark.parametrize("act", ["dswiglu", "dgeglu"])
 def test_dglu_bs_bf16_out(cuda_dev, mode, act):
     offsets = [256, 256, 768, 1024]          # empty group 1; rows >= 1024 untouched
-    ref, d_row, _, dprob, dbias = run(mode, act, offsets, 1152, 256, 256, seed=7)
+    ref, d_row, _, dprob, dbias = run(mode, act, offsets, 1152, 256, 256, seed=7, amax=True)
+    am = run.last_amax.cpu().numpy().astype(np.float64)
+    am_ref = glu.group_amax(ref["D"], ref["group"], len(offsets))
+    assert am[1].tolist() == [0.0, 0.0]                            # empty group
+    assert (np.abs(am - am_ref) <= 2.0 ** -8 * am_ref + 1e-6 * am_ref.max()).all(), "amax"
     w = ref["written"]
     D = d_row.float().cpu().numpy().astype(np.float64)
     tol = 2.0 ** -8 * np.abs(ref["D"]) + 2.0 ** -20 * ref["D_mag"] + 1e-30

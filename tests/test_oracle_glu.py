@@ -260,3 +260,11 @@ def test_column_quantiser_is_the_row_quantiser_of_the_transpose():
     c1, s1 = glu.quantize_cols_fp8(D, 0.5)
     c2, s2 = glu.quantize_rows_fp8(D.T.copy(), 0.5)
     assert np.array_equal(c1, c2.T) and np.array_equal(s1, s2)
+
+
+def test_group_amax_by_hand():
+    # N = 32 compact: columns 0..31 gate, 32..63 input; rows 0-1 group 0, row 2 group 2
+    D = np.zeros((3, 64))
+    D[0, 5], D[1, 40], D[2, 63], D[2, 0] = -3.0, 2.5, -7.0, 1.0
+    a = glu.group_amax(D, [0, 0, 2], 3)
+    assert a.tolist() == [[3.0, 2.5], [0.0, 0.0], [1.0, 7.0]]
