@@ -45,6 +45,10 @@ Readings (also listed in the design notes):
       SFD_col[column, b] and D_col[m, column] = E4M3(fp32(D * norm_const) *
       2^(127 - SFD_col[column, m // 32])); D_col is stored [rows, 2N] like
       D_row, SFD_col in the SfAtom layout of a [2N, ceil(rows/128) * 4] matrix.
+  F1  Up-proj GEMM with SwiGLU + requantisation fused into its epilogue:
+      gate_up = alpha_g * (A . B_g^T) kept in float (not rounded to BF16 as
+      the unfused GEMM output is), y = up * silu(gate) as S1, quantised as
+      fused_swiglu_quant; rows past padded_offsets[L-1] are not written.
   Q3  amax (BF16 D output, shape (L, 2)): amax[g, 0] = max |D| over group g's
       rows and the gate columns, amax[g, 1] over the input (up) columns; 0 for
       an empty group.
@@ -337,3 +341,21 @@ def group_amax(D, group, L):
             out[g, 0] = np.abs(D[np.ix_(rows, gc)]).max()
             out[g, 1] = np.abs(D[np.ix_(rows, ic)]).max()
     return out
+
+
+def gemm_swiglu_quant(a_deq, b_deq, padded_offsets, alpha, mode, global_scale=None):
+    """F1: the grouped up-proj GEMM (oracle.gemm G3 groups) followed by SwiGLU
+    and requantisation of its float result.
+
+    Returns dict with y64 (float64 y), q / sf_plain (the quantised rows from
+    the float32-rounded gate_up), written rows, and the bound magnitudes
+    gu_mag (|alpha| |A| |B|^T) of gate_up.
+    """
+    from . import gemm as ogemm
+    ref, mag, written = ogemm.grouped_contig(a_deq, b_deq, padded_offsets, alpha=alpha)
+    H = ref.shape[1] // 2
+    g64, u64 = ref[:, :H], ref[:, H:]
+    y64 = u64 * g64 / (1.0 + np.exp(-g64))
+    out = swiglu_quant(ref.astype(np.float32), mode, global_scale=global_scale)
+    return {"y64": np.where(written[:, None], y64, 0.0), "q": out["q"], "sf_plain": out["sf_plain"],
+            "written": written, "gu_mag": mag, "gate_up": ref}

@@ -268,3 +268,20 @@ def test_group_amax_by_hand():
     D[0, 5], D[1, 40], D[2, 63], D[2, 0] = -3.0, 2.5, -7.0, 1.0
     a = glu.group_amax(D, [0, 0, 2], 3)
     assert a.tolist() == [[3.0, 2.5], [0.0, 0.0], [1.0, 7.0]]
+
+
+def test_fused_up_proj_matches_the_two_step_path_on_exact_values():
+    # operands whose products and sums are exact in float32: the fused oracle
+    # equals GEMM -> SwiGLU quantisation on the same float values
+    r = rng_(13)
+    K, H = 32, 64
+    a = r.integers(-3, 4, (256, K)).astype(np.float64)
+    b = (r.integers(-3, 4, (2, 2 * H, K)) * 0.25).astype(np.float64)
+    out = glu.gemm_swiglu_quant(a, b, [128, 256], [1.0, 2.0], "mxfp8")
+    gu = np.concatenate([a[:128] @ b[0].T, 2.0 * (a[128:] @ b[1].T)])
+    ref = glu.swiglu_quant(gu.astype(np.float32), "mxfp8")
+    assert np.array_equal(out["q"], ref["q"]) and np.array_equal(out["sf_plain"], ref["sf_plain"])
+    assert out["written"].all()
+    # y64 is up * silu(gate) of the exact gate_up
+    g, u = gu[:, :H], gu[:, H:]
+    assert np.allclose(out["y64"], u * g / (1 + np.exp(-g)), rtol=1e-14, atol=0)
