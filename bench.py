@@ -505,6 +505,14 @@ class Extras:
         byts = M * n * 2 + M * H + sfs.numel()
         res["swiglu_quant_mxfp8_17408x3072"] = {"us": t * 1e6, "gbs": byts / t / 1e9,
                                                 "frac_hbm": byts / t / 1e9 / self.hbm}
+        # the same up-proj with SwiGLU + MXFP8 requantisation in the GEMM's
+        # epilogue (one launch instead of GEMM + separate pass)
+        t = time_kernel(lambda: hq.hq_gemm_grouped_contig_swiglu_quant(qa, sfa, qbv, sfb, off, M, H, k, "mxfp8",
+                                                                       "mxfp8", q_out=qs, sf_out=sfs),
+                        20, self.flush)
+        res["moe_contig_mxfp8_L8_fused_swiglu_quant"] = {
+            "us": t * 1e6, "tflops": fl / t / 1e12, "frac_fp8": fl / t / 1e12 / self.p_fp8,
+            "unfused_us": res["moe_contig_mxfp8_L8"]["us"] + res["swiglu_quant_mxfp8_17408x3072"]["us"]}
         return res
 
     def moe_masked(self):

@@ -22,7 +22,7 @@ __all__ = [
     "hq_gemm_dense", "hq_gemm_grouped_contig", "hq_gemm_grouped_masked", "hq_swiglu_quant",
     "hq_gemm_dswiglu", "hq_gemm_dswiglu_workspace_size", "hq_gemm_dgeglu", "swiglu_kb_dim",
     "hq_prefill_permute", "hq_prefill_permute_workspace_size", "hq_gemm_grouped_rows",
-    "hq_gemm_grouped_rows_workspace_size", "hq_gemm_dglu_bs",
+    "hq_gemm_grouped_rows_workspace_size", "hq_gemm_dglu_bs", "hq_gemm_grouped_contig_swiglu_quant",
 ]
 
 _MODES = {"mxfp8": HQ_MXFP8, "w8a8-mxfp8": HQ_MXFP8, "mxfp4": HQ_MXFP4, "w4a4-mxfp4": HQ_MXFP4,
@@ -196,6 +196,26 @@ def hq_swiglu_quant(x, mode, token_nums=None, rows_per_expert=0, global_scale=No
                                      mode_id(mode), _ptr(global_scale), _ptr(q_out), _ptr(sf_out),
                                      _stream(stream))
     _check(rc, "hq_swiglu_quant")
+    return q_out, sf_out
+
+
+def hq_gemm_grouped_contig_swiglu_quant(a, sfa, b, sfb, padded_offsets, m_rows, H, k, mode,
+                                        out_mode, alpha=None, global_scale=None, q_out=None,
+                                        sf_out=None, sm_count=-1, stream=None):
+    """Grouped up-proj GEMM with SwiGLU + requantisation in its epilogue.
+
+    b: [L, 2H, k] quantised weights (gate rows [0, H), up rows [H, 2H)).
+    Returns (q_out, sf_out) in out_mode, laid out as hq_swiglu_quant's."""
+    if q_out is None:
+        q_out = torch.empty(_q_shape(m_rows, H, out_mode), dtype=torch.uint8, device=a.device)
+    if sf_out is None:
+        nbytes = -(-m_rows // 128) * 128 * swiglu_kb_dim(H, out_mode)
+        sf_out = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=a.device)
+    rc = _abi.load().hq_gemm_grouped_contig_swiglu_quant(
+        _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(padded_offsets), padded_offsets.numel(),
+        _ptr(alpha), m_rows, H, k, mode_id(mode), mode_id(out_mode), _ptr(global_scale),
+        _ptr(q_out), _ptr(sf_out), sm_count, _stream(stream))
+    _check(rc, "hq_gemm_grouped_contig_swiglu_quant")
     return q_out, sf_out
 
 

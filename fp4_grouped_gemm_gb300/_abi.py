@@ -65,6 +65,9 @@ SIGNATURES = {
     "hq_gemm_grouped_masked": (c_i32, [c_p, c_p, c_p, c_p, c_p, c_i32, c_i64, c_p, c_p, c_p,
                                        c_i64, c_i64, c_i32, c_i32, c_p]),
     "hq_swiglu_quant": (c_i32, [c_p, c_i64, c_i64, c_p, c_i32, c_i64, c_i32, c_p, c_p, c_p, c_p]),
+    "hq_gemm_grouped_contig_swiglu_quant": (c_i32, [c_p, c_p, c_p, c_p, c_p, c_i32, c_p, c_i64,
+                                                    c_i64, c_i64, c_i32, c_i32, c_p, c_p, c_p,
+                                                    c_i32, c_p]),
     "hq_gemm_dswiglu": (c_i32, [c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_p, c_p, c_p, c_p, c_i64,
                                 c_i64, c_i64, c_p, c_sz, c_i32, c_p]),
     "hq_gemm_dswiglu_workspace_size": (c_sz, [c_i32, c_i64]),

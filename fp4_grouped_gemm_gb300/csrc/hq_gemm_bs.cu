@@ -69,9 +69,17 @@ struct GemmParams {
   uint8_t* sfd_col;          // SfAtom UE8M0 of [2n rows, ceil(a_rows/128)*4 cols], or null
   int64_t sfd_col_s;         // scale columns of sfd_col (ceil(a_rows / 128) * 4)
   float* amax;               // [groups, 2]: max |D| over gate / input columns, or null
+  // fused up-proj epilogue only: n is H, B holds 2H rows per group (gate rows
+  // [0, H), up rows [H, 2H)); out is not used, y = up * silu(gate) is
+  // quantised instead
+  uint8_t* q;                // [a_rows, H] E4M3 (MXFP8) or [a_rows, H / 2] packed E2M1 (NVFP4)
+  uint8_t* sfq;              // SfAtom scales of q, sfq_cols columns
+  int64_t sfq_cols;          // MXFP8: ceil(H / 512) * 16; NVFP4: H / 16
+  int q_mode;                // HQ_MXFP8 or HQ_NVFP4
+  const float* q_gscale;     // NVFP4 global scale (device [1]) or null (= 1)
 };
 
-enum Epi : int { kEpiGemm = 0, kEpiDSwiGLU = 1, kEpiDGeGLU = 2 };
+enum Epi : int { kEpiGemm = 0, kEpiDSwiGLU = 1, kEpiDGeGLU = 2, kEpiSwiGLUQ = 3 };
 
 // TABLE: entries of the per-CTA group table (0 for the dense GEMM, which
 // needs none and spends the shared memory on a deeper pipeline instead).
@@ -447,6 +455,102 @@ __device__ __forceinline__ void dglu_chunk(const GemmParams& p, const uint32_t (
   }
 }
 
+// ---------------------------------------------------------------------------
+// Fused up-proj epilogue: SwiGLU of the GEMM's float32 result followed by the
+// group-wise requantisation (cuDNN frontend "Grouped GEMM + dGLU (SM100)",
+// forward SwiGLU and Step 3; HALOps group_wise_quant encodings).  The tile's
+// accumulator holds 128 gate columns (TMEM columns [0, 128)) and the matching
+// 128 up columns ([128, 256)) of one expert; the calling warp owns compact
+// columns [cw, cw + 64) of its lane quarter, one row per thread:
+//   gate = alpha acc_g, up = alpha acc_u, y = up * (gate / (1 + exp(-gate)))
+// swiglu_drain forms y while reading TMEM; swiglu_store (after TMEM is
+// released) encodes each scale group of y and writes the codes and the scale
+// bytes:
+//   MXFP8  per 32: UE8M0 = ceil(log2(amax / 448)) + 127, q = E4M3(y 2^(127 - UE8M0))
+//   NVFP4  per 16: UE4M3 = E4M3((g amax) / 6), q = E2M1(y (g / value(UE4M3)))
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void swiglu_drain(uint32_t tcol, float alpha, float (&y)[64]) {
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    uint32_t rg[16], ru[16];
+    tmem_ld_32x32b_x16(tcol + 16 * s, rg);
+    tmem_ld_32x32b_x16(tcol + 128 + 16 * s, ru);
+    tmem_ld_wait(rg);
+    tmem_ld_wait(ru);
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      float g0, g1, u0, u1;
+      mul_f32x2(g0, g1, __uint_as_float(rg[i]), __uint_as_float(rg[i + 1]), alpha);
+      mul_f32x2(u0, u1, __uint_as_float(ru[i]), __uint_as_float(ru[i + 1]), alpha);
+      const float t0 = __fmul_rn(g0, dglu_rcp(__fadd_rn(1.0f, __expf(-g0))));
+      const float t1 = __fmul_rn(g1, dglu_rcp(__fadd_rn(1.0f, __expf(-g1))));
+      mul2_f32x2(y[16 * s + i], y[16 * s + i + 1], u0, u1, t0, t1);
+    }
+  }
+}
+
+__device__ __forceinline__ int64_t sfatom_offset(int64_t r, int64_t s, int64_t S) {
+  return ((r >> 7) * (S >> 2) + (s >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (s & 3);
+}
+
+__device__ __forceinline__ void swiglu_store(const GemmParams& p, const float (&y)[64], int64_t row,
+                                             int64_t j0, float gq) {
+  const int64_t H = p.n;
+  if (p.q_mode == HQ_MXFP8) {
+    uint32_t bytes2 = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float* v = y + 32 * h;
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      const uint32_t byte = ue8m0_ceil(__fmul_rn(amax, 1.0f / 448.0f));
+      const float mult = pow2_neg_unbiased(byte);
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t lo = cvt_e4m3x2(__fmul_rn(v[4 * i + 1], mult), __fmul_rn(v[4 * i], mult));
+        const uint32_t hi = cvt_e4m3x2(__fmul_rn(v[4 * i + 3], mult), __fmul_rn(v[4 * i + 2], mult));
+        w[i] = lo | (hi << 16);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(p.q + row * H + j0 + 32 * h);
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      bytes2 |= byte << (8 * h);
+    }
+    // scale columns j0 / 32 (even) and the next one are adjacent in the atom row
+    *reinterpret_cast<uint16_t*>(p.sfq + sfatom_offset(row, j0 / 32, p.sfq_cols)) =
+        static_cast<uint16_t>(bytes2);
+  } else {
+    uint32_t bytes4 = 0;
+    uint32_t w[8];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const float* v = y + 16 * h;
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      const uint32_t byte = cvt_e4m3x2(0.0f, __fmul_rn(__fmul_rn(gq, amax), 1.0f / 6.0f)) & 0x7Fu;
+      const float sd = ue4m3_value(byte);
+      const float r = sd == 0.0f ? 0.0f : __fdiv_rn(gq, sd);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        uint32_t x = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          x |= cvt_e2m1x2(__fmul_rn(v[8 * i + 2 * j + 1], r), __fmul_rn(v[8 * i + 2 * j], r)) << (8 * j);
+        w[2 * h + i] = x;
+      }
+      bytes4 |= byte << (8 * h);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(p.q + (row * H + j0) / 2);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    // scale columns j0 / 16 .. + 3 form one 32-bit word of the atom row
+    *reinterpret_cast<uint32_t*>(p.sfq + sfatom_offset(row, j0 / 16, p.sfq_cols)) = bytes4;
+  }
+}
+
 template <int MODE, int BN, int STAGES, int ACC, int TABLE, int EPI = kEpiGemm>
 __global__ void __launch_bounds__(kThreads, 1)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -501,8 +605,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // the fused up-proj tile covers 128 compact columns: its 256 B rows are
+  // gate rows [n0, n0 + 128) and up rows [H + n0, H + n0 + 128)
+  constexpr bool kUpProj = EPI == kEpiSwiGLUQ;
+  constexpr int TW = kUpProj ? BN / 2 : BN;
+  static_assert(!kUpProj || (BN == 256 && ACC == 1), "fused up-proj tiles are 128 + 128 wide");
+  auto rb_of = [&](const TileInfo& ti) -> int {
+    if (kUpProj) return C::RB;
+    const int v = static_cast<int>((p.n - ti.n0 + 127) / 128);
+    return v < C::RB ? v : C::RB;
+  };
   Schedule sch;
-  sch.n_tiles = static_cast<int>((p.n + BN - 1) / BN);
+  sch.n_tiles = static_cast<int>((p.n + TW - 1) / TW);
   sch.total_tiles = *total_mtiles_s * sch.n_tiles;
   sch.tab0 = tab0;
   sch.tab1 = tab1;
@@ -518,26 +632,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t filled_mask = 0, last_parity = 0;
       bool ok = true;
       for (int64_t t = blockIdx.x; ok && t < sch.total_tiles; t += gridDim.x) {
-        const TileInfo ti = decode_tile(p.gs, sch, t, BN);
+        const TileInfo ti = decode_tile(p.gs, sch, t, TW);
         const uint8_t* sfa_rows = p.sfa + (ti.row0 / kBM) * atoms_total * 512;
         const uint8_t* sfb_grp = p.sfb + static_cast<int64_t>(ti.g) * p.sfb_group_bytes;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, wctx)) { ok = false; break; }
           int atoms = atoms_total - kb * C::ATOMS;
           atoms = atoms < C::ATOMS ? atoms : C::ATOMS;
-          int rb_valid = static_cast<int>((p.n - ti.n0 + 127) / 128);
-          rb_valid = rb_valid < C::RB ? rb_valid : C::RB;
+          const int rb_valid = rb_of(ti);
           const uint32_t bytes = C::A_BYTES + C::B_BYTES + atoms * 512u * (1 + rb_valid);
           mbar_arrive_expect_tx(full_bar(stage), bytes);
           tma_load_2d(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, full_bar(stage),
                       kb * kBKBytes, static_cast<int32_t>(ti.row0));
-          tma_load_3d(sbase + C::OFF_B + stage * C::B_BYTES, &tmB, full_bar(stage),
-                      kb * kBKBytes, ti.n0, ti.g);
+          if (kUpProj) {
+            // two 128-row boxes; with the 128-byte swizzle repeating every 8
+            // rows the pair lands exactly as one 256-row box would
+            tma_load_3d(sbase + C::OFF_B + stage * C::B_BYTES, &tmB, full_bar(stage),
+                        kb * kBKBytes, ti.n0, ti.g);
+            tma_load_3d(sbase + C::OFF_B + stage * C::B_BYTES + 128 * kBKBytes, &tmB, full_bar(stage),
+                        kb * kBKBytes, static_cast<int32_t>(p.n + ti.n0), ti.g);
+          } else {
+            tma_load_3d(sbase + C::OFF_B + stage * C::B_BYTES, &tmB, full_bar(stage),
+                        kb * kBKBytes, ti.n0, ti.g);
+          }
           bulk_load(sbase + C::OFF_SFA + stage * C::SFA_BYTES, sfa_rows + kb * C::ATOMS * 512,
                     atoms * 512u, full_bar(stage));
           for (int rb = 0; rb < rb_valid; ++rb) {
-            const uint8_t* src =
-                sfb_grp + ((ti.n0 / 128 + rb) * static_cast<int64_t>(atoms_total) + kb * C::ATOMS) * 512;
+            // 128-row block of B holding tile rows [128 rb, 128 rb + 128)
+            const int64_t blk = kUpProj ? (rb * p.n + ti.n0) / 128 : ti.n0 / 128 + rb;
+            const uint8_t* src = sfb_grp + (blk * atoms_total + kb * C::ATOMS) * 512;
             bulk_load(sbase + C::OFF_SFB + stage * C::SFB_BYTES + rb * C::ATOMS * 512, src,
                       atoms * 512u, full_bar(stage));
           }
@@ -566,9 +689,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t bdesc0 = smem_desc_sw128(sbase + C::OFF_B);
       constexpr int kFullMma = MODE == HQ_NVFP4 ? C::ATOMS : kBKBytes / kMmaKBytes;
       for (int64_t t = blockIdx.x; ok && t < sch.total_tiles; t += gridDim.x) {
-        const TileInfo ti = decode_tile(p.gs, sch, t, BN);
-        int rb_valid = static_cast<int>((p.n - ti.n0 + 127) / 128);
-        rb_valid = rb_valid < C::RB ? rb_valid : C::RB;
+        const TileInfo ti = decode_tile(p.gs, sch, t, TW);
+        const int rb_valid = rb_of(ti);
         if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, wctx)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
@@ -643,9 +765,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; ok && t < sch.total_tiles; t += gridDim.x) {
-      const TileInfo ti = decode_tile(p.gs, sch, t, BN);
-      int rb_valid = static_cast<int>((p.n - ti.n0 + 127) / 128);
-      rb_valid = rb_valid < C::RB ? rb_valid : C::RB;
+      const TileInfo ti = decode_tile(p.gs, sch, t, TW);
+      const int rb_valid = rb_of(ti);
       for (int kb = 0; kb < num_kb; ++kb) {
         int atoms = atoms_total - kb * C::ATOMS;
         atoms = atoms < C::ATOMS ? atoms : C::ATOMS;
@@ -722,14 +843,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - 2;
     int acc = 0;
     uint32_t acc_phase = 0;
-    if (EPI != kEpiGemm) {
+    if (kUpProj) {
+      // fused up-proj: the warp owns compact columns [64 h, 64 h + 64) of
+      // the tile; y is formed while TMEM is drained, TMEM is released, then
+      // y is quantised and stored (one row per thread)
+      const float gq = p.q_gscale ? __ldg(p.q_gscale) : 1.0f;
+      const int h = ew >> 2;
+      for (int64_t t = blockIdx.x; t < sch.total_tiles; t += gridDim.x) {
+        const TileInfo ti = decode_tile(p.gs, sch, t, TW);
+        const float alpha = p.alpha ? __ldg(p.alpha + ti.g) : 1.0f;  // loaded before the wait
+        const bool okw = wait_bounded(tfull_bar(acc), acc_phase, wctx);
+        if (!__all_sync(0xFFFFFFFFu, okw)) break;
+        tc_fence_after();
+        float y[64];
+        swiglu_drain(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + 64 * h, alpha, y);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(acc));
+        const int r_local = q * 32 + lane;
+        if (r_local >= ti.row_lo && r_local < ti.rows_valid) {
+          const int64_t row = ti.row0 + r_local;
+          swiglu_store(p, y, row, ti.n0 + 64 * h, gq);
+          // MXFP8 scale columns past H / 32 (the layout pads them to a
+          // multiple of 16) hold 0; the last tile of the row writes them
+          if (p.q_mode == HQ_MXFP8 && h == 1 && ti.n0 + TW == p.n)
+            for (int64_t sc = p.n / 32; sc < p.sfq_cols; sc += 4)
+              *reinterpret_cast<uint32_t*>(p.sfq + sfatom_offset(row, sc, p.sfq_cols)) = 0u;
+        }
+        if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
+      }
+    }
+    if (EPI == kEpiDSwiGLU || EPI == kEpiDGeGLU) {
       // dGLU: the warp owns two 32-column chunks of its lane quarter; C of a
       // chunk is loaded before its accumulator columns are read
-      static_assert(EPI == kEpiGemm || (BN == 128 && ACC == 2), "dGLU tiles are 128 wide");
+      static_assert(EPI == kEpiGemm || kUpProj || (BN == 128 && ACC == 2), "dGLU tiles are 128 wide");
       const float norm = p.norm_const ? __ldg(p.norm_const) : 1.0f;
       const int64_t two_n = 2 * p.n;
       for (int64_t t = blockIdx.x; t < sch.total_tiles; t += gridDim.x) {
-        const TileInfo ti = decode_tile(p.gs, sch, t, BN);
+        const TileInfo ti = decode_tile(p.gs, sch, t, TW);
         const int r_local = q * 32 + lane;
         const bool row_ok = r_local < ti.rows_valid;
         const int64_t row = ti.row0 + r_local;
@@ -769,7 +920,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     for (int64_t t = blockIdx.x; EPI == kEpiGemm && t < sch.total_tiles; t += gridDim.x) {
-      const TileInfo ti = decode_tile(p.gs, sch, t, BN);
+      const TileInfo ti = decode_tile(p.gs, sch, t, TW);
       const float alpha = p.alpha ? __ldg(p.alpha + ti.g) : 1.0f;  // loaded before the wait
       // every lane waits; the warp proceeds only if all lanes saw completion
       const bool ok = wait_bounded(tfull_bar(acc), acc_phase, wctx);
@@ -1157,10 +1308,13 @@ int run_bs(const void* a, const void* b, const GemmParams& p0, int sm_count, boo
                                strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != HQ_OK) return rc;
   }
+  // the fused up-proj B holds 2 n rows per group, loaded as two 128-row boxes
+  constexpr bool kUpProj = EPI == kEpiSwiGLUQ;
+  const uint64_t b_rows = static_cast<uint64_t>(kUpProj ? 2 * p.n : p.n);
   {
-    const uint64_t dims[3] = {kbytes, static_cast<uint64_t>(p.n), static_cast<uint64_t>(p.gs.groups)};
-    const uint64_t strides[2] = {kbytes, kbytes * static_cast<uint64_t>(p.n)};
-    const uint32_t box[3] = {kBKBytes, static_cast<uint32_t>(BN), 1};
+    const uint64_t dims[3] = {kbytes, b_rows, static_cast<uint64_t>(p.gs.groups)};
+    const uint64_t strides[2] = {kbytes, kbytes * b_rows};
+    const uint32_t box[3] = {kBKBytes, static_cast<uint32_t>(kUpProj ? 128 : BN), 1};
     int rc = encode_tensor_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(b), dims,
                                strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != HQ_OK) return rc;
@@ -1176,7 +1330,8 @@ int run_bs(const void* a, const void* b, const GemmParams& p0, int sm_count, boo
     mtiles_bound = static_cast<int64_t>(p.gs.groups) * ((p.gs.max_m + kBM - 1) / kBM);
   else
     mtiles_bound = (p.gs.a_rows + kBM - 1) / kBM;
-  const int64_t tiles_bound = mtiles_bound * ((p.n + BN - 1) / BN);
+  const int64_t tw = kUpProj ? BN / 2 : BN;
+  const int64_t tiles_bound = mtiles_bound * ((p.n + tw - 1) / tw);
   int64_t grid = sm_count > 0 ? sm_count : sms;
   if (grid > sms) grid = sms;
   if (grid > tiles_bound) grid = tiles_bound;
@@ -1471,6 +1626,43 @@ int hq_gemm_grouped_contig(const void* a, const uint8_t* sfa, const void* b, con
   p.gs.group_info = padded_offsets;
   p.gs.sched = hq::kContig;
   return hq::run_gemm(mode, a, b, p, sm_count, false, reinterpret_cast<cudaStream_t>(s));
+}
+
+int hq_gemm_grouped_contig_swiglu_quant(const void* a, const uint8_t* sfa, const void* b,
+                                        const uint8_t* sfb, const int32_t* padded_offsets, int L,
+                                        const float* alpha, int64_t m_rows, int64_t H, int64_t k,
+                                        hq_mode mode, hq_mode out_mode, const float* global_scale,
+                                        void* q_out, uint8_t* sf_out, int sm_count, hq_stream_t s) {
+  if (H <= 0 || H % 128 != 0 || H > (1ll << 28)) return HQ_ERR_INVALID;
+  int rc = hq::check_common(a, sfa, b, sfb, alpha, nullptr, static_cast<const hq_bf16*>(q_out), 2 * H,
+                            k, mode);
+  if (rc != HQ_OK) return rc;
+  if (out_mode != HQ_MXFP8 && out_mode != HQ_NVFP4) return HQ_ERR_INVALID;
+  if (out_mode == HQ_MXFP8 && global_scale) return HQ_ERR_UNSUPPORTED;
+  if (!sf_out || !hq::aligned16(sf_out)) return HQ_ERR_INVALID;
+  if (global_scale && (reinterpret_cast<uintptr_t>(global_scale) & 3u)) return HQ_ERR_INVALID;
+  if (!padded_offsets || L < 1 || L > hq::kMaxGroups) return HQ_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(padded_offsets) & 3u) return HQ_ERR_INVALID;
+  if (m_rows < 0 || m_rows > (1ll << 31) - 256) return HQ_ERR_INVALID;
+  if (m_rows == 0) return HQ_OK;
+  hq::GemmParams p = hq::base_params(sfa, sfb, alpha, nullptr, nullptr, 2 * H, k, mode);
+  if (!p.gs.status) return HQ_ERR_CUDA;
+  p.n = H;  // compact columns; the B scale blocks stay those of 2H rows
+  p.gs.a_rows = m_rows;
+  p.gs.groups = L;
+  p.gs.group_info = padded_offsets;
+  p.gs.sched = hq::kContig;
+  p.q = static_cast<uint8_t*>(q_out);
+  p.sfq = sf_out;
+  p.sfq_cols = out_mode == HQ_MXFP8 ? (H + 511) / 512 * 16 : H / 16;
+  p.q_mode = out_mode;
+  p.q_gscale = global_scale;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  constexpr int T = hq::kMaxGroups + 1;
+  constexpr int E = hq::kEpiSwiGLUQ;
+  if (mode == HQ_MXFP8) return hq::run_bs<HQ_MXFP8, 256, 4, 1, T, E>(a, b, p, sm_count, false, st);
+  if (mode == HQ_MXFP4) return hq::run_bs<HQ_MXFP4, 256, 3, 1, T, E>(a, b, p, sm_count, false, st);
+  return hq::run_bs<HQ_NVFP4, 256, 3, 1, T, E>(a, b, p, sm_count, false, st);
 }
 
 int hq_gemm_dglu_bs(const void* a, const uint8_t* sfa, const void* b, const uint8_t* sfb,

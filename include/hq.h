@@ -269,6 +269,35 @@ int hq_swiglu_quant(const hq_bf16 *in, int64_t rows, int64_t H, const int32_t *t
                     int64_t rows_per_expert, hq_mode mode, const float *global_scale,
                     void *q_out, uint8_t *sf_out, hq_stream_t s);
 
+/* The grouped up-proj GEMM with the SwiGLU + requantisation above fused into
+ * its epilogue (HALOps fused_swiglu_quant applied to the output of
+ * group_contiguous_gemm; cuDNN "Grouped GEMM + dGLU (SM100)" forward
+ * SwiGLU): per group g and row m of the group
+ *     gate_up = alpha_g * (a[m] . b[g]^T)      (float32, never rounded to BF16)
+ *     y       = up * gate / (1 + exp(-gate)),  gate = gate_up[0, H), up = [H, 2H)
+ * and y is quantised in out_mode as hq_swiglu_quant quantises its float32 y.
+ *   a, sfa          [m_rows, k] quantised in `mode` (as hq_gemm_grouped_contig)
+ *   b, sfb          [L, 2H, k] quantised in `mode`: rows [0, H) of expert g
+ *                   are its gate weights, rows [H, 2H) its up weights
+ *   padded_offsets  as hq_gemm_grouped_contig; alpha as there (per group)
+ *   out_mode        HQ_MXFP8 or HQ_NVFP4 (the format of y)
+ *   global_scale    NVFP4 output norm_const (device float [1]) or NULL (= 1);
+ *                   not accepted with HQ_MXFP8 output (HQ_ERR_UNSUPPORTED)
+ *   q_out, sf_out   as hq_swiglu_quant: MXFP8 [m_rows, H] codes, NVFP4
+ *                   [m_rows, H/2]; SfAtom scales of kb_dim columns (MXFP8
+ *                   ceil(H / 512) * 16 with columns [H/32, kb_dim) written 0;
+ *                   NVFP4 H / 16) over ceil(m_rows/128)*128 rows.
+ * Rows >= padded_offsets[L-1] (codes and scales) are not written.  No bias.
+ * Requires H % 128 == 0, k % (4 * group) == 0; pointers 16-byte aligned.
+ * Differs from the unfused path (GEMM to BF16, then hq_swiglu_quant) only in
+ * that gate_up keeps its float32 value: codes and scale bytes may differ by
+ * one rounding step where the BF16 rounding of gate_up would decide them. */
+int hq_gemm_grouped_contig_swiglu_quant(const void *a, const uint8_t *sfa, const void *b,
+                                        const uint8_t *sfb, const int32_t *padded_offsets, int L,
+                                        const float *alpha, int64_t m_rows, int64_t H, int64_t k,
+                                        hq_mode mode, hq_mode out_mode, const float *global_scale,
+                                        void *q_out, uint8_t *sf_out, int sm_count, hq_stream_t s);
+
 /* ------------------------------------------------------------------------- *
  * cuDNN "Grouped GEMM + dGLU (SM100)", BF16 contract, act_func = "dswiglu",
  * dense B:  R_g = alpha_g^2 A_g B_g^T,  X_g = beta_g C_g; X is split into

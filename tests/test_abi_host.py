@@ -119,6 +119,24 @@ def test_swiglu_and_dswiglu_reject_bad_arguments(lib):
     assert d(*args) == _abi.HQ_ERR_INVALID
 
 
+def test_fused_up_proj_rejects_bad_arguments(lib):
+    f = lib.hq_gemm_grouped_contig_swiglu_quant
+
+    def call(H=256, k=256, mode=0, out_mode=0, alpha=None, gscale=None, off=FAKE, L=4, m=1024, sf=FAKE):
+        return f(FAKE, FAKE, FAKE, FAKE, off, L, alpha, m, H, k, mode, out_mode, gscale, FAKE, sf, -1, None)
+
+    assert call(H=192) == _abi.HQ_ERR_INVALID                  # H % 128
+    assert call(k=96) == _abi.HQ_ERR_INVALID                   # k % (4 * group)
+    assert call(out_mode=1) == _abi.HQ_ERR_INVALID             # MXFP4 output
+    assert call(gscale=FAKE) == _abi.HQ_ERR_UNSUPPORTED        # global scale with MXFP8 output
+    assert call(mode=2) == _abi.HQ_ERR_UNSUPPORTED             # NVFP4 operands need alpha
+    assert call(mode=1, alpha=FAKE) == _abi.HQ_ERR_UNSUPPORTED  # MXFP4 operands take no alpha
+    assert call(off=None) == _abi.HQ_ERR_INVALID
+    assert call(L=1025) == _abi.HQ_ERR_INVALID
+    assert call(sf=None) == _abi.HQ_ERR_INVALID
+    assert call(m=0) == _abi.HQ_OK                             # no rows: nothing to do
+
+
 def test_grouped_rows_rejects_bad_arguments(lib):
     f = lib.hq_gemm_grouped_rows
     ws = hq.hq_gemm_grouped_rows_workspace_size(1000, 8)
