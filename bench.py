@@ -559,6 +559,14 @@ class Extras:
                                                   dbias=dbias, d_row=d_row, workspace=ws_t), 20, self.flush)
         res["dgeglu_bwd_L16"] = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_bf16": fl / t / 1e12 / self.p_bf16,
                                  "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / self.hbm}
+        # discrete weights: one pointer per expert (tensor maps built on the device each call)
+        b_ptrs = torch.tensor([c5["b"][e].data_ptr() for e in range(L)], dtype=torch.int64, device=dev)
+        ws_d = torch.empty(hq.hq_gemm_discrete_workspace_size(L, n), dtype=torch.uint8, device=dev)
+        t = time_kernel(lambda: hq.hq_gemm_dglu_discrete(c5["a"], b_ptrs, c5["c"], off, c5["alpha"], c5["prob"],
+                                                         dprob, n, beta=c5["beta"], dbias=dbias, d_row=d_row,
+                                                         workspace=ws_d), 20, self.flush)
+        res["dswiglu_bwd_L16_discrete"] = {"us": t * 1e6, "tflops": fl / t / 1e12,
+                                           "frac_bf16": fl / t / 1e12 / self.p_bf16}
         # block-scaled contract on the same shapes: MXFP8 operands, FP8 D_row + SFD_row
         qa, sfa = hq.hq_quant(c5["a"], "mxfp8")
         qb, sfb = hq.hq_quant(c5["b"].view(L * n, k), "mxfp8")

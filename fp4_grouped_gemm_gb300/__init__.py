@@ -14,7 +14,8 @@ import torch
 
 from . import _abi
 from ._abi import (HQ_MXFP8, HQ_MXFP4, HQ_NVFP4, HQ_STATUS_WAIT_TIMEOUT, HQ_STATUS_MASK_CLAMPED,  # noqa: F401
-                   HQ_STATUS_BAD_OFFSETS, HQ_STATUS_TOKENS_CLAMPED, HQ_STATUS_ROUTING_DROPPED)
+                   HQ_STATUS_BAD_OFFSETS, HQ_STATUS_TOKENS_CLAMPED, HQ_STATUS_ROUTING_DROPPED,
+                   HQ_STATUS_BAD_POINTER)
 
 __all__ = [
     "HQError", "mode_id", "group_size", "sf_bytes", "capabilities", "get_device_status",
@@ -23,6 +24,8 @@ __all__ = [
     "hq_gemm_dswiglu", "hq_gemm_dswiglu_workspace_size", "hq_gemm_dgeglu", "swiglu_kb_dim",
     "hq_prefill_permute", "hq_prefill_permute_workspace_size", "hq_gemm_grouped_rows",
     "hq_gemm_grouped_rows_workspace_size", "hq_gemm_dglu_bs", "hq_gemm_grouped_contig_swiglu_quant",
+    "hq_gemm_discrete_workspace_size", "hq_gemm_grouped_contig_discrete", "hq_gemm_dglu_bs_discrete",
+    "hq_gemm_dglu_discrete",
 ]
 
 _MODES = {"mxfp8": HQ_MXFP8, "w8a8-mxfp8": HQ_MXFP8, "mxfp4": HQ_MXFP4, "w4a4-mxfp4": HQ_MXFP4,
@@ -320,10 +323,30 @@ def hq_gemm_dglu_bs(a, sfa, b, sfb, c, padded_offsets, alpha, prob, dprob, k, mo
     (sfd_row) and optional norm_const; col_out (with fp8_out) also produces the
     column-quantised D_col / SFD_col.  Returns (d_row, sfd_row, dprob, dbias)
     or, with col_out, (d_row, sfd_row, d_col, sfd_col, dprob, dbias)."""
+    return _dglu_bs(a, sfa, b, sfb, None, None, c, padded_offsets, alpha, prob, dprob, k, mode, act,
+                    beta, dbias, d_row, fp8_out, sfd_row, norm_const, col_out, d_col, sfd_col, amax,
+                    workspace, sm_count, stream)
+
+
+def hq_gemm_dglu_bs_discrete(a, sfa, b_ptrs, sfb_ptrs, c, padded_offsets, alpha, prob, dprob, k, mode,
+                             act="dswiglu", beta=None, dbias=None, d_row=None, fp8_out=False,
+                             sfd_row=None, norm_const=None, col_out=False, d_col=None, sfd_col=None,
+                             amax=None, workspace=None, sm_count=-1, stream=None):
+    """hq_gemm_dglu_bs with per-expert weights: b_ptrs / sfb_ptrs are device
+    int64 [L] tensors of the experts' quantised B [n, k] and SfAtom scales."""
+    return _dglu_bs(a, sfa, None, None, b_ptrs, sfb_ptrs, c, padded_offsets, alpha, prob, dprob, k, mode,
+                    act, beta, dbias, d_row, fp8_out, sfd_row, norm_const, col_out, d_col, sfd_col, amax,
+                    workspace, sm_count, stream)
+
+
+def _dglu_bs(a, sfa, b, sfb, b_ptrs, sfb_ptrs, c, padded_offsets, alpha, prob, dprob, k, mode, act, beta,
+             dbias, d_row, fp8_out, sfd_row, norm_const, col_out, d_col, sfd_col, amax, workspace, sm_count,
+             stream):
     m, two_n = c.shape
     n = two_n // 2
     L = padded_offsets.numel()
     dev = c.device
+    discrete = b_ptrs is not None
     if d_row is None:
         d_row = torch.empty(m, two_n, dtype=torch.uint8 if fp8_out else torch.bfloat16, device=dev)
     if fp8_out and sfd_row is None:
@@ -336,17 +359,67 @@ def hq_gemm_dglu_bs(a, sfa, b, sfb, c, padded_offsets, alpha, prob, dprob, k, mo
         if sfd_col is None:
             sfd_col = torch.empty(sf_bytes(two_n, (m + 127) // 128 * 128, "mxfp8"), dtype=torch.uint8,
                                   device=dev)
-    ws_bytes = hq_gemm_dswiglu_workspace_size(L, n)
-    if dbias is not None and workspace is None:
+    if discrete:
+        ws_bytes = hq_gemm_discrete_workspace_size(L, n if dbias is not None else 0)
+    else:
+        ws_bytes = hq_gemm_dswiglu_workspace_size(L, n) if dbias is not None else 0
+    if ws_bytes and workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     acts = {"dswiglu": 0, "dgeglu": 1}
-    rc = _abi.load().hq_gemm_dglu_bs(
-        _ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(c), _ptr(padded_offsets), L, _ptr(alpha),
+    lib = _abi.load()
+    if discrete:
+        fn, name, wargs = lib.hq_gemm_dglu_bs_discrete, "hq_gemm_dglu_bs_discrete", (_ptr(b_ptrs), _ptr(sfb_ptrs))
+    else:
+        fn, name, wargs = lib.hq_gemm_dglu_bs, "hq_gemm_dglu_bs", (_ptr(b), _ptr(sfb))
+    rc = fn(
+        _ptr(a), _ptr(sfa), *wargs, _ptr(c), _ptr(padded_offsets), L, _ptr(alpha),
         _ptr(beta), _ptr(prob), acts[act], _ptr(d_row), _ptr(sfd_row if fp8_out else None),
         _ptr(d_col if col_out else None), _ptr(sfd_col if col_out else None), _ptr(norm_const),
         _ptr(dprob), _ptr(dbias), _ptr(amax), m, n, k, mode_id(mode), _ptr(workspace),
         0 if workspace is None else workspace.numel(), sm_count, _stream(stream))
-    _check(rc, "hq_gemm_dglu_bs")
+    _check(rc, name)
     if col_out:
         return d_row, sfd_row, d_col, sfd_col, dprob, dbias
     return d_row, (sfd_row if fp8_out else None), dprob, dbias
+
+
+def hq_gemm_discrete_workspace_size(L, dbias_n=0):
+    return _abi.load().hq_gemm_discrete_workspace_size(L, dbias_n)
+
+
+def hq_gemm_grouped_contig_discrete(a, sfa, b_ptrs, sfb_ptrs, padded_offsets, m_rows, n, k, mode,
+                                    alpha=None, bias=None, out=None, workspace=None, sm_count=-1,
+                                    stream=None):
+    """hq_gemm_grouped_contig with per-expert weights (device int64 [L] tensors
+    of the experts' quantised B [n, k] and SfAtom scale pointers)."""
+    L = padded_offsets.numel()
+    if out is None:
+        out = torch.empty(m_rows, n, dtype=torch.bfloat16, device=a.device)
+    if workspace is None:
+        workspace = torch.empty(hq_gemm_discrete_workspace_size(L), dtype=torch.uint8, device=a.device)
+    rc = _abi.load().hq_gemm_grouped_contig_discrete(
+        _ptr(a), _ptr(sfa), _ptr(b_ptrs), _ptr(sfb_ptrs), _ptr(padded_offsets), L, _ptr(alpha),
+        _ptr(bias), _ptr(out), m_rows, n, k, mode_id(mode), _ptr(workspace), workspace.numel(), sm_count,
+        _stream(stream))
+    _check(rc, "hq_gemm_grouped_contig_discrete")
+    return out
+
+
+def hq_gemm_dglu_discrete(a, b_ptrs, c, padded_offsets, alpha, prob, dprob, n, act="dswiglu", beta=None,
+                          dbias=None, d_row=None, workspace=None, sm_count=-1, stream=None):
+    """BF16 grouped GEMM + dSwiGLU / dGeGLU with per-expert K-major BF16 weights
+    [n, k] at b_ptrs (device int64 [L]).  dprob (and dbias) accumulate (+=)."""
+    m, k = a.shape
+    L = padded_offsets.numel()
+    if d_row is None:
+        d_row = torch.empty(m, 2 * n, dtype=torch.bfloat16, device=a.device)
+    if workspace is None:
+        workspace = torch.empty(hq_gemm_discrete_workspace_size(L, n if dbias is not None else 0),
+                                dtype=torch.uint8, device=a.device)
+    acts = {"dswiglu": 0, "dgeglu": 1}
+    rc = _abi.load().hq_gemm_dglu_discrete(
+        _ptr(a), _ptr(b_ptrs), _ptr(c), _ptr(padded_offsets), L, _ptr(alpha), _ptr(beta), _ptr(prob),
+        acts[act], _ptr(d_row), _ptr(dprob), _ptr(dbias), m, n, k, _ptr(workspace), workspace.numel(),
+        sm_count, _stream(stream))
+    _check(rc, "hq_gemm_dglu_discrete")
+    return d_row, dprob, dbias

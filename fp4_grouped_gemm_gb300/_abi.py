@@ -31,6 +31,7 @@ HQ_STATUS_MASK_CLAMPED = 0x2
 HQ_STATUS_BAD_OFFSETS = 0x4
 HQ_STATUS_TOKENS_CLAMPED = 0x8
 HQ_STATUS_ROUTING_DROPPED = 0x10
+HQ_STATUS_BAD_POINTER = 0x20
 
 
 class Capabilities(ctypes.Structure):
@@ -62,6 +63,14 @@ SIGNATURES = {
     "hq_gemm_grouped_rows": (c_i32, [c_p, c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_p, c_i64, c_i64,
                                      c_i64, c_i32, c_p, c_sz, c_i32, c_p]),
     "hq_gemm_grouped_rows_workspace_size": (c_sz, [c_i64, c_i32]),
+    "hq_gemm_discrete_workspace_size": (c_sz, [c_i32, c_i64]),
+    "hq_gemm_grouped_contig_discrete": (c_i32, [c_p, c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_p, c_i64,
+                                                c_i64, c_i64, c_i32, c_p, c_sz, c_i32, c_p]),
+    "hq_gemm_dglu_bs_discrete": (c_i32, [c_p, c_p, c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_p, c_i32, c_p,
+                                         c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_i32,
+                                         c_p, c_sz, c_i32, c_p]),
+    "hq_gemm_dglu_discrete": (c_i32, [c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_p, c_i32, c_p, c_p, c_p,
+                                      c_i64, c_i64, c_i64, c_p, c_sz, c_i32, c_p]),
     "hq_gemm_grouped_masked": (c_i32, [c_p, c_p, c_p, c_p, c_p, c_i32, c_i64, c_p, c_p, c_p,
                                        c_i64, c_i64, c_i32, c_i32, c_p]),
     "hq_swiglu_quant": (c_i32, [c_p, c_i64, c_i64, c_p, c_i32, c_i64, c_i32, c_p, c_p, c_p, c_p]),

@@ -112,9 +112,66 @@ __global__ void selftest_wait_kernel(uint32_t* status, uint64_t limit_ns) {
   __syncthreads();
 }
 
+// ---------------------------------------------------------------------------
+// Discrete weights (cuDNN frontend "Grouped GEMM + dGLU (SM100)", discrete
+// mode: b_ptrs / sfb_ptrs hold one device pointer per expert).  One warp per
+// expert copies the host-encoded template tensor map (the stacked layout of one
+// expert) into shared memory, replaces its global address with b_ptrs[g] and
+// publishes the result to maps[g] with the release fence of the tensor-map
+// proxy; a kernel that loads through maps[g] issues the matching acquire
+// before its first copy.  ok[g] = 1 when the expert's pointers are non-null
+// and 16-byte aligned; otherwise ok[g] = 0, maps[g] keeps the template's
+// address, HQ_STATUS_BAD_POINTER is set, and the GEMMs skip that expert.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) weight_maps_kernel(const __grid_constant__ CUtensorMap tmpl,
+                                                          const int64_t* b_ptrs, const int64_t* sfb_ptrs,
+                                                          CUtensorMap* maps, int32_t* ok, int L,
+                                                          uint32_t* status) {
+  __shared__ alignas(128) CUtensorMap sm[4];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = blockIdx.x * 4 + warp;
+  if (g >= L) return;  // warp-uniform
+  const uint64_t b = static_cast<uint64_t>(__ldg(b_ptrs + g));
+  const uint64_t sf = sfb_ptrs ? static_cast<uint64_t>(__ldg(sfb_ptrs + g)) : 16u;
+  const bool good = b != 0 && (b & 15u) == 0 && sf != 0 && (sf & 15u) == 0;
+  reinterpret_cast<uint32_t*>(&sm[warp])[lane] = reinterpret_cast<const uint32_t*>(&tmpl)[lane];
+  __syncwarp();
+  const uint32_t sa = smem_u32(&sm[warp]);
+  if (lane == 0 && good)
+    asm volatile("tensormap.replace.tile.global_address.shared::cta.b1024.b64 [%0], %1;" ::"r"(sa),
+                 "l"(b)
+                 : "memory");
+  __syncwarp();
+  asm volatile(
+      "tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.gpu.sync.aligned"
+      " [%0], [%1], 128;" ::"l"(reinterpret_cast<uint64_t>(maps + g)),
+      "r"(sa)
+      : "memory");
+  if (lane == 0) {
+    ok[g] = good ? 1 : 0;
+    if (!good) atomicOr(status, HQ_STATUS_BAD_POINTER);
+  }
+}
+
+int build_weight_maps(const CUtensorMap& tmpl, const int64_t* b_ptrs, const int64_t* sfb_ptrs,
+                      CUtensorMap* maps, int32_t* ok, int L, cudaStream_t st) {
+  uint32_t* status = status_word_ptr();
+  if (!status) return HQ_ERR_CUDA;
+  weight_maps_kernel<<<(L + 3) / 4, 128, 0, st>>>(tmpl, b_ptrs, sfb_ptrs, maps, ok, L, status);
+  return cudaGetLastError() == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
+}
+
 }  // namespace hq
 
 extern "C" {
+
+size_t hq_gemm_discrete_workspace_size(int L, int64_t dbias_n) {
+  if (L < 1 || dbias_n < 0) return 0;
+  size_t bytes = hq::discrete_maps_bytes(L);
+  if (dbias_n > 0) bytes += (static_cast<size_t>(L) * 2 * dbias_n * sizeof(float) + 255) / 256 * 256;
+  return bytes;
+}
+
 
 int hq_capabilities(hq_capabilities_t* out) {
   if (!out) return HQ_ERR_INVALID;

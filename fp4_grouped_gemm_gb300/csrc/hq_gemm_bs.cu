@@ -77,6 +77,14 @@ struct GemmParams {
   int64_t sfq_cols;          // MXFP8: ceil(H / 512) * 16; NVFP4: H / 16
   int q_mode;                // HQ_MXFP8 or HQ_NVFP4
   const float* q_gscale;     // NVFP4 global scale (device [1]) or null (= 1)
+  // discrete weights (one pointer per expert): B of group g is loaded through
+  // b_maps[g], built on the device from b_ptrs[g] before the GEMM; its scales
+  // start at sfb_ptrs[g]; w_ok[g] == 0 marks an expert whose pointers failed
+  // the device checks (its tiles load nothing from B and write nothing)
+  const int64_t* b_ptrs;     // [groups], or null: B stacked as [groups, n, k]
+  const int64_t* sfb_ptrs;   // [groups]
+  CUtensorMap* b_maps;       // [groups] in the caller's workspace
+  int32_t* w_ok;             // [groups] in the caller's workspace
 };
 
 enum Epi : int { kEpiGemm = 0, kEpiDSwiGLU = 1, kEpiDGeGLU = 2, kEpiSwiGLUQ = 3 };
@@ -615,6 +623,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int v = static_cast<int>((p.n - ti.n0 + 127) / 128);
     return v < C::RB ? v : C::RB;
   };
+  // discrete weights: an expert whose pointers failed the checks writes nothing
+  auto tile_ok = [&](const TileInfo& ti) -> bool { return !p.w_ok || __ldg(p.w_ok + ti.g) != 0; };
   Schedule sch;
   sch.n_tiles = static_cast<int>((p.n + TW - 1) / TW);
   sch.total_tiles = *total_mtiles_s * sch.n_tiles;
@@ -631,29 +641,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       uint32_t filled_mask = 0, last_parity = 0;
       bool ok = true;
+      int map_g = -1;  // group whose discrete tensor map was last acquired
       for (int64_t t = blockIdx.x; ok && t < sch.total_tiles; t += gridDim.x) {
         const TileInfo ti = decode_tile(p.gs, sch, t, TW);
         const uint8_t* sfa_rows = p.sfa + (ti.row0 / kBM) * atoms_total * 512;
-        const uint8_t* sfb_grp = p.sfb + static_cast<int64_t>(ti.g) * p.sfb_group_bytes;
+        // stacked B: one map over all groups (z = group); discrete B: the
+        // group's own map (z = 0) and scale pointer
+        const CUtensorMap* mapB = &tmB;
+        int32_t zb = ti.g;
+        bool w_ok = true;
+        const uint8_t* sfb_grp;
+        if (p.b_maps) {
+          mapB = p.b_maps + ti.g;
+          zb = 0;
+          w_ok = __ldg(p.w_ok + ti.g) != 0;
+          sfb_grp = reinterpret_cast<const uint8_t*>(__ldg(p.sfb_ptrs + ti.g));
+          if (ti.g != map_g) {
+            tensormap_acquire(mapB);
+            map_g = ti.g;
+          }
+        } else {
+          sfb_grp = p.sfb + static_cast<int64_t>(ti.g) * p.sfb_group_bytes;
+        }
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, wctx)) { ok = false; break; }
           int atoms = atoms_total - kb * C::ATOMS;
           atoms = atoms < C::ATOMS ? atoms : C::ATOMS;
-          const int rb_valid = rb_of(ti);
-          const uint32_t bytes = C::A_BYTES + C::B_BYTES + atoms * 512u * (1 + rb_valid);
+          // a skipped expert's stage holds stale B data: its MMAs run, its
+          // results are never stored
+          const int rb_valid = w_ok ? rb_of(ti) : 0;
+          const uint32_t bytes =
+              C::A_BYTES + (w_ok ? C::B_BYTES : 0u) + atoms * 512u * (1 + rb_valid);
           mbar_arrive_expect_tx(full_bar(stage), bytes);
           tma_load_2d(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, full_bar(stage),
                       kb * kBKBytes, static_cast<int32_t>(ti.row0));
-          if (kUpProj) {
+          if (!w_ok) {
+          } else if (kUpProj) {
             // two 128-row boxes; with the 128-byte swizzle repeating every 8
             // rows the pair lands exactly as one 256-row box would
-            tma_load_3d(sbase + C::OFF_B + stage * C::B_BYTES, &tmB, full_bar(stage),
-                        kb * kBKBytes, ti.n0, ti.g);
-            tma_load_3d(sbase + C::OFF_B + stage * C::B_BYTES + 128 * kBKBytes, &tmB, full_bar(stage),
-                        kb * kBKBytes, static_cast<int32_t>(p.n + ti.n0), ti.g);
+            tma_load_3d(sbase + C::OFF_B + stage * C::B_BYTES, mapB, full_bar(stage),
+                        kb * kBKBytes, ti.n0, zb);
+            tma_load_3d(sbase + C::OFF_B + stage * C::B_BYTES + 128 * kBKBytes, mapB, full_bar(stage),
+                        kb * kBKBytes, static_cast<int32_t>(p.n + ti.n0), zb);
           } else {
-            tma_load_3d(sbase + C::OFF_B + stage * C::B_BYTES, &tmB, full_bar(stage),
-                        kb * kBKBytes, ti.n0, ti.g);
+            tma_load_3d(sbase + C::OFF_B + stage * C::B_BYTES, mapB, full_bar(stage),
+                        kb * kBKBytes, ti.n0, zb);
           }
           bulk_load(sbase + C::OFF_SFA + stage * C::SFA_BYTES, sfa_rows + kb * C::ATOMS * 512,
                     atoms * 512u, full_bar(stage));
@@ -861,7 +893,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(tempty_bar(acc));
         const int r_local = q * 32 + lane;
-        if (r_local >= ti.row_lo && r_local < ti.rows_valid) {
+        if (r_local >= ti.row_lo && r_local < ti.rows_valid && tile_ok(ti)) {
           const int64_t row = ti.row0 + r_local;
           swiglu_store(p, y, row, ti.n0 + 64 * h, gq);
           // MXFP8 scale columns past H / 32 (the layout pads them to a
@@ -913,7 +945,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));
           }
-          if (chunk_ok) dglu_chunk<EPI>(p, r, cv, row_ok, row, j0, ti.g, a2, beta, prob, norm, lane);
+          if (chunk_ok && tile_ok(ti))
+            dglu_chunk<EPI>(p, r, cv, row_ok, row, j0, ti.g, a2, beta, prob, norm, lane);
         }
         if (!ok) break;
         if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
@@ -934,7 +967,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       e.alpha = alpha;
       e.bias = p.bias ? p.bias + static_cast<int64_t>(ti.g) * p.n : nullptr;
       e.out = p.out + (ti.row0 + q * 32) * p.n;
-      e.rows_here = ti.rows_valid - q * 32;
+      e.rows_here = tile_ok(ti) ? ti.rows_valid - q * 32 : 0;
       e.rows_lo = ti.row_lo - q * 32;
       e.stage_s = sbase + C::OFF_STAGE_OUT + ew * 1024;
       e.lane = lane;
@@ -1312,12 +1345,22 @@ int run_bs(const void* a, const void* b, const GemmParams& p0, int sm_count, boo
   constexpr bool kUpProj = EPI == kEpiSwiGLUQ;
   const uint64_t b_rows = static_cast<uint64_t>(kUpProj ? 2 * p.n : p.n);
   {
-    const uint64_t dims[3] = {kbytes, b_rows, static_cast<uint64_t>(p.gs.groups)};
+    // discrete weights: a one-group map whose address the device replaces per
+    // expert; it is encoded over the workspace (a valid address) and is never
+    // loaded through as it stands
+    const bool discrete = p.b_ptrs != nullptr;
+    const uint64_t groups = discrete ? 1 : static_cast<uint64_t>(p.gs.groups);
+    const uint64_t dims[3] = {kbytes, b_rows, groups};
     const uint64_t strides[2] = {kbytes, kbytes * b_rows};
     const uint32_t box[3] = {kBKBytes, static_cast<uint32_t>(kUpProj ? 128 : BN), 1};
-    int rc = encode_tensor_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(b), dims,
-                               strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    void* base = discrete ? static_cast<void*>(p.b_maps) : const_cast<void*>(b);
+    int rc = encode_tensor_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != HQ_OK) return rc;
+    if (discrete) {
+      rc = build_weight_maps(tmB, p.b_ptrs, p.sfb_ptrs, p.b_maps, p.w_ok, p.gs.groups, st);
+      if (rc != HQ_OK) return rc;
+    }
   }
   auto kern = bs_gemm_kernel<MODE, BN, STAGES, ACC, TABLE, EPI>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
@@ -1425,15 +1468,19 @@ int run_gemm(hq_mode mode, const void* a, const void* b, const GemmParams& p, in
 }
 
 // Host-side checks shared by the three entry points.
-int check_common(const void* a, const uint8_t* sfa, const void* b, const uint8_t* sfb,
-                 const float* alpha, const hq_bf16* bias, const hq_bf16* out, int64_t n, int64_t k,
-                 hq_mode mode) {
+// With discrete weights b and sfb are the device arrays of per-expert
+// pointers (8-byte aligned); the pointers themselves are checked on the device.
+int check_common(const void* a, const uint8_t* sfa, const void* b, const void* sfb,
+                 const float* alpha, const hq_bf16* bias, const void* out, int64_t n, int64_t k,
+                 hq_mode mode, bool discrete = false) {
   if (mode != HQ_MXFP8 && mode != HQ_MXFP4 && mode != HQ_NVFP4) return HQ_ERR_INVALID;
   const int64_t gs = mode == HQ_NVFP4 ? 16 : 32;
   if (n <= 0 || k <= 0 || k % (4 * gs) != 0 || n % 128 != 0) return HQ_ERR_INVALID;
   if (n > (1ll << 30) || k > (1ll << 30)) return HQ_ERR_INVALID;
   if (!a || !sfa || !b || !sfb || !out) return HQ_ERR_INVALID;
-  if (!aligned16(a) || !aligned16(sfa) || !aligned16(b) || !aligned16(sfb) || !aligned16(out))
+  if (!aligned16(a) || !aligned16(sfa) || !aligned16(out)) return HQ_ERR_INVALID;
+  if (discrete ? ((reinterpret_cast<uintptr_t>(b) | reinterpret_cast<uintptr_t>(sfb)) & 7u) != 0
+               : (!aligned16(b) || !aligned16(sfb)))
     return HQ_ERR_INVALID;
   if (bias && !aligned16(bias)) return HQ_ERR_INVALID;
   if (alpha && (reinterpret_cast<uintptr_t>(alpha) & 3u)) return HQ_ERR_INVALID;
@@ -1589,6 +1636,108 @@ GemmParams base_params(const uint8_t* sfa, const uint8_t* sfb, const float* alph
   return p;
 }
 
+// Points p at per-expert weights: the tensor maps and flags go to the start
+// of the caller's workspace (checked by the caller to hold
+// discrete_maps_bytes(L) bytes, 256-byte aligned).
+void set_discrete(GemmParams& p, const int64_t* b_ptrs, const int64_t* sfb_ptrs, void* workspace,
+                  int L) {
+  p.b_ptrs = b_ptrs;
+  p.sfb_ptrs = sfb_ptrs;
+  p.b_maps = static_cast<CUtensorMap*>(workspace);
+  p.w_ok = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) +
+                                      static_cast<size_t>(L) * sizeof(CUtensorMap));
+}
+
+bool workspace_ok(const void* ws, size_t ws_bytes, size_t need) {
+  return ws && (reinterpret_cast<uintptr_t>(ws) & 255u) == 0 && ws_bytes >= need;
+}
+
+// Block-scaled grouped GEMM + dGLU backward, stacked (b, sfb) or discrete
+// (b_ptrs, sfb_ptrs) weights.
+int dglu_bs_impl(const void* a, const uint8_t* sfa, const void* b, const uint8_t* sfb,
+                 const int64_t* b_ptrs, const int64_t* sfb_ptrs, const hq_bf16* c, const int32_t* padded_offsets, int L, const float* alpha,
+                    const float* beta, const float* prob, int act, void* d_row, uint8_t* sfd_row,
+                    void* d_col, uint8_t* sfd_col, const float* norm_const, float* dprob,
+                    hq_bf16* dbias, float* amax, int64_t m, int64_t n, int64_t k, hq_mode mode,
+                    void* workspace, size_t ws_bytes, int sm_count, hq_stream_t s) {
+  if (act != 0 && act != 1) return HQ_ERR_INVALID;
+  if (mode != HQ_MXFP8 && mode != HQ_MXFP4 && mode != HQ_NVFP4) return HQ_ERR_INVALID;
+  const int64_t gs = mode == HQ_NVFP4 ? 16 : 32;
+  if (n <= 0 || k <= 0 || k % (4 * gs) != 0 || n % 128 != 0) return HQ_ERR_INVALID;
+  if (n > (1ll << 28) || k > (1ll << 30)) return HQ_ERR_INVALID;
+  if (m < 0 || m > (1ll << 31) - 256) return HQ_ERR_INVALID;
+  if (L < 1 || L > kMaxGroups) return HQ_ERR_INVALID;
+  const bool discrete = b_ptrs != nullptr;
+  if (discrete ? (!sfb_ptrs || ((reinterpret_cast<uintptr_t>(b_ptrs) |
+                                 reinterpret_cast<uintptr_t>(sfb_ptrs)) & 7u))
+               : (!b || !sfb))
+    return HQ_ERR_INVALID;
+  if (!a || !sfa || !c || !padded_offsets || !alpha || !prob || !d_row || !dprob)
+    return HQ_ERR_INVALID;
+  if (act == 0 && !beta) return HQ_ERR_INVALID;
+  if (!aligned16(a) || !aligned16(sfa) || (!discrete && (!aligned16(b) || !aligned16(sfb))) ||
+      !aligned16(c) || !aligned16(d_row) || (sfd_row && !aligned16(sfd_row)))
+    return HQ_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(padded_offsets) | reinterpret_cast<uintptr_t>(alpha) |
+       reinterpret_cast<uintptr_t>(beta ? beta : alpha) | reinterpret_cast<uintptr_t>(prob) |
+       reinterpret_cast<uintptr_t>(dprob) |
+       reinterpret_cast<uintptr_t>(norm_const ? norm_const : alpha)) & 3u)
+    return HQ_ERR_INVALID;
+  if (norm_const && !sfd_row) return HQ_ERR_INVALID;  // norm_const belongs to the FP8 output
+  if ((d_col != nullptr) != (sfd_col != nullptr) || (d_col && !sfd_row)) return HQ_ERR_INVALID;
+  if (d_col && (!aligned16(d_col) || !aligned16(sfd_col))) return HQ_ERR_INVALID;
+  if (amax && (reinterpret_cast<uintptr_t>(amax) & 3u)) return HQ_ERR_INVALID;
+  // workspace: [per-expert tensor maps and flags (discrete weights)] [dbias sums]
+  const size_t maps_bytes = discrete ? discrete_maps_bytes(L) : 0;
+  if (dbias && (reinterpret_cast<uintptr_t>(dbias) & 1u)) return HQ_ERR_INVALID;
+  if ((dbias || discrete) &&
+      !workspace_ok(workspace, ws_bytes, maps_bytes + (dbias ? hq_gemm_dswiglu_workspace_size(L, n) : 0)))
+    return HQ_ERR_INVALID;
+  if (m == 0) return HQ_OK;
+  GemmParams p = base_params(sfa, sfb, alpha, nullptr, nullptr, n, k, mode);
+  if (discrete) set_discrete(p, b_ptrs, sfb_ptrs, workspace, L);
+  void* dbias_ws = dbias ? static_cast<uint8_t*>(workspace) + maps_bytes : nullptr;
+  if (!p.gs.status) return HQ_ERR_CUDA;
+  p.gs.a_rows = m;
+  p.gs.groups = L;
+  p.gs.group_info = padded_offsets;
+  p.gs.sched = kContig;
+  p.c = c;
+  p.beta = beta;
+  p.prob = prob;
+  p.dprob = dprob;
+  p.dbias_ws = static_cast<float*>(dbias_ws);
+  p.d_row = static_cast<uint8_t*>(d_row);
+  p.sfd_row = sfd_row;
+  p.norm_const = norm_const;
+  p.d_col = static_cast<uint8_t*>(d_col);
+  p.sfd_col = sfd_col;
+  p.sfd_col_s = (m + 127) / 128 * 4;
+  p.amax = amax;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  if (amax && cudaMemsetAsync(amax, 0, static_cast<size_t>(L) * 2 * sizeof(float), st) != cudaSuccess)
+    return HQ_ERR_CUDA;
+  const int64_t ws_count = static_cast<int64_t>(L) * 2 * n;
+  if (dbias && cudaMemsetAsync(dbias_ws, 0, ws_count * sizeof(float), st) != cudaSuccess)
+    return HQ_ERR_CUDA;
+  constexpr int T = kMaxGroups + 1;
+  int rc;
+  if (mode == HQ_MXFP8)
+    rc = act == 0 ? run_bs<HQ_MXFP8, 128, 6, 2, T, kEpiDSwiGLU>(a, b, p, sm_count, false, st)
+                  : run_bs<HQ_MXFP8, 128, 6, 2, T, kEpiDGeGLU>(a, b, p, sm_count, false, st);
+  else if (mode == HQ_MXFP4)
+    rc = act == 0 ? run_bs<HQ_MXFP4, 128, 5, 2, T, kEpiDSwiGLU>(a, b, p, sm_count, false, st)
+                  : run_bs<HQ_MXFP4, 128, 5, 2, T, kEpiDGeGLU>(a, b, p, sm_count, false, st);
+  else
+    rc = act == 0 ? run_bs<HQ_NVFP4, 128, 5, 2, T, kEpiDSwiGLU>(a, b, p, sm_count, false, st)
+                  : run_bs<HQ_NVFP4, 128, 5, 2, T, kEpiDGeGLU>(a, b, p, sm_count, false, st);
+  if (rc != HQ_OK) return rc;
+  if (dbias)
+    return dbias_finalize(reinterpret_cast<uint16_t*>(dbias), static_cast<const float*>(dbias_ws),
+                          ws_count, st);
+  return HQ_OK;
+}
+
 }  // namespace
 }  // namespace hq
 
@@ -1626,6 +1775,28 @@ int hq_gemm_grouped_contig(const void* a, const uint8_t* sfa, const void* b, con
   p.gs.group_info = padded_offsets;
   p.gs.sched = hq::kContig;
   return hq::run_gemm(mode, a, b, p, sm_count, false, reinterpret_cast<cudaStream_t>(s));
+}
+
+int hq_gemm_grouped_contig_discrete(const void* a, const uint8_t* sfa, const int64_t* b_ptrs,
+                                    const int64_t* sfb_ptrs, const int32_t* padded_offsets, int L,
+                                    const float* alpha, const hq_bf16* bias, hq_bf16* out,
+                                    int64_t m_rows, int64_t n, int64_t k, hq_mode mode,
+                                    void* workspace, size_t ws_bytes, int sm_count, hq_stream_t s) {
+  int rc = hq::check_common(a, sfa, b_ptrs, sfb_ptrs, alpha, bias, out, n, k, mode, true);
+  if (rc != HQ_OK) return rc;
+  if (!padded_offsets || L < 1 || L > hq::kMaxGroups) return HQ_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(padded_offsets) & 3u) return HQ_ERR_INVALID;
+  if (m_rows < 0 || m_rows > (1ll << 31) - 256) return HQ_ERR_INVALID;
+  if (!hq::workspace_ok(workspace, ws_bytes, hq::discrete_maps_bytes(L))) return HQ_ERR_INVALID;
+  if (m_rows == 0) return HQ_OK;
+  hq::GemmParams p = hq::base_params(sfa, nullptr, alpha, bias, out, n, k, mode);
+  if (!p.gs.status) return HQ_ERR_CUDA;
+  p.gs.a_rows = m_rows;
+  p.gs.groups = L;
+  p.gs.group_info = padded_offsets;
+  p.gs.sched = hq::kContig;
+  hq::set_discrete(p, b_ptrs, sfb_ptrs, workspace, L);
+  return hq::run_gemm(mode, a, nullptr, p, sm_count, false, reinterpret_cast<cudaStream_t>(s));
 }
 
 int hq_gemm_grouped_contig_swiglu_quant(const void* a, const uint8_t* sfa, const void* b,
@@ -1671,74 +1842,23 @@ int hq_gemm_dglu_bs(const void* a, const uint8_t* sfa, const void* b, const uint
                     void* d_col, uint8_t* sfd_col, const float* norm_const, float* dprob,
                     hq_bf16* dbias, float* amax, int64_t m, int64_t n, int64_t k, hq_mode mode,
                     void* workspace, size_t ws_bytes, int sm_count, hq_stream_t s) {
-  if (act != 0 && act != 1) return HQ_ERR_INVALID;
-  if (mode != HQ_MXFP8 && mode != HQ_MXFP4 && mode != HQ_NVFP4) return HQ_ERR_INVALID;
-  const int64_t gs = mode == HQ_NVFP4 ? 16 : 32;
-  if (n <= 0 || k <= 0 || k % (4 * gs) != 0 || n % 128 != 0) return HQ_ERR_INVALID;
-  if (n > (1ll << 28) || k > (1ll << 30)) return HQ_ERR_INVALID;
-  if (m < 0 || m > (1ll << 31) - 256) return HQ_ERR_INVALID;
-  if (L < 1 || L > hq::kMaxGroups) return HQ_ERR_INVALID;
-  if (!a || !sfa || !b || !sfb || !c || !padded_offsets || !alpha || !prob || !d_row || !dprob)
-    return HQ_ERR_INVALID;
-  if (act == 0 && !beta) return HQ_ERR_INVALID;
-  if (!hq::aligned16(a) || !hq::aligned16(sfa) || !hq::aligned16(b) || !hq::aligned16(sfb) ||
-      !hq::aligned16(c) || !hq::aligned16(d_row) || (sfd_row && !hq::aligned16(sfd_row)))
-    return HQ_ERR_INVALID;
-  if ((reinterpret_cast<uintptr_t>(padded_offsets) | reinterpret_cast<uintptr_t>(alpha) |
-       reinterpret_cast<uintptr_t>(beta ? beta : alpha) | reinterpret_cast<uintptr_t>(prob) |
-       reinterpret_cast<uintptr_t>(dprob) |
-       reinterpret_cast<uintptr_t>(norm_const ? norm_const : alpha)) & 3u)
-    return HQ_ERR_INVALID;
-  if (norm_const && !sfd_row) return HQ_ERR_INVALID;  // norm_const belongs to the FP8 output
-  if ((d_col != nullptr) != (sfd_col != nullptr) || (d_col && !sfd_row)) return HQ_ERR_INVALID;
-  if (d_col && (!hq::aligned16(d_col) || !hq::aligned16(sfd_col))) return HQ_ERR_INVALID;
-  if (amax && (reinterpret_cast<uintptr_t>(amax) & 3u)) return HQ_ERR_INVALID;
-  if (dbias) {
-    if (reinterpret_cast<uintptr_t>(dbias) & 1u) return HQ_ERR_INVALID;
-    if (!workspace || ws_bytes < hq_gemm_dswiglu_workspace_size(L, n)) return HQ_ERR_INVALID;
-    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return HQ_ERR_INVALID;
-  }
-  if (m == 0) return HQ_OK;
-  hq::GemmParams p = hq::base_params(sfa, sfb, alpha, nullptr, nullptr, n, k, mode);
-  if (!p.gs.status) return HQ_ERR_CUDA;
-  p.gs.a_rows = m;
-  p.gs.groups = L;
-  p.gs.group_info = padded_offsets;
-  p.gs.sched = hq::kContig;
-  p.c = c;
-  p.beta = beta;
-  p.prob = prob;
-  p.dprob = dprob;
-  p.dbias_ws = dbias ? static_cast<float*>(workspace) : nullptr;
-  p.d_row = static_cast<uint8_t*>(d_row);
-  p.sfd_row = sfd_row;
-  p.norm_const = norm_const;
-  p.d_col = static_cast<uint8_t*>(d_col);
-  p.sfd_col = sfd_col;
-  p.sfd_col_s = (m + 127) / 128 * 4;
-  p.amax = amax;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
-  if (amax && cudaMemsetAsync(amax, 0, static_cast<size_t>(L) * 2 * sizeof(float), st) != cudaSuccess)
-    return HQ_ERR_CUDA;
-  const int64_t ws_count = static_cast<int64_t>(L) * 2 * n;
-  if (dbias && cudaMemsetAsync(workspace, 0, ws_count * sizeof(float), st) != cudaSuccess)
-    return HQ_ERR_CUDA;
-  constexpr int T = hq::kMaxGroups + 1;
-  int rc;
-  if (mode == HQ_MXFP8)
-    rc = act == 0 ? hq::run_bs<HQ_MXFP8, 128, 6, 2, T, hq::kEpiDSwiGLU>(a, b, p, sm_count, false, st)
-                  : hq::run_bs<HQ_MXFP8, 128, 6, 2, T, hq::kEpiDGeGLU>(a, b, p, sm_count, false, st);
-  else if (mode == HQ_MXFP4)
-    rc = act == 0 ? hq::run_bs<HQ_MXFP4, 128, 5, 2, T, hq::kEpiDSwiGLU>(a, b, p, sm_count, false, st)
-                  : hq::run_bs<HQ_MXFP4, 128, 5, 2, T, hq::kEpiDGeGLU>(a, b, p, sm_count, false, st);
-  else
-    rc = act == 0 ? hq::run_bs<HQ_NVFP4, 128, 5, 2, T, hq::kEpiDSwiGLU>(a, b, p, sm_count, false, st)
-                  : hq::run_bs<HQ_NVFP4, 128, 5, 2, T, hq::kEpiDGeGLU>(a, b, p, sm_count, false, st);
-  if (rc != HQ_OK) return rc;
-  if (dbias)
-    return hq::dbias_finalize(reinterpret_cast<uint16_t*>(dbias), static_cast<const float*>(workspace),
-                              ws_count, st);
-  return HQ_OK;
+  return hq::dglu_bs_impl(a, sfa, b, sfb, nullptr, nullptr, c, padded_offsets, L, alpha, beta, prob,
+                          act, d_row, sfd_row, d_col, sfd_col, norm_const, dprob, dbias, amax, m, n,
+                          k, mode, workspace, ws_bytes, sm_count, s);
+}
+
+int hq_gemm_dglu_bs_discrete(const void* a, const uint8_t* sfa, const int64_t* b_ptrs,
+                             const int64_t* sfb_ptrs, const hq_bf16* c,
+                             const int32_t* padded_offsets, int L, const float* alpha,
+                             const float* beta, const float* prob, int act, void* d_row,
+                             uint8_t* sfd_row, void* d_col, uint8_t* sfd_col,
+                             const float* norm_const, float* dprob, hq_bf16* dbias, float* amax,
+                             int64_t m, int64_t n, int64_t k, hq_mode mode, void* workspace,
+                             size_t ws_bytes, int sm_count, hq_stream_t s) {
+  if (!b_ptrs) return HQ_ERR_INVALID;
+  return hq::dglu_bs_impl(a, sfa, nullptr, nullptr, b_ptrs, sfb_ptrs, c, padded_offsets, L, alpha,
+                          beta, prob, act, d_row, sfd_row, d_col, sfd_col, norm_const, dprob, dbias,
+                          amax, m, n, k, mode, workspace, ws_bytes, sm_count, s);
 }
 
 size_t hq_gemm_grouped_rows_workspace_size(int64_t m_rows, int L) {

@@ -66,6 +66,10 @@ struct DsParams {
   float* dbias_ws;        // [L, 2n] float32 partial sums, or null
   int64_t n, k;
   uint64_t wait_limit_ns;
+  // discrete weights: B of group g through b_maps[g] (built on the device
+  // from per-expert pointers); w_ok[g] == 0: the expert is skipped
+  CUtensorMap* b_maps;    // [L] or null (B stacked as [L, n, k])
+  int32_t* w_ok;          // [L]
 };
 
 __device__ __forceinline__ float rcp_approx(float x) {
@@ -140,15 +144,30 @@ __global__ void __maxnreg__(96)
       int stage = 0;
       uint32_t phase = 0, filled_mask = 0, last_parity = 0;
       bool ok = true;
+      int map_g = -1;  // group whose discrete tensor map was last acquired
       for (int64_t t = blockIdx.x; ok && t < sch.total_tiles; t += gridDim.x) {
         const TileInfo ti = decode_tile(p.gs, sch, t, kBN);
+        const CUtensorMap* mapB = &tmB;
+        int32_t zb = ti.g;
+        bool w_ok = true;
+        if (p.b_maps) {
+          mapB = p.b_maps + ti.g;
+          zb = 0;
+          w_ok = __ldg(p.w_ok + ti.g) != 0;
+          if (ti.g != map_g) {
+            tensormap_acquire(mapB);
+            map_g = ti.g;
+          }
+        }
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, wctx)) { ok = false; break; }
-          mbar_arrive_expect_tx(full_bar(stage), kABytes + kBBytes);
+          // a skipped expert's stage holds stale B data; its results are never stored
+          mbar_arrive_expect_tx(full_bar(stage), kABytes + (w_ok ? kBBytes : 0u));
           tma_load_2d(sbase + kOffA + stage * kABytes, &tmA, full_bar(stage), kb * kBKElems,
                       static_cast<int32_t>(ti.row0));
-          tma_load_3d(sbase + kOffB + stage * kBBytes, &tmB, full_bar(stage), kb * kBKElems, ti.n0,
-                      ti.g);
+          if (w_ok)
+            tma_load_3d(sbase + kOffB + stage * kBBytes, mapB, full_bar(stage), kb * kBKElems, ti.n0,
+                        zb);
           filled_mask |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -201,7 +220,8 @@ __global__ void __maxnreg__(96)
       const bool row_ok = r_local < ti.rows_valid;
       const int64_t row = ti.row0 + r_local;
       const int64_t j0 = ti.n0 + c * 32;
-      const bool chunk_ok = j0 < p.n;  // n % 32 == 0: a chunk is all in or all out
+      // n % 32 == 0: a chunk is all in or all out; a skipped expert writes nothing
+      const bool chunk_ok = j0 < p.n && (!p.w_ok || __ldg(p.w_ok + ti.g) != 0);
       // this row's C segment (32 gate then 32 input values) is loaded before
       // the accumulator is ready, so its latency overlaps the wait
       const int64_t cbase = row * two_n + 2 * j0;
@@ -373,28 +393,37 @@ size_t hq_gemm_dswiglu_workspace_size(int L, int64_t n) {
 namespace hq {
 namespace {
 
+// b: stacked weights [L, n, k]; or b == null and b_ptrs: one device pointer
+// per expert (discrete weights), tensor maps built in the workspace's head.
 template <int ACT>
-int run_dglu(const hq_bf16* a, const hq_bf16* b, const hq_bf16* c, const int32_t* padded_offsets,
-             int L, const float* alpha, const float* beta, const float* prob, hq_bf16* d_row,
-             float* dprob, hq_bf16* dbias, int64_t m, int64_t n, int64_t k, void* workspace,
-             size_t ws_bytes, int sm_count, hq_stream_t s) {
+int run_dglu(const hq_bf16* a, const hq_bf16* b, const int64_t* b_ptrs, const hq_bf16* c,
+             const int32_t* padded_offsets, int L, const float* alpha, const float* beta,
+             const float* prob, hq_bf16* d_row, float* dprob, hq_bf16* dbias, int64_t m, int64_t n,
+             int64_t k, void* workspace, size_t ws_bytes, int sm_count, hq_stream_t s) {
   if (L < 1 || L > kMaxGroups) return HQ_ERR_INVALID;
   if (m < 0 || n <= 0 || k <= 0 || n % 32 != 0 || k % 8 != 0) return HQ_ERR_INVALID;
   if (m > (1ll << 31) - 256 || n > (1ll << 28) || k > (1ll << 30)) return HQ_ERR_INVALID;
-  if (!a || !b || !c || !padded_offsets || !alpha || !prob || !d_row || !dprob)
+  const bool discrete = b_ptrs != nullptr;
+  if (!a || !(b || discrete) || !c || !padded_offsets || !alpha || !prob || !d_row || !dprob)
     return HQ_ERR_INVALID;
   if (ACT == kSwiGLU && !beta) return HQ_ERR_INVALID;
-  if (!aligned16(a) || !aligned16(b) || !aligned16(c) || !aligned16(d_row)) return HQ_ERR_INVALID;
+  if (!aligned16(a) || (!discrete && !aligned16(b)) || !aligned16(c) || !aligned16(d_row))
+    return HQ_ERR_INVALID;
+  if (discrete && (reinterpret_cast<uintptr_t>(b_ptrs) & 7u)) return HQ_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(padded_offsets) | reinterpret_cast<uintptr_t>(alpha) |
        reinterpret_cast<uintptr_t>(beta ? beta : alpha) | reinterpret_cast<uintptr_t>(prob) |
        reinterpret_cast<uintptr_t>(dprob)) & 3u)
     return HQ_ERR_INVALID;
-  if (dbias) {
-    if (reinterpret_cast<uintptr_t>(dbias) & 1u) return HQ_ERR_INVALID;
-    if (!workspace || ws_bytes < hq_gemm_dswiglu_workspace_size(L, n)) return HQ_ERR_INVALID;
-    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return HQ_ERR_INVALID;
+  // workspace: [per-expert tensor maps and flags (discrete weights)] [dbias sums]
+  const size_t maps_bytes = discrete ? discrete_maps_bytes(L) : 0;
+  if (dbias && (reinterpret_cast<uintptr_t>(dbias) & 1u)) return HQ_ERR_INVALID;
+  if (dbias || discrete) {
+    const size_t need = maps_bytes + (dbias ? hq_gemm_dswiglu_workspace_size(L, n) : 0);
+    if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+      return HQ_ERR_INVALID;
   }
   if (m == 0) return HQ_OK;
+  void* dbias_ws = dbias ? static_cast<uint8_t*>(workspace) + maps_bytes : nullptr;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
   DsParams p{};
   p.gs.group_info = padded_offsets;
@@ -409,7 +438,12 @@ int run_dglu(const hq_bf16* a, const hq_bf16* b, const hq_bf16* c, const int32_t
   p.prob = prob;
   p.d_row = d_row;
   p.dprob = dprob;
-  p.dbias_ws = dbias ? static_cast<float*>(workspace) : nullptr;
+  p.dbias_ws = static_cast<float*>(dbias_ws);
+  if (discrete) {
+    p.b_maps = static_cast<CUtensorMap*>(workspace);
+    p.w_ok = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) +
+                                        static_cast<size_t>(L) * sizeof(CUtensorMap));
+  }
   p.n = n;
   p.k = k;
   p.wait_limit_ns = wait_limit_ns();
@@ -424,17 +458,25 @@ int run_dglu(const hq_bf16* a, const hq_bf16* b, const hq_bf16* c, const int32_t
     if (rc != HQ_OK) return rc;
   }
   {
+    // discrete weights: a one-expert map encoded over the workspace (a valid
+    // address, never loaded through as it stands) whose address the device
+    // replaces per expert
     const uint64_t dims[3] = {static_cast<uint64_t>(k), static_cast<uint64_t>(n),
-                              static_cast<uint64_t>(L)};
+                              static_cast<uint64_t>(discrete ? 1 : L)};
     const uint64_t strides[2] = {static_cast<uint64_t>(k) * 2, static_cast<uint64_t>(k) * 2 * n};
     const uint32_t box[3] = {kBKElems, kBN, 1};
-    int rc = encode_tensor_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<hq_bf16*>(b),
-                               dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    void* base = discrete ? workspace : const_cast<hq_bf16*>(b);
+    int rc = encode_tensor_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != HQ_OK) return rc;
+    if (discrete) {
+      rc = build_weight_maps(tmB, b_ptrs, nullptr, p.b_maps, p.w_ok, L, st);
+      if (rc != HQ_OK) return rc;
+    }
   }
   if (dbias) {
     const size_t bytes = static_cast<size_t>(L) * static_cast<size_t>(2 * n) * sizeof(float);
-    if (cudaMemsetAsync(workspace, 0, bytes, st) != cudaSuccess) return HQ_ERR_CUDA;
+    if (cudaMemsetAsync(dbias_ws, 0, bytes, st) != cudaSuccess) return HQ_ERR_CUDA;
   }
   if (cudaFuncSetAttribute(dglu_kernel<ACT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemBytes) != cudaSuccess)
@@ -451,7 +493,7 @@ int run_dglu(const hq_bf16* a, const hq_bf16* b, const hq_bf16* c, const int32_t
     return HQ_ERR_CUDA;
   if (dbias) {
     const int rc = dbias_finalize(reinterpret_cast<uint16_t*>(dbias),
-                                  static_cast<const float*>(workspace),
+                                  static_cast<const float*>(dbias_ws),
                                   static_cast<int64_t>(L) * 2 * n, st);
     if (rc != HQ_OK) return rc;
   }
@@ -468,7 +510,7 @@ int hq_gemm_dswiglu(const hq_bf16* a, const hq_bf16* b, const hq_bf16* c,
                     const float* prob, hq_bf16* d_row, float* dprob, hq_bf16* dbias, int64_t m,
                     int64_t n, int64_t k, void* workspace, size_t ws_bytes, int sm_count,
                     hq_stream_t s) {
-  return hq::run_dglu<hq::kSwiGLU>(a, b, c, padded_offsets, L, alpha, beta, prob, d_row, dprob,
+  return hq::run_dglu<hq::kSwiGLU>(a, b, nullptr, c, padded_offsets, L, alpha, beta, prob, d_row, dprob,
                                    dbias, m, n, k, workspace, ws_bytes, sm_count, s);
 }
 
@@ -476,8 +518,23 @@ int hq_gemm_dgeglu(const hq_bf16* a, const hq_bf16* b, const hq_bf16* c,
                    const int32_t* padded_offsets, int L, const float* alpha, const float* prob,
                    hq_bf16* d_row, float* dprob, hq_bf16* dbias, int64_t m, int64_t n, int64_t k,
                    void* workspace, size_t ws_bytes, int sm_count, hq_stream_t s) {
-  return hq::run_dglu<hq::kGeGLU>(a, b, c, padded_offsets, L, alpha, nullptr, prob, d_row, dprob,
+  return hq::run_dglu<hq::kGeGLU>(a, b, nullptr, c, padded_offsets, L, alpha, nullptr, prob, d_row, dprob,
                                   dbias, m, n, k, workspace, ws_bytes, sm_count, s);
+}
+
+int hq_gemm_dglu_discrete(const hq_bf16* a, const int64_t* b_ptrs, const hq_bf16* c,
+                          const int32_t* padded_offsets, int L, const float* alpha,
+                          const float* beta, const float* prob, int act, hq_bf16* d_row,
+                          float* dprob, hq_bf16* dbias, int64_t m, int64_t n, int64_t k,
+                          void* workspace, size_t ws_bytes, int sm_count, hq_stream_t s) {
+  if (!b_ptrs) return HQ_ERR_INVALID;
+  if (act == 0)
+    return hq::run_dglu<hq::kSwiGLU>(a, nullptr, b_ptrs, c, padded_offsets, L, alpha, beta, prob,
+                                     d_row, dprob, dbias, m, n, k, workspace, ws_bytes, sm_count, s);
+  if (act == 1)
+    return hq::run_dglu<hq::kGeGLU>(a, nullptr, b_ptrs, c, padded_offsets, L, alpha, nullptr, prob,
+                                    d_row, dprob, dbias, m, n, k, workspace, ws_bytes, sm_count, s);
+  return HQ_ERR_INVALID;
 }
 
 }  // extern "C"

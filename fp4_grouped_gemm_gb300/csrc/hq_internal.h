@@ -37,6 +37,19 @@ int encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, voi
 // final pass of the dGLU GEMMs' dbias reduction).  Returns HQ_OK or HQ_ERR_CUDA.
 int dbias_finalize(uint16_t* dbias, const float* ws, int64_t count, cudaStream_t st);
 
+// Discrete weights: the leading part of the caller's workspace holds one
+// 128-byte tensor map per expert, then one int32 flag per expert (1: the
+// expert's pointers passed the device checks), rounded up to 256 bytes.
+inline size_t discrete_maps_bytes(int L) {
+  return (static_cast<size_t>(L) * (sizeof(CUtensorMap) + sizeof(int32_t)) + 255) / 256 * 256;
+}
+
+// Launches the kernel that turns b_ptrs (and the checks of sfb_ptrs, which
+// may be null) into per-expert tensor maps built from tmpl.  Returns HQ_OK or
+// HQ_ERR_CUDA.
+int build_weight_maps(const CUtensorMap& tmpl, const int64_t* b_ptrs, const int64_t* sfb_ptrs,
+                      CUtensorMap* maps, int32_t* ok, int L, cudaStream_t st);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Launch with optional programmatic-dependent-launch attribute.

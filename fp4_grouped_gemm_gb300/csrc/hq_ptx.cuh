@@ -98,6 +98,15 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, uint64
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
+// Orders a tensor map that an earlier kernel wrote to global memory (and
+// published with the tensor-map proxy's release fence) before this thread's
+// TMA copies through it; also drops any stale copy of the map the TMA unit
+// may hold from an earlier use of the same address.
+__device__ __forceinline__ void tensormap_acquire(const CUtensorMap* map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(
+                   reinterpret_cast<uint64_t>(map))
+               : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int32_t c0, int32_t c1) {
   asm volatile(

@@ -84,6 +84,8 @@ enum {
                                          beyond the row count: rows skipped      */
 #define HQ_STATUS_TOKENS_CLAMPED 0x8u /* token_nums[e] outside [0, rows/expert]    */
 #define HQ_STATUS_ROUTING_DROPPED 0x10u /* permute: a bad expert id or a full expert */
+#define HQ_STATUS_BAD_POINTER 0x20u   /* discrete weights: a null or unaligned
+                                         per-expert pointer; that expert skipped */
 
 /* Layout and alignment constants, so integrations need not copy them
  * (FlashRT fp4-gemm notes: "Read capabilities() instead of duplicating
@@ -377,6 +379,57 @@ int hq_gemm_dglu_bs(const void *a, const uint8_t *sfa, const void *b, const uint
                     void *d_col, uint8_t *sfd_col, const float *norm_const, float *dprob,
                     hq_bf16 *dbias, float *amax, int64_t m, int64_t n, int64_t k, hq_mode mode,
                     void *workspace, size_t ws_bytes, int sm_count, hq_stream_t s);
+
+/* ------------------------------------------------------------------------- *
+ * Discrete weights (cuDNN frontend "Grouped GEMM + dGLU (SM100)", weight
+ * layout modes: "Discrete mode: Per-expert weight pointers (no weight
+ * stacking required)"; b_ptrs / sfb_ptrs are device int64 arrays of shape
+ * (num_experts,)).  Instead of one stacked B [L, n, k] (and its stacked
+ * scales), expert g's K-major B [n, k] starts at b_ptrs[g] and, for the
+ * block-scaled modes, its SfAtom scales (ceil(n/128)*128 * k/group bytes) at
+ * sfb_ptrs[g].  Both arrays are device memory, 8-byte aligned.
+ *
+ * Before the GEMM a small kernel builds one TMA tensor map per expert in the
+ * head of the caller's workspace (from a host-encoded template whose global
+ * address it replaces with b_ptrs[g]).  An expert whose b_ptrs[g] or
+ * sfb_ptrs[g] is 0 or not 16-byte aligned is skipped: nothing is loaded
+ * through its pointers, none of its rows is written (dprob, dbias and amax
+ * get nothing from it), and HQ_STATUS_BAD_POINTER is set.  Any other pointer
+ * value must address a whole [n, k] matrix (and its scales), as for every
+ * device pointer of this API.
+ *
+ * Workspace: hq_gemm_discrete_workspace_size(L, dbias_n) bytes, 256-byte
+ * aligned, where dbias_n is the dGLU call's n when it produces dbias, else 0
+ * (the head holds L tensor maps of 128 bytes and L int32 flags, the rest the
+ * dbias partial sums). */
+size_t hq_gemm_discrete_workspace_size(int L, int64_t dbias_n);
+
+/* hq_gemm_grouped_contig with discrete weights. */
+int hq_gemm_grouped_contig_discrete(const void *a, const uint8_t *sfa, const int64_t *b_ptrs,
+                                    const int64_t *sfb_ptrs, const int32_t *padded_offsets, int L,
+                                    const float *alpha, const hq_bf16 *bias, hq_bf16 *out,
+                                    int64_t m_rows, int64_t n, int64_t k, hq_mode mode,
+                                    void *workspace, size_t ws_bytes, int sm_count, hq_stream_t s);
+
+/* hq_gemm_dglu_bs with discrete weights (the block-scaled contract). */
+int hq_gemm_dglu_bs_discrete(const void *a, const uint8_t *sfa, const int64_t *b_ptrs,
+                             const int64_t *sfb_ptrs, const hq_bf16 *c,
+                             const int32_t *padded_offsets, int L, const float *alpha,
+                             const float *beta, const float *prob, int act, void *d_row,
+                             uint8_t *sfd_row, void *d_col, uint8_t *sfd_col,
+                             const float *norm_const, float *dprob, hq_bf16 *dbias, float *amax,
+                             int64_t m, int64_t n, int64_t k, hq_mode mode, void *workspace,
+                             size_t ws_bytes, int sm_count, hq_stream_t s);
+
+/* hq_gemm_dswiglu (act 0) / hq_gemm_dgeglu (act 1) with discrete BF16
+ * weights: b_ptrs[g] -> K-major BF16 [n, k] (the BF16 contract's
+ * b_major = "k"; N-major per-expert weights are not supported).  beta as
+ * hq_gemm_dswiglu (ignored, may be NULL, for act 1). */
+int hq_gemm_dglu_discrete(const hq_bf16 *a, const int64_t *b_ptrs, const hq_bf16 *c,
+                          const int32_t *padded_offsets, int L, const float *alpha,
+                          const float *beta, const float *prob, int act, hq_bf16 *d_row,
+                          float *dprob, hq_bf16 *dbias, int64_t m, int64_t n, int64_t k,
+                          void *workspace, size_t ws_bytes, int sm_count, hq_stream_t s);
 
 /* ------------------------------------------------------------------------- *
  * hq_gemm_dswiglu without caller-provided scratch.  The paper has no

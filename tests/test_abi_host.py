@@ -137,6 +137,45 @@ def test_fused_up_proj_rejects_bad_arguments(lib):
     assert call(m=0) == _abi.HQ_OK                             # no rows: nothing to do
 
 
+def test_discrete_weights_reject_bad_arguments(lib):
+    L = 4
+    ws = hq.hq_gemm_discrete_workspace_size(L)
+    assert ws == 768 and ws % 256 == 0                            # 4 maps of 128 B + 4 flags
+    assert hq.hq_gemm_discrete_workspace_size(L, 128) == ws + L * 256 * 4
+    assert hq.hq_gemm_discrete_workspace_size(0) == 0
+    W = ctypes.c_void_p(0x10000)
+    c = lib.hq_gemm_grouped_contig_discrete
+
+    def call(bp=FAKE, sp=FAKE, w=W, wb=ws, n=128, k=256, mode=0, m=1024):
+        return c(FAKE, FAKE, bp, sp, FAKE, L, None, None, FAKE, m, n, k, mode, w, wb, -1, None)
+
+    assert call(bp=None) == _abi.HQ_ERR_INVALID                   # no pointer array
+    assert call(sp=ctypes.c_void_p(0x10004)) == _abi.HQ_ERR_INVALID  # pointer array not 8-byte aligned
+    assert call(w=None) == _abi.HQ_ERR_INVALID                    # no workspace
+    assert call(wb=ws - 1) == _abi.HQ_ERR_INVALID                 # workspace too small
+    assert call(w=ctypes.c_void_p(0x10080)) == _abi.HQ_ERR_INVALID  # workspace not 256-byte aligned
+    assert call(n=100) == _abi.HQ_ERR_INVALID                     # n % 128
+    assert call(mode=2) == _abi.HQ_ERR_UNSUPPORTED                # NVFP4 without alpha
+    assert call(m=0) == _abi.HQ_OK
+    d = lib.hq_gemm_dglu_discrete
+    args = [FAKE, FAKE, FAKE, FAKE, L, FAKE, FAKE, FAKE, 0, FAKE, FAKE, None, 512, 64, 64, W, ws, -1, None]
+    assert d(*args[:1], None, *args[2:]) == _abi.HQ_ERR_INVALID   # no b_ptrs
+    bad_act = list(args)
+    bad_act[8] = 2
+    assert d(*bad_act) == _abi.HQ_ERR_INVALID
+    dbias_args = list(args)
+    dbias_args[11] = FAKE                                         # dbias needs the larger workspace
+    assert d(*dbias_args) == _abi.HQ_ERR_INVALID
+    dbias_args[16] = hq.hq_gemm_discrete_workspace_size(L, 64)
+    no_rows = list(dbias_args)
+    no_rows[12] = 0
+    assert d(*no_rows) == _abi.HQ_OK
+    b = lib.hq_gemm_dglu_bs_discrete
+    bargs = [FAKE, FAKE, FAKE, None, FAKE, FAKE, L, FAKE, FAKE, FAKE, 0, FAKE, None, None, None, None, FAKE,
+             None, None, 512, 128, 256, 0, W, ws, -1, None]
+    assert b(*bargs) == _abi.HQ_ERR_INVALID                       # no sfb_ptrs
+
+
 def test_grouped_rows_rejects_bad_arguments(lib):
     f = lib.hq_gemm_grouped_rows
     ws = hq.hq_gemm_grouped_rows_workspace_size(1000, 8)
