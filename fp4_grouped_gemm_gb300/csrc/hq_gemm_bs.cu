@@ -1034,7 +1034,8 @@ struct Cfg2 {
   static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
   static constexpr int OFF_STAGE_OUT = OFF_SFB + STAGES * SFB_BYTES;
-  static constexpr int OFF_BAR = OFF_STAGE_OUT + kEpiWarps * 1024;
+  static constexpr int OFF_TABLE = OFF_STAGE_OUT + kEpiWarps * 1024;  // masked: 2 x (kMaxGroups + 1) int32
+  static constexpr int OFF_BAR = OFF_TABLE + 2 * (kMaxGroups + 1) * 4 + 8;
   static constexpr int NUM_BARS = 4 * STAGES + 3;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
@@ -1072,6 +1073,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t drain_bar = tfull_bar + 16u;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  int64_t* total_pairs_s = reinterpret_cast<int64_t*>(smem + C::OFF_MISC + 8);
+  int32_t* tab0 = reinterpret_cast<int32_t*>(smem + C::OFF_TABLE);
+  int32_t* tab1 = tab0 + (kMaxGroups + 1);
+  const bool masked = p.gs.sched == kMasked;
 
   if (warp == 0 && lane == 0) {
     *abort_flag = 0;
@@ -1093,13 +1098,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish_2sm();
   }
   pdl_wait();
+  // masked layout: per expert the number of 256-row pairs holding valid rows
+  // and their exclusive prefix (both CTAs build the same table)
+  if (warp == 2 && masked) build_table(p.gs, tab0, tab1, lane, total_pairs_s, 256);
   __syncthreads();
   cluster_sync();  // both CTAs' barriers and TMEM exist before any cross-CTA use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   const int n_tiles = static_cast<int>((p.n + C::BN - 1) / C::BN);
-  const int64_t m_pairs = (p.gs.a_rows + 255) / 256;
+  const int64_t m_pairs = masked ? *total_pairs_s : (p.gs.a_rows + 255) / 256;
   const int64_t total = m_pairs * n_tiles;
   const int64_t cluster_id = blockIdx.x >> 1;
   const int64_t num_clusters = gridDim.x >> 1;
@@ -1107,10 +1115,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_kb = static_cast<int>((p.k + C::BK - 1) / C::BK);
   const int atoms_total = static_cast<int>(p.S / 4);
   const WaitCtx wctx{p.gs.status, abort_flag, p.wait_limit_ns};
-  auto tile_rows = [&](int64_t t, int64_t& row0, int& n0) {
+  // Tile t of the pair: 256 rows from `base` (dense: all rows; masked: one
+  // expert's rows, from e * max_m), columns [n0, n0 + 256).  CTA r owns rows
+  // [base + 128 r, base + 128 r + 128), of which valid0 / valid1 (0..128) hold data.
+  struct PairTile {
+    int64_t row0;  // this CTA's first row
+    int n0;
+    int g;
+    int valid0, valid1;  // valid rows of the even / odd CTA
+    int mine;            // valid rows of this CTA
+  };
+  auto pair_tile = [&](int64_t t) {
+    PairTile pt;
     const int64_t mt = t / n_tiles;
-    n0 = static_cast<int>(t - mt * n_tiles) * C::BN;
-    row0 = mt * 256 + rank * kBM;
+    pt.n0 = static_cast<int>(t - mt * n_tiles) * C::BN;
+    int64_t base, cnt;
+    if (masked) {
+      int lo = 0, hi = p.gs.groups - 1;  // last e with prefix[e] <= mt
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tab0[mid] <= mt) lo = mid; else hi = mid - 1;
+      }
+      const int64_t local = mt - tab0[lo];
+      pt.g = lo;
+      base = static_cast<int64_t>(lo) * p.gs.max_m + local * 256;
+      cnt = static_cast<int64_t>(tab1[lo]) - local * 256;
+    } else {
+      pt.g = 0;
+      base = mt * 256;
+      cnt = p.gs.a_rows - base;
+    }
+    pt.valid0 = cnt <= 0 ? 0 : (cnt >= 128 ? 128 : static_cast<int>(cnt));
+    pt.valid1 = cnt <= 128 ? 0 : (cnt >= 256 ? 128 : static_cast<int>(cnt - 128));
+    pt.mine = rank ? pt.valid1 : pt.valid0;
+    pt.row0 = base + rank * kBM;
+    return pt;
   };
 
   if (warp == 0) {
@@ -1120,24 +1159,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, filled_a = 0, filled_s = 0, par_a = 0, par_s = 0;
       bool ok = true;
       for (int64_t t = cluster_id; ok && t < total; t += num_clusters) {
-        int64_t row0;
-        int n0;
-        tile_rows(t, row0, n0);
-        const int nh0 = n0 + static_cast<int>(rank) * 128;  // this CTA's B rows
-        const bool has_sfa = row0 < rows_pad;
+        const PairTile pt = pair_tile(t);
+        const int64_t row0 = pt.row0;
+        const int nh0 = pt.n0 + static_cast<int>(rank) * 128;  // this CTA's B rows
+        // a CTA whose 128 rows hold no valid row loads no A and no A scales
+        // (its accumulator half is never stored)
+        const bool has_a = pt.mine > 0;
+        const bool has_sfa = has_a && row0 < rows_pad;
+        const uint32_t pair_bytes = (pt.valid0 > 0 ? C::A_BYTES : 0u) +
+                                    (pt.valid1 > 0 ? C::A_BYTES : 0u) + 2u * C::B_BYTES;
         const uint8_t* sfa_rows = p.sfa + (row0 / kBM) * atoms_total * 512;
-        const uint8_t* sfb_rows = p.sfb + (n0 / 128) * static_cast<int64_t>(atoms_total) * 512;
+        const uint8_t* sfb_rows = p.sfb + static_cast<int64_t>(pt.g) * p.sfb_group_bytes +
+                                  (pt.n0 / 128) * static_cast<int64_t>(atoms_total) * 512;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, wctx)) { ok = false; break; }
           int atoms = atoms_total - kb * C::ATOMS;
           atoms = atoms < C::ATOMS ? atoms : C::ATOMS;
           // both CTAs' A / B tiles complete on the even CTA's full barrier,
           // which expects the bytes of the pair
-          if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * (C::A_BYTES + C::B_BYTES));
+          if (leader) mbar_arrive_expect_tx(full_bar(stage), pair_bytes);
           const uint32_t fb = mapa_shared(full_bar(stage), 0);
-          tma_load_2d_pair(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, fb, kb * kBKBytes,
-                           static_cast<int32_t>(row0));
-          tma_load_3d_pair(sbase + C::OFF_B + stage * C::B_BYTES, &tmB, fb, kb * kBKBytes, nh0, 0);
+          if (has_a)
+            tma_load_2d_pair(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, fb, kb * kBKBytes,
+                             static_cast<int32_t>(row0));
+          tma_load_3d_pair(sbase + C::OFF_B + stage * C::B_BYTES, &tmB, fb, kb * kBKBytes, nh0, pt.g);
           mbar_arrive_expect_tx(sffull_bar(stage), atoms * 512u * (has_sfa ? 3u : 2u));
           if (has_sfa)
             bulk_load(sbase + C::OFF_SFA + stage * C::SFA_BYTES, sfa_rows + kb * C::ATOMS * 512,
@@ -1288,23 +1333,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tempty_leader = mapa_shared(tempty_bar, 0);
     uint32_t acc_phase = 0;
     for (int64_t t = cluster_id; t < total; t += num_clusters) {
-      int64_t row0;
-      int n0;
-      tile_rows(t, row0, n0);
-      const float alpha = p.alpha ? __ldg(p.alpha) : 1.0f;  // loaded before the wait
+      const PairTile pt = pair_tile(t);
+      const float alpha = p.alpha ? __ldg(p.alpha + pt.g) : 1.0f;  // loaded before the wait
       const bool okw = wait_bounded(tfull_bar, acc_phase, wctx);
       if (!__all_sync(0xFFFFFFFFu, okw)) break;
       tc_fence_after();
-      const int64_t rem = p.gs.a_rows - row0 - q * 32;
       EpiArgs e;
       e.acc_t = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
       e.cw = (ew >> 2) * (C::BN / 2);
-      e.n0 = n0;
+      e.n0 = pt.n0;
       e.n = p.n;
       e.alpha = alpha;
-      e.bias = p.bias;
-      e.out = p.out + (row0 + q * 32) * p.n;
-      e.rows_here = rem < 0 ? 0 : (rem > 32 ? 32 : static_cast<int>(rem));
+      e.bias = p.bias ? p.bias + static_cast<int64_t>(pt.g) * p.n : nullptr;
+      e.out = p.out + (pt.row0 + q * 32) * p.n;
+      e.rows_here = pt.mine - q * 32;
       e.rows_lo = 0;
       e.stage_s = sbase + C::OFF_STAGE_OUT + ew * 1024;
       e.lane = lane;
@@ -1399,7 +1441,7 @@ int run_bs_2sm(const void* a, const void* b, const GemmParams& p, int sm_count, 
     if (rc != HQ_OK) return rc;
   }
   {
-    const uint64_t dims[3] = {kbytes, static_cast<uint64_t>(p.n), 1};
+    const uint64_t dims[3] = {kbytes, static_cast<uint64_t>(p.n), static_cast<uint64_t>(p.gs.groups)};
     const uint64_t strides[2] = {kbytes, kbytes * static_cast<uint64_t>(p.n)};
     const uint32_t box[3] = {kBKBytes, 128, 1};
     int rc = encode_tensor_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(b), dims,
@@ -1412,7 +1454,10 @@ int run_bs_2sm(const void* a, const void* b, const GemmParams& p, int sm_count, 
     return HQ_ERR_CUDA;
   const int sms = num_sms();
   if (sms < 2) return HQ_ERR_CUDA;
-  const int64_t pairs_needed = ((p.gs.a_rows + 255) / 256) * ((p.n + 255) / 256);
+  const int64_t m_pairs = p.gs.sched == kMasked
+                             ? static_cast<int64_t>(p.gs.groups) * ((p.gs.max_m + 255) / 256)
+                             : (p.gs.a_rows + 255) / 256;
+  const int64_t pairs_needed = m_pairs * ((p.n + 255) / 256);
   int64_t pairs = (sm_count > 0 ? sm_count : sms) / 2;
   if (pairs > sms / 2) pairs = sms / 2;
   if (pairs > pairs_needed) pairs = pairs_needed;
@@ -1438,9 +1483,11 @@ int run_bs_2sm(const void* a, const void* b, const GemmParams& p, int sm_count, 
 int run_gemm(hq_mode mode, const void* a, const void* b, const GemmParams& p, int sm_count,
              bool pdl, cudaStream_t st) {
   int bn = forced_tile_n();
-  // dense problems with whole 256-column tiles use the 2-SM kernel unless a
+  // dense and masked problems with whole 256-column tiles (masked: experts
+  // padded to a multiple of 256 rows) use the 2-SM kernel unless a
   // single-SM tile width is forced
-  if (bn == 0 && p.gs.sched == kDense && p.n % 256 == 0 && use_2sm()) {
+  const bool pairable = p.gs.sched == kDense || (p.gs.sched == kMasked && p.gs.max_m % 256 == 0);
+  if (bn == 0 && pairable && p.n % 256 == 0 && use_2sm()) {
     if (mode == HQ_MXFP8) return run_bs_2sm<HQ_MXFP8, 6>(a, b, p, sm_count, pdl, st);
     if (mode == HQ_MXFP4) return run_bs_2sm<HQ_MXFP4, 5>(a, b, p, sm_count, pdl, st);
     return run_bs_2sm<HQ_NVFP4, 5>(a, b, p, sm_count, pdl, st);

@@ -98,8 +98,10 @@ __device__ __forceinline__ TileInfo decode_tile(const GroupSched& p, const Sched
 }
 
 // Warp-cooperative construction of the group table (one warp, L <= 1024).
+// unit: rows per scheduled m-tile of the masked layout (128, or 256 for the
+// two-CTA pairs); the other layouts use 128.
 __device__ inline void build_table(const GroupSched& p, int32_t* tab0, int32_t* tab1, int lane,
-                            int64_t* total_mtiles) {
+                            int64_t* total_mtiles, int unit = kBM) {
   if (p.sched == kDense) {
     if (lane == 0) *total_mtiles = (p.a_rows + kBM - 1) / kBM;
     return;
@@ -146,7 +148,7 @@ __device__ inline void build_table(const GroupSched& p, int32_t* tab0, int32_t* 
         if (raw > p.max_m) { cnt = static_cast<int32_t>(p.max_m); bad = true; }
         tab1[e] = cnt;
       }
-      const int32_t tiles = (cnt + kBM - 1) / kBM;
+      const int32_t tiles = (cnt + unit - 1) / unit;
       int32_t incl = tiles;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {

@@ -263,6 +263,24 @@ def test_grouped_masked_small(cuda_dev, tile_n, mode):
     assert status == 0
 
 
+@pytest.mark.parametrize("two_sm", [1, 0])
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4", "mxfp4"])
+def test_grouped_masked_pairs(cuda_dev, mode, two_sm):
+    """max_m % 256 == 0 and n % 256 == 0: 256-row pairs on two-CTA clusters
+    (two_sm=1), counts that end inside the even CTA's half, exactly at the
+    half, inside the odd half, at a pair boundary, and empty experts."""
+    hq.set_gemm_2sm(two_sm)
+    masked = [0, 1, 127, 128, 129, 255, 256, 300, 512, 0, 77]
+    alpha = None if mode == "mxfp4" else [0.5 + 0.125 * e for e in range(len(masked))]
+    status = masked_case(masked, 512, 512, 384 if mode == "mxfp8" else 512, mode, 0, alpha=alpha, seed=13)
+    assert status == 0
+
+
+def test_grouped_masked_pairs_clamp_and_flag(cuda_dev):
+    status = masked_case([600, -4, 256, 129], 256, 256, 256, "nvfp4", 0, alpha=[1.0, 2.0, 0.5, 1.5], seed=17)
+    assert status & hq.HQ_STATUS_MASK_CLAMPED
+
+
 def test_grouped_masked_clamps_and_flags(cuda_dev):
     status = masked_case([300, -4, 128], 128, 256, 128, "mxfp8", seed=8)
     assert status & hq.HQ_STATUS_MASK_CLAMPED
