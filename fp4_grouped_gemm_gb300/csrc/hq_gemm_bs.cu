@@ -1077,6 +1077,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* tab0 = reinterpret_cast<int32_t*>(smem + C::OFF_TABLE);
   int32_t* tab1 = tab0 + (kMaxGroups + 1);
   const bool masked = p.gs.sched == kMasked;
+  const bool contig = p.gs.sched == kContig;
 
   if (warp == 0 && lane == 0) {
     *abort_flag = 0;
@@ -1099,15 +1100,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   pdl_wait();
   // masked layout: per expert the number of 256-row pairs holding valid rows
-  // and their exclusive prefix (both CTAs build the same table)
+  // and their exclusive prefix (both CTAs build the same table).
+  // contiguous layout: tab0 = the sanitised group ends, tab1 = the exclusive
+  // prefix of each group's 256-row pairs (a group's pairs start at its first
+  // row, so a pair never mixes two groups)
   if (warp == 2 && masked) build_table(p.gs, tab0, tab1, lane, total_pairs_s, 256);
+  if (warp == 2 && contig) {
+    build_table(p.gs, tab0, tab1, lane, total_pairs_s);
+    __syncwarp();
+    int32_t carry = 0;
+    for (int base = 0; base < p.gs.groups; base += 32) {
+      const int g = base + lane;
+      int32_t pairs = 0;
+      if (g < p.gs.groups) {
+        const int32_t start = g > 0 ? tab0[g - 1] : 0;
+        pairs = (tab0[g] - start + 255) / 256;
+      }
+      int32_t incl = pairs;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      if (g < p.gs.groups) tab1[g] = carry + incl - pairs;
+      carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    if (lane == 0) *total_pairs_s = carry;
+  }
   __syncthreads();
   cluster_sync();  // both CTAs' barriers and TMEM exist before any cross-CTA use
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   const int n_tiles = static_cast<int>((p.n + C::BN - 1) / C::BN);
-  const int64_t m_pairs = masked ? *total_pairs_s : (p.gs.a_rows + 255) / 256;
+  const int64_t m_pairs = (masked || contig) ? *total_pairs_s : (p.gs.a_rows + 255) / 256;
   const int64_t total = m_pairs * n_tiles;
   const int64_t cluster_id = blockIdx.x >> 1;
   const int64_t num_clusters = gridDim.x >> 1;
@@ -1130,16 +1156,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t mt = t / n_tiles;
     pt.n0 = static_cast<int>(t - mt * n_tiles) * C::BN;
     int64_t base, cnt;
-    if (masked) {
-      int lo = 0, hi = p.gs.groups - 1;  // last e with prefix[e] <= mt
+    if (masked || contig) {
+      const int32_t* prefix = masked ? tab0 : tab1;
+      int lo = 0, hi = p.gs.groups - 1;  // last group with prefix[g] <= mt
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (tab0[mid] <= mt) lo = mid; else hi = mid - 1;
+        if (prefix[mid] <= mt) lo = mid; else hi = mid - 1;
       }
-      const int64_t local = mt - tab0[lo];
+      const int64_t local = mt - prefix[lo];
       pt.g = lo;
-      base = static_cast<int64_t>(lo) * p.gs.max_m + local * 256;
-      cnt = static_cast<int64_t>(tab1[lo]) - local * 256;
+      if (masked) {
+        base = static_cast<int64_t>(lo) * p.gs.max_m + local * 256;
+        cnt = static_cast<int64_t>(tab1[lo]) - local * 256;
+      } else {
+        const int64_t start = lo > 0 ? tab0[lo - 1] : 0;
+        base = start + local * 256;
+        cnt = static_cast<int64_t>(tab0[lo]) - base;
+      }
     } else {
       pt.g = 0;
       base = mt * 256;
@@ -1454,9 +1487,11 @@ int run_bs_2sm(const void* a, const void* b, const GemmParams& p, int sm_count, 
     return HQ_ERR_CUDA;
   const int sms = num_sms();
   if (sms < 2) return HQ_ERR_CUDA;
+  // an upper bound of the pairs (contiguous: each group adds at most one
+  // partial pair)
   const int64_t m_pairs = p.gs.sched == kMasked
                              ? static_cast<int64_t>(p.gs.groups) * ((p.gs.max_m + 255) / 256)
-                             : (p.gs.a_rows + 255) / 256;
+                             : (p.gs.a_rows + 255) / 256 + (p.gs.sched == kContig ? p.gs.groups : 0);
   const int64_t pairs_needed = m_pairs * ((p.n + 255) / 256);
   int64_t pairs = (sm_count > 0 ? sm_count : sms) / 2;
   if (pairs > sms / 2) pairs = sms / 2;
@@ -1483,10 +1518,11 @@ int run_bs_2sm(const void* a, const void* b, const GemmParams& p, int sm_count, 
 int run_gemm(hq_mode mode, const void* a, const void* b, const GemmParams& p, int sm_count,
              bool pdl, cudaStream_t st) {
   int bn = forced_tile_n();
-  // dense and masked problems with whole 256-column tiles (masked: experts
-  // padded to a multiple of 256 rows) use the 2-SM kernel unless a
-  // single-SM tile width is forced
-  const bool pairable = p.gs.sched == kDense || (p.gs.sched == kMasked && p.gs.max_m % 256 == 0);
+  // dense, contiguous and masked problems with whole 256-column tiles
+  // (masked: experts padded to a multiple of 256 rows) use the 2-SM kernel
+  // unless a single-SM tile width is forced
+  const bool pairable = !p.b_maps && (p.gs.sched == kDense || p.gs.sched == kContig ||
+                                      (p.gs.sched == kMasked && p.gs.max_m % 256 == 0));
   if (bn == 0 && pairable && p.n % 256 == 0 && use_2sm()) {
     if (mode == HQ_MXFP8) return run_bs_2sm<HQ_MXFP8, 6>(a, b, p, sm_count, pdl, st);
     if (mode == HQ_MXFP4) return run_bs_2sm<HQ_MXFP4, 5>(a, b, p, sm_count, pdl, st);

@@ -162,6 +162,18 @@ def test_grouped_contig_small(cuda_dev, tile_n, mode):
     contig_case(offsets, 1152, 256, 256, mode, tile_n, alpha=alpha, bias=(mode == "mxfp8"), seed=3)
 
 
+@pytest.mark.parametrize("two_sm", [1, 0])
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4", "mxfp4"])
+def test_grouped_contig_pairs(cuda_dev, mode, two_sm):
+    """n % 256 == 0: 256-row pairs per group on two-CTA clusters (two_sm=1);
+    group ends on odd multiples of 128 (a pair's odd half beyond its group),
+    a 128-row group, empty groups, rows past the last group untouched."""
+    hq.set_gemm_2sm(two_sm)
+    offsets = [384, 384, 512, 1152, 1280, 1280]
+    alpha = None if mode == "mxfp4" else [0.5, 1.0, 2.0, 1.25, 0.75, 1.5]
+    contig_case(offsets, 1408, 512, 512, mode, 0, alpha=alpha, bias=(mode == "mxfp8"), seed=23)
+
+
 def test_grouped_contig_batch_equivalence(cuda_dev):
     """batch_gemm == grouped contiguous with equal offsets == grouped masked with full masks."""
     B, M, n, k = 3, 256, 256, 256
