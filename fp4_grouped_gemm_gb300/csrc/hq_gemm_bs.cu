@@ -1048,11 +1048,18 @@ struct Cfg2 {
       | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(256 >> 4) << 24);
 };
 
-template <int MODE, int STAGES>
+// EPI = kEpiSwiGLUQ: the fused up-proj (p.n = H): the tile's 256 B rows are
+// gate rows [n0, n0 + 128) (even CTA) and up rows [H + n0, H + n0 + 128) (odd
+// CTA), so each CTA's accumulator half holds gate in columns [0, 128) and up
+// in [128, 256), as in the single-SM fused tile; tiles step 128 compact columns.
+template <int MODE, int STAGES, int EPI = kEpiGemm>
 __global__ void __launch_bounds__(kThreads, 1)
     bs_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const GemmParams p) {
   using C = Cfg2<MODE, STAGES>;
+  constexpr bool kUpProj = EPI == kEpiSwiGLUQ;
+  static_assert(EPI == kEpiGemm || kUpProj, "2-SM epilogues: plain GEMM or fused up-proj");
+  constexpr int TW = kUpProj ? C::BN / 2 : C::BN;  // output columns per tile
   static_assert(kSfPath == 2, "the 2-SM kernel stages scales with tcgen05.st");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1132,7 +1139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int n_tiles = static_cast<int>((p.n + C::BN - 1) / C::BN);
+  const int n_tiles = static_cast<int>((p.n + TW - 1) / TW);
   const int64_t m_pairs = (masked || contig) ? *total_pairs_s : (p.gs.a_rows + 255) / 256;
   const int64_t total = m_pairs * n_tiles;
   const int64_t cluster_id = blockIdx.x >> 1;
@@ -1154,7 +1161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto pair_tile = [&](int64_t t) {
     PairTile pt;
     const int64_t mt = t / n_tiles;
-    pt.n0 = static_cast<int>(t - mt * n_tiles) * C::BN;
+    pt.n0 = static_cast<int>(t - mt * n_tiles) * TW;
     int64_t base, cnt;
     if (masked || contig) {
       const int32_t* prefix = masked ? tab0 : tab1;
@@ -1194,7 +1201,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t t = cluster_id; ok && t < total; t += num_clusters) {
         const PairTile pt = pair_tile(t);
         const int64_t row0 = pt.row0;
-        const int nh0 = pt.n0 + static_cast<int>(rank) * 128;  // this CTA's B rows
+        // this CTA's 128 B rows, and the 128-row blocks of the tile's 256 B rows
+        const int nh0 = kUpProj ? (rank ? static_cast<int>(p.n) + pt.n0 : pt.n0)
+                                : pt.n0 + static_cast<int>(rank) * 128;
+        const int64_t sfb_blk0 = pt.n0 / 128;
+        const int64_t sfb_blk1 = kUpProj ? (p.n + pt.n0) / 128 : pt.n0 / 128 + 1;
         // a CTA whose 128 rows hold no valid row loads no A and no A scales
         // (its accumulator half is never stored)
         const bool has_a = pt.mine > 0;
@@ -1202,8 +1213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t pair_bytes = (pt.valid0 > 0 ? C::A_BYTES : 0u) +
                                     (pt.valid1 > 0 ? C::A_BYTES : 0u) + 2u * C::B_BYTES;
         const uint8_t* sfa_rows = p.sfa + (row0 / kBM) * atoms_total * 512;
-        const uint8_t* sfb_rows = p.sfb + static_cast<int64_t>(pt.g) * p.sfb_group_bytes +
-                                  (pt.n0 / 128) * static_cast<int64_t>(atoms_total) * 512;
+        const uint8_t* sfb_grp = p.sfb + static_cast<int64_t>(pt.g) * p.sfb_group_bytes;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, wctx)) { ok = false; break; }
           int atoms = atoms_total - kb * C::ATOMS;
@@ -1222,7 +1232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       atoms * 512u, sffull_bar(stage));
           for (int rb = 0; rb < 2; ++rb)
             bulk_load(sbase + C::OFF_SFB + stage * C::SFB_BYTES + rb * C::ATOMS * 512,
-                      sfb_rows + (rb * static_cast<int64_t>(atoms_total) + kb * C::ATOMS) * 512,
+                      sfb_grp + ((rb ? sfb_blk1 : sfb_blk0) * atoms_total + kb * C::ATOMS) * 512,
                       atoms * 512u, sffull_bar(stage));
           filled_a |= 1u << stage;
           filled_s |= 1u << stage;
@@ -1365,7 +1375,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - 2;
     const uint32_t tempty_leader = mapa_shared(tempty_bar, 0);
     uint32_t acc_phase = 0;
-    for (int64_t t = cluster_id; t < total; t += num_clusters) {
+    if (kUpProj) {
+      // as the single-SM fused epilogue: y formed while draining, TMEM
+      // released, then quantised and stored (one row per thread)
+      const float gq = p.q_gscale ? __ldg(p.q_gscale) : 1.0f;
+      const int h = ew >> 2;
+      for (int64_t t = cluster_id; t < total; t += num_clusters) {
+        const PairTile pt = pair_tile(t);
+        const float alpha = p.alpha ? __ldg(p.alpha + pt.g) : 1.0f;
+        const bool okw = wait_bounded(tfull_bar, acc_phase, wctx);
+        if (!__all_sync(0xFFFFFFFFu, okw)) break;
+        tc_fence_after();
+        float y[64];
+        swiglu_drain(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + 64 * h, alpha, y);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader);
+        const int r_local = q * 32 + lane;
+        if (r_local < pt.mine) {
+          const int64_t row = pt.row0 + r_local;
+          swiglu_store(p, y, row, pt.n0 + 64 * h, gq);
+          if (p.q_mode == HQ_MXFP8 && h == 1 && pt.n0 + TW == p.n)
+            for (int64_t sc = p.n / 32; sc < p.sfq_cols; sc += 4)
+              *reinterpret_cast<uint32_t*>(p.sfq + sfatom_offset(row, sc, p.sfq_cols)) = 0u;
+        }
+        acc_phase ^= 1u;
+      }
+    }
+    for (int64_t t = cluster_id; !kUpProj && t < total; t += num_clusters) {
       const PairTile pt = pair_tile(t);
       const float alpha = p.alpha ? __ldg(p.alpha + pt.g) : 1.0f;  // loaded before the wait
       const bool okw = wait_bounded(tfull_bar, acc_phase, wctx);
@@ -1459,10 +1496,12 @@ int run_bs(const void* a, const void* b, const GemmParams& p0, int sm_count, boo
   return e == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
 }
 
-template <int MODE, int STAGES>
+template <int MODE, int STAGES, int EPI = kEpiGemm>
 int run_bs_2sm(const void* a, const void* b, const GemmParams& p, int sm_count, bool pdl,
                cudaStream_t st) {
   using C = Cfg2<MODE, STAGES>;
+  constexpr bool kUpProj = EPI == kEpiSwiGLUQ;
+  const uint64_t b_rows = static_cast<uint64_t>(kUpProj ? 2 * p.n : p.n);
   const uint64_t kbytes = static_cast<uint64_t>(p.k) / C::EPB;
   CUtensorMap tmA, tmB;
   {
@@ -1474,14 +1513,14 @@ int run_bs_2sm(const void* a, const void* b, const GemmParams& p, int sm_count, 
     if (rc != HQ_OK) return rc;
   }
   {
-    const uint64_t dims[3] = {kbytes, static_cast<uint64_t>(p.n), static_cast<uint64_t>(p.gs.groups)};
-    const uint64_t strides[2] = {kbytes, kbytes * static_cast<uint64_t>(p.n)};
+    const uint64_t dims[3] = {kbytes, b_rows, static_cast<uint64_t>(p.gs.groups)};
+    const uint64_t strides[2] = {kbytes, kbytes * b_rows};
     const uint32_t box[3] = {kBKBytes, 128, 1};
     int rc = encode_tensor_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(b), dims,
                                strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != HQ_OK) return rc;
   }
-  auto kern = bs_gemm_2sm_kernel<MODE, STAGES>;
+  auto kern = bs_gemm_2sm_kernel<MODE, STAGES, EPI>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
       cudaSuccess)
     return HQ_ERR_CUDA;
@@ -1492,7 +1531,8 @@ int run_bs_2sm(const void* a, const void* b, const GemmParams& p, int sm_count, 
   const int64_t m_pairs = p.gs.sched == kMasked
                              ? static_cast<int64_t>(p.gs.groups) * ((p.gs.max_m + 255) / 256)
                              : (p.gs.a_rows + 255) / 256 + (p.gs.sched == kContig ? p.gs.groups : 0);
-  const int64_t pairs_needed = m_pairs * ((p.n + 255) / 256);
+  const int64_t tw = kUpProj ? 128 : 256;
+  const int64_t pairs_needed = m_pairs * ((p.n + tw - 1) / tw);
   int64_t pairs = (sm_count > 0 ? sm_count : sms) / 2;
   if (pairs > sms / 2) pairs = sms / 2;
   if (pairs > pairs_needed) pairs = pairs_needed;
@@ -1914,6 +1954,12 @@ int hq_gemm_grouped_contig_swiglu_quant(const void* a, const uint8_t* sfa, const
   cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
   constexpr int T = hq::kMaxGroups + 1;
   constexpr int E = hq::kEpiSwiGLUQ;
+  if (hq::use_2sm() && hq::forced_tile_n() == 0) {
+    // two-CTA pairs: the even CTA holds the gate rows, the odd CTA the up rows
+    if (mode == HQ_MXFP8) return hq::run_bs_2sm<HQ_MXFP8, 6, E>(a, b, p, sm_count, false, st);
+    if (mode == HQ_MXFP4) return hq::run_bs_2sm<HQ_MXFP4, 5, E>(a, b, p, sm_count, false, st);
+    return hq::run_bs_2sm<HQ_NVFP4, 5, E>(a, b, p, sm_count, false, st);
+  }
   if (mode == HQ_MXFP8) return hq::run_bs<HQ_MXFP8, 256, 4, 1, T, E>(a, b, p, sm_count, false, st);
   if (mode == HQ_MXFP4) return hq::run_bs<HQ_MXFP4, 256, 3, 1, T, E>(a, b, p, sm_count, false, st);
   return hq::run_bs<HQ_NVFP4, 256, 3, 1, T, E>(a, b, p, sm_count, false, st);

@@ -110,15 +110,30 @@ def run_small(mode, out_mode, offsets, m, H, k, alpha, g, seed):
         assert (sf_plain[:last, H // gs:] == 0).all(), "padding scale columns not zeroed"
 
 
+@pytest.fixture(autouse=True)
+def _reset_knobs():
+    yield
+    hq.set_gemm_2sm(1)
+
+
+@pytest.mark.parametrize("two_sm", [1, 0])
 @pytest.mark.parametrize("mode,out_mode,alpha,g,H,k", [
     ("mxfp8", "mxfp8", [0.5, 1.0, 2.0, 1.25], None, 384, 256),   # kb_dim 16 > 12 real columns
     ("nvfp4", "nvfp4", [0.5, 1.0, 2.0, 1.25], 64.0, 256, 512),
     ("mxfp4", "mxfp8", None, None, 256, 512),
     ("mxfp8", "nvfp4", None, None, 512, 384),
 ])
-def test_fused_up_proj_small(cuda_dev, mode, out_mode, alpha, g, H, k):
+def test_fused_up_proj_small(cuda_dev, mode, out_mode, alpha, g, H, k, two_sm):
+    """two_sm=1: two-CTA pairs (gate rows on the even CTA, up rows on the odd)."""
+    hq.set_gemm_2sm(two_sm)
     offsets = [256, 256, 768, 1024]            # empty group 1; rows >= 1024 untouched
     run_small(mode, out_mode, offsets, 1152, H, k, alpha, g, seed=H + k)
+
+
+def test_fused_up_proj_pairs_odd_group_ends(cuda_dev):
+    """Group ends on odd multiples of 128: a pair's odd half past its group
+    stores nothing (those rows belong to the next group's pairs)."""
+    run_small("mxfp8", "mxfp8", [384, 512, 1152], 1280, 256, 256, [1.0, 0.5, 2.0], None, seed=77)
 
 
 def test_fused_up_proj_matches_unfused_path_on_exact_sums(cuda_dev):
