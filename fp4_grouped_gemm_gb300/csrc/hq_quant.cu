@@ -141,6 +141,7 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
   constexpr int NV = GS / 8;          // 16-byte loads per operand and group
   constexpr int U = MODE == HQ_NVFP4 ? 2 : 1;  // groups a lane holds in flight
   __shared__ float r_table[128];
+  pdl_wait();  // the global scale and the input may come from the preceding kernel
   const float g = (MODE == HQ_NVFP4 && p.global_scale) ? __ldg(p.global_scale) : 1.0f;
   if (MODE == HQ_NVFP4) {
     // g / value(UE4M3 code) for every positive code, IEEE division
@@ -150,7 +151,6 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
     }
     __syncthreads();
   }
-  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
