@@ -84,6 +84,117 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // 96 registers per thread is the most that lets the block launch.
 enum Act : int { kSwiGLU = 0, kGeGLU = 1 };
 
+// dGLU of one 32-column chunk (compact columns [j0, j0 + 32)) for the calling
+// thread's row: r holds alpha_g^2-unscaled accumulator values (R = a2 r), cv the
+// row's 32 gate then 32 input C values; writes the row's D_row segment and
+// dprob partial (row_ok), and the warp's dbias column sums (when requested).
+template <int ACT>
+__device__ __forceinline__ void dglu_row_chunk(const DsParams& p, const uint32_t (&r)[32],
+                                               const uint4 (&cv)[8], bool row_ok, int64_t row,
+                                               int64_t j0, int g, float a2, float beta,
+                                               float prob, int lane) {
+  const int64_t two_n = 2 * p.n;
+  const int64_t cbase = row * two_n + 2 * j0;
+  float dg[32], di[32];
+  // per element pair (2i, 2i+1), in packed f32x2 arithmetic; dprob is
+  // accumulated pairwise and the two halves added at the end
+  float dp0 = 0.0f, dp1 = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    // gate words cv[0..15], input words cv[16..31] (as 32-bit words)
+    const uint32_t gw = reinterpret_cast<const uint32_t*>(cv)[i];
+    const uint32_t iw = reinterpret_cast<const uint32_t*>(cv)[16 + i];
+    float R0, R1, rp0, rp1;
+    mul_f32x2(R0, R1, __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), a2);
+    mul_f32x2(rp0, rp1, R0, R1, prob);
+    if (ACT == kSwiGLU) {
+      float g0, g1, x0, x1;
+      mul_f32x2(g0, g1, bf16_lo(gw), bf16_hi(gw), beta);
+      mul_f32x2(x0, x1, bf16_lo(iw), bf16_hi(iw), beta);
+      const float s0 = rcp_approx(__fadd_rn(1.0f, __expf(-g0)));  // sigmoid(gate)
+      const float s1 = rcp_approx(__fadd_rn(1.0f, __expf(-g1)));
+      float om0, om1, t0, t1, gs0, gs1, u0, u1;
+      fma_f32x2(om0, om1, s0, s1, -1.0f, -1.0f, 1.0f, 1.0f);      // 1 - s
+      fma_f32x2(t0, t1, g0, g1, om0, om1, 1.0f, 1.0f);            // 1 + gate (1 - s)
+      mul2_f32x2(gs0, gs1, g0, g1, s0, s1);                       // gate s
+      mul2_f32x2(u0, u1, rp0, rp1, x0, x1);                       // R prob input
+      mul2_f32x2(u0, u1, u0, u1, s0, s1);
+      mul2_f32x2(dg[2 * i], dg[2 * i + 1], u0, u1, t0, t1);
+      mul2_f32x2(di[2 * i], di[2 * i + 1], rp0, rp1, gs0, gs1);
+      float q0, q1;
+      mul2_f32x2(q0, q1, R0, R1, gs0, gs1);
+      fma_f32x2(dp0, dp1, q0, q1, x0, x1, dp0, dp1);             // += R gate s input
+    } else {
+      // clamped GeGLU: gate <= 7, up in [-7, 7], s = sigmoid(1.702 gate_c),
+      // gradients kept at equality with the bounds, linear offset 1
+      const float g0 = bf16_lo(gw), g1 = bf16_hi(gw);
+      const float x0 = bf16_lo(iw), x1 = bf16_hi(iw);
+      const float gc0 = fminf(g0, 7.0f), gc1 = fminf(g1, 7.0f);
+      const float uc0 = fminf(fmaxf(x0, -7.0f), 7.0f), uc1 = fminf(fmaxf(x1, -7.0f), 7.0f);
+      float kg0, kg1;
+      mul_f32x2(kg0, kg1, gc0, gc1, 1.702f);
+      const float s0 = rcp_approx(__fadd_rn(1.0f, __expf(-kg0)));
+      const float s1 = rcp_approx(__fadd_rn(1.0f, __expf(-kg1)));
+      float om0, om1, t0, t1, up0, up1, gs0, gs1, w0, w1, a0, a1, b0, b1;
+      fma_f32x2(om0, om1, s0, s1, -1.0f, -1.0f, 1.0f, 1.0f);      // 1 - s
+      fma_f32x2(t0, t1, kg0, kg1, om0, om1, 1.0f, 1.0f);          // 1 + 1.702 gate_c (1 - s)
+      add_f32x2(up0, up1, uc0, uc1, 1.0f, 1.0f);                  // up_c + 1
+      mul2_f32x2(gs0, gs1, gc0, gc1, s0, s1);                     // gate_c s
+      mul2_f32x2(w0, w1, rp0, rp1, up0, up1);
+      mul2_f32x2(w0, w1, w0, w1, s0, s1);
+      mul2_f32x2(a0, a1, w0, w1, t0, t1);
+      mul2_f32x2(b0, b1, rp0, rp1, gs0, gs1);
+      dg[2 * i] = g0 <= 7.0f ? a0 : 0.0f;
+      dg[2 * i + 1] = g1 <= 7.0f ? a1 : 0.0f;
+      di[2 * i] = (x0 >= -7.0f && x0 <= 7.0f) ? b0 : 0.0f;
+      di[2 * i + 1] = (x1 >= -7.0f && x1 <= 7.0f) ? b1 : 0.0f;
+      float q0, q1;
+      mul2_f32x2(q0, q1, R0, R1, gs0, gs1);
+      fma_f32x2(dp0, dp1, q0, q1, up0, up1, dp0, dp1);           // += R gate_c s (up_c + 1)
+    }
+  }
+  const float dprob_part = dp0 + dp1;
+  if (row_ok) {
+    uint32_t w[32];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      __nv_bfloat162 bg = __floats2bfloat162_rn(dg[2 * i], dg[2 * i + 1]);
+      __nv_bfloat162 bi = __floats2bfloat162_rn(di[2 * i], di[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&bg);
+      w[16 + i] = *reinterpret_cast<uint32_t*>(&bi);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(p.d_row + cbase);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    atomicAdd(p.dprob + row, dprob_part);
+  }
+  if (p.dbias_ws) {
+    // column sums over the warp's 32 rows by a butterfly reduce-scatter:
+    // afterwards lane l holds the sums of gate column l and input column l
+    if (!row_ok) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) { dg[i] = 0.0f; di[i] = 0.0f; }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const bool upper = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < o; ++i) {
+        const float sg = upper ? dg[i] : dg[i + o];
+        const float si = upper ? di[i] : di[i + o];
+        const float kg = upper ? dg[i + o] : dg[i];
+        const float ki = upper ? di[i + o] : di[i];
+        dg[i] = kg + __shfl_xor_sync(0xFFFFFFFFu, sg, o);
+        di[i] = ki + __shfl_xor_sync(0xFFFFFFFFu, si, o);
+      }
+    }
+    float* ws = p.dbias_ws + static_cast<int64_t>(g) * two_n + 2 * j0;
+    atomicAdd(ws + lane, dg[0]);
+    atomicAdd(ws + 32 + lane, di[0]);
+  }
+}
+
 template <int ACT>
 __global__ void __maxnreg__(96)
     dglu_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -248,104 +359,7 @@ __global__ void __maxnreg__(96)
       if (lane == 0) mbar_arrive(tempty_bar(acc));
       if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
       if (!chunk_ok) continue;
-      float dg[32], di[32];
-      // per element pair (2i, 2i+1), in packed f32x2 arithmetic; dprob is
-      // accumulated pairwise and the two halves added at the end
-      float dp0 = 0.0f, dp1 = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        // gate words cv[0..15], input words cv[16..31] (as 32-bit words)
-        const uint32_t gw = reinterpret_cast<const uint32_t*>(cv)[i];
-        const uint32_t iw = reinterpret_cast<const uint32_t*>(cv)[16 + i];
-        float R0, R1, rp0, rp1;
-        mul_f32x2(R0, R1, __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), a2);
-        mul_f32x2(rp0, rp1, R0, R1, prob);
-        if (ACT == kSwiGLU) {
-          float g0, g1, x0, x1;
-          mul_f32x2(g0, g1, bf16_lo(gw), bf16_hi(gw), beta);
-          mul_f32x2(x0, x1, bf16_lo(iw), bf16_hi(iw), beta);
-          const float s0 = rcp_approx(__fadd_rn(1.0f, __expf(-g0)));  // sigmoid(gate)
-          const float s1 = rcp_approx(__fadd_rn(1.0f, __expf(-g1)));
-          float om0, om1, t0, t1, gs0, gs1, u0, u1;
-          fma_f32x2(om0, om1, s0, s1, -1.0f, -1.0f, 1.0f, 1.0f);      // 1 - s
-          fma_f32x2(t0, t1, g0, g1, om0, om1, 1.0f, 1.0f);            // 1 + gate (1 - s)
-          mul2_f32x2(gs0, gs1, g0, g1, s0, s1);                       // gate s
-          mul2_f32x2(u0, u1, rp0, rp1, x0, x1);                       // R prob input
-          mul2_f32x2(u0, u1, u0, u1, s0, s1);
-          mul2_f32x2(dg[2 * i], dg[2 * i + 1], u0, u1, t0, t1);
-          mul2_f32x2(di[2 * i], di[2 * i + 1], rp0, rp1, gs0, gs1);
-          float q0, q1;
-          mul2_f32x2(q0, q1, R0, R1, gs0, gs1);
-          fma_f32x2(dp0, dp1, q0, q1, x0, x1, dp0, dp1);             // += R gate s input
-        } else {
-          // clamped GeGLU: gate <= 7, up in [-7, 7], s = sigmoid(1.702 gate_c),
-          // gradients kept at equality with the bounds, linear offset 1
-          const float g0 = bf16_lo(gw), g1 = bf16_hi(gw);
-          const float x0 = bf16_lo(iw), x1 = bf16_hi(iw);
-          const float gc0 = fminf(g0, 7.0f), gc1 = fminf(g1, 7.0f);
-          const float uc0 = fminf(fmaxf(x0, -7.0f), 7.0f), uc1 = fminf(fmaxf(x1, -7.0f), 7.0f);
-          float kg0, kg1;
-          mul_f32x2(kg0, kg1, gc0, gc1, 1.702f);
-          const float s0 = rcp_approx(__fadd_rn(1.0f, __expf(-kg0)));
-          const float s1 = rcp_approx(__fadd_rn(1.0f, __expf(-kg1)));
-          float om0, om1, t0, t1, up0, up1, gs0, gs1, w0, w1, a0, a1, b0, b1;
-          fma_f32x2(om0, om1, s0, s1, -1.0f, -1.0f, 1.0f, 1.0f);      // 1 - s
-          fma_f32x2(t0, t1, kg0, kg1, om0, om1, 1.0f, 1.0f);          // 1 + 1.702 gate_c (1 - s)
-          add_f32x2(up0, up1, uc0, uc1, 1.0f, 1.0f);                  // up_c + 1
-          mul2_f32x2(gs0, gs1, gc0, gc1, s0, s1);                     // gate_c s
-          mul2_f32x2(w0, w1, rp0, rp1, up0, up1);
-          mul2_f32x2(w0, w1, w0, w1, s0, s1);
-          mul2_f32x2(a0, a1, w0, w1, t0, t1);
-          mul2_f32x2(b0, b1, rp0, rp1, gs0, gs1);
-          dg[2 * i] = g0 <= 7.0f ? a0 : 0.0f;
-          dg[2 * i + 1] = g1 <= 7.0f ? a1 : 0.0f;
-          di[2 * i] = (x0 >= -7.0f && x0 <= 7.0f) ? b0 : 0.0f;
-          di[2 * i + 1] = (x1 >= -7.0f && x1 <= 7.0f) ? b1 : 0.0f;
-          float q0, q1;
-          mul2_f32x2(q0, q1, R0, R1, gs0, gs1);
-          fma_f32x2(dp0, dp1, q0, q1, up0, up1, dp0, dp1);           // += R gate_c s (up_c + 1)
-        }
-      }
-      const float dprob_part = dp0 + dp1;
-      if (row_ok) {
-        uint32_t w[32];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          __nv_bfloat162 bg = __floats2bfloat162_rn(dg[2 * i], dg[2 * i + 1]);
-          __nv_bfloat162 bi = __floats2bfloat162_rn(di[2 * i], di[2 * i + 1]);
-          w[i] = *reinterpret_cast<uint32_t*>(&bg);
-          w[16 + i] = *reinterpret_cast<uint32_t*>(&bi);
-        }
-        uint4* dst = reinterpret_cast<uint4*>(p.d_row + cbase);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-        atomicAdd(p.dprob + row, dprob_part);
-      }
-      if (p.dbias_ws) {
-        // column sums over the warp's 32 rows by a butterfly reduce-scatter:
-        // afterwards lane l holds the sums of gate column l and input column l
-        if (!row_ok) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) { dg[i] = 0.0f; di[i] = 0.0f; }
-        }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
-          const bool upper = (lane & o) != 0;
-#pragma unroll
-          for (int i = 0; i < o; ++i) {
-            const float sg = upper ? dg[i] : dg[i + o];
-            const float si = upper ? di[i] : di[i + o];
-            const float kg = upper ? dg[i + o] : dg[i];
-            const float ki = upper ? di[i + o] : di[i];
-            dg[i] = kg + __shfl_xor_sync(0xFFFFFFFFu, sg, o);
-            di[i] = ki + __shfl_xor_sync(0xFFFFFFFFu, si, o);
-          }
-        }
-        float* ws = p.dbias_ws + static_cast<int64_t>(ti.g) * two_n + 2 * j0;
-        atomicAdd(ws + lane, dg[0]);
-        atomicAdd(ws + 32 + lane, di[0]);
-      }
+      dglu_row_chunk<ACT>(p, r, cv, row_ok, row, j0, ti.g, a2, beta, prob, lane);
     }
   }
 
@@ -478,11 +492,11 @@ int run_dglu(const hq_bf16* a, const hq_bf16* b, const int64_t* b_ptrs, const hq
     const size_t bytes = static_cast<size_t>(L) * static_cast<size_t>(2 * n) * sizeof(float);
     if (cudaMemsetAsync(dbias_ws, 0, bytes, st) != cudaSuccess) return HQ_ERR_CUDA;
   }
+  const int sms = num_sms();
+  if (sms <= 0) return HQ_ERR_CUDA;
   if (cudaFuncSetAttribute(dglu_kernel<ACT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemBytes) != cudaSuccess)
     return HQ_ERR_CUDA;
-  const int sms = num_sms();
-  if (sms <= 0) return HQ_ERR_CUDA;
   const int64_t tiles_bound = ((m + kBM - 1) / kBM) * ((n + kBN - 1) / kBN);
   int64_t grid = sm_count > 0 ? sm_count : sms;
   if (grid > sms) grid = sms;

@@ -71,7 +71,7 @@ def check(ref, d_row, dprob, dbias):
         assert (np.abs(db - ref["dbias"]) <= db_tol).all(), "dbias outside tolerance"
 
 
-@pytest.mark.parametrize("n", [64, 128, 160])
+@pytest.mark.parametrize("n", [64, 128, 160, 288])
 def test_dswiglu_small(cuda_dev, n):
     offsets = [256, 256, 768, 1024]       # empty group 1; rows >= 1024 not written
     check(*run_case(offsets, 1152, n, 192, seed=n))
@@ -82,6 +82,13 @@ def test_dgeglu_small(cuda_dev, n):
     """dGeGLU (fixed 1.702 / +-7 / +1 constants); C spread wide enough to hit both clamps."""
     offsets = [256, 256, 768, 1024]
     check(*run_case(offsets, 1152, n, 192, seed=100 + n, act="dgeglu", c_std=5.0))
+
+
+def test_dswiglu_odd_group_ends(cuda_dev):
+    """Group ends on odd multiples of 128, a 128-row group and an empty one,
+    K over many stages."""
+    offsets = [384, 512, 512, 1408]
+    check(*run_case(offsets, 1536, 256, 640, seed=31))
 
 
 def test_dgeglu_clamp_boundaries_exact(cuda_dev):
