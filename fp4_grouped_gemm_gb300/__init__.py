@@ -98,7 +98,10 @@ def set_gemm_tile_n(tile_n):
 
 
 def set_gemm_2sm(enable):
-    _check(_abi.load().hq_set_gemm_2sm(1 if enable else 0), "hq_set_gemm_2sm")
+    """1 / True: pair tiles with the automatic width; 256 or 384: pair tiles of
+    that width where n allows it; 0 / False: single-SM tiles."""
+    v = enable if enable in (256, 384) else (1 if enable else 0)
+    _check(_abi.load().hq_set_gemm_2sm(v), "hq_set_gemm_2sm")
 
 
 def _q_shape(rows, k, mode):

@@ -52,6 +52,11 @@ int forced_tile_n() { return g_tile_n.load(); }
 
 bool use_2sm() { return g_use_2sm.load() != 0; }
 
+int pair_width() {
+  const int v = g_use_2sm.load();
+  return v == 256 || v == 384 ? v : 0;
+}
+
 int num_sms() {
   const int dev = current_device();
   if (dev < 0) return 0;
@@ -234,7 +239,8 @@ int hq_set_gemm_tile_n(int tile_n) {
 }
 
 int hq_set_gemm_2sm(int enable) {
-  hq::g_use_2sm.store(enable ? 1 : 0);
+  if (enable != 0 && enable != 1 && enable != 256 && enable != 384) return HQ_ERR_INVALID;
+  hq::g_use_2sm.store(enable);
   return HQ_OK;
 }
 

@@ -251,6 +251,47 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& e, Release release)
   }
 }
 
+// Wide pair tile (384 columns): the warp drains tile columns [cw, cw + 128)
+// of the first 256 into registers as epilogue_tile does, converts and stores
+// its 64 columns [256 + cw2, 256 + cw2 + 64) of the last 128 straight from
+// TMEM (16 at a time), then releases the accumulator and stores the drained
+// part.
+template <typename Release>
+__device__ __forceinline__ void epilogue_tile_wide(const EpiArgs& e, int cw2, Release release) {
+  constexpr int kPieces = 8;
+  uint32_t packed[kPieces * 8];
+  {
+    uint32_t r[2][16];
+    tmem_ld_32x32b_x16(e.acc_t + e.cw, r[0]);
+    tmem_ld_wait(r[0]);
+#pragma unroll
+    for (int s = 0; s < kPieces; ++s) {
+      if (s + 1 < kPieces) tmem_ld_32x32b_x16(e.acc_t + e.cw + (s + 1) * 16, r[(s + 1) & 1]);
+      const int64_t col0 = e.n0 + e.cw + s * 16;
+      if (col0 < e.n) epi_convert16(e, col0, r[s & 1], packed + 8 * s);
+      if (s + 1 < kPieces) tmem_ld_wait(r[(s + 1) & 1]);
+    }
+  }
+#pragma unroll 1
+  for (int s = 0; s < 4; ++s) {
+    uint32_t r[16], pk[8];
+    tmem_ld_32x32b_x16(e.acc_t + 256 + cw2 + s * 16, r);
+    tmem_ld_wait(r);
+    const int64_t col0 = e.n0 + 256 + cw2 + s * 16;
+    if (col0 >= e.n) continue;
+    epi_convert16(e, col0, r, pk);
+    epi_store16(e, col0, pk);
+  }
+  tc_fence_before();
+  __syncwarp();
+  release();
+#pragma unroll
+  for (int s = 0; s < kPieces; ++s) {
+    const int64_t col0 = e.n0 + e.cw + s * 16;
+    if (col0 < e.n) epi_store16(e, col0, packed + 8 * s);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // dGLU epilogue of one 32-column chunk (compact columns [j0, j0 + 32)) for the
 // calling thread's row: R = a2 * acc, C's 32 gate and 32 input values of the
@@ -1011,24 +1052,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 // its own 128 rows and the B scales of all 256 tile columns in its TMEM, in
 // the same layout as the single-SM N = 256 tile.
 // ---------------------------------------------------------------------------
-template <int MODE, int STAGES>
+// BN_ = 256: one M = 256, N = 256 MMA per K step.  BN_ = 384 (the wide
+// tile): an N = 256 MMA into accumulator columns [0, 256) and an N = 128 MMA
+// into [256, 384); each CTA holds 192 B rows (128 for the first MMA, then 64
+// for the second), the B scales of all 384 tile rows, and TMEM has room for
+// only SF_SLOTS stages of scales, reused once the MMAs of an older stage are
+// done.
+template <int MODE, int STAGES, int BN_ = 256>
 struct Cfg2 {
   static constexpr int GS = MODE == HQ_NVFP4 ? 16 : 32;
   static constexpr int EPB = MODE == HQ_MXFP8 ? 1 : 2;
   static constexpr int BK = kBKBytes * EPB;
   static constexpr int ATOMS = BK / GS / 4;
-  static constexpr int BN = 256;                       // tile columns (both CTAs)
+  static constexpr int BN = BN_;                       // tile columns (both CTAs)
+  static constexpr int RB = BN / 128;                  // 128-row blocks of the tile's B scales
   static constexpr int A_BYTES = kBM * kBKBytes;       // this CTA's 128 rows of A
-  static constexpr int B_BYTES = 128 * kBKBytes;       // this CTA's 128 rows of B
+  static constexpr int B_BYTES = (BN / 2) * kBKBytes;  // this CTA's BN / 2 rows of B
   static constexpr int SFA_BYTES = ATOMS * 512;        // this CTA's 128 A rows
-  static constexpr int SFB_BYTES = 2 * ATOMS * 512;    // all 256 B rows of the tile
+  static constexpr int SFB_BYTES = RB * ATOMS * 512;   // all BN B rows of the tile
   static constexpr int SFA_COLS = (ATOMS * 4 + 7) / 8 * 8;
-  static constexpr int SFB_COLS = 2 * ATOMS * 4;
+  static constexpr int SFB_COLS = RB * ATOMS * 4;      // first MMA: 8 per atom; second: 4
   static constexpr int SF_STAGE_COLS = (SFA_COLS + SFB_COLS + 15) / 16 * 16;
   static constexpr int SF_BASE_COL = BN;
-  static constexpr int TMEM_USED = BN + STAGES * SF_STAGE_COLS;
+  static constexpr int SF_FIT = (512 - BN) / SF_STAGE_COLS;
+  static constexpr int SF_SLOTS = SF_FIT < STAGES ? SF_FIT : STAGES;
+  static_assert(SF_SLOTS >= 1 && STAGES % SF_SLOTS == 0, "scale slots");
+  static constexpr int TMEM_USED = BN + SF_SLOTS * SF_STAGE_COLS;
   static constexpr int TMEM_COLS = 512;
   static_assert(TMEM_USED <= 512, "TMEM budget");
+  static_assert(BN == 256 || BN == 384, "pair tiles of 256 or 384 columns");
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
@@ -1040,25 +1092,30 @@ struct Cfg2 {
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget");
-  // M = 256 across the pair, N = 256
-  static constexpr uint32_t IDESC_BASE =
+  // M = 256 across the pair; N = 256 (IDESC_BASE) and, for the wide tile's
+  // second MMA, N = 128 (IDESC_N128)
+  static constexpr uint32_t IDESC_KIND =
       (MODE == HQ_MXFP8 ? ((0u << 7) | (0u << 10) | (1u << 23))
        : MODE == HQ_MXFP4 ? ((1u << 7) | (1u << 10) | (1u << 23))
                           : ((1u << 7) | (1u << 10) | (0u << 23)))
-      | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(256 >> 4) << 24);
+      | (static_cast<uint32_t>(256 >> 4) << 24);
+  static constexpr uint32_t IDESC_BASE = IDESC_KIND | (static_cast<uint32_t>(256 >> 3) << 17);
+  static constexpr uint32_t IDESC_N128 = IDESC_KIND | (static_cast<uint32_t>(128 >> 3) << 17);
 };
 
 // EPI = kEpiSwiGLUQ: the fused up-proj (p.n = H): the tile's 256 B rows are
 // gate rows [n0, n0 + 128) (even CTA) and up rows [H + n0, H + n0 + 128) (odd
 // CTA), so each CTA's accumulator half holds gate in columns [0, 128) and up
 // in [128, 256), as in the single-SM fused tile; tiles step 128 compact columns.
-template <int MODE, int STAGES, int EPI = kEpiGemm>
+template <int MODE, int STAGES, int EPI = kEpiGemm, int BN = 256>
 __global__ void __launch_bounds__(kThreads, 1)
     bs_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const GemmParams p) {
-  using C = Cfg2<MODE, STAGES>;
+  using C = Cfg2<MODE, STAGES, BN>;
   constexpr bool kUpProj = EPI == kEpiSwiGLUQ;
+  constexpr bool kWide = BN == 384;
   static_assert(EPI == kEpiGemm || kUpProj, "2-SM epilogues: plain GEMM or fused up-proj");
+  static_assert(!(kWide && kUpProj), "the fused up-proj uses 256-column pair tiles");
   constexpr int TW = kUpProj ? C::BN / 2 : C::BN;  // output columns per tile
   static_assert(kSfPath == 2, "the 2-SM kernel stages scales with tcgen05.st");
   extern __shared__ uint8_t smem_raw[];
@@ -1201,11 +1258,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t t = cluster_id; ok && t < total; t += num_clusters) {
         const PairTile pt = pair_tile(t);
         const int64_t row0 = pt.row0;
-        // this CTA's 128 B rows, and the 128-row blocks of the tile's 256 B rows
+        // this CTA's first 128 B rows, and the 128-row blocks of the tile's B
         const int nh0 = kUpProj ? (rank ? static_cast<int>(p.n) + pt.n0 : pt.n0)
                                 : pt.n0 + static_cast<int>(rank) * 128;
-        const int64_t sfb_blk0 = pt.n0 / 128;
-        const int64_t sfb_blk1 = kUpProj ? (p.n + pt.n0) / 128 : pt.n0 / 128 + 1;
+        auto sfb_blk = [&](int rb) -> int64_t {
+          return kUpProj && rb == 1 ? (p.n + pt.n0) / 128 : pt.n0 / 128 + rb;
+        };
         // a CTA whose 128 rows hold no valid row loads no A and no A scales
         // (its accumulator half is never stored)
         const bool has_a = pt.mine > 0;
@@ -1225,14 +1283,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (has_a)
             tma_load_2d_pair(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, fb, kb * kBKBytes,
                              static_cast<int32_t>(row0));
-          tma_load_3d_pair(sbase + C::OFF_B + stage * C::B_BYTES, &tmB, fb, kb * kBKBytes, nh0, pt.g);
-          mbar_arrive_expect_tx(sffull_bar(stage), atoms * 512u * (has_sfa ? 3u : 2u));
+          const uint32_t b_s = sbase + C::OFF_B + stage * C::B_BYTES;
+          if (kWide) {
+            // 64-row boxes: B rows [n0 + 128 r, + 128) for the N = 256 MMA,
+            // then [n0 + 256 + 64 r, + 64) for the N = 128 MMA
+            tma_load_3d_pair(b_s, &tmB, fb, kb * kBKBytes, nh0, pt.g);
+            tma_load_3d_pair(b_s + 64 * kBKBytes, &tmB, fb, kb * kBKBytes, nh0 + 64, pt.g);
+            tma_load_3d_pair(b_s + 128 * kBKBytes, &tmB, fb, kb * kBKBytes,
+                             pt.n0 + 256 + static_cast<int>(rank) * 64, pt.g);
+          } else {
+            tma_load_3d_pair(b_s, &tmB, fb, kb * kBKBytes, nh0, pt.g);
+          }
+          mbar_arrive_expect_tx(sffull_bar(stage), atoms * 512u * (has_sfa ? 1u + C::RB : C::RB));
           if (has_sfa)
             bulk_load(sbase + C::OFF_SFA + stage * C::SFA_BYTES, sfa_rows + kb * C::ATOMS * 512,
                       atoms * 512u, sffull_bar(stage));
-          for (int rb = 0; rb < 2; ++rb)
+          for (int rb = 0; rb < C::RB; ++rb)
             bulk_load(sbase + C::OFF_SFB + stage * C::SFB_BYTES + rb * C::ATOMS * 512,
-                      sfb_grp + ((rb ? sfb_blk1 : sfb_blk0) * atoms_total + kb * C::ATOMS) * 512,
+                      sfb_grp + (sfb_blk(rb) * atoms_total + kb * C::ATOMS) * 512,
                       atoms * 512u, sffull_bar(stage));
           filled_a |= 1u << stage;
           filled_s |= 1u << stage;
@@ -1273,27 +1341,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           int atoms = atoms_total - kb * C::ATOMS;
           atoms = atoms < C::ATOMS ? atoms : C::ATOMS;
-          const uint32_t sfa_t = tmem_base + C::SF_BASE_COL + stage * C::SF_STAGE_COLS;
+          const int slot = stage % C::SF_SLOTS;
+          const uint32_t sfa_t = tmem_base + C::SF_BASE_COL + slot * C::SF_STAGE_COLS;
           const uint32_t sfb_t = sfa_t + C::SFA_COLS;
+          const uint32_t sfb2_t = sfb_t + C::ATOMS * 8;  // wide tile: the N = 128 MMA's scales
           const uint64_t ad = adesc0 + static_cast<uint64_t>((stage * C::A_BYTES) >> 4);
           const uint64_t bd = bdesc0 + static_cast<uint64_t>((stage * C::B_BYTES) >> 4);
+          const uint64_t bd2 = bd + static_cast<uint64_t>((128 * kBKBytes) >> 4);
           const uint32_t acc0 = kb > 0 ? 1u : 0u;
           auto issue = [&](int j, uint32_t acc_flag) {
             if (MODE == HQ_MXFP8) {
-              const uint32_t idesc = C::IDESC_BASE | (static_cast<uint32_t>(j) << 4) |
-                                     (static_cast<uint32_t>(j) << 29);
-              mma_mxf8_2sm(tmem_base, ad + 2 * j, bd + 2 * j, idesc,
-                           sfa_t | (static_cast<uint32_t>(j) << 30),
-                           sfb_t | (static_cast<uint32_t>(j) << 30), acc_flag);
+              const uint32_t sel = (static_cast<uint32_t>(j) << 4) | (static_cast<uint32_t>(j) << 29);
+              const uint32_t sfs = static_cast<uint32_t>(j) << 30;
+              mma_mxf8_2sm(tmem_base, ad + 2 * j, bd + 2 * j, C::IDESC_BASE | sel, sfa_t | sfs,
+                           sfb_t | sfs, acc_flag);
+              if (kWide)
+                mma_mxf8_2sm(tmem_base + 256, ad + 2 * j, bd2 + 2 * j, C::IDESC_N128 | sel, sfa_t | sfs,
+                             sfb2_t | sfs, acc_flag);
             } else if (MODE == HQ_MXFP4) {
               const uint32_t sf = static_cast<uint32_t>(j & 1) * 2u;
-              const uint32_t idesc = C::IDESC_BASE | (sf << 4) | (sf << 29);
-              mma_mxf4_2sm(tmem_base, ad + 2 * j, bd + 2 * j, idesc,
+              const uint32_t sel = (sf << 4) | (sf << 29);
+              mma_mxf4_2sm(tmem_base, ad + 2 * j, bd + 2 * j, C::IDESC_BASE | sel,
                            (sfa_t + (j >> 1) * 4) | (sf << 30), (sfb_t + (j >> 1) * 8) | (sf << 30),
                            acc_flag);
+              if (kWide)
+                mma_mxf4_2sm(tmem_base + 256, ad + 2 * j, bd2 + 2 * j, C::IDESC_N128 | sel,
+                             (sfa_t + (j >> 1) * 4) | (sf << 30), (sfb2_t + (j >> 1) * 4) | (sf << 30),
+                             acc_flag);
             } else {
               mma_nvf4_2sm(tmem_base, ad + 2 * j, bd + 2 * j, C::IDESC_BASE, sfa_t + j * 4,
                            sfb_t + j * 8, acc_flag);
+              if (kWide)
+                mma_nvf4_2sm(tmem_base + 256, ad + 2 * j, bd2 + 2 * j, C::IDESC_N128, sfa_t + j * 4,
+                             sfb2_t + j * 4, acc_flag);
             }
           };
           if (MODE == HQ_MXFP8 || atoms == C::ATOMS) {
@@ -1320,6 +1400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
+    int64_t kbi = 0;  // k-blocks this warp has staged
     for (int64_t t = cluster_id; ok && t < total; t += num_clusters) {
       for (int kb = 0; kb < num_kb; ++kb) {
         int atoms = atoms_total - kb * C::ATOMS;
@@ -1327,23 +1408,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool w = wait_bounded(sffull_bar(stage), phase, wctx);
         ok = __all_sync(0xFFFFFFFFu, w);
         if (!ok) break;
-        const uint32_t sfa_t = tmem_base + C::SF_BASE_COL + stage * C::SF_STAGE_COLS;
+        if (C::SF_SLOTS < STAGES && kbi >= C::SF_SLOTS) {
+          // the TMEM scale slot is shared with k-block kbi - SF_SLOTS: its
+          // MMAs (committed to that stage's empty barrier) must be done
+          const int64_t j = kbi - C::SF_SLOTS;
+          const bool we = wait_bounded(empty_bar(static_cast<int>(j % STAGES)),
+                                       static_cast<uint32_t>(j / STAGES) & 1u, wctx);
+          ok = __all_sync(0xFFFFFFFFu, we);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        const int slot = stage % C::SF_SLOTS;
+        const uint32_t sfa_t = tmem_base + C::SF_BASE_COL + slot * C::SF_STAGE_COLS;
         const uint32_t sfb_t = sfa_t + C::SFA_COLS;
+        const uint32_t sfb2_t = sfb_t + C::ATOMS * 8;
         const uint32_t sfa_s = sbase + C::OFF_SFA + stage * C::SFA_BYTES;
         const uint32_t sfb_s = sbase + C::OFF_SFB + stage * C::SFB_BYTES;
-        // B scales at columns sfb_t + (a * 2 + rb) * 4: k-atom a, 128-row block rb
+        // B scales at columns sfb_t + (a * 2 + rb) * 4 (k-atom a, 128-row
+        // block rb = 0, 1) and, for the wide tile, sfb2_t + a * 4 (block 2)
         if (atoms == C::ATOMS) {
           constexpr int NA = 4 * C::ATOMS;
-          uint32_t va[NA], vb[2 * NA];
+          uint32_t va[NA], vb[2 * NA], vb2[NA];
 #pragma unroll
           for (int a = 0; a < C::ATOMS; ++a) {
             lds128(sfa_s + a * 512 + lane * 16, va + 4 * a);
 #pragma unroll
             for (int rb = 0; rb < 2; ++rb)
               lds128(sfb_s + (rb * C::ATOMS + a) * 512 + lane * 16, vb + 4 * (a * 2 + rb));
+            if (kWide) lds128(sfb_s + (2 * C::ATOMS + a) * 512 + lane * 16, vb2 + 4 * a);
           }
           tmem_st_32x32b<NA>(lq + sfa_t, va);
           tmem_st_32x32b<2 * NA>(lq + sfb_t, vb);
+          if (kWide) tmem_st_32x32b<NA>(lq + sfb2_t, vb2);
         } else {
           for (int a = 0; a < atoms; ++a) {
             uint32_t v[4];
@@ -1352,6 +1448,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int rb = 0; rb < 2; ++rb) {
               lds128(sfb_s + (rb * C::ATOMS + a) * 512 + lane * 16, v);
               tmem_st_32x32b<4>(lq + sfb_t + (a * 2 + rb) * 4, v);
+            }
+            if (kWide) {
+              lds128(sfb_s + (2 * C::ATOMS + a) * 512 + lane * 16, v);
+              tmem_st_32x32b<4>(lq + sfb2_t + a * 4, v);
             }
           }
         }
@@ -1366,6 +1466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(ready_bar(stage), 0));
+        ++kbi;
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }
@@ -1410,7 +1511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       EpiArgs e;
       e.acc_t = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-      e.cw = (ew >> 2) * (C::BN / 2);
+      e.cw = (ew >> 2) * 128;  // the first 256 columns (the wide tile's rest: epilogue_tile_wide)
       e.n0 = pt.n0;
       e.n = p.n;
       e.alpha = alpha;
@@ -1420,7 +1521,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       e.rows_lo = 0;
       e.stage_s = sbase + C::OFF_STAGE_OUT + ew * 1024;
       e.lane = lane;
-      epilogue_tile<C::BN, true>(e, [&] { if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader); });
+      auto release = [&] { if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader); };
+      if (kWide) epilogue_tile_wide(e, (ew >> 2) * 64, release);
+      else epilogue_tile<C::BN, true>(e, release);
       acc_phase ^= 1u;
     }
   }
@@ -1496,10 +1599,10 @@ int run_bs(const void* a, const void* b, const GemmParams& p0, int sm_count, boo
   return e == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
 }
 
-template <int MODE, int STAGES, int EPI = kEpiGemm>
+template <int MODE, int STAGES, int EPI = kEpiGemm, int BN = 256>
 int run_bs_2sm(const void* a, const void* b, const GemmParams& p, int sm_count, bool pdl,
                cudaStream_t st) {
-  using C = Cfg2<MODE, STAGES>;
+  using C = Cfg2<MODE, STAGES, BN>;
   constexpr bool kUpProj = EPI == kEpiSwiGLUQ;
   const uint64_t b_rows = static_cast<uint64_t>(kUpProj ? 2 * p.n : p.n);
   const uint64_t kbytes = static_cast<uint64_t>(p.k) / C::EPB;
@@ -1515,12 +1618,12 @@ int run_bs_2sm(const void* a, const void* b, const GemmParams& p, int sm_count, 
   {
     const uint64_t dims[3] = {kbytes, b_rows, static_cast<uint64_t>(p.gs.groups)};
     const uint64_t strides[2] = {kbytes, kbytes * b_rows};
-    const uint32_t box[3] = {kBKBytes, 128, 1};
+    const uint32_t box[3] = {kBKBytes, BN == 384 ? 64u : 128u, 1};  // wide tile: 64-row boxes
     int rc = encode_tensor_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(b), dims,
                                strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != HQ_OK) return rc;
   }
-  auto kern = bs_gemm_2sm_kernel<MODE, STAGES, EPI>;
+  auto kern = bs_gemm_2sm_kernel<MODE, STAGES, EPI, BN>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
       cudaSuccess)
     return HQ_ERR_CUDA;
@@ -1531,7 +1634,7 @@ int run_bs_2sm(const void* a, const void* b, const GemmParams& p, int sm_count, 
   const int64_t m_pairs = p.gs.sched == kMasked
                              ? static_cast<int64_t>(p.gs.groups) * ((p.gs.max_m + 255) / 256)
                              : (p.gs.a_rows + 255) / 256 + (p.gs.sched == kContig ? p.gs.groups : 0);
-  const int64_t tw = kUpProj ? 128 : 256;
+  const int64_t tw = kUpProj ? 128 : BN;
   const int64_t pairs_needed = m_pairs * ((p.n + tw - 1) / tw);
   int64_t pairs = (sm_count > 0 ? sm_count : sms) / 2;
   if (pairs > sms / 2) pairs = sms / 2;
@@ -1561,8 +1664,17 @@ int run_gemm(hq_mode mode, const void* a, const void* b, const GemmParams& p, in
   // dense, contiguous and masked problems with whole 256-column tiles
   // (masked: experts padded to a multiple of 256 rows) use the 2-SM kernel
   // unless a single-SM tile width is forced
+  // (384-column pair tiles: n a multiple of 384; chosen automatically for
+  // dense problems)
   const bool pairable = !p.b_maps && (p.gs.sched == kDense || p.gs.sched == kContig ||
                                       (p.gs.sched == kMasked && p.gs.max_m % 256 == 0));
+  const int pw = pair_width();
+  const bool wide = p.n % 384 == 0 && (pw == 384 || (pw == 0 && p.gs.sched == kDense));
+  if (bn == 0 && pairable && use_2sm() && wide) {
+    if (mode == HQ_MXFP8) return run_bs_2sm<HQ_MXFP8, 4, kEpiGemm, 384>(a, b, p, sm_count, pdl, st);
+    if (mode == HQ_MXFP4) return run_bs_2sm<HQ_MXFP4, 4, kEpiGemm, 384>(a, b, p, sm_count, pdl, st);
+    return run_bs_2sm<HQ_NVFP4, 4, kEpiGemm, 384>(a, b, p, sm_count, pdl, st);
+  }
   if (bn == 0 && pairable && p.n % 256 == 0 && use_2sm()) {
     if (mode == HQ_MXFP8) return run_bs_2sm<HQ_MXFP8, 6>(a, b, p, sm_count, pdl, st);
     if (mode == HQ_MXFP4) return run_bs_2sm<HQ_MXFP4, 5>(a, b, p, sm_count, pdl, st);

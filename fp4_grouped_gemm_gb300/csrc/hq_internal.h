@@ -24,8 +24,11 @@ int num_sms();
 // Forced GEMM tile width (0 = automatic).
 int forced_tile_n();
 
-// Whether dense GEMMs may use the 2-SM (cluster pair) kernel.
+// Whether GEMMs may use the 2-SM (cluster pair) kernel.
 bool use_2sm();
+
+// Forced pair tile width (256 or 384), or 0 to choose automatically.
+int pair_width();
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point.
 // Returns HQ_OK or HQ_ERR_CUDA.

@@ -137,10 +137,14 @@ int hq_selftest_wait_expiry(uint64_t limit_ns, hq_stream_t s);
  * calls. */
 int hq_set_gemm_tile_n(int tile_n);
 
-/* Tuning knob: 1 (default, the faster choice on GB300) runs dense
- * block-scaled GEMMs whose n is a multiple of 256 on pairs of SMs (a two-CTA
- * cluster computing 256 x 256 tiles with cta_group::2 MMAs, which halves the
- * B bytes each SM loads); 0 keeps every GEMM on single-SM tiles.  Applies to
+/* Tuning knob for the pair tiles.  1 (default, the faster choice on GB300)
+ * runs the dense, contiguous-grouped (padded_offsets), masked (max_m a
+ * multiple of 256) and fused up-proj block-scaled GEMMs on pairs of SMs: a
+ * two-CTA cluster computing 256-row tiles with cta_group::2 MMAs, which cuts
+ * the operand bytes each SM loads per FLOP.  Tiles are 256 columns wide, or
+ * 384 (an N = 256 and an N = 128 MMA per K step) for dense GEMMs whose n is a
+ * multiple of 384.  256 or 384 forces that width where n allows it; 0 keeps
+ * every GEMM on single-SM tiles.  Other values: HQ_ERR_INVALID.  Applies to
  * later calls. */
 int hq_set_gemm_2sm(int enable);
 

@@ -220,6 +220,10 @@ def test_knobs_validate(lib):
     assert lib.hq_set_gemm_tile_n(0) == _abi.HQ_OK
     assert lib.hq_set_wait_limit_ns(0) == _abi.HQ_ERR_INVALID
     assert lib.hq_selftest_wait_expiry(0, None) == _abi.HQ_ERR_INVALID
+    for v in (0, 1, 256, 384):
+        assert lib.hq_set_gemm_2sm(v) == _abi.HQ_OK
+    assert lib.hq_set_gemm_2sm(128) == _abi.HQ_ERR_INVALID
+    assert lib.hq_set_gemm_2sm(1) == _abi.HQ_OK
 
 
 def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):

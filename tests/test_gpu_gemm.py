@@ -275,6 +275,29 @@ def test_grouped_masked_small(cuda_dev, tile_n, mode):
     assert status == 0
 
 
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4", "mxfp4"])
+@pytest.mark.parametrize("m,n,k", [(300, 384, 512), (129, 1152, 640), (512, 384, 1536)])
+def test_dense_wide_pair_tiles(cuda_dev, mode, m, n, k):
+    """n % 384 == 0: 256 x 384 pair tiles (an N = 256 and an N = 128 MMA per K
+    step, two TMEM scale slots for NVFP4), ragged M and K."""
+    if mode != "nvfp4" and k % 128:
+        pytest.skip("MXFP8 and MXFP4 need k % 128 == 0")
+    hq.set_gemm_2sm(1)
+    dense_case(m, n, k, mode, 0, alpha={"nvfp4": 0.5, "mxfp8": 1.25, "mxfp4": None}[mode],
+               bias=(mode == "mxfp8"), seed=m + n + k, g_a=2.0 if mode == "nvfp4" else None,
+               g_b=64.0 if mode == "nvfp4" else None)
+
+
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4"])
+def test_grouped_wide_pair_tiles_forced(cuda_dev, mode):
+    """hq_set_gemm_2sm(384) puts the grouped layouts on 384-column pair tiles too."""
+    hq.set_gemm_2sm(384)
+    alpha = [0.5, 1.0, 2.0, 1.25]
+    contig_case([384, 384, 512, 1152], 1280, 768, 512, mode, 0, alpha=alpha, bias=(mode == "mxfp8"), seed=41)
+    status = masked_case([0, 129, 256, 300], 512, 768, 512, mode, 0, alpha=alpha, seed=43)
+    assert status == 0
+
+
 @pytest.mark.parametrize("two_sm", [1, 0])
 @pytest.mark.parametrize("mode", ["mxfp8", "nvfp4", "mxfp4"])
 def test_grouped_masked_pairs(cuda_dev, mode, two_sm):
