@@ -373,7 +373,7 @@ def headline(hq, dev, args, ws, peaks, pk_src):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_fp4, "unit": "TFLOP/s",
                      "frac": achieved / peak_fp4, "traffic": profiled_traffic(),
                      "traffic_unit": "bytes per launch (ncu dram read + write)",
-                     "kernel": "bs_gemm_2sm_kernel<NVFP4,5> (cluster pair, 256x256 tiles)",
+                     "kernel": "bs_gemm_2sm_kernel<NVFP4,4,GEMM,384> (cluster pair, 256x384 tiles)",
                      "peak_source": f"{pk_src} bf16 burst {peaks['bf16_tflops']} x 6 (nominal FP4/BF16)"},
         "e2e": {"value": ws * flops / e2e_t / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
