@@ -294,9 +294,16 @@ def headline(hq, dev, args, ws, peaks, pk_src):
     a, b = cfg["a"], cfg["b"]
     st = torch.cuda.current_stream()
 
+    # A and B are quantised concurrently (B on a side stream): the small A
+    # launch's ramp and tail overlap B's
+    side = torch.cuda.Stream(device=dev)
+
     def step(gemm_events=None):
+        side.wait_stream(st)
+        with torch.cuda.stream(side):
+            hq.hq_quant(b, "nvfp4", global_scale=gb, q_out=qb, sf_out=sfb)
         hq.hq_quant(a, "nvfp4", global_scale=ga, q_out=qa, sf_out=sfa)
-        hq.hq_quant(b, "nvfp4", global_scale=gb, q_out=qb, sf_out=sfb)
+        st.wait_stream(side)
         if gemm_events:
             gemm_events[0].record(st)
         hq.hq_gemm_dense(qa, sfa, qb, sfb, m, n, k, "nvfp4", alpha=alpha, out=out)
@@ -367,7 +374,7 @@ def headline(hq, dev, args, ws, peaks, pk_src):
     return {
         "value": value, "ms_per_step": total_max / args.steps * 1e3,
         "config": {"workload": cfg["name"], "M": m, "N": n, "K": k, "mode": "nvfp4",
-                   "step": "hq_quant(A) + hq_quant(B) + hq_gemm_dense",
+                   "step": "hq_quant(A) || hq_quant(B) on two streams, then hq_gemm_dense",
                    "l2": "flushed before every timed step (256 MiB written, then 256 MiB read)",
                    "inputs": "A ~ N(0,1), B ~ N(0,0.02) BF16, seeded; g = 2688/amax per tensor"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_fp4, "unit": "TFLOP/s",
