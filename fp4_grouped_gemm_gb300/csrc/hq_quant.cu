@@ -139,7 +139,7 @@ template <int MODE, bool SWIGLU, bool F16IN = false>
 __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
   constexpr int GS = MODE == HQ_NVFP4 ? 16 : 32;
   constexpr int NV = GS / 8;          // 16-byte loads per operand and group
-  constexpr int U = MODE == HQ_NVFP4 ? 2 : 1;  // groups a lane holds in flight
+  constexpr int U = MODE == HQ_NVFP4 ? (SWIGLU ? 2 : 4) : 1;  // groups a lane holds in flight
   __shared__ float r_table[128];
   pdl_wait();  // the global scale and the input may come from the preceding kernel
   const float g = (MODE == HQ_NVFP4 && p.global_scale) ? __ldg(p.global_scale) : 1.0f;
