@@ -82,6 +82,22 @@ __device__ __forceinline__ void f16x8_to_f32(const uint4& v, float (&x)[8]) {
 }
 
 
+// Eight floats -> one word of eight E2M1 codes (element 2 j in the low nibble
+// of byte j): four paired conversions packed with one vector move.
+__device__ __forceinline__ uint32_t cvt_e2m1x8(float x0, float x1, float x2, float x3, float x4,
+                                               float x5, float x6, float x7) {
+  uint32_t w;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(w)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3), "f"(x4), "f"(x5), "f"(x6), "f"(x7));
+  return w;
+}
+
 // One lane quantises one whole scale group of GS values x[0..GS).
 // MXFP8 writes GS E4M3 bytes to qw[0..GS/4); NVFP4 and MXFP4 write GS/2 packed
 // bytes to qw[0..GS/8).
@@ -110,12 +126,10 @@ __device__ __forceinline__ uint32_t encode_group(const float (&x)[GS], float g,
     const float mult = pow2_neg_unbiased(byte);
 #pragma unroll
     for (int i = 0; i < GS / 8; ++i) {
-      uint32_t w = 0;
+      float y[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        w |= cvt_e2m1x2(__fmul_rn(x[8 * i + 2 * j + 1], mult), __fmul_rn(x[8 * i + 2 * j], mult))
-             << (8 * j);
-      qw[i] = w;
+      for (int j = 0; j < 4; ++j) mul_f32x2(y[2 * j], y[2 * j + 1], x[8 * i + 2 * j], x[8 * i + 2 * j + 1], mult);
+      qw[i] = cvt_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
     }
     return byte;
   } else {
@@ -124,11 +138,10 @@ __device__ __forceinline__ uint32_t encode_group(const float (&x)[GS], float g,
     const float r = r_table[byte];  // g / value(byte), 0 for a zero scale
 #pragma unroll
     for (int i = 0; i < GS / 8; ++i) {
-      uint32_t w = 0;
+      float y[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        w |= cvt_e2m1x2(__fmul_rn(x[8 * i + 2 * j + 1], r), __fmul_rn(x[8 * i + 2 * j], r)) << (8 * j);
-      qw[i] = w;
+      for (int j = 0; j < 4; ++j) mul_f32x2(y[2 * j], y[2 * j + 1], x[8 * i + 2 * j], x[8 * i + 2 * j + 1], r);
+      qw[i] = cvt_e2m1x8(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
     }
     return byte;
   }
