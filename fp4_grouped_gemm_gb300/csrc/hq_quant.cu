@@ -98,6 +98,18 @@ __device__ __forceinline__ uint32_t cvt_e2m1x8(float x0, float x1, float x2, flo
   return w;
 }
 
+// Four floats -> one word of four E4M3 codes (element j in byte j).
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float x0, float x1, float x2, float x3) {
+  uint32_t w;
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 l, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 h, %4, %3;\n\t"
+      "mov.b32 %0, {l, h};\n\t}"
+      : "=r"(w)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
+  return w;
+}
+
 // One lane quantises one whole scale group of GS values x[0..GS).
 // MXFP8 writes GS E4M3 bytes to qw[0..GS/4); NVFP4 and MXFP4 write GS/2 packed
 // bytes to qw[0..GS/8).
@@ -113,9 +125,10 @@ __device__ __forceinline__ uint32_t encode_group(const float (&x)[GS], float g,
     const float mult = pow2_neg_unbiased(byte);
 #pragma unroll
     for (int i = 0; i < GS / 4; ++i) {
-      const uint32_t lo = cvt_e4m3x2(__fmul_rn(x[4 * i + 1], mult), __fmul_rn(x[4 * i], mult));
-      const uint32_t hi = cvt_e4m3x2(__fmul_rn(x[4 * i + 3], mult), __fmul_rn(x[4 * i + 2], mult));
-      qw[i] = lo | (hi << 16);
+      float y[4];
+      mul_f32x2(y[0], y[1], x[4 * i], x[4 * i + 1], mult);
+      mul_f32x2(y[2], y[3], x[4 * i + 2], x[4 * i + 3], mult);
+      qw[i] = cvt_e4m3x4(y[0], y[1], y[2], y[3]);
     }
     return byte;
   } else if (MODE == HQ_MXFP4) {
