@@ -12,7 +12,7 @@
 // Persistent warp-specialised kernel: warp 0 streams A / B tiles with TMA into
 // a ring of shared-memory stages, warp 1 issues the MMAs into one of two TMEM
 // accumulators (so the epilogue of tile i overlaps the main loop of tile i+1),
-// warps 2..17 run the epilogue (four per TMEM lane quarter, each owning one of
+// warps 2..9 run the epilogue (two per TMEM lane quarter, each owning two of
 // the tile's four 32-column chunks).  A compact tile of 128 columns j maps to the
 // 256 C / D_row columns [2 j0, 2 j0 + 256).  Each epilogue thread owns one
 // row: it reads that row's C segment, writes its D_row segment, adds its
@@ -33,7 +33,8 @@
 namespace hq {
 namespace {
 
-constexpr int kEpiWarps = 16;     // four per TMEM lane quarter, one 32-column chunk each
+constexpr int kEpiWarps = 8;      // two per TMEM lane quarter, two 32-column chunks each
+constexpr int kChunksPerWarp = 16 / kEpiWarps;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kBN = 128;          // compact columns per tile
 constexpr int kBKElems = 64;      // BF16 elements of K per stage (128 bytes)
@@ -80,8 +81,6 @@ __device__ __forceinline__ float rcp_approx(float x) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// 18 warps share four 16K-register sub-partitions (up to 5 warps on one):
-// 96 registers per thread is the most that lets the block launch.
 enum Act : int { kSwiGLU = 0, kGeGLU = 1 };
 
 // dGLU of one 32-column chunk (compact columns [j0, j0 + 32)) for the calling
@@ -196,7 +195,7 @@ __device__ __forceinline__ void dglu_row_chunk(const DsParams& p, const uint32_t
 }
 
 template <int ACT>
-__global__ void __maxnreg__(96)
+__global__ void __launch_bounds__(kThreads, 1)
     dglu_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const DsParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -320,8 +319,8 @@ __global__ void __maxnreg__(96)
       wait_drain(drain_bar, 0, p.wait_limit_ns);
     }
   } else {
-    const int q = warp & 3;         // TMEM lane quarter this warp may access
-    const int c = (warp - 2) >> 2;  // the tile's 32-column chunk this warp owns
+    const int q = warp & 3;          // TMEM lane quarter this warp may access
+    const int cg = (warp - 2) >> 2;  // the warp's chunks: cg * kChunksPerWarp + 0, 1, ...
     const int64_t two_n = 2 * p.n;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -330,36 +329,46 @@ __global__ void __maxnreg__(96)
       const int r_local = q * 32 + lane;
       const bool row_ok = r_local < ti.rows_valid;
       const int64_t row = ti.row0 + r_local;
-      const int64_t j0 = ti.n0 + c * 32;
-      // n % 32 == 0: a chunk is all in or all out; a skipped expert writes nothing
-      const bool chunk_ok = j0 < p.n && (!p.w_ok || __ldg(p.w_ok + ti.g) != 0);
-      // this row's C segment (32 gate then 32 input values) is loaded before
-      // the accumulator is ready, so its latency overlaps the wait
-      const int64_t cbase = row * two_n + 2 * j0;
-      uint4 cv[8];
-      {
-        const bool ld = row_ok && chunk_ok;
-        const uint4* src = reinterpret_cast<const uint4*>(p.c + cbase);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) cv[i] = ld ? __ldcs(src + i) : make_uint4(0, 0, 0, 0);
-      }
+      // a skipped expert (discrete weights) writes nothing
+      const bool tile_ok = !p.w_ok || __ldg(p.w_ok + ti.g) != 0;
       const float alpha = __ldg(p.alpha + ti.g);
       const float a2 = __fmul_rn(alpha, alpha);
       const float beta = ACT == kSwiGLU ? __ldg(p.beta + ti.g) : 1.0f;
       const float prob = row_ok ? __ldg(p.prob + row) : 0.0f;
-      const bool ok = wait_bounded(tfull_bar(acc), acc_phase, wctx);
-      if (!__all_sync(0xFFFFFFFFu, ok)) break;
-      tc_fence_after();
-      uint32_t r[32];
-      tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN + c * 32, r);
-      tmem_ld_wait();
-      // the accumulator chunk is in registers: release it to the MMA issuer
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      bool ok = true;
+#pragma unroll 1
+      for (int cc = 0; cc < kChunksPerWarp; ++cc) {
+        const int c = cg * kChunksPerWarp + cc;
+        const int64_t j0 = ti.n0 + c * 32;
+        // n % 32 == 0: a chunk is all in or all out
+        const bool chunk_ok = j0 < p.n && tile_ok;
+        // this row's C segment (32 gate then 32 input values) is loaded before
+        // its accumulator columns are read, so its latency overlaps the wait
+        uint4 cv[8];
+        {
+          const bool ld = row_ok && chunk_ok;
+          const uint4* src = reinterpret_cast<const uint4*>(p.c + row * two_n + 2 * j0);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) cv[i] = ld ? __ldcs(src + i) : make_uint4(0, 0, 0, 0);
+        }
+        if (cc == 0) {
+          const bool w = wait_bounded(tfull_bar(acc), acc_phase, wctx);
+          if (!__all_sync(0xFFFFFFFFu, w)) { ok = false; break; }
+          tc_fence_after();
+        }
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN + c * 32, r);
+        tmem_ld_wait();
+        if (cc == kChunksPerWarp - 1) {
+          // the warp's last chunk is in registers: release the accumulator
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(acc));
+        }
+        if (chunk_ok) dglu_row_chunk<ACT>(p, r, cv, row_ok, row, j0, ti.g, a2, beta, prob, lane);
+      }
+      if (!ok) break;
       if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
-      if (!chunk_ok) continue;
-      dglu_row_chunk<ACT>(p, r, cv, row_ok, row, j0, ti.g, a2, beta, prob, lane);
     }
   }
 
