@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstring>
 #include <mutex>
 
 #include "hq_internal.h"
@@ -69,9 +70,47 @@ int num_sms() {
   return g_sms[dev];
 }
 
+// A tensor map depends only on its encoding arguments (not on the memory's
+// contents), so recently encoded maps are kept and reused when every argument
+// matches: encoding through the driver costs host time on every small call.
+namespace {
+struct MapKey {
+  int dtype, rank, swizzle, dev;
+  void* base;
+  uint64_t dims[5], strides[4];
+  uint32_t box[5];
+};
+constexpr int kMapCache = 32;
+MapKey g_map_keys[kMapCache];
+CUtensorMap g_maps[kMapCache];
+int g_map_used = 0, g_map_next = 0;
+std::mutex g_map_mu;
+}  // namespace
+
 int encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, void* base,
                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
                       CUtensorMapSwizzle swizzle) {
+  if (rank < 1 || rank > 5) return HQ_ERR_INVALID;
+  MapKey key;
+  memset(&key, 0, sizeof(key));
+  key.dtype = static_cast<int>(dtype);
+  key.rank = rank;
+  key.swizzle = static_cast<int>(swizzle);
+  key.dev = current_device();
+  key.base = base;
+  for (int i = 0; i < rank; ++i) {
+    key.dims[i] = dims[i];
+    key.box[i] = box[i];
+    if (i > 0) key.strides[i - 1] = strides_bytes[i - 1];
+  }
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    for (int i = 0; i < g_map_used; ++i)
+      if (memcmp(&g_map_keys[i], &key, sizeof(key)) == 0) {
+        *map = g_maps[i];
+        return HQ_OK;
+      }
+  }
   {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_encode) {
@@ -97,7 +136,15 @@ int encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, voi
   CUresult r = g_encode(map, dtype, rank, base, gdim, gstride, bdim, estride,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? HQ_OK : HQ_ERR_CUDA;
+  if (r != CUDA_SUCCESS) return HQ_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    g_map_keys[g_map_next] = key;
+    g_maps[g_map_next] = *map;
+    g_map_next = (g_map_next + 1) % kMapCache;
+    if (g_map_used < kMapCache) ++g_map_used;
+  }
+  return HQ_OK;
 }
 
 // Waits on an mbarrier that nothing arrives on; the bounded wait expires.

@@ -1578,8 +1578,7 @@ int run_bs(const void* a, const void* b, const GemmParams& p0, int sm_count, boo
     }
   }
   auto kern = bs_gemm_kernel<MODE, BN, STAGES, ACC, TABLE, EPI>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
-      cudaSuccess)
+  if (set_smem_once<bs_gemm_kernel<MODE, BN, STAGES, ACC, TABLE, EPI>>(C::SMEM_BYTES) != HQ_OK)
     return HQ_ERR_CUDA;
   const int sms = num_sms();
   if (sms <= 0) return HQ_ERR_CUDA;
@@ -1624,8 +1623,7 @@ int run_bs_2sm(const void* a, const void* b, const GemmParams& p, int sm_count, 
     if (rc != HQ_OK) return rc;
   }
   auto kern = bs_gemm_2sm_kernel<MODE, STAGES, EPI, BN>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
-      cudaSuccess)
+  if (set_smem_once<bs_gemm_2sm_kernel<MODE, STAGES, EPI, BN>>(C::SMEM_BYTES) != HQ_OK)
     return HQ_ERR_CUDA;
   const int sms = num_sms();
   if (sms < 2) return HQ_ERR_CUDA;
@@ -1669,6 +1667,11 @@ int run_gemm(hq_mode mode, const void* a, const void* b, const GemmParams& p, in
   const bool pairable = !p.b_maps && (p.gs.sched == kDense || p.gs.sched == kContig ||
                                       (p.gs.sched == kMasked && p.gs.max_m % 256 == 0));
   const int pw = pair_width();
+  // a dense problem with fewer pair tiles than clusters keeps more SMs busy
+  // with single-SM 128 x 128 tiles (unless a pair width is forced)
+  if (bn == 0 && pw == 0 && p.gs.sched == kDense &&
+      ((p.gs.a_rows + 255) / 256) * ((p.n + 255) / 256) < num_sms() / 2)
+    bn = 128;
   const bool wide = p.n % 384 == 0 && (pw == 384 || (pw == 0 && p.gs.sched == kDense));
   if (bn == 0 && pairable && use_2sm() && wide) {
     if (mode == HQ_MXFP8) return run_bs_2sm<HQ_MXFP8, 4, kEpiGemm, 384>(a, b, p, sm_count, pdl, st);

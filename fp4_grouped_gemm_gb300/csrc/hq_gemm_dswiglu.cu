@@ -503,9 +503,7 @@ int run_dglu(const hq_bf16* a, const hq_bf16* b, const int64_t* b_ptrs, const hq
   }
   const int sms = num_sms();
   if (sms <= 0) return HQ_ERR_CUDA;
-  if (cudaFuncSetAttribute(dglu_kernel<ACT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes) != cudaSuccess)
-    return HQ_ERR_CUDA;
+  if (set_smem_once<dglu_kernel<ACT>>(kSmemBytes) != HQ_OK) return HQ_ERR_CUDA;
   const int64_t tiles_bound = ((m + kBM - 1) / kBM) * ((n + kBN - 1) / kBN);
   int64_t grid = sm_count > 0 ? sm_count : sms;
   if (grid > sms) grid = sms;

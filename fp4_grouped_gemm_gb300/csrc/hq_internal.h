@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "../../include/hq.h"
@@ -52,6 +53,22 @@ inline size_t discrete_maps_bytes(int L) {
 // HQ_ERR_CUDA.
 int build_weight_maps(const CUtensorMap& tmpl, const int64_t* b_ptrs, const int64_t* sfb_ptrs,
                       CUtensorMap* maps, int32_t* ok, int L, cudaStream_t st);
+
+// Raises the dynamic shared-memory limit of kernel Kern to `bytes` once per
+// device (the attribute persists, and setting it on every launch costs host
+// time on the small problems).  Returns HQ_OK or HQ_ERR_CUDA.
+template <auto Kern>
+int set_smem_once(int bytes) {
+  static std::atomic<uint64_t> done{0};  // one bit per device 0..63
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return HQ_ERR_CUDA;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return HQ_OK;
+  if (cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return HQ_ERR_CUDA;
+  done.fetch_or(bit, std::memory_order_release);
+  return HQ_OK;
+}
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

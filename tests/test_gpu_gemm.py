@@ -99,7 +99,7 @@ def test_dense_256_column_tiles(cuda_dev, mode, m, n, k, two_sm):
     tiles) and the single-SM 128 x 256 kernel, ragged M and K."""
     if mode != "nvfp4" and k % 128:
         pytest.skip("MXFP8 and MXFP4 need k % 128 == 0")
-    hq.set_gemm_2sm(two_sm)
+    hq.set_gemm_2sm(256 if two_sm else 0)  # forced: these sizes would otherwise take 128 x 128 tiles
     dense_case(m, n, k, mode, 0, alpha={"nvfp4": 0.5, "mxfp8": 1.25, "mxfp4": None}[mode],
                bias=(mode == "mxfp8"), seed=m + k + {"nvfp4": 7, "mxfp8": 0, "mxfp4": 3}[mode],
                g_a=2.0 if mode == "nvfp4" else None, g_b=64.0 if mode == "nvfp4" else None)
@@ -282,7 +282,7 @@ def test_dense_wide_pair_tiles(cuda_dev, mode, m, n, k):
     step, two TMEM scale slots for NVFP4), ragged M and K."""
     if mode != "nvfp4" and k % 128:
         pytest.skip("MXFP8 and MXFP4 need k % 128 == 0")
-    hq.set_gemm_2sm(1)
+    hq.set_gemm_2sm(384)  # forced: small problems otherwise take 128 x 128 tiles
     dense_case(m, n, k, mode, 0, alpha={"nvfp4": 0.5, "mxfp8": 1.25, "mxfp4": None}[mode],
                bias=(mode == "mxfp8"), seed=m + n + k, g_a=2.0 if mode == "nvfp4" else None,
                g_b=64.0 if mode == "nvfp4" else None)
@@ -309,6 +309,13 @@ def test_grouped_masked_pairs(cuda_dev, mode, two_sm):
     alpha = None if mode == "mxfp4" else [0.5 + 0.125 * e for e in range(len(masked))]
     status = masked_case(masked, 512, 512, 384 if mode == "mxfp8" else 512, mode, 0, alpha=alpha, seed=13)
     assert status == 0
+
+
+def test_dense_small_problem_takes_single_sm_tiles(cuda_dev):
+    """Automatic choice for a problem smaller than one wave of pair tiles
+    (128 x 128 single-SM tiles): same results as forcing that tile."""
+    dense_case(256, 256, 256, "mxfp8", 0, alpha=1.25, bias=True, seed=91)
+    dense_case(640, 768, 512, "nvfp4", 0, alpha=0.5, seed=92, g_a=2.0, g_b=64.0)
 
 
 def test_grouped_masked_pairs_clamp_and_flag(cuda_dev):
