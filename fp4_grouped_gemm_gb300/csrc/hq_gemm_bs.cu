@@ -1,23 +1,33 @@
-// hq_gemm_bs.cu -- block-scaled GEMMs (MXFP8 and NVFP4) on 5th-generation
-// tensor cores: out = alpha_g * (A . B_g^T) + bias_g, BF16 output.
+// hq_gemm_bs.cu -- block-scaled GEMMs (MXFP8, MXFP4, NVFP4) on 5th-generation
+// tensor cores: out = alpha_g * (A . B_g^T) + bias_g, BF16 output, and the
+// epilogues built on the same main loop.
 //
-// One persistent kernel serves the dense, grouped-contiguous and
-// grouped-masked problems (HALOps "GEMM" API dense_gemm / group_masked_gemm,
-// cuDNN frontend "Grouped GEMM + dGLU (SM100)" Step 1).  Per CTA:
-//   warp 0      TMA producer: A and B tiles (128-byte swizzled, K-major) and
-//               the matching 512-byte SfAtom scale atoms into a ring of
-//               shared-memory stages, completion tracked by mbarriers;
-//   warp 1      MMA issuer: copies each stage's scale atoms shared -> TMEM
-//               (tcgen05.cp 32x128b.warpx4) and issues block-scaled
-//               tcgen05.mma into a TMEM accumulator; owns the TMEM allocation;
-//   warps 2..5  epilogue: TMEM -> registers (tcgen05.ld), alpha/bias, BF16
-//               round-to-nearest-even, staged through shared memory and
-//               written as coalesced 16-byte row segments; rows outside the
-//               group's valid range are never written.
-// Tiles are 128 rows x BN columns; the tile sequence (n fastest inside each
-// 128-row block, so the CTAs of a wave share A rows and walk one expert's
-// weights together) is decoded identically by every role from device-resident
-// group information (padded_offsets or masked_m), validated on the device.
+// Two persistent kernels serve the dense, grouped-contiguous (padded_offsets),
+// per-row expert-id and grouped-masked problems (HALOps "GEMM" API
+// dense_gemm / group_contiguous_gemm / group_masked_gemm; cuDNN frontend
+// "Grouped GEMM + dGLU (SM100)" Step 1):
+//   bs_gemm_kernel      one CTA per SM, tiles of 128 rows x BN (128 or 256)
+//                       columns, one or two TMEM accumulators; also carries
+//                       the dSwiGLU / dGeGLU epilogues (block-scaled dGLU
+//                       backward) and the fused up-proj SwiGLU + requant
+//                       epilogue, and discrete (per-expert pointer) weights;
+//   bs_gemm_2sm_kernel  two-CTA clusters, cta_group::2 MMAs of M = 256 over
+//                       tiles of 256 x 256 (or 256 x 384) columns, for the
+//                       dense, contiguous, masked and fused up-proj problems.
+// Warp roles in both (448 threads):
+//   warp 0       TMA producer: A and B tiles (128-byte swizzled, K-major) and
+//                bulk copies of the 512-byte SfAtom scale atoms into a ring of
+//                shared-memory stages, completion tracked by mbarriers;
+//   warp 1       MMA issuer (the even CTA's in a pair); owns TMEM;
+//   warps 2..9   epilogue: TMEM -> registers (tcgen05.ld), alpha / bias,
+//                BF16 round-to-nearest-even (or the fused epilogue's math),
+//                coalesced stores; rows outside the valid range never written;
+//   warps 10..13 scale staging: the stage's scale atoms shared -> TMEM
+//                (tcgen05.st into each TMEM lane quarter), then a "ready"
+//                signal to the MMA issuer.
+// Every role decodes the same tile sequence (n fastest inside each row block)
+// from device-resident group information (padded_offsets, masked_m or the
+// per-row segment list), validated on the device; every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
