@@ -1,6 +1,7 @@
-// hq_gemm_dswiglu.cu -- BF16 grouped GEMM fused with the dSwiGLU backward
-// epilogue (cuDNN frontend "Grouped GEMM + dGLU (SM100)", BF16 contract,
-// act_func = "dswiglu", dense B).
+// hq_gemm_dswiglu.cu -- BF16 grouped GEMM fused with the dSwiGLU or clamped
+// dGeGLU backward epilogue (cuDNN frontend "Grouped GEMM + dGLU (SM100)", BF16
+// contract, act_func = "dswiglu" / "dgeglu"; B stacked [L, n, k] or one
+// pointer per expert).  Shown for dSwiGLU:
 //
 //   R_g = alpha_g^2 A_g B_g^T  (tcgen05.mma kind::f16, BF16 x BF16 -> FP32 in TMEM)
 //   X_g = beta_g C_g, split into alternating 32-column gate / input blocks
