@@ -18,7 +18,7 @@ import synth
 from oracle import gemm as ogemm
 from oracle import quant as oquant
 
-from gpu_util import (assert_gemm_close, assert_rows_untouched, bf16_rows, np_f32,
+from gpu_util import (assert_gemm_close, assert_rows_untouched, bf16_rows, bits16, np_f32,
                       oracle_quant_to_device, sentinel_bf16, stacked_weights_to_device)
 
 pytestmark = pytest.mark.gpu
@@ -423,3 +423,75 @@ def test_full_moe_masked_nvfp4_sampled_and_untouched(cuda_dev):
         rr, mg = ogemm.dense(a_deq[i:i + 1], oquant.dequantize(qb_np, sb_np, "nvfp4"), alpha=[alpha[e]])
         ref[i], mag[i] = rr[0], mg[0]
     assert_gemm_close(got, ref, mag, "moe masked full size")
+
+
+# ----------------------------------------------------------------------------- maximum group count
+
+
+def _expert_deq(qb_np, sfb_np, e, n, k, mode):
+    S = k // 32
+    per = -(-n // 128) * 128 * S
+    sf = oquant.from_sfatom(sfb_np[e * per:(e + 1) * per], n, S)
+    return oquant.dequantize(qb_np[e], sf, mode)
+
+
+def test_max_groups_contig_and_masked(cuda_dev):
+    """The largest group count (1024 experts) on 256-row pairs: contiguous
+    groups of 0, 128 or 256 rows, and masked experts with 0..256 valid rows;
+    sampled rows against the oracle (operands quantised by the GPU quantiser,
+    which is bit-exact against the oracle elsewhere), untouched rows checked
+    in full."""
+    L, n, k, mode = 1024, 256, 128, "mxfp8"
+    rng = np.random.default_rng(5)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    w = (torch.randn(L * n, k, generator=g, device="cuda") * 0.05).to(torch.bfloat16)
+    qb, sfb = hq.hq_quant(w, mode)
+    qb_np, sfb_np = qb.view(L, n, k).cpu().numpy(), sfb.cpu().numpy()
+
+    # contiguous: group e holds counts[e] rows; 128 trailing rows stay untouched
+    counts = rng.choice([0, 128, 256], size=L)
+    offsets = np.cumsum(counts).astype(np.int32)
+    m = int(offsets[-1]) + 128
+    a = torch.randn(m, k, generator=g, device="cuda").to(torch.bfloat16)
+    qa, sfa = hq.hq_quant(a, mode)
+    out = sentinel_bf16((m, n))
+    hq.get_device_status(clear=True)
+    hq.hq_gemm_grouped_contig(qa, sfa, qb.view(L, n, k), sfb, torch.from_numpy(offsets).cuda(), m, n, k, mode,
+                              out=out)
+    torch.cuda.synchronize()
+    assert hq.get_device_status(clear=True)[0] == 0
+    grp = ogemm.group_of_rows_contig(offsets, m)
+    rows = np.sort(rng.choice(int(offsets[-1]), 1536, replace=False))
+    sfa_plain = oquant.from_sfatom(sfa.cpu().numpy(), m, k // 32)
+    a_deq = oquant.dequantize(qa.cpu().numpy()[rows], sfa_plain[rows], mode)
+    ref = np.zeros((len(rows), n))
+    mag = np.zeros_like(ref)
+    for e in np.unique(grp[rows]):
+        sel = grp[rows] == e
+        ref[sel], mag[sel] = ogemm.dense(a_deq[sel], _expert_deq(qb_np, sfb_np, e, n, k, mode))
+    assert_gemm_close(out[torch.from_numpy(rows).cuda()], ref, mag, "contig, 1024 groups")
+    assert (bits16(out[int(offsets[-1]):]) == 0xAAAA).all()
+
+    # masked: expert e's rows at e * 256, masked_m[e] in 0..256 of them valid
+    max_m = 256
+    masked = rng.integers(0, max_m + 1, size=L).astype(np.int32)
+    am = torch.randn(L * max_m, k, generator=g, device="cuda").to(torch.bfloat16)
+    qam, sfam = hq.hq_quant(am, mode)
+    outm = sentinel_bf16((L * max_m, n))
+    hq.hq_gemm_grouped_masked(qam, sfam, qb.view(L, n, k), sfb, torch.from_numpy(masked).cuda(), max_m, n, k,
+                              mode, out=outm)
+    torch.cuda.synchronize()
+    assert hq.get_device_status(clear=True)[0] == 0
+    local = np.arange(L * max_m) % max_m
+    written = local < np.repeat(masked, max_m)
+    wr = np.nonzero(written)[0]
+    rows = np.sort(rng.choice(wr, 1536, replace=False))
+    sfm_plain = oquant.from_sfatom(sfam.cpu().numpy(), L * max_m, k // 32)
+    a_deq = oquant.dequantize(qam.cpu().numpy()[rows], sfm_plain[rows], mode)
+    ref = np.zeros((len(rows), n))
+    mag = np.zeros_like(ref)
+    for e in np.unique(rows // max_m):
+        sel = rows // max_m == e
+        ref[sel], mag[sel] = ogemm.dense(a_deq[sel], _expert_deq(qb_np, sfb_np, e, n, k, mode))
+    assert_gemm_close(outm[torch.from_numpy(rows).cuda()], ref, mag, "masked, 1024 experts")
+    assert_rows_untouched(outm, written, "masked, 1024 experts")
