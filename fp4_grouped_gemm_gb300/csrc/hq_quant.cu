@@ -29,7 +29,22 @@ namespace hq {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kGroupsPerWarpStep = 32;  // one scale group per lane
+
+// Lanes that share one scale group: the MXFP8 SwiGLU pass splits each
+// 32-value group over a lane pair (two groups in flight per lane pair: fewer
+// registers per lane and more warps resident per SM than one whole group per
+// lane, which the other passes keep).
+__host__ __device__ constexpr int lanes_per_group(int mode, bool swiglu) {
+  return swiglu && mode == HQ_MXFP8 ? 2 : 1;
+}
+// Groups a lane (or lane pair) holds in flight.
+__host__ __device__ constexpr int groups_per_lane(int mode, bool swiglu) {
+  return mode == HQ_NVFP4 ? (swiglu ? 2 : 4) : (swiglu ? 2 : 1);
+}
+// Scale groups of one row a warp takes per item.
+__host__ __device__ constexpr int groups_per_item(int mode, bool swiglu) {
+  return 32 / lanes_per_group(mode, swiglu) * groups_per_lane(mode, swiglu);
+}
 
 struct QuantParams {
   const uint16_t* in;        // BF16 (or FP16) rows (quant: [rows, k]; swiglu: [rows, 2k])
@@ -110,15 +125,18 @@ __device__ __forceinline__ uint32_t cvt_e4m3x4(float x0, float x1, float x2, flo
   return w;
 }
 
-// One lane quantises one whole scale group of GS values x[0..GS).
-// MXFP8 writes GS E4M3 bytes to qw[0..GS/4); NVFP4 and MXFP4 write GS/2 packed
-// bytes to qw[0..GS/8).
-template <int MODE, int GS>
-__device__ __forceinline__ uint32_t encode_group(const float (&x)[GS], float g,
-                                                 const float* r_table, uint32_t (&qw)[GS / 4]) {
+// LPG lanes quantise one scale group; each holds GL = group / LPG of its
+// values x[0..GL) (a lane pair: the even lane the first half).  MXFP8 writes
+// GL E4M3 bytes to qw[0..GL/4); NVFP4 and MXFP4 write GL/2 packed bytes to
+// qw[0..GL/8).  All 32 lanes must call it (the pair's amax is a shuffle).
+template <int MODE, int GL, int LPG = 1>
+__device__ __forceinline__ uint32_t encode_group(const float (&x)[GL], float g,
+                                                 const float* r_table, uint32_t (&qw)[GL / 4]) {
+  constexpr int GS = GL;  // values this lane encodes
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < GS; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  if (LPG == 2) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
   if (MODE == HQ_MXFP8) {
     const float s = __fmul_rn(__fmul_rn(g, amax), 1.0f / 448.0f);
     const uint32_t byte = ue8m0_ceil(s);
@@ -164,8 +182,12 @@ __device__ __forceinline__ uint32_t encode_group(const float (&x)[GS], float g,
 template <int MODE, bool SWIGLU, bool F16IN = false>
 __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
   constexpr int GS = MODE == HQ_NVFP4 ? 16 : 32;
-  constexpr int NV = GS / 8;          // 16-byte loads per operand and group
-  constexpr int U = MODE == HQ_NVFP4 ? (SWIGLU ? 2 : 4) : 1;  // groups a lane holds in flight
+  constexpr int LPG = lanes_per_group(MODE, SWIGLU);
+  constexpr int GL = GS / LPG;        // values per lane and group
+  constexpr int NV = GL / 8;          // 16-byte loads per operand, group and lane
+  constexpr int U = groups_per_lane(MODE, SWIGLU);  // groups a lane holds in flight
+  constexpr int GPI = groups_per_item(MODE, SWIGLU);
+  constexpr int GPU_ = GPI / U;       // groups per warp and u
   __shared__ float r_table[128];
   pdl_wait();  // the global scale and the input may come from the preceding kernel
   const float g = (MODE == HQ_NVFP4 && p.global_scale) ? __ldg(p.global_scale) : 1.0f;
@@ -180,9 +202,10 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
-  // an item is 32 * U consecutive groups of one row; lane l owns groups l, l+32, ...
+  // an item is GPI consecutive groups of one row; lane l works on groups
+  // l / LPG, l / LPG + GPI / U, ... (part l % LPG of each)
   const int64_t groups_row = p.S_real;
-  const int64_t chunks = (groups_row + 32 * U - 1) / (32 * U);
+  const int64_t chunks = (groups_row + GPI - 1) / GPI;
   const int64_t items = p.rows * chunks;
   const bool small = items < (1ll << 31);
 
@@ -207,14 +230,14 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
   uint4 v0[U][NV], v1[U][NV];
   auto load_item = [&](int64_t item) {
     const int64_t row = row_of(item);
-    const int64_t s0 = (item - row * chunks) * (32 * U);
+    const int64_t s0 = (item - row * chunks) * GPI;
     const bool rv = row_valid(row);
     const uint16_t* src_row = p.in + row * p.in_stride;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int64_t s = s0 + u * 32 + lane;
+      const int64_t s = s0 + u * GPU_ + lane / LPG;
       const bool ok = rv && s < groups_row;
-      const uint4* src = reinterpret_cast<const uint4*>(src_row + s * GS);
+      const uint4* src = reinterpret_cast<const uint4*>(src_row + s * GS + (lane % LPG) * GL);
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
         v0[u][i] = ok ? __ldcs(src + i) : make_uint4(0, 0, 0, 0);
@@ -234,13 +257,13 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
       }
     if (item + nwarps < items) load_item(item + nwarps);
     const int64_t row = row_of(item);
-    const int64_t s0 = (item - row * chunks) * (32 * U);
+    const int64_t s0 = (item - row * chunks) * GPI;
     if (!row_valid(row)) continue;  // warp-uniform
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int64_t s = s0 + u * 32 + lane;
-      if (s0 + u * 32 >= groups_row) break;  // warp-uniform
-      float x[GS];
+      const int64_t s = s0 + u * GPU_ + lane / LPG;
+      if (s0 + u * GPU_ >= groups_row) break;  // warp-uniform
+      float x[GL];
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
         float a[8];
@@ -262,23 +285,26 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
           for (int j = 0; j < 8; ++j) x[8 * i + j] = a[j];
         }
       }
-      uint32_t qw[GS / 4];
-      const uint32_t byte = encode_group<MODE, GS>(x, g, r_table, qw);
-      // four consecutive groups (lanes 4j..4j+3) share one 32-bit scale word
-      const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, byte, 1);
-      const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, byte, 2);
-      const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, byte, 3);
+      uint32_t qw[GL / 4];
+      const uint32_t byte = encode_group<MODE, GL, LPG>(x, g, r_table, qw);
+      // four consecutive groups (lane groups 4j..4j+3) share one 32-bit scale word
+      const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, byte, LPG);
+      const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, byte, 2 * LPG);
+      const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, byte, 3 * LPG);
       if (s >= groups_row) continue;
+      const int64_t e0 = row * p.k + s * GS + (lane % LPG) * GL;  // first element of this lane
       if (MODE == HQ_MXFP8) {
-        uint4* dst = reinterpret_cast<uint4*>(p.q + row * p.k + s * GS);
-        dst[0] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-        dst[1] = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+        uint4* dst = reinterpret_cast<uint4*>(p.q + e0);
+#pragma unroll
+        for (int i = 0; i < GL / 16; ++i) dst[i] = make_uint4(qw[4 * i], qw[4 * i + 1], qw[4 * i + 2], qw[4 * i + 3]);
       } else if (MODE == HQ_MXFP4) {
-        *reinterpret_cast<uint4*>(p.q + (row * p.k + s * GS) / 2) = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+        *reinterpret_cast<uint4*>(p.q + e0 / 2) = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+      } else if (GL == 16) {
+        *reinterpret_cast<uint2*>(p.q + e0 / 2) = make_uint2(qw[0], qw[1]);
       } else {
-        *reinterpret_cast<uint2*>(p.q + (row * p.k + s * GS) / 2) = make_uint2(qw[0], qw[1]);
+        *reinterpret_cast<uint32_t*>(p.q + e0 / 2) = qw[0];
       }
-      if ((lane & 3) == 0) {
+      if ((lane & (4 * LPG - 1)) == 0) {
         const uint32_t word = byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
         *reinterpret_cast<uint32_t*>(p.sf + sf_offset(row, s, p.S, p.swizzle)) = word;
       }
@@ -322,7 +348,8 @@ int launch_quant(const QuantParams& p, cudaStream_t st, bool pdl) {
                                                     kThreads, 0) != cudaSuccess)
     return HQ_ERR_CUDA;
   if (per_sm < 1) per_sm = 1;
-  const int64_t warps_needed = p.rows * ((p.S_real + kGroupsPerWarpStep - 1) / kGroupsPerWarpStep) + 1;
+  constexpr int64_t kItem = groups_per_item(MODE, SWIGLU);
+  const int64_t warps_needed = p.rows * ((p.S_real + kItem - 1) / kItem);
   int64_t blocks = (warps_needed + (kThreads / 32) - 1) / (kThreads / 32);
   const int64_t cap = static_cast<int64_t>(sms) * per_sm;
   if (blocks > cap) blocks = cap;
