@@ -14,6 +14,7 @@ import pytest
 import torch
 
 import fp4_grouped_gemm_gb300 as hq
+import synth
 from oracle import formats, glu
 from oracle import quant as oquant
 
@@ -144,3 +145,57 @@ def test_dglu_bs_column_quantised_output(cuda_dev, mode, act, norm):
     assert not bad.any(), f"{int(bad.sum())} bad D_col values"
     assert (d_col.cpu().numpy()[rows_w:] == 0x5A).all()
     check_common(ref, dprob, dbias)
+
+
+def test_dswiglu_bs_fp8_out_full_size_sampled(cuda_dev):
+    """The dSwiGLU backward workload (L=16, M=32768, N=1408, K=2048) with
+    MXFP8 operands and FP8 D_row + SFD_row, as timed; sampled rows against the
+    oracle (their groups' R from the dequantised operands), dprob on the same
+    rows, rows past the last group untouched."""
+    cfg = synth.dswiglu_bwd(device="cuda")
+    m, n, k, L = cfg["m"], cfg["n"], cfg["k"], cfg["L"]
+    dev = torch.device("cuda")
+    qa, sfa = hq.hq_quant(cfg["a"], "mxfp8")
+    qb, sfb = hq.hq_quant(cfg["b"].view(L * n, k), "mxfp8")
+    off = torch.from_numpy(cfg["padded_offsets"]).to(dev)
+    dprob = torch.zeros(m, dtype=torch.float32, device=dev)
+    dbias = torch.zeros(L, 2 * n, dtype=torch.bfloat16, device=dev)
+    d8 = torch.full((m, 2 * n), 0x5A, dtype=torch.uint8, device=dev)
+    sfd = torch.empty(hq.sf_bytes(m, 2 * n, "mxfp8"), dtype=torch.uint8, device=dev)
+    hq.hq_gemm_dglu_bs(qa, sfa, qb.view(L, n, k), sfb, cfg["c"], off, cfg["alpha"], cfg["prob"], dprob, k,
+                       "mxfp8", beta=cfg["beta"], dbias=dbias, d_row=d8, fp8_out=True, sfd_row=sfd)
+    torch.cuda.synchronize()
+    valid = int(cfg["padded_offsets"][-1])
+    rows = np.sort(np.random.default_rng(31).choice(valid, 32, replace=False))
+    ri = torch.from_numpy(rows).to(dev)
+    grp = np.searchsorted(cfg["padded_offsets"], rows, side="right")
+    qa_np, sa_np = oquant.quantize(np_f32(cfg["a"][ri]), "mxfp8")
+    a_deq = oquant.dequantize(qa_np, sa_np, "mxfp8")
+    c_s, p_s = np_f32(cfg["c"][ri]), cfg["prob"][ri].cpu().numpy()
+    alpha, beta = cfg["alpha"].cpu().numpy(), cfg["beta"].cpu().numpy()
+    S = 2 * n // 32
+    sf_all = oquant.from_sfatom(sfd.cpu().numpy(), m, S)
+    codes_all = d8.cpu().numpy()
+    gc, ic = glu.interleave_columns(n)
+    for g in np.unique(grp):
+        sel = np.nonzero(grp == g)[0]
+        qb_np, sb_np = oquant.quantize(np_f32(cfg["b"][g]), "mxfp8")
+        b_deq = oquant.dequantize(qb_np, sb_np, "mxfp8")
+        R, magR, _ = glu.grouped_R(a_deq[sel], b_deq[None], [len(sel)], [alpha[g]])
+        D, dp, dp_mag, mult = glu.dswiglu_epilogue(R, c_s[sel], p_s[sel], np.full(len(sel), beta[g]))
+        magD = np.zeros_like(D)
+        magD[:, gc] = magR * mult[:, gc]
+        magD[:, ic] = magR * mult[:, ic]
+        sf_plain = sf_all[rows[sel]]
+        _, sf_ref = glu.quantize_rows_fp8(D.astype(np.float32))
+        diff = np.abs(sf_plain.astype(np.int64) - sf_ref.astype(np.int64))
+        assert diff.max() <= 1 and (diff == 0).mean() > 0.98, f"scale bytes, group {g}"
+        scale = np.repeat(formats.decode_ue8m0(sf_plain), 32, axis=1)
+        deq = formats.decode_e4m3(codes_all[rows[sel]]) * scale
+        tol = 2.0 ** -4 * np.abs(D) + scale * 2.0 ** -10 + 2.0 ** -8 * np.abs(D) + 2.0 ** -20 * magD
+        bad = np.abs(deq - D) > tol
+        assert not bad.any(), f"{int(bad.sum())} bad FP8 D_row values, group {g}"
+        got_p = dprob[ri[torch.from_numpy(sel).to(dev)]].cpu().numpy().astype(np.float64)
+        assert (np.abs(got_p - dp) <= 1e-3 * dp_mag + 1e-30).all(), f"dprob, group {g}"
+    if valid < m:
+        assert bool((d8[valid:] == 0x5A).all()), "rows past the last group written"

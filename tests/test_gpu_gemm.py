@@ -368,6 +368,23 @@ def test_full_dense_nvfp4_4096x12288x5120_sampled(cuda_dev):
     assert_gemm_close(got, ref, mag, "dense nvfp4 full size")
 
 
+def test_full_dense_mxfp4_4096x12288x5120_sampled(cuda_dev):
+    """MXFP4 (UE8M0 per 32, no alpha) on the headline shapes, as timed: the
+    256x384 pair tiles."""
+    cfg = synth.dense_nvfp4(device="cuda")
+    m, n, k = cfg["m"], cfg["n"], cfg["k"]
+    qa, sfa = hq.hq_quant(cfg["a"], "mxfp4")
+    qb, sfb = hq.hq_quant(cfg["b"], "mxfp4")
+    out = hq.hq_gemm_dense(qa, sfa, qb, sfb, m, n, k, "mxfp4")
+    torch.cuda.synchronize()
+    rows, cols = _sample(m, 48, 21), _sample(n, 512, 22)
+    qa_np, sa_np = oquant.quantize(np_f32(cfg["a"][torch.from_numpy(rows).cuda()]), "mxfp4")
+    qb_np, sb_np = oquant.quantize(np_f32(cfg["b"][torch.from_numpy(cols).cuda()]), "mxfp4")
+    ref, mag = ogemm.dense(oquant.dequantize(qa_np, sa_np, "mxfp4"), oquant.dequantize(qb_np, sb_np, "mxfp4"))
+    got = out[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()]
+    assert_gemm_close(got, ref, mag, "dense mxfp4 full size")
+
+
 def test_full_moe_contig_mxfp8_sampled(cuda_dev):
     cfg = synth.moe_contig(device="cuda")
     M, n, k, L = cfg["m"], cfg["n"], cfg["k"], cfg["L"]
