@@ -112,3 +112,42 @@ def test_permute_then_masked_gemm_mxfp8(cuda_dev):
     r, mag, written = ogemm.grouped_masked(a_deq, b_deq, ref["token_nums"].tolist(), cap)
     rows = np.nonzero(written)[0]
     assert_gemm_close(out[torch.from_numpy(rows).to(dev)], r[rows], mag[rows], "permute -> masked")
+
+
+def test_permute_full_size_sampled(cuda_dev):
+    """The routing workload as timed: 8192 FP8 tokens, hidden 7168, top-8 of
+    32 experts (uniform routing), direct per-32 scales, 4096 rows per expert.
+    The index map and per-expert counts are compared whole (the oracle's
+    routing does not depend on the row contents, so it runs on one byte per
+    token); sampled routed rows and their SfAtom scale bytes are compared
+    with their source token; every row past an expert's count is untouched."""
+    T, hidden, topk, E, cap = 8192, 7168, 8, 32, 4096
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev).manual_seed(6)
+    x = torch.randint(0, 256, (T, hidden), generator=g, device=dev, dtype=torch.uint8)
+    sc = torch.randint(0, 256, (T, hidden // 32), generator=g, device=dev, dtype=torch.uint8)
+    ids = torch.argsort(torch.rand(T, E, generator=g, device=dev), dim=1)[:, :topk].contiguous()
+    rows = E * cap
+    px = torch.full((rows, hidden), 0x5A, dtype=torch.uint8, device=dev)
+    osf = torch.full((rows * hidden // 32,), 0xA5, dtype=torch.uint8, device=dev)
+    hq.get_device_status(clear=True)
+    _, _, imap, tn = hq.hq_prefill_permute(x.view(torch.float8_e4m3fn), sc, ids, E, cap,
+                                           permute_x=px.view(torch.float8_e4m3fn), out_scale=osf)
+    torch.cuda.synchronize()
+    status, _ = hq.get_device_status(clear=True)
+    assert not status & hq.HQ_STATUS_ROUTING_DROPPED
+    ids_np = ids.cpu().numpy()
+    ref = operm.prefill_permute(np.zeros((T, 128), np.uint8), np.zeros((T, 4), np.uint8), ids_np, E, cap, "direct")
+    assert np.array_equal(tn.cpu().numpy(), ref["token_nums"])
+    imap_np = imap.cpu().numpy()
+    assert np.array_equal(imap_np, ref["indice_map"])
+    unw = torch.from_numpy(~ref["written"]).to(dev)
+    assert bool((px[unw] == 0x5A).all()), "rows past token_nums were written"
+    rng = np.random.default_rng(7)
+    S = hidden // 32
+    sf_got = osf.cpu().numpy()
+    sc_np = sc.cpu().numpy()
+    for t, k in zip(rng.integers(0, T, 64), rng.integers(0, topk, 64)):
+        row = int(ids_np[t, k]) * cap + int(imap_np[t, k])
+        assert torch.equal(px[row], x[t]), f"token {t} slot {k}"
+        assert np.array_equal(sf_got[oquant.sfatom_offset(np.full(S, row), np.arange(S), S)], sc_np[t])
