@@ -32,8 +32,8 @@ Readings (also listed in the design notes):
       64*(j//32) + j%32, input column gate + 32).  D_row at a column is the
       gradient with respect to X at that same column (beta not re-applied).
   D2  dbias sums the float values of D_row before their BF16 rounding.
-  D3  dGeGLU masks multiply by 0/1 (the value-bearing "filter" of the first
-      formula listing is read as the mask of the second).
+  D3  dGeGLU masks multiply by 0/1 (the value-bearing "filter" in the first
+      statement of the formulas is read as the mask of the second).
   Q1  Block-scaled contract, Step 3 (FP8 D_row): per row and 32 consecutive
       D_row columns, s = fp32(fp32(norm_const * amax) * fp32(1/448)),
       SFD_row = UE8M0 s rounded up to a power of two (R2 of oracle.quant),
