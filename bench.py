@@ -458,7 +458,18 @@ class Extras:
         g.replay()
         torch.cuda.synchronize()
         tg = time_kernel(lambda: g.replay(), 10) / 100
+        # the same graph with programmatic dependent launch: each call's
+        # prologue (barriers, TMEM, tensor-map prefetch) overlaps the previous
+        # call's tail, its first read waits for that call to finish
+        gp = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gp):
+            for _ in range(100):
+                hq.hq_gemm_dense(qa, sfa, qb, sfb, 256, 256, 256, "mxfp8", out=out1, use_pdl=True)
+        gp.replay()
+        torch.cuda.synchronize()
+        tgp = time_kernel(lambda: gp.replay(), 10) / 100
         return {"dense_mxfp8_256": {"us_per_call": t * 1e6, "us_per_call_graph": tg * 1e6,
+                                    "us_per_call_graph_pdl": tgp * 1e6,
                                     "tflops": 2 * 256 ** 3 / t / 1e12}}
 
     def quant_nvfp4(self):

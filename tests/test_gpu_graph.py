@@ -121,3 +121,45 @@ def test_grouped_discrete_and_dswiglu_replay_bit_identically(cuda_dev):
     b0, b1 = ref_dbias.float(), dbias.float()
     assert ((b1 - b0).abs() <= 2 ** -7 * b0.abs() + 1e-5 * b0.abs().max()).all()
     assert np.isfinite(out.float().cpu().numpy()).all()
+
+
+def test_programmatic_dependent_launch_in_a_graph(cuda_dev):
+    """GEMMs launched with programmatic dependent launch, eagerly and as a
+    captured chain that rewrites its own input between calls, give the bytes
+    of plain launches: each call reads its operands only after the previous
+    kernel in the stream has finished."""
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev).manual_seed(5)
+    m = n = k = 256
+    a = torch.randn(m, k, generator=gen, device=dev).to(torch.bfloat16)
+    b = torch.randn(n, k, generator=gen, device=dev).to(torch.bfloat16)
+    qa, sfa = hq.hq_quant(a, "mxfp8")
+    qb, sfb = hq.hq_quant(b, "mxfp8")
+    ref = hq.hq_gemm_dense(qa, sfa, qb, sfb, m, n, k, "mxfp8")
+    out = torch.zeros(m, n, dtype=torch.bfloat16, device=dev)
+    hq.hq_gemm_dense(qa, sfa, qb, sfb, m, n, k, "mxfp8", out=out, use_pdl=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+    # chain: quantise (PDL) -> GEMM (PDL) -> quantise the GEMM's output as the
+    # next A (PDL) -> GEMM (PDL); the second GEMM must see the first's output
+    qa2 = torch.empty_like(qa)
+    sfa2 = torch.empty_like(sfa)
+    out2 = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+
+    def chain():
+        hq.hq_quant(a, "mxfp8", q_out=qa, sf_out=sfa, use_pdl=True)
+        hq.hq_gemm_dense(qa, sfa, qb, sfb, m, n, k, "mxfp8", out=out, use_pdl=True)
+        hq.hq_quant(out, "mxfp8", q_out=qa2, sf_out=sfa2, use_pdl=True)
+        hq.hq_gemm_dense(qa2, sfa2, qb, sfb, m, n, k, "mxfp8", out=out2, use_pdl=True)
+
+    qa_r, sfa_r = hq.hq_quant(ref, "mxfp8")
+    ref2 = hq.hq_gemm_dense(qa_r, sfa_r, qb, sfb, m, n, k, "mxfp8")
+    g = _capture(chain)
+    out.zero_()
+    out2.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert torch.equal(out2.view(torch.int16), ref2.view(torch.int16))
