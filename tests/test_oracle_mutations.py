@@ -1,0 +1,169 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case plants one mistake in the oracle (on the CPU, for the duration of
+the case, by replacing a module attribute), runs the pins that guard that
+part of it, and requires at least one of them to fail; the same pins pass on
+the unmodified oracle.  The mistakes are the kinds a restatement of the pages
+is prone to: a wrong rounding rule, a swapped nibble or index, a wrong
+constant, a dropped factor, an off-by-one count, a transposed interleave.
+"""
+
+import functools
+
+import numpy as np
+import pytest
+
+import test_golden as tg
+import test_oracle_formats as tfm
+import test_oracle_gemm as tgm
+import test_oracle_glu as tgl
+import test_oracle_quant as tq
+from oracle import formats, gemm, glu, quant
+
+
+def expand(fn):
+    """The calls a (possibly parametrised) pin test makes under pytest."""
+    marks = [m for m in getattr(fn, "pytestmark", []) if m.name == "parametrize"]
+    if not marks:
+        return [functools.partial(fn)]
+    calls = [{}]
+    for m in marks:
+        names = [n.strip() for n in m.args[0].split(",")] if isinstance(m.args[0], str) else list(m.args[0])
+        nxt = []
+        for kw in calls:
+            for vals in m.args[1]:
+                vals = vals.values if hasattr(vals, "values") else vals
+                vals = vals if len(names) > 1 else (vals,)
+                nxt.append({**kw, **dict(zip(names, vals))})
+        calls = nxt
+    return [functools.partial(fn, **kw) for kw in calls]
+
+
+def failures(pins):
+    n = 0
+    for pin in pins:
+        for call in expand(pin):
+            try:
+                call()
+            except AssertionError:
+                n += 1
+    return n
+
+
+# ------------------------------------------------------------------ mistakes
+
+def e2m1_ties_away(monkeypatch):
+    orig = formats.encode_e2m1
+
+    def enc(v):  # ties rounded away from zero instead of to the even code
+        v = np.asarray(v, dtype=np.float64)
+        return orig(v * (1.0 + 2.0 ** -12))
+    monkeypatch.setattr(formats, "encode_e2m1", enc)
+
+
+def nibbles_swapped(monkeypatch):
+    orig = formats.pack_e2m1
+
+    def pack(codes):
+        c = np.array(codes, dtype=np.uint8, copy=True)
+        c[..., 0::2], c[..., 1::2] = np.asarray(codes)[..., 1::2], np.asarray(codes)[..., 0::2]
+        return orig(c)
+    monkeypatch.setattr(formats, "pack_e2m1", pack)
+
+
+def mxfp8_wrong_rcp_max(monkeypatch):
+    orig = quant.scale_byte_mxfp8
+
+    def sb(amax, g=np.float32(1.0)):  # 1/512 instead of 1/448
+        return orig(np.asarray(amax, dtype=np.float32) * np.float32(448.0 / 512.0), g)
+    monkeypatch.setattr(quant, "scale_byte_mxfp8", sb)
+
+
+def nvfp4_e4m3_range(monkeypatch):
+    orig = quant.scale_byte_nvfp4
+
+    def sb(amax, g=np.float32(1.0)):  # the E4M3 range (1/448) where E2M1's (1/6) belongs
+        return orig(np.asarray(amax, dtype=np.float32) * np.float32(6.0 / 448.0), g)
+    monkeypatch.setattr(quant, "scale_byte_nvfp4", sb)
+
+
+def nvfp4_reciprocal_inverted(monkeypatch):
+    orig = quant.scale_byte_nvfp4
+
+    def sb(amax, g=np.float32(1.0)):  # x * value(scale) / g instead of x * g / value(scale)
+        sf, r = orig(amax, g)
+        with np.errstate(divide="ignore"):
+            inv = np.where(r > 0, np.float32(1.0) / np.where(r > 0, r, 1), 0).astype(np.float32)
+        return sf, inv
+    monkeypatch.setattr(quant, "scale_byte_nvfp4", sb)
+
+
+def sfatom_index_swapped(monkeypatch):
+    def off(r, s, S):  # row-in-32 and 32-row block exchanged
+        r = np.asarray(r, dtype=np.int64)
+        s = np.asarray(s, dtype=np.int64)
+        return ((r // 128) * (S // 4) + s // 4) * 512 + ((r % 128) // 32) * 16 + (r % 32) * 4 + s % 4
+    monkeypatch.setattr(quant, "sfatom_offset", off)
+
+
+def gemm_alpha_dropped(monkeypatch):
+    orig = gemm.dense
+    monkeypatch.setattr(gemm, "dense", lambda a, b, alpha=None, bias=None: orig(a, b, None, bias))
+
+
+def masked_count_off_by_one(monkeypatch):
+    orig = gemm.grouped_masked
+
+    def gm(a, b, masked_m, max_m, alpha=None, bias=None):
+        return orig(a, b, [min(int(c) + 1, max_m) if int(c) > 0 else 0 for c in masked_m], max_m, alpha, bias)
+    monkeypatch.setattr(gemm, "grouped_masked", gm)
+
+
+def interleave_input_first(monkeypatch):
+    orig = glu.interleave_columns
+
+    def il(n):
+        gc, ic = orig(n)
+        return ic, gc
+    monkeypatch.setattr(glu, "interleave_columns", il)
+
+
+def sigmoid_sign(monkeypatch):
+    monkeypatch.setattr(glu, "sigmoid", lambda z: 1.0 / (1.0 + np.exp(np.asarray(z, dtype=np.float64))))
+
+
+def geglu_alpha_wrong(monkeypatch):
+    monkeypatch.setattr(glu, "dgeglu_epilogue", functools.partial(glu.dgeglu_epilogue, geglu_alpha=1.72))
+
+
+CASES = {
+    "e2m1 ties away from zero": (e2m1_ties_away, [tfm.test_e2m1_rounding_points, tq.test_round_trip_error_bound]),
+    "fp4 nibbles swapped": (nibbles_swapped, [tfm.test_fp4_packing_even_index_low_nibble,
+                                              tg.test_fp4_nibble_order, tg.test_fp4_worked_quantiser_groups]),
+    "mxfp8 rcp_max 1/512": (mxfp8_wrong_rcp_max, [tq.test_mxfp8_amax_448_gives_unit_scale, tq.test_mxfp8_amax_1,
+                                                  tq.test_mxfp8_power_of_two_boundary]),
+    "nvfp4 scale over the E4M3 range": (nvfp4_e4m3_range, [tq.test_nvfp4_amax_6_gives_unit_scale,
+                                                           tg.test_fp4_worked_quantiser_groups]),
+    "nvfp4 reciprocal inverted": (nvfp4_reciprocal_inverted, [tq.test_nvfp4_global_scale_multiplies_scale,
+                                                              tq.test_round_trip_error_bound,
+                                                              tg.test_fp4_worked_quantiser_groups]),
+    "sfatom index swapped": (sfatom_index_swapped, [tq.test_sfatom_hand_offsets,
+                                                    tq.test_sfatom_is_a_bijection_of_512_byte_atoms]),
+    "gemm alpha dropped": (gemm_alpha_dropped, [tgm.test_dense_nvfp4_exact_brute_force,
+                                                tgm.test_closed_form_all_ones]),
+    "masked count off by one": (masked_count_off_by_one, [tgm.test_grouped_masked_rows, tg.test_masked_example_rows]),
+    "interleave input first": (interleave_input_first, [tgl.test_interleave_columns_hand,
+                                                        tgl.test_dswiglu_matches_finite_differences]),
+    "sigmoid sign flipped": (sigmoid_sign, [tgl.test_dswiglu_matches_finite_differences,
+                                            tgl.test_dswiglu_gate_zero_and_prob_zero]),
+    "geglu alpha 1.72": (geglu_alpha_wrong, [tg.test_dgeglu_constants_are_the_pages_defaults,
+                                             tgl.test_dgeglu_matches_finite_differences_away_from_clamps]),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_pins_pass_on_the_oracle_and_catch_the_planted_mistake(name, monkeypatch):
+    plant, pins = CASES[name]
+    assert failures(pins) == 0, "the pins fail on the unmodified oracle"
+    plant(monkeypatch)
+    assert failures(pins) > 0, f"no pin caught: {name}"
