@@ -4,8 +4,10 @@ Each case plants one mistake in the oracle (on the CPU, for the duration of
 the case, by replacing a module attribute), runs the pins that guard that
 part of it, and requires at least one of them to fail; the same pins pass on
 the unmodified oracle.  The mistakes are the kinds a restatement of the pages
-is prone to: a wrong rounding rule, a swapped nibble or index, a wrong
-constant, a dropped factor, an off-by-one count, a transposed interleave.
+is prone to: a wrong rounding rule, a swapped nibble, index or byte order, a
+wrong constant, a dropped or doubled factor, an off-by-one count, a
+transposed interleave, a reversed fill order, a reduction over rounded
+values.
 """
 
 import functools
@@ -17,8 +19,9 @@ import test_golden as tg
 import test_oracle_formats as tfm
 import test_oracle_gemm as tgm
 import test_oracle_glu as tgl
+import test_oracle_permute as tpm
 import test_oracle_quant as tq
-from oracle import formats, gemm, glu, quant
+from oracle import formats, gemm, glu, permute, quant
 
 
 def expand(fn):
@@ -136,6 +139,47 @@ def geglu_alpha_wrong(monkeypatch):
     monkeypatch.setattr(glu, "dgeglu_epilogue", functools.partial(glu.dgeglu_epilogue, geglu_alpha=1.72))
 
 
+def permute_tokens_reversed(monkeypatch):
+    orig = permute.prefill_permute
+
+    def pp(x, scale, topk_ids, num_experts, max_token_num, scale_mode):
+        res = orig(np.asarray(x)[::-1], np.asarray(scale)[::-1], np.asarray(topk_ids)[::-1], num_experts,
+                   max_token_num, scale_mode)
+        res["indice_map"] = res["indice_map"][::-1]
+        return res
+    monkeypatch.setattr(permute, "prefill_permute", pp)
+
+
+def broadcast_bytes_big_endian(monkeypatch):
+    def bb(scale_i32, hidden):
+        s = np.asarray(scale_i32).astype(np.int64) & 0xFFFFFFFF
+        tokens, words = s.shape
+        g128 = np.stack([(s >> (8 * (3 - b))) & 0xFF for b in range(4)], axis=-1).reshape(tokens, words * 4)
+        return np.repeat(g128, 4, axis=1).astype(np.uint8)
+    monkeypatch.setattr(permute, "broadcast_scale_bytes", bb)
+
+
+def dbias_after_bf16_rounding(monkeypatch):
+    import torch
+    orig = glu.dbias_from_D
+
+    def db(D, group, L):
+        Db = torch.from_numpy(np.asarray(D, dtype=np.float32)).to(torch.bfloat16).double().numpy()
+        return orig(Db, group, L)
+    monkeypatch.setattr(glu, "dbias_from_D", db)
+
+
+def group_amax_swapped(monkeypatch):
+    orig = glu.group_amax
+    monkeypatch.setattr(glu, "group_amax", lambda D, group, L: orig(D, group, L)[:, ::-1])
+
+
+def norm_const_twice(monkeypatch):
+    orig = glu.quantize_rows_fp8
+    monkeypatch.setattr(glu, "quantize_rows_fp8",
+                        lambda D, norm_const=1.0: orig(np.asarray(D, np.float32) * np.float32(norm_const), norm_const))
+
+
 CASES = {
     "e2m1 ties away from zero": (e2m1_ties_away, [tfm.test_e2m1_rounding_points, tq.test_round_trip_error_bound]),
     "fp4 nibbles swapped": (nibbles_swapped, [tfm.test_fp4_packing_even_index_low_nibble,
@@ -158,6 +202,11 @@ CASES = {
                                             tgl.test_dswiglu_gate_zero_and_prob_zero]),
     "geglu alpha 1.72": (geglu_alpha_wrong, [tg.test_dgeglu_constants_are_the_pages_defaults,
                                              tgl.test_dgeglu_matches_finite_differences_away_from_clamps]),
+    "permute tokens in reverse order": (permute_tokens_reversed, [tpm.test_hand_worked_routing]),
+    "broadcast scale bytes big-endian": (broadcast_bytes_big_endian, [tpm.test_broadcast_scale_bytes_by_hand]),
+    "dbias after BF16 rounding": (dbias_after_bf16_rounding, [tgl.test_dswiglu_full_L1_is_plain_gemm_and_dbias_loop]),
+    "amax gate and input swapped": (group_amax_swapped, [tgl.test_group_amax_by_hand]),
+    "norm_const applied twice": (norm_const_twice, [tgl.test_row_quantiser_norm_const_by_hand]),
 }
 
 
