@@ -180,6 +180,31 @@ def norm_const_twice(monkeypatch):
                         lambda D, norm_const=1.0: orig(np.asarray(D, np.float32) * np.float32(norm_const), norm_const))
 
 
+def swiglu_halves_swapped(monkeypatch):
+    orig = glu.swiglu_y
+
+    def sy(gate_up):  # [up | gate] read as [gate | up]
+        gu = np.asarray(gate_up, dtype=np.float32)
+        H = gu.shape[1] // 2
+        return orig(np.concatenate([gu[:, H:], gu[:, :H]], axis=1))
+    monkeypatch.setattr(glu, "swiglu_y", sy)
+
+
+def swiglu_kb_dim_per_128(monkeypatch):
+    orig = glu.swiglu_kb_dim
+    monkeypatch.setattr(glu, "swiglu_kb_dim",
+                        lambda H, mode: -(-H // 128) * 4 if mode == quant.MODE_MXFP8 else orig(H, mode))
+
+
+def swiglu_token_count_inclusive(monkeypatch):
+    orig = glu.swiglu_quant
+
+    def sq(gate_up, mode, token_nums=None, rows_per_expert=None, global_scale=None):
+        tn = None if token_nums is None else [int(t) + 1 for t in token_nums]
+        return orig(gate_up, mode, tn, rows_per_expert, global_scale)
+    monkeypatch.setattr(glu, "swiglu_quant", sq)
+
+
 CASES = {
     "e2m1 ties away from zero": (e2m1_ties_away, [tfm.test_e2m1_rounding_points, tq.test_round_trip_error_bound]),
     "fp4 nibbles swapped": (nibbles_swapped, [tfm.test_fp4_packing_even_index_low_nibble,
@@ -207,6 +232,10 @@ CASES = {
     "dbias after BF16 rounding": (dbias_after_bf16_rounding, [tgl.test_dswiglu_full_L1_is_plain_gemm_and_dbias_loop]),
     "amax gate and input swapped": (group_amax_swapped, [tgl.test_group_amax_by_hand]),
     "norm_const applied twice": (norm_const_twice, [tgl.test_row_quantiser_norm_const_by_hand]),
+    "swiglu halves swapped": (swiglu_halves_swapped, [tgl.test_swiglu_halves_gate_then_up]),
+    "swiglu FP8 kb_dim per 128 columns": (swiglu_kb_dim_per_128, [tgl.test_swiglu_quant_token_nums_and_kb_dim,
+                                                                 tg.test_swiglu_scale_width]),
+    "swiglu token count off by one": (swiglu_token_count_inclusive, [tgl.test_swiglu_quant_token_nums_and_kb_dim]),
 }
 
 
