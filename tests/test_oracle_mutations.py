@@ -205,6 +205,39 @@ def swiglu_token_count_inclusive(monkeypatch):
     monkeypatch.setattr(glu, "swiglu_quant", sq)
 
 
+def contig_boundary_row_left(monkeypatch):
+    def gr(padded_offsets, m_rows):  # a row equal to off[g] kept in group g
+        off = np.asarray(padded_offsets, dtype=np.int64)
+        rows = np.arange(m_rows)
+        g = np.searchsorted(off, rows, side="left")
+        return np.where(rows < (off[-1] if len(off) else 0), g, -1)
+    monkeypatch.setattr(gemm, "group_of_rows_contig", gr)
+
+
+def dswiglu_beta_on_D(monkeypatch):
+    orig = glu.dswiglu_epilogue
+
+    def ep(R, C, prob, beta_row):
+        D, dp, dpm, mult = orig(R, C, prob, beta_row)
+        return D * np.asarray(beta_row, dtype=np.float64)[:, None], dp, dpm, mult
+    monkeypatch.setattr(glu, "dswiglu_epilogue", ep)
+
+
+def rows_order_unchecked(monkeypatch):
+    def gr(a_deq, b_deq, expert_ids, alpha=None, bias=None):  # range checked, order not
+        a_deq = np.asarray(a_deq, dtype=np.float64)
+        b_deq = np.asarray(b_deq, dtype=np.float64)
+        L, N, _ = b_deq.shape
+        ids = np.asarray(expert_ids, dtype=np.int64)
+        al = np.ones(L) if alpha is None else np.asarray(alpha, dtype=np.float64)
+        ref = np.zeros((a_deq.shape[0], N))
+        written = (ids >= 0) & (ids < L)
+        for m in np.nonzero(written)[0]:
+            ref[m] = al[ids[m]] * (b_deq[ids[m]] @ a_deq[m])
+        return ref, np.abs(ref), written
+    monkeypatch.setattr(gemm, "grouped_rows", gr)
+
+
 CASES = {
     "e2m1 ties away from zero": (e2m1_ties_away, [tfm.test_e2m1_rounding_points, tq.test_round_trip_error_bound]),
     "fp4 nibbles swapped": (nibbles_swapped, [tfm.test_fp4_packing_even_index_low_nibble,
@@ -236,6 +269,10 @@ CASES = {
     "swiglu FP8 kb_dim per 128 columns": (swiglu_kb_dim_per_128, [tgl.test_swiglu_quant_token_nums_and_kb_dim,
                                                                  tg.test_swiglu_scale_width]),
     "swiglu token count off by one": (swiglu_token_count_inclusive, [tgl.test_swiglu_quant_token_nums_and_kb_dim]),
+    "contig boundary row in the previous group": (contig_boundary_row_left,
+                                                  [tgm.test_grouped_contig_groups_rows_and_skips_tail]),
+    "dswiglu beta applied to D": (dswiglu_beta_on_D, [tgl.test_dswiglu_beta_scales_X_not_D]),
+    "expert ids order unchecked": (rows_order_unchecked, [tgm.test_grouped_rows_skips_bad_ids]),
 }
 
 
