@@ -1052,8 +1052,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // cta_group::2 form of the TMA load), which expects the bytes of the pair; the
 // scale copies complete on each CTA's own barrier.  Each CTA's scale warps
 // stage its scales into its TMEM and arrive on the even CTA's "ready" barrier;
-// the even CTA's scale warps arrive only once the pair's A / B tiles landed, so
-// the MMA issuer waits on that single barrier per stage.
+// the MMA issuer waits on "ready" and on "full" for each stage, so whichever
+// completes last releases it without a hop through another warp.
 // The even CTA's commits are multicast to both CTAs' "empty" and "accumulator
 // full" barriers; all epilogue warps arrive on the even CTA's "accumulator
 // empty" barrier.  Those cross-CTA arrivals are relaxed: what they order is
@@ -1345,9 +1345,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_bounded(tempty_bar, acc_phase ^ 1u, wctx)) break;
         tc_fence_after();
         for (int kb = 0; kb < num_kb; ++kb) {
-          // "ready" completes after the pair's A / B tiles landed and both
-          // CTAs' scales for the stage are in TMEM
+          // "ready" completes once both CTAs' scales for the stage are in
+          // TMEM, "full" once the pair's A / B tiles landed: the issuer waits
+          // on both itself, so the later of the two releases it directly
           if (!wait_bounded(ready_bar(stage), phase, wctx)) { ok = false; break; }
+          if (!wait_bounded(full_bar(stage), phase, wctx)) { ok = false; break; }
           tc_fence_after();
           int atoms = atoms_total - kb * C::ATOMS;
           atoms = atoms < C::ATOMS ? atoms : C::ATOMS;
@@ -1468,13 +1470,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (leader) {
-          // the pair's A / B tiles of this stage landed (counted on this CTA's
-          // full barrier) before the MMA issuer is released
-          const bool wf = wait_bounded(full_bar(stage), phase, wctx);
-          ok = __all_sync(0xFFFFFFFFu, wf);
-          if (!ok) break;
-        }
         if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(ready_bar(stage), 0));
         ++kbi;
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
