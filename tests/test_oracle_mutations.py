@@ -238,6 +238,38 @@ def rows_order_unchecked(monkeypatch):
     monkeypatch.setattr(gemm, "grouped_rows", gr)
 
 
+def ue8m0_exponent_sign(monkeypatch):
+    orig = formats.decode_ue8m0
+    monkeypatch.setattr(formats, "decode_ue8m0",
+                        lambda b: orig(254 - np.asarray(b, dtype=np.int64)))  # 2^(127 - b) for 2^(b - 127)
+
+
+def sfatom_padding_filled(monkeypatch):
+    orig = quant.to_sfatom
+
+    def ts(sf_plain, rows_total=None):  # padding rows hold a copy of the last row
+        sf_plain = np.asarray(sf_plain, dtype=np.uint8)
+        m, S = sf_plain.shape
+        rows = quant.padded_rows(m) if rows_total is None else rows_total
+        full = np.concatenate([sf_plain, np.repeat(sf_plain[-1:], rows - m, axis=0)]) if rows > m else sf_plain
+        return orig(full, rows)
+    monkeypatch.setattr(quant, "to_sfatom", ts)
+
+
+def e4m3_overflow_wraps(monkeypatch):
+    orig = formats.encode_e4m3
+
+    def enc(v):  # out-of-range values wrap to the largest finite code's neighbour (no saturation)
+        v = np.asarray(v, dtype=np.float64)
+        return np.where(np.abs(v) > 464.0, np.where(v > 0, 0x7F, 0xFF), orig(np.clip(v, -464.0, 464.0)))
+    monkeypatch.setattr(formats, "encode_e4m3", enc)
+
+
+def nvfp4_global_scale_ignored(monkeypatch):
+    orig = quant.scale_byte_nvfp4
+    monkeypatch.setattr(quant, "scale_byte_nvfp4", lambda amax, g=np.float32(1.0): orig(amax, np.float32(1.0)))
+
+
 CASES = {
     "e2m1 ties away from zero": (e2m1_ties_away, [tfm.test_e2m1_rounding_points, tq.test_round_trip_error_bound]),
     "fp4 nibbles swapped": (nibbles_swapped, [tfm.test_fp4_packing_even_index_low_nibble,
@@ -273,6 +305,12 @@ CASES = {
                                                   [tgm.test_grouped_contig_groups_rows_and_skips_tail]),
     "dswiglu beta applied to D": (dswiglu_beta_on_D, [tgl.test_dswiglu_beta_scales_X_not_D]),
     "expert ids order unchecked": (rows_order_unchecked, [tgm.test_grouped_rows_skips_bad_ids]),
+    "UE8M0 exponent sign flipped": (ue8m0_exponent_sign, [tfm.test_ue8m0_decode_matches_torch,
+                                                          tq.test_round_trip_error_bound]),
+    "SfAtom padding rows not zero": (sfatom_padding_filled, [tq.test_sfatom_round_trip_and_padding]),
+    "E4M3 overflow not saturated": (e4m3_overflow_wraps, [tfm.test_e4m3_saturates_and_keeps_sign_of_zero]),
+    "NVFP4 global scale ignored": (nvfp4_global_scale_ignored, [tq.test_nvfp4_global_scale_multiplies_scale,
+                                                                tg.test_fp4_worked_quantiser_groups]),
 }
 
 
