@@ -270,6 +270,16 @@ def nvfp4_global_scale_ignored(monkeypatch):
     monkeypatch.setattr(quant, "scale_byte_nvfp4", lambda amax, g=np.float32(1.0): orig(amax, np.float32(1.0)))
 
 
+def permute_overflow_unflagged(monkeypatch):
+    orig = permute.prefill_permute
+
+    def pp(*args, **kw):
+        res = orig(*args, **kw)
+        res["flagged"] = False
+        return res
+    monkeypatch.setattr(permute, "prefill_permute", pp)
+
+
 CASES = {
     "e2m1 ties away from zero": (e2m1_ties_away, [tfm.test_e2m1_rounding_points, tq.test_round_trip_error_bound]),
     "fp4 nibbles swapped": (nibbles_swapped, [tfm.test_fp4_packing_even_index_low_nibble,
@@ -311,6 +321,7 @@ CASES = {
     "E4M3 overflow not saturated": (e4m3_overflow_wraps, [tfm.test_e4m3_saturates_and_keeps_sign_of_zero]),
     "NVFP4 global scale ignored": (nvfp4_global_scale_ignored, [tq.test_nvfp4_global_scale_multiplies_scale,
                                                                 tg.test_fp4_worked_quantiser_groups]),
+    "permute overflow not flagged": (permute_overflow_unflagged, [tpm.test_overflow_and_bad_ids_are_dropped_and_flagged]),
 }
 
 
