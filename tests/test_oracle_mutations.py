@@ -280,6 +280,20 @@ def permute_overflow_unflagged(monkeypatch):
     monkeypatch.setattr(permute, "prefill_permute", pp)
 
 
+def column_blocks_of_16(monkeypatch):
+    def qc(D, norm_const=1.0):  # column scales over 16-row blocks instead of 32
+        D = np.asarray(D, dtype=np.float32)
+        rows, cols = D.shape
+        g = np.float32(norm_const)
+        amax = np.max(np.abs(D.reshape(rows // 16, 16, cols)), axis=1)[0::2]
+        sf = quant.scale_byte_mxfp8(amax, g)
+        y = (D * g).astype(np.float32).astype(np.float64)
+        mult = np.ldexp(1.0, 127 - sf.astype(np.int64))
+        codes = formats.encode_e4m3(y.reshape(rows // 32, 32, cols) * mult[:, None, :])
+        return codes.reshape(rows, cols), sf.T.copy()
+    monkeypatch.setattr(glu, "quantize_cols_fp8", qc)
+
+
 CASES = {
     "e2m1 ties away from zero": (e2m1_ties_away, [tfm.test_e2m1_rounding_points, tq.test_round_trip_error_bound]),
     "fp4 nibbles swapped": (nibbles_swapped, [tfm.test_fp4_packing_even_index_low_nibble,
@@ -322,6 +336,8 @@ CASES = {
     "NVFP4 global scale ignored": (nvfp4_global_scale_ignored, [tq.test_nvfp4_global_scale_multiplies_scale,
                                                                 tg.test_fp4_worked_quantiser_groups]),
     "permute overflow not flagged": (permute_overflow_unflagged, [tpm.test_overflow_and_bad_ids_are_dropped_and_flagged]),
+    "column scales over 16-row blocks": (column_blocks_of_16, [tgl.test_column_quantiser_by_hand,
+                                                               tgl.test_column_quantiser_is_the_row_quantiser_of_the_transpose]),
 }
 
 
