@@ -174,3 +174,23 @@ def test_contig_example_rows():
     assert written.all()
     for s, e, g in _ranges(row):
         assert np.array_equal(ref[s:e], a[s:e] @ b[g].T)
+
+
+@pytest.mark.parametrize("row", rows_of("cudnn_dglu_scale_shapes.txt"), ids=lambda r: "-".join(r[:2]))
+def test_dglu_scale_tensor_sizes(row):
+    """The library's scale-buffer sizes (and the oracle's SfAtom buffers) equal
+    the products of the page's scale-tensor shapes."""
+    valid_m, N, K, L, sfa, sfb, sfd_row, sfd_col = map(int, row)
+    pad_m = -(-valid_m // 128) * 128
+    assert hq.sf_bytes(valid_m, K, "mxfp8") == sfa
+    assert L * hq.sf_bytes(N, K, "mxfp8") == sfb
+    assert hq.sf_bytes(valid_m, 2 * N, "mxfp8") == sfd_row
+    assert hq.sf_bytes(2 * N, pad_m, "mxfp8") == sfd_col
+    if valid_m <= 256:
+        D = bf16_exact(np.random.default_rng(valid_m), (valid_m, 2 * N))
+        _, sf_r = glu.quantize_rows_fp8(D)
+        assert oquant.to_sfatom(sf_r).size == sfd_row
+        Dp = np.zeros((pad_m, 2 * N), np.float32)
+        Dp[:valid_m] = D
+        _, sf_c = glu.quantize_cols_fp8(Dp)
+        assert oquant.to_sfatom(sf_c).size == sfd_col
