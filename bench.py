@@ -542,6 +542,10 @@ class Extras:
         t = time_kernel(lambda: hq.hq_quant(c3["a"], "mxfp8", q_out=qa, sf_out=sfa), 10, self.flush)
         byts = 3 * M * k + sfa.numel()
         res["quant_mxfp8_A_17408x4096"] = {"us": t * 1e6, "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / self.hbm}
+        bw = c3["b"].view(L * n, k)
+        t = time_kernel(lambda: hq.hq_quant(bw, "mxfp8", q_out=qb, sf_out=sfb), 10, self.flush)
+        byts = 3 * L * n * k + sfb.numel()
+        res["quant_mxfp8_W_24576x4096"] = {"us": t * 1e6, "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / self.hbm}
         off = torch.from_numpy(c3["padded_offsets"]).to(dev)
         out3 = torch.empty(M, n, dtype=torch.bfloat16, device=dev)
         qbv = qb.view(L, n, k)
