@@ -3,10 +3,19 @@ block-scaled contract) against the oracle: Step 1 on the oracle's dequantised
 operands, Step 2 the dSwiGLU / dGeGLU closed forms, Step 3 the FP8 row
 quantisation (reading Q1).
 
-BF16 D_row, dprob and dbias use the BF16 dGLU tolerances.  FP8 D_row: every
-scale byte within one step of the oracle's byte for the exact D (equal except
-where the group maximum sits at a power-of-two boundary), and the dequantised
-values within an E4M3 half-step of D plus the D tolerance.
+BF16 D_row, dprob and dbias use the BF16 dGLU tolerances.  FP8 D_row and
+D_col are quantised from the kernel's float32 D, whose distance from the exact
+D is bounded per element by
+
+    err = 2^-18 * D_mag,   D_mag = alpha^2 sum_k |a_k b_k| * |activation factor|
+
+(the GEMM accumulation bound 2^-20 alpha^2 sum|a b| carried through the
+activation factor, plus the float32 evaluation of that factor with the fast
+exponential and approximate reciprocal: a relative 2^-23 per operation and
+|gate| 2^-23 through 1 - sigmoid(gate), under 2^-18 of the same magnitude for
+|gate| <= 32).  Every scale byte and code must be one the Step-3 rule gives for
+some D inside that window (gpu_util.window_check); the bytes that differ from
+the oracle's are counted and printed.
 """
 
 import numpy as np
@@ -15,13 +24,16 @@ import torch
 
 import fp4_grouped_gemm_gb300 as hq
 import synth
-from oracle import formats, glu
+from oracle import glu
 from oracle import quant as oquant
 
 from gpu_util import (assert_rows_untouched, bf16_rows, np_f32, oracle_quant_to_device,
-                      sentinel_bf16, stacked_weights_to_device)
+                      sentinel_bf16, stacked_weights_to_device, window_check)
 
 pytestmark = pytest.mark.gpu
+
+
+D_ERR = 2.0 ** -18  # window on the kernel's float32 D, relative to D_mag (see above)
 
 
 def bf16_ulp(x):
@@ -103,20 +115,14 @@ def test_dglu_bs_fp8_out(cuda_dev, mode, act, norm):
     offsets = [256, 512]
     m, n = 640, 128
     ref, d_row, sfd, dprob, dbias = run(mode, act, offsets, m, n, 256, seed=9, fp8=True, norm=norm)
-    g = 1.0 if norm is None else norm
     w = ref["written"]
     codes = d_row.cpu().numpy()
     S = 2 * n // 32
     sf_plain = oquant.from_sfatom(sfd.cpu().numpy(), m, S)
-    _, sf_ref = glu.quantize_rows_fp8(ref["D"].astype(np.float32), g)
-    diff = np.abs(sf_plain.astype(np.int64) - sf_ref.astype(np.int64))[w]
-    assert diff.max() <= 1 and (diff == 0).mean() > 0.98, "scale bytes"
-    scale = np.repeat(formats.decode_ue8m0(sf_plain), 32, axis=1)
-    deq = formats.decode_e4m3(codes) * scale / g
-    D = ref["D"]
-    tol = 2.0 ** -4 * np.abs(D) + scale / g * 2.0 ** -10 + 2.0 ** -8 * np.abs(D) + 2.0 ** -20 * ref["D_mag"]
-    bad = (np.abs(deq - D) > tol) & w[:, None]
-    assert not bad.any(), f"{int(bad.sum())} bad FP8 D_row values"
+    n_sf, n_c = window_check(codes[w], sf_plain[w], ref["D"][w], D_ERR * ref["D_mag"][w], "mxfp8", g=norm,
+                             what=f"FP8 D_row {mode} {act}")
+    print(f"FP8 D_row {mode} {act}: {n_sf} of {sf_plain[w].size} scale bytes and {n_c} of "
+          f"{codes[w].size} values differ from the oracle's, all inside the window")
     assert (codes[~w] == 0x5A).all(), "rows past the last group written"
     check_common(ref, dprob, dbias)
 
@@ -128,21 +134,16 @@ def test_dglu_bs_column_quantised_output(cuda_dev, mode, act, norm):
     m, n = 640, 128
     ref, d_row, sfd, dprob, dbias, d_col, sfd_col = run(mode, act, offsets, m, n, 256, seed=13, fp8=True,
                                                         norm=norm, col=True)
-    g = 1.0 if norm is None else norm
     w = ref["written"]
     rows_w = int(w.sum())                     # written rows form a prefix (offsets end at 512)
     S = (m + 127) // 128 * 4
     sf_plain = oquant.from_sfatom(sfd_col.cpu().numpy(), 2 * n, S)[:, : rows_w // 32]
-    _, sf_ref = glu.quantize_cols_fp8(ref["D"][:rows_w].astype(np.float32), g)
-    diff = np.abs(sf_plain.astype(np.int64) - sf_ref.astype(np.int64))
-    assert diff.max() <= 1 and (diff == 0).mean() > 0.98, "column scale bytes"
     codes = d_col.cpu().numpy()[:rows_w]
-    scale = np.repeat(formats.decode_ue8m0(sf_plain).T, 32, axis=0)        # [rows_w, 2n]
-    deq = formats.decode_e4m3(codes) * scale / g
-    D = ref["D"][:rows_w]
-    tol = 2.0 ** -4 * np.abs(D) + scale / g * 2.0 ** -10 + 2.0 ** -8 * np.abs(D) + 2.0 ** -20 * ref["D_mag"][:rows_w]
-    bad = np.abs(deq - D) > tol
-    assert not bad.any(), f"{int(bad.sum())} bad D_col values"
+    # column quantisation is the row rule applied to the transpose
+    n_sf, n_c = window_check(codes.T, sf_plain, ref["D"][:rows_w].T, D_ERR * ref["D_mag"][:rows_w].T, "mxfp8",
+                             g=norm, what=f"FP8 D_col {mode} {act}")
+    print(f"FP8 D_col {mode} {act}: {n_sf} of {sf_plain.size} scale bytes and {n_c} of {codes.size} "
+          f"values differ from the oracle's, all inside the window")
     assert (d_col.cpu().numpy()[rows_w:] == 0x5A).all()
     check_common(ref, dprob, dbias)
 
@@ -177,6 +178,7 @@ def test_dswiglu_bs_fp8_out_full_size_sampled(cuda_dev):
     sf_all = oquant.from_sfatom(sfd.cpu().numpy(), m, S)
     codes_all = d8.cpu().numpy()
     gc, ic = glu.interleave_columns(n)
+    boundary = [0, 0]
     for g in np.unique(grp):
         sel = np.nonzero(grp == g)[0]
         qb_np, sb_np = oquant.quantize(np_f32(cfg["b"][g]), "mxfp8")
@@ -187,15 +189,13 @@ def test_dswiglu_bs_fp8_out_full_size_sampled(cuda_dev):
         magD[:, gc] = magR * mult[:, gc]
         magD[:, ic] = magR * mult[:, ic]
         sf_plain = sf_all[rows[sel]]
-        _, sf_ref = glu.quantize_rows_fp8(D.astype(np.float32))
-        diff = np.abs(sf_plain.astype(np.int64) - sf_ref.astype(np.int64))
-        assert diff.max() <= 1 and (diff == 0).mean() > 0.98, f"scale bytes, group {g}"
-        scale = np.repeat(formats.decode_ue8m0(sf_plain), 32, axis=1)
-        deq = formats.decode_e4m3(codes_all[rows[sel]]) * scale
-        tol = 2.0 ** -4 * np.abs(D) + scale * 2.0 ** -10 + 2.0 ** -8 * np.abs(D) + 2.0 ** -20 * magD
-        bad = np.abs(deq - D) > tol
-        assert not bad.any(), f"{int(bad.sum())} bad FP8 D_row values, group {g}"
+        n_sf, n_c = window_check(codes_all[rows[sel]], sf_plain, D, D_ERR * magD, "mxfp8",
+                                 what=f"full-size FP8 D_row, group {g}")
+        boundary[0] += n_sf
+        boundary[1] += n_c
         got_p = dprob[ri[torch.from_numpy(sel).to(dev)]].cpu().numpy().astype(np.float64)
         assert (np.abs(got_p - dp) <= 1e-3 * dp_mag + 1e-30).all(), f"dprob, group {g}"
+    print(f"full-size FP8 D_row: {boundary[0]} of {len(rows) * S} scale bytes and {boundary[1]} of "
+          f"{len(rows) * 2 * n} values differ from the oracle's, all inside the window")
     if valid < m:
         assert bool((d8[valid:] == 0x5A).all()), "rows past the last group written"

@@ -3,8 +3,9 @@ GEMM + dGLU (SM100)", discrete mode).
 
 Each expert's weights live in their own allocation; the discrete entry points
 must give the same bytes as the stacked entry points on the same values (the
-stacked paths are oracle-tested elsewhere; one case here is also checked
-against the oracle directly).  An expert whose pointer is null or unaligned is
+stacked paths are oracle-tested elsewhere); the contiguous NVFP4 GEMM and both
+discrete dGLU backwards (BF16, and MXFP8 with FP8 D_row) are also checked
+against the oracle directly.  An expert whose pointer is null or unaligned is
 skipped: its rows stay untouched and HQ_STATUS_BAD_POINTER is set.
 """
 
@@ -14,10 +15,11 @@ import torch
 
 import fp4_grouped_gemm_gb300 as hq
 from oracle import gemm as ogemm
+from oracle import glu
 from oracle import quant as oquant
 
-from gpu_util import (assert_gemm_close, bf16_rows, bits16, oracle_quant_to_device, sentinel_bf16,
-                      stacked_weights_to_device)
+from gpu_util import (assert_gemm_close, assert_rows_untouched, bf16_rows, bits16, np_f32,
+                      oracle_quant_to_device, sentinel_bf16, stacked_weights_to_device, window_check)
 
 pytestmark = pytest.mark.gpu
 
@@ -119,6 +121,24 @@ def assert_sums_close(dprob1, dprob0, dbias1, dbias0):
     assert ((b1 - b0).abs() <= 2 ** -7 * b0.abs() + 1e-5 * b0.abs().max()).all()
 
 
+def _bf16_ulp(x):
+    a = np.abs(x)
+    e = np.floor(np.log2(np.where(a > 0, a, 1e-300)))
+    return np.where(a > 0, 2.0 ** (e - 7), 2.0 ** -133)
+
+
+def assert_dglu_oracle(ref, dprob, dbias):
+    """dprob within 1e-3 sum_j |R swish input|, dbias within 1e-3 sum_m |D|
+    plus one BF16 ulp of the oracle's value, rows past the last group zero."""
+    w = ref["written"]
+    dp = dprob.cpu().numpy().astype(np.float64)
+    assert (np.abs(dp - ref["dprob"]) <= 1e-3 * ref["dprob_mag"] + 1e-30)[w].all(), "dprob vs oracle"
+    assert not dp[~w].any()
+    db = dbias.float().cpu().numpy().astype(np.float64)
+    assert (np.abs(db - ref["dbias"]) <= 1e-3 * ref["dbias_mag"] + _bf16_ulp(ref["dbias"])).all(), \
+        "dbias vs oracle"
+
+
 def _dglu_inputs(seed, L, m, n, k, offsets):
     a = bf16_rows(m, k, seed).cuda()
     w = torch.stack([bf16_rows(n, k, seed + 1 + e, std=0.05) for e in range(L)]).cuda()
@@ -153,6 +173,16 @@ def test_bf16_dglu_discrete_matches_stacked(cuda_dev, act):
     assert torch.equal(d1.view(torch.int16), d0.view(torch.int16))
     # dprob / dbias are sums of float atomics: equal up to the order of the adds
     assert_sums_close(dprob1, dprob0, dbias1, dbias0)
+    # and the discrete call against the oracle directly
+    args = (np_f32(a), np_f32(w), np_f32(c), offsets, alpha.cpu().numpy())
+    ref = (glu.dswiglu(*args, beta.cpu().numpy(), prob.cpu().numpy()) if act == "dswiglu"
+           else glu.dgeglu(*args, prob.cpu().numpy()))
+    D = d1.float().cpu().numpy().astype(np.float64)
+    tol = 2.0 ** -8 * np.abs(ref["D"]) + 2.0 ** -20 * ref["D_mag"] + 1e-30
+    bad = (np.abs(D - ref["D"]) > tol) & ref["written"][:, None]
+    assert not bad.any(), f"discrete D_row vs oracle: {int(bad.sum())} values outside the bound"
+    assert_rows_untouched(d1, ref["written"], "discrete D_row")
+    assert_dglu_oracle(ref, dprob1, dbias1)
     del keep
 
 
@@ -182,3 +212,18 @@ def test_block_scaled_dglu_discrete_matches_stacked(cuda_dev):
     (d0, s0, p0, b0), (d1, s1, p1, b1) = outs
     assert torch.equal(d0, d1) and torch.equal(s0, s1)
     assert_sums_close(p1, p0, b1, b0)
+    # the discrete call against the oracle: Step 1 on the oracle's dequantised
+    # operands, FP8 D_row within the window of the kernel's float32 D (2^-18
+    # of D_mag, as in the stacked block-scaled tests)
+    qa_np, sa_np = oquant.quantize(np_f32(a), "mxfp8")
+    a_deq = oquant.dequantize(qa_np, sa_np, "mxfp8")
+    b_deq = np.stack([oquant.dequantize(*oquant.quantize(np_f32(w[e]), "mxfp8"), "mxfp8") for e in range(L)])
+    ref = glu.dswiglu(a_deq, b_deq, np_f32(c), offsets, alpha.cpu().numpy(), beta.cpu().numpy(),
+                      prob.cpu().numpy())
+    wr = ref["written"]
+    sf_plain = oquant.from_sfatom(s1.cpu().numpy(), m, 2 * n // 32)
+    codes = d1.cpu().numpy()
+    window_check(codes[wr], sf_plain[wr], ref["D"][wr], 2.0 ** -18 * ref["D_mag"][wr], "mxfp8",
+                 what="discrete FP8 D_row vs oracle")
+    assert (codes[~wr] == 0x5A).all(), "rows past the last group written"
+    assert_dglu_oracle(ref, p1, b1)

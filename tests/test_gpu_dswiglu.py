@@ -169,14 +169,36 @@ def test_dswiglu_full_size_sampled(cuda_dev):
         assert (np.abs(got - D) <= 2.0 ** -8 * np.abs(D) + 2.0 ** -20 * magD + 1e-30).all()
         got_p = dprob[ri[torch.from_numpy(np.nonzero(sel)[0]).cuda()]].cpu().numpy()
         assert (np.abs(got_p - dp) <= 1e-3 * dp_mag + 1e-30).all()
-    # dbias equals the per-group column sums of the GPU's own D_row (any size)
-    D_all = d_row.double()
+    # dbias against the oracle for every group, on two blocks of 32 compact
+    # columns (64 D_row columns each): R restricted to those columns needs
+    # every row of the group, M_g x 64 x K multiply-adds
+    blocks = np.sort(np.random.default_rng(6).choice(n // 32, 2, replace=False))
+    cols = (blocks[:, None] * 32 + np.arange(32)).reshape(-1)              # compact columns
+    dcols = (blocks[:, None] * 64 + np.arange(64)).reshape(-1)             # D_row / C columns
+    a_all = np_f32(cfg["a"]).astype(np.float64)
+    c_all = np_f32(cfg["c"][:, torch.from_numpy(dcols).cuda()])
+    p_all = cfg["prob"].cpu().numpy()
+    db_gpu = dbias.double().cpu().numpy()
     starts = np.concatenate([[0], cfg["padded_offsets"][:-1]])
+    for g in range(L):
+        s, e = int(starts[g]), int(cfg["padded_offsets"][g])
+        if e <= s:
+            assert not db_gpu[g].any(), f"dbias of empty group {g}"
+            continue
+        b_g = np_f32(cfg["b"][g][torch.from_numpy(cols).cuda()]).astype(np.float64)
+        R = alpha[g] ** 2 * (a_all[s:e] @ b_g.T)
+        D, _, _, _ = glu.dswiglu_epilogue(R, c_all[s:e], p_all[s:e], np.full(e - s, beta[g]))
+        ref_b = glu.dbias_from_D(D, np.zeros(e - s, dtype=np.int64), 1)[0]
+        mag_b = glu.dbias_from_D(np.abs(D), np.zeros(e - s, dtype=np.int64), 1)[0]
+        got = db_gpu[g, dcols]
+        assert (np.abs(got - ref_b) <= 1e-3 * mag_b + bf16_ulp(ref_b)).all(), f"dbias vs oracle, group {g}"
+    # and, over every column, dbias equals the per-group column sums of the
+    # GPU's own D_row up to the BF16 rounding of D_row's elements
+    D_all = d_row.double()
     for g in range(L):
         s, e = int(starts[g]), int(cfg["padded_offsets"][g])
         colsum = D_all[s:e].sum(dim=0) if e > s else torch.zeros(2 * n, dtype=torch.float64, device="cuda")
         absum = D_all[s:e].abs().sum(dim=0) if e > s else torch.zeros(2 * n, dtype=torch.float64, device="cuda")
         got = dbias[g].double()
-        # bf16 rounding of each D element (2^-9 relative) bounds the difference
         tol = 2.0 ** -8 * absum + 2.0 ** -7 * got.abs() + 1e-6
         assert bool(((got - colsum).abs() <= tol).all()), f"dbias group {g}"

@@ -7,14 +7,11 @@ y64 by the GEMM's accumulation error propagated through SwiGLU:
     E_y  = |silu(gate)| d_up + 1.1 |up| d_gate + 2^-18 |y|
 (|d y / d gate| = |up sigmoid(gate) (1 + gate (1 - sigmoid(gate)))| <= 1.1 |up|;
 the last term covers the float32 SwiGLU arithmetic).  Checks:
-  * scale bytes: within one step of the oracle's bytes for the float32
-    gate_up and equal for all but a few groups;
-  * codes: the dequantised value within half a code step of y64 plus E_y
-    (E4M3: 2^-4 |y| + 2^-10 scale; E2M1: max(1/4 scale, |y| / 4), which also
-    covers the saturation at 6 after a rounded-down UE4M3 scale);
-    Where the UE4M3 scale saturates (g amax / 6 > 448) the codes clamp at
-    +-6 and so does the reference value;
-  * codes equal the oracle's codes for nearly all elements;
+  * every scale byte is one the quantiser's rule gives for some group maximum
+    within E_y of the exact one, and every code one the rule gives, under the
+    GPU's scale byte, for some y within E_y of y64 (gpu_util.window_check;
+    both rules are monotone, so the window is an interval of bytes); the bytes
+    that differ from the oracle's are counted and printed;
   * rows at or past padded_offsets[L-1] untouched (codes and scale bytes),
     MXFP8 scale columns past H / 32 written 0.
 """
@@ -29,7 +26,7 @@ from oracle import gemm as ogemm
 from oracle import formats, glu
 from oracle import quant as oquant
 
-from gpu_util import bf16_rows, np_f32, oracle_quant_to_device, stacked_weights_to_device
+from gpu_util import bf16_rows, np_f32, oracle_quant_to_device, stacked_weights_to_device, window_check
 
 pytestmark = pytest.mark.gpu
 
@@ -48,33 +45,11 @@ def y_error_bound(gu, mag):
 def check_block(q_gpu, sf_gpu, gu, mag, out_mode, g, what):
     """q_gpu / sf_gpu: the GPU's codes and plain scale bytes of the rows and
     compact columns of gu (float64 gate_up [r, 2H'], H' whole scale groups)."""
-    H = gu.shape[1] // 2
-    gs = 32 if out_mode == "mxfp8" else 16
     y64, ey = y_error_bound(gu, mag)
-    ref = glu.swiglu_quant(gu.astype(np.float32), out_mode, global_scale=g)
-    sf_ref = ref["sf_plain"][:, : H // gs].astype(np.int64)
-    diff = np.abs(sf_gpu.astype(np.int64) - sf_ref)
-    assert diff.max() <= 1, f"{what}: scale byte off by {diff.max()}"
-    assert (diff == 0).mean() > 0.98, f"{what}: {int((diff != 0).sum())} scale bytes differ"
-    deq = oquant.dequantize(q_gpu, sf_gpu, out_mode)
-    if out_mode == "mxfp8":
-        scale = np.repeat(2.0 ** (sf_gpu.astype(np.float64) - 127), gs, axis=1)
-        tol = 2.0 ** -4 * (np.abs(y64) + ey) + 2.0 ** -10 * scale + ey
-    else:
-        gf = 1.0 if g is None else float(g)
-        deq = deq / gf
-        sv = np.repeat(formats.decode_ue4m3(sf_gpu), gs, axis=1) / gf
-        tol = np.maximum(0.25 * sv, (np.abs(y64) + ey) / 4.0) + ey
-        # a scale saturated at the largest UE4M3 value (448) clamps the codes
-        # at +-6: the reference value is clamped alike
-        y64 = np.clip(y64, -6.0 * sv, 6.0 * sv)
-    bad = np.abs(deq - y64) > tol
-    if bad.any():
-        i = tuple(np.argwhere(bad)[0])
-        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} values outside the bound; first {i}: "
-                             f"gpu={deq[i]!r} y={y64[i]!r} tol={tol[i]!r}")
-    same = (q_gpu == ref["q"]).mean()
-    assert same > 0.99, f"{what}: only {same:.4f} of the codes equal the oracle's"
+    codes = q_gpu if out_mode == "mxfp8" else formats.unpack_e2m1(q_gpu)
+    n_sf, n_c = window_check(codes, sf_gpu, y64, ey, out_mode, g=g, what=what)
+    print(f"{what}: {n_sf} of {sf_gpu.size} scale bytes and {n_c} of {codes.size} values differ from "
+          f"the oracle's, all inside the window")
 
 
 def run_small(mode, out_mode, offsets, m, H, k, alpha, g, seed):
@@ -138,8 +113,8 @@ def test_fused_up_proj_pairs_odd_group_ends(cuda_dev):
 
 def test_fused_up_proj_matches_unfused_path_on_exact_sums(cuda_dev):
     """With small-integer operands every gate_up is exact in BF16 and float32,
-    so the fused path and GEMM -> BF16 -> hq_swiglu_quant agree up to the
-    last-bit rounding of the two SwiGLU evaluations."""
+    so the fused path and GEMM -> BF16 -> hq_swiglu_quant both meet the oracle
+    within the last-bit rounding of their own SwiGLU evaluations."""
     dev = torch.device("cuda")
     L, m, H, k = 2, 512, 256, 256
     gen = torch.Generator().manual_seed(5)
@@ -153,13 +128,21 @@ def test_fused_up_proj_matches_unfused_path_on_exact_sums(cuda_dev):
     gu = hq.hq_gemm_grouped_contig(qa, sfa, qb.view(L, 2 * H, k), sfb, off, m, 2 * H, k, "mxfp8")
     qu, sfu = hq.hq_swiglu_quant(gu, "mxfp8")
     torch.cuda.synchronize()
-    # the two SwiGLU evaluations may still round differently in the last bit
-    # (the fused epilogue uses the fast exponential): a scale byte can move
-    # only where amax / 448 sits exactly on a power of two, a code only where
-    # y sits on a rounding boundary
-    d = (sff.cpu().numpy().astype(np.int64) - sfu.cpu().numpy().astype(np.int64))
-    assert np.abs(d).max() <= 1 and (d != 0).sum() <= 2
-    assert (qf != qu).float().mean().item() < 1e-3
+    # gate_up is exact here (small integers times powers of two), so each
+    # path is checked against the oracle's y with only its own SwiGLU
+    # arithmetic in the window: 2^-18 |y| for the fused epilogue's fast
+    # exponential, reading D5's 2^-20 |y| for the separate pass
+    a64 = a.double().numpy()
+    gu64 = np.zeros((m, 2 * H))
+    for gidx, (r0, r1) in enumerate([(0, 256), (256, 512)]):
+        gu64[r0:r1] = a64[r0:r1] @ w[gidx].double().numpy().T
+    assert np.array_equal(gu64.astype(np.float32), gu.float().cpu().numpy()), "exact gate_up"
+    y64 = gu64[:, H:] * gu64[:, :H] / (1.0 + np.exp(-gu64[:, :H]))
+    kb = hq.swiglu_kb_dim(H, "mxfp8")
+    for what, q_, sf_, rel in (("fused", qf, sff, 2.0 ** -18), ("separate pass", qu, sfu, 2.0 ** -20)):
+        sf_plain = oquant.from_sfatom(sf_.cpu().numpy(), m, kb)[:, : H // 32]
+        n_sf, n_c = window_check(q_.cpu().numpy(), sf_plain, y64, rel * np.abs(y64), "mxfp8", what=what)
+        print(f"exact gate_up, {what}: {n_sf} scale bytes and {n_c} values differ from the oracle's")
 
 
 def test_full_moe_up_proj_mxfp8_sampled(cuda_dev):
