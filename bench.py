@@ -43,7 +43,7 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # nominal dense tensor-core ratios to BF16 (2.25 PFLOP/s): FP8 x2, FP4 x6
 RATIO = {"bf16": 1.0, "fp8": 2.0, "fp4": 6.0}
 SECTIONS = ("dense_mxfp8_256", "quant_nvfp4", "moe_contig", "moe_masked", "dswiglu", "dense_mxfp4",
-            "permute")
+            "permute", "mma_rate")
 
 
 GEMM_PROFILE = os.path.join(ROOT, "profiles", "bs_gemm_2sm_kernel_dense_nvfp4_4096x12288x5120.md")
@@ -249,6 +249,77 @@ def oracle_cpu_baseline(budget_s=10.0, ms=64, ns=512):
                       f"float64 GEMM) in {dt:.1f} s, from the {4096}x{12288}x{5120} workload"}
 
 
+def _oracle_quant_chunk(job):
+    """One process's share of the all-cores quantiser baseline: quantise a
+    seeded [rows, k] BF16-valued block `reps` times; returns elapsed seconds."""
+    rows, k, seed, mode, reps = job
+    from oracle import quant as oquant
+    x = torch.randn(rows, k, generator=torch.Generator().manual_seed(seed)).to(torch.bfloat16).float().numpy()
+    t0 = time.time()
+    for _ in range(reps):
+        oquant.quantize(x, mode, 37.0 if mode == "nvfp4" else None)
+    return time.time() - t0
+
+
+def oracle_kernel_baselines(budget_s=2.0):
+    """The CPU oracle per kernel of the path, each on a bounded sample:
+    the quantiser single-threaded and on all cores (a process pool), and each
+    GEMM workload's dequantise-then-float64 GEMM on all cores (numpy's BLAS
+    threads).  Values in the unit of the matching GPU line."""
+    import multiprocessing as mp
+    from oracle import gemm as ogemm, glu, quant as oquant
+    cores = len(os.sched_getaffinity(0))
+    res = {}
+    # quantiser, NVFP4 rows of the headline A (k = 5120), single thread
+    rows, k = 64, 5120
+    x = torch.randn(rows, k, generator=torch.Generator().manual_seed(2)).to(torch.bfloat16).float().numpy()
+    n_rep, t0 = 0, time.time()
+    while time.time() - t0 < budget_s:
+        oquant.quantize(x, "nvfp4", 37.0)
+        n_rep += 1
+    dt = time.time() - t0
+    byts = rows * k * 2 + rows * k // 2 + rows * k // 16
+    res["quant_nvfp4_single_thread"] = {"gbs": n_rep * byts / dt / 1e9, "cores": 1,
+                                        "sample": f"{n_rep} x [{rows},{k}] in {dt:.1f} s"}
+    # the same on all cores: one process per core, each its own rows
+    reps = max(1, int(n_rep / dt * budget_s / 2))
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores) as pool:
+        pool.map(_oracle_quant_chunk, [(8, k, i, "nvfp4", 1) for i in range(cores)])  # start-up
+        t0 = time.time()
+        pool.map(_oracle_quant_chunk, [(rows, k, i, "nvfp4", reps) for i in range(cores)])
+        dt = time.time() - t0
+    res["quant_nvfp4_all_cores"] = {"gbs": cores * reps * byts / dt / 1e9, "cores": cores,
+                                    "sample": f"{cores} processes x {reps} x [{rows},{k}] in {dt:.1f} s"}
+
+    def gemm(name, m, n, k, mode, std_b):
+        a = torch.randn(m, k, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16).float().numpy()
+        b = (torch.randn(n, k, generator=torch.Generator().manual_seed(4)) * std_b).to(torch.bfloat16).float().numpy()
+        if mode == "bf16":
+            ad, bd = a.astype(np.float64), b.astype(np.float64)
+        else:
+            g = 37.0 if mode == "nvfp4" else None
+            ad = oquant.dequantize(*oquant.quantize(a, mode, g), mode)
+            bd = oquant.dequantize(*oquant.quantize(b, mode, g), mode)
+        reps, t0 = 0, time.time()
+        while time.time() - t0 < budget_s:
+            if mode == "bf16":   # the dSwiGLU backward: R, then the closed form on C
+                R, _, _ = glu.grouped_R(ad, bd[None], [m], [1.0])
+                c = np.ones((m, 2 * n))
+                glu.dswiglu_epilogue(R, c, np.ones(m), np.ones(m))
+            else:
+                ogemm.dense(ad, bd)
+            reps += 1
+        dt = time.time() - t0
+        res[name] = {"tflops": reps * 2.0 * m * n * k / dt / 1e12, "cores": cores,
+                     "sample": f"{reps} x [{m}x{n}x{k}] ({mode} operands dequantised, float64) in {dt:.1f} s"}
+    gemm("dense_nvfp4_gemm", 64, 512, 5120, "nvfp4", 0.02)
+    gemm("moe_contig_mxfp8_gemm", 64, 512, 4096, "mxfp8", 0.02)
+    gemm("moe_masked_nvfp4_gemm", 64, 512, 7168, "nvfp4", 0.02)
+    gemm("dswiglu_bwd_bf16_gemm", 64, 256, 2048, "bf16", 0.02)
+    return res
+
+
 # --------------------------------------------------------------------------- reference arm
 
 
@@ -345,6 +416,14 @@ def headline(hq, dev, args, ws, peaks, pk_src):
     value = ws * args.steps * flops / total_max / 1e12
     peak_fp4 = peaks["bf16_tflops"] * RATIO["fp4"]
     achieved = flops / gemm_avg / 1e12
+    # the tensor pipe's own FP4 rate, measured here after the timed region
+    # (the library's issue-rate probe: back-to-back kind::mxf4nvf4 MMAs of
+    # M = 256, N = 256 on CTA pairs), at the SM clock sampled while timing
+    clk = Clocks.summarize(rows)
+    mma = hq.probe_mma_rate("nvfp4", pair=True)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    bench_mhz = clk["sm_mhz"] or mma["sm_mhz"]
+    peak_mma = mma["flop_per_clk_sm"] * sms * bench_mhz * 1e6 / 1e12
 
     # end to end through the public API from pinned host buffers, as a
     # serving loop runs it: every step copies its own A and B from the host,
@@ -415,11 +494,17 @@ def headline(hq, dev, args, ws, peaks, pk_src):
                      "frac": achieved / peak_fp4, "traffic": profiled_traffic(),
                      "traffic_unit": "bytes per launch (ncu dram read + write)",
                      "kernel": "bs_gemm_2sm_kernel<NVFP4,4,GEMM,384> (cluster pair, 256x384 tiles)",
-                     "peak_source": f"{pk_src} bf16 burst {peaks['bf16_tflops']} x 6 (nominal FP4/BF16)"},
+                     "peak_source": f"{pk_src} bf16 burst {peaks['bf16_tflops']} x 6 (nominal FP4/BF16)",
+                     "frac_measured_mma": achieved / peak_mma, "peak_measured_mma": peak_mma,
+                     "measured_mma": {"kind": "mxf4nvf4.block_scale.scale_vec::4X, cta_group::2, 256x256x64",
+                                      "cycles_per_mma": mma["cycles_per_mma"],
+                                      "flop_per_clk_sm": mma["flop_per_clk_sm"], "sms": sms,
+                                      "sm_mhz": bench_mhz,
+                                      "note": "peak = FLOP/clk/SM x SMs x median SM clock of the timed region"}},
         "e2e": {"value": ws * flops / e2e_t / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": 3 * args.steps,
-        "clocks": Clocks.summarize(rows),
+        "clocks": clk,
         "gemm_ms": gemm_avg * 1e3,
     }
 
@@ -451,25 +536,26 @@ class Extras:
         qb, sfb = hq.hq_quant(c1["b"], "mxfp8")
         out1 = torch.empty(256, 256, dtype=torch.bfloat16, device=dev)
         t = time_kernel(lambda: hq.hq_gemm_dense(qa, sfa, qb, sfb, 256, 256, 256, "mxfp8", out=out1), 200)
+        calls = 1000  # back-to-back calls captured in one graph
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            for _ in range(100):
+            for _ in range(calls):
                 hq.hq_gemm_dense(qa, sfa, qb, sfb, 256, 256, 256, "mxfp8", out=out1)
         g.replay()
         torch.cuda.synchronize()
-        tg = time_kernel(lambda: g.replay(), 10) / 100
+        tg = time_kernel(lambda: g.replay(), 10) / calls
         # the same graph with programmatic dependent launch: each call's
         # prologue (barriers, TMEM, tensor-map prefetch) overlaps the previous
         # call's tail, its first read waits for that call to finish
         gp = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gp):
-            for _ in range(100):
+            for _ in range(calls):
                 hq.hq_gemm_dense(qa, sfa, qb, sfb, 256, 256, 256, "mxfp8", out=out1, use_pdl=True)
         gp.replay()
         torch.cuda.synchronize()
-        tgp = time_kernel(lambda: gp.replay(), 10) / 100
+        tgp = time_kernel(lambda: gp.replay(), 10) / calls
         return {"dense_mxfp8_256": {"us_per_call": t * 1e6, "us_per_call_graph": tg * 1e6,
-                                    "us_per_call_graph_pdl": tgp * 1e6,
+                                    "us_per_call_graph_pdl": tgp * 1e6, "graph_calls": calls,
                                     "tflops": 2 * 256 ** 3 / t / 1e12}}
 
     def quant_nvfp4(self):
@@ -589,11 +675,62 @@ class Extras:
         byts = E * n * k // 2 + sfb.numel() + tiles * 128 * (k // 2 + k // 16) + valid * n * 2
         res["moe_masked_nvfp4_E32"] = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_fp4": fl / t / 1e12 / self.p_fp4,
                                       "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / self.hbm}
+        # the hot-path step on this workload: quantise the activations
+        # (E * max_m rows, BF16 -> NVFP4) and run the masked GEMM against the
+        # resident NVFP4 expert weights
+        a4 = c4["a"]
+
+        def step():
+            hq.hq_quant(a4, "nvfp4", q_out=qa, sf_out=sfa)
+            hq.hq_gemm_grouped_masked(qa, sfa, qbv, sfb, mm, max_m, n, k, "nvfp4", alpha=c4["alpha"], out=out4)
+        t_step = time_kernel(step, 20, self.flush)
+        t_qa = time_kernel(lambda: hq.hq_quant(a4, "nvfp4", q_out=qa, sf_out=sfa), 20, self.flush)
+        # end to end through the public API: every step uploads the activations
+        # from pinned host memory, quantises them, runs the GEMM and downloads
+        # the output rows, one stream, steady state
+        a_h = a4.cpu().pin_memory()
+        out_h = torch.empty(E * max_m, n, dtype=torch.bfloat16).pin_memory()
+        a_d = torch.empty_like(a4)
+
+        def e2e():
+            a_d.copy_(a_h, non_blocking=True)
+            hq.hq_quant(a_d, "nvfp4", q_out=qa, sf_out=sfa)
+            hq.hq_gemm_grouped_masked(qa, sfa, qbv, sfb, mm, max_m, n, k, "nvfp4", alpha=c4["alpha"], out=out4)
+            out_h.copy_(out4, non_blocking=True)
+        for _ in range(3):
+            e2e()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 10
+        e0.record()
+        for _ in range(reps):
+            e2e()
+        e1.record()
+        torch.cuda.synchronize()
+        t_e2e = e0.elapsed_time(e1) / reps / 1e3
+        res["moe_masked_nvfp4_E32_step"] = {
+            "step": "hq_quant(A [E*max_m, K] -> NVFP4), then hq_gemm_grouped_masked", "us": t_step * 1e6,
+            "quant_us": t_qa * 1e6, "tflops": fl / t_step / 1e12, "launches": 2,
+            "e2e": {"us": t_e2e * 1e6, "tflops": fl / t_e2e / 1e12, "h2d_bytes_per_step": a4.numel() * 2,
+                    "d2h_bytes_per_step": out4.numel() * 2,
+                    "note": "weights resident; activations up, output rows down, one stream"}}
         t = time_kernel(lambda: hq.hq_quant(c4["b"].view(E * n, k), "nvfp4", q_out=qb, sf_out=sfb), 5, self.flush)
         byts = 2 * E * n * k + E * n * k // 2 + sfb.numel()
         res["quant_nvfp4_W_131072x7168"] = {"us": t * 1e6, "gbs": byts / t / 1e9,
                                             "frac_hbm": byts / t / 1e9 / self.hbm}
         return res
+
+    def mma_rate(self):
+        """Issue rate of back-to-back tcgen05.mma per kind (the library's probe,
+        M = 128 per SM, N = 256, one wave), single SM and CTA pairs."""
+        res = {}
+        for kind in ("bf16", "mxfp8", "nvfp4", "mxfp4"):
+            for pair in (False, True):
+                r = self.hq.probe_mma_rate(kind, pair=pair)
+                res[f"{kind}_{'pair' if pair else 'single'}"] = {
+                    "cycles_per_mma": r["cycles_per_mma"], "flop_per_clk_sm": r["flop_per_clk_sm"],
+                    "sm_mhz": r["sm_mhz"], "ctas": r["ctas"]}
+        return {"mma_rate": res}
 
     def dswiglu(self):
         hq, dev = self.hq, self.dev
@@ -665,6 +802,7 @@ def main():
         line["workloads"] = Extras(hq, dev, peaks).run(Extras.NAMES)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_cpu_baseline()
+        line["cpu_baseline"]["per_kernel"] = oracle_kernel_baselines()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:

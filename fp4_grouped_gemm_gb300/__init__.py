@@ -19,7 +19,7 @@ from ._abi import (HQ_MXFP8, HQ_MXFP4, HQ_NVFP4, HQ_STATUS_WAIT_TIMEOUT, HQ_STAT
 
 __all__ = [
     "HQError", "mode_id", "group_size", "sf_bytes", "capabilities", "get_device_status",
-    "set_wait_limit_ns", "selftest_wait_expiry", "set_gemm_tile_n", "set_gemm_2sm", "hq_quant",
+    "set_wait_limit_ns", "selftest_wait_expiry", "probe_mma_rate", "set_gemm_tile_n", "set_gemm_2sm", "hq_quant",
     "hq_gemm_dense", "hq_gemm_grouped_contig", "hq_gemm_grouped_masked", "hq_swiglu_quant",
     "hq_gemm_dswiglu", "hq_gemm_dswiglu_workspace_size", "hq_gemm_dgeglu", "swiglu_kb_dim",
     "hq_prefill_permute", "hq_prefill_permute_workspace_size", "hq_gemm_grouped_rows",
@@ -91,6 +91,34 @@ def set_wait_limit_ns(ns):
 def selftest_wait_expiry(limit_ns, stream=None):
     _check(_abi.load().hq_selftest_wait_expiry(int(limit_ns), _stream(stream)),
            "hq_selftest_wait_expiry")
+
+
+MMA_KINDS = {"bf16": (0, 16), "mxfp8": (1, 32), "nvfp4": (2, 64), "mxfp4": (3, 64)}
+
+
+def probe_mma_rate(kind, pair=True, n=256, iters=4096, stream=None):
+    """Issue rate of back-to-back tcgen05.mma of `kind` (hq_probe_mma_rate).
+
+    Returns a dict: median cycles per MMA over the issuing CTAs, the FLOP per
+    SM clock that implies (M = 128 per SM), the SM clock the probe ran at
+    (cycles / ns) and the number of issuing CTAs that reported."""
+    kid, kk = MMA_KINDS[kind]
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    ctas = sms // 2 if pair else sms
+    out = torch.zeros(2 * ctas, dtype=torch.int64, device="cuda")
+    _check(_abi.load().hq_probe_mma_rate(kid, 1 if pair else 0, n, iters, _ptr(out), _stream(stream)),
+           "hq_probe_mma_rate")
+    torch.cuda.synchronize()
+    v = out.view(ctas, 2).cpu().double()
+    good = v[:, 0] > 0
+    cyc = (v[good, 0] / (4.0 * iters)).sort().values
+    mhz = (v[good, 0] / v[good, 1] * 1e3).sort().values
+    if cyc.numel() == 0:
+        raise RuntimeError("hq_probe_mma_rate: no issuing CTA finished its timed MMAs")
+    med = float(cyc[cyc.numel() // 2])
+    return {"kind": kind, "pair": bool(pair), "n": n, "cycles_per_mma": med,
+            "flop_per_clk_sm": 2.0 * 128 * n * kk / med, "sm_mhz": float(mhz[mhz.numel() // 2]),
+            "ctas": int(cyc.numel())}
 
 
 def set_gemm_tile_n(tile_n):

@@ -213,6 +213,147 @@ int build_weight_maps(const CUtensorMap& tmpl, const int64_t* b_ptrs, const int6
   return cudaGetLastError() == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-core issue-rate probe: one thread per CTA (per cluster pair) issues
+// MMAs back to back on operands resident in shared memory; clock64 and the
+// global timer bracket the timed MMAs, which complete on an mbarrier through
+// tcgen05.commit.  Waits are bounded (2 s); a CTA whose wait expired reports
+// zero cycles.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr int kProbeThreads = 128;
+
+template <int KIND>
+__host__ __device__ constexpr uint32_t probe_idesc(int m, int n) {
+  return (KIND == 0 ? ((1u << 4) | (1u << 7) | (1u << 10))          // f32 <- bf16 x bf16
+          : KIND == 1 ? ((0u << 7) | (0u << 10) | (1u << 23))        // E4M3, UE8M0
+          : KIND == 3 ? ((1u << 7) | (1u << 10) | (1u << 23))        // E2M1, UE8M0
+                      : ((1u << 7) | (1u << 10) | (0u << 23))) |     // E2M1, UE4M3
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+template <int KIND, int PAIR>
+__global__ void __launch_bounds__(kProbeThreads, 1) mma_rate_kernel(int n, int iters, uint64_t* out) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int b_rows = PAIR ? n / 2 : n;
+  const int bytes = 16384 + b_rows * 128;  // A: 128 rows x 128 B, B: b_rows x 128 B
+  const int warp = threadIdx.x >> 5;
+  // operand bytes: small E4M3 / E2M1 / BF16 values, never NaN
+  for (int i = threadIdx.x * 4; i < bytes; i += kProbeThreads * 4) {
+    uint32_t h = static_cast<uint32_t>(i) * 2654435761u ^ blockIdx.x * 97u;
+    h ^= h >> 13;
+    h *= 0x5bd1e995u;
+    h ^= h >> 15;
+    *reinterpret_cast<uint32_t*>(smem + i) = h & 0x3F3F3F3Fu;
+  }
+  const uint32_t bar = sbase + bytes;
+  uint32_t* slot = reinterpret_cast<uint32_t*>(smem + bytes + 16);
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    if (PAIR) { tmem_alloc_2sm(smem_u32(slot), 512); tmem_relinquish_2sm(); }
+    else { tmem_alloc(smem_u32(slot), 512); tmem_relinquish(); }
+  }
+  __syncthreads();
+  if (PAIR) cluster_sync();
+  tc_fence_after();
+  const uint32_t tb = *slot;
+  {
+    // scale columns [256, 288) of every lane: 1.0 (UE8M0 127, UE4M3 0x38)
+    uint32_t v[16];
+    const uint32_t one = KIND == 2 ? 0x38383838u : 0x7F7F7F7Fu;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = one;
+    const uint32_t lq = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    tmem_st_32x32b<16>(lq + tb + 256, v);
+    tmem_st_32x32b<16>(lq + tb + 272, v);
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (PAIR) cluster_sync();
+  tc_fence_after();
+  const bool issuer = threadIdx.x == 0 && (!PAIR || cluster_ctarank() == 0);
+  if (issuer) {
+    const uint64_t ad = smem_desc_sw128(sbase), bd = smem_desc_sw128(sbase + 16384);
+    const uint32_t id = probe_idesc<KIND>(PAIR ? 256 : 128, n);
+    const uint32_t sfa = tb + 256, sfb = tb + 272;
+    auto run = [&](int count) {
+      for (int it = 0; it < count; ++it) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t acc = (it | j) ? 1u : 0u;
+          if (PAIR) {
+            if (KIND == 0) mma_bf16_2sm(tb, ad + 2 * j, bd + 2 * j, id, acc);
+            else if (KIND == 1) mma_mxf8_2sm(tb, ad + 2 * j, bd + 2 * j, id, sfa, sfb, acc);
+            else if (KIND == 2) mma_nvf4_2sm(tb, ad + 2 * j, bd + 2 * j, id, sfa, sfb, acc);
+            else mma_mxf4_2sm(tb, ad + 2 * j, bd + 2 * j, id, sfa, sfb, acc);
+          } else {
+            if (KIND == 0) mma_bf16(tb, ad + 2 * j, bd + 2 * j, id, acc);
+            else if (KIND == 1) mma_mxf8(tb, ad + 2 * j, bd + 2 * j, id, sfa, sfb, acc);
+            else if (KIND == 2) mma_nvf4(tb, ad + 2 * j, bd + 2 * j, id, sfa, sfb, acc);
+            else mma_mxf4(tb, ad + 2 * j, bd + 2 * j, id, sfa, sfb, acc);
+          }
+        }
+      }
+      if (PAIR) tc_commit_2sm_mc(bar, 0x1);
+      else tc_commit(bar);
+    };
+    run(16);  // warm-up
+    bool ok = wait_drain(bar, 0, 2000000000ull);
+    const uint64_t c0 = clock64(), g0 = globaltimer_ns();
+    run(iters);
+    ok = wait_drain(bar, 1, 2000000000ull) && ok;
+    const uint64_t c1 = clock64(), g1 = globaltimer_ns();
+    const int slot_i = PAIR ? blockIdx.x >> 1 : blockIdx.x;
+    out[2 * slot_i] = ok ? c1 - c0 : 0;
+    out[2 * slot_i + 1] = ok ? g1 - g0 : 0;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (PAIR) cluster_sync();
+  if (warp == 0) {
+    tc_fence_after();
+    if (PAIR) tmem_dealloc_2sm(tb, 512);
+    else tmem_dealloc(tb, 512);
+  }
+}
+
+template <int KIND, int PAIR>
+int launch_mma_rate(int n, int iters, uint64_t* out, cudaStream_t st) {
+  auto kern = mma_rate_kernel<KIND, PAIR>;
+  // at least 120 KB of shared memory: one CTA per SM
+  constexpr int kSmem = 120 * 1024;
+  if (set_smem_once<mma_rate_kernel<KIND, PAIR>>(kSmem) != HQ_OK) return HQ_ERR_CUDA;
+  const int sms = num_sms();
+  if (sms < 2) return HQ_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(PAIR ? sms / 2 * 2 : sms));
+  cfg.blockDim = dim3(kProbeThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = PAIR ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, n, iters, out) == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
+}
+
+template <int KIND>
+int launch_mma_rate_kind(int pair, int n, int iters, uint64_t* out, cudaStream_t st) {
+  return pair ? launch_mma_rate<KIND, 1>(n, iters, out, st) : launch_mma_rate<KIND, 0>(n, iters, out, st);
+}
+}  // namespace
+
 }  // namespace hq
 
 extern "C" {
@@ -297,6 +438,18 @@ int hq_selftest_wait_expiry(uint64_t limit_ns, hq_stream_t s) {
   if (!status) return HQ_ERR_CUDA;
   hq::selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(s)>>>(status, limit_ns);
   return cudaGetLastError() == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
+}
+
+int hq_probe_mma_rate(int kind, int pair, int n, int iters, uint64_t* out, hq_stream_t s) {
+  if (kind < 0 || kind > 3 || (n != 128 && n != 256) || iters < 1 || iters > (1 << 20)) return HQ_ERR_INVALID;
+  if (!out || (reinterpret_cast<uintptr_t>(out) & 7u)) return HQ_ERR_INVALID;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  switch (kind) {
+    case 0: return hq::launch_mma_rate_kind<0>(pair, n, iters, out, st);
+    case 1: return hq::launch_mma_rate_kind<1>(pair, n, iters, out, st);
+    case 2: return hq::launch_mma_rate_kind<2>(pair, n, iters, out, st);
+    default: return hq::launch_mma_rate_kind<3>(pair, n, iters, out, st);
+  }
 }
 
 }  // extern "C"

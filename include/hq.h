@@ -132,6 +132,22 @@ int hq_set_wait_limit_ns(uint64_t ns);
  * returns; the context stays usable.  No GPU fault is involved. */
 int hq_selftest_wait_expiry(uint64_t limit_ns, hq_stream_t s);
 
+/* Tensor-core issue-rate probe (a measurement aid, no counterpart on the
+ * pages): every CTA of one wave (one per SM, or one two-CTA cluster per SM
+ * pair when pair != 0) issues `iters` x 4 back-to-back tcgen05.mma of the
+ * given kind from one thread into one TMEM accumulator, with the operands
+ * resident in shared memory (M = 128 per SM, N = n, K = 16 for BF16, 32 for
+ * MXFP8, 64 for NVFP4 / MXFP4; scales constant), and records per issuing CTA
+ * the SM clock cycles and the nanoseconds of the timed MMAs.
+ *   kind   0 kind::f16 (BF16), 1 kind::mxf8f6f4 (MXFP8),
+ *          2 kind::mxf4nvf4 scale_vec::4X (NVFP4), 3 kind::mxf4 scale_vec::2X
+ *   n      128 or 256
+ *   out    device uint64 [2 * ctas]: out[2 i] = cycles, out[2 i + 1] = ns of
+ *          issuing CTA i (ctas = the number of SMs, halved when pair != 0)
+ * Cycles per MMA = cycles / (4 iters).  Returns HQ_ERR_INVALID for a bad
+ * kind, n, iters outside [1, 1 << 20] or a null / unaligned out. */
+int hq_probe_mma_rate(int kind, int pair, int n, int iters, uint64_t *out, hq_stream_t s);
+
 /* Tuning knob: GEMM tile width in N for the block-scaled GEMMs (0 = choose
  * automatically, 128 or 256 = force a single-SM tile).  Applies to later
  * calls. */

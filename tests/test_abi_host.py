@@ -220,6 +220,13 @@ def test_knobs_validate(lib):
     assert lib.hq_set_gemm_tile_n(0) == _abi.HQ_OK
     assert lib.hq_set_wait_limit_ns(0) == _abi.HQ_ERR_INVALID
     assert lib.hq_selftest_wait_expiry(0, None) == _abi.HQ_ERR_INVALID
+    # the tensor-core issue-rate probe validates before launching
+    buf = ctypes.c_void_p(4096)
+    assert lib.hq_probe_mma_rate(4, 1, 256, 16, buf, None) == _abi.HQ_ERR_INVALID   # kind
+    assert lib.hq_probe_mma_rate(2, 1, 192, 16, buf, None) == _abi.HQ_ERR_INVALID   # n
+    assert lib.hq_probe_mma_rate(2, 1, 256, 0, buf, None) == _abi.HQ_ERR_INVALID    # iters
+    assert lib.hq_probe_mma_rate(2, 1, 256, 16, None, None) == _abi.HQ_ERR_INVALID  # out
+    assert lib.hq_probe_mma_rate(2, 1, 256, 16, ctypes.c_void_p(4097), None) == _abi.HQ_ERR_INVALID
     for v in (0, 1, 256, 384):
         assert lib.hq_set_gemm_2sm(v) == _abi.HQ_OK
     assert lib.hq_set_gemm_2sm(128) == _abi.HQ_ERR_INVALID
