@@ -43,7 +43,7 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # nominal dense tensor-core ratios to BF16 (2.25 PFLOP/s): FP8 x2, FP4 x6
 RATIO = {"bf16": 1.0, "fp8": 2.0, "fp4": 6.0}
 SECTIONS = ("dense_mxfp8_256", "quant_nvfp4", "moe_contig", "moe_masked", "dswiglu", "dense_mxfp4",
-            "permute", "mma_rate")
+            "permute", "mma_rate", "host_link")
 
 
 GEMM_PROFILE = os.path.join(ROOT, "profiles", "bs_gemm_2sm_kernel_dense_nvfp4_4096x12288x5120.md")
@@ -719,6 +719,49 @@ class Extras:
         res["quant_nvfp4_W_131072x7168"] = {"us": t * 1e6, "gbs": byts / t / 1e9,
                                             "frac_hbm": byts / t / 1e9 / self.hbm}
         return res
+
+    def host_link(self):
+        """Copy rates between pinned host memory and the device (cudaMemcpyAsync
+        through torch) at the headline step's sizes: A and B up (167.8 MB), the
+        output down (100.7 MB); each direction alone and both at once on two
+        streams.  No host pointer reaches a kernel."""
+        dev = self.dev
+        up_n, down_n = (4096 + 12288) * 5120, 4096 * 12288   # BF16 elements
+        h_up = torch.empty(up_n, dtype=torch.bfloat16).pin_memory()
+        d_up = torch.empty(up_n, dtype=torch.bfloat16, device=dev)
+        h_down = torch.empty(down_n, dtype=torch.bfloat16).pin_memory()
+        d_down = torch.empty(down_n, dtype=torch.bfloat16, device=dev)
+        s_up, s_down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+        def timed(fn, reps=10):
+            for _ in range(2):
+                fn()
+            torch.cuda.synchronize()
+            t0 = time.time()
+            for _ in range(reps):
+                fn()
+            torch.cuda.synchronize()
+            return (time.time() - t0) / reps
+
+        def up():
+            with torch.cuda.stream(s_up):
+                d_up.copy_(h_up, non_blocking=True)
+
+        def down():
+            with torch.cuda.stream(s_down):
+                h_down.copy_(d_down, non_blocking=True)
+
+        def both():
+            up()
+            down()
+        t_up, t_down, t_both = timed(up), timed(down), timed(both)
+        ub, db = up_n * 2, down_n * 2
+        return {"host_link": {"h2d_gbs": ub / t_up / 1e9, "d2h_gbs": db / t_down / 1e9,
+                              "both_directions_gbs": (ub + db) / t_both / 1e9,
+                              "h2d_bytes": ub, "d2h_bytes": db,
+                              # a step that moves these bytes cannot beat the
+                              # time of the two copies running together
+                              "e2e_bound_tflops": 2.0 * 4096 * 12288 * 5120 / t_both / 1e12}}
 
     def mma_rate(self):
         """Issue rate of back-to-back tcgen05.mma per kind (the library's probe,

@@ -19,7 +19,7 @@ from ._abi import (HQ_MXFP8, HQ_MXFP4, HQ_NVFP4, HQ_STATUS_WAIT_TIMEOUT, HQ_STAT
 
 __all__ = [
     "HQError", "mode_id", "group_size", "sf_bytes", "capabilities", "get_device_status",
-    "set_wait_limit_ns", "selftest_wait_expiry", "probe_mma_rate", "set_gemm_tile_n", "set_gemm_2sm", "hq_quant",
+    "set_wait_limit_ns", "selftest_wait_expiry", "set_fault_injection", "probe_mma_rate", "set_gemm_tile_n", "set_gemm_2sm", "hq_quant",
     "hq_gemm_dense", "hq_gemm_grouped_contig", "hq_gemm_grouped_masked", "hq_swiglu_quant",
     "hq_gemm_dswiglu", "hq_gemm_dswiglu_workspace_size", "hq_gemm_dgeglu", "swiglu_kb_dim",
     "hq_prefill_permute", "hq_prefill_permute_workspace_size", "hq_gemm_grouped_rows",
@@ -119,6 +119,12 @@ def probe_mma_rate(kind, pair=True, n=256, iters=4096, stream=None):
     return {"kind": kind, "pair": bool(pair), "n": n, "cycles_per_mma": med,
             "flop_per_clk_sm": 2.0 * 128 * n * kk / med, "sm_mhz": float(mhz[mhz.numel() // 2]),
             "ctas": int(cyc.numel())}
+
+
+def set_fault_injection(skip_stage):
+    """Test aid: the pair GEMM's first cluster withholds the arrival of its
+    skip_stage-th operand stage (-1: off)."""
+    _check(_abi.load().hq_set_fault_injection(int(skip_stage)), "hq_set_fault_injection")
 
 
 def set_gemm_tile_n(tile_n):

@@ -50,6 +50,7 @@ SIGNATURES = {
     "hq_set_wait_limit_ns": (c_i32, [c_u64]),
     "hq_selftest_wait_expiry": (c_i32, [c_u64, c_p]),
     "hq_probe_mma_rate": (c_i32, [c_i32, c_i32, c_i32, c_i32, c_p, c_p]),
+    "hq_set_fault_injection": (c_i32, [c_i64]),
     "hq_set_gemm_tile_n": (c_i32, [c_i32]),
     "hq_set_gemm_2sm": (c_i32, [c_i32]),
     "hq_quant": (c_i32, [c_p, c_i64, c_i64, c_i32, c_i32, c_p, c_p, c_p, c_i32, c_p]),

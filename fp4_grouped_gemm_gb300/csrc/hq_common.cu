@@ -21,10 +21,12 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 uint32_t* g_status_ptr[kMaxDevices] = {};
+void* g_status_ctx[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 std::atomic<uint64_t> g_wait_limit_ns{1000000000ull};
 std::atomic<int> g_tile_n{0};
 std::atomic<int> g_use_2sm{1};
+std::atomic<int64_t> g_inject_skip{-1};
 using EncodeFn = decltype(&cuTensorMapEncodeTiled);
 EncodeFn g_encode = nullptr;
 
@@ -35,14 +37,34 @@ int current_device() {
 }
 }  // namespace
 
+void* current_context() {
+  using CtxFn = CUresult (*)(CUcontext*);
+  static CtxFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<CtxFn>(nullptr);
+    return reinterpret_cast<CtxFn>(f);
+  }();
+  CUcontext c = nullptr;
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
 uint32_t* status_word_ptr() {
   const int dev = current_device();
   if (dev < 0) return nullptr;
+  void* ctx = current_context();
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_status_ptr[dev]) {
+  // the cached address belongs to the context it was resolved in: resolve it
+  // again when another context is current on this device
+  if (!g_status_ptr[dev] || g_status_ctx[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
     g_status_ptr[dev] = static_cast<uint32_t*>(p);
+    g_status_ctx[dev] = ctx;
   }
   return g_status_ptr[dev];
 }
@@ -50,6 +72,8 @@ uint32_t* status_word_ptr() {
 uint64_t wait_limit_ns() { return g_wait_limit_ns.load(); }
 
 int forced_tile_n() { return g_tile_n.load(); }
+
+int64_t fault_injection_stage() { return g_inject_skip.load(); }
 
 bool use_2sm() { return g_use_2sm.load() != 0; }
 
@@ -429,6 +453,12 @@ int hq_set_gemm_tile_n(int tile_n) {
 int hq_set_gemm_2sm(int enable) {
   if (enable != 0 && enable != 1 && enable != 256 && enable != 384) return HQ_ERR_INVALID;
   hq::g_use_2sm.store(enable);
+  return HQ_OK;
+}
+
+int hq_set_fault_injection(int64_t skip_stage) {
+  if (skip_stage < -1) return HQ_ERR_INVALID;
+  hq::g_inject_skip.store(skip_stage);
   return HQ_OK;
 }
 

@@ -65,6 +65,10 @@ struct GemmParams {
   int64_t S;                 // scale columns = k / group
   int64_t sfb_group_bytes;   // ceil(n/128)*128*S
   uint64_t wait_limit_ns;
+  // test aid (hq_set_fault_injection): cluster 0's producer withholds the
+  // arrival on the "full" barrier of this stage (count of stages it issued);
+  // -1 = never
+  int64_t inject_skip;
   // dGLU epilogues only (cuDNN "Grouped GEMM + dGLU (SM100)", block-scaled
   // contract): out is not used; D_row = dGLU(alpha_g^2 acc, C) instead
   const uint16_t* c;         // [a_rows, 2n] BF16 forward intermediate
@@ -1264,6 +1268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0, filled_a = 0, filled_s = 0, par_a = 0, par_s = 0;
+      int64_t issued = 0;  // stages issued by this producer
       bool ok = true;
       for (int64_t t = cluster_id; ok && t < total; t += num_clusters) {
         const PairTile pt = pair_tile(t);
@@ -1287,8 +1292,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           int atoms = atoms_total - kb * C::ATOMS;
           atoms = atoms < C::ATOMS ? atoms : C::ATOMS;
           // both CTAs' A / B tiles complete on the even CTA's full barrier,
-          // which expects the bytes of the pair
-          if (leader) mbar_arrive_expect_tx(full_bar(stage), pair_bytes);
+          // which expects the bytes of the pair (a fault-injection test
+          // withholds this arrival once: the stage never completes and the
+          // MMA issuer's bounded wait expires)
+          if (leader && !(cluster_id == 0 && issued == p.inject_skip))
+            mbar_arrive_expect_tx(full_bar(stage), pair_bytes);
+          ++issued;
           const uint32_t fb = mapa_shared(full_bar(stage), 0);
           if (has_a)
             tma_load_2d_pair(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, fb, kb * kBKBytes,
@@ -1876,6 +1885,7 @@ GemmParams base_params(const uint8_t* sfa, const uint8_t* sfb, const float* alph
   p.sfb_group_bytes = (n + 127) / 128 * 128 * (k / gs);
   p.gs.status = status_word_ptr();
   p.wait_limit_ns = wait_limit_ns();
+  p.inject_skip = fault_injection_stage();
   return p;
 }
 

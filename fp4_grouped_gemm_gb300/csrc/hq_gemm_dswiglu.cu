@@ -580,18 +580,22 @@ static __device__ __align__(256) float g_dswiglu_scratch[kNoAllocScratchFloats];
 constexpr int kMaxDev = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_addr[kMaxDev] = {};
+void* g_scratch_ctx[kMaxDev] = {};
 
 // Device address of g_dswiglu_scratch on the current device.  Host code must
 // not use the symbol itself (on the host it names a stand-in, not device
-// memory); the address is resolved once per device, with that device current.
+// memory); the address is resolved once per device, with that device current,
+// and again if another context has become current on the device since.
 void* scratch_address() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+  void* ctx = current_context();
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  if (!g_scratch_addr[dev] || g_scratch_ctx[dev] != ctx) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_dswiglu_scratch) != cudaSuccess || !ptr) return nullptr;
     g_scratch_addr[dev] = ptr;
+    g_scratch_ctx[dev] = ctx;
   }
   return g_scratch_addr[dev];
 }
@@ -605,7 +609,8 @@ extern "C" int hq_gemm_dswiglu_noalloc(const hq_bf16* a, const hq_bf16* b, const
                                        float* dprob, hq_bf16* dbias, int64_t m, int64_t n,
                                        int64_t k, int sm_count, hq_stream_t s) {
   if (L < 1 || n <= 0) return HQ_ERR_INVALID;
-  if (dbias && static_cast<uint64_t>(L) * static_cast<uint64_t>(2 * n) > hq::kNoAllocScratchFloats)
+  // L * 2n in unsigned arithmetic: no signed overflow for any n > 0
+  if (dbias && static_cast<uint64_t>(L) * 2u * static_cast<uint64_t>(n) > hq::kNoAllocScratchFloats)
     return HQ_ERR_UNSUPPORTED;
   void* ws = nullptr;
   size_t ws_bytes = 0;

@@ -12,8 +12,11 @@
 
 namespace hq {
 
-// Device address of the status word on the current device (resolved once per
-// device with cudaGetSymbolAddress); nullptr on failure.
+// The CUDA context current on the calling thread (driver handle), or nullptr.
+void* current_context();
+
+// Device address of the status word on the current device (resolved with
+// cudaGetSymbolAddress once per device and context); nullptr on failure.
 uint32_t* status_word_ptr();
 
 // Current limit for bounded pipeline waits, in nanoseconds.
@@ -21,6 +24,10 @@ uint64_t wait_limit_ns();
 
 // Number of SMs of the current device (cached per device); 0 on failure.
 int num_sms();
+
+// Stage whose "full" arrival the pair GEMM's first producer withholds (-1:
+// none; set by hq_set_fault_injection for the abort-path test).
+int64_t fault_injection_stage();
 
 // Forced GEMM tile width (0 = automatic).
 int forced_tile_n();

@@ -15,6 +15,13 @@
  *    allocates no memory; where a call needs scratch space the caller passes
  *    it (sized by a *_workspace_size query), so it can be allocated before a
  *    CUDA-graph capture (FlashRT fp4-gemm notes, large-M tier workspace).
+ *    Host memory is not a supported argument, pinned (cudaHostAlloc,
+ *    cudaHostRegister) or pageable, even on a platform whose GPU can address
+ *    it (coherent host links): the GEMMs read their operands through TMA
+ *    tensor maps and the other kernels assume device-memory bandwidth and
+ *    alignment.  The host does not check where a pointer points (that would
+ *    cost a driver query per pointer and call); passing host memory is a
+ *    precondition violation.  Move host data with cudaMemcpyAsync first.
  *  - Every call is asynchronous on the given stream (NULL = legacy default
  *    stream).  The library keeps no pointer after it returns, but every
  *    buffer must stay alive and unchanged until the stream reaches the work.
@@ -131,6 +138,18 @@ int hq_set_wait_limit_ns(uint64_t ns);
  * HQ_STATUS_WAIT_TIMEOUT is set in the device status word and the kernel
  * returns; the context stays usable.  No GPU fault is involved. */
 int hq_selftest_wait_expiry(uint64_t limit_ns, hq_stream_t s);
+
+/* Test aid for the GEMMs' abort path (no counterpart on the pages): from
+ * the next launch on, the two-CTA pair GEMM kernel's first cluster withholds
+ * the arrival that completes its skip_stage-th operand stage (counted from 0
+ * over the stages its producer issues), so the MMA issuer's bounded wait
+ * expires: the kernel sets HQ_STATUS_WAIT_TIMEOUT, stops every role, drains
+ * its copies and MMAs with bounded waits, frees TMEM and returns.  Tiles the
+ * aborted cluster had not finished are not written; nothing outside the
+ * output's valid rows is written.  -1 (the default) turns it off.  Nothing
+ * faults or hangs: the failure is a barrier that nothing completes.
+ * Returns HQ_ERR_INVALID for skip_stage < -1. */
+int hq_set_fault_injection(int64_t skip_stage);
 
 /* Tensor-core issue-rate probe (a measurement aid, no counterpart on the
  * pages): every CTA of one wave (one per SM, or one two-CTA cluster per SM
@@ -468,8 +487,10 @@ int hq_gemm_dglu_discrete(const hq_bf16 *a, const int64_t *b_ptrs, const hq_bf16
  * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
  *
  * The first call on a device resolves the scratch array's device address
- * (once per device, with that device current); make that first call before
- * any stream capture.  Every call clears the part of the scratch it uses
+ * (once per device and CUDA context, with that device current); make that
+ * first call before any stream capture.  Calling cudaDeviceReset while the
+ * library is loaded is not supported: the library keeps per-device state
+ * (resolved addresses, kernel attributes) that a reset discards.  Every call clears the part of the scratch it uses
  * before accumulating into it, because the array keeps the previous call's
  * contents.  All calls share the one array, so two calls whose work overlaps
  * on the GPU (different streams, no ordering between them) race on it and

@@ -215,6 +215,19 @@ def test_permute_rejects_bad_arguments(lib):
     assert call(a13=None) == _abi.HQ_ERR_INVALID                   # token_nums
 
 
+def test_noalloc_dswiglu_rejects_oversized_scratch(lib):
+    """The allocation-free dSwiGLU checks L * 2n against its fixed scratch
+    before anything else, without overflowing for any n."""
+    p = ctypes.c_void_p(4096)
+    for L, n in ((1, 131073), (2, 65600), (1, (1 << 62) + 1), (1024, 1 << 40)):
+        assert lib.hq_gemm_dswiglu_noalloc(p, p, p, p, L, p, p, p, p, p, p, 256, n, 256, -1, None) \
+            == _abi.HQ_ERR_UNSUPPORTED
+    assert lib.hq_gemm_dswiglu_noalloc(p, p, p, p, 0, p, p, p, p, p, p, 256, 128, 256, -1, None) \
+        == _abi.HQ_ERR_INVALID
+    assert lib.hq_gemm_dswiglu_noalloc(p, p, p, p, 1, p, p, p, p, p, p, 256, -2, 256, -1, None) \
+        == _abi.HQ_ERR_INVALID
+
+
 def test_knobs_validate(lib):
     assert lib.hq_set_gemm_tile_n(96) == _abi.HQ_ERR_INVALID
     assert lib.hq_set_gemm_tile_n(0) == _abi.HQ_OK
