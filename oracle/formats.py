@@ -8,11 +8,15 @@ Sources (page titles and sections):
     w4a4-nvfp4.
   * cuDNN frontend "Grouped GEMM + dGLU (SM100)", Data Types table -- the same
     element/scale pairings (float8_e4m3fn with float8_e8m0fnu, E2M1 with
-    float8_e4m3fn scales).
+    float8_e4m3fn scales), and float8_e5m2 as the other MXFP8 operand type
+    and FP8 output type.
 
 The bit layouts are the standard OCP microscaling ones the names denote:
   E4M3 (e4m3fn): sign | 4 exponent bits (bias 7) | 3 mantissa bits; exponent 0
     is subnormal (m * 2^-9); S.1111.111 is NaN; no infinities; max 448.
+  E5M2: sign | 5 exponent bits (bias 15) | 2 mantissa bits; exponent 0 is
+    subnormal (m * 2^-16); exponent 31 holds the infinities and NaNs; max
+    finite 57344.
   E2M1: sign | 2 exponent bits (bias 1) | 1 mantissa bit; values
     {0, 0.5, 1, 1.5, 2, 3, 4, 6}.
   UE8M0: unsigned biased exponent, value 2^(b-127); 0xFF is NaN.
@@ -44,6 +48,17 @@ def _e4m3_value(code: int) -> float:
     return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
 
 
+def _e5m2_value(code: int) -> float:
+    sign = -1.0 if code & 0x80 else 1.0
+    e = (code >> 2) & 0x1F
+    m = code & 0x3
+    if e == 0x1F:
+        return sign * float("inf") if m == 0 else float("nan")
+    if e == 0:
+        return sign * m * 2.0 ** -16
+    return sign * (1.0 + m / 4.0) * 2.0 ** (e - 15)
+
+
 def _e2m1_value(code: int) -> float:
     sign = -1.0 if code & 0x8 else 1.0
     e = (code >> 1) & 0x3
@@ -54,12 +69,15 @@ def _e2m1_value(code: int) -> float:
 
 
 E4M3_TABLE = np.array([_e4m3_value(c) for c in range(256)], dtype=np.float64)
+E5M2_TABLE = np.array([_e5m2_value(c) for c in range(256)], dtype=np.float64)
 E2M1_TABLE = np.array([_e2m1_value(c) for c in range(16)], dtype=np.float64)
 E4M3_MAX = 448.0
+E5M2_MAX = 57344.0
 E2M1_MAX = 6.0
 
 # positive finite codes in increasing value order (code == index for both)
 _E4M3_POS = E4M3_TABLE[:0x7F].copy()  # codes 0x00..0x7E
+_E5M2_POS = E5M2_TABLE[:0x7C].copy()  # codes 0x00..0x7B (finite)
 _E2M1_POS = E2M1_TABLE[:8].copy()     # codes 0..7
 
 
@@ -85,6 +103,11 @@ def encode_e4m3(v):
     return _encode_by_table(v, _E4M3_POS, E4M3_MAX, 0x80)
 
 
+def encode_e5m2(v):
+    """float -> float8_e5m2 code (uint8), RNE ties-to-even, satfinite."""
+    return _encode_by_table(v, _E5M2_POS, E5M2_MAX, 0x80)
+
+
 def encode_e2m1(v):
     """float -> E2M1 code in the low 4 bits (uint8), RNE ties-to-even, satfinite."""
     return _encode_by_table(v, _E2M1_POS, E2M1_MAX, 0x8)
@@ -92,6 +115,10 @@ def encode_e2m1(v):
 
 def decode_e4m3(code):
     return E4M3_TABLE[np.asarray(code, dtype=np.uint8)]
+
+
+def decode_e5m2(code):
+    return E5M2_TABLE[np.asarray(code, dtype=np.uint8)]
 
 
 def decode_e2m1(code):

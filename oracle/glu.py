@@ -49,6 +49,9 @@ Readings (also listed in the design notes):
       gate_up = alpha_g * (A . B_g^T) kept in float (not rounded to BF16 as
       the unfused GEMM output is), y = up * silu(gate) as S1, quantised as
       fused_swiglu_quant; rows past padded_offsets[L-1] are not written.
+  Q4  FP8 output as float8_e5m2 (the cuDNN page's Data Types table lists it
+      beside float8_e4m3fn for d_dtype): Q1 / Q2 with rcp_max =
+      fp32(1/57344) and E5M2 codes (RNE ties-to-even, saturating at 57344).
   Q3  amax (BF16 D output, shape (L, 2)): amax[g, 0] = max |D| over group g's
       rows and the gate columns, amax[g, 1] over the input (up) columns; 0 for
       an empty group.
@@ -298,35 +301,48 @@ def dswiglu(a, b, c, padded_offsets, alpha, beta, prob):
     }
 
 
-def quantize_rows_fp8(D, norm_const=1.0):
-    """Step-3 row quantisation of D [rows, cols] (cols % 32 == 0) under Q1.
+def _fp8_rule(elem):
+    """(scale-byte rule, element encoder) of an FP8 output type (Q1, Q4)."""
+    if elem == "e4m3":
+        return quant.scale_byte_mxfp8, formats.encode_e4m3
+    if elem == "e5m2":
+        return quant.scale_byte_mxfp8_e5m2, formats.encode_e5m2
+    raise ValueError(elem)
 
-    Returns (codes uint8 [rows, cols] E4M3, sf uint8 [rows, cols / 32]).
+
+def quantize_rows_fp8(D, norm_const=1.0, elem="e4m3"):
+    """Step-3 row quantisation of D [rows, cols] (cols % 32 == 0) under Q1
+    (E4M3 codes) or Q4 (E5M2 codes).
+
+    Returns (codes uint8 [rows, cols], sf uint8 [rows, cols / 32]).
     """
+    scale_byte, encode = _fp8_rule(elem)
     D = np.asarray(D, dtype=np.float32)
     rows, cols = D.shape
     g = np.float32(norm_const)
     amax = np.max(np.abs(D.reshape(rows, cols // 32, 32)), axis=2)
-    sf = quant.scale_byte_mxfp8(amax, g)
+    sf = scale_byte(amax, g)
     y = (D * g).astype(np.float32).astype(np.float64)          # fp32 product
     mult = np.ldexp(1.0, 127 - sf.astype(np.int64))
-    codes = formats.encode_e4m3(y.reshape(rows, cols // 32, 32) * mult[..., None])
+    codes = encode(y.reshape(rows, cols // 32, 32) * mult[..., None])
     return codes.reshape(rows, cols), sf
 
 
-def quantize_cols_fp8(D, norm_const=1.0):
-    """Step-3 column quantisation of D [rows, cols] (rows % 32 == 0) under Q2.
+def quantize_cols_fp8(D, norm_const=1.0, elem="e4m3"):
+    """Step-3 column quantisation of D [rows, cols] (rows % 32 == 0) under Q2
+    (E4M3 codes) or Q4 (E5M2 codes).
 
-    Returns (codes uint8 [rows, cols] E4M3, sf uint8 [cols, rows / 32]).
+    Returns (codes uint8 [rows, cols], sf uint8 [cols, rows / 32]).
     """
+    scale_byte, encode = _fp8_rule(elem)
     D = np.asarray(D, dtype=np.float32)
     rows, cols = D.shape
     g = np.float32(norm_const)
     amax = np.max(np.abs(D.reshape(rows // 32, 32, cols)), axis=1)   # [rows/32, cols]
-    sf = quant.scale_byte_mxfp8(amax, g)                              # [rows/32, cols]
+    sf = scale_byte(amax, g)                                          # [rows/32, cols]
     y = (D * g).astype(np.float32).astype(np.float64)
     mult = np.ldexp(1.0, 127 - sf.astype(np.int64))
-    codes = formats.encode_e4m3(y.reshape(rows // 32, 32, cols) * mult[:, None, :])
+    codes = encode(y.reshape(rows // 32, 32, cols) * mult[:, None, :])
     return codes.reshape(rows, cols), np.ascontiguousarray(sf.T)
 
 

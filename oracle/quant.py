@@ -28,6 +28,10 @@ design notes):
       R2's power-of-two round-up, byte = clamp(ceil(log2 s) + 127, 0, 254);
       elements are E2M1(x * 2^(127 - byte)) (an exact product), packed two
       per byte as NVFP4's.
+  R7  MXFP8 with E5M2 elements (the other MXFP8 operand type of the cuDNN
+      page's Data Types table): R1 with g = 1 and rcp_max = fp32(1/57344),
+      R2's power-of-two round-up; elements E5M2(x * 2^(127 - byte)) (an
+      exact product), RNE ties-to-even, saturating at 57344.
   R4  SfAtom byte offset of scale (row r, scale column s), S columns:
         ((r // 128) * (S // 4) + s // 4) * 512
         + (r % 32) * 16 + ((r % 128) // 32) * 4 + (s % 4)
@@ -44,11 +48,13 @@ from . import formats
 MODE_MXFP8 = "mxfp8"
 MODE_NVFP4 = "nvfp4"
 MODE_MXFP4 = "mxfp4"
+MODE_MXFP8_E5M2 = "mxfp8_e5m2"
 
-GROUP_SIZE = {MODE_MXFP8: 32, MODE_NVFP4: 16, MODE_MXFP4: 32}
+GROUP_SIZE = {MODE_MXFP8: 32, MODE_NVFP4: 16, MODE_MXFP4: 32, MODE_MXFP8_E5M2: 32}
 
 RCP_E4M3_MAX = np.float32(1.0) / np.float32(448.0)
 RCP_E2M1_MAX = np.float32(1.0) / np.float32(6.0)
+RCP_E5M2_MAX = np.float32(1.0) / np.float32(57344.0)
 
 
 # --------------------------------------------------------------------------- #
@@ -69,6 +75,11 @@ def _ue8m0_round_up(amax, rcp_max, g=np.float32(1.0)):
 def scale_byte_mxfp8(amax, g=np.float32(1.0)):
     """UE8M0 scale byte for groups with absolute maximum ``amax`` (R1, R2)."""
     return _ue8m0_round_up(amax, RCP_E4M3_MAX, g)
+
+
+def scale_byte_mxfp8_e5m2(amax, g=np.float32(1.0)):
+    """UE8M0 scale byte for E5M2 elements (R7)."""
+    return _ue8m0_round_up(amax, RCP_E5M2_MAX, g)
 
 
 def scale_byte_mxfp4(amax):
@@ -114,6 +125,14 @@ def quantize(x, mode, global_scale=None):
         y = xg.astype(np.float64) * mult[..., None]       # exact power-of-two scaling
         q = formats.encode_e4m3(y).reshape(m, k)
         return q, sf
+    if mode == MODE_MXFP8_E5M2:
+        if global_scale is not None:
+            raise ValueError("MXFP8 uses no global scale")
+        sf = scale_byte_mxfp8_e5m2(amax)
+        mult = np.ldexp(1.0, 127 - sf.astype(np.int64))  # 2^(127 - byte)
+        y = xg.astype(np.float64) * mult[..., None]       # exact power-of-two scaling
+        q = formats.encode_e5m2(y).reshape(m, k)
+        return q, sf
     if mode == MODE_MXFP4:
         if global_scale is not None:
             raise ValueError("MXFP4 uses no global scale")
@@ -136,6 +155,9 @@ def dequantize(q, sf_plain, mode):
     gs = GROUP_SIZE[mode]
     if mode == MODE_MXFP8:
         vals = formats.decode_e4m3(q)
+        scl = formats.decode_ue8m0(sf_plain)
+    elif mode == MODE_MXFP8_E5M2:
+        vals = formats.decode_e5m2(q)
         scl = formats.decode_ue8m0(sf_plain)
     elif mode == MODE_NVFP4:
         vals = formats.decode_e2m1(formats.unpack_e2m1(q))

@@ -118,3 +118,54 @@ def test_fp4_packing_even_index_low_nibble():
     packed = formats.pack_e2m1(codes)
     assert packed.tolist() == [[0x21, 0x43, 0x0F]]
     assert np.array_equal(formats.unpack_e2m1(packed), codes)
+
+
+# --------------------------------------------------------------------------- #
+# E5M2 (float8_e5m2): bias 15, subnormals m * 2^-16, max finite 57344
+# --------------------------------------------------------------------------- #
+
+
+def test_e5m2_table_matches_torch_decoder():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e5m2).float().double().numpy()
+    ours = formats.E5M2_TABLE
+    assert np.array_equal(np.isnan(ref), np.isnan(ours))
+    fin = np.isfinite(ref)
+    assert np.array_equal(fin, np.isfinite(ours))
+    assert np.array_equal(ref[fin], ours[fin])
+    assert set(np.nonzero(~fin)[0].tolist()) == {0x7C, 0x7D, 0x7E, 0x7F, 0xFC, 0xFD, 0xFE, 0xFF}
+
+
+@pytest.mark.parametrize("code,value", [
+    (0x00, 0.0), (0x01, 2.0 ** -16), (0x03, 3 * 2.0 ** -16), (0x04, 2.0 ** -14),
+    (0x3C, 1.0), (0x3D, 1.25), (0x3E, 1.5), (0x3F, 1.75), (0x40, 2.0), (0x7B, 57344.0),
+    (0xBC, -1.0), (0xFB, -57344.0),
+])
+def test_e5m2_hand_values(code, value):
+    assert formats.decode_e5m2(code) == value
+    assert formats.encode_e5m2(value) == code
+
+
+def test_e5m2_encode_matches_torch_on_all_bf16_in_range():
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    v = bits.view(torch.bfloat16).float()
+    v = v[torch.isfinite(v) & (v.abs() <= 57344)]
+    ref = v.to(torch.float8_e5m2).view(torch.uint8).numpy()
+    assert np.array_equal(ref, formats.encode_e5m2(v.double().numpy()))
+
+
+def test_e5m2_midpoints_tie_to_even_code_like_torch():
+    pos = formats.E5M2_TABLE[:0x7C]
+    mids = (pos[:-1] + pos[1:]) / 2.0            # exact in float32
+    vals = np.concatenate([mids, -mids])
+    ref = torch.from_numpy(vals.astype(np.float32)).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    assert np.array_equal(ref, formats.encode_e5m2(vals))
+    # by hand: 1.125 lies between 1.0 (0x3C, even) and 1.25 (0x3D) -> 0x3C;
+    # 1.375 between 1.25 (0x3D) and 1.5 (0x3E, even) -> 0x3E
+    assert formats.encode_e5m2(1.125) == 0x3C and formats.encode_e5m2(1.375) == 0x3E
+
+
+def test_e5m2_saturates_and_keeps_the_sign_of_zero():
+    assert formats.encode_e5m2(61440.0) == 0x7B      # the midpoint to the next binade saturates
+    assert formats.encode_e5m2(1.0e9) == 0x7B and formats.encode_e5m2(-1.0e9) == 0xFB
+    assert formats.encode_e5m2(-2.0 ** -20) == 0x80

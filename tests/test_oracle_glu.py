@@ -17,7 +17,7 @@ import pytest
 import scipy.special
 import torch
 
-from oracle import glu, quant
+from oracle import formats, glu, quant
 
 
 def rng_(seed):
@@ -285,3 +285,24 @@ def test_fused_up_proj_matches_the_two_step_path_on_exact_values():
     # y64 is up * silu(gate) of the exact gate_up
     g, u = gu[:, :H], gu[:, H:]
     assert np.allclose(out["y64"], u * g / (1 + np.exp(-g)), rtol=1e-14, atol=0)
+
+
+def test_row_quantiser_e5m2_unit_norm_equals_the_e5m2_quantiser():
+    """Reading Q4: the E5M2 Step-3 row rule with norm_const 1 is the MXFP8
+    E5M2 quantiser (reading R7) on the same rows."""
+    rng = np.random.default_rng(3)
+    D = (rng.standard_normal((8, 128)) * np.exp2(rng.integers(-6, 7, (8, 1)))).astype(np.float32)
+    c1, s1 = glu.quantize_rows_fp8(D, 1.0, elem="e5m2")
+    c2, s2 = quant.quantize(D, "mxfp8_e5m2")
+    assert np.array_equal(c1, c2) and np.array_equal(s1, s2)
+
+
+def test_row_quantiser_e5m2_norm_const_by_hand():
+    # norm_const 4, amax 3: s = fp32(12 * fp32(1/57344)) in (2^-13, 2^-12] -> byte 115;
+    # D = 3 -> 12 * 2^12 = 49152 = E5M2 0x7A; D = -0.75 -> -3 * 2^12 = -12288 = 0xF2
+    D = np.zeros((1, 32), np.float32)
+    D[0, 0], D[0, 1] = 3.0, -0.75
+    c, s = glu.quantize_rows_fp8(D, 4.0, elem="e5m2")
+    assert s.tolist() == [[115]]
+    assert c[0, 0] == 0x7A and c[0, 1] == 0xF2
+    assert formats.decode_e5m2(0x7A) == 49152.0 and formats.decode_e5m2(0xF2) == -12288.0

@@ -294,6 +294,34 @@ def column_blocks_of_16(monkeypatch):
     monkeypatch.setattr(glu, "quantize_cols_fp8", qc)
 
 
+def e5m2_ties_away(monkeypatch):
+    def enc(v):  # nearest E5M2 magnitude, ties away from zero
+        v = np.asarray(v, dtype=np.float64)
+        pos = formats.E5M2_TABLE[:0x7C]
+        a = np.minimum(np.abs(v), formats.E5M2_MAX)
+        hi = np.clip(np.searchsorted(pos, a, side="left"), 0, len(pos) - 1)
+        lo = np.clip(hi - 1, 0, len(pos) - 1)
+        code = np.where(np.abs(pos[hi] - a) <= np.abs(a - pos[lo]), hi, lo).astype(np.uint8)
+        return np.where(np.signbit(v), code | 0x80, code).astype(np.uint8)
+    monkeypatch.setattr(formats, "encode_e5m2", enc)
+
+
+def e5m2_rcp_max_of_e4m3(monkeypatch):
+    monkeypatch.setattr(quant, "RCP_E5M2_MAX", quant.RCP_E4M3_MAX)
+
+
+def e5m2_bias_16(monkeypatch):
+    def val(code):
+        sign = -1.0 if code & 0x80 else 1.0
+        e, m = (code >> 2) & 0x1F, code & 0x3
+        if e == 0x1F:
+            return sign * float("inf") if m == 0 else float("nan")
+        return sign * (m * 2.0 ** -17 if e == 0 else (1.0 + m / 4.0) * 2.0 ** (e - 16))
+    table = np.array([val(c) for c in range(256)], dtype=np.float64)
+    monkeypatch.setattr(formats, "E5M2_TABLE", table)
+    monkeypatch.setattr(formats, "_E5M2_POS", table[:0x7C].copy())
+
+
 CASES = {
     "e2m1 ties away from zero": (e2m1_ties_away, [tfm.test_e2m1_rounding_points, tq.test_round_trip_error_bound]),
     "fp4 nibbles swapped": (nibbles_swapped, [tfm.test_fp4_packing_even_index_low_nibble,
@@ -338,6 +366,11 @@ CASES = {
     "permute overflow not flagged": (permute_overflow_unflagged, [tpm.test_overflow_and_bad_ids_are_dropped_and_flagged]),
     "column scales over 16-row blocks": (column_blocks_of_16, [tgl.test_column_quantiser_by_hand,
                                                                tgl.test_column_quantiser_is_the_row_quantiser_of_the_transpose]),
+    "e5m2 ties away from zero": (e5m2_ties_away, [tfm.test_e5m2_midpoints_tie_to_even_code_like_torch]),
+    "mxfp8 e5m2 scale with the E4M3 rcp_max": (e5m2_rcp_max_of_e4m3, [tq.test_mxfp8_e5m2_amax_57344_gives_unit_scale,
+                                                                      tq.test_mxfp8_e5m2_amax_1,
+                                                                      tgl.test_row_quantiser_e5m2_norm_const_by_hand]),
+    "E5M2 exponent bias 16": (e5m2_bias_16, [tfm.test_e5m2_table_matches_torch_decoder, tfm.test_e5m2_hand_values]),
 }
 
 

@@ -219,3 +219,44 @@ def test_group_wise_quant_rowmajor_variant():
     _, sf = quant.group_wise_quant(x, "mxfp8", use_swizzle=False)
     assert sf.size == 128 * 2
     assert sf.reshape(128, 2)[2, 1] == 119 and sf.sum() == 119
+
+
+# --------------------------------------------------------------------------- #
+# MXFP8 with E5M2 elements (reading R7): UE8M0 of amax * fp32(1/57344)
+# rounded up to a power of two; elements E5M2(x * 2^(127 - byte))
+# --------------------------------------------------------------------------- #
+
+
+def test_mxfp8_e5m2_amax_57344_gives_unit_scale():
+    # 57344 * fp32(1/57344) is exactly 1.0 in float32 -> byte 127, element 0x7B
+    assert np.float32(57344.0) * quant.RCP_E5M2_MAX == np.float32(1.0)
+    x = np.zeros((1, 32), np.float32)
+    x[0, 3] = 57344.0
+    x[0, 4] = -1.0
+    q, sf = quant.quantize(x, "mxfp8_e5m2")
+    assert sf.tolist() == [[127]]
+    assert q[0, 3] == 0x7B and q[0, 4] == 0xBC and q[0, 0] == 0x00
+
+
+def test_mxfp8_e5m2_amax_1():
+    # s = fp32(1/57344) = 2^-15.81 -> rounded up to 2^-15 -> byte 112; the
+    # element 1.0 is scaled by 2^15 and encodes 32768 exactly (0x78)
+    x = np.full((1, 32), 0.5, np.float32)
+    x[0, 0] = 1.0
+    q, sf = quant.quantize(x, "mxfp8_e5m2")
+    assert sf.tolist() == [[112]]
+    assert formats.decode_e5m2(q[0, 0]) == 32768.0 and formats.decode_e5m2(q[0, 1]) == 16384.0
+
+
+def test_mxfp8_e5m2_round_trip_bound_and_torch_cast():
+    rng = np.random.default_rng(7)
+    x = torch.from_numpy(rng.standard_normal((16, 256)).astype(np.float32)).to(torch.bfloat16).float().numpy()
+    q, sf = quant.quantize(x, "mxfp8_e5m2")
+    deq = quant.dequantize(q, sf, "mxfp8_e5m2")
+    scale = np.repeat(formats.decode_ue8m0(sf), 32, axis=1)
+    # half an E5M2 step: 2^-3 relative in the normal range, 2^-17 * scale below it
+    assert (np.abs(deq - x) <= 2.0 ** -3 * np.abs(x) + 2.0 ** -17 * scale).all()
+    # the elements are torch's E5M2 cast of the exactly scaled values
+    y = torch.from_numpy((x.reshape(16, 8, 32) * np.ldexp(1.0, 127 - sf.astype(np.int64))[..., None])
+                         .reshape(16, 256).astype(np.float32))
+    assert np.array_equal(y.to(torch.float8_e5m2).view(torch.uint8).numpy(), q)
