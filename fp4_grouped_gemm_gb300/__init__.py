@@ -29,8 +29,10 @@ __all__ = [
 ]
 
 _MODES = {"mxfp8": HQ_MXFP8, "w8a8-mxfp8": HQ_MXFP8, "mxfp4": HQ_MXFP4, "w4a4-mxfp4": HQ_MXFP4,
-          "nvfp4": HQ_NVFP4, "w4a4-nvfp4": HQ_NVFP4, HQ_MXFP8: HQ_MXFP8, HQ_MXFP4: HQ_MXFP4,
-          HQ_NVFP4: HQ_NVFP4}
+          "nvfp4": HQ_NVFP4, "w4a4-nvfp4": HQ_NVFP4, "mxfp8_e5m2": _abi.HQ_MXFP8_E5M2,
+          HQ_MXFP8: HQ_MXFP8, HQ_MXFP4: HQ_MXFP4, HQ_NVFP4: HQ_NVFP4,
+          _abi.HQ_MXFP8_E5M2: _abi.HQ_MXFP8_E5M2}
+_D_TYPES = {"bf16": _abi.HQ_D_BF16, "f32": _abi.HQ_D_F32, "e4m3": _abi.HQ_D_E4M3, "e5m2": _abi.HQ_D_E5M2}
 
 
 class HQError(RuntimeError):
@@ -139,7 +141,7 @@ def set_gemm_2sm(enable):
 
 
 def _q_shape(rows, k, mode):
-    return (rows, k) if mode_id(mode) == HQ_MXFP8 else (rows, k // 2)
+    return (rows, k) if mode_id(mode) in (HQ_MXFP8, _abi.HQ_MXFP8_E5M2) else (rows, k // 2)
 
 
 def hq_quant(x, mode, use_swizzle=True, global_scale=None, q_out=None, sf_out=None,
@@ -353,16 +355,18 @@ def hq_prefill_permute(x, scale, topk_ids, num_experts, max_token_num, permute_x
 def hq_gemm_dglu_bs(a, sfa, b, sfb, c, padded_offsets, alpha, prob, dprob, k, mode, act="dswiglu",
                     beta=None, dbias=None, d_row=None, fp8_out=False, sfd_row=None, norm_const=None,
                     col_out=False, d_col=None, sfd_col=None, amax=None, workspace=None, sm_count=-1,
-                    stream=None):
+                    stream=None, d_dtype=None):
     """Block-scaled grouped GEMM + dSwiGLU / dGeGLU backward (cuDNN block-scaled
     contract).  a, b quantised as hq_quant writes them (b stacked [L, n, k]);
     c [m, 2n] BF16.  With fp8_out the D_row is E4M3 with UE8M0 SfAtom scales
     (sfd_row) and optional norm_const; col_out (with fp8_out) also produces the
-    column-quantised D_col / SFD_col.  Returns (d_row, sfd_row, dprob, dbias)
-    or, with col_out, (d_row, sfd_row, d_col, sfd_col, dprob, dbias)."""
+    column-quantised D_col / SFD_col.  d_dtype ("bf16", "f32", "e4m3",
+    "e5m2") names the D type explicitly (hq_gemm_dglu_bs_typed; "e4m3" and
+    "e5m2" imply fp8_out).  Returns (d_row, sfd_row, dprob, dbias) or, with
+    col_out, (d_row, sfd_row, d_col, sfd_col, dprob, dbias)."""
     return _dglu_bs(a, sfa, b, sfb, None, None, c, padded_offsets, alpha, prob, dprob, k, mode, act,
                     beta, dbias, d_row, fp8_out, sfd_row, norm_const, col_out, d_col, sfd_col, amax,
-                    workspace, sm_count, stream)
+                    workspace, sm_count, stream, d_dtype)
 
 
 def hq_gemm_dglu_bs_discrete(a, sfa, b_ptrs, sfb_ptrs, c, padded_offsets, alpha, prob, dprob, k, mode,
@@ -378,14 +382,17 @@ def hq_gemm_dglu_bs_discrete(a, sfa, b_ptrs, sfb_ptrs, c, padded_offsets, alpha,
 
 def _dglu_bs(a, sfa, b, sfb, b_ptrs, sfb_ptrs, c, padded_offsets, alpha, prob, dprob, k, mode, act, beta,
              dbias, d_row, fp8_out, sfd_row, norm_const, col_out, d_col, sfd_col, amax, workspace, sm_count,
-             stream):
+             stream, d_dtype=None):
+    if d_dtype is not None:
+        fp8_out = d_dtype in ("e4m3", "e5m2")
     m, two_n = c.shape
     n = two_n // 2
     L = padded_offsets.numel()
     dev = c.device
     discrete = b_ptrs is not None
     if d_row is None:
-        d_row = torch.empty(m, two_n, dtype=torch.uint8 if fp8_out else torch.bfloat16, device=dev)
+        d_row = torch.empty(m, two_n, dtype=torch.uint8 if fp8_out else
+                            (torch.float32 if d_dtype == "f32" else torch.bfloat16), device=dev)
     if fp8_out and sfd_row is None:
         sfd_row = torch.empty(max(sf_bytes(m, two_n, "mxfp8"), 1), dtype=torch.uint8, device=dev)
     if col_out:
@@ -404,15 +411,21 @@ def _dglu_bs(a, sfa, b, sfb, b_ptrs, sfb_ptrs, c, padded_offsets, alpha, prob, d
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     acts = {"dswiglu": 0, "dgeglu": 1}
     lib = _abi.load()
+    typed = d_dtype is not None
     if discrete:
+        if typed:
+            raise ValueError("d_dtype is available with stacked weights (hq_gemm_dglu_bs_typed)")
         fn, name, wargs = lib.hq_gemm_dglu_bs_discrete, "hq_gemm_dglu_bs_discrete", (_ptr(b_ptrs), _ptr(sfb_ptrs))
+    elif typed:
+        fn, name, wargs = lib.hq_gemm_dglu_bs_typed, "hq_gemm_dglu_bs_typed", (_ptr(b), _ptr(sfb))
     else:
         fn, name, wargs = lib.hq_gemm_dglu_bs, "hq_gemm_dglu_bs", (_ptr(b), _ptr(sfb))
+    tail = (_D_TYPES[d_dtype],) if typed else ()
     rc = fn(
         _ptr(a), _ptr(sfa), *wargs, _ptr(c), _ptr(padded_offsets), L, _ptr(alpha),
         _ptr(beta), _ptr(prob), acts[act], _ptr(d_row), _ptr(sfd_row if fp8_out else None),
         _ptr(d_col if col_out else None), _ptr(sfd_col if col_out else None), _ptr(norm_const),
-        _ptr(dprob), _ptr(dbias), _ptr(amax), m, n, k, mode_id(mode), _ptr(workspace),
+        _ptr(dprob), _ptr(dbias), _ptr(amax), m, n, k, mode_id(mode), *tail, _ptr(workspace),
         0 if workspace is None else workspace.numel(), sm_count, _stream(stream))
     _check(rc, name)
     if col_out:

@@ -19,6 +19,12 @@ c_p = ctypes.c_void_p
 HQ_MXFP8 = 0
 HQ_MXFP4 = 1
 HQ_NVFP4 = 2
+HQ_MXFP8_E5M2 = 3
+
+HQ_D_BF16 = 0
+HQ_D_F32 = 1
+HQ_D_E4M3 = 2
+HQ_D_E5M2 = 3
 
 HQ_OK = 0
 HQ_ERR_INVALID = 1
@@ -62,6 +68,9 @@ SIGNATURES = {
     "hq_gemm_dglu_bs": (c_i32, [c_p, c_p, c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_p, c_i32, c_p, c_p,
                                 c_p, c_p, c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_i32, c_p, c_sz,
                                 c_i32, c_p]),
+    "hq_gemm_dglu_bs_typed": (c_i32, [c_p, c_p, c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_p, c_i32, c_p, c_p,
+                                      c_p, c_p, c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_i32, c_i32, c_p,
+                                      c_sz, c_i32, c_p]),
     "hq_gemm_grouped_rows": (c_i32, [c_p, c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_p, c_i64, c_i64,
                                      c_i64, c_i32, c_p, c_sz, c_i32, c_p]),
     "hq_gemm_grouped_rows_workspace_size": (c_sz, [c_i64, c_i32]),

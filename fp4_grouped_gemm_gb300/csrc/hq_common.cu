@@ -419,7 +419,8 @@ const char* hq_status_string(int status) {
 }
 
 size_t hq_sf_bytes(int64_t rows, int64_t k, hq_mode mode) {
-  int64_t gs = (mode == HQ_MXFP8 || mode == HQ_MXFP4) ? 32 : (mode == HQ_NVFP4 ? 16 : 0);
+  int64_t gs = (mode == HQ_MXFP8 || mode == HQ_MXFP4 || mode == HQ_MXFP8_E5M2) ? 32
+              : (mode == HQ_NVFP4 ? 16 : 0);
   if (gs == 0 || rows < 0 || k <= 0 || k % (4 * gs) != 0) return 0;
   return static_cast<size_t>((rows + 127) / 128 * 128) * static_cast<size_t>(k / gs);
 }

@@ -65,6 +65,11 @@ struct GemmParams {
   int64_t S;                 // scale columns = k / group
   int64_t sfb_group_bytes;   // ceil(n/128)*128*S
   uint64_t wait_limit_ns;
+  // bits ORed into every MMA instruction descriptor: the E5M2 operand type of
+  // kind::mxf8f6f4 (A and B format fields), 0 for the other modes
+  uint32_t idesc_ab;
+  // D_row / D_col element type of the dGLU epilogues (kDBf16 .. kDE5M2)
+  int d_type;
   // test aid (hq_set_fault_injection): cluster 0's producer withholds the
   // arrival on the "full" barrier of this stage (count of stages it issued);
   // -1 = never
@@ -102,6 +107,15 @@ struct GemmParams {
 };
 
 enum Epi : int { kEpiGemm = 0, kEpiDSwiGLU = 1, kEpiDGeGLU = 2, kEpiSwiGLUQ = 3 };
+enum DType : int { kDBf16 = HQ_D_BF16, kDF32 = HQ_D_F32, kDE4M3 = HQ_D_E4M3, kDE5M2 = HQ_D_E5M2 };
+
+// The kernel instantiation a mode runs on: E5M2 operands take the MXFP8
+// kernels (same bytes per element, scales and MMA kind; the operand type is
+// in the instruction descriptor bits that base_params sets).
+inline hq_mode kernel_mode(hq_mode mode) { return mode == HQ_MXFP8_E5M2 ? HQ_MXFP8 : mode; }
+inline bool valid_mode(hq_mode mode) {
+  return mode == HQ_MXFP8 || mode == HQ_MXFP4 || mode == HQ_NVFP4 || mode == HQ_MXFP8_E5M2;
+}
 
 // TABLE: entries of the per-CTA group table (0 for the dense GEMM, which
 // needs none and spends the shared memory on a deeper pipeline instead).
@@ -384,8 +398,19 @@ __device__ __forceinline__ void dglu_chunk(const GemmParams& p, const uint32_t (
     }
   }
   const int64_t two_n = 2 * p.n;
+  // FP8 D (Step 3): E4M3 or E5M2 codes, the scale rule's range to match
+  const bool e5 = p.d_type == kDE5M2;
+  const float rcp_max = e5 ? 1.0f / 57344.0f : 1.0f / 448.0f;
+  auto cvt8x2 = [&](float hi, float lo) -> uint32_t { return e5 ? cvt_e5m2x2(hi, lo) : cvt_e4m3x2(hi, lo); };
   if (row_ok) {
-    if (!p.sfd_row) {
+    if (p.d_type == kDF32) {
+      float4* dst = reinterpret_cast<float4*>(p.d_row + (row * two_n + 2 * j0) * 4);
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const float* v = u < 8 ? dg + 4 * u : di + 4 * (u - 8);
+        dst[u] = make_float4(v[0], v[1], v[2], v[3]);
+      }
+    } else if (!p.sfd_row) {
       uint4* dst = reinterpret_cast<uint4*>(p.d_row + (row * two_n + 2 * j0) * 2);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -396,8 +421,8 @@ __device__ __forceinline__ void dglu_chunk(const GemmParams& p, const uint32_t (
                             *reinterpret_cast<uint32_t*>(&b2), *reinterpret_cast<uint32_t*>(&b3));
       }
     } else {
-      // Step 3: per 32 D_row values, s = (norm * amax) / 448 rounded up to a
-      // power of two, codes E4M3((D * norm) * 2^(127 - byte))
+      // Step 3: per 32 D_row values, s = (norm * amax) / 448 (E5M2: 57344)
+      // rounded up to a power of two, codes E4M3 / E5M2 ((D * norm) * 2^(127 - byte))
       uint32_t bytes2 = 0;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -405,15 +430,15 @@ __device__ __forceinline__ void dglu_chunk(const GemmParams& p, const uint32_t (
         float amax = 0.0f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-        const uint32_t byte = ue8m0_ceil(__fmul_rn(__fmul_rn(norm, amax), 1.0f / 448.0f));
+        const uint32_t byte = ue8m0_ceil(__fmul_rn(__fmul_rn(norm, amax), rcp_max));
         const float mult = pow2_neg_unbiased(byte);
         uint32_t w[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const uint32_t lo = cvt_e4m3x2(__fmul_rn(__fmul_rn(v[4 * i + 1], norm), mult),
-                                         __fmul_rn(__fmul_rn(v[4 * i], norm), mult));
-          const uint32_t hi = cvt_e4m3x2(__fmul_rn(__fmul_rn(v[4 * i + 3], norm), mult),
-                                         __fmul_rn(__fmul_rn(v[4 * i + 2], norm), mult));
+          const uint32_t lo = cvt8x2(__fmul_rn(__fmul_rn(v[4 * i + 1], norm), mult),
+                                     __fmul_rn(__fmul_rn(v[4 * i], norm), mult));
+          const uint32_t hi = cvt8x2(__fmul_rn(__fmul_rn(v[4 * i + 3], norm), mult),
+                                     __fmul_rn(__fmul_rn(v[4 * i + 2], norm), mult));
           w[i] = lo | (hi << 16);
         }
         uint4* dst = reinterpret_cast<uint4*>(p.d_row + row * two_n + 2 * j0 + 32 * h);
@@ -469,11 +494,11 @@ __device__ __forceinline__ void dglu_chunk(const GemmParams& p, const uint32_t (
           float mx = fabsf(x);
 #pragma unroll
           for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-          const uint32_t byte = ue8m0_ceil(__fmul_rn(__fmul_rn(norm, mx), 1.0f / 448.0f));
+          const uint32_t byte = ue8m0_ceil(__fmul_rn(__fmul_rn(norm, mx), rcp_max));
           if (lane == 2 * i + u) my_byte[h] = byte;
           y[u] = __fmul_rn(__fmul_rn(x, norm), pow2_neg_unbiased(byte));
         }
-        const uint32_t pair = cvt_e4m3x2(y[1], y[0]);
+        const uint32_t pair = cvt8x2(y[1], y[0]);
         if ((i & 1) == 0) w[i >> 1] = pair;
         else w[i >> 1] |= pair << 16;
       }
@@ -809,7 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           auto issue = [&](int j, uint32_t acc_flag) {
             if (MODE == HQ_MXFP8) {
               // one scale per row per MMA: byte j of the atom's 32-bit columns
-              const uint32_t idesc = C::IDESC_BASE | (static_cast<uint32_t>(j) << 4) |
+              const uint32_t idesc = C::IDESC_BASE | p.idesc_ab | (static_cast<uint32_t>(j) << 4) |
                                      (static_cast<uint32_t>(j) << 29);
               mma_mxf8(d_tmem, ad + 2 * j, bd + 2 * j, idesc,
                        sfa_t | (static_cast<uint32_t>(j) << 30),
@@ -1374,10 +1399,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (MODE == HQ_MXFP8) {
               const uint32_t sel = (static_cast<uint32_t>(j) << 4) | (static_cast<uint32_t>(j) << 29);
               const uint32_t sfs = static_cast<uint32_t>(j) << 30;
-              mma_mxf8_2sm(tmem_base, ad + 2 * j, bd + 2 * j, C::IDESC_BASE | sel, sfa_t | sfs,
+              mma_mxf8_2sm(tmem_base, ad + 2 * j, bd + 2 * j, C::IDESC_BASE | p.idesc_ab | sel, sfa_t | sfs,
                            sfb_t | sfs, acc_flag);
               if (kWide)
-                mma_mxf8_2sm(tmem_base + 256, ad + 2 * j, bd2 + 2 * j, C::IDESC_N128 | sel, sfa_t | sfs,
+                mma_mxf8_2sm(tmem_base + 256, ad + 2 * j, bd2 + 2 * j, C::IDESC_N128 | p.idesc_ab | sel, sfa_t | sfs,
                              sfb2_t | sfs, acc_flag);
             } else if (MODE == HQ_MXFP4) {
               const uint32_t sf = static_cast<uint32_t>(j & 1) * 2u;
@@ -1672,6 +1697,7 @@ int run_bs_2sm(const void* a, const void* b, const GemmParams& p, int sm_count, 
 
 int run_gemm(hq_mode mode, const void* a, const void* b, const GemmParams& p, int sm_count,
              bool pdl, cudaStream_t st) {
+  mode = kernel_mode(mode);
   int bn = forced_tile_n();
   // dense, contiguous and masked problems with whole 256-column tiles
   // (masked: experts padded to a multiple of 256 rows) use the 2-SM kernel
@@ -1725,7 +1751,7 @@ int run_gemm(hq_mode mode, const void* a, const void* b, const GemmParams& p, in
 int check_common(const void* a, const uint8_t* sfa, const void* b, const void* sfb,
                  const float* alpha, const hq_bf16* bias, const void* out, int64_t n, int64_t k,
                  hq_mode mode, bool discrete = false) {
-  if (mode != HQ_MXFP8 && mode != HQ_MXFP4 && mode != HQ_NVFP4) return HQ_ERR_INVALID;
+  if (!valid_mode(mode)) return HQ_ERR_INVALID;
   const int64_t gs = mode == HQ_NVFP4 ? 16 : 32;
   if (n <= 0 || k <= 0 || k % (4 * gs) != 0 || n % 128 != 0) return HQ_ERR_INVALID;
   if (n > (1ll << 30) || k > (1ll << 30)) return HQ_ERR_INVALID;
@@ -1740,7 +1766,7 @@ int check_common(const void* a, const uint8_t* sfa, const void* b, const void* s
   // w4a4-mxfp4; bias only in w8a8-mxfp8 mode
   if (mode == HQ_NVFP4 && !alpha) return HQ_ERR_UNSUPPORTED;
   if (mode == HQ_MXFP4 && alpha) return HQ_ERR_UNSUPPORTED;
-  if (mode != HQ_MXFP8 && bias) return HQ_ERR_UNSUPPORTED;
+  if (mode != HQ_MXFP8 && mode != HQ_MXFP8_E5M2 && bias) return HQ_ERR_UNSUPPORTED;
   return HQ_OK;
 }
 
@@ -1886,6 +1912,8 @@ GemmParams base_params(const uint8_t* sfa, const uint8_t* sfb, const float* alph
   p.gs.status = status_word_ptr();
   p.wait_limit_ns = wait_limit_ns();
   p.inject_skip = fault_injection_stage();
+  p.idesc_ab = mode == HQ_MXFP8_E5M2 ? ((1u << 7) | (1u << 10)) : 0u;
+  p.d_type = kDBf16;
   return p;
 }
 
@@ -1912,9 +1940,16 @@ int dglu_bs_impl(const void* a, const uint8_t* sfa, const void* b, const uint8_t
                     const float* beta, const float* prob, int act, void* d_row, uint8_t* sfd_row,
                     void* d_col, uint8_t* sfd_col, const float* norm_const, float* dprob,
                     hq_bf16* dbias, float* amax, int64_t m, int64_t n, int64_t k, hq_mode mode,
-                    void* workspace, size_t ws_bytes, int sm_count, hq_stream_t s) {
+                    int d_type, void* workspace, size_t ws_bytes, int sm_count, hq_stream_t s) {
   if (act != 0 && act != 1) return HQ_ERR_INVALID;
-  if (mode != HQ_MXFP8 && mode != HQ_MXFP4 && mode != HQ_NVFP4) return HQ_ERR_INVALID;
+  if (!valid_mode(mode)) return HQ_ERR_INVALID;
+  if (d_type != kDBf16 && d_type != kDF32 && d_type != kDE4M3 && d_type != kDE5M2) return HQ_ERR_INVALID;
+  // FP8 D_row carries its SFD_row scales; BF16 and float32 D_row carry none
+  const bool fp8_d = d_type == kDE4M3 || d_type == kDE5M2;
+  if (fp8_d != (sfd_row != nullptr)) return HQ_ERR_INVALID;
+  // cuDNN "Grouped GEMM + dGLU (SM100)", Additional Type Constraints: FP4
+  // operands with 16-value scale groups and float32 D need the dbias path
+  if (d_type == kDF32 && mode == HQ_NVFP4 && !dbias) return HQ_ERR_UNSUPPORTED;
   const int64_t gs = mode == HQ_NVFP4 ? 16 : 32;
   if (n <= 0 || k <= 0 || k % (4 * gs) != 0 || n % 128 != 0) return HQ_ERR_INVALID;
   if (n > (1ll << 28) || k > (1ll << 30)) return HQ_ERR_INVALID;
@@ -1967,6 +2002,8 @@ int dglu_bs_impl(const void* a, const uint8_t* sfa, const void* b, const uint8_t
   p.sfd_col = sfd_col;
   p.sfd_col_s = (m + 127) / 128 * 4;
   p.amax = amax;
+  p.d_type = d_type;
+  mode = kernel_mode(mode);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
   if (amax && cudaMemsetAsync(amax, 0, static_cast<size_t>(L) * 2 * sizeof(float), st) != cudaSuccess)
     return HQ_ERR_CUDA;
@@ -2071,6 +2108,7 @@ int hq_gemm_grouped_contig_swiglu_quant(const void* a, const uint8_t* sfa, const
   if (m_rows == 0) return HQ_OK;
   hq::GemmParams p = hq::base_params(sfa, sfb, alpha, nullptr, nullptr, 2 * H, k, mode);
   if (!p.gs.status) return HQ_ERR_CUDA;
+  mode = hq::kernel_mode(mode);
   p.n = H;  // compact columns; the B scale blocks stay those of 2H rows
   p.gs.a_rows = m_rows;
   p.gs.groups = L;
@@ -2103,7 +2141,18 @@ int hq_gemm_dglu_bs(const void* a, const uint8_t* sfa, const void* b, const uint
                     void* workspace, size_t ws_bytes, int sm_count, hq_stream_t s) {
   return hq::dglu_bs_impl(a, sfa, b, sfb, nullptr, nullptr, c, padded_offsets, L, alpha, beta, prob,
                           act, d_row, sfd_row, d_col, sfd_col, norm_const, dprob, dbias, amax, m, n,
-                          k, mode, workspace, ws_bytes, sm_count, s);
+                          k, mode, sfd_row ? hq::kDE4M3 : hq::kDBf16, workspace, ws_bytes, sm_count, s);
+}
+
+int hq_gemm_dglu_bs_typed(const void* a, const uint8_t* sfa, const void* b, const uint8_t* sfb,
+                          const hq_bf16* c, const int32_t* padded_offsets, int L, const float* alpha,
+                          const float* beta, const float* prob, int act, void* d_row, uint8_t* sfd_row,
+                          void* d_col, uint8_t* sfd_col, const float* norm_const, float* dprob,
+                          hq_bf16* dbias, float* amax, int64_t m, int64_t n, int64_t k, hq_mode mode,
+                          hq_dtype d_type, void* workspace, size_t ws_bytes, int sm_count, hq_stream_t s) {
+  return hq::dglu_bs_impl(a, sfa, b, sfb, nullptr, nullptr, c, padded_offsets, L, alpha, beta, prob,
+                          act, d_row, sfd_row, d_col, sfd_col, norm_const, dprob, dbias, amax, m, n,
+                          k, mode, static_cast<int>(d_type), workspace, ws_bytes, sm_count, s);
 }
 
 int hq_gemm_dglu_bs_discrete(const void* a, const uint8_t* sfa, const int64_t* b_ptrs,
@@ -2117,7 +2166,8 @@ int hq_gemm_dglu_bs_discrete(const void* a, const uint8_t* sfa, const int64_t* b
   if (!b_ptrs) return HQ_ERR_INVALID;
   return hq::dglu_bs_impl(a, sfa, nullptr, nullptr, b_ptrs, sfb_ptrs, c, padded_offsets, L, alpha,
                           beta, prob, act, d_row, sfd_row, d_col, sfd_col, norm_const, dprob, dbias,
-                          amax, m, n, k, mode, workspace, ws_bytes, sm_count, s);
+                          amax, m, n, k, mode, sfd_row ? hq::kDE4M3 : hq::kDBf16, workspace, ws_bytes,
+                          sm_count, s);
 }
 
 size_t hq_gemm_grouped_rows_workspace_size(int64_t m_rows, int L) {

@@ -392,6 +392,12 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// Two floats -> two E5M2 bytes: `hi` in bits 15..8, `lo` in bits 7..0.
+__device__ __forceinline__ uint32_t cvt_e5m2x2(float hi, float lo) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 // Two floats -> one byte of two E2M1 codes: `hi` in bits 7..4, `lo` in 3..0.
 __device__ __forceinline__ uint32_t cvt_e2m1x2(float hi, float lo) {
   uint32_t r;

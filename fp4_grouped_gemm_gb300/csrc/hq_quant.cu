@@ -13,7 +13,7 @@
 //
 // Scale rule (cuDNN frontend "Grouped GEMM + dGLU (SM100)", Step 3, with the
 // HALOps group_wise_quant encodings), evaluated in IEEE float32:
-//   s = (g * amax) * rcp_max,   rcp_max = 1/448 (E4M3) or 1/6 (E2M1)
+//   s = (g * amax) * rcp_max,   rcp_max = 1/448 (E4M3), 1/57344 (E5M2) or 1/6 (E2M1)
 //   MXFP8: UE8M0 = clamp(ceil(log2 s) + 127, 0, 254) (0 if s == 0),
 //          q = E4M3(x * 2^(127 - UE8M0))
 //   NVFP4: UE4M3 = E4M3(s), q = E2M1(x * (g / value(UE4M3))) (0 if value 0)
@@ -125,6 +125,18 @@ __device__ __forceinline__ uint32_t cvt_e4m3x4(float x0, float x1, float x2, flo
   return w;
 }
 
+// Four floats -> one word of four E5M2 codes (element j in byte j).
+__device__ __forceinline__ uint32_t cvt_e5m2x4(float x0, float x1, float x2, float x3) {
+  uint32_t w;
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "cvt.rn.satfinite.e5m2x2.f32 l, %2, %1;\n\t"
+      "cvt.rn.satfinite.e5m2x2.f32 h, %4, %3;\n\t"
+      "mov.b32 %0, {l, h};\n\t}"
+      : "=r"(w)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
+  return w;
+}
+
 // LPG lanes quantise one scale group; each holds GL = group / LPG of its
 // values x[0..GL) (a lane pair: the even lane the first half).  MXFP8 writes
 // GL E4M3 bytes to qw[0..GL/4); NVFP4 and MXFP4 write GL/2 packed bytes to
@@ -137,8 +149,11 @@ __device__ __forceinline__ uint32_t encode_group(const float (&x)[GL], float g,
 #pragma unroll
   for (int i = 0; i < GS; ++i) amax = fmaxf(amax, fabsf(x[i]));
   if (LPG == 2) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-  if (MODE == HQ_MXFP8) {
-    const float s = __fmul_rn(__fmul_rn(g, amax), 1.0f / 448.0f);
+  if (MODE == HQ_MXFP8 || MODE == HQ_MXFP8_E5M2) {
+    // s = (g amax) / max element (448 for E4M3, 57344 for E5M2), rounded up
+    // to a power of two; the products x * 2^(127 - byte) are exact
+    constexpr float kRcpMax = MODE == HQ_MXFP8 ? 1.0f / 448.0f : 1.0f / 57344.0f;
+    const float s = __fmul_rn(__fmul_rn(g, amax), kRcpMax);
     const uint32_t byte = ue8m0_ceil(s);
     const float mult = pow2_neg_unbiased(byte);
 #pragma unroll
@@ -146,7 +161,7 @@ __device__ __forceinline__ uint32_t encode_group(const float (&x)[GL], float g,
       float y[4];
       mul_f32x2(y[0], y[1], x[4 * i], x[4 * i + 1], mult);
       mul_f32x2(y[2], y[3], x[4 * i + 2], x[4 * i + 3], mult);
-      qw[i] = cvt_e4m3x4(y[0], y[1], y[2], y[3]);
+      qw[i] = MODE == HQ_MXFP8 ? cvt_e4m3x4(y[0], y[1], y[2], y[3]) : cvt_e5m2x4(y[0], y[1], y[2], y[3]);
     }
     return byte;
   } else if (MODE == HQ_MXFP4) {
@@ -293,7 +308,7 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
       const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, byte, 3 * LPG);
       if (s >= groups_row) continue;
       const int64_t e0 = row * p.k + s * GS + (lane % LPG) * GL;  // first element of this lane
-      if (MODE == HQ_MXFP8) {
+      if (MODE == HQ_MXFP8 || MODE == HQ_MXFP8_E5M2) {
         uint4* dst = reinterpret_cast<uint4*>(p.q + e0);
 #pragma unroll
         for (int i = 0; i < GL / 16; ++i) dst[i] = make_uint4(qw[4 * i], qw[4 * i + 1], qw[4 * i + 2], qw[4 * i + 3]);
@@ -361,6 +376,7 @@ int launch_quant(const QuantParams& p, cudaStream_t st, bool pdl) {
 
 int dispatch_f16(hq_mode mode, const QuantParams& p, cudaStream_t st, bool pdl) {
   if (mode == HQ_MXFP8) return launch_quant<HQ_MXFP8, false, true>(p, st, pdl);
+  if (mode == HQ_MXFP8_E5M2) return launch_quant<HQ_MXFP8_E5M2, false, true>(p, st, pdl);
   if (mode == HQ_MXFP4) return launch_quant<HQ_MXFP4, false, true>(p, st, pdl);
   return launch_quant<HQ_NVFP4, false, true>(p, st, pdl);
 }
@@ -369,6 +385,7 @@ int dispatch(hq_mode mode, bool swiglu, const QuantParams& p, cudaStream_t st, b
   if (mode == HQ_MXFP8)
     return swiglu ? launch_quant<HQ_MXFP8, true>(p, st, pdl) : launch_quant<HQ_MXFP8, false>(p, st, pdl);
   if (mode == HQ_MXFP4) return swiglu ? HQ_ERR_INVALID : launch_quant<HQ_MXFP4, false>(p, st, pdl);
+  if (mode == HQ_MXFP8_E5M2) return swiglu ? HQ_ERR_INVALID : launch_quant<HQ_MXFP8_E5M2, false>(p, st, pdl);
   return swiglu ? launch_quant<HQ_NVFP4, true>(p, st, pdl) : launch_quant<HQ_NVFP4, false>(p, st, pdl);
 }
 
@@ -376,7 +393,8 @@ int dispatch(hq_mode mode, bool swiglu, const QuantParams& p, cudaStream_t st, b
 int quant_entry(const uint16_t* x, bool f16, int64_t m, int64_t k, hq_mode mode, int use_swizzle,
                 const float* global_scale, void* q_out, uint8_t* sf_out, int use_pdl,
                 hq_stream_t s) {
-  if (mode != HQ_MXFP8 && mode != HQ_MXFP4 && mode != HQ_NVFP4) return HQ_ERR_INVALID;
+  if (mode != HQ_MXFP8 && mode != HQ_MXFP4 && mode != HQ_NVFP4 && mode != HQ_MXFP8_E5M2)
+    return HQ_ERR_INVALID;
   const int64_t gs = mode == HQ_NVFP4 ? 16 : 32;
   if (m < 0 || k <= 0 || k % (4 * gs) != 0) return HQ_ERR_INVALID;
   if (mode != HQ_NVFP4 && global_scale) return HQ_ERR_UNSUPPORTED;

@@ -72,7 +72,9 @@ typedef uint16_t hq_bf16;
 typedef enum {
   HQ_MXFP8 = 0, /* "w8a8-mxfp8": E4M3 elements, UE8M0 scale per 32          */
   HQ_MXFP4 = 1, /* "w4a4-mxfp4": packed E2M1, UE8M0 scale per 32, no alpha  */
-  HQ_NVFP4 = 2  /* "w4a4-nvfp4": packed E2M1, UE4M3 scale per 16, FP32 alpha */
+  HQ_NVFP4 = 2, /* "w4a4-nvfp4": packed E2M1, UE4M3 scale per 16, FP32 alpha */
+  HQ_MXFP8_E5M2 = 3 /* MXFP8 with float8_e5m2 elements, UE8M0 scale per 32
+                       (cuDNN "Grouped GEMM + dGLU (SM100)", Data Types) */
 } hq_mode;
 
 /* Return codes. */
@@ -191,20 +193,21 @@ int hq_set_gemm_2sm(int enable);
  * use_swizzle, plain row-major otherwise).  Scale rule (cuDNN "Grouped GEMM +
  * dGLU (SM100)", Step 3): SF = norm_const * amax(group) * rcp_max,
  * q = x * norm_const / SF, with norm_const = *global_scale (NVFP4; 1 when
- * NULL) or 1 (MXFP8, MXFP4), rcp_max = 1/448 (E4M3) or 1/6 (E2M1), evaluated
- * in IEEE float32 in that order.  MXFP8 and MXFP4 round SF up to a power of
- * two (UE8M0 = clamp(ceil(log2 SF) + 127, 0, 254), 0 for an all-zero group)
- * and store E4M3 or E2M1 of x * 2^(127 - UE8M0); NVFP4 stores
+ * NULL) or 1 (MXFP8, MXFP4), rcp_max = 1/448 (E4M3), 1/57344 (E5M2) or 1/6
+ * (E2M1), evaluated in IEEE float32 in that order.  MXFP8 (either element
+ * type) and MXFP4 round SF up to a power of two (UE8M0 = clamp(ceil(log2 SF)
+ * + 127, 0, 254), 0 for an all-zero group) and store E4M3, E5M2 or E2M1 of
+ * x * 2^(127 - UE8M0); NVFP4 stores
  * UE4M3 = E4M3(SF) and E2M1(x * (g / SF_decoded)).  Element encodes round to
  * nearest even and saturate; E2M1 codes are packed two per byte, the even
  * element in the low nibble.
  *
  *   x            [m, k] BF16, 16-byte aligned
- *   mode         HQ_MXFP8, HQ_MXFP4 or HQ_NVFP4
+ *   mode         HQ_MXFP8, HQ_MXFP8_E5M2, HQ_MXFP4 or HQ_NVFP4
  *   use_swizzle  1: SfAtom layout; 0: row-major [ceil(m/128)*128, k/group]
  *   global_scale NVFP4 only: device float [1] or NULL (=1); must be NULL for
  *                MXFP8 and MXFP4 (HQ_ERR_UNSUPPORTED otherwise)
- *   q_out        MXFP8 [m, k] bytes; MXFP4 / NVFP4 [m, k/2] bytes; 16-byte
+ *   q_out        MXFP8 (E4M3 or E5M2) [m, k] bytes; MXFP4 / NVFP4 [m, k/2] bytes; 16-byte
  *                aligned
  *   sf_out       hq_sf_bytes(m, k, mode) bytes; padding rows written as 0
  *   use_pdl      1: launch with programmatic dependent launch
@@ -228,10 +231,12 @@ int hq_quant_f16(const uint16_t *x, int64_t m, int64_t k, hq_mode mode, int use_
  *   a, sfa   quantised A and its SfAtom scales (as hq_quant writes them)
  *   b, sfb   quantised B (one [n, k] matrix per group, stacked) and its
  *            SfAtom scales (per group ceil(n/128)*128*(k/group) bytes)
+ *   mode     HQ_MXFP8, HQ_MXFP8_E5M2 (A and B both float8_e5m2), HQ_MXFP4
+ *            or HQ_NVFP4
  *   alpha    device float per group, or NULL (= 1).  Required for HQ_NVFP4
- *            (HQ_ERR_UNSUPPORTED if NULL), optional for HQ_MXFP8, not
+ *            (HQ_ERR_UNSUPPORTED if NULL), optional for the MXFP8 modes, not
  *            accepted for HQ_MXFP4 (HQ_ERR_UNSUPPORTED if given)
- *   bias     device BF16 [groups, n] or NULL.  HQ_MXFP8 only
+ *   bias     device BF16 [groups, n] or NULL.  MXFP8 modes only
  *            (HQ_ERR_UNSUPPORTED with the FP4 modes), as the HALOps API states
  *   sm_count number of persistent CTAs (<= 0: all SMs)
  * Shape rules: k % (4 * group) == 0; n % 128 == 0; all pointers 16-byte
@@ -391,8 +396,8 @@ int hq_gemm_dgeglu(const hq_bf16 *a, const hq_bf16 *b, const hq_bf16 *c,
 
 /* cuDNN frontend "Grouped GEMM + dGLU (SM100)", block-scaled contract:
  * Step 1 R = alpha_g^2 * (dequantised A . dequantised B_g^T) with A, B and
- * their SfAtom scales as hq_quant writes them (mode HQ_MXFP8, HQ_MXFP4 or
- * HQ_NVFP4), groups contiguous in M by padded_offsets (as
+ * their SfAtom scales as hq_quant writes them (mode HQ_MXFP8, HQ_MXFP8_E5M2,
+ * HQ_MXFP4 or HQ_NVFP4), groups contiguous in M by padded_offsets (as
  * hq_gemm_grouped_contig); Step 2 the dGLU epilogue of hq_gemm_dswiglu
  * (act 0) or hq_gemm_dgeglu (act 1) on the BF16 C [m, 2n]; Step 3 optional
  * FP8 output.
@@ -418,6 +423,36 @@ int hq_gemm_dglu_bs(const void *a, const uint8_t *sfa, const void *b, const uint
                     void *d_col, uint8_t *sfd_col, const float *norm_const, float *dprob,
                     hq_bf16 *dbias, float *amax, int64_t m, int64_t n, int64_t k, hq_mode mode,
                     void *workspace, size_t ws_bytes, int sm_count, hq_stream_t s);
+
+/* D_row / D_col element type of hq_gemm_dglu_bs_typed (the cuDNN page's
+ * d_dtype values). */
+typedef enum {
+  HQ_D_BF16 = 0, /* bfloat16                                              */
+  HQ_D_F32 = 1,  /* float32 (4 bytes per element)                         */
+  HQ_D_E4M3 = 2, /* float8_e4m3fn with UE8M0 SFD scales (Step 3)          */
+  HQ_D_E5M2 = 3  /* float8_e5m2 with UE8M0 SFD scales (Step 3)            */
+} hq_dtype;
+
+/* hq_gemm_dglu_bs with the D element type given explicitly (cuDNN
+ * "Grouped GEMM + dGLU (SM100)", Data Types table: d_dtype bfloat16 /
+ * float32 for FP4 operands, float8_e4m3fn / float8_e5m2 for FP8 operands;
+ * the other pairings run as well).
+ *   d_type  HQ_D_BF16 or HQ_D_F32: sfd_row, d_col, sfd_col, norm_const NULL;
+ *           d_row is [m, 2n] of bfloat16 or float32.
+ *           HQ_D_E4M3 or HQ_D_E5M2: sfd_row required, D_row (and D_col) as
+ *           hq_gemm_dglu_bs's FP8 output with rcp_max = 1/448 (E4M3) or
+ *           1/57344 (E5M2) and codes of that type.
+ * HQ_ERR_INVALID for another d_type or a mismatched sfd_row;
+ * HQ_ERR_UNSUPPORTED for HQ_D_F32 with HQ_NVFP4 operands and dbias == NULL
+ * (the page's "non-dbias paths" constraint).  Everything else as
+ * hq_gemm_dglu_bs. */
+int hq_gemm_dglu_bs_typed(const void *a, const uint8_t *sfa, const void *b, const uint8_t *sfb,
+                          const hq_bf16 *c, const int32_t *padded_offsets, int L,
+                          const float *alpha, const float *beta, const float *prob, int act,
+                          void *d_row, uint8_t *sfd_row, void *d_col, uint8_t *sfd_col,
+                          const float *norm_const, float *dprob, hq_bf16 *dbias, float *amax,
+                          int64_t m, int64_t n, int64_t k, hq_mode mode, hq_dtype d_type,
+                          void *workspace, size_t ws_bytes, int sm_count, hq_stream_t s);
 
 /* ------------------------------------------------------------------------- *
  * Discrete weights (cuDNN frontend "Grouped GEMM + dGLU (SM100)", weight

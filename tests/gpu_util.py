@@ -99,6 +99,8 @@ def _scale_byte(amax, out_mode, g):
     a32 = np.asarray(amax, dtype=np.float32)
     if out_mode == "mxfp8":
         return oquant.scale_byte_mxfp8(a32, gf).astype(np.int64)
+    if out_mode == "mxfp8_e5m2":
+        return oquant.scale_byte_mxfp8_e5m2(a32, gf).astype(np.int64)
     return oquant.scale_byte_nvfp4(a32, gf)[0].astype(np.int64)
 
 
@@ -107,8 +109,10 @@ def _codes_value(v, sf, out_mode, g):
     (float64, v [r, G, gs], sf [r, G])."""
     from oracle import formats
     gf = np.float32(1.0 if g is None else g)
-    if out_mode == "mxfp8":
+    if out_mode in ("mxfp8", "mxfp8_e5m2"):
         mult = np.ldexp(1.0, 127 - sf.astype(np.int64))[..., None]
+        if out_mode == "mxfp8_e5m2":
+            return formats.decode_e5m2(formats.encode_e5m2(v * float(gf) * mult))
         return formats.decode_e4m3(formats.encode_e4m3(v * float(gf) * mult))
     sd = formats.decode_ue4m3(sf.astype(np.uint8)).astype(np.float32)
     with np.errstate(divide="ignore", invalid="ignore"):
@@ -119,8 +123,8 @@ def _codes_value(v, sf, out_mode, g):
 def window_check(codes_gpu, sf_gpu, y, err, out_mode, g=None, what=""):
     """Checks a row-wise quantisation of y done on the GPU.
 
-    codes_gpu [r, c] unpacked element codes (E4M3 for "mxfp8", E2M1 for
-    "nvfp4"), sf_gpu [r, c / gs] plain scale bytes, y [r, c] the exact
+    codes_gpu [r, c] unpacked element codes (E4M3 for "mxfp8", E5M2 for
+    "mxfp8_e5m2", E2M1 for "nvfp4"), sf_gpu [r, c / gs] plain scale bytes, y [r, c] the exact
     (float64) values and err [r, c] a bound on |y_gpu - y| of the kernel's
     float32 intermediate; g the norm_const / global scale (None = 1).
 
@@ -136,7 +140,7 @@ def window_check(codes_gpu, sf_gpu, y, err, out_mode, g=None, what=""):
     y = np.asarray(y, dtype=np.float64)
     err = np.asarray(err, dtype=np.float64)
     r, c = y.shape
-    gs = 32 if out_mode == "mxfp8" else 16
+    gs = 16 if out_mode == "nvfp4" else 32
     G = c // gs
     yg, eg = y.reshape(r, G, gs), err.reshape(r, G, gs)
     sf_gpu = np.asarray(sf_gpu).astype(np.int64).reshape(r, G)
@@ -151,7 +155,7 @@ def window_check(codes_gpu, sf_gpu, y, err, out_mode, g=None, what=""):
                              f"gpu {sf_gpu[i]} allowed [{sb_lo[i]}, {sb_hi[i]}]")
     v_lo = _codes_value(_lower(yg - eg), sf_gpu, out_mode, g)
     v_hi = _codes_value(_upper(yg + eg), sf_gpu, out_mode, g)
-    dec = formats.decode_e4m3 if out_mode == "mxfp8" else formats.decode_e2m1
+    dec = {"mxfp8": formats.decode_e4m3, "mxfp8_e5m2": formats.decode_e5m2}.get(out_mode, formats.decode_e2m1)
     v_gpu = dec(np.asarray(codes_gpu).reshape(r, G, gs))
     c_bad = (v_gpu < v_lo) | (v_gpu > v_hi)
     if c_bad.any():
@@ -165,7 +169,7 @@ def window_check(codes_gpu, sf_gpu, y, err, out_mode, g=None, what=""):
     v_ref = _codes_value(y32, sf_ref, out_mode, g)
 
     def scale_value(sf):
-        if out_mode == "mxfp8":
+        if out_mode in ("mxfp8", "mxfp8_e5m2"):
             return np.ldexp(1.0, sf.astype(np.int64) - 127)[..., None]
         return formats.decode_ue4m3(sf.astype(np.uint8)).astype(np.float64)[..., None]
 

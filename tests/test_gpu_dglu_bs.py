@@ -42,7 +42,8 @@ def bf16_ulp(x):
     return np.where(a > 0, 2.0 ** (e - 7), 2.0 ** -133)
 
 
-def run(mode, act, offsets, m, n, k, seed, fp8=False, norm=None, with_dbias=True, col=False, amax=False):
+def run(mode, act, offsets, m, n, k, seed, fp8=False, norm=None, with_dbias=True, col=False, amax=False,
+        d_dtype=None):
     L = len(offsets)
     dev = torch.device("cuda")
     a = bf16_rows(m, k, seed)
@@ -57,7 +58,14 @@ def run(mode, act, offsets, m, n, k, seed, fp8=False, norm=None, with_dbias=True
     a_deq = oquant.dequantize(qa_np, sfa_np, mode)
     dprob = torch.zeros(m, dtype=torch.float32, device=dev)
     dbias = torch.zeros(L, 2 * n, dtype=torch.bfloat16, device=dev) if with_dbias else None
-    d_row = (torch.full((m, 2 * n), 0x5A, dtype=torch.uint8, device=dev) if fp8 else sentinel_bf16((m, 2 * n)))
+    if d_dtype in ("e4m3", "e5m2"):
+        fp8 = True
+    if fp8:
+        d_row = torch.full((m, 2 * n), 0x5A, dtype=torch.uint8, device=dev)
+    elif d_dtype == "f32":
+        d_row = torch.full((m, 2 * n), float("nan"), dtype=torch.float32, device=dev)
+    else:
+        d_row = sentinel_bf16((m, 2 * n))
     nc = torch.tensor([norm], dtype=torch.float32, device=dev) if norm is not None else None
     off = torch.tensor(offsets, dtype=torch.int32, device=dev)
     d_col = torch.full((m, 2 * n), 0x5A, dtype=torch.uint8, device=dev) if col else None
@@ -66,7 +74,7 @@ def run(mode, act, offsets, m, n, k, seed, fp8=False, norm=None, with_dbias=True
     outs = hq.hq_gemm_dglu_bs(
         qa, sfa, qb, sfb, c.to(dev), off, alpha.to(dev), prob.to(dev), dprob, k, mode, act=act,
         beta=beta.to(dev) if act == "dswiglu" else None, dbias=dbias, d_row=d_row, fp8_out=fp8,
-        norm_const=nc, col_out=col, d_col=d_col, amax=am)
+        norm_const=nc, col_out=col, d_col=d_col, amax=am, d_dtype=d_dtype)
     torch.cuda.synchronize()
     if col:
         d_row, sfd, d_col, sfd_col, dprob, dbias = outs
@@ -199,3 +207,69 @@ def test_dswiglu_bs_fp8_out_full_size_sampled(cuda_dev):
           f"{len(rows) * 2 * n} values differ from the oracle's, all inside the window")
     if valid < m:
         assert bool((d8[valid:] == 0x5A).all()), "rows past the last group written"
+
+
+# --------------------------------------------------------------------------- #
+# The rest of the cuDNN page's type matrix: float8_e5m2 operands (reading R7),
+# float8_e5m2 D_row / D_col (reading Q4) and float32 D_row
+# --------------------------------------------------------------------------- #
+
+
+@pytest.mark.parametrize("act", ["dswiglu", "dgeglu"])
+def test_dglu_bs_e5m2_operands_bf16_out(cuda_dev, act):
+    offsets = [256, 256, 768, 1024]
+    ref, d_row, _, dprob, dbias = run("mxfp8_e5m2", act, offsets, 1152, 256, 256, seed=17)
+    w = ref["written"]
+    D = d_row.float().cpu().numpy().astype(np.float64)
+    tol = 2.0 ** -8 * np.abs(ref["D"]) + 2.0 ** -20 * ref["D_mag"] + 1e-30
+    bad = (np.abs(D - ref["D"]) > tol) & w[:, None]
+    assert not bad.any(), f"{int(bad.sum())} bad D_row values"
+    assert_rows_untouched(d_row, w, "D_row")
+    check_common(ref, dprob, dbias)
+
+
+@pytest.mark.parametrize("mode,act,norm", [("mxfp8", "dswiglu", None), ("mxfp8_e5m2", "dgeglu", 8.0),
+                                           ("nvfp4", "dswiglu", 0.5)])
+def test_dglu_bs_e5m2_d_row_and_col(cuda_dev, mode, act, norm):
+    offsets = [256, 512]
+    m, n = 640, 128
+    ref, d_row, sfd, dprob, dbias, d_col, sfd_col = run(mode, act, offsets, m, n, 256, seed=19, norm=norm,
+                                                        col=True, d_dtype="e5m2")
+    w = ref["written"]
+    codes = d_row.cpu().numpy()
+    sf_plain = oquant.from_sfatom(sfd.cpu().numpy(), m, 2 * n // 32)
+    n_sf, n_c = window_check(codes[w], sf_plain[w], ref["D"][w], D_ERR * ref["D_mag"][w], "mxfp8_e5m2",
+                             g=norm, what=f"E5M2 D_row {mode} {act}")
+    print(f"E5M2 D_row {mode} {act}: {n_sf} scale bytes and {n_c} values differ from the oracle's")
+    assert (codes[~w] == 0x5A).all(), "rows past the last group written"
+    rows_w = int(w.sum())
+    S = (m + 127) // 128 * 4
+    sfc = oquant.from_sfatom(sfd_col.cpu().numpy(), 2 * n, S)[:, : rows_w // 32]
+    cc = d_col.cpu().numpy()[:rows_w]
+    window_check(cc.T, sfc, ref["D"][:rows_w].T, D_ERR * ref["D_mag"][:rows_w].T, "mxfp8_e5m2", g=norm,
+                 what=f"E5M2 D_col {mode} {act}")
+    check_common(ref, dprob, dbias)
+
+
+@pytest.mark.parametrize("mode,with_dbias", [("nvfp4", True), ("mxfp4", False), ("mxfp8", True)])
+def test_dglu_bs_float32_d_row(cuda_dev, mode, with_dbias):
+    """float32 D_row: the kernel's float32 D itself, within the GEMM bound
+    carried through the activation (no BF16 rounding)."""
+    offsets = [256, 256, 768, 1024]
+    ref, d_row, _, dprob, dbias = run(mode, "dswiglu", offsets, 1152, 256, 256, seed=23,
+                                      with_dbias=with_dbias, d_dtype="f32")
+    w = ref["written"]
+    assert d_row.dtype == torch.float32
+    D = d_row.cpu().numpy().astype(np.float64)
+    tol = D_ERR * ref["D_mag"] + 2.0 ** -23 * np.abs(ref["D"]) + 1e-30
+    bad = (np.abs(D - ref["D"]) > tol) & w[:, None]
+    assert not bad.any(), f"{int(bad.sum())} bad float32 D_row values"
+    assert np.isnan(D[~w]).all(), "rows past the last group written"
+    check_common(ref, dprob, dbias)
+
+
+def test_dglu_bs_float32_nvfp4_needs_dbias(cuda_dev):
+    """The page: FP4 operands with 16-value scale groups and float32 D are
+    not supported on the non-dbias path."""
+    with pytest.raises(hq.HQError):
+        run("nvfp4", "dswiglu", [256], 256, 128, 256, seed=29, with_dbias=False, d_dtype="f32")

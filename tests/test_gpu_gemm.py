@@ -512,3 +512,43 @@ def test_max_groups_contig_and_masked(cuda_dev):
         ref[sel], mag[sel] = ogemm.dense(a_deq[sel], _expert_deq(qb_np, sfb_np, e, n, k, mode))
     assert_gemm_close(outm[torch.from_numpy(rows).cuda()], ref, mag, "masked, 1024 experts")
     assert_rows_untouched(outm, written, "masked, 1024 experts")
+
+
+# --------------------------------------------------------------------------- #
+# float8_e5m2 operands (MXFP8 with E5M2 elements, reading R7)
+# --------------------------------------------------------------------------- #
+
+
+@pytest.mark.parametrize("two_sm,tile_n", [(256, 0), (0, 128), (0, 256)])
+@pytest.mark.parametrize("m,n,k", [(256, 256, 256), (300, 512, 1024), (129, 768, 640)])
+def test_dense_mxfp8_e5m2(cuda_dev, m, n, k, two_sm, tile_n):
+    hq.set_gemm_2sm(two_sm)
+    dense_case(m, n, k, "mxfp8_e5m2", tile_n, alpha=0.75, bias=True, seed=m + n + k)
+
+
+@pytest.mark.parametrize("two_sm", [1, 0])
+def test_grouped_mxfp8_e5m2(cuda_dev, two_sm):
+    hq.set_gemm_2sm(two_sm)
+    contig_case([256, 256, 768, 1024], 1152, 256, 256, "mxfp8_e5m2", 0, alpha=[0.5, 1.0, 2.0, 1.25], bias=True,
+                seed=31)
+    status = masked_case([256, 64, 0, 129, 512], 512, 512, 384, "mxfp8_e5m2", 0,
+                         alpha=[1.0, 0.5, 2.0, 0.75, 1.5], seed=33)
+    assert status == 0
+
+
+def test_e5m2_end_to_end_quant_then_gemm(cuda_dev):
+    """BF16 -> hq_quant(E5M2) on the GPU -> hq_gemm_dense, against the oracle
+    quantising the same inputs itself."""
+    m, n, k = 384, 512, 1024
+    a = bf16_rows(m, k, 41, spread=3)
+    b = bf16_rows(n, k, 42, std=0.02)
+    qa, sfa = hq.hq_quant(a.cuda(), "mxfp8_e5m2")
+    qb, sfb = hq.hq_quant(b.cuda(), "mxfp8_e5m2")
+    out = hq.hq_gemm_dense(qa, sfa, qb, sfb, m, n, k, "mxfp8_e5m2")
+    torch.cuda.synchronize()
+    qa_np, sa_np = oquant.quantize(np_f32(a), "mxfp8_e5m2")
+    qb_np, sb_np = oquant.quantize(np_f32(b), "mxfp8_e5m2")
+    assert np.array_equal(qa.cpu().numpy(), qa_np)
+    ref, mag = ogemm.dense(oquant.dequantize(qa_np, sa_np, "mxfp8_e5m2"),
+                           oquant.dequantize(qb_np, sb_np, "mxfp8_e5m2"))
+    assert_gemm_close(out, ref, mag, "end-to-end mxfp8_e5m2")

@@ -19,7 +19,8 @@ def run_and_compare(x_cpu, mode, swizzle=True, g=None, rows_check=None):
     x = x_cpu.to(dev)
     gs_t = torch.tensor([g], dtype=torch.float32, device=dev) if g is not None else None
     m, k = x.shape
-    q_out = torch.full(((m, k) if mode == "mxfp8" else (m, k // 2)), 0xAA, dtype=torch.uint8, device=dev)  # FP4 packed
+    one_byte = mode in ("mxfp8", "mxfp8_e5m2")
+    q_out = torch.full(((m, k) if one_byte else (m, k // 2)), 0xAA, dtype=torch.uint8, device=dev)  # FP4 packed
     sf_out = torch.full((hq.sf_bytes(m, k, mode),), 0xAA, dtype=torch.uint8, device=dev)
     hq.hq_quant(x, mode, use_swizzle=swizzle, global_scale=gs_t, q_out=q_out, sf_out=sf_out)
     torch.cuda.synchronize()
@@ -109,3 +110,23 @@ def test_quant_pdl_launch_matches(cuda_dev):
     q2, s2 = hq.hq_quant(x, "mxfp8", use_pdl=True)
     torch.cuda.synchronize()
     assert torch.equal(q1, q2) and torch.equal(s1, s2)
+
+
+@pytest.mark.parametrize("swizzle", [True, False])
+@pytest.mark.parametrize("m,k", [(1, 128), (129, 256), (300, 1024)])
+def test_quant_mxfp8_e5m2_bit_exact(cuda_dev, m, k, swizzle):
+    """MXFP8 with float8_e5m2 elements (reading R7): bytes and scale bytes
+    equal the oracle's, rows scaled over a wide range of magnitudes."""
+    run_and_compare(bf16_rows(m, k, seed=m + k, spread=6), "mxfp8_e5m2", swizzle)
+
+
+def test_quant_mxfp8_e5m2_special_values(cuda_dev):
+    """Zero groups, a group at the top of the E5M2 range (57344), a group of
+    values of very different magnitudes (the small ones land in the
+    subnormal range or at zero), a group of tiny values, and a ramp."""
+    x = torch.zeros(128, 128)
+    x[1, :32] = 57344.0
+    x[2, 0], x[2, 1], x[2, 2], x[2, 3] = 1.0, 1.125, -1.375, 3.0e-6
+    x[3, 0], x[3, 1] = 1.0e-30, -1.0e-30
+    x[4, 32:64] = torch.linspace(-3.0e4, 3.0e4, 32)
+    run_and_compare(x.to(torch.bfloat16), "mxfp8_e5m2", True)
