@@ -456,20 +456,28 @@ def hq_gemm_grouped_contig_discrete(a, sfa, b_ptrs, sfb_ptrs, padded_offsets, m_
 
 
 def hq_gemm_dglu_discrete(a, b_ptrs, c, padded_offsets, alpha, prob, dprob, n, act="dswiglu", beta=None,
-                          dbias=None, d_row=None, workspace=None, sm_count=-1, stream=None):
-    """BF16 grouped GEMM + dSwiGLU / dGeGLU with per-expert K-major BF16 weights
-    [n, k] at b_ptrs (device int64 [L]).  dprob (and dbias) accumulate (+=)."""
+                          dbias=None, d_row=None, workspace=None, sm_count=-1, stream=None, b_major="k"):
+    """BF16 grouped GEMM + dSwiGLU / dGeGLU with per-expert BF16 weights at
+    b_ptrs (device int64 [L]): K-major [n, k] (b_major "k") or N-major [k, n]
+    (b_major "n", hq_gemm_dglu_discrete_nmajor).  dprob (and dbias)
+    accumulate (+=)."""
     m, k = a.shape
     L = padded_offsets.numel()
+    lib = _abi.load()
+    if b_major not in ("k", "n"):
+        raise ValueError("b_major is 'k' or 'n'")
     if d_row is None:
         d_row = torch.empty(m, 2 * n, dtype=torch.bfloat16, device=a.device)
     if workspace is None:
-        workspace = torch.empty(hq_gemm_discrete_workspace_size(L, n if dbias is not None else 0),
-                                dtype=torch.uint8, device=a.device)
+        size = (lib.hq_gemm_dglu_discrete_nmajor_workspace_size(L, n, k, 1 if dbias is not None else 0)
+                if b_major == "n" else hq_gemm_discrete_workspace_size(L, n if dbias is not None else 0))
+        workspace = torch.empty(size, dtype=torch.uint8, device=a.device)
     acts = {"dswiglu": 0, "dgeglu": 1}
-    rc = _abi.load().hq_gemm_dglu_discrete(
+    fn, name = ((lib.hq_gemm_dglu_discrete_nmajor, "hq_gemm_dglu_discrete_nmajor") if b_major == "n"
+                else (lib.hq_gemm_dglu_discrete, "hq_gemm_dglu_discrete"))
+    rc = fn(
         _ptr(a), _ptr(b_ptrs), _ptr(c), _ptr(padded_offsets), L, _ptr(alpha), _ptr(beta), _ptr(prob),
         acts[act], _ptr(d_row), _ptr(dprob), _ptr(dbias), m, n, k, _ptr(workspace), workspace.numel(),
         sm_count, _stream(stream))
-    _check(rc, "hq_gemm_dglu_discrete")
+    _check(rc, name)
     return d_row, dprob, dbias

@@ -71,6 +71,9 @@ SIGNATURES = {
     "hq_gemm_dglu_bs_typed": (c_i32, [c_p, c_p, c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_p, c_i32, c_p, c_p,
                                       c_p, c_p, c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_i32, c_i32, c_p,
                                       c_sz, c_i32, c_p]),
+    "hq_gemm_dglu_discrete_nmajor_workspace_size": (c_sz, [c_i32, c_i64, c_i64, c_i32]),
+    "hq_gemm_dglu_discrete_nmajor": (c_i32, [c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_p, c_i32, c_p, c_p, c_p,
+                                             c_i64, c_i64, c_i64, c_p, c_sz, c_i32, c_p]),
     "hq_gemm_grouped_rows": (c_i32, [c_p, c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_p, c_i64, c_i64,
                                      c_i64, c_i32, c_p, c_sz, c_i32, c_p]),
     "hq_gemm_grouped_rows_workspace_size": (c_sz, [c_i64, c_i32]),

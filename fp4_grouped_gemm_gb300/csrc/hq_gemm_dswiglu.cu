@@ -415,6 +415,63 @@ size_t hq_gemm_dswiglu_workspace_size(int L, int64_t n) {
 }  // extern "C"
 
 namespace hq {
+
+// ---------------------------------------------------------------------------
+// N-major discrete BF16 weights (cuDNN frontend "Grouped GEMM + dGLU (SM100)",
+// BF16 contract, discrete b_ptrs with b_major = "n"): expert g's B is stored
+// [k, n] (n contiguous).  A transpose pass writes a K-major copy of each
+// expert into the caller's workspace (coalesced reads along n and writes
+// along k through a shared-memory tile) and the expert's pointer list, which
+// the K-major discrete path then consumes.  An expert whose pointer is null
+// or not 16-byte aligned gets pointer 0 (skipped downstream, flagged).
+// ---------------------------------------------------------------------------
+size_t nmajor_copy_bytes(int64_t n, int64_t k) {
+  return (static_cast<size_t>(n) * static_cast<size_t>(k) * 2 + 255) / 256 * 256;
+}
+
+namespace {
+constexpr int kTr = 64;  // transpose tile (elements per side)
+
+__global__ void __launch_bounds__(256) nmajor_transpose_kernel(const int64_t* b_ptrs, uint16_t* copies,
+                                                              int64_t* ptrs, int64_t n, int64_t k,
+                                                              size_t copy_elems, uint32_t* status) {
+  __shared__ uint16_t tile[kTr][kTr + 2];
+  const int g = blockIdx.z;
+  const uint64_t src_addr = static_cast<uint64_t>(__ldg(b_ptrs + g));
+  const bool good = src_addr != 0 && (src_addr & 15u) == 0;
+  uint16_t* dst = copies + static_cast<size_t>(g) * copy_elems;
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    ptrs[g] = good ? static_cast<int64_t>(reinterpret_cast<uintptr_t>(dst)) : 0;
+    if (!good) atomicOr(status, HQ_STATUS_BAD_POINTER);
+  }
+  if (!good) return;  // block-uniform
+  const uint16_t* src = reinterpret_cast<const uint16_t*>(src_addr);
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kTr;  // source columns (n)
+  const int64_t k0 = static_cast<int64_t>(blockIdx.y) * kTr;  // source rows (k)
+  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;     // 64 x 4 threads
+  for (int r = ty; r < kTr; r += 4) {
+    const int64_t kk = k0 + r, nn = n0 + tx;
+    tile[r][tx] = (kk < k && nn < n) ? src[kk * n + nn] : 0;
+  }
+  __syncthreads();
+  for (int r = ty; r < kTr; r += 4) {
+    const int64_t nn = n0 + r, kk = k0 + tx;
+    if (nn < n && kk < k) dst[nn * k + kk] = tile[tx][r];
+  }
+}
+}  // namespace
+
+int nmajor_to_kmajor(const int64_t* b_ptrs, uint16_t* copies, int64_t* ptrs, int L, int64_t n, int64_t k,
+                     cudaStream_t st) {
+  uint32_t* status = status_word_ptr();
+  if (!status) return HQ_ERR_CUDA;
+  const dim3 grid(static_cast<unsigned>((n + kTr - 1) / kTr), static_cast<unsigned>((k + kTr - 1) / kTr),
+                  static_cast<unsigned>(L));
+  if (grid.y > 65535u) return HQ_ERR_INVALID;
+  nmajor_transpose_kernel<<<grid, 256, 0, st>>>(b_ptrs, copies, ptrs, n, k, nmajor_copy_bytes(n, k) / 2, status);
+  return cudaGetLastError() == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
+}
+
 namespace {
 
 // b: stacked weights [L, n, k]; or b == null and b_ptrs: one device pointer
@@ -542,6 +599,38 @@ int hq_gemm_dgeglu(const hq_bf16* a, const hq_bf16* b, const hq_bf16* c,
                    void* workspace, size_t ws_bytes, int sm_count, hq_stream_t s) {
   return hq::run_dglu<hq::kGeGLU>(a, b, nullptr, c, padded_offsets, L, alpha, nullptr, prob, d_row, dprob,
                                   dbias, m, n, k, workspace, ws_bytes, sm_count, s);
+}
+
+size_t hq_gemm_dglu_discrete_nmajor_workspace_size(int L, int64_t n, int64_t k, int with_dbias) {
+  if (L < 1 || n <= 0 || k <= 0) return 0;
+  return static_cast<size_t>(L) * hq::nmajor_copy_bytes(n, k) + (static_cast<size_t>(L) * 8 + 255) / 256 * 256 +
+         hq_gemm_discrete_workspace_size(L, with_dbias ? n : 0);
+}
+
+int hq_gemm_dglu_discrete_nmajor(const hq_bf16* a, const int64_t* b_ptrs, const hq_bf16* c,
+                                 const int32_t* padded_offsets, int L, const float* alpha,
+                                 const float* beta, const float* prob, int act, hq_bf16* d_row,
+                                 float* dprob, hq_bf16* dbias, int64_t m, int64_t n, int64_t k,
+                                 void* workspace, size_t ws_bytes, int sm_count, hq_stream_t s) {
+  if (!b_ptrs || (reinterpret_cast<uintptr_t>(b_ptrs) & 7u)) return HQ_ERR_INVALID;
+  if (act != 0 && act != 1) return HQ_ERR_INVALID;
+  if (L < 1 || L > hq::kMaxGroups || n <= 0 || k <= 0 || n % 32 != 0 || k % 8 != 0) return HQ_ERR_INVALID;
+  if (n > (1ll << 28) || k > (1ll << 30) || m < 0) return HQ_ERR_INVALID;
+  const size_t need = hq_gemm_dglu_discrete_nmajor_workspace_size(L, n, k, dbias != nullptr);
+  if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return HQ_ERR_INVALID;
+  if (m == 0) return HQ_OK;
+  // workspace: [K-major copies of the experts' weights] [their pointers]
+  //            [the discrete path's tensor maps, flags and dbias sums]
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t copies = static_cast<size_t>(L) * hq::nmajor_copy_bytes(n, k);
+  int64_t* ptrs = reinterpret_cast<int64_t*>(ws + copies);
+  uint8_t* rest = ws + copies + (static_cast<size_t>(L) * 8 + 255) / 256 * 256;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
+  int rc = hq::nmajor_to_kmajor(b_ptrs, reinterpret_cast<uint16_t*>(ws), ptrs, L, n, k, st);
+  if (rc != HQ_OK) return rc;
+  return hq_gemm_dglu_discrete(a, ptrs, c, padded_offsets, L, alpha, beta, prob, act, d_row, dprob, dbias,
+                               m, n, k, rest, ws_bytes - static_cast<size_t>(rest - ws), sm_count, s);
 }
 
 int hq_gemm_dglu_discrete(const hq_bf16* a, const int64_t* b_ptrs, const hq_bf16* c,

@@ -55,6 +55,12 @@ inline size_t discrete_maps_bytes(int L) {
   return (static_cast<size_t>(L) * (sizeof(CUtensorMap) + sizeof(int32_t)) + 255) / 256 * 256;
 }
 
+// N-major discrete BF16 weights: bytes of one expert's K-major copy (256-byte
+// multiple), and the pass that writes every expert's copy and pointer.
+size_t nmajor_copy_bytes(int64_t n, int64_t k);
+int nmajor_to_kmajor(const int64_t* b_ptrs, uint16_t* copies, int64_t* ptrs, int L, int64_t n, int64_t k,
+                     cudaStream_t st);
+
 // Launches the kernel that turns b_ptrs (and the checks of sfb_ptrs, which
 // may be null) into per-expert tensor maps built from tmpl.  Returns HQ_OK or
 // HQ_ERR_CUDA.

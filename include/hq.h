@@ -497,13 +497,29 @@ int hq_gemm_dglu_bs_discrete(const void *a, const uint8_t *sfa, const int64_t *b
 
 /* hq_gemm_dswiglu (act 0) / hq_gemm_dgeglu (act 1) with discrete BF16
  * weights: b_ptrs[g] -> K-major BF16 [n, k] (the BF16 contract's
- * b_major = "k"; N-major per-expert weights are not supported).  beta as
+ * b_major = "k"; N-major per-expert weights: hq_gemm_dglu_discrete_nmajor).  beta as
  * hq_gemm_dswiglu (ignored, may be NULL, for act 1). */
 int hq_gemm_dglu_discrete(const hq_bf16 *a, const int64_t *b_ptrs, const hq_bf16 *c,
                           const int32_t *padded_offsets, int L, const float *alpha,
                           const float *beta, const float *prob, int act, hq_bf16 *d_row,
                           float *dprob, hq_bf16 *dbias, int64_t m, int64_t n, int64_t k,
                           void *workspace, size_t ws_bytes, int sm_count, hq_stream_t s);
+
+/* hq_gemm_dglu_discrete with N-major per-expert BF16 weights (the BF16
+ * contract's discrete b_major = "n"): b_ptrs[g] -> BF16 [k, n], n
+ * contiguous, 16-byte aligned.  A transpose pass first writes a K-major copy
+ * of every expert into the workspace, then the K-major discrete path runs on
+ * the copies; an expert whose pointer is null or unaligned is skipped and
+ * flagged (HQ_STATUS_BAD_POINTER) as there.
+ *   workspace  hq_gemm_dglu_discrete_nmajor_workspace_size(L, n, k,
+ *              dbias != NULL) bytes, 256-byte aligned, caller-owned
+ * Arguments, results and errors otherwise as hq_gemm_dglu_discrete. */
+size_t hq_gemm_dglu_discrete_nmajor_workspace_size(int L, int64_t n, int64_t k, int with_dbias);
+int hq_gemm_dglu_discrete_nmajor(const hq_bf16 *a, const int64_t *b_ptrs, const hq_bf16 *c,
+                                 const int32_t *padded_offsets, int L, const float *alpha,
+                                 const float *beta, const float *prob, int act, hq_bf16 *d_row,
+                                 float *dprob, hq_bf16 *dbias, int64_t m, int64_t n, int64_t k,
+                                 void *workspace, size_t ws_bytes, int sm_count, hq_stream_t s);
 
 /* ------------------------------------------------------------------------- *
  * hq_gemm_dswiglu without caller-provided scratch.  The paper has no

@@ -228,6 +228,22 @@ def test_noalloc_dswiglu_rejects_oversized_scratch(lib):
         == _abi.HQ_ERR_INVALID
 
 
+def test_nmajor_discrete_dglu_rejects_bad_arguments(lib):
+    p = ctypes.c_void_p(4096)
+    size = lib.hq_gemm_dglu_discrete_nmajor_workspace_size(4, 128, 256, 1)
+    assert size >= 4 * 128 * 256 * 2
+    assert lib.hq_gemm_dglu_discrete_nmajor_workspace_size(0, 128, 256, 1) == 0
+    ws = ctypes.c_void_p(1 << 20)
+    args = lambda b_ptrs, act, n, k, ws_bytes: (p, b_ptrs, p, p, 4, p, p, p, act, p, p, None, 256, n, k, ws,
+                                                ws_bytes, -1, None)
+    assert lib.hq_gemm_dglu_discrete_nmajor(*args(None, 0, 128, 256, size)) == _abi.HQ_ERR_INVALID
+    assert lib.hq_gemm_dglu_discrete_nmajor(*args(ctypes.c_void_p(4100), 0, 128, 256, size)) == _abi.HQ_ERR_INVALID
+    assert lib.hq_gemm_dglu_discrete_nmajor(*args(p, 2, 128, 256, size)) == _abi.HQ_ERR_INVALID
+    assert lib.hq_gemm_dglu_discrete_nmajor(*args(p, 0, 100, 256, size)) == _abi.HQ_ERR_INVALID
+    size0 = lib.hq_gemm_dglu_discrete_nmajor_workspace_size(4, 128, 256, 0)   # no dbias
+    assert lib.hq_gemm_dglu_discrete_nmajor(*args(p, 0, 128, 256, size0 - 1)) == _abi.HQ_ERR_INVALID
+
+
 def test_knobs_validate(lib):
     assert lib.hq_set_gemm_tile_n(96) == _abi.HQ_ERR_INVALID
     assert lib.hq_set_gemm_tile_n(0) == _abi.HQ_OK

@@ -227,3 +227,49 @@ def test_block_scaled_dglu_discrete_matches_stacked(cuda_dev):
                  what="discrete FP8 D_row vs oracle")
     assert (codes[~wr] == 0x5A).all(), "rows past the last group written"
     assert_dglu_oracle(ref, p1, b1)
+
+
+@pytest.mark.parametrize("act", ["dswiglu", "dgeglu"])
+def test_bf16_dglu_discrete_n_major(cuda_dev, act):
+    """N-major per-expert BF16 weights (b_major = "n": expert g stored [k, n])
+    give the K-major discrete result bit for bit, and the oracle's within the
+    dGLU bounds; an expert with a null pointer is skipped and flagged."""
+    offsets = [256, 256, 768, 1024]
+    L, m, n, k = 4, 1152, 128, 320
+    a, w, c, prob, alpha, beta, off = _dglu_inputs(5, L, m, n, k, offsets)
+    b_ptrs_k, _, keep_k = separate_copies(w, None, L)
+    w_nmajor = [w[e].t().contiguous() for e in range(L)]                 # [k, n], n contiguous
+    b_ptrs_n = torch.tensor([t.data_ptr() for t in w_nmajor], dtype=torch.int64, device="cuda")
+    outs = []
+    for ptrs, major in ((b_ptrs_k, "k"), (b_ptrs_n, "n")):
+        dprob = torch.zeros(m, device="cuda")
+        dbias = torch.zeros(L, 2 * n, dtype=torch.bfloat16, device="cuda")
+        d = sentinel_bf16((m, 2 * n))
+        hq.hq_gemm_dglu_discrete(a, ptrs, c, off, alpha, prob, dprob, n, act=act,
+                                 beta=beta if act == "dswiglu" else None, dbias=dbias, d_row=d, b_major=major)
+        torch.cuda.synchronize()
+        outs.append((d, dprob, dbias))
+    (dk, pk, bk), (dn, pn, bn) = outs
+    assert torch.equal(dk.view(torch.int16), dn.view(torch.int16))
+    assert_sums_close(pn, pk, bn, bk)
+    args = (np_f32(a), np_f32(w), np_f32(c), offsets, alpha.cpu().numpy())
+    ref = (glu.dswiglu(*args, beta.cpu().numpy(), prob.cpu().numpy()) if act == "dswiglu"
+           else glu.dgeglu(*args, prob.cpu().numpy()))
+    D = dn.float().cpu().numpy().astype(np.float64)
+    tol = 2.0 ** -8 * np.abs(ref["D"]) + 2.0 ** -20 * ref["D_mag"] + 1e-30
+    assert not ((np.abs(D - ref["D"]) > tol) & ref["written"][:, None]).any()
+    assert_rows_untouched(dn, ref["written"], "N-major D_row")
+    assert_dglu_oracle(ref, pn, bn)
+    # a null expert pointer: that expert's rows untouched, flag set
+    hq.get_device_status(clear=True)
+    bad = b_ptrs_n.clone()
+    bad[2] = 0
+    d = sentinel_bf16((m, 2 * n))
+    hq.hq_gemm_dglu_discrete(a, bad, c, off, alpha, prob, torch.zeros(m, device="cuda"), n, act=act,
+                             beta=beta if act == "dswiglu" else None, d_row=d, b_major="n")
+    torch.cuda.synchronize()
+    status, _ = hq.get_device_status(clear=True)
+    assert status & hq._abi.HQ_STATUS_BAD_POINTER
+    assert (bits16(d)[256:768] == 0xAAAA).all(), "rows of the skipped expert written"
+    assert torch.equal(d[:256].view(torch.int16), dk[:256].view(torch.int16))
+    del keep_k, w_nmajor
