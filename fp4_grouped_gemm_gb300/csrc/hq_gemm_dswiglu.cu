@@ -38,20 +38,38 @@ constexpr int kEpiWarps = 8;      // two per TMEM lane quarter, two 32-column ch
 constexpr int kChunksPerWarp = 16 / kEpiWarps;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kBN = 128;          // compact columns per tile
-constexpr int kBKElems = 64;      // BF16 elements of K per stage (128 bytes)
-constexpr int kStages = 4;
+constexpr int kBKElems = 64;      // BF16 elements of K per k-block (128 bytes)
 constexpr int kAcc = 2;
 constexpr int kTmemCols = kAcc * kBN;
-constexpr int kABytes = kBM * kBKElems * 2;
-constexpr int kBBytes = kBN * kBKElems * 2;
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kStages * kABytes;
-constexpr int kOffTable = kOffB + kStages * kBBytes;
-constexpr int kOffBar = (kOffTable + 2 * (kMaxGroups + 1) * 4 + 15) / 16 * 16;
-constexpr int kNumBars = 2 * kStages + 2 * kAcc + 1;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+constexpr int kABytes = kBM * kBKElems * 2;  // one k-block of A (16 KB)
+constexpr int kBBytes = kBN * kBKElems * 2;  // one k-block of B (16 KB)
+
+constexpr int kEpiBytes = 32 * 128;          // one epilogue warp's C / D_row buffer
+constexpr int kSmemMax = 232448;
+
+// Shared-memory plan for KPS k-blocks per pipeline stage.  The copy engine's
+// cost is per copy more than per byte, so when K is a whole number of
+// k-blocks each stage loads two k-blocks of A and of B as one 32 KB box per
+// operand (a view of the [rows, K] matrix with the k-block as its outer
+// dimension), three stages deep; otherwise one 16 KB box each, four deep.
+// The group table (2 x (L + 1) int32) closes the block and is sized at launch.
+template <int KPS>
+struct DsCfg {
+  static constexpr int kStages = KPS == 1 ? 4 : 3;
+  static constexpr int kAStage = KPS * kABytes;
+  static constexpr int kBStage = KPS * kBBytes;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kStages * kAStage;
+  static constexpr int kOffEpi = kOffB + kStages * kBStage;  // 1024-aligned (TMA swizzle)
+  static constexpr int kOffBar = kOffEpi + kEpiWarps * kEpiBytes;
+  static constexpr int kNumBars = 2 * kStages + 2 * kAcc + 1 + kEpiWarps;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kOffTable = kOffMisc + 16;
+  // bytes for L groups (+1024: the dynamic block is aligned up to 1024 in the kernel)
+  static constexpr int64_t smem_bytes(int L) { return kOffTable + 8 * (static_cast<int64_t>(L) + 1) + 1024; }
+  static_assert(kOffEpi % 1024 == 0, "epilogue buffers 1024-aligned");
+};
+static_assert(DsCfg<1>::smem_bytes(kMaxGroups) <= kSmemMax, "shared memory budget");
 // kind::f16 instruction descriptor: D f32, A/B bf16, K-major, M=128, N=128
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                             (static_cast<uint32_t>(kBN >> 3) << 17) |
@@ -85,17 +103,13 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 enum Act : int { kSwiGLU = 0, kGeGLU = 1 };
 
 // dGLU of one 32-column chunk (compact columns [j0, j0 + 32)) for the calling
-// thread's row: r holds alpha_g^2-unscaled accumulator values (R = a2 r), cv the
-// row's 32 gate then 32 input C values; writes the row's D_row segment and
-// dprob partial (row_ok), and the warp's dbias column sums (when requested).
+// thread's row: r holds the alpha_g^2-unscaled accumulator values (R = a2 r),
+// cv the row's 32 gate then 32 input C values; produces the row's 32 gate and
+// 32 input D values (float32) and its dprob partial.
 template <int ACT>
-__device__ __forceinline__ void dglu_row_chunk(const DsParams& p, const uint32_t (&r)[32],
-                                               const uint4 (&cv)[8], bool row_ok, int64_t row,
-                                               int64_t j0, int g, float a2, float beta,
-                                               float prob, int lane) {
-  const int64_t two_n = 2 * p.n;
-  const int64_t cbase = row * two_n + 2 * j0;
-  float dg[32], di[32];
+__device__ __forceinline__ void dglu_row_math(const uint32_t (&r)[32], const uint4 (&cv)[8], float a2,
+                                              float beta, float prob, float (&dg)[32], float (&di)[32],
+                                              float& dprob_part) {
   // per element pair (2i, 2i+1), in packed f32x2 arithmetic; dprob is
   // accumulated pairwise and the two halves added at the end
   float dp0 = 0.0f, dp1 = 0.0f;
@@ -153,52 +167,47 @@ __device__ __forceinline__ void dglu_row_chunk(const DsParams& p, const uint32_t
       fma_f32x2(dp0, dp1, q0, q1, up0, up1, dp0, dp1);           // += R gate_c s (up_c + 1)
     }
   }
-  const float dprob_part = dp0 + dp1;
-  if (row_ok) {
-    uint32_t w[32];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      __nv_bfloat162 bg = __floats2bfloat162_rn(dg[2 * i], dg[2 * i + 1]);
-      __nv_bfloat162 bi = __floats2bfloat162_rn(di[2 * i], di[2 * i + 1]);
-      w[i] = *reinterpret_cast<uint32_t*>(&bg);
-      w[16 + i] = *reinterpret_cast<uint32_t*>(&bi);
-    }
-    uint4* dst = reinterpret_cast<uint4*>(p.d_row + cbase);
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-    atomicAdd(p.dprob + row, dprob_part);
-  }
-  if (p.dbias_ws) {
-    // column sums over the warp's 32 rows by a butterfly reduce-scatter:
-    // afterwards lane l holds the sums of gate column l and input column l
-    if (!row_ok) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) { dg[i] = 0.0f; di[i] = 0.0f; }
-    }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      const bool upper = (lane & o) != 0;
-#pragma unroll
-      for (int i = 0; i < o; ++i) {
-        const float sg = upper ? dg[i] : dg[i + o];
-        const float si = upper ? di[i] : di[i + o];
-        const float kg = upper ? dg[i + o] : dg[i];
-        const float ki = upper ? di[i + o] : di[i];
-        dg[i] = kg + __shfl_xor_sync(0xFFFFFFFFu, sg, o);
-        di[i] = ki + __shfl_xor_sync(0xFFFFFFFFu, si, o);
-      }
-    }
-    float* ws = p.dbias_ws + static_cast<int64_t>(g) * two_n + 2 * j0;
-    atomicAdd(ws + lane, dg[0]);
-    atomicAdd(ws + 32 + lane, di[0]);
-  }
+  dprob_part = dp0 + dp1;
 }
 
-template <int ACT>
+// Column sums of the warp's 32 rows by a butterfly reduce-scatter (afterwards
+// lane l holds the sums of gate column l and input column l), added to the
+// float32 dbias workspace with one atomic per column.
+__device__ __forceinline__ void dbias_reduce(const DsParams& p, float (&dg)[32], float (&di)[32], int g,
+                                             int64_t j0, int lane) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float sg = upper ? dg[i] : dg[i + o];
+      const float si = upper ? di[i] : di[i + o];
+      const float kg = upper ? dg[i + o] : dg[i];
+      const float ki = upper ? di[i + o] : di[i];
+      dg[i] = kg + __shfl_xor_sync(0xFFFFFFFFu, sg, o);
+      di[i] = ki + __shfl_xor_sync(0xFFFFFFFFu, si, o);
+    }
+  }
+  float* ws = p.dbias_ws + static_cast<int64_t>(g) * (2 * p.n) + 2 * j0;
+  atomicAdd(ws + lane, dg[0]);
+  atomicAdd(ws + 32 + lane, di[0]);
+}
+
+// A warp's 4 KB epilogue buffer holds 32 rows x 128 bytes (one chunk's C or
+// D_row segment: 32 gate then 32 input BF16 values per row) in the TMA
+// 128-byte swizzle: 16-byte unit u of row r sits at unit u ^ (r & 7), so the
+// eight lanes of a 16-byte access phase, one row each, hit distinct banks.
+__device__ __forceinline__ uint32_t epi_unit(uint32_t buf, int row, int u) {
+  return buf + static_cast<uint32_t>(row) * 128u + (static_cast<uint32_t>(u ^ (row & 7)) << 4);
+}
+
+template <int ACT, int KPS>
 __global__ void __launch_bounds__(kThreads, 1)
     dglu_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                 const DsParams p) {
+  using C = DsCfg<KPS>;
+  constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -206,17 +215,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  int32_t* tab0 = reinterpret_cast<int32_t*>(smem + kOffTable);
-  int32_t* tab1 = tab0 + (kMaxGroups + 1);
-  const uint32_t bar0 = sbase + kOffBar;
+  int32_t* tab0 = reinterpret_cast<int32_t*>(smem + C::kOffTable);
+  int32_t* tab1 = tab0 + (p.gs.groups + 1);
+  const uint32_t bar0 = sbase + C::kOffBar;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + kAcc + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 2 * kAcc);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
-  int64_t* total_mtiles_s = reinterpret_cast<int64_t*>(smem + kOffMisc + 8);
+  const uint32_t cbar0 = bar0 + 8u * (2 * kStages + 2 * kAcc + 1);  // one per epilogue warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  int64_t* total_mtiles_s = reinterpret_cast<int64_t*>(smem + C::kOffMisc + 8);
 
   if (warp == 0 && lane == 0) {
     *abort_flag = 0;
@@ -229,9 +239,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tempty_bar(a), kEpiWarps);
     }
     mbar_init(drain_bar, 1);
+    for (int w = 0; w < kEpiWarps; ++w) mbar_init(cbar0 + 8u * w, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
+    tma_prefetch_desc(&tmD);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -248,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   sch.tab0 = tab0;
   sch.tab1 = tab1;
   const int num_kb = static_cast<int>((p.k + kBKElems - 1) / kBKElems);
+  const int num_st = (num_kb + KPS - 1) / KPS;  // stages per tile (an odd tail k-block loads zeros)
   const WaitCtx wctx{p.gs.status, abort_flag, p.wait_limit_ns};
 
   if (warp == 0) {
@@ -270,15 +284,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             map_g = ti.g;
           }
         }
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int si = 0; si < num_st; ++si) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, wctx)) { ok = false; break; }
           // a skipped expert's stage holds stale B data; its results are never stored
-          mbar_arrive_expect_tx(full_bar(stage), kABytes + (w_ok ? kBBytes : 0u));
-          tma_load_2d(sbase + kOffA + stage * kABytes, &tmA, full_bar(stage), kb * kBKElems,
-                      static_cast<int32_t>(ti.row0));
-          if (w_ok)
-            tma_load_3d(sbase + kOffB + stage * kBBytes, mapB, full_bar(stage), kb * kBKElems, ti.n0,
-                        zb);
+          mbar_arrive_expect_tx(full_bar(stage), C::kAStage + (w_ok ? C::kBStage : 0u));
+          const uint32_t dA = sbase + C::kOffA + stage * C::kAStage;
+          const uint32_t dB = sbase + C::kOffB + stage * C::kBStage;
+          if (KPS == 1) {
+            tma_load_2d(dA, &tmA, full_bar(stage), si * kBKElems, static_cast<int32_t>(ti.row0));
+            if (w_ok) tma_load_3d(dB, mapB, full_bar(stage), si * kBKElems, ti.n0, zb);
+          } else {
+            tma_load_3d(dA, &tmA, full_bar(stage), 0, static_cast<int32_t>(ti.row0), si * KPS);
+            if (w_ok) tma_load_4d(dB, mapB, full_bar(stage), 0, ti.n0, si * KPS, zb);
+          }
           filled_mask |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -294,21 +312,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       // the tensor pipe keeps only about one MMA queued behind the executing
       // one: descriptors advance by constants and the MMAs are unrolled
-      const uint64_t adesc0 = smem_desc_sw128(sbase + kOffA);
-      const uint64_t bdesc0 = smem_desc_sw128(sbase + kOffB);
+      const uint64_t adesc0 = smem_desc_sw128(sbase + C::kOffA);
+      const uint64_t bdesc0 = smem_desc_sw128(sbase + C::kOffB);
       for (int64_t t = blockIdx.x; ok && t < sch.total_tiles; t += gridDim.x) {
         if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, wctx)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBN;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int si = 0; si < num_st; ++si) {
           if (!wait_bounded(full_bar(stage), phase, wctx)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t ad = adesc0 + static_cast<uint64_t>((stage * kABytes) >> 4);
-          const uint64_t bd = bdesc0 + static_cast<uint64_t>((stage * kBBytes) >> 4);
-          const uint32_t acc0 = kb > 0 ? 1u : 0u;
+          const uint64_t ad = adesc0 + static_cast<uint64_t>((stage * C::kAStage) >> 4);
+          const uint64_t bd = bdesc0 + static_cast<uint64_t>((stage * C::kBStage) >> 4);
+          const uint32_t acc0 = si > 0 ? 1u : 0u;
 #pragma unroll
-          for (int j = 0; j < 4; ++j)  // 4 x K=16 per 128-byte swizzle row (32 bytes each)
-            mma_bf16(d_tmem, ad + 2 * j, bd + 2 * j, kIdesc, j > 0 ? 1u : acc0);
+          for (int kk = 0; kk < KPS; ++kk)  // k-block kk of the stage: 16 KB further on
+#pragma unroll
+            for (int j = 0; j < 4; ++j)  // 4 x K=16 per 128-byte swizzle row (32 bytes each)
+              mma_bf16(d_tmem, ad + static_cast<uint64_t>((kk * kABytes) >> 4) + 2 * j,
+                       bd + static_cast<uint64_t>((kk * kBBytes) >> 4) + 2 * j, kIdesc,
+                       (kk > 0 || j > 0) ? 1u : acc0);
           tc_commit(empty_bar(stage));
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
@@ -320,38 +342,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_drain(drain_bar, 0, p.wait_limit_ns);
     }
   } else {
-    const int q = warp & 3;          // TMEM lane quarter this warp may access
-    const int cg = (warp - 2) >> 2;  // the warp's chunks: cg * kChunksPerWarp + 0, 1, ...
-    const int64_t two_n = 2 * p.n;
+    // Each epilogue warp owns one TMEM lane quarter (q) and 32 rows of every
+    // tile, and two of its four 32-column chunks.  Per chunk: the C segment
+    // [32 rows x 64 values] arrives by TMA in the warp's buffer, each lane
+    // reads its row, computes its D_row segment and writes it back in place,
+    // and one TMA store writes the segment to D_row.  The next chunk's C load
+    // is issued once that store has read the buffer, so it overlaps the dbias
+    // reduction and the next accumulator wait.  Contiguous-schedule tiles are
+    // whole 128-row tiles (group ends are multiples of 128), so every row of
+    // a warp's segment is written.
+    const int ew = warp - 2;
+    const int q = warp & 3;           // TMEM lane quarter this warp may access
+    const int cg = ew >> 2;           // the warp's chunks: cg * kChunksPerWarp + 0, 1, ...
+    const uint32_t eb = sbase + C::kOffEpi + ew * kEpiBytes;
+    const uint32_t cbar = cbar0 + 8u * ew;
+    uint32_t c_phase = 0;
+    bool c_pending = false;
+    auto chunk_live = [&](const TileInfo& ti, int c) -> bool {
+      return ti.n0 + c * 32 < p.n && (!p.w_ok || __ldg(p.w_ok + ti.g) != 0);
+    };
+    auto load_c = [&](const TileInfo& ti, int c) {
+      if (lane == 0) {
+        bulk_wait_group_read0();  // the previous D store has read the buffer
+        mbar_arrive_expect_tx(cbar, kEpiBytes);
+        tma_load_2d(eb, &tmC, cbar, static_cast<int32_t>(2 * (ti.n0 + c * 32)),
+                    static_cast<int32_t>(ti.row0 + q * 32));
+      }
+      c_pending = true;
+    };
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int64_t t = blockIdx.x; t < sch.total_tiles; t += gridDim.x) {
-      const TileInfo ti = decode_tile(p.gs, sch, t, kBN);
-      const int r_local = q * 32 + lane;
-      const bool row_ok = r_local < ti.rows_valid;
-      const int64_t row = ti.row0 + r_local;
-      // a skipped expert (discrete weights) writes nothing
-      const bool tile_ok = !p.w_ok || __ldg(p.w_ok + ti.g) != 0;
+    int64_t t = blockIdx.x;
+    TileInfo ti{};
+    if (t < sch.total_tiles) {
+      ti = decode_tile(p.gs, sch, t, kBN);
+      if (chunk_live(ti, cg * kChunksPerWarp)) load_c(ti, cg * kChunksPerWarp);
+    }
+    bool ok = true;
+    for (; ok && t < sch.total_tiles; t += gridDim.x) {
+      const int64_t row = ti.row0 + q * 32 + lane;
       const float alpha = __ldg(p.alpha + ti.g);
       const float a2 = __fmul_rn(alpha, alpha);
       const float beta = ACT == kSwiGLU ? __ldg(p.beta + ti.g) : 1.0f;
-      const float prob = row_ok ? __ldg(p.prob + row) : 0.0f;
-      bool ok = true;
+      const float prob = __ldg(p.prob + row);
 #pragma unroll 1
       for (int cc = 0; cc < kChunksPerWarp; ++cc) {
         const int c = cg * kChunksPerWarp + cc;
         const int64_t j0 = ti.n0 + c * 32;
-        // n % 32 == 0: a chunk is all in or all out
-        const bool chunk_ok = j0 < p.n && tile_ok;
-        // this row's C segment (32 gate then 32 input values) is loaded before
-        // its accumulator columns are read, so its latency overlaps the wait
-        uint4 cv[8];
-        {
-          const bool ld = row_ok && chunk_ok;
-          const uint4* src = reinterpret_cast<const uint4*>(p.c + row * two_n + 2 * j0);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) cv[i] = ld ? __ldcs(src + i) : make_uint4(0, 0, 0, 0);
-        }
+        const bool live = chunk_live(ti, c);
         if (cc == 0) {
           const bool w = wait_bounded(tfull_bar(acc), acc_phase, wctx);
           if (!__all_sync(0xFFFFFFFFu, w)) { ok = false; break; }
@@ -366,11 +404,65 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty_bar(acc));
         }
-        if (chunk_ok) dglu_row_chunk<ACT>(p, r, cv, row_ok, row, j0, ti.g, a2, beta, prob, lane);
+        float dg[32], di[32], dprob_part = 0.0f;
+        if (live) {
+          const bool w = wait_bounded(cbar, c_phase, wctx);
+          if (!__all_sync(0xFFFFFFFFu, w)) { ok = false; break; }
+          c_pending = false;
+          c_phase ^= 1u;
+          uint4 cv[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            uint32_t v[4];
+            lds128(epi_unit(eb, lane, i), v);
+            cv[i] = make_uint4(v[0], v[1], v[2], v[3]);
+          }
+          dglu_row_math<ACT>(r, cv, a2, beta, prob, dg, di, dprob_part);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              // units 0..3: gate values 8i.., units 4..7: input values
+              const float* src = i < 4 ? dg : di;
+              const int e = (i & 3) * 8 + 4 * h;
+              __nv_bfloat162 b0 = __floats2bfloat162_rn(src[e], src[e + 1]);
+              __nv_bfloat162 b1 = __floats2bfloat162_rn(src[e + 2], src[e + 3]);
+              w4[2 * h] = *reinterpret_cast<uint32_t*>(&b0);
+              w4[2 * h + 1] = *reinterpret_cast<uint32_t*>(&b1);
+            }
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(epi_unit(eb, lane, i)),
+                         "r"(w4[0]), "r"(w4[1]), "r"(w4[2]), "r"(w4[3])
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmD, eb, static_cast<int32_t>(2 * j0), static_cast<int32_t>(ti.row0 + q * 32));
+            bulk_commit_group();
+          }
+        }
+        // the next C segment this warp reads: its next chunk of this tile, or
+        // its first chunk of its next tile
+        if (cc + 1 < kChunksPerWarp) {
+          if (chunk_live(ti, c + 1)) load_c(ti, c + 1);
+        } else if (t + gridDim.x < sch.total_tiles) {
+          const TileInfo tn = decode_tile(p.gs, sch, t + gridDim.x, kBN);
+          if (chunk_live(tn, cg * kChunksPerWarp)) load_c(tn, cg * kChunksPerWarp);
+        }
+        if (live) {
+          atomicAdd(p.dprob + row, dprob_part);
+          if (p.dbias_ws) dbias_reduce(p, dg, di, ti.g, j0, lane);
+        }
       }
       if (!ok) break;
       if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
+      if (t + gridDim.x < sch.total_tiles) ti = decode_tile(p.gs, sch, t + gridDim.x, kBN);
     }
+    // abort: a C load still in flight lands before the CTA exits; every TMA
+    // store has completed before the CTA exits
+    if (c_pending) wait_drain(cbar, c_phase, p.wait_limit_ns);
+    if (lane == 0) bulk_wait_group0();
   }
 
   __syncthreads();
@@ -529,31 +621,68 @@ int run_dglu(const hq_bf16* a, const hq_bf16* b, const int64_t* b_ptrs, const hq
   p.k = k;
   p.wait_limit_ns = wait_limit_ns();
 
+  // two k-blocks per stage when K is a whole number of at least two k-blocks
+  // (the k-block view must not run past a row's end)
+  const bool kb2 = k % kBKElems == 0 && k >= 2 * kBKElems && DsCfg<2>::smem_bytes(L) <= kSmemMax;
+  const uint64_t nkb = static_cast<uint64_t>(k / kBKElems);
   CUtensorMap tmA, tmB;
   {
-    const uint64_t dims[2] = {static_cast<uint64_t>(k), static_cast<uint64_t>(m)};
-    const uint64_t strides[1] = {static_cast<uint64_t>(k) * 2};
-    const uint32_t box[2] = {kBKElems, kBM};
-    int rc = encode_tensor_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<hq_bf16*>(a),
-                               dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    int rc;
+    if (kb2) {
+      // [rows, K] viewed as [k-block][row][64 elements]
+      const uint64_t dims[3] = {kBKElems, static_cast<uint64_t>(m), nkb};
+      const uint64_t strides[2] = {static_cast<uint64_t>(k) * 2, kBKElems * 2};
+      const uint32_t box[3] = {kBKElems, kBM, 2};
+      rc = encode_tensor_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<hq_bf16*>(a), dims,
+                             strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    } else {
+      const uint64_t dims[2] = {static_cast<uint64_t>(k), static_cast<uint64_t>(m)};
+      const uint64_t strides[1] = {static_cast<uint64_t>(k) * 2};
+      const uint32_t box[2] = {kBKElems, kBM};
+      rc = encode_tensor_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<hq_bf16*>(a), dims,
+                             strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
     if (rc != HQ_OK) return rc;
   }
   {
     // discrete weights: a one-expert map encoded over the workspace (a valid
     // address, never loaded through as it stands) whose address the device
     // replaces per expert
-    const uint64_t dims[3] = {static_cast<uint64_t>(k), static_cast<uint64_t>(n),
-                              static_cast<uint64_t>(discrete ? 1 : L)};
-    const uint64_t strides[2] = {static_cast<uint64_t>(k) * 2, static_cast<uint64_t>(k) * 2 * n};
-    const uint32_t box[3] = {kBKElems, kBN, 1};
+    const uint64_t groups = static_cast<uint64_t>(discrete ? 1 : L);
     void* base = discrete ? workspace : const_cast<hq_bf16*>(b);
-    int rc = encode_tensor_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box,
-                               CU_TENSOR_MAP_SWIZZLE_128B);
+    int rc;
+    if (kb2) {
+      const uint64_t dims[4] = {kBKElems, static_cast<uint64_t>(n), nkb, groups};
+      const uint64_t strides[3] = {static_cast<uint64_t>(k) * 2, kBKElems * 2,
+                                   static_cast<uint64_t>(k) * 2 * n};
+      const uint32_t box[4] = {kBKElems, kBN, 2, 1};
+      rc = encode_tensor_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+    } else {
+      const uint64_t dims[3] = {static_cast<uint64_t>(k), static_cast<uint64_t>(n), groups};
+      const uint64_t strides[2] = {static_cast<uint64_t>(k) * 2, static_cast<uint64_t>(k) * 2 * n};
+      const uint32_t box[3] = {kBKElems, kBN, 1};
+      rc = encode_tensor_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+    }
     if (rc != HQ_OK) return rc;
     if (discrete) {
       rc = build_weight_maps(tmB, b_ptrs, nullptr, p.b_maps, p.w_ok, L, st);
       if (rc != HQ_OK) return rc;
     }
+  }
+  // C and D_row [m, 2n]: the epilogue's 32-row x 64-value segments
+  CUtensorMap tmC, tmD;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(2 * n), static_cast<uint64_t>(m)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(2 * n) * 2};
+    const uint32_t box[2] = {64, 32};
+    int rc = encode_tensor_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<hq_bf16*>(c), dims,
+                               strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != HQ_OK) return rc;
+    rc = encode_tensor_map(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d_row, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != HQ_OK) return rc;
   }
   if (dbias) {
     const size_t bytes = static_cast<size_t>(L) * static_cast<size_t>(2 * n) * sizeof(float);
@@ -561,15 +690,20 @@ int run_dglu(const hq_bf16* a, const hq_bf16* b, const int64_t* b_ptrs, const hq
   }
   const int sms = num_sms();
   if (sms <= 0) return HQ_ERR_CUDA;
-  if (set_smem_once<dglu_kernel<ACT>>(kSmemBytes) != HQ_OK) return HQ_ERR_CUDA;
+  if (set_smem_once<dglu_kernel<ACT, 1>>(kSmemMax) != HQ_OK ||
+      set_smem_once<dglu_kernel<ACT, 2>>(kSmemMax) != HQ_OK)
+    return HQ_ERR_CUDA;
   const int64_t tiles_bound = ((m + kBM - 1) / kBM) * ((n + kBN - 1) / kBN);
   int64_t grid = sm_count > 0 ? sm_count : sms;
   if (grid > sms) grid = sms;
   if (grid > tiles_bound) grid = tiles_bound;
   if (grid < 1) grid = 1;
-  if (launch(dglu_kernel<ACT>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes, st,
-             false, tmA, tmB, p) != cudaSuccess)
-    return HQ_ERR_CUDA;
+  const cudaError_t le =
+      kb2 ? launch(dglu_kernel<ACT, 2>, dim3(static_cast<unsigned>(grid)), dim3(kThreads),
+                   static_cast<int>(DsCfg<2>::smem_bytes(L)), st, false, tmA, tmB, tmC, tmD, p)
+          : launch(dglu_kernel<ACT, 1>, dim3(static_cast<unsigned>(grid)), dim3(kThreads),
+                   static_cast<int>(DsCfg<1>::smem_bytes(L)), st, false, tmA, tmB, tmC, tmD, p);
+  if (le != cudaSuccess) return HQ_ERR_CUDA;
   if (dbias) {
     const int rc = dbias_finalize(reinterpret_cast<uint16_t*>(dbias),
                                   static_cast<const float*>(dbias_ws),

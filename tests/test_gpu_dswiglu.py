@@ -91,6 +91,17 @@ def test_dswiglu_odd_group_ends(cuda_dev):
     check(*run_case(offsets, 1536, 256, 640, seed=31))
 
 
+def test_dswiglu_many_groups(cuda_dev):
+    """300 groups (most empty): the group table outgrows the shared memory
+    left beside two-k-block stages, so the one-k-block pipeline runs; K a
+    whole number of k-blocks."""
+    sizes = [0] * 300
+    for g, r in ((0, 128), (7, 256), (150, 128), (299, 128)):
+        sizes[g] = r
+    offsets = list(np.cumsum(sizes))
+    check(*run_case(offsets, 768, 96, 256, seed=9))
+
+
 def test_dgeglu_clamp_boundaries_exact(cuda_dev):
     """Gate and up values exactly at the clamp bounds keep their gradients."""
     m, n, k = 256, 32, 64
