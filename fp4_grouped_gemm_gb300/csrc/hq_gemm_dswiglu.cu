@@ -56,7 +56,6 @@ template <int KPS, int BN>
 struct DsCfg {
   static_assert(BN == 128 || (BN == 256 && KPS == 1), "tile plans");
   static constexpr int kBBytes = BN * kBKElems * 2;   // one k-block of B
-  static constexpr int kChunksPerWarp = BN / 64;      // 32-column chunks per epilogue warp and tile
   static constexpr int kTmemCols = kAcc * BN;
   // kind::f16 instruction descriptor: D f32, A/B bf16, K-major, M = 128, N = BN
   static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
@@ -204,6 +203,158 @@ __device__ __forceinline__ uint32_t epi_unit(uint32_t buf, int row, int u) {
   return buf + static_cast<uint32_t>(row) * 128u + (static_cast<uint32_t>(u ^ (row & 7)) << 4);
 }
 
+// One tile of the epilogue as this CTA sees it: its first row, the tile's
+// first compact column, the group, and whether its rows are to be written
+// (a pair's odd half past its group's end is not).
+struct EpiTile {
+  int64_t row0;
+  int n0;
+  int g;
+  bool rows;
+};
+
+// The epilogue role of one warp (ew = warp - 2): it owns one TMEM lane
+// quarter q and 32 rows of every tile, and BN / 64 of the quarter's BN / 32
+// chunks of 32 compact columns.  Per chunk: the C segment [32 rows x 64
+// values] arrives by TMA in the warp's buffer, each lane reads its row,
+// computes its D_row segment and writes it back in place, and one TMA store
+// writes the segment to D_row.  The next chunk's C load is issued once that
+// store has read the buffer, so it overlaps the dbias reduction and the next
+// accumulator wait.  Contiguous-schedule tiles are whole 128-row blocks
+// (group ends are multiples of 128), so a warp writes all 32 rows or none.
+// Tiles t0, t0 + stride, ... < total; decode(t) describes tile t; the
+// accumulator of the i-th tile is a = i % 2 (TMEM columns a * BN), its
+// "full" barrier tfull0 + 8 a, and release(a) hands it back.
+template <int ACT, int BN, typename Decode, typename Release>
+__device__ __forceinline__ void dglu_epilogue(const DsParams& p, const CUtensorMap* tmC,
+                                              const CUtensorMap* tmD, int64_t t0, int64_t stride,
+                                              int64_t total, Decode decode, uint32_t tfull0,
+                                              Release release, uint32_t tmem_base, uint32_t eb,
+                                              uint32_t cbar, const WaitCtx& wctx, int warp, int lane) {
+  constexpr int kChunksPerWarp = BN / 64;
+  const int q = warp & 3;                // TMEM lane quarter this warp may access
+  const int cg = ((warp - 2) >> 2);      // the warp's chunks: cg * kChunksPerWarp + 0, 1, ...
+  uint32_t c_phase = 0;
+  bool c_pending = false;
+  auto chunk_live = [&](const EpiTile& et, int c) -> bool {
+    return et.rows && et.n0 + c * 32 < p.n && (!p.w_ok || __ldg(p.w_ok + et.g) != 0);
+  };
+  auto load_c = [&](const EpiTile& et, int c) {
+    if (lane == 0) {
+      bulk_wait_group_read0();  // the previous D store has read the buffer
+      mbar_arrive_expect_tx(cbar, kEpiBytes);
+      tma_load_2d(eb, tmC, cbar, static_cast<int32_t>(2 * (et.n0 + c * 32)),
+                  static_cast<int32_t>(et.row0 + q * 32));
+    }
+    c_pending = true;
+  };
+  int acc = 0;
+  uint32_t acc_phase = 0;
+  int64_t t = t0;
+  // a tile's per-row / per-group factors are loaded while the previous tile
+  // is still being processed
+  EpiTile et{0, 0, 0, false};
+  float alpha = 0.0f, beta = 1.0f, prob = 0.0f;
+  auto factors = [&](const EpiTile& e, float& al, float& be, float& pr) {
+    al = __ldg(p.alpha + e.g);
+    be = ACT == kSwiGLU ? __ldg(p.beta + e.g) : 1.0f;
+    pr = e.rows ? __ldg(p.prob + e.row0 + q * 32 + lane) : 0.0f;
+  };
+  if (t < total) {
+    et = decode(t);
+    if (chunk_live(et, cg * kChunksPerWarp)) load_c(et, cg * kChunksPerWarp);
+    factors(et, alpha, beta, prob);
+  }
+  bool ok = true;
+  for (; ok && t < total; t += stride) {
+    const int64_t row = et.row0 + q * 32 + lane;
+    const float a2 = __fmul_rn(alpha, alpha);
+    EpiTile en = et;
+    float alpha_n = alpha, beta_n = beta, prob_n = prob;
+#pragma unroll 1
+    for (int cc = 0; cc < kChunksPerWarp; ++cc) {
+      const int c = cg * kChunksPerWarp + cc;
+      const int64_t j0 = et.n0 + c * 32;
+      const bool live = chunk_live(et, c);
+      if (cc == 0) {
+        const bool w = wait_bounded(tfull0 + 8u * acc, acc_phase, wctx);
+        if (!__all_sync(0xFFFFFFFFu, w)) { ok = false; break; }
+        tc_fence_after();
+      }
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN + c * 32, r);
+      tmem_ld_wait();
+      if (cc == kChunksPerWarp - 1) {
+        // the warp's last chunk is in registers: release the accumulator
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) release(acc);
+      }
+      float dg[32], di[32], dprob_part = 0.0f;
+      if (live) {
+        const bool w = wait_bounded(cbar, c_phase, wctx);
+        if (!__all_sync(0xFFFFFFFFu, w)) { ok = false; break; }
+        c_pending = false;
+        c_phase ^= 1u;
+        uint4 cv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uint32_t v[4];
+          lds128(epi_unit(eb, lane, i), v);
+          cv[i] = make_uint4(v[0], v[1], v[2], v[3]);
+        }
+        dglu_row_math<ACT>(r, cv, a2, beta, prob, dg, di, dprob_part);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            // units 0..3: gate values 8i.., units 4..7: input values
+            const float* src = i < 4 ? dg : di;
+            const int e = (i & 3) * 8 + 4 * h;
+            __nv_bfloat162 b0 = __floats2bfloat162_rn(src[e], src[e + 1]);
+            __nv_bfloat162 b1 = __floats2bfloat162_rn(src[e + 2], src[e + 3]);
+            w4[2 * h] = *reinterpret_cast<uint32_t*>(&b0);
+            w4[2 * h + 1] = *reinterpret_cast<uint32_t*>(&b1);
+          }
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(epi_unit(eb, lane, i)),
+                       "r"(w4[0]), "r"(w4[1]), "r"(w4[2]), "r"(w4[3])
+                       : "memory");
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(tmD, eb, static_cast<int32_t>(2 * j0), static_cast<int32_t>(et.row0 + q * 32));
+          bulk_commit_group();
+        }
+      }
+      // the next C segment this warp reads: its next chunk of this tile, or
+      // its first chunk of its next tile
+      if (cc + 1 < kChunksPerWarp) {
+        if (chunk_live(et, c + 1)) load_c(et, c + 1);
+      } else if (t + stride < total) {
+        en = decode(t + stride);
+        if (chunk_live(en, cg * kChunksPerWarp)) load_c(en, cg * kChunksPerWarp);
+        factors(en, alpha_n, beta_n, prob_n);
+      }
+      if (live) {
+        atomicAdd(p.dprob + row, dprob_part);
+        if (p.dbias_ws) dbias_reduce(p, dg, di, et.g, j0, lane);
+      }
+    }
+    if (!ok) break;
+    if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
+    et = en;
+    alpha = alpha_n;
+    beta = beta_n;
+    prob = prob_n;
+  }
+  // abort: a C load still in flight lands before the CTA exits; every TMA
+  // store has completed before the CTA exits
+  if (c_pending) wait_drain(cbar, c_phase, wctx.limit_ns);
+  if (lane == 0) bulk_wait_group0();
+}
+
 template <int ACT, int KPS, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     dglu_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -212,7 +363,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = DsCfg<KPS, BN>;
   constexpr int kStages = C::kStages;
   constexpr int kBN = BN;
-  constexpr int kChunksPerWarp = C::kChunksPerWarp;
   constexpr int kBBytes = C::kBBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -348,133 +498,252 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_drain(drain_bar, 0, p.wait_limit_ns);
     }
   } else {
-    // Each epilogue warp owns one TMEM lane quarter (q) and 32 rows of every
-    // tile, and two of its four 32-column chunks.  Per chunk: the C segment
-    // [32 rows x 64 values] arrives by TMA in the warp's buffer, each lane
-    // reads its row, computes its D_row segment and writes it back in place,
-    // and one TMA store writes the segment to D_row.  The next chunk's C load
-    // is issued once that store has read the buffer, so it overlaps the dbias
-    // reduction and the next accumulator wait.  Contiguous-schedule tiles are
-    // whole 128-row tiles (group ends are multiples of 128), so every row of
-    // a warp's segment is written.
     const int ew = warp - 2;
-    const int q = warp & 3;           // TMEM lane quarter this warp may access
-    const int cg = ew >> 2;           // the warp's chunks: cg * kChunksPerWarp + 0, 1, ...
-    const uint32_t eb = sbase + C::kOffEpi + ew * kEpiBytes;
-    const uint32_t cbar = cbar0 + 8u * ew;
-    uint32_t c_phase = 0;
-    bool c_pending = false;
-    auto chunk_live = [&](const TileInfo& ti, int c) -> bool {
-      return ti.n0 + c * 32 < p.n && (!p.w_ok || __ldg(p.w_ok + ti.g) != 0);
+    auto decode = [&](int64_t t) -> EpiTile {
+      const TileInfo ti = decode_tile(p.gs, sch, t, kBN);
+      return EpiTile{ti.row0, ti.n0, ti.g, true};
     };
-    auto load_c = [&](const TileInfo& ti, int c) {
-      if (lane == 0) {
-        bulk_wait_group_read0();  // the previous D store has read the buffer
-        mbar_arrive_expect_tx(cbar, kEpiBytes);
-        tma_load_2d(eb, &tmC, cbar, static_cast<int32_t>(2 * (ti.n0 + c * 32)),
-                    static_cast<int32_t>(ti.row0 + q * 32));
-      }
-      c_pending = true;
-    };
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    int64_t t = blockIdx.x;
-    TileInfo ti{};
-    if (t < sch.total_tiles) {
-      ti = decode_tile(p.gs, sch, t, kBN);
-      if (chunk_live(ti, cg * kChunksPerWarp)) load_c(ti, cg * kChunksPerWarp);
-    }
-    bool ok = true;
-    for (; ok && t < sch.total_tiles; t += gridDim.x) {
-      const int64_t row = ti.row0 + q * 32 + lane;
-      const float alpha = __ldg(p.alpha + ti.g);
-      const float a2 = __fmul_rn(alpha, alpha);
-      const float beta = ACT == kSwiGLU ? __ldg(p.beta + ti.g) : 1.0f;
-      const float prob = __ldg(p.prob + row);
-#pragma unroll 1
-      for (int cc = 0; cc < kChunksPerWarp; ++cc) {
-        const int c = cg * kChunksPerWarp + cc;
-        const int64_t j0 = ti.n0 + c * 32;
-        const bool live = chunk_live(ti, c);
-        if (cc == 0) {
-          const bool w = wait_bounded(tfull_bar(acc), acc_phase, wctx);
-          if (!__all_sync(0xFFFFFFFFu, w)) { ok = false; break; }
-          tc_fence_after();
-        }
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN + c * 32, r);
-        tmem_ld_wait();
-        if (cc == kChunksPerWarp - 1) {
-          // the warp's last chunk is in registers: release the accumulator
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(tempty_bar(acc));
-        }
-        float dg[32], di[32], dprob_part = 0.0f;
-        if (live) {
-          const bool w = wait_bounded(cbar, c_phase, wctx);
-          if (!__all_sync(0xFFFFFFFFu, w)) { ok = false; break; }
-          c_pending = false;
-          c_phase ^= 1u;
-          uint4 cv[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            uint32_t v[4];
-            lds128(epi_unit(eb, lane, i), v);
-            cv[i] = make_uint4(v[0], v[1], v[2], v[3]);
-          }
-          dglu_row_math<ACT>(r, cv, a2, beta, prob, dg, di, dprob_part);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            uint32_t w4[4];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              // units 0..3: gate values 8i.., units 4..7: input values
-              const float* src = i < 4 ? dg : di;
-              const int e = (i & 3) * 8 + 4 * h;
-              __nv_bfloat162 b0 = __floats2bfloat162_rn(src[e], src[e + 1]);
-              __nv_bfloat162 b1 = __floats2bfloat162_rn(src[e + 2], src[e + 3]);
-              w4[2 * h] = *reinterpret_cast<uint32_t*>(&b0);
-              w4[2 * h + 1] = *reinterpret_cast<uint32_t*>(&b1);
-            }
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(epi_unit(eb, lane, i)),
-                         "r"(w4[0]), "r"(w4[1]), "r"(w4[2]), "r"(w4[3])
-                         : "memory");
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmD, eb, static_cast<int32_t>(2 * j0), static_cast<int32_t>(ti.row0 + q * 32));
-            bulk_commit_group();
-          }
-        }
-        // the next C segment this warp reads: its next chunk of this tile, or
-        // its first chunk of its next tile
-        if (cc + 1 < kChunksPerWarp) {
-          if (chunk_live(ti, c + 1)) load_c(ti, c + 1);
-        } else if (t + gridDim.x < sch.total_tiles) {
-          const TileInfo tn = decode_tile(p.gs, sch, t + gridDim.x, kBN);
-          if (chunk_live(tn, cg * kChunksPerWarp)) load_c(tn, cg * kChunksPerWarp);
-        }
-        if (live) {
-          atomicAdd(p.dprob + row, dprob_part);
-          if (p.dbias_ws) dbias_reduce(p, dg, di, ti.g, j0, lane);
-        }
-      }
-      if (!ok) break;
-      if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
-      if (t + gridDim.x < sch.total_tiles) ti = decode_tile(p.gs, sch, t + gridDim.x, kBN);
-    }
-    // abort: a C load still in flight lands before the CTA exits; every TMA
-    // store has completed before the CTA exits
-    if (c_pending) wait_drain(cbar, c_phase, p.wait_limit_ns);
-    if (lane == 0) bulk_wait_group0();
+    auto release = [&](int a) { mbar_arrive(tempty_bar(a)); };
+    dglu_epilogue<ACT, BN>(p, &tmC, &tmD, blockIdx.x, gridDim.x, sch.total_tiles, decode, tfull_bar(0),
+                           release, tmem_base, sbase + C::kOffEpi + ew * kEpiBytes, cbar0 + 8u * ew, wctx,
+                           warp, lane);
   }
 
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Two-CTA pairs (tcgen05 cta_group::2): a cluster of two CTAs computes a
+// 256 x 256 tile of one group.  Each CTA loads its 128 rows of A and its 128
+// of the tile's 256 B rows per k-block (two k-blocks per stage, the
+// shared-memory plan of the 128 x 128 two-k-block tiles), the even CTA issues
+// M = 256, N = 256 MMAs over both CTAs' stages, and each CTA's TMEM receives
+// its 128 rows x 256 columns, which its own epilogue warps drain.  Per SM
+// this moves two thirds of the operand bytes of the 128 x 256 single-SM tile
+// for the same FLOPs.  A group's pairs start at its first row; when a group
+// holds an odd number of 128-row blocks its last pair's odd CTA has no rows:
+// it loads no A and writes nothing.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kPairIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(256 >> 3) << 17) |
+                                (static_cast<uint32_t>(256 >> 4) << 24);
+
+template <int ACT>
+__global__ void __launch_bounds__(kThreads, 1)
+    dglu_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+                     const DsParams p) {
+  using C = DsCfg<2, 128>;  // per CTA: 128 A rows and 128 B rows per k-block
+  constexpr int kStages = C::kStages;
+  constexpr int kTN = 256;  // tile columns
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs
+  const bool leader = rank == 0;
+
+  int32_t* tab0 = reinterpret_cast<int32_t*>(smem + C::kOffTable);
+  int32_t* tab1 = tab0 + (p.gs.groups + 1);
+  const uint32_t bar0 = sbase + C::kOffBar;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };                      // the pair's A, B (leader)
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };         // the leader's commit
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };     // the leader's commit
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + kAcc + a); };  // used in the leader
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 2 * kAcc);
+  const uint32_t cbar0 = bar0 + 8u * (2 * kStages + 2 * kAcc + 1);  // one per epilogue warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  int64_t* total_pairs_s = reinterpret_cast<int64_t*>(smem + C::kOffMisc + 8);
+
+  if (warp == 0 && lane == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < kAcc; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 2 * kEpiWarps);  // every epilogue warp of both CTAs
+    }
+    mbar_init(drain_bar, 1);
+    for (int w = 0; w < kEpiWarps; ++w) mbar_init(cbar0 + 8u * w, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
+    tma_prefetch_desc(&tmD);
+  }
+  if (warp == 1) {  // one warp in each CTA allocates, collectively for the pair
+    tmem_alloc_2sm(smem_u32(tmem_slot), 512);
+    tmem_relinquish_2sm();
+  }
+  if (warp == 2) {
+    // tab0 = the sanitised group ends, tab1 = the exclusive prefix of each
+    // group's 256-row pairs (both CTAs build the same table)
+    build_table(p.gs, tab0, tab1, lane, total_pairs_s);
+    __syncwarp();
+    int32_t carry = 0;
+    for (int base = 0; base < p.gs.groups; base += 32) {
+      const int g = base + lane;
+      int32_t pairs = 0;
+      if (g < p.gs.groups) {
+        const int32_t start = g > 0 ? tab0[g - 1] : 0;
+        pairs = (tab0[g] - start + 255) / 256;
+      }
+      int32_t incl = pairs;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      if (g < p.gs.groups) tab1[g] = carry + incl - pairs;
+      carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    if (lane == 0) *total_pairs_s = carry;
+  }
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers and TMEM exist before any cross-CTA use
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int n_tiles = static_cast<int>((p.n + kTN - 1) / kTN);
+  const int64_t total = *total_pairs_s * n_tiles;
+  const int64_t cluster_id = blockIdx.x >> 1;
+  const int64_t num_clusters = gridDim.x >> 1;
+  const int num_kb = static_cast<int>(p.k / kBKElems);  // K is a whole number of k-blocks
+  const int num_st = (num_kb + 1) / 2;                  // an odd tail k-block loads zeros
+  const WaitCtx wctx{p.gs.status, abort_flag, p.wait_limit_ns};
+  struct PairTile {
+    int64_t row0;  // this CTA's first row
+    int n0;
+    int g;
+    bool valid0, valid1;  // the even / odd CTA's 128 rows belong to the group
+  };
+  auto pair_tile = [&](int64_t t) {
+    PairTile pt;
+    const int64_t mt = t / n_tiles;
+    pt.n0 = static_cast<int>(t - mt * n_tiles) * kTN;
+    int lo = 0, hi = p.gs.groups - 1;  // last group with prefix <= mt
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tab1[mid] <= mt) lo = mid; else hi = mid - 1;
+    }
+    pt.g = lo;
+    const int64_t start = lo > 0 ? tab0[lo - 1] : 0;
+    const int64_t base = start + (mt - tab1[lo]) * 256;
+    const int64_t cnt = static_cast<int64_t>(tab0[lo]) - base;  // a multiple of 128, >= 128
+    pt.valid0 = cnt > 0;
+    pt.valid1 = cnt > 128;
+    pt.row0 = base + rank * kBM;
+    return pt;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, filled_mask = 0, last_parity = 0;
+      bool ok = true;
+      int map_g = -1;
+      for (int64_t t = cluster_id; ok && t < total; t += num_clusters) {
+        const PairTile pt = pair_tile(t);
+        const CUtensorMap* mapB = &tmB;
+        int32_t zb = pt.g;
+        bool w_ok = true;
+        if (p.b_maps) {
+          mapB = p.b_maps + pt.g;
+          zb = 0;
+          w_ok = __ldg(p.w_ok + pt.g) != 0;
+          if (pt.g != map_g) {
+            tensormap_acquire(mapB);
+            map_g = pt.g;
+          }
+        }
+        const bool has_a = rank ? pt.valid1 : pt.valid0;
+        // the even CTA's full barrier expects the bytes of both CTAs' copies
+        const uint32_t pair_bytes = (pt.valid0 ? C::kAStage : 0u) + (pt.valid1 ? C::kAStage : 0u) +
+                                    (w_ok ? 2u * C::kBStage : 0u);
+        for (int si = 0; si < num_st; ++si) {
+          if (!wait_bounded(empty_bar(stage), phase ^ 1u, wctx)) { ok = false; break; }
+          if (leader) mbar_arrive_expect_tx(full_bar(stage), pair_bytes);
+          const uint32_t fb = mapa_shared(full_bar(stage), 0);
+          if (has_a)
+            tma_load_3d_pair(sbase + C::kOffA + stage * C::kAStage, &tmA, fb, 0,
+                             static_cast<int32_t>(pt.row0), 2 * si);
+          if (w_ok)
+            tma_load_4d_pair(sbase + C::kOffB + stage * C::kBStage, mapB, fb, 0,
+                             pt.n0 + static_cast<int>(rank) * 128, 2 * si, zb);
+          filled_mask |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // the even CTA's full barriers count both CTAs' bytes, so its drain
+      // covers the odd CTA's copies too (the odd CTA stays resident until the
+      // final cluster barrier)
+      if (leader)
+        for (int s = 0; s < kStages; ++s)
+          if (filled_mask & (1u << s)) wait_drain(full_bar(s), (last_parity >> s) & 1u, p.wait_limit_ns);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (leader && lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      const uint64_t adesc0 = smem_desc_sw128(sbase + C::kOffA);
+      const uint64_t bdesc0 = smem_desc_sw128(sbase + C::kOffB);
+      for (int64_t t = cluster_id; ok && t < total; t += num_clusters) {
+        if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, wctx)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kTN;
+        for (int si = 0; si < num_st; ++si) {
+          if (!wait_bounded(full_bar(stage), phase, wctx)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t ad = adesc0 + static_cast<uint64_t>((stage * C::kAStage) >> 4);
+          const uint64_t bd = bdesc0 + static_cast<uint64_t>((stage * C::kBStage) >> 4);
+          const uint32_t acc0 = si > 0 ? 1u : 0u;
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk)  // k-block kk of the stage: 16 KB further on
+#pragma unroll
+            for (int j = 0; j < 4; ++j)   // 4 x K=16 per 128-byte swizzle row
+              mma_bf16_2sm(d_tmem, ad + static_cast<uint64_t>((kk * kABytes) >> 4) + 2 * j,
+                           bd + static_cast<uint64_t>((kk * kABytes) >> 4) + 2 * j, kPairIdesc,
+                           (kk > 0 || j > 0) ? 1u : acc0);
+          tc_commit_2sm_mc(empty_bar(stage), 0x3);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit_2sm_mc(tfull_bar(acc), 0x3);
+        if (++acc == kAcc) { acc = 0; acc_phase ^= 1u; }
+      }
+      tc_commit_2sm_mc(drain_bar, 0x1);
+      wait_drain(drain_bar, 0, p.wait_limit_ns);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int ew = warp - 2;
+    auto decode = [&](int64_t t) -> EpiTile {
+      const PairTile pt = pair_tile(t);
+      return EpiTile{pt.row0, pt.n0, pt.g, rank ? pt.valid1 : pt.valid0};
+    };
+    auto release = [&](int a) { mbar_arrive_cluster_relaxed(mapa_shared(tempty_bar(a), 0)); };
+    dglu_epilogue<ACT, kTN>(p, &tmC, &tmD, cluster_id, num_clusters, total, decode, tfull_bar(0), release,
+                            tmem_base, sbase + C::kOffEpi + ew * kEpiBytes, cbar0 + 8u * ew, wctx, warp,
+                            lane);
+  }
+
+  __syncthreads();
+  cluster_sync();  // the peer may still read this CTA's shared memory and TMEM until here
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_2sm(tmem_base, 512);
   }
 }
 
@@ -633,11 +902,21 @@ int run_dglu(const hq_bf16* a, const hq_bf16* b, const int64_t* b_ptrs, const hq
   // quarter beyond the 128-wide tiling or the group table does not fit.
   // Otherwise two k-blocks per stage when K is a whole number of at least
   // two k-blocks (the k-block view must not run past a row's end).
+  // 256 x 256 tiles on CTA pairs halve the B bytes per SM again; they take
+  // the two-k-block stages and run when the problem has at least a wave of
+  // pairs (counting 256-row blocks of all m rows).
   const int64_t pad128 = (n + 127) / 128 * 128, pad256 = (n + 255) / 256 * 256;
-  const bool wide = 4 * pad256 <= 5 * pad128 && DsCfg<1, 256>::smem_bytes(L) <= kSmemMax;
-  const bool kb2 = !wide && k % kBKElems == 0 && k >= 2 * kBKElems &&
-                   DsCfg<2, 128>::smem_bytes(L) <= kSmemMax;
-  const int bn = wide ? 256 : 128;
+  const int sms = num_sms();
+  if (sms <= 0) return HQ_ERR_CUDA;
+  int64_t cap = sm_count > 0 ? sm_count : sms;
+  if (cap > sms) cap = sms;
+  const bool kwhole = k % kBKElems == 0 && k >= 2 * kBKElems;
+  const bool wide = 4 * pad256 <= 5 * pad128;
+  const bool pair = wide && kwhole && cap >= 2 && DsCfg<2, 128>::smem_bytes(L) <= kSmemMax &&
+                    ((m + 255) / 256) * (pad256 / 256) >= cap / 2;
+  const bool wide1 = wide && !pair && DsCfg<1, 256>::smem_bytes(L) <= kSmemMax;
+  const bool kb2 = (pair || !wide1) && kwhole && DsCfg<2, 128>::smem_bytes(L) <= kSmemMax;
+  const int bn = wide1 ? 256 : 128;  // B box rows (a pair CTA loads 128 of its tile's 256)
   const uint64_t nkb = static_cast<uint64_t>(k / kBKElems);
   CUtensorMap tmA, tmB;
   {
@@ -702,20 +981,38 @@ int run_dglu(const hq_bf16* a, const hq_bf16* b, const int64_t* b_ptrs, const hq
     const size_t bytes = static_cast<size_t>(L) * static_cast<size_t>(2 * n) * sizeof(float);
     if (cudaMemsetAsync(dbias_ws, 0, bytes, st) != cudaSuccess) return HQ_ERR_CUDA;
   }
-  const int sms = num_sms();
-  if (sms <= 0) return HQ_ERR_CUDA;
   if (set_smem_once<dglu_kernel<ACT, 1, 128>>(kSmemMax) != HQ_OK ||
       set_smem_once<dglu_kernel<ACT, 2, 128>>(kSmemMax) != HQ_OK ||
-      set_smem_once<dglu_kernel<ACT, 1, 256>>(kSmemMax) != HQ_OK)
+      set_smem_once<dglu_kernel<ACT, 1, 256>>(kSmemMax) != HQ_OK ||
+      set_smem_once<dglu_pair_kernel<ACT>>(kSmemMax) != HQ_OK)
     return HQ_ERR_CUDA;
+  if (pair) {
+    int64_t pairs = cap / 2;
+    const int64_t pairs_bound = ((m + 255) / 256) * (pad256 / 256);
+    if (pairs > pairs_bound) pairs = pairs_bound;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(DsCfg<2, 128>::smem_bytes(L));
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, dglu_pair_kernel<ACT>, tmA, tmB, tmC, tmD, p) != cudaSuccess)
+      return HQ_ERR_CUDA;
+  }
   const int64_t tiles_bound = ((m + kBM - 1) / kBM) * ((n + bn - 1) / bn);
-  int64_t grid = sm_count > 0 ? sm_count : sms;
-  if (grid > sms) grid = sms;
+  int64_t grid = cap;
   if (grid > tiles_bound) grid = tiles_bound;
   if (grid < 1) grid = 1;
   const dim3 g1(static_cast<unsigned>(grid));
   const cudaError_t le =
-      wide ? launch(dglu_kernel<ACT, 1, 256>, g1, dim3(kThreads),
+      pair ? cudaSuccess
+      : wide1 ? launch(dglu_kernel<ACT, 1, 256>, g1, dim3(kThreads),
                     static_cast<int>(DsCfg<1, 256>::smem_bytes(L)), st, false, tmA, tmB, tmC, tmD, p)
       : kb2 ? launch(dglu_kernel<ACT, 2, 128>, g1, dim3(kThreads),
                      static_cast<int>(DsCfg<2, 128>::smem_bytes(L)), st, false, tmA, tmB, tmC, tmD, p)

@@ -186,6 +186,57 @@ def test_bf16_dglu_discrete_matches_stacked(cuda_dev, act):
     del keep
 
 
+@pytest.mark.parametrize("act", ["dswiglu", "dgeglu"])
+def test_bf16_dglu_discrete_pair_tiles(cuda_dev, act):
+    """256 x 256 tiles on CTA pairs (sm_count = 8 holds the grid to four
+    clusters) with per-expert pointers: bit-equal to the stacked call on the
+    same path and within the oracle's bounds, group ends on odd multiples of
+    128 (a pair's odd half past its group writes nothing); an expert with a
+    null pointer is skipped and flagged."""
+    offsets = [384, 512, 1280]
+    L, m, n, k = 3, 1408, 256, 320
+    a, w, c, prob, alpha, beta, off = _dglu_inputs(13, L, m, n, k, offsets)
+    beta_arg = beta if act == "dswiglu" else None
+    dprob0 = torch.zeros(m, device="cuda")
+    dbias0 = torch.zeros(L, 2 * n, dtype=torch.bfloat16, device="cuda")
+    d0 = sentinel_bf16((m, 2 * n))
+    if act == "dswiglu":
+        hq.hq_gemm_dswiglu(a, w, c, off, alpha, beta, prob, dprob0, dbias=dbias0, d_row=d0, sm_count=8)
+    else:
+        hq.hq_gemm_dgeglu(a, w, c, off, alpha, prob, dprob0, dbias=dbias0, d_row=d0, sm_count=8)
+    b_ptrs, _, keep = separate_copies(w, None, L)
+    dprob1 = torch.zeros(m, device="cuda")
+    dbias1 = torch.zeros(L, 2 * n, dtype=torch.bfloat16, device="cuda")
+    d1 = sentinel_bf16((m, 2 * n))
+    hq.hq_gemm_dglu_discrete(a, b_ptrs, c, off, alpha, prob, dprob1, n, act=act, beta=beta_arg,
+                             dbias=dbias1, d_row=d1, sm_count=8)
+    torch.cuda.synchronize()
+    assert torch.equal(d1.view(torch.int16), d0.view(torch.int16))
+    assert_sums_close(dprob1, dprob0, dbias1, dbias0)
+    args = (np_f32(a), np_f32(w), np_f32(c), offsets, alpha.cpu().numpy())
+    ref = (glu.dswiglu(*args, beta.cpu().numpy(), prob.cpu().numpy()) if act == "dswiglu"
+           else glu.dgeglu(*args, prob.cpu().numpy()))
+    D = d1.float().cpu().numpy().astype(np.float64)
+    tol = 2.0 ** -8 * np.abs(ref["D"]) + 2.0 ** -20 * ref["D_mag"] + 1e-30
+    assert not ((np.abs(D - ref["D"]) > tol) & ref["written"][:, None]).any()
+    assert_rows_untouched(d1, ref["written"], "pair-tile D_row")
+    assert_dglu_oracle(ref, dprob1, dbias1)
+    # expert 1 (rows 384..511, one 128-row block: a half pair) without weights
+    hq.get_device_status(clear=True)
+    bad = b_ptrs.clone()
+    bad[1] = 0
+    d2 = sentinel_bf16((m, 2 * n))
+    hq.hq_gemm_dglu_discrete(a, bad, c, off, alpha, prob, torch.zeros(m, device="cuda"), n, act=act,
+                             beta=beta_arg, d_row=d2, sm_count=8)
+    torch.cuda.synchronize()
+    status, _ = hq.get_device_status(clear=True)
+    assert status & hq._abi.HQ_STATUS_BAD_POINTER
+    assert (bits16(d2)[384:512] == 0xAAAA).all(), "rows of the skipped expert written"
+    keep_rows = np.r_[0:384, 512:1280]
+    assert torch.equal(d2[keep_rows].view(torch.int16), d0[keep_rows].view(torch.int16))
+    del keep
+
+
 def test_block_scaled_dglu_discrete_matches_stacked(cuda_dev):
     offsets = [256, 512]
     L, m, n, k = 2, 640, 128, 256

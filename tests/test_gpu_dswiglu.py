@@ -25,7 +25,7 @@ def bf16_ulp(x):
     return np.where(a > 0, 2.0 ** (e - 7), 2.0 ** -133)
 
 
-def run_case(offsets, m, n, k, seed, with_dbias=True, act="dswiglu", c_std=2.0):
+def run_case(offsets, m, n, k, seed, with_dbias=True, act="dswiglu", c_std=2.0, sm_count=-1):
     L = len(offsets)
     a = bf16_rows(m, k, seed)
     b = torch.stack([bf16_rows(n, k, seed + 1 + e, std=0.05) for e in range(L)])
@@ -41,10 +41,10 @@ def run_case(offsets, m, n, k, seed, with_dbias=True, act="dswiglu", c_std=2.0):
     off_t = torch.tensor(offsets, dtype=torch.int32, device=dev)
     if act == "dswiglu":
         hq.hq_gemm_dswiglu(a.to(dev), b.to(dev), c.to(dev), off_t, alpha.to(dev), beta.to(dev), prob.to(dev),
-                           dprob, dbias=dbias, d_row=d_row)
+                           dprob, dbias=dbias, d_row=d_row, sm_count=sm_count)
     else:
         hq.hq_gemm_dgeglu(a.to(dev), b.to(dev), c.to(dev), off_t, alpha.to(dev), prob.to(dev), dprob,
-                          dbias=dbias, d_row=d_row)
+                          dbias=dbias, d_row=d_row, sm_count=sm_count)
     torch.cuda.synchronize()
     if act == "dswiglu":
         ref = glu.dswiglu(np_f32(a), np_f32(b), np_f32(c), offsets, alpha.numpy(), beta.numpy(), prob.numpy())
@@ -71,24 +71,31 @@ def check(ref, d_row, dprob, dbias):
         assert (np.abs(db - ref["dbias"]) <= db_tol).all(), "dbias outside tolerance"
 
 
+# sm_count = 8 caps the grid at four clusters, so the 256 x 256 pair tiles
+# run where the problem holds at least four of them (n = 160, 256 here; the
+# other widths take the single-SM tiles under the cap)
+@pytest.mark.parametrize("sm_count", [-1, 8])
 @pytest.mark.parametrize("n", [64, 128, 160, 288])
-def test_dswiglu_small(cuda_dev, n):
+def test_dswiglu_small(cuda_dev, n, sm_count):
     offsets = [256, 256, 768, 1024]       # empty group 1; rows >= 1024 not written
-    check(*run_case(offsets, 1152, n, 192, seed=n))
+    check(*run_case(offsets, 1152, n, 192, seed=n, sm_count=sm_count))
 
 
+@pytest.mark.parametrize("sm_count", [-1, 8])
 @pytest.mark.parametrize("n", [64, 160])
-def test_dgeglu_small(cuda_dev, n):
+def test_dgeglu_small(cuda_dev, n, sm_count):
     """dGeGLU (fixed 1.702 / +-7 / +1 constants); C spread wide enough to hit both clamps."""
     offsets = [256, 256, 768, 1024]
-    check(*run_case(offsets, 1152, n, 192, seed=100 + n, act="dgeglu", c_std=5.0))
+    check(*run_case(offsets, 1152, n, 192, seed=100 + n, act="dgeglu", c_std=5.0, sm_count=sm_count))
 
 
-def test_dswiglu_odd_group_ends(cuda_dev):
-    """Group ends on odd multiples of 128, a 128-row group and an empty one,
-    K over many stages."""
+@pytest.mark.parametrize("sm_count", [-1, 8])
+def test_dswiglu_odd_group_ends(cuda_dev, sm_count):
+    """Group ends on odd multiples of 128 (a pair whose odd half lies past its
+    group writes nothing), a 128-row group and an empty one, K over many
+    stages."""
     offsets = [384, 512, 512, 1408]
-    check(*run_case(offsets, 1536, 256, 640, seed=31))
+    check(*run_case(offsets, 1536, 256, 640, seed=31, sm_count=sm_count))
 
 
 def test_dswiglu_many_groups(cuda_dev):
