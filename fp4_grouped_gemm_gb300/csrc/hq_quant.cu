@@ -76,6 +76,33 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return r;
 }
 
+// exp(-a) for two values without a library call: with t = -a log2(e) split
+// as t_hi = fl(-a * L) (L = log2(e) rounded to float) plus r, where the FMA
+// residual fma(-a, L, -t_hi) recovers the product's rounding error exactly
+// (the error-free product transformation of Ogita, Rump and Oishi, "Accurate
+// sum and dot product", 2005) and -a * L_lo adds log2(e) - L, exp(-a) =
+// 2^t_hi * 2^r with 2^t_hi from the hardware base-2 exponential and
+// 2^r = 1 + r ln 2 to within r^2 (|r| < 2^-16 wherever 2^t_hi is finite and
+// normal).  The error is that of ex2.approx plus about 2^-23, independent of
+// |a|: a product fl(-a * L) alone would add |a| 2^-24.  2^t_hi = inf (a <
+// -88.7) stays inf and 0 stays 0: the correction factor is positive.
+__device__ __forceinline__ float ex2_approx_ftz(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void exp_neg_x2(float a0, float a1, float& e0, float& e1) {
+  constexpr float kL2E = 1.44269502162933349609375f;  // log2(e) rounded to float
+  constexpr float kL2ELo = 1.925963033500011e-08f;    // log2(e) - kL2E
+  constexpr float kLn2 = 0.693147182464599609375f;
+  float t0, t1, r0, r1;
+  mul_f32x2(t0, t1, a0, a1, -kL2E);
+  fma_f32x2(r0, r1, a0, a1, -kL2E, -kL2E, -t0, -t1);       // exact residual
+  fma_f32x2(r0, r1, a0, a1, -kL2ELo, -kL2ELo, r0, r1);     // + (-a) (log2 e - L)
+  fma_f32x2(r0, r1, r0, r1, kLn2, kLn2, 1.0f, 1.0f);       // 1 + r ln 2
+  mul2_f32x2(e0, e1, ex2_approx_ftz(t0), ex2_approx_ftz(t1), r0, r1);
+}
+
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&x)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -288,12 +315,14 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
           float b[8];
           bf16x8_to_f32(c1[u][i], b);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            // silu(gate) = gate / (1 + exp(-gate)); the reciprocal is the
-            // hardware approximation (within 1 ulp)
-            const float e = expf(-a[j]);
-            const float t = __fmul_rn(a[j], rcp_approx(__fadd_rn(1.0f, e)));
-            x[8 * i + j] = __fmul_rn(b[j], t);
+          for (int j = 0; j < 8; j += 2) {
+            // silu(gate) = gate / (1 + exp(-gate)), in pairs; the reciprocal
+            // is the hardware approximation (within 1 ulp)
+            float e0, e1, d0, d1, t0, t1;
+            exp_neg_x2(a[j], a[j + 1], e0, e1);
+            add_f32x2(d0, d1, e0, e1, 1.0f, 1.0f);
+            mul2_f32x2(t0, t1, a[j], a[j + 1], rcp_approx(d0), rcp_approx(d1));
+            mul2_f32x2(x[8 * i + j], x[8 * i + j + 1], b[j], b[j + 1], t0, t1);
           }
         } else {
 #pragma unroll

@@ -1,7 +1,8 @@
 """GPU parity of the fused SwiGLU + requantisation against the oracle.
 
-The GPU evaluates silu with CUDA's expf and the oracle with a correctly rounded
-exp, so the float32 activation may differ by an ulp.  Bytes must match except
+The GPU evaluates silu with a compensated base-2 exponential (within about
+2^-22 of exp) and an approximate reciprocal, the oracle with a correctly
+rounded exp, so the float32 activation may differ by an ulp or two.  Bytes must match except
 where the oracle's float64 value lies within a relative 2^-20 of the rounding
 boundary that separates the two codes; such boundary cases are counted and
 must stay rare.
