@@ -129,6 +129,18 @@ def set_fault_injection(skip_stage):
     _check(_abi.load().hq_set_fault_injection(int(skip_stage)), "hq_set_fault_injection")
 
 
+def debug_build():
+    """True when the loaded library is libhq_debug.so (HQ_DEBUG=1 in the
+    environment; device bounds checks on global writes)."""
+    return bool(_abi.load().hq_debug_build())
+
+
+def debug_selftest(stream=None):
+    """Debug library only: a one-thread kernel fails one bounds check, skips
+    its write and sets HQ_STATUS_BOUNDS (read it with get_device_status)."""
+    _check(_abi.load().hq_debug_selftest(_stream(stream)), "hq_debug_selftest")
+
+
 def set_gemm_tile_n(tile_n):
     _check(_abi.load().hq_set_gemm_tile_n(int(tile_n)), "hq_set_gemm_tile_n")
 

@@ -1,7 +1,9 @@
 """ctypes declarations of libhq.so's C ABI (see include/hq.h).
 
 The library must have been built (``fp4_grouped_gemm_gb300.build.build()``);
-loading fails loudly otherwise -- there is no fallback implementation.
+loading fails loudly otherwise -- there is no fallback implementation.  With
+the environment variable HQ_DEBUG=1 the package loads libhq_debug.so, the
+build with device bounds checks (``build(debug=True)``), instead.
 """
 
 import ctypes
@@ -38,6 +40,7 @@ HQ_STATUS_BAD_OFFSETS = 0x4
 HQ_STATUS_TOKENS_CLAMPED = 0x8
 HQ_STATUS_ROUTING_DROPPED = 0x10
 HQ_STATUS_BAD_POINTER = 0x20
+HQ_STATUS_BOUNDS = 0x40
 
 
 class Capabilities(ctypes.Structure):
@@ -57,6 +60,8 @@ SIGNATURES = {
     "hq_selftest_wait_expiry": (c_i32, [c_u64, c_p]),
     "hq_probe_mma_rate": (c_i32, [c_i32, c_i32, c_i32, c_i32, c_p, c_p]),
     "hq_set_fault_injection": (c_i32, [c_i64]),
+    "hq_debug_build": (c_i32, []),
+    "hq_debug_selftest": (c_i32, [c_p]),
     "hq_set_gemm_tile_n": (c_i32, [c_i32]),
     "hq_set_gemm_2sm": (c_i32, [c_i32]),
     "hq_quant": (c_i32, [c_p, c_i64, c_i64, c_i32, c_i32, c_p, c_p, c_p, c_i32, c_p]),
@@ -106,8 +111,12 @@ SIGNATURES = {
 _LIB = None
 
 
+def debug_requested():
+    return os.environ.get("HQ_DEBUG", "0") not in ("", "0")
+
+
 def lib_path():
-    return _build.LIB_PATH
+    return _build.DEBUG_LIB_PATH if debug_requested() else _build.LIB_PATH
 
 
 def load():
@@ -119,7 +128,8 @@ def load():
     if not os.path.exists(path):
         raise RuntimeError(
             f"{path} is missing: build the CUDA library first "
-            "(python -c 'import fp4_grouped_gemm_gb300.build as b; b.build()')")
+            "(python -c 'import fp4_grouped_gemm_gb300.build as b; b.build()'"
+            + (", with debug=True for HQ_DEBUG=1" if debug_requested() else "") + ")")
     lib = ctypes.CDLL(path)
     for name, (res, args) in SIGNATURES.items():
         fn = getattr(lib, name)

@@ -171,6 +171,20 @@ int encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, voi
   return HQ_OK;
 }
 
+// Debug builds: one thread checks index 4 against the 4-element buffer below;
+// the check fails, so the write is skipped and HQ_STATUS_BOUNDS is set.  The
+// release build compiles the body away (and the host never launches it).
+__device__ int g_debug_sink[4];
+__global__ void debug_selftest_kernel(uint32_t* status) {
+#if HQ_DEBUG
+  const int n = 4;
+  const int idx = n;
+  if (in_bounds(idx < n, status)) g_debug_sink[idx & 3] = 1;
+#else
+  (void)status;
+#endif
+}
+
 // Waits on an mbarrier that nothing arrives on; the bounded wait expires.
 __global__ void selftest_wait_kernel(uint32_t* status, uint64_t limit_ns) {
   __shared__ __align__(8) uint64_t bar;
@@ -468,6 +482,16 @@ int hq_selftest_wait_expiry(uint64_t limit_ns, hq_stream_t s) {
   uint32_t* status = hq::status_word_ptr();
   if (!status) return HQ_ERR_CUDA;
   hq::selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(s)>>>(status, limit_ns);
+  return cudaGetLastError() == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
+}
+
+int hq_debug_build(void) { return HQ_DEBUG ? 1 : 0; }
+
+int hq_debug_selftest(hq_stream_t s) {
+  if (!HQ_DEBUG) return HQ_ERR_UNSUPPORTED;
+  uint32_t* status = hq::status_word_ptr();
+  if (!status) return HQ_ERR_CUDA;
+  hq::debug_selftest_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(s)>>>(status);
   return cudaGetLastError() == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
 }
 

@@ -180,6 +180,9 @@ struct EpiArgs {
   int rows_lo;           // ... from this row of the quarter on (may be <= 0)
   uint32_t stage_s;      // this warp's staging buffer (shared address)
   int lane;
+  int64_t row_abs;       // absolute row of lane 0 of this quarter (debug bounds checks)
+  int64_t rows_total;    // rows of out
+  uint32_t* status;
 };
 
 __device__ __forceinline__ void epi_convert16(const EpiArgs& e, int64_t col0, const uint32_t (&r)[16],
@@ -233,7 +236,8 @@ __device__ __forceinline__ void epi_store16(const EpiArgs& e, int64_t col0, cons
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(e.stage_s + off)
                  : "memory");
-    if (rr >= e.rows_lo && rr < e.rows_here)
+    if (rr >= e.rows_lo && rr < e.rows_here &&
+        in_bounds(e.row_abs + rr < e.rows_total && col0 + u * 8 + 8 <= e.n, e.status))
       *reinterpret_cast<uint4*>(e.out + rr * e.n + col0 + u * 8) = v;
   }
   __syncwarp();
@@ -398,6 +402,8 @@ __device__ __forceinline__ void dglu_chunk(const GemmParams& p, const uint32_t (
     }
   }
   const int64_t two_n = 2 * p.n;
+  // debug builds: this row and chunk lie inside D_row (and D_col)
+  row_ok = row_ok && in_bounds(row < p.gs.a_rows && j0 + 32 <= p.n && g < p.gs.groups, p.gs.status);
   // FP8 D (Step 3): E4M3 or E5M2 codes, the scale rule's range to match
   const bool e5 = p.d_type == kDE5M2;
   const float rcp_max = e5 ? 1.0f / 57344.0f : 1.0f / 448.0f;
@@ -584,6 +590,7 @@ __device__ __forceinline__ int64_t sfatom_offset(int64_t r, int64_t s, int64_t S
 __device__ __forceinline__ void swiglu_store(const GemmParams& p, const float (&y)[64], int64_t row,
                                              int64_t j0, float gq) {
   const int64_t H = p.n;
+  if (!in_bounds(row < p.gs.a_rows && j0 + 64 <= H, p.gs.status)) return;
   if (p.q_mode == HQ_MXFP8) {
     uint32_t bytes2 = 0;
 #pragma unroll
@@ -1051,6 +1058,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       e.rows_lo = ti.row_lo - q * 32;
       e.stage_s = sbase + C::OFF_STAGE_OUT + ew * 1024;
       e.lane = lane;
+      e.row_abs = ti.row0 + q * 32;
+      e.rows_total = p.gs.a_rows;
+      e.status = p.gs.status;
       const uint32_t tempty = tempty_bar(acc);
       // with one accumulator the next tile's MMAs wait for this epilogue:
       // release TMEM before storing
@@ -1560,6 +1570,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       e.rows_lo = 0;
       e.stage_s = sbase + C::OFF_STAGE_OUT + ew * 1024;
       e.lane = lane;
+      e.row_abs = pt.row0 + q * 32;
+      e.rows_total = p.gs.a_rows;
+      e.status = p.gs.status;
       auto release = [&] { if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader); };
       if (kWide) epilogue_tile_wide(e, (ew >> 2) * 64, release);
       else epilogue_tile<C::BN, true>(e, release);

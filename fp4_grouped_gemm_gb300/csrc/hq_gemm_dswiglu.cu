@@ -237,7 +237,11 @@ __device__ __forceinline__ void dglu_epilogue(const DsParams& p, const CUtensorM
   uint32_t c_phase = 0;
   bool c_pending = false;
   auto chunk_live = [&](const EpiTile& et, int c) -> bool {
-    return et.rows && et.n0 + c * 32 < p.n && (!p.w_ok || __ldg(p.w_ok + et.g) != 0);
+    return et.rows && et.n0 + c * 32 < p.n && (!p.w_ok || __ldg(p.w_ok + et.g) != 0) &&
+           // debug builds: the segment's rows, columns and group lie inside D_row / dbias
+           in_bounds(et.row0 + q * 32 + 32 <= p.gs.a_rows && et.n0 + c * 32 + 32 <= p.n &&
+                         et.g < p.gs.groups,
+                     p.gs.status);
   };
   auto load_c = [&](const EpiTile& et, int c) {
     if (lane == 0) {

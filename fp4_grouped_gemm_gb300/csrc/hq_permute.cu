@@ -22,6 +22,7 @@
 #include <cuda_runtime.h>
 
 #include "hq_internal.h"
+#include "hq_ptx.cuh"
 
 namespace hq {
 namespace {
@@ -128,6 +129,8 @@ __global__ void __launch_bounds__(kThreads) permute_scatter(const PermuteParams 
   for (int j = warp; j < entries; j += nwarps) {
     const int32_t d = dest[j];
     if (d < 0) continue;
+    // debug builds: the destination row lies inside the [E * cap] output
+    if (!in_bounds(d < static_cast<int64_t>(p.E) * p.cap, p.status)) continue;
     const int64_t t = t0 + j / p.topk;
     const uint4* src = reinterpret_cast<const uint4*>(p.x + t * row_bytes);
     uint4* dst = reinterpret_cast<uint4*>(p.out_x + static_cast<int64_t>(d) * row_bytes);

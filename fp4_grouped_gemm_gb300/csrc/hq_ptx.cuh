@@ -9,7 +9,25 @@
 
 #include "../../include/hq.h"
 
+#ifndef HQ_DEBUG
+#define HQ_DEBUG 0
+#endif
+
 namespace hq {
+
+// Debug builds (HQ_DEBUG=1) check the data-dependent index of a global write:
+// a failed check sets HQ_STATUS_BOUNDS in the device status word and the
+// caller skips the write.  Release builds compile the check away.
+__device__ __forceinline__ bool in_bounds(bool ok, uint32_t* status) {
+#if HQ_DEBUG
+  if (!ok) atomicOr(status, HQ_STATUS_BOUNDS);
+  return ok;
+#else
+  (void)ok;
+  (void)status;
+  return true;
+#endif
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

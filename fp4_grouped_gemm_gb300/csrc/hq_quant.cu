@@ -337,6 +337,8 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
       const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, byte, 3 * LPG);
       if (s >= groups_row) continue;
       const int64_t e0 = row * p.k + s * GS + (lane % LPG) * GL;  // first element of this lane
+      // debug builds: the codes lie inside q (the scale word: below)
+      if (!in_bounds(row < p.rows && s * GS + (lane % LPG) * GL + GL <= p.k, p.status)) continue;
       if (MODE == HQ_MXFP8 || MODE == HQ_MXFP8_E5M2) {
         uint4* dst = reinterpret_cast<uint4*>(p.q + e0);
 #pragma unroll
@@ -348,7 +350,9 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
       } else {
         *reinterpret_cast<uint32_t*>(p.q + e0 / 2) = qw[0];
       }
-      if ((lane & (4 * LPG - 1)) == 0) {
+      // the lane of the first of four groups (s % 4 == 0) writes their word
+      if ((lane & (4 * LPG - 1)) == 0 &&
+          in_bounds(sf_offset(row, s, p.S, p.swizzle) + 4 <= p.rows_pad * p.S, p.status)) {
         const uint32_t word = byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
         *reinterpret_cast<uint32_t*>(p.sf + sf_offset(row, s, p.S, p.swizzle)) = word;
       }
@@ -363,7 +367,8 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
     const int64_t n = (p.rows_pad - p.rows) * p.S;
     for (int64_t i = tid; i < n; i += nthreads) {
       const int64_t r = p.rows + i / p.S, s = i % p.S;
-      p.sf[sf_offset(r, s, p.S, p.swizzle)] = 0;
+      if (in_bounds(sf_offset(r, s, p.S, p.swizzle) < p.rows_pad * p.S, p.status))
+        p.sf[sf_offset(r, s, p.S, p.swizzle)] = 0;
     }
   }
   if (p.S > p.S_real) {
@@ -377,7 +382,8 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
         tn = tn < 0 ? 0 : (tn > p.rows_per_expert ? p.rows_per_expert : tn);
         if (r - e * p.rows_per_expert >= tn) continue;
       }
-      p.sf[sf_offset(r, s, p.S, p.swizzle)] = 0;
+      if (in_bounds(sf_offset(r, s, p.S, p.swizzle) < p.rows_pad * p.S, p.status))
+        p.sf[sf_offset(r, s, p.S, p.swizzle)] = 0;
     }
   }
   pdl_launch_dependents();

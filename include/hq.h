@@ -95,6 +95,8 @@ enum {
 #define HQ_STATUS_ROUTING_DROPPED 0x10u /* permute: a bad expert id or a full expert */
 #define HQ_STATUS_BAD_POINTER 0x20u   /* discrete weights: a null or unaligned
                                          per-expert pointer; that expert skipped */
+#define HQ_STATUS_BOUNDS 0x40u        /* debug build only: a device bounds check on
+                                         a global write failed; that write skipped */
 
 /* Layout and alignment constants, so integrations need not copy them
  * (FlashRT fp4-gemm notes: "Read capabilities() instead of duplicating
@@ -152,6 +154,21 @@ int hq_selftest_wait_expiry(uint64_t limit_ns, hq_stream_t s);
  * faults or hangs: the failure is a barrier that nothing completes.
  * Returns HQ_ERR_INVALID for skip_stage < -1. */
 int hq_set_fault_injection(int64_t skip_stage);
+
+/* Debug build (libhq_debug.so: the same sources compiled with HQ_DEBUG=1;
+ * a device-side check for the sanitizer the pool does not offer).  Its
+ * kernels check the data-dependent indices of their global writes (output
+ * rows and columns, scale-atom offsets, the dGLU dprob / dbias rows and the
+ * TMA store coordinates, the permute's destination rows); a failed check sets
+ * HQ_STATUS_BOUNDS in the device status word and skips that write instead of
+ * trapping.  In the release library the checks compile to nothing.
+ * hq_debug_build returns 1 in the debug library, 0 otherwise (no GPU needed).
+ * hq_debug_selftest (debug library only) launches one thread that checks
+ * index n against an n-element buffer: the check fails, the write is skipped
+ * and HQ_STATUS_BOUNDS is set; read it with hq_get_device_status.  Returns
+ * HQ_ERR_UNSUPPORTED in the release library, where it launches nothing. */
+int hq_debug_build(void);
+int hq_debug_selftest(hq_stream_t s);
 
 /* Tensor-core issue-rate probe (a measurement aid, no counterpart on the
  * pages): every CTA of one wave (one per SM, or one two-CTA cluster per SM
