@@ -70,6 +70,9 @@ struct GemmParams {
   uint32_t idesc_ab;
   // D_row / D_col element type of the dGLU epilogues (kDBf16 .. kDE5M2)
   int d_type;
+  // dGLU epilogues: D_row leaves through the warp's buffer and a TMA store
+  // (1: BF16 D_row, 2: FP8 D_row with SFD_row), 0: straight from registers
+  int d_tma;
   // test aid (hq_set_fault_injection): cluster 0's producer withholds the
   // arrival on the "full" barrier of this stage (count of stages it issued);
   // -1 = never
@@ -119,7 +122,7 @@ inline bool valid_mode(hq_mode mode) {
 
 // TABLE: entries of the per-CTA group table (0 for the dense GEMM, which
 // needs none and spends the shared memory on a deeper pipeline instead).
-template <int MODE, int BN, int STAGES, int ACC, int TABLE>
+template <int MODE, int BN, int STAGES, int ACC, int TABLE, int OUTB = 1024>
 struct Cfg {
   static constexpr int GS = MODE == HQ_NVFP4 ? 16 : 32;
   static constexpr int EPB = MODE == HQ_MXFP8 ? 1 : 2;            // elements per byte
@@ -143,10 +146,12 @@ struct Cfg {
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-  static constexpr int OFF_STAGE_OUT = OFF_SFB + STAGES * SFB_BYTES;  // 1 KB per epilogue warp
-  static constexpr int OFF_TABLE = OFF_STAGE_OUT + kEpiWarps * 1024;  // 2 x TABLE int32
+  // OUTB bytes per epilogue warp: 1 KB of output staging, 4 KB for the dGLU's
+  // C / D_row segments (1024-aligned for the TMA swizzle)
+  static constexpr int OFF_STAGE_OUT = (OFF_SFB + STAGES * SFB_BYTES + 1023) / 1024 * 1024;
+  static constexpr int OFF_TABLE = OFF_STAGE_OUT + kEpiWarps * OUTB;  // 2 x TABLE int32
   static constexpr int OFF_BAR = OFF_TABLE + 2 * TABLE * 4 + 8;
-  static constexpr int NUM_BARS = 3 * STAGES + 2 * ACC + 2;
+  static constexpr int NUM_BARS = 3 * STAGES + 2 * ACC + 2 + kEpiWarps;  // + one C barrier per epilogue warp
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= kSmemLimit, "shared memory budget");
@@ -346,11 +351,8 @@ __device__ __forceinline__ float dglu_rcp(float x) {
 }
 
 template <int EPI>
-__device__ __forceinline__ void dglu_chunk(const GemmParams& p, const uint32_t (&r)[32],
-                                           const uint4 (&cv)[8], bool row_ok, int64_t row,
-                                           int64_t j0, int g, float a2, float beta, float prob,
-                                           float norm, int lane) {
-  float dg[32], di[32];
+__device__ __forceinline__ void dglu_math(const uint32_t (&r)[32], const uint4 (&cv)[8], float a2, float beta,
+                                          float prob, float (&dg)[32], float (&di)[32], float& dprob) {
   float dp0 = 0.0f, dp1 = 0.0f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
@@ -401,9 +403,18 @@ __device__ __forceinline__ void dglu_chunk(const GemmParams& p, const uint32_t (
       fma_f32x2(dp0, dp1, q0, q1, up0, up1, dp0, dp1);
     }
   }
+  dprob = dp0 + dp1;
+}
+
+// The row's D_row segment (and SFD_row bytes) and its dprob partial.  D_row
+// goes to the warp's buffer at dbuf (sent by the caller with one TMA store:
+// BF16 in the 128-byte swizzle, FP8 as plain 64-byte rows) when dbuf != 0,
+// else straight to global memory.
+__device__ __forceinline__ void dglu_write_row(const GemmParams& p, const float (&dg)[32],
+                                               const float (&di)[32], bool row_ok, int64_t row,
+                                               int64_t j0, float norm, float dprob, uint32_t dbuf,
+                                               int lane) {
   const int64_t two_n = 2 * p.n;
-  // debug builds: this row and chunk lie inside D_row (and D_col)
-  row_ok = row_ok && in_bounds(row < p.gs.a_rows && j0 + 32 <= p.n && g < p.gs.groups, p.gs.status);
   // FP8 D (Step 3): E4M3 or E5M2 codes, the scale rule's range to match
   const bool e5 = p.d_type == kDE5M2;
   const float rcp_max = e5 ? 1.0f / 57344.0f : 1.0f / 448.0f;
@@ -423,8 +434,17 @@ __device__ __forceinline__ void dglu_chunk(const GemmParams& p, const uint32_t (
         const float* v = u < 4 ? dg + 8 * u : di + 8 * (u - 4);
         __nv_bfloat162 b0 = __floats2bfloat162_rn(v[0], v[1]), b1 = __floats2bfloat162_rn(v[2], v[3]),
                        b2 = __floats2bfloat162_rn(v[4], v[5]), b3 = __floats2bfloat162_rn(v[6], v[7]);
-        dst[u] = make_uint4(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1),
-                            *reinterpret_cast<uint32_t*>(&b2), *reinterpret_cast<uint32_t*>(&b3));
+        const uint4 w4 = make_uint4(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1),
+                                    *reinterpret_cast<uint32_t*>(&b2), *reinterpret_cast<uint32_t*>(&b3));
+        if (dbuf) {
+          // 16-byte unit u of row `lane` at unit u ^ (lane & 7): the TMA 128-byte swizzle
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           dbuf + static_cast<uint32_t>(lane) * 128u + ((static_cast<uint32_t>(u) ^ (lane & 7)) << 4)),
+                       "r"(w4.x), "r"(w4.y), "r"(w4.z), "r"(w4.w)
+                       : "memory");
+        } else {
+          dst[u] = w4;
+        }
       }
     } else {
       // Step 3: per 32 D_row values, s = (norm * amax) / 448 (E5M2: 57344)
@@ -447,9 +467,20 @@ __device__ __forceinline__ void dglu_chunk(const GemmParams& p, const uint32_t (
                                      __fmul_rn(__fmul_rn(v[4 * i + 2], norm), mult));
           w[i] = lo | (hi << 16);
         }
-        uint4* dst = reinterpret_cast<uint4*>(p.d_row + row * two_n + 2 * j0 + 32 * h);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        if (dbuf) {
+          // plain 64-byte rows: this half's 32 codes are units 2 h and 2 h + 1 of row `lane`
+          const uint32_t a0 = dbuf + static_cast<uint32_t>(lane) * 64u + 32u * h;
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                       "r"(w[3])
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a0 + 16u), "r"(w[4]), "r"(w[5]),
+                       "r"(w[6]), "r"(w[7])
+                       : "memory");
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(p.d_row + row * two_n + 2 * j0 + 32 * h);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
         bytes2 |= byte << (8 * h);
       }
       // the chunk's two scale columns s, s + 1 (s even) are adjacent in the atom row
@@ -457,8 +488,18 @@ __device__ __forceinline__ void dglu_chunk(const GemmParams& p, const uint32_t (
       const int64_t off = ((row >> 7) * (S >> 2) + (s >> 2)) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4 + (s & 3);
       *reinterpret_cast<uint16_t*>(p.sfd_row + off) = static_cast<uint16_t>(bytes2);
     }
-    atomicAdd(p.dprob + row, dp0 + dp1);
+    atomicAdd(p.dprob + row, dprob);
   }
+}
+
+// The chunk's warp-collective parts: the per-group amax, D_col with its
+// column scales, and the dbias column sums.
+__device__ __forceinline__ void dglu_tail(const GemmParams& p, float (&dg)[32], float (&di)[32], bool row_ok,
+                                          int64_t row, int64_t j0, int g, float norm, int lane) {
+  const int64_t two_n = 2 * p.n;
+  const bool e5 = p.d_type == kDE5M2;
+  const float rcp_max = e5 ? 1.0f / 57344.0f : 1.0f / 448.0f;
+  auto cvt8x2 = [&](float hi, float lo) -> uint32_t { return e5 ? cvt_e5m2x2(hi, lo) : cvt_e4m3x2(hi, lo); };
   if (p.amax) {
     // per-group max |D| over the gate and the input columns: a max all-reduce
     // over the warp, then one integer atomic max per value (|D| >= 0, so the
@@ -646,11 +687,15 @@ __device__ __forceinline__ void swiglu_store(const GemmParams& p, const float (&
   }
 }
 
+// tmC / tmD: the dGLU epilogues' C and D_row segment maps (other epilogues
+// get unused placeholders)
 template <int MODE, int BN, int STAGES, int ACC, int TABLE, int EPI = kEpiGemm>
 __global__ void __launch_bounds__(kThreads, 1)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                    const GemmParams p) {
-  using C = Cfg<MODE, BN, STAGES, ACC, TABLE>;
+  constexpr bool kDglu = EPI == kEpiDSwiGLU || EPI == kEpiDGeGLU;
+  using C = Cfg<MODE, BN, STAGES, ACC, TABLE, kDglu ? 4096 : 1024>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -669,6 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * ACC);
   const uint32_t drain_sf_bar = drain_bar + 8u;
   auto sfready_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * ACC + 2 + s); };
+  const uint32_t cbar0 = bar0 + 8u * (3 * STAGES + 2 * ACC + 2);  // dGLU: one per epilogue warp
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   int64_t* total_mtiles_s = reinterpret_cast<int64_t*>(smem + C::OFF_MISC + 8);
@@ -686,9 +732,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain_bar, 1);
     mbar_init(drain_sf_bar, 1);
     for (int s = 0; s < STAGES; ++s) mbar_init(sfready_bar(s), kSfPath == 2 ? 4 : 1);
+    for (int w = 0; w < kEpiWarps; ++w) mbar_init(cbar0 + 8u * w, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (kDglu) {
+      tma_prefetch_desc(&tmC);
+      if (p.d_tma) tma_prefetch_desc(&tmD);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -993,12 +1044,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (EPI == kEpiDSwiGLU || EPI == kEpiDGeGLU) {
-      // dGLU: the warp owns two 32-column chunks of its lane quarter; C of a
-      // chunk is loaded before its accumulator columns are read
+      // dGLU: the warp owns two 32-column chunks of its lane quarter.  A
+      // chunk's C segment [32 rows x 64 values] arrives by TMA in the warp's
+      // 4 KB buffer (128-byte swizzle); each lane reads its row, and when
+      // d_tma is set writes its D_row segment back into the buffer for one
+      // TMA store.  The next chunk's C load is issued once that store has
+      // read the buffer, so it overlaps the chunk's amax / D_col / dbias
+      // work and the next accumulator wait.  Contiguous-schedule tiles are
+      // whole 128-row blocks (group ends are multiples of 128).
       static_assert(EPI == kEpiGemm || kUpProj || (BN == 128 && ACC == 2), "dGLU tiles are 128 wide");
       const float norm = p.norm_const ? __ldg(p.norm_const) : 1.0f;
-      const int64_t two_n = 2 * p.n;
-      for (int64_t t = blockIdx.x; t < sch.total_tiles; t += gridDim.x) {
+      const uint32_t eb = sbase + C::OFF_STAGE_OUT + ew * 4096;
+      const uint32_t cbar = cbar0 + 8u * ew;
+      uint32_t c_phase = 0;
+      bool c_pending = false;
+      auto chunk_live = [&](const TileInfo& ti, int c) -> bool {
+        return ti.n0 + c * 32 < p.n && ti.rows_valid > q * 32 && tile_ok(ti);
+      };
+      auto load_c = [&](const TileInfo& ti, int c) {
+        if (lane == 0) {
+          bulk_wait_group_read0();  // the previous D_row store has read the buffer
+          mbar_arrive_expect_tx(cbar, 4096);
+          tma_load_2d(eb, &tmC, cbar, static_cast<int32_t>(2 * (ti.n0 + c * 32)),
+                      static_cast<int32_t>(ti.row0 + q * 32));
+        }
+        c_pending = true;
+      };
+      const int cw0 = (ew >> 2) * 2;  // the warp's first chunk
+      int64_t t = blockIdx.x;
+      if (t < sch.total_tiles) {
+        const TileInfo t0i = decode_tile(p.gs, sch, t, TW);
+        if (chunk_live(t0i, cw0)) load_c(t0i, cw0);
+      }
+      bool ok = true;
+      for (; ok && t < sch.total_tiles; t += gridDim.x) {
         const TileInfo ti = decode_tile(p.gs, sch, t, TW);
         const int r_local = q * 32 + lane;
         const bool row_ok = r_local < ti.rows_valid;
@@ -1007,18 +1086,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float a2 = __fmul_rn(alpha, alpha);
         const float beta = EPI == kEpiDSwiGLU ? __ldg(p.beta + ti.g) : 1.0f;
         const float prob = row_ok ? __ldg(p.prob + row) : 0.0f;
-        bool ok = true;
         for (int cc = 0; cc < 2; ++cc) {
-          const int c = (ew >> 2) * 2 + cc;
+          const int c = cw0 + cc;
           const int64_t j0 = ti.n0 + c * 32;
-          const bool chunk_ok = j0 < p.n;
-          uint4 cv[8];
-          {
-            const bool ld = row_ok && chunk_ok;
-            const uint4* src = reinterpret_cast<const uint4*>(p.c + row * two_n + 2 * j0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) cv[i] = ld ? __ldcs(src + i) : make_uint4(0, 0, 0, 0);
-          }
+          const bool live = chunk_live(ti, c);
           if (cc == 0) {
             const bool w = wait_bounded(tfull_bar(acc), acc_phase, wctx);
             if (!__all_sync(0xFFFFFFFFu, w)) { ok = false; break; }
@@ -1032,12 +1103,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));
           }
-          if (chunk_ok && tile_ok(ti))
-            dglu_chunk<EPI>(p, r, cv, row_ok, row, j0, ti.g, a2, beta, prob, norm, lane);
+          float dg[32], di[32];
+          bool row_w = false;
+          if (live) {
+            const bool w = wait_bounded(cbar, c_phase, wctx);
+            if (!__all_sync(0xFFFFFFFFu, w)) { ok = false; break; }
+            c_pending = false;
+            c_phase ^= 1u;
+            uint4 cv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              uint32_t v[4];
+              lds128(eb + static_cast<uint32_t>(lane) * 128u + ((static_cast<uint32_t>(i) ^ (lane & 7)) << 4), v);
+              cv[i] = make_uint4(v[0], v[1], v[2], v[3]);
+            }
+            float dprob = 0.0f;
+            dglu_math<EPI>(r, cv, a2, beta, prob, dg, di, dprob);
+            // debug builds: this row and chunk lie inside D_row (and D_col)
+            row_w = row_ok && in_bounds(row < p.gs.a_rows && j0 + 32 <= p.n && ti.g < p.gs.groups,
+                                        p.gs.status);
+            const uint32_t dbuf = (p.d_tma && __all_sync(0xFFFFFFFFu, row_w)) ? eb : 0u;
+            dglu_write_row(p, dg, di, row_w, row, j0, norm, dprob, dbuf, lane);
+            if (dbuf) {
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmD, eb, static_cast<int32_t>(2 * j0), static_cast<int32_t>(ti.row0 + q * 32));
+                bulk_commit_group();
+              }
+            }
+          }
+          // the next C segment: this tile's second chunk, or the next tile's first
+          if (cc == 0) {
+            if (chunk_live(ti, c + 1)) load_c(ti, c + 1);
+          } else if (t + gridDim.x < sch.total_tiles) {
+            const TileInfo tn = decode_tile(p.gs, sch, t + gridDim.x, TW);
+            if (chunk_live(tn, cw0)) load_c(tn, cw0);
+          }
+          if (live) dglu_tail(p, dg, di, row_w, row, j0, ti.g, norm, lane);
         }
         if (!ok) break;
         if (++acc == ACC) { acc = 0; acc_phase ^= 1u; }
       }
+      // abort: a C load still in flight lands before the CTA exits; every TMA
+      // store has completed before the CTA exits
+      if (c_pending) wait_drain(cbar, c_phase, p.wait_limit_ns);
+      if (lane == 0) bulk_wait_group0();
     }
     for (int64_t t = blockIdx.x; EPI == kEpiGemm && t < sch.total_tiles; t += gridDim.x) {
       const TileInfo ti = decode_tile(p.gs, sch, t, TW);
@@ -1596,7 +1707,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int MODE, int BN, int STAGES, int ACC, int TABLE, int EPI = kEpiGemm>
 int run_bs(const void* a, const void* b, const GemmParams& p0, int sm_count, bool pdl,
            cudaStream_t st) {
-  using C = Cfg<MODE, BN, STAGES, ACC, TABLE>;
+  constexpr bool kDglu = EPI == kEpiDSwiGLU || EPI == kEpiDGeGLU;
+  using C = Cfg<MODE, BN, STAGES, ACC, TABLE, kDglu ? 4096 : 1024>;
   GemmParams p = p0;
   const uint64_t kbytes = static_cast<uint64_t>(p.k) / C::EPB;
   CUtensorMap tmA, tmB;
@@ -1629,6 +1741,31 @@ int run_bs(const void* a, const void* b, const GemmParams& p0, int sm_count, boo
       if (rc != HQ_OK) return rc;
     }
   }
+  // dGLU: C and D_row [a_rows, 2n] in 32-row x 64-value segments; D_row by
+  // TMA for BF16 (128-byte swizzle, like C) and for FP8 with SFD_row (plain
+  // 64-byte rows); other D types are stored from registers
+  CUtensorMap tmC = tmA, tmD = tmA;
+  p.d_tma = 0;
+  if (kDglu) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(2 * p.n), static_cast<uint64_t>(p.gs.a_rows)};
+    const uint32_t box[2] = {64, 32};
+    const uint64_t sc[1] = {static_cast<uint64_t>(2 * p.n) * 2};
+    int rc = encode_tensor_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(p.c), dims,
+                               sc, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != HQ_OK) return rc;
+    if (p.d_type == kDBf16 && !p.sfd_row) {
+      rc = encode_tensor_map(&tmD, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.d_row, dims, sc, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+      if (rc != HQ_OK) return rc;
+      p.d_tma = 1;
+    } else if ((p.d_type == kDE4M3 || p.d_type == kDE5M2) && p.sfd_row) {
+      const uint64_t s8[1] = {static_cast<uint64_t>(2 * p.n)};
+      rc = encode_tensor_map(&tmD, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, p.d_row, dims, s8, box,
+                             CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (rc != HQ_OK) return rc;
+      p.d_tma = 2;
+    }
+  }
   auto kern = bs_gemm_kernel<MODE, BN, STAGES, ACC, TABLE, EPI>;
   if (set_smem_once<bs_gemm_kernel<MODE, BN, STAGES, ACC, TABLE, EPI>>(C::SMEM_BYTES) != HQ_OK)
     return HQ_ERR_CUDA;
@@ -1646,7 +1783,7 @@ int run_bs(const void* a, const void* b, const GemmParams& p0, int sm_count, boo
   if (grid > tiles_bound) grid = tiles_bound;
   if (grid < 1) grid = 1;
   cudaError_t e = launch(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), C::SMEM_BYTES, st,
-                         pdl, tmA, tmB, p);
+                         pdl, tmA, tmB, tmC, tmD, p);
   return e == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
 }
 
@@ -2026,8 +2163,8 @@ int dglu_bs_impl(const void* a, const uint8_t* sfa, const void* b, const uint8_t
   constexpr int T = kMaxGroups + 1;
   int rc;
   if (mode == HQ_MXFP8)
-    rc = act == 0 ? run_bs<HQ_MXFP8, 128, 6, 2, T, kEpiDSwiGLU>(a, b, p, sm_count, false, st)
-                  : run_bs<HQ_MXFP8, 128, 6, 2, T, kEpiDGeGLU>(a, b, p, sm_count, false, st);
+    rc = act == 0 ? run_bs<HQ_MXFP8, 128, 5, 2, T, kEpiDSwiGLU>(a, b, p, sm_count, false, st)
+                  : run_bs<HQ_MXFP8, 128, 5, 2, T, kEpiDGeGLU>(a, b, p, sm_count, false, st);
   else if (mode == HQ_MXFP4)
     rc = act == 0 ? run_bs<HQ_MXFP4, 128, 5, 2, T, kEpiDSwiGLU>(a, b, p, sm_count, false, st)
                   : run_bs<HQ_MXFP4, 128, 5, 2, T, kEpiDGeGLU>(a, b, p, sm_count, false, st);
