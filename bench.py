@@ -569,8 +569,14 @@ class Extras:
             gsc = torch.tensor([1.0], device=dev)
             t = time_kernel(lambda: hq.hq_quant(x, "nvfp4", global_scale=gsc, q_out=q, sf_out=sf), 20, self.flush)
             byts = 2 * m * k + m * k // 2 + sf.numel()
+            # the floor this launch size allows under the same timing: a plain
+            # streaming pass over the same input with the same output ratio
+            t_floor = time_kernel(lambda: hq.probe_stream(x, q), 20, self.flush)
             res[f"quant_nvfp4_{name}_{m}x{k}"] = {"us": t * 1e6, "gbs": byts / t / 1e9,
-                                                  "frac_hbm": byts / t / 1e9 / self.hbm}
+                                                  "frac_hbm": byts / t / 1e9 / self.hbm,
+                                                  "stream_floor_us": t_floor * 1e6,
+                                                  "frac_of_stream_floor": t_floor / t}
+        res["empty_launch_us"] = time_kernel(lambda: hq.probe_stream(None, None), 20, self.flush) * 1e6
         return res
 
     def dense_mxfp4(self):
@@ -645,8 +651,11 @@ class Extras:
         sfs = torch.empty(M * hq.swiglu_kb_dim(H, "mxfp8"), dtype=torch.uint8, device=dev)
         t = time_kernel(lambda: hq.hq_swiglu_quant(out3, "mxfp8", q_out=qs, sf_out=sfs), 20, self.flush)
         byts = M * n * 2 + M * H + sfs.numel()
+        t_floor = time_kernel(lambda: hq.probe_stream(out3, qs), 20, self.flush)  # same bytes, plain stream
         res["swiglu_quant_mxfp8_17408x3072"] = {"us": t * 1e6, "gbs": byts / t / 1e9,
-                                                "frac_hbm": byts / t / 1e9 / self.hbm}
+                                                "frac_hbm": byts / t / 1e9 / self.hbm,
+                                                "stream_floor_us": t_floor * 1e6,
+                                                "frac_of_stream_floor": t_floor / t}
         # the same up-proj with SwiGLU + MXFP8 requantisation in the GEMM's
         # epilogue (one launch instead of GEMM + separate pass)
         t = time_kernel(lambda: hq.hq_gemm_grouped_contig_swiglu_quant(qa, sfa, qbv, sfb, off, M, H, k, "mxfp8",

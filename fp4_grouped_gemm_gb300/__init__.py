@@ -129,6 +129,20 @@ def set_fault_injection(skip_stage):
     _check(_abi.load().hq_set_fault_injection(int(skip_stage)), "hq_set_fault_injection")
 
 
+def probe_stream(src, dst, stream=None):
+    """Streaming floor probe: reads src's bytes (a multiple of 32) and writes
+    one 8-byte word per 32 bytes to dst (uint8, at least a quarter of src's
+    bytes); src None launches the grid with no work."""
+    if src is None:
+        rc = _abi.load().hq_probe_stream(None, 0, None, _stream(stream))
+    else:
+        nbytes = src.numel() * src.element_size()
+        if dst.numel() * dst.element_size() < nbytes // 4:
+            raise ValueError("dst holds fewer than a quarter of src's bytes")
+        rc = _abi.load().hq_probe_stream(_ptr(src), nbytes, _ptr(dst), _stream(stream))
+    _check(rc, "hq_probe_stream")
+
+
 def debug_build():
     """True when the loaded library is libhq_debug.so (HQ_DEBUG=1 in the
     environment; device bounds checks on global writes)."""

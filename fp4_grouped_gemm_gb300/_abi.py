@@ -62,6 +62,7 @@ SIGNATURES = {
     "hq_set_fault_injection": (c_i32, [c_i64]),
     "hq_debug_build": (c_i32, []),
     "hq_debug_selftest": (c_i32, [c_p]),
+    "hq_probe_stream": (c_i32, [c_p, c_sz, c_p, c_p]),
     "hq_set_gemm_tile_n": (c_i32, [c_i32]),
     "hq_set_gemm_2sm": (c_i32, [c_i32]),
     "hq_quant": (c_i32, [c_p, c_i64, c_i64, c_i32, c_i32, c_p, c_p, c_p, c_i32, c_p]),

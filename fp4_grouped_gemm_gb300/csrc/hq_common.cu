@@ -171,6 +171,33 @@ int encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, voi
   return HQ_OK;
 }
 
+// Streaming floor probe: every 32-byte group of src is read (16-byte loads,
+// four groups per thread in flight) and one 8-byte word, the XOR of its two
+// halves, is written to dst (the quantiser's NVFP4 byte ratio).  bytes == 0
+// launches the same grid with no work: the fixed cost of one launch.
+__global__ void __launch_bounds__(256) stream_probe_kernel(const uint4* __restrict__ src, size_t groups,
+                                                           uint2* __restrict__ dst) {
+  const size_t tid = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const size_t nt = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t base = tid; base < groups; base += 4 * nt) {
+    uint4 v[4][2];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const size_t g = base + u * nt;
+      const bool ok = g < groups;
+      v[u][0] = ok ? __ldcs(src + 2 * g) : make_uint4(0, 0, 0, 0);
+      v[u][1] = ok ? __ldcs(src + 2 * g + 1) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const size_t g = base + u * nt;
+      if (g < groups)
+        dst[g] = make_uint2(v[u][0].x ^ v[u][0].z ^ v[u][1].x ^ v[u][1].z,
+                            v[u][0].y ^ v[u][0].w ^ v[u][1].y ^ v[u][1].w);
+    }
+  }
+}
+
 // Debug builds: one thread checks index 4 against the 4-element buffer below;
 // the check fails, so the write is skipped and HQ_STATUS_BOUNDS is set.  The
 // release build compiles the body away (and the host never launches it).
@@ -482,6 +509,17 @@ int hq_selftest_wait_expiry(uint64_t limit_ns, hq_stream_t s) {
   uint32_t* status = hq::status_word_ptr();
   if (!status) return HQ_ERR_CUDA;
   hq::selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(s)>>>(status, limit_ns);
+  return cudaGetLastError() == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
+}
+
+int hq_probe_stream(const void* src, size_t bytes, void* dst, hq_stream_t s) {
+  if (bytes % 32 != 0) return HQ_ERR_INVALID;
+  if (bytes > 0 && (!src || !dst)) return HQ_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15u) return HQ_ERR_INVALID;
+  const int sms = hq::num_sms();
+  if (sms <= 0) return HQ_ERR_CUDA;
+  hq::stream_probe_kernel<<<static_cast<unsigned>(4 * sms), 256, 0, reinterpret_cast<cudaStream_t>(s)>>>(
+      static_cast<const uint4*>(src), bytes / 32, static_cast<uint2*>(dst));
   return cudaGetLastError() == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
 }
 

@@ -170,6 +170,18 @@ int hq_set_fault_injection(int64_t skip_stage);
 int hq_debug_build(void);
 int hq_debug_selftest(hq_stream_t s);
 
+/* Measurement aid for the HBM-bound passes (no counterpart on the pages): a
+ * plain streaming kernel with the quantiser's byte ratio.  It reads `bytes`
+ * from src (device memory, 16-byte aligned, bytes a multiple of 32) with
+ * 16-byte loads, four 32-byte groups per thread in flight over 4 CTAs per SM,
+ * and writes bytes / 4 to dst: per 32-byte group one 8-byte word, the XOR of
+ * the group's two 16-byte halves (words 0^2 of each half, words 1^3).
+ * bytes == 0 launches the same grid with no work.  Timed like a quantiser
+ * launch it gives the floor that launch size allows: the quantiser's time
+ * over it is the part the encoding adds.  Returns HQ_ERR_INVALID for a size
+ * or alignment outside that contract. */
+int hq_probe_stream(const void* src, size_t bytes, void* dst, hq_stream_t s);
+
 /* Tensor-core issue-rate probe (a measurement aid, no counterpart on the
  * pages): every CTA of one wave (one per SM, or one two-CTA cluster per SM
  * pair when pair != 0) issues `iters` x 4 back-to-back tcgen05.mma of the

@@ -267,3 +267,11 @@ def test_python_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_abi, "lib_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         _abi.load()
+
+
+def test_stream_probe_rejects_bad_arguments(lib):
+    buf = ctypes.c_void_p(4096)
+    assert lib.hq_probe_stream(buf, 48, buf, None) == _abi.HQ_ERR_INVALID                  # not 32-byte groups
+    assert lib.hq_probe_stream(None, 64, buf, None) == _abi.HQ_ERR_INVALID                 # null src
+    assert lib.hq_probe_stream(buf, 64, None, None) == _abi.HQ_ERR_INVALID                 # null dst
+    assert lib.hq_probe_stream(ctypes.c_void_p(4104), 64, buf, None) == _abi.HQ_ERR_INVALID  # unaligned
