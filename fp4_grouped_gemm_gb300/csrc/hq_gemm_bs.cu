@@ -1428,6 +1428,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // a CTA whose 128 rows hold no valid row loads no A and no A scales
         // (its accumulator half is never stored)
         const bool has_a = pt.mine > 0;
+        // B scale blocks inside n (a 384-wide tile may end past n: its last
+        // block's scales do not exist; those columns are never stored)
+        const int64_t rb_in = (p.n - pt.n0 + 127) / 128;
+        const uint32_t rb_valid = static_cast<uint32_t>(kUpProj || rb_in >= C::RB ? C::RB : rb_in);
         const bool has_sfa = has_a && row0 < rows_pad;
         const uint32_t pair_bytes = (pt.valid0 > 0 ? C::A_BYTES : 0u) +
                                     (pt.valid1 > 0 ? C::A_BYTES : 0u) + 2u * C::B_BYTES;
@@ -1459,11 +1463,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             tma_load_3d_pair(b_s, &tmB, fb, kb * kBKBytes, nh0, pt.g);
           }
-          mbar_arrive_expect_tx(sffull_bar(stage), atoms * 512u * (has_sfa ? 1u + C::RB : C::RB));
+          mbar_arrive_expect_tx(sffull_bar(stage), atoms * 512u * (has_sfa ? 1u + rb_valid : rb_valid));
           if (has_sfa)
             bulk_load(sbase + C::OFF_SFA + stage * C::SFA_BYTES, sfa_rows + kb * C::ATOMS * 512,
                       atoms * 512u, sffull_bar(stage));
-          for (int rb = 0; rb < C::RB; ++rb)
+          for (int rb = 0; rb < rb_valid; ++rb)
             bulk_load(sbase + C::OFF_SFB + stage * C::SFB_BYTES + rb * C::ATOMS * 512,
                       sfb_grp + (sfb_blk(rb) * atoms_total + kb * C::ATOMS) * 512,
                       atoms * 512u, sffull_bar(stage));
@@ -1862,7 +1866,10 @@ int run_gemm(hq_mode mode, const void* a, const void* b, const GemmParams& p, in
   if (bn == 0 && pw == 0 && p.gs.sched == kDense &&
       ((p.gs.a_rows + 255) / 256) * ((p.n + 255) / 256) < num_sms() / 2)
     bn = 128;
-  const bool wide = p.n % 384 == 0 && (pw == 384 || (pw == 0 && p.gs.sched == kDense));
+  // 384-wide pair tiles: automatically for dense problems with n a multiple
+  // of 384; forced (pair width 384) for any n of at least 384 (the last tile
+  // may end past n)
+  const bool wide = (p.n % 384 == 0 && pw == 0 && p.gs.sched == kDense) || (pw == 384 && p.n >= 384);
   if (bn == 0 && pairable && use_2sm() && wide) {
     if (mode == HQ_MXFP8) return run_bs_2sm<HQ_MXFP8, 4, kEpiGemm, 384>(a, b, p, sm_count, pdl, st);
     if (mode == HQ_MXFP4) return run_bs_2sm<HQ_MXFP4, 4, kEpiGemm, 384>(a, b, p, sm_count, pdl, st);

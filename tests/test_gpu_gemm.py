@@ -298,6 +298,32 @@ def test_grouped_wide_pair_tiles_forced(cuda_dev, mode):
     assert status == 0
 
 
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4", "mxfp4"])
+@pytest.mark.parametrize("m,n,k", [(300, 512, 512), (129, 640, 640), (256, 896, 512)])
+def test_dense_wide_pair_tiles_partial_last_tile(cuda_dev, mode, m, n, k):
+    """Forced 384-column pair tiles with n not a multiple of 384: the last
+    tile ends 256 or 128 columns short of n + 384 (its B rows past n load as
+    zeros, its B scale blocks past n are not loaded, its columns past n are
+    not stored)."""
+    if mode != "nvfp4" and k % 128:
+        pytest.skip("MXFP8 and MXFP4 need k % 128 == 0")
+    hq.set_gemm_2sm(384)
+    dense_case(m, n, k, mode, 0, alpha={"nvfp4": 0.5, "mxfp8": 1.25, "mxfp4": None}[mode],
+               bias=(mode == "mxfp8"), seed=m + n + k + 5, g_a=2.0 if mode == "nvfp4" else None,
+               g_b=64.0 if mode == "nvfp4" else None)
+
+
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4"])
+def test_grouped_wide_pair_tiles_partial_last_tile(cuda_dev, mode):
+    """The grouped layouts on forced 384-column pair tiles with n = 1024
+    (384 + 384 + 256)."""
+    hq.set_gemm_2sm(384)
+    alpha = [0.5, 1.0, 2.0, 1.25]
+    contig_case([384, 384, 512, 1152], 1280, 1024, 512, mode, 0, alpha=alpha, bias=(mode == "mxfp8"), seed=47)
+    status = masked_case([0, 129, 256, 512], 512, 1024, 512, mode, 0, alpha=alpha, seed=49)
+    assert status == 0
+
+
 @pytest.mark.parametrize("two_sm", [1, 0])
 @pytest.mark.parametrize("mode", ["mxfp8", "nvfp4", "mxfp4"])
 def test_grouped_masked_pairs(cuda_dev, mode, two_sm):
