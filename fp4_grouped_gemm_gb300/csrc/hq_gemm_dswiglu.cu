@@ -99,6 +99,19 @@ __device__ __forceinline__ float rcp_approx(float x) {
   asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
 }
+// sigmoid of a pair, 1 / (1 + 2^(-x log2 e)): the product in one f32x2
+// multiply, the hardware base-2 exponential and approximate reciprocal (the
+// error of a fast exponential, far inside D_row's BF16 rounding)
+__device__ __forceinline__ void sigmoid_x2(float x0, float x1, float& s0, float& s1) {
+  constexpr float kNegLog2e = -1.44269502162933349609375f;  // -log2(e) rounded to float
+  float t0, t1, e0, e1, d0, d1;
+  mul_f32x2(t0, t1, x0, x1, kNegLog2e);
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(t0));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(t1));
+  add_f32x2(d0, d1, e0, e1, 1.0f, 1.0f);
+  s0 = rcp_approx(d0);
+  s1 = rcp_approx(d1);
+}
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
@@ -127,8 +140,8 @@ __device__ __forceinline__ void dglu_row_math(const uint32_t (&r)[32], const uin
       float g0, g1, x0, x1;
       mul_f32x2(g0, g1, bf16_lo(gw), bf16_hi(gw), beta);
       mul_f32x2(x0, x1, bf16_lo(iw), bf16_hi(iw), beta);
-      const float s0 = rcp_approx(__fadd_rn(1.0f, __expf(-g0)));  // sigmoid(gate)
-      const float s1 = rcp_approx(__fadd_rn(1.0f, __expf(-g1)));
+      float s0, s1;
+      sigmoid_x2(g0, g1, s0, s1);  // sigmoid(gate)
       float om0, om1, t0, t1, gs0, gs1, u0, u1;
       fma_f32x2(om0, om1, s0, s1, -1.0f, -1.0f, 1.0f, 1.0f);      // 1 - s
       fma_f32x2(t0, t1, g0, g1, om0, om1, 1.0f, 1.0f);            // 1 + gate (1 - s)
@@ -149,8 +162,8 @@ __device__ __forceinline__ void dglu_row_math(const uint32_t (&r)[32], const uin
       const float uc0 = fminf(fmaxf(x0, -7.0f), 7.0f), uc1 = fminf(fmaxf(x1, -7.0f), 7.0f);
       float kg0, kg1;
       mul_f32x2(kg0, kg1, gc0, gc1, 1.702f);
-      const float s0 = rcp_approx(__fadd_rn(1.0f, __expf(-kg0)));
-      const float s1 = rcp_approx(__fadd_rn(1.0f, __expf(-kg1)));
+      float s0, s1;
+      sigmoid_x2(kg0, kg1, s0, s1);
       float om0, om1, t0, t1, up0, up1, gs0, gs1, w0, w1, a0, a1, b0, b1;
       fma_f32x2(om0, om1, s0, s1, -1.0f, -1.0f, 1.0f, 1.0f);      // 1 - s
       fma_f32x2(t0, t1, kg0, kg1, om0, om1, 1.0f, 1.0f);          // 1 + 1.702 gate_c (1 - s)
@@ -236,6 +249,9 @@ __device__ __forceinline__ void dglu_epilogue(const DsParams& p, const CUtensorM
   const int cg = ((warp - 2) >> 2);      // the warp's chunks: cg * kChunksPerWarp + 0, 1, ...
   uint32_t c_phase = 0;
   bool c_pending = false;
+  // launched as a programmatic dependent of the workspace zeroing: its
+  // zeroes are visible before this warp's first dbias / dprob add
+  pdl_wait();
   auto chunk_live = [&](const EpiTile& et, int c) -> bool {
     return et.rows && et.n0 + c * 32 < p.n && (!p.w_ok || __ldg(p.w_ok + et.g) != 0) &&
            // debug builds: the segment's rows, columns and group lie inside D_row / dbias
@@ -514,6 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
+  pdl_launch_dependents();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
@@ -744,6 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
+  pdl_launch_dependents();
   cluster_sync();  // the peer may still read this CTA's shared memory and TMEM until here
   if (warp == 1) {
     tc_fence_after();
@@ -753,6 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // dbias[i] = bf16(float(dbias[i]) + ws[i])
 __global__ void dbias_finalize_kernel(uint16_t* dbias, const float* ws, int64_t count) {
+  pdl_wait();  // the dGLU kernel's sums are complete and visible
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const float v = __fadd_rn(__uint_as_float(static_cast<uint32_t>(dbias[i]) << 16), ws[i]);
@@ -761,15 +780,36 @@ __global__ void dbias_finalize_kernel(uint16_t* dbias, const float* ws, int64_t 
   }
 }
 
+__global__ void zero_floats_kernel(float* a, int64_t na, float* b, int64_t nb) {
+  pdl_launch_dependents();  // the dGLU kernel may start; it waits for these zeroes before adding
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t nt = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = tid; i < na; i += nt) a[i] = 0.0f;
+  for (int64_t i = tid; i < nb; i += nt) b[i] = 0.0f;
+}
+
 }  // namespace
 
-int dbias_finalize(uint16_t* dbias, const float* ws, int64_t count, cudaStream_t st) {
+int dbias_finalize(uint16_t* dbias, const float* ws, int64_t count, cudaStream_t st, bool pdl) {
   const int sms = num_sms();
   if (sms <= 0) return HQ_ERR_CUDA;
   int64_t blocks = (count + 255) / 256;
   if (blocks > 4 * sms) blocks = 4 * sms;
   if (blocks < 1) blocks = 1;
-  dbias_finalize_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(dbias, ws, count);
+  return launch(dbias_finalize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, pdl, dbias, ws,
+                count) == cudaSuccess
+             ? HQ_OK
+             : HQ_ERR_CUDA;
+}
+
+int zero_floats(float* a, int64_t na, float* b, int64_t nb, cudaStream_t st) {
+  const int sms = num_sms();
+  if (sms <= 0) return HQ_ERR_CUDA;
+  const int64_t n = na > nb ? na : nb;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 2 * sms) blocks = 2 * sms;
+  if (blocks < 1) blocks = 1;
+  zero_floats_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(a, na, b, nb);
   return cudaGetLastError() == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
 }
 
@@ -981,10 +1021,14 @@ int run_dglu(const hq_bf16* a, const hq_bf16* b, const int64_t* b_ptrs, const hq
                            CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != HQ_OK) return rc;
   }
+  // with dbias: zero the sums, then the dGLU kernel and the final pass as
+  // programmatic dependents (each waits for its predecessor's results where
+  // it needs them; the launches overlap)
   if (dbias) {
-    const size_t bytes = static_cast<size_t>(L) * static_cast<size_t>(2 * n) * sizeof(float);
-    if (cudaMemsetAsync(dbias_ws, 0, bytes, st) != cudaSuccess) return HQ_ERR_CUDA;
+    const int rc = zero_floats(static_cast<float*>(dbias_ws), static_cast<int64_t>(L) * 2 * n, nullptr, 0, st);
+    if (rc != HQ_OK) return rc;
   }
+  const bool pdl = dbias != nullptr;
   if (set_smem_once<dglu_kernel<ACT, 1, 128>>(kSmemMax) != HQ_OK ||
       set_smem_once<dglu_kernel<ACT, 2, 128>>(kSmemMax) != HQ_OK ||
       set_smem_once<dglu_kernel<ACT, 1, 256>>(kSmemMax) != HQ_OK ||
@@ -999,13 +1043,15 @@ int run_dglu(const hq_bf16* a, const hq_bf16* b, const int64_t* b_ptrs, const hq
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = static_cast<size_t>(DsCfg<2, 128>::smem_bytes(L));
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, dglu_pair_kernel<ACT>, tmA, tmB, tmC, tmD, p) != cudaSuccess)
       return HQ_ERR_CUDA;
   }
@@ -1017,16 +1063,16 @@ int run_dglu(const hq_bf16* a, const hq_bf16* b, const int64_t* b_ptrs, const hq
   const cudaError_t le =
       pair ? cudaSuccess
       : wide1 ? launch(dglu_kernel<ACT, 1, 256>, g1, dim3(kThreads),
-                    static_cast<int>(DsCfg<1, 256>::smem_bytes(L)), st, false, tmA, tmB, tmC, tmD, p)
+                    static_cast<int>(DsCfg<1, 256>::smem_bytes(L)), st, pdl, tmA, tmB, tmC, tmD, p)
       : kb2 ? launch(dglu_kernel<ACT, 2, 128>, g1, dim3(kThreads),
-                     static_cast<int>(DsCfg<2, 128>::smem_bytes(L)), st, false, tmA, tmB, tmC, tmD, p)
+                     static_cast<int>(DsCfg<2, 128>::smem_bytes(L)), st, pdl, tmA, tmB, tmC, tmD, p)
             : launch(dglu_kernel<ACT, 1, 128>, g1, dim3(kThreads),
-                     static_cast<int>(DsCfg<1, 128>::smem_bytes(L)), st, false, tmA, tmB, tmC, tmD, p);
+                     static_cast<int>(DsCfg<1, 128>::smem_bytes(L)), st, pdl, tmA, tmB, tmC, tmD, p);
   if (le != cudaSuccess) return HQ_ERR_CUDA;
   if (dbias) {
     const int rc = dbias_finalize(reinterpret_cast<uint16_t*>(dbias),
                                   static_cast<const float*>(dbias_ws),
-                                  static_cast<int64_t>(L) * 2 * n, st);
+                                  static_cast<int64_t>(L) * 2 * n, st, true);
     if (rc != HQ_OK) return rc;
   }
   return HQ_OK;

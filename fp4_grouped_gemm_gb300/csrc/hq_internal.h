@@ -46,7 +46,13 @@ int encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, voi
 
 // dbias[i] = bf16(float(dbias[i]) + ws[i]) for i < count, on stream st (the
 // final pass of the dGLU GEMMs' dbias reduction).  Returns HQ_OK or HQ_ERR_CUDA.
-int dbias_finalize(uint16_t* dbias, const float* ws, int64_t count, cudaStream_t st);
+// dbias[i] = bf16(dbias[i] + ws[i]); pdl: launched as a programmatic
+// dependent of the preceding kernel, whose completion it waits for first.
+int dbias_finalize(uint16_t* dbias, const float* ws, int64_t count, cudaStream_t st, bool pdl = false);
+// Zeroes a[0..na) and b[0..nb) (either may be empty); lets the next kernel,
+// if launched as a programmatic dependent, start at once (that kernel waits
+// for the zeroes before it adds into them).
+int zero_floats(float* a, int64_t na, float* b, int64_t nb, cudaStream_t st);
 
 // Discrete weights: the leading part of the caller's workspace holds one
 // 128-byte tensor map per expert, then one int32 flag per expert (1: the
