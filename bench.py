@@ -684,16 +684,17 @@ class Extras:
         byts = E * n * k // 2 + sfb.numel() + tiles * 128 * (k // 2 + k // 16) + valid * n * 2
         res["moe_masked_nvfp4_E32"] = {"us": t * 1e6, "tflops": fl / t / 1e12, "frac_fp4": fl / t / 1e12 / self.p_fp4,
                                       "gbs": byts / t / 1e9, "frac_hbm": byts / t / 1e9 / self.hbm}
-        # the hot-path step on this workload: quantise the activations
-        # (E * max_m rows, BF16 -> NVFP4) and run the masked GEMM against the
-        # resident NVFP4 expert weights
+        # the hot-path step on this workload: quantise the activations' valid
+        # rows (masked_m[e] of each expert's max_m, BF16 -> NVFP4) and run the
+        # masked GEMM against the resident NVFP4 expert weights
         a4 = c4["a"]
 
         def step():
-            hq.hq_quant(a4, "nvfp4", q_out=qa, sf_out=sfa)
+            hq.hq_quant_masked(a4, mm, max_m, "nvfp4", q_out=qa, sf_out=sfa)
             hq.hq_gemm_grouped_masked(qa, sfa, qbv, sfb, mm, max_m, n, k, "nvfp4", alpha=c4["alpha"], out=out4)
         t_step = time_kernel(step, 20, self.flush)
-        t_qa = time_kernel(lambda: hq.hq_quant(a4, "nvfp4", q_out=qa, sf_out=sfa), 20, self.flush)
+        t_qa = time_kernel(lambda: hq.hq_quant_masked(a4, mm, max_m, "nvfp4", q_out=qa, sf_out=sfa), 20, self.flush)
+        t_qa_all = time_kernel(lambda: hq.hq_quant(a4, "nvfp4", q_out=qa, sf_out=sfa), 20, self.flush)
         # end to end through the public API: every step uploads the activations
         # from pinned host memory, quantises them, runs the GEMM and downloads
         # the output rows, one stream, steady state
@@ -703,7 +704,7 @@ class Extras:
 
         def e2e():
             a_d.copy_(a_h, non_blocking=True)
-            hq.hq_quant(a_d, "nvfp4", q_out=qa, sf_out=sfa)
+            hq.hq_quant_masked(a_d, mm, max_m, "nvfp4", q_out=qa, sf_out=sfa)
             hq.hq_gemm_grouped_masked(qa, sfa, qbv, sfb, mm, max_m, n, k, "nvfp4", alpha=c4["alpha"], out=out4)
             out_h.copy_(out4, non_blocking=True)
         for _ in range(3):
@@ -718,8 +719,9 @@ class Extras:
         torch.cuda.synchronize()
         t_e2e = e0.elapsed_time(e1) / reps / 1e3
         res["moe_masked_nvfp4_E32_step"] = {
-            "step": "hq_quant(A [E*max_m, K] -> NVFP4), then hq_gemm_grouped_masked", "us": t_step * 1e6,
-            "quant_us": t_qa * 1e6, "tflops": fl / t_step / 1e12, "launches": 2,
+            "step": "hq_quant_masked(A's valid rows -> NVFP4), then hq_gemm_grouped_masked", "us": t_step * 1e6,
+            "quant_us": t_qa * 1e6, "quant_all_rows_us": t_qa_all * 1e6, "tflops": fl / t_step / 1e12,
+            "launches": 2,
             "e2e": {"us": t_e2e * 1e6, "tflops": fl / t_e2e / 1e12, "h2d_bytes_per_step": a4.numel() * 2,
                     "d2h_bytes_per_step": out4.numel() * 2,
                     "note": "weights resident; activations up, output rows down, one stream"}}

@@ -189,6 +189,29 @@ def hq_quant(x, mode, use_swizzle=True, global_scale=None, q_out=None, sf_out=No
     return q_out, sf_out
 
 
+def hq_quant_masked(x, masked_m, max_m, mode, use_swizzle=True, global_scale=None, q_out=None,
+                    sf_out=None, use_pdl=False, stream=None):
+    """hq_quant over the grouped-masked layout: x [E * max_m, k] BF16,
+    masked_m device int32 [E]; only rows below masked_m[e] in each expert's
+    block are quantised (the others keep q_out / sf_out's bytes).
+    Returns (q, sf)."""
+    m, k = x.shape
+    E = masked_m.numel()
+    if x.dtype != torch.bfloat16:
+        raise ValueError("hq_quant_masked takes bfloat16 input")
+    if m != E * max_m:
+        raise ValueError("x must hold E * max_m rows")
+    if q_out is None:
+        q_out = torch.empty(_q_shape(m, k, mode), dtype=torch.uint8, device=x.device)
+    if sf_out is None:
+        sf_out = torch.empty(max(sf_bytes(m, k, mode), 1), dtype=torch.uint8, device=x.device)
+    rc = _abi.load().hq_quant_masked(_ptr(x), E, max_m, _ptr(masked_m), k, mode_id(mode),
+                                     1 if use_swizzle else 0, _ptr(global_scale), _ptr(q_out), _ptr(sf_out),
+                                     1 if use_pdl else 0, _stream(stream))
+    _check(rc, "hq_quant_masked")
+    return q_out, sf_out
+
+
 def hq_gemm_dense(a, sfa, b, sfb, m, n, k, mode, alpha=None, bias=None, out=None, sm_count=-1,
                   use_pdl=False, stream=None):
     if out is None:

@@ -67,6 +67,7 @@ SIGNATURES = {
     "hq_set_gemm_2sm": (c_i32, [c_i32]),
     "hq_quant": (c_i32, [c_p, c_i64, c_i64, c_i32, c_i32, c_p, c_p, c_p, c_i32, c_p]),
     "hq_quant_f16": (c_i32, [c_p, c_i64, c_i64, c_i32, c_i32, c_p, c_p, c_p, c_i32, c_p]),
+    "hq_quant_masked": (c_i32, [c_p, c_i32, c_i64, c_p, c_i64, c_i32, c_i32, c_p, c_p, c_p, c_i32, c_p]),
     "hq_gemm_dense": (c_i32, [c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_i64, c_i64, c_i64, c_i32,
                               c_i32, c_i32, c_p]),
     "hq_gemm_grouped_contig": (c_i32, [c_p, c_p, c_p, c_p, c_p, c_i32, c_p, c_p, c_p, c_i64,

@@ -29,6 +29,9 @@ namespace hq {
 namespace {
 
 constexpr int kThreads = 256;
+// experts a token-count array may hold (their valid-row prefix is kept in
+// shared memory)
+constexpr int kMaxCountExperts = 8192;
 
 // Lanes that share one scale group: the MXFP8 SwiGLU pass splits each
 // 32-value group over a lane pair (two groups in flight per lane pair: fewer
@@ -58,7 +61,7 @@ struct QuantParams {
   const float* global_scale; // NVFP4 norm_const, may be null (= 1)
   uint8_t* q;
   uint8_t* sf;
-  const int32_t* token_nums; // swiglu only, may be null
+  const int32_t* token_nums; // valid rows per block of rows_per_expert rows, or null (all valid)
   int64_t rows_per_expert;
   int E;
   int zero_pad_rows;         // write 0 to the scale bytes of padding rows
@@ -220,8 +223,9 @@ __device__ __forceinline__ uint32_t encode_group(const float (&x)[GL], float g,
   }
 }
 
-// F16IN: the input rows hold IEEE binary16 values instead of BF16
-template <int MODE, bool SWIGLU, bool F16IN = false>
+// F16IN: the input rows hold IEEE binary16 values instead of BF16.
+// COUNTS: p.token_nums is set (only each expert's first token_nums[e] rows).
+template <int MODE, bool SWIGLU, bool F16IN = false, bool COUNTS = false>
 __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
   constexpr int GS = MODE == HQ_NVFP4 ? 16 : 32;
   constexpr int LPG = lanes_per_group(MODE, SWIGLU);
@@ -244,41 +248,84 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
-  // an item is GPI consecutive groups of one row; lane l works on groups
-  // l / LPG, l / LPG + GPI / U, ... (part l % LPG of each)
+  // token_nums: only the first token_nums[e] rows of each expert's
+  // rows_per_expert are processed.  One warp turns the (clamped, flagged)
+  // counts into an exclusive prefix of valid rows in shared memory, so the
+  // items below run over valid rows only.
+  extern __shared__ int32_t s_valid_prefix[];  // [E + 1] with token_nums
+  if (COUNTS) {
+    if (threadIdx.x < 32) {
+      int32_t carry = 0;
+      bool clamped = false;
+      for (int base = 0; base < p.E; base += 32) {
+        const int e = base + lane;
+        int32_t c = 0;
+        if (e < p.E) {
+          c = __ldg(p.token_nums + e);
+          if (c < 0 || c > p.rows_per_expert) {
+            clamped = true;
+            c = c < 0 ? 0 : static_cast<int32_t>(p.rows_per_expert);
+          }
+        }
+        int32_t incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += u;
+        }
+        if (e < p.E) s_valid_prefix[e] = carry + incl - c;
+        carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      }
+      if (lane == 0) s_valid_prefix[p.E] = carry;
+      if (__any_sync(0xFFFFFFFFu, clamped) && lane == 0 && blockIdx.x == 0)
+        atomicOr(p.status, HQ_STATUS_TOKENS_CLAMPED);
+    }
+    __syncthreads();
+  }
+  // an item is GPI consecutive groups of one (valid) row; lane l works on
+  // groups l / LPG, l / LPG + GPI / U, ... (part l % LPG of each)
   const int64_t groups_row = p.S_real;
   const int64_t chunks = (groups_row + GPI - 1) / GPI;
-  const int64_t items = p.rows * chunks;
+  const int64_t valid_rows = COUNTS ? s_valid_prefix[p.E] : p.rows;
+  const int64_t items = valid_rows * chunks;
   const bool small = items < (1ll << 31);
 
   // Software pipeline: the loads of a warp's next item are issued before the
   // current item is encoded, so load latency overlaps the arithmetic.
-  auto row_of = [&](int64_t item) -> int64_t {
-    return small ? static_cast<int64_t>(static_cast<uint32_t>(item) / static_cast<uint32_t>(chunks))
-                 : item / chunks;
+  // item -> (row, first group): valid row vr = item / chunks, which with
+  // token_nums lies in the last expert e whose prefix is <= vr; a warp's
+  // items increase, so its expert index only moves forward
+  // cur_e's first valid row and the next expert's, kept in registers
+  int cur_e = 0;
+  int64_t cur_base = 0, next_bound = 0;
+  auto set_expert = [&](int e) {
+    cur_e = e;
+    cur_base = s_valid_prefix[e];
+    next_bound = e + 1 < p.E ? s_valid_prefix[e + 1] : INT64_MAX;
   };
-  // token_nums: rows past an expert's count are skipped (data and scales)
-  auto row_valid = [&](int64_t row) -> bool {
-    if (!(SWIGLU && p.token_nums)) return true;
-    const int64_t e = row / p.rows_per_expert;
-    const int64_t local = row - e * p.rows_per_expert;
-    int tn = __ldg(p.token_nums + e);
-    if (tn < 0 || tn > p.rows_per_expert) {
-      if (lane == 0 && local == 0) atomicOr(p.status, HQ_STATUS_TOKENS_CLAMPED);
-      tn = tn < 0 ? 0 : static_cast<int>(p.rows_per_expert);
+  auto item_pos = [&](int64_t item, int64_t& row, int64_t& s0) {
+    const int64_t vr = small ? static_cast<int64_t>(static_cast<uint32_t>(item) / static_cast<uint32_t>(chunks))
+                             : item / chunks;
+    s0 = (item - vr * chunks) * GPI;
+    if (!COUNTS) {
+      row = vr;
+      return;
     }
-    return local < tn;
+    while (vr >= next_bound) set_expert(cur_e + 1);
+    row = static_cast<int64_t>(cur_e) * p.rows_per_expert + (vr - cur_base);
   };
   uint4 v0[U][NV], v1[U][NV];
+  int64_t next_row = 0, next_s0 = 0;  // position of the item whose loads are in v0 / v1
   auto load_item = [&](int64_t item) {
-    const int64_t row = row_of(item);
-    const int64_t s0 = (item - row * chunks) * GPI;
-    const bool rv = row_valid(row);
+    int64_t row, s0;
+    item_pos(item, row, s0);
+    next_row = row;
+    next_s0 = s0;
     const uint16_t* src_row = p.in + row * p.in_stride;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t s = s0 + u * GPU_ + lane / LPG;
-      const bool ok = rv && s < groups_row;
+      const bool ok = s < groups_row;
       const uint4* src = reinterpret_cast<const uint4*>(src_row + s * GS + (lane % LPG) * GL);
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
@@ -287,6 +334,16 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
       }
     }
   };
+  if (COUNTS && warp < items) {
+    // the warp's first expert by binary search; later ones by stepping
+    const int64_t vr = warp / chunks;
+    int lo = 0, hi = p.E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_valid_prefix[mid] <= vr) lo = mid; else hi = mid - 1;
+    }
+    set_expert(lo);
+  }
   if (warp < items) load_item(warp);
   for (int64_t item = warp; item < items; item += nwarps) {
     uint4 c0[U][NV], c1[U][NV];
@@ -297,10 +354,8 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
         c0[u][i] = v0[u][i];
         if (SWIGLU) c1[u][i] = v1[u][i];
       }
+    const int64_t row = next_row, s0 = next_s0;  // this item's position (set when its loads were issued)
     if (item + nwarps < items) load_item(item + nwarps);
-    const int64_t row = row_of(item);
-    const int64_t s0 = (item - row * chunks) * GPI;
-    if (!row_valid(row)) continue;  // warp-uniform
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t s = s0 + u * GPU_ + lane / LPG;
@@ -376,7 +431,7 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
     const int64_t n = p.rows * extra;
     for (int64_t i = tid; i < n; i += nthreads) {
       const int64_t r = i / extra, s = p.S_real + i % extra;
-      if (SWIGLU && p.token_nums) {
+      if (COUNTS) {
         const int64_t e = r / p.rows_per_expert;
         int64_t tn = __ldg(p.token_nums + e);
         tn = tn < 0 ? 0 : (tn > p.rows_per_expert ? p.rows_per_expert : tn);
@@ -389,13 +444,15 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(const QuantParams p) {
   pdl_launch_dependents();
 }
 
-template <int MODE, bool SWIGLU, bool F16IN = false>
+template <int MODE, bool SWIGLU, bool F16IN = false, bool COUNTS = false>
 int launch_quant(const QuantParams& p, cudaStream_t st, bool pdl) {
   const int sms = num_sms();
   if (sms <= 0) return HQ_ERR_CUDA;
+  // the valid-row prefix (token counts only) lives in dynamic shared memory
+  const size_t smem = COUNTS ? static_cast<size_t>(p.E + 1) * sizeof(int32_t) : 0;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_kernel<MODE, SWIGLU, F16IN>,
-                                                    kThreads, 0) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_kernel<MODE, SWIGLU, F16IN, COUNTS>,
+                                                    kThreads, smem) != cudaSuccess)
     return HQ_ERR_CUDA;
   if (per_sm < 1) per_sm = 1;
   constexpr int64_t kItem = groups_per_item(MODE, SWIGLU);
@@ -404,8 +461,8 @@ int launch_quant(const QuantParams& p, cudaStream_t st, bool pdl) {
   const int64_t cap = static_cast<int64_t>(sms) * per_sm;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  cudaError_t e = launch(quant_kernel<MODE, SWIGLU, F16IN>, dim3(static_cast<unsigned>(blocks)),
-                         dim3(kThreads), 0, st, pdl, p);
+  cudaError_t e = launch(quant_kernel<MODE, SWIGLU, F16IN, COUNTS>, dim3(static_cast<unsigned>(blocks)),
+                         dim3(kThreads), smem, st, pdl, p);
   return e == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
 }
 
@@ -416,18 +473,29 @@ int dispatch_f16(hq_mode mode, const QuantParams& p, cudaStream_t st, bool pdl) 
   return launch_quant<HQ_NVFP4, false, true>(p, st, pdl);
 }
 
-int dispatch(hq_mode mode, bool swiglu, const QuantParams& p, cudaStream_t st, bool pdl) {
+// With per-expert counts (token_nums) only the valid rows are mapped to work.
+template <bool COUNTS>
+int dispatch_bf16(hq_mode mode, bool swiglu, const QuantParams& p, cudaStream_t st, bool pdl) {
   if (mode == HQ_MXFP8)
-    return swiglu ? launch_quant<HQ_MXFP8, true>(p, st, pdl) : launch_quant<HQ_MXFP8, false>(p, st, pdl);
-  if (mode == HQ_MXFP4) return swiglu ? HQ_ERR_INVALID : launch_quant<HQ_MXFP4, false>(p, st, pdl);
-  if (mode == HQ_MXFP8_E5M2) return swiglu ? HQ_ERR_INVALID : launch_quant<HQ_MXFP8_E5M2, false>(p, st, pdl);
-  return swiglu ? launch_quant<HQ_NVFP4, true>(p, st, pdl) : launch_quant<HQ_NVFP4, false>(p, st, pdl);
+    return swiglu ? launch_quant<HQ_MXFP8, true, false, COUNTS>(p, st, pdl)
+                  : launch_quant<HQ_MXFP8, false, false, COUNTS>(p, st, pdl);
+  if (mode == HQ_MXFP4) return swiglu ? HQ_ERR_INVALID : launch_quant<HQ_MXFP4, false, false, COUNTS>(p, st, pdl);
+  if (mode == HQ_MXFP8_E5M2)
+    return swiglu ? HQ_ERR_INVALID : launch_quant<HQ_MXFP8_E5M2, false, false, COUNTS>(p, st, pdl);
+  return swiglu ? launch_quant<HQ_NVFP4, true, false, COUNTS>(p, st, pdl)
+                : launch_quant<HQ_NVFP4, false, false, COUNTS>(p, st, pdl);
+}
+
+int dispatch(hq_mode mode, bool swiglu, const QuantParams& p, cudaStream_t st, bool pdl) {
+  return p.token_nums ? dispatch_bf16<true>(mode, swiglu, p, st, pdl)
+                      : dispatch_bf16<false>(mode, swiglu, p, st, pdl);
 }
 
 // Shared host side of hq_quant / hq_quant_f16: validation, then the launch.
 int quant_entry(const uint16_t* x, bool f16, int64_t m, int64_t k, hq_mode mode, int use_swizzle,
                 const float* global_scale, void* q_out, uint8_t* sf_out, int use_pdl,
-                hq_stream_t s) {
+                hq_stream_t s, const int32_t* token_nums = nullptr, int E = 0,
+                int64_t rows_per_expert = 0) {
   if (mode != HQ_MXFP8 && mode != HQ_MXFP4 && mode != HQ_NVFP4 && mode != HQ_MXFP8_E5M2)
     return HQ_ERR_INVALID;
   const int64_t gs = mode == HQ_NVFP4 ? 16 : 32;
@@ -450,6 +518,14 @@ int quant_entry(const uint16_t* x, bool f16, int64_t m, int64_t k, hq_mode mode,
   p.q = static_cast<uint8_t*>(q_out);
   p.sf = sf_out;
   p.zero_pad_rows = 1;
+  if (token_nums) {
+    p.token_nums = token_nums;
+    p.rows_per_expert = rows_per_expert;
+    p.E = E;
+  } else {
+    p.rows_per_expert = m;
+    p.E = 1;
+  }
   p.status = status_word_ptr();
   if (!p.status) return HQ_ERR_CUDA;
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
@@ -473,6 +549,16 @@ int hq_quant_f16(const uint16_t* x, int64_t m, int64_t k, hq_mode mode, int use_
   return hq::quant_entry(x, true, m, k, mode, use_swizzle, global_scale, q_out, sf_out, use_pdl, s);
 }
 
+int hq_quant_masked(const hq_bf16* x, int E, int64_t max_m, const int32_t* masked_m, int64_t k,
+                    hq_mode mode, int use_swizzle, const float* global_scale, void* q_out,
+                    uint8_t* sf_out, int use_pdl, hq_stream_t s) {
+  if (E <= 0 || E > hq::kMaxCountExperts || max_m <= 0 || max_m % 128 != 0) return HQ_ERR_INVALID;
+  if (!masked_m || (reinterpret_cast<uintptr_t>(masked_m) & 3u)) return HQ_ERR_INVALID;
+  if (max_m > (1ll << 31) / E) return HQ_ERR_INVALID;
+  return hq::quant_entry(x, false, static_cast<int64_t>(E) * max_m, k, mode, use_swizzle, global_scale, q_out,
+                         sf_out, use_pdl, s, masked_m, E, max_m);
+}
+
 int hq_swiglu_quant(const hq_bf16* in, int64_t rows, int64_t H, const int32_t* token_nums, int E,
                     int64_t rows_per_expert, hq_mode mode, const float* global_scale,
                     void* q_out, uint8_t* sf_out, hq_stream_t s) {
@@ -482,7 +568,8 @@ int hq_swiglu_quant(const hq_bf16* in, int64_t rows, int64_t H, const int32_t* t
   if (mode == HQ_NVFP4 && H % 64 != 0) return HQ_ERR_INVALID;
   if (mode == HQ_MXFP8 && global_scale) return HQ_ERR_UNSUPPORTED;
   if (token_nums) {
-    if (E <= 0 || rows_per_expert <= 0 || static_cast<int64_t>(E) * rows_per_expert != rows)
+    if (E <= 0 || E > hq::kMaxCountExperts || rows_per_expert <= 0 ||
+        static_cast<int64_t>(E) * rows_per_expert != rows)
       return HQ_ERR_INVALID;
   }
   if (rows == 0) return HQ_OK;

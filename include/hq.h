@@ -253,6 +253,20 @@ int hq_quant_f16(const uint16_t *x, int64_t m, int64_t k, hq_mode mode, int use_
                  const float *global_scale, void *q_out, uint8_t *sf_out, int use_pdl,
                  hq_stream_t s);
 
+/* hq_quant over the grouped-masked layout (HALOps group_masked_gemm: E
+ * experts of max_m rows each, masked_m[e] valid rows from row e * max_m):
+ * quantises only the valid rows of x [E * max_m, k], as the masked GEMM
+ * reads no other row's result.  Rows past masked_m[e] keep their codes and
+ * scale bytes untouched; masked_m[e] outside [0, max_m] is clamped and sets
+ * HQ_STATUS_TOKENS_CLAMPED.  Only valid rows are visited (their prefix is
+ * kept in shared memory: E <= 8192).  max_m % 128 == 0 (HQ_ERR_INVALID otherwise), so
+ * sf_out holds hq_sf_bytes(E * max_m, k, mode) bytes and no padding rows.
+ * masked_m: device int32 [E], 4-byte aligned.  The other arguments are
+ * hq_quant's. */
+int hq_quant_masked(const hq_bf16 *x, int E, int64_t max_m, const int32_t *masked_m, int64_t k,
+                    hq_mode mode, int use_swizzle, const float *global_scale, void *q_out,
+                    uint8_t *sf_out, int use_pdl, hq_stream_t s);
+
 /* ------------------------------------------------------------------------- *
  * Block-scaled GEMMs: out = alpha * (A . B^T) + bias, BF16 output (RNE).
  *
@@ -339,7 +353,9 @@ int hq_gemm_grouped_masked(const void *a, const uint8_t *sfa, const void *b, con
  *               MXFP8 columns [H/32, kb_dim) of written rows hold 0; with
  *               token_nums == NULL the padding rows hold 0.
  * Requires H % 128 == 0 (MXFP8) or H % 64 == 0 (NVFP4), rows_per_expert > 0
- * and E * rows_per_expert == rows when token_nums is given. */
+ * and E * rows_per_expert == rows when token_nums is given, with E <= 8192
+ * (the valid-row prefix is kept in shared memory); only valid rows are
+ * visited, so the time follows the valid rows, not all of them. */
 int hq_swiglu_quant(const hq_bf16 *in, int64_t rows, int64_t H, const int32_t *token_nums, int E,
                     int64_t rows_per_expert, hq_mode mode, const float *global_scale,
                     void *q_out, uint8_t *sf_out, hq_stream_t s);

@@ -76,6 +76,15 @@ def test_quant_rejects_bad_arguments(lib):
     assert lib.hq_quant_f16(FAKE, 4, 96, 0, 1, None, FAKE, FAKE, 0, None) == _abi.HQ_ERR_INVALID
     assert lib.hq_quant_f16(FAKE, 4, 128, 1, 1, FAKE, FAKE, FAKE, 0, None) == _abi.HQ_ERR_UNSUPPORTED
     assert lib.hq_quant_f16(FAKE, 0, 128, 2, 1, None, FAKE, FAKE, 0, None) == _abi.HQ_OK
+    # the masked-layout entry: E in [1, 8192], max_m a multiple of 128, an aligned count array
+    qm = lib.hq_quant_masked
+    assert qm(FAKE, 0, 128, FAKE, 128, 2, 1, None, FAKE, FAKE, 0, None) == _abi.HQ_ERR_INVALID
+    assert qm(FAKE, 8193, 128, FAKE, 128, 2, 1, None, FAKE, FAKE, 0, None) == _abi.HQ_ERR_INVALID
+    assert qm(FAKE, 4, 100, FAKE, 128, 2, 1, None, FAKE, FAKE, 0, None) == _abi.HQ_ERR_INVALID
+    assert qm(FAKE, 4, 128, None, 128, 2, 1, None, FAKE, FAKE, 0, None) == _abi.HQ_ERR_INVALID
+    assert qm(FAKE, 4, 128, ctypes.c_void_p(0x10002), 128, 2, 1, None, FAKE, FAKE, 0, None) == \
+        _abi.HQ_ERR_INVALID
+    assert qm(FAKE, 4, 128, FAKE, 96, 0, 1, None, FAKE, FAKE, 0, None) == _abi.HQ_ERR_INVALID
 
 
 def test_gemm_rejects_bad_arguments(lib):

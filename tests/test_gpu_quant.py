@@ -130,3 +130,69 @@ def test_quant_mxfp8_e5m2_special_values(cuda_dev):
     x[3, 0], x[3, 1] = 1.0e-30, -1.0e-30
     x[4, 32:64] = torch.linspace(-3.0e4, 3.0e4, 32)
     run_and_compare(x.to(torch.bfloat16), "mxfp8_e5m2", True)
+
+
+@pytest.mark.parametrize("mode", ["mxfp8", "nvfp4", "mxfp4"])
+@pytest.mark.parametrize("swizzle", [True, False])
+def test_quant_masked_layout(cuda_dev, mode, swizzle):
+    """hq_quant_masked (grouped-masked layout, E experts of max_m rows): the
+    valid rows are hq_quant's bytes (oracle, bit for bit); rows past
+    masked_m[e] keep their codes and scale bytes; a count above max_m is
+    clamped and flagged."""
+    E, max_m, k = 5, 256, 512
+    masked = [0, 1, 129, 256, 300]            # the last is clamped to 256
+    dev = torch.device("cuda")
+    x_cpu = bf16_rows(E * max_m, k, seed=71, spread=2)
+    g = 3.0 if mode == "nvfp4" else None
+    gs_t = torch.tensor([g], dtype=torch.float32, device=dev) if g is not None else None
+    one_byte = mode == "mxfp8"
+    q = torch.full(((E * max_m, k) if one_byte else (E * max_m, k // 2)), 0xAA, dtype=torch.uint8, device=dev)
+    sf = torch.full((hq.sf_bytes(E * max_m, k, mode),), 0xAA, dtype=torch.uint8, device=dev)
+    mm = torch.tensor(masked, dtype=torch.int32, device=dev)
+    hq.get_device_status(clear=True)
+    hq.hq_quant_masked(x_cpu.to(dev), mm, max_m, mode, use_swizzle=swizzle, global_scale=gs_t, q_out=q, sf_out=sf)
+    torch.cuda.synchronize()
+    status, _ = hq.get_device_status(clear=True)
+    assert status & hq._abi.HQ_STATUS_TOKENS_CLAMPED
+    valid = np.zeros(E * max_m, dtype=bool)
+    for e, c in enumerate(masked):
+        valid[e * max_m: e * max_m + min(c, max_m)] = True
+    q_ref, sf_ref = oquant.group_wise_quant(np_f32(x_cpu), mode, swizzle, g)
+    q_gpu, sf_gpu = q.cpu().numpy(), sf.cpu().numpy()
+    assert np.array_equal(q_gpu[valid], q_ref[valid]), "valid rows' codes"
+    assert (q_gpu[~valid] == 0xAA).all(), "codes written for rows past masked_m"
+    S = k // oquant.GROUP_SIZE[mode]
+    rr, ss = np.meshgrid(np.arange(E * max_m), np.arange(S), indexing="ij")
+    off = oquant.sfatom_offset(rr, ss, S) if swizzle else rr * S + ss
+    assert np.array_equal(sf_gpu[off][valid], sf_ref[off][valid]), "valid rows' scale bytes"
+    assert (sf_gpu[off][~valid] == 0xAA).all(), "scale bytes written for rows past masked_m"
+
+
+def test_quant_masked_many_experts(cuda_dev):
+    """hq_quant_masked with 2000 experts of random counts (a third empty):
+    the valid-row prefix spans many warps' worth of experts, so each warp's
+    first expert comes from the search and later ones from stepping; valid
+    rows match the oracle bit for bit, the others stay untouched."""
+    E, max_m, k, mode = 2000, 128, 64, "nvfp4"
+    rng = np.random.default_rng(72)
+    counts = rng.integers(0, max_m + 1, size=E)
+    counts[rng.random(E) < 0.33] = 0
+    dev = torch.device("cuda")
+    x_cpu = bf16_rows(E * max_m, k, seed=73, spread=2)
+    q = torch.full((E * max_m, k // 2), 0xAA, dtype=torch.uint8, device=dev)
+    sf = torch.full((hq.sf_bytes(E * max_m, k, mode),), 0xAA, dtype=torch.uint8, device=dev)
+    mm = torch.tensor(counts, dtype=torch.int32, device=dev)
+    hq.get_device_status(clear=True)
+    hq.hq_quant_masked(x_cpu.to(dev), mm, max_m, mode, use_swizzle=False, q_out=q, sf_out=sf)
+    torch.cuda.synchronize()
+    status, _ = hq.get_device_status(clear=True)
+    assert status == 0
+    valid = (np.arange(E * max_m) % max_m) < np.repeat(counts, max_m)
+    rows = np.nonzero(valid)[0]
+    q_ref, sf_ref = oquant.quantize(np_f32(x_cpu[torch.from_numpy(rows)]), mode, None)
+    q_gpu = q.cpu().numpy()
+    S = k // oquant.GROUP_SIZE[mode]
+    sf_gpu = sf.cpu().numpy()[:E * max_m * S].reshape(E * max_m, S)
+    assert np.array_equal(q_gpu[rows], q_ref), "valid rows' codes"
+    assert np.array_equal(sf_gpu[rows], sf_ref.reshape(len(rows), S)), "valid rows' scale bytes"
+    assert (q_gpu[~valid] == 0xAA).all() and (sf_gpu[~valid] == 0xAA).all(), "rows past masked_m written"
