@@ -344,11 +344,6 @@ __device__ __forceinline__ void epilogue_tile_wide(const EpiArgs& e, int cw2, Re
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float dglu_bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float dglu_bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-__device__ __forceinline__ float dglu_rcp(float x) {
-  float r;
-  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
-  return r;
-}
 
 template <int EPI>
 __device__ __forceinline__ void dglu_math(const uint32_t (&r)[32], const uint4 (&cv)[8], float a2, float beta,
@@ -365,8 +360,8 @@ __device__ __forceinline__ void dglu_math(const uint32_t (&r)[32], const uint4 (
       float g0, g1, x0, x1;
       mul_f32x2(g0, g1, dglu_bf16_lo(gw), dglu_bf16_hi(gw), beta);
       mul_f32x2(x0, x1, dglu_bf16_lo(iw), dglu_bf16_hi(iw), beta);
-      const float s0 = dglu_rcp(__fadd_rn(1.0f, __expf(-g0)));
-      const float s1 = dglu_rcp(__fadd_rn(1.0f, __expf(-g1)));
+      float s0, s1;
+      sigmoid_x2(g0, g1, s0, s1);  // sigmoid(gate)
       float om0, om1, t0, t1, gs0, gs1, u0, u1, q0, q1;
       fma_f32x2(om0, om1, s0, s1, -1.0f, -1.0f, 1.0f, 1.0f);
       fma_f32x2(t0, t1, g0, g1, om0, om1, 1.0f, 1.0f);
@@ -384,8 +379,8 @@ __device__ __forceinline__ void dglu_math(const uint32_t (&r)[32], const uint4 (
       const float uc0 = fminf(fmaxf(x0, -7.0f), 7.0f), uc1 = fminf(fmaxf(x1, -7.0f), 7.0f);
       float kg0, kg1;
       mul_f32x2(kg0, kg1, gc0, gc1, 1.702f);
-      const float s0 = dglu_rcp(__fadd_rn(1.0f, __expf(-kg0)));
-      const float s1 = dglu_rcp(__fadd_rn(1.0f, __expf(-kg1)));
+      float s0, s1;
+      sigmoid_x2(kg0, kg1, s0, s1);
       float om0, om1, t0, t1, up0, up1, gs0, gs1, w0, w1, a0, a1, b0, b1, q0, q1;
       fma_f32x2(om0, om1, s0, s1, -1.0f, -1.0f, 1.0f, 1.0f);
       fma_f32x2(t0, t1, kg0, kg1, om0, om1, 1.0f, 1.0f);
@@ -461,11 +456,14 @@ __device__ __forceinline__ void dglu_write_row(const GemmParams& p, const float 
         uint32_t w[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const uint32_t lo = cvt8x2(__fmul_rn(__fmul_rn(v[4 * i + 1], norm), mult),
-                                     __fmul_rn(__fmul_rn(v[4 * i], norm), mult));
-          const uint32_t hi = cvt8x2(__fmul_rn(__fmul_rn(v[4 * i + 3], norm), mult),
-                                     __fmul_rn(__fmul_rn(v[4 * i + 2], norm), mult));
-          w[i] = lo | (hi << 16);
+          // (D * norm) * mult, each product rounded, two values per instruction
+          float y[4];
+#pragma unroll
+          for (int u = 0; u < 4; u += 2) {
+            mul_f32x2(y[u], y[u + 1], v[4 * i + u], v[4 * i + u + 1], norm);
+            mul_f32x2(y[u], y[u + 1], y[u], y[u + 1], mult);
+          }
+          w[i] = cvt8x2(y[1], y[0]) | (cvt8x2(y[3], y[2]) << 16);
         }
         if (dbuf) {
           // plain 64-byte rows: this half's 32 codes are units 2 h and 2 h + 1 of row `lane`
@@ -617,8 +615,8 @@ __device__ __forceinline__ void swiglu_drain(uint32_t tcol, float alpha, float (
       float g0, g1, u0, u1;
       mul_f32x2(g0, g1, __uint_as_float(rg[i]), __uint_as_float(rg[i + 1]), alpha);
       mul_f32x2(u0, u1, __uint_as_float(ru[i]), __uint_as_float(ru[i + 1]), alpha);
-      const float t0 = __fmul_rn(g0, dglu_rcp(__fadd_rn(1.0f, __expf(-g0))));
-      const float t1 = __fmul_rn(g1, dglu_rcp(__fadd_rn(1.0f, __expf(-g1))));
+      const float t0 = __fmul_rn(g0, rcp_approx(__fadd_rn(1.0f, __expf(-g0))));
+      const float t1 = __fmul_rn(g1, rcp_approx(__fadd_rn(1.0f, __expf(-g1))));
       mul2_f32x2(y[16 * s + i], y[16 * s + i + 1], u0, u1, t0, t1);
     }
   }
@@ -1270,6 +1268,7 @@ struct Cfg2 {
 template <int MODE, int STAGES, int EPI = kEpiGemm, int BN = 256>
 __global__ void __launch_bounds__(kThreads, 1)
     bs_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmB64, const __grid_constant__ CUtensorMap tmSFB,
                        const GemmParams p) {
   using C = Cfg2<MODE, STAGES, BN>;
   constexpr bool kUpProj = EPI == kEpiSwiGLUQ;
@@ -1317,6 +1316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (kWide) tma_prefetch_desc(&tmB64);
+    if (!kUpProj) tma_prefetch_desc(&tmSFB);
   }
   if (warp == 1) {  // one warp in each CTA allocates, collectively for the pair
     tmem_alloc_2sm(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -1437,6 +1438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     (pt.valid1 > 0 ? C::A_BYTES : 0u) + 2u * C::B_BYTES;
         const uint8_t* sfa_rows = p.sfa + (row0 / kBM) * atoms_total * 512;
         const uint8_t* sfb_grp = p.sfb + static_cast<int64_t>(pt.g) * p.sfb_group_bytes;
+        const int64_t sfb_blk0 = static_cast<int64_t>(pt.g) * (p.sfb_group_bytes / (128 * p.S));
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, wctx)) { ok = false; break; }
           int atoms = atoms_total - kb * C::ATOMS;
@@ -1453,24 +1455,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d_pair(sbase + C::OFF_A + stage * C::A_BYTES, &tmA, fb, kb * kBKBytes,
                              static_cast<int32_t>(row0));
           const uint32_t b_s = sbase + C::OFF_B + stage * C::B_BYTES;
-          if (kWide) {
-            // 64-row boxes: B rows [n0 + 128 r, + 128) for the N = 256 MMA,
-            // then [n0 + 256 + 64 r, + 64) for the N = 128 MMA
-            tma_load_3d_pair(b_s, &tmB, fb, kb * kBKBytes, nh0, pt.g);
-            tma_load_3d_pair(b_s + 64 * kBKBytes, &tmB, fb, kb * kBKBytes, nh0 + 64, pt.g);
-            tma_load_3d_pair(b_s + 128 * kBKBytes, &tmB, fb, kb * kBKBytes,
+          // B rows [n0 + 128 r, + 128) for the N = 256 MMA and, for the wide
+          // tile, [n0 + 256 + 64 r, + 64) for the N = 128 MMA
+          tma_load_3d_pair(b_s, &tmB, fb, kb * kBKBytes, nh0, pt.g);
+          if (kWide)
+            tma_load_3d_pair(b_s + 128 * kBKBytes, &tmB64, fb, kb * kBKBytes,
                              pt.n0 + 256 + static_cast<int>(rank) * 64, pt.g);
-          } else {
-            tma_load_3d_pair(b_s, &tmB, fb, kb * kBKBytes, nh0, pt.g);
-          }
-          mbar_arrive_expect_tx(sffull_bar(stage), atoms * 512u * (has_sfa ? 1u + rb_valid : rb_valid));
+          // B scales: one box of the tile's RB consecutive 128-row blocks
+          // (atoms past K and blocks past the tensor read as zeros and count
+          // in full; blocks past n are never used); the fused up-proj's two
+          // blocks are apart, one bulk copy each
+          const uint32_t sfb_bytes = kUpProj ? atoms * 512u * rb_valid : static_cast<uint32_t>(C::SFB_BYTES);
+          mbar_arrive_expect_tx(sffull_bar(stage), (has_sfa ? atoms * 512u : 0u) + sfb_bytes);
           if (has_sfa)
             bulk_load(sbase + C::OFF_SFA + stage * C::SFA_BYTES, sfa_rows + kb * C::ATOMS * 512,
                       atoms * 512u, sffull_bar(stage));
-          for (int rb = 0; rb < rb_valid; ++rb)
-            bulk_load(sbase + C::OFF_SFB + stage * C::SFB_BYTES + rb * C::ATOMS * 512,
-                      sfb_grp + (sfb_blk(rb) * atoms_total + kb * C::ATOMS) * 512,
-                      atoms * 512u, sffull_bar(stage));
+          if (kUpProj) {
+            for (int rb = 0; rb < rb_valid; ++rb)
+              bulk_load(sbase + C::OFF_SFB + stage * C::SFB_BYTES + rb * C::ATOMS * 512,
+                        sfb_grp + (sfb_blk(rb) * atoms_total + kb * C::ATOMS) * 512,
+                        atoms * 512u, sffull_bar(stage));
+          } else {
+            tma_load_3d(sbase + C::OFF_SFB + stage * C::SFB_BYTES, &tmSFB, sffull_bar(stage), 0, kb * C::ATOMS,
+                        static_cast<int32_t>(sfb_blk0 + pt.n0 / 128));
+          }
           filled_a |= 1u << stage;
           filled_s |= 1u << stage;
           par_a = (par_a & ~(1u << stage)) | (phase << stage);
@@ -1807,12 +1815,34 @@ int run_bs_2sm(const void* a, const void* b, const GemmParams& p, int sm_count, 
                                strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != HQ_OK) return rc;
   }
+  CUtensorMap tmB64, tmSFB;
   {
     const uint64_t dims[3] = {kbytes, b_rows, static_cast<uint64_t>(p.gs.groups)};
     const uint64_t strides[2] = {kbytes, kbytes * b_rows};
-    const uint32_t box[3] = {kBKBytes, BN == 384 ? 64u : 128u, 1};  // wide tile: 64-row boxes
+    const uint32_t box[3] = {kBKBytes, 128u, 1};
     int rc = encode_tensor_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(b), dims,
                                strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != HQ_OK) return rc;
+    tmB64 = tmB;
+    if (BN == 384) {  // the wide tile's last 128 rows: 64 per CTA
+      const uint32_t box64[3] = {kBKBytes, 64u, 1};
+      rc = encode_tensor_map(&tmB64, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(b), dims, strides,
+                             box64, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (rc != HQ_OK) return rc;
+    }
+  }
+  // B scale atoms as [blocks of 128 rows][k-atoms][128 words of 32 bits]; a
+  // box is a tile's RB blocks of one k-block
+  tmSFB = tmB;
+  if (!kUpProj) {
+    const uint64_t atoms_total = static_cast<uint64_t>(p.S / 4);
+    const uint64_t blocks = static_cast<uint64_t>(p.sfb_group_bytes / (128 * p.S)) *
+                            static_cast<uint64_t>(p.gs.groups);
+    const uint64_t dims[3] = {128, atoms_total, blocks};
+    const uint64_t strides[2] = {512, atoms_total * 512};
+    const uint32_t box[3] = {128, static_cast<uint32_t>(C::ATOMS), static_cast<uint32_t>(C::RB)};
+    int rc = encode_tensor_map(&tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint8_t*>(p.sfb), dims,
+                               strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (rc != HQ_OK) return rc;
   }
   auto kern = bs_gemm_2sm_kernel<MODE, STAGES, EPI, BN>;
@@ -1845,7 +1875,7 @@ int run_bs_2sm(const void* a, const void* b, const GemmParams& p, int sm_count, 
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmB64, tmSFB, p);
   return e == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
 }
 

@@ -94,24 +94,6 @@ struct DsParams {
   int32_t* w_ok;          // [L]
 };
 
-__device__ __forceinline__ float rcp_approx(float x) {
-  float r;
-  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
-  return r;
-}
-// sigmoid of a pair, 1 / (1 + 2^(-x log2 e)): the product in one f32x2
-// multiply, the hardware base-2 exponential and approximate reciprocal (the
-// error of a fast exponential, far inside D_row's BF16 rounding)
-__device__ __forceinline__ void sigmoid_x2(float x0, float x1, float& s0, float& s1) {
-  constexpr float kNegLog2e = -1.44269502162933349609375f;  // -log2(e) rounded to float
-  float t0, t1, e0, e1, d0, d1;
-  mul_f32x2(t0, t1, x0, x1, kNegLog2e);
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(t0));
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(t1));
-  add_f32x2(d0, d1, e0, e1, 1.0f, 1.0f);
-  s0 = rcp_approx(d0);
-  s1 = rcp_approx(d1);
-}
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

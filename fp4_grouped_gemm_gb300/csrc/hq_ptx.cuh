@@ -443,6 +443,32 @@ __device__ __forceinline__ void fma_f32x2(float& o0, float& o1, float a0, float 
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 
+// Hardware approximations: the reciprocal (within 1 ulp) and the base-2
+// exponential (flushing subnormals).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ float ex2_approx_ftz(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// sigmoid of a pair, 1 / (1 + 2^(-x log2 e)): the product in one f32x2
+// multiply, the hardware base-2 exponential and approximate reciprocal (the
+// error of a fast exponential, far inside a BF16 or FP8 rounding of the
+// dGLU outputs it feeds)
+__device__ __forceinline__ void sigmoid_x2(float x0, float x1, float& s0, float& s1) {
+  constexpr float kNegLog2e = -1.44269502162933349609375f;  // -log2(e) rounded to float
+  float t0, t1, d0, d1;
+  mul_f32x2(t0, t1, x0, x1, kNegLog2e);
+  add_f32x2(d0, d1, ex2_approx_ftz(t0), ex2_approx_ftz(t1), 1.0f, 1.0f);
+  s0 = rcp_approx(d0);
+  s1 = rcp_approx(d1);
+}
+
 // Two floats -> two E4M3 bytes: `hi` in bits 15..8, `lo` in bits 7..0.
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
   uint16_t r;

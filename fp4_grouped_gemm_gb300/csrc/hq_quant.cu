@@ -73,12 +73,6 @@ __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t s, int64_t S, in
   return ((r >> 7) * (S >> 2) + (s >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (s & 3);
 }
 
-__device__ __forceinline__ float rcp_approx(float x) {
-  float r;
-  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
-  return r;
-}
-
 // exp(-a) for two values without a library call: with t = -a log2(e) split
 // as t_hi = fl(-a * L) (L = log2(e) rounded to float) plus r, where the FMA
 // residual fma(-a, L, -t_hi) recovers the product's rounding error exactly
@@ -89,11 +83,6 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // normal).  The error is that of ex2.approx plus about 2^-23, independent of
 // |a|: a product fl(-a * L) alone would add |a| 2^-24.  2^t_hi = inf (a <
 // -88.7) stays inf and 0 stays 0: the correction factor is positive.
-__device__ __forceinline__ float ex2_approx_ftz(float x) {
-  float r;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-  return r;
-}
 __device__ __forceinline__ void exp_neg_x2(float a0, float a1, float& e0, float& e1) {
   constexpr float kL2E = 1.44269502162933349609375f;  // log2(e) rounded to float
   constexpr float kL2ELo = 1.925963033500011e-08f;    // log2(e) - kL2E
