@@ -289,42 +289,28 @@ __device__ __forceinline__ void epilogue_tile(const EpiArgs& e, Release release)
 }
 
 // Wide pair tile (384 columns): the warp drains tile columns [cw, cw + 128)
-// of the first 256 into registers as epilogue_tile does, converts and stores
-// its 64 columns [256 + cw2, 256 + cw2 + 64) of the last 128 straight from
-// TMEM (16 at a time), then releases the accumulator and stores the drained
-// part.
+// of the first 256 and its 64 columns [256 + cw2, 256 + cw2 + 64) of the
+// last 128 into registers (converted to BF16 while the next piece is read),
+// releases the accumulator, then stores both parts.
 template <typename Release>
 __device__ __forceinline__ void epilogue_tile_wide(const EpiArgs& e, int cw2, Release release) {
-  constexpr int kPieces = 8;
+  constexpr int kPieces = 12;  // 8 of the first 256 columns, 4 of the last 128
+  auto piece_col = [&](int s) { return s < 8 ? e.cw + s * 16 : 256 + cw2 + (s - 8) * 16; };
   uint32_t packed[kPieces * 8];
-  {
-    uint32_t r[2][16];
-    tmem_ld_32x32b_x16(e.acc_t + e.cw, r[0]);
-    tmem_ld_wait(r[0]);
 #pragma unroll
-    for (int s = 0; s < kPieces; ++s) {
-      if (s + 1 < kPieces) tmem_ld_32x32b_x16(e.acc_t + e.cw + (s + 1) * 16, r[(s + 1) & 1]);
-      const int64_t col0 = e.n0 + e.cw + s * 16;
-      if (col0 < e.n) epi_convert16(e, col0, r[s & 1], packed + 8 * s);
-      if (s + 1 < kPieces) tmem_ld_wait(r[(s + 1) & 1]);
-    }
-  }
-#pragma unroll 1
-  for (int s = 0; s < 4; ++s) {
-    uint32_t r[16], pk[8];
-    tmem_ld_32x32b_x16(e.acc_t + 256 + cw2 + s * 16, r);
+  for (int s = 0; s < kPieces; ++s) {
+    uint32_t r[16];
+    tmem_ld_32x32b_x16(e.acc_t + piece_col(s), r);
     tmem_ld_wait(r);
-    const int64_t col0 = e.n0 + 256 + cw2 + s * 16;
-    if (col0 >= e.n) continue;
-    epi_convert16(e, col0, r, pk);
-    epi_store16(e, col0, pk);
+    const int64_t col0 = e.n0 + piece_col(s);
+    if (col0 < e.n) epi_convert16(e, col0, r, packed + 8 * s);
   }
   tc_fence_before();
   __syncwarp();
   release();
 #pragma unroll
   for (int s = 0; s < kPieces; ++s) {
-    const int64_t col0 = e.n0 + e.cw + s * 16;
+    const int64_t col0 = e.n0 + piece_col(s);
     if (col0 < e.n) epi_store16(e, col0, packed + 8 * s);
   }
 }
