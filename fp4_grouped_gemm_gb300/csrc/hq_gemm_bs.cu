@@ -39,17 +39,21 @@
 namespace hq {
 namespace {
 
-// How scale atoms reach TMEM:
-//   0  the MMA thread issues tcgen05.cp (32x128b.warpx4) before its MMAs;
+// How scale atoms reach TMEM (the SFP parameter of the single-SM kernel):
+//   0  the MMA thread issues tcgen05.cp (32x128b.warpx4) before its MMAs:
+//      no scale warps, so the CTA's ten warps may hold 168 registers each
+//      (the tensor pipe spends time on the copies);
 //   1  a dedicated warp issues the tcgen05.cp and signals the MMA thread;
 //   2  four scale warps (one per TMEM lane quarter) read the atoms from shared
 //      memory and write them with tcgen05.st, replicated into every quarter
-//      exactly as the warpx4 copy would, then signal the MMA thread.
+//      exactly as the warpx4 copy would, then signal the MMA thread (the
+//      default; the 2-SM kernel always stages this way).
 constexpr int kSfPath = 2;
-constexpr int kSfWarps = kSfPath == 1 ? 1 : (kSfPath == 2 ? 4 : 0);
+constexpr int sf_warps(int path) { return path == 1 ? 1 : (path == 2 ? 4 : 0); }
 constexpr int kEpiWarps = 8;             // warps 2..9: two per TMEM lane quarter
 constexpr int kSfWarp0 = 2 + kEpiWarps;  // first scale-staging warp
-constexpr int kThreads = 32 * (kSfWarp0 + kSfWarps);
+constexpr int threads_for(int path) { return 32 * (kSfWarp0 + sf_warps(path)); }
+constexpr int kThreads = threads_for(kSfPath);
 constexpr int kBKBytes = 128;   // bytes of K per stage and row (one 128B swizzle span)
 constexpr int kMmaKBytes = 32;  // bytes of K consumed by one MMA
 constexpr int kSmemLimit = 232448;
@@ -673,8 +677,8 @@ __device__ __forceinline__ void swiglu_store(const GemmParams& p, const float (&
 
 // tmC / tmD: the dGLU epilogues' C and D_row segment maps (other epilogues
 // get unused placeholders)
-template <int MODE, int BN, int STAGES, int ACC, int TABLE, int EPI = kEpiGemm>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int MODE, int BN, int STAGES, int ACC, int TABLE, int EPI = kEpiGemm, int SFP = kSfPath>
+__global__ void __launch_bounds__(threads_for(SFP), 1)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                    const GemmParams p) {
@@ -715,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(drain_bar, 1);
     mbar_init(drain_sf_bar, 1);
-    for (int s = 0; s < STAGES; ++s) mbar_init(sfready_bar(s), kSfPath == 2 ? 4 : 1);
+    for (int s = 0; s < STAGES; ++s) mbar_init(sfready_bar(s), SFP == 2 ? 4 : 1);
     for (int w = 0; w < kEpiWarps; ++w) mbar_init(cbar0 + 8u * w, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
@@ -849,16 +853,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         for (int kb = 0; kb < num_kb; ++kb) {
-          // kSfPath 0: this thread stages the scales; otherwise the scale
+          // SFP 0: this thread stages the scales; otherwise the scale
           // warp(s) signal sfready after the stage's scales are in TMEM
-          const uint32_t ready = kSfPath == 0 ? full_bar(stage) : sfready_bar(stage);
+          const uint32_t ready = SFP == 0 ? full_bar(stage) : sfready_bar(stage);
           if (!wait_bounded(ready, phase, wctx)) { ok = false; break; }
           tc_fence_after();
           int atoms = atoms_total - kb * C::ATOMS;
           atoms = atoms < C::ATOMS ? atoms : C::ATOMS;
           const uint32_t sfa_t = tmem_base + C::SF_BASE_COL + stage * C::SF_STAGE_COLS;
           const uint32_t sfb_t = sfa_t + C::SFA_COLS;
-          if (kSfPath == 0) {
+          if (SFP == 0) {
             const uint32_t sfa_s = sbase + C::OFF_SFA + stage * C::SFA_BYTES;
             const uint32_t sfb_s = sbase + C::OFF_SFB + stage * C::SFB_BYTES;
             for (int a = 0; a < atoms; ++a) {
@@ -928,7 +932,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sfb_t = sfa_t + C::SFA_COLS;
         const uint32_t sfa_s = sbase + C::OFF_SFA + stage * C::SFA_BYTES;
         const uint32_t sfb_s = sbase + C::OFF_SFB + stage * C::SFB_BYTES;
-        if (kSfPath == 1) {
+        if (SFP == 1) {
           if (lane == 0) {
             ok = wait_bounded(full_bar(stage), phase, wctx);
             if (ok) {
@@ -987,7 +991,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }
-    if (kSfPath == 1 && lane == 0) {
+    if (SFP == 1 && lane == 0) {
       tc_commit(drain_sf_bar);
       wait_drain(drain_sf_bar, 0, p.wait_limit_ns);
     }
@@ -1262,7 +1266,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(EPI == kEpiGemm || kUpProj, "2-SM epilogues: plain GEMM or fused up-proj");
   static_assert(!(kWide && kUpProj), "the fused up-proj uses 256-column pair tiles");
   constexpr int TW = kUpProj ? C::BN / 2 : C::BN;  // output columns per tile
-  static_assert(kSfPath == 2, "the 2-SM kernel stages scales with tcgen05.st");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -1702,7 +1705,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // host side
 // ---------------------------------------------------------------------------
 
-template <int MODE, int BN, int STAGES, int ACC, int TABLE, int EPI = kEpiGemm>
+template <int MODE, int BN, int STAGES, int ACC, int TABLE, int EPI = kEpiGemm, int SFP = kSfPath>
 int run_bs(const void* a, const void* b, const GemmParams& p0, int sm_count, bool pdl,
            cudaStream_t st) {
   constexpr bool kDglu = EPI == kEpiDSwiGLU || EPI == kEpiDGeGLU;
@@ -1764,8 +1767,8 @@ int run_bs(const void* a, const void* b, const GemmParams& p0, int sm_count, boo
       p.d_tma = 2;
     }
   }
-  auto kern = bs_gemm_kernel<MODE, BN, STAGES, ACC, TABLE, EPI>;
-  if (set_smem_once<bs_gemm_kernel<MODE, BN, STAGES, ACC, TABLE, EPI>>(C::SMEM_BYTES) != HQ_OK)
+  auto kern = bs_gemm_kernel<MODE, BN, STAGES, ACC, TABLE, EPI, SFP>;
+  if (set_smem_once<bs_gemm_kernel<MODE, BN, STAGES, ACC, TABLE, EPI, SFP>>(C::SMEM_BYTES) != HQ_OK)
     return HQ_ERR_CUDA;
   const int sms = num_sms();
   if (sms <= 0) return HQ_ERR_CUDA;
@@ -1780,7 +1783,7 @@ int run_bs(const void* a, const void* b, const GemmParams& p0, int sm_count, boo
   if (grid > sms) grid = sms;
   if (grid > tiles_bound) grid = tiles_bound;
   if (grid < 1) grid = 1;
-  cudaError_t e = launch(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), C::SMEM_BYTES, st,
+  cudaError_t e = launch(kern, dim3(static_cast<unsigned>(grid)), dim3(threads_for(SFP)), C::SMEM_BYTES, st,
                          pdl, tmA, tmB, tmC, tmD, p);
   return e == cudaSuccess ? HQ_OK : HQ_ERR_CUDA;
 }
@@ -2189,8 +2192,14 @@ int dglu_bs_impl(const void* a, const uint8_t* sfa, const void* b, const uint8_t
   constexpr int T = kMaxGroups + 1;
   int rc;
   if (mode == HQ_MXFP8)
-    rc = act == 0 ? run_bs<HQ_MXFP8, 128, 5, 2, T, kEpiDSwiGLU>(a, b, p, sm_count, pdl, st)
-                  : run_bs<HQ_MXFP8, 128, 5, 2, T, kEpiDGeGLU>(a, b, p, sm_count, pdl, st);
+    // MXFP8 with dbias: the MMA thread copies the scales (two atoms per
+    // k-block), so the epilogue's column sums get 168 registers instead of 128
+    if (dbias)
+      rc = act == 0 ? run_bs<HQ_MXFP8, 128, 5, 2, T, kEpiDSwiGLU, 0>(a, b, p, sm_count, pdl, st)
+                    : run_bs<HQ_MXFP8, 128, 5, 2, T, kEpiDGeGLU, 0>(a, b, p, sm_count, pdl, st);
+    else
+      rc = act == 0 ? run_bs<HQ_MXFP8, 128, 5, 2, T, kEpiDSwiGLU>(a, b, p, sm_count, pdl, st)
+                    : run_bs<HQ_MXFP8, 128, 5, 2, T, kEpiDGeGLU>(a, b, p, sm_count, pdl, st);
   else if (mode == HQ_MXFP4)
     rc = act == 0 ? run_bs<HQ_MXFP4, 128, 5, 2, T, kEpiDSwiGLU>(a, b, p, sm_count, pdl, st)
                   : run_bs<HQ_MXFP4, 128, 5, 2, T, kEpiDGeGLU>(a, b, p, sm_count, pdl, st);
