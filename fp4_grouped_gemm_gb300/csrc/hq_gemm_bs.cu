@@ -1576,22 +1576,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool w = wait_bounded(sffull_bar(stage), phase, wctx);
         ok = __all_sync(0xFFFFFFFFu, w);
         if (!ok) break;
-        if (C::SF_SLOTS < STAGES && kbi >= C::SF_SLOTS) {
-          // the TMEM scale slot is shared with k-block kbi - SF_SLOTS: its
-          // MMAs (committed to that stage's empty barrier) must be done
-          const int64_t j = kbi - C::SF_SLOTS;
-          const bool we = wait_bounded(empty_bar(static_cast<int>(j % STAGES)),
-                                       static_cast<uint32_t>(j / STAGES) & 1u, wctx);
-          ok = __all_sync(0xFFFFFFFFu, we);
-          if (!ok) break;
-          tc_fence_after();
-        }
         const int slot = stage % C::SF_SLOTS;
         const uint32_t sfa_t = tmem_base + C::SF_BASE_COL + slot * C::SF_STAGE_COLS;
         const uint32_t sfb_t = sfa_t + C::SFA_COLS;
         const uint32_t sfb2_t = sfb_t + C::ATOMS * 8;
         const uint32_t sfa_s = sbase + C::OFF_SFA + stage * C::SFA_BYTES;
         const uint32_t sfb_s = sbase + C::OFF_SFB + stage * C::SFB_BYTES;
+        // the TMEM scale slot is shared with k-block kbi - SF_SLOTS: its MMAs
+        // (committed to that stage's empty barrier) must be done before the
+        // slot is written; the stage's atoms are read from shared memory
+        // first, so only the TMEM writes wait
+        auto wait_slot = [&]() -> bool {
+          if (C::SF_SLOTS < STAGES && kbi >= C::SF_SLOTS) {
+            const int64_t j = kbi - C::SF_SLOTS;
+            const bool we = wait_bounded(empty_bar(static_cast<int>(j % STAGES)),
+                                         static_cast<uint32_t>(j / STAGES) & 1u, wctx);
+            if (!__all_sync(0xFFFFFFFFu, we)) return false;
+            tc_fence_after();
+          }
+          return true;
+        };
         // B scales at columns sfb_t + (a * 2 + rb) * 4 (k-atom a, 128-row
         // block rb = 0, 1) and, for the wide tile, sfb2_t + a * 4 (block 2)
         if (atoms == C::ATOMS) {
@@ -1605,10 +1609,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               lds128(sfb_s + (rb * C::ATOMS + a) * 512 + lane * 16, vb + 4 * (a * 2 + rb));
             if (kWide) lds128(sfb_s + (2 * C::ATOMS + a) * 512 + lane * 16, vb2 + 4 * a);
           }
+          if (!wait_slot()) { ok = false; break; }
           tmem_st_32x32b<NA>(lq + sfa_t, va);
           tmem_st_32x32b<2 * NA>(lq + sfb_t, vb);
           if (kWide) tmem_st_32x32b<NA>(lq + sfb2_t, vb2);
         } else {
+          if (!wait_slot()) { ok = false; break; }
           for (int a = 0; a < atoms; ++a) {
             uint32_t v[4];
             lds128(sfa_s + a * 512 + lane * 16, v);
