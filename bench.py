@@ -618,9 +618,9 @@ class Extras:
         fn = lambda: hq.hq_prefill_permute(xf, sc, ids, E, cap, permute_x=px, out_scale=osf,  # noqa: E731
                                            indice_map=imap, token_nums=tn, workspace=ws)
         t = time_kernel(fn, 20, self.flush)
-        # algorithmic bytes: each routed row read once per slot and written once,
-        # scales likewise, ids read, map written
-        byts = T * topk * (2 * hidden + 2 * hidden // 32) + T * topk * (8 + 4)
+        # algorithmic bytes: each token's row and scales read once, written
+        # once per routed slot; ids read, map written
+        byts = T * (hidden + hidden // 32) + T * topk * (hidden + hidden // 32) + T * topk * (8 + 4)
         return {"permute_fp8_T8192_top8_E32_h7168": {"us": t * 1e6, "gbs": byts / t / 1e9,
                                                      "frac_hbm": byts / t / 1e9 / self.hbm}}
 

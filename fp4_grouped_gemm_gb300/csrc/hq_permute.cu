@@ -4,17 +4,19 @@
 //
 // Three passes over blocks of kTok tokens, all deterministic:
 //   count    per block, a shared-memory histogram of its valid expert ids
-//            -> counts[block][e] (workspace);
-//   scan     one CTA: for every expert the exclusive prefix of the block
-//            counts -> base[block][e] (workspace), and
-//            token_nums[e] = min(total, max_token_num);
+//            -> counts[e][block] (workspace);
+//   scan     one warp per expert: the exclusive prefix of its block counts,
+//            32 blocks at a time with a warp scan -> base[e][block]
+//            (workspace), and token_nums[e] = min(total, max_token_num);
 //   scatter  per block, warp 0 ranks the block's (token, slot) entries in
 //            order -- 32 at a time with __match_any_sync, plus a running
 //            per-expert count in shared memory -- so every expert's rows are
-//            filled in increasing (token, slot) order; then every warp copies
-//            token rows with 16-byte loads and stores and writes the scale
-//            bytes into SfAtom positions, one 4-byte store per four scale
-//            columns (the four columns of an atom row are contiguous).
+//            filled in increasing (token, slot) order; then each warp takes
+//            whole tokens: it reads a token's row once with 16-byte loads and
+//            stores it to every destination row of the token's slots, and
+//            writes the scale bytes into SfAtom positions the same way, one
+//            4-byte store per four scale columns (the four columns of an
+//            atom row are contiguous).
 // An id outside [0, E) other than -1, or an entry that finds its expert full,
 // is dropped: its map entry is -1 and HQ_STATUS_ROUTING_DROPPED is set.  Rows
 // past token_nums[e] (data and scales) are not written.
@@ -43,8 +45,8 @@ struct PermuteParams {
   uint8_t* out_sf;           // SfAtom bytes of [E * cap, hidden / 32]
   int32_t* imap;             // [T, topk]
   int32_t* token_nums;       // [E]
-  int32_t* counts;           // [nblk, E] workspace
-  int32_t* base;             // [nblk, E] workspace
+  int32_t* counts;           // [E, nblk] workspace
+  int32_t* base;             // [E, nblk] workspace
   int nblk;
   uint32_t* status;
 };
@@ -63,17 +65,31 @@ __global__ void __launch_bounds__(kThreads) permute_count(const PermuteParams p)
   }
   __syncthreads();
   for (int i = threadIdx.x; i < p.E; i += blockDim.x)
-    p.counts[static_cast<int64_t>(blockIdx.x) * p.E + i] = hist[i];
+    p.counts[static_cast<int64_t>(i) * p.nblk + blockIdx.x] = hist[i];
 }
 
+// One warp per expert (32 experts per CTA of 1024 threads).
 __global__ void __launch_bounds__(1024) permute_scan(const PermuteParams p) {
-  for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
-    int64_t run = 0;
-    for (int b = 0; b < p.nblk; ++b) {
-      const int64_t i = static_cast<int64_t>(b) * p.E + e;
-      p.base[i] = static_cast<int32_t>(run < p.cap ? run : p.cap);
-      run += p.counts[i];
+  const int lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 32 + (threadIdx.x >> 5);
+  if (e >= p.E) return;
+  const int32_t* cnt = p.counts + static_cast<int64_t>(e) * p.nblk;
+  int32_t* base = p.base + static_cast<int64_t>(e) * p.nblk;
+  int64_t run = 0;
+  for (int b0 = 0; b0 < p.nblk; b0 += 32) {
+    const int b = b0 + lane;
+    const int32_t c = b < p.nblk ? cnt[b] : 0;
+    int32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += u;
     }
+    const int64_t excl = run + incl - c;
+    if (b < p.nblk) base[b] = static_cast<int32_t>(excl < p.cap ? excl : p.cap);
+    run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+  }
+  if (lane == 0) {
     p.token_nums[e] = static_cast<int32_t>(run < p.cap ? run : p.cap);
     if (run > p.cap) atomicOr(p.status, HQ_STATUS_ROUTING_DROPPED);
   }
@@ -87,7 +103,7 @@ __global__ void __launch_bounds__(kThreads) permute_scatter(const PermuteParams 
   const int64_t ntok = p.T - t0 < kTok ? p.T - t0 : kTok;
   const int entries = static_cast<int>(ntok) * p.topk;
   for (int i = threadIdx.x; i < p.E; i += blockDim.x)
-    running[i] = p.base[static_cast<int64_t>(blockIdx.x) * p.E + i];
+    running[i] = p.base[static_cast<int64_t>(i) * p.nblk + blockIdx.x];
   __syncthreads();
   if (warp == 0) {
     // rank the entries in (token, slot) order, 32 at a time
@@ -120,31 +136,42 @@ __global__ void __launch_bounds__(kThreads) permute_scatter(const PermuteParams 
     if (__any_sync(0xFFFFFFFFu, dropped) && lane == 0) atomicOr(p.status, HQ_STATUS_ROUTING_DROPPED);
   }
   __syncthreads();
-  // copy rows: one warp per entry
+  // copy rows: one warp per token, its row read once and stored to each of
+  // its destination rows
   const int64_t row_bytes = p.hidden * p.elem_bytes;
   const int nvec = static_cast<int>(row_bytes / 16);
   const int64_t S = p.hidden / 32;       // scale columns
   const int words = static_cast<int>(S / 4);
   const int nwarps = blockDim.x >> 5;
-  for (int j = warp; j < entries; j += nwarps) {
-    const int32_t d = dest[j];
-    if (d < 0) continue;
-    // debug builds: the destination row lies inside the [E * cap] output
-    if (!in_bounds(d < static_cast<int64_t>(p.E) * p.cap, p.status)) continue;
-    const int64_t t = t0 + j / p.topk;
+  const int64_t rows_out = static_cast<int64_t>(p.E) * p.cap;
+  for (int tt = warp; tt < ntok; tt += nwarps) {
+    const int32_t* dt = dest + tt * p.topk;
+    const int64_t t = t0 + tt;
     const uint4* src = reinterpret_cast<const uint4*>(p.x + t * row_bytes);
-    uint4* dst = reinterpret_cast<uint4*>(p.out_x + static_cast<int64_t>(d) * row_bytes);
+    // debug builds: every destination row lies inside the [E * cap] output
+    auto dst_ok = [&](int32_t d) { return d >= 0 && in_bounds(d < rows_out, p.status); };
     int v = lane;
     for (; v + 96 < nvec; v += 128) {  // four 16-byte loads in flight per lane
       const uint4 a = __ldg(src + v), b = __ldg(src + v + 32), c = __ldg(src + v + 64),
                   e = __ldg(src + v + 96);
-      dst[v] = a;
-      dst[v + 32] = b;
-      dst[v + 64] = c;
-      dst[v + 96] = e;
+      for (int k = 0; k < p.topk; ++k) {
+        const int32_t d = dt[k];
+        if (!dst_ok(d)) continue;
+        uint4* dst = reinterpret_cast<uint4*>(p.out_x + static_cast<int64_t>(d) * row_bytes);
+        dst[v] = a;
+        dst[v + 32] = b;
+        dst[v + 64] = c;
+        dst[v + 96] = e;
+      }
     }
-    for (; v < nvec; v += 32) dst[v] = __ldg(src + v);
-    const int64_t r = d;
+    for (; v < nvec; v += 32) {
+      const uint4 a = __ldg(src + v);
+      for (int k = 0; k < p.topk; ++k) {
+        const int32_t d = dt[k];
+        if (!dst_ok(d)) continue;
+        reinterpret_cast<uint4*>(p.out_x + static_cast<int64_t>(d) * row_bytes)[v] = a;
+      }
+    }
     for (int w = lane; w < words; w += 32) {
       uint32_t word;
       if (p.broadcast) {
@@ -154,8 +181,13 @@ __global__ void __launch_bounds__(kThreads) permute_scatter(const PermuteParams 
       } else {
         word = __ldg(reinterpret_cast<const uint32_t*>(p.scale + t * S) + w);
       }
-      const int64_t off = ((r >> 7) * (S >> 2) + w) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
-      *reinterpret_cast<uint32_t*>(p.out_sf + off) = word;
+      for (int k = 0; k < p.topk; ++k) {
+        const int32_t d = dt[k];
+        if (!dst_ok(d)) continue;
+        const int64_t r = d;
+        const int64_t off = ((r >> 7) * (S >> 2) + w) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4;
+        *reinterpret_cast<uint32_t*>(p.out_sf + off) = word;
+      }
     }
   }
 }
@@ -222,7 +254,7 @@ int hq_prefill_permute(const void* x, int elem_bytes, const void* scale, int sca
     hq::permute_count<<<p.nblk, hq::kThreads, 0, st>>>(p);
     if (cudaGetLastError() != cudaSuccess) return HQ_ERR_CUDA;
   }
-  hq::permute_scan<<<1, 1024, 0, st>>>(p);
+  hq::permute_scan<<<(num_experts + 31) / 32, 1024, 0, st>>>(p);
   if (cudaGetLastError() != cudaSuccess) return HQ_ERR_CUDA;
   if (p.nblk > 0) {
     hq::permute_scatter<<<p.nblk, hq::kThreads, 0, st>>>(p);
