@@ -29,8 +29,8 @@
 namespace hq {
 namespace {
 
-constexpr int kTok = 32;       // tokens per block (small blocks: many CTAs copy in parallel)
-constexpr int kThreads = 512;
+constexpr int kTok = 16;             // tokens per block (small blocks: many CTAs copy in parallel)
+constexpr int kThreads = 32 * kTok;  // the scatter copies one token per warp
 constexpr int kMaxTopk = 32;
 constexpr int kMaxExperts = 1024;
 
@@ -76,18 +76,28 @@ __global__ void __launch_bounds__(1024) permute_scan(const PermuteParams p) {
   const int32_t* cnt = p.counts + static_cast<int64_t>(e) * p.nblk;
   int32_t* base = p.base + static_cast<int64_t>(e) * p.nblk;
   int64_t run = 0;
-  for (int b0 = 0; b0 < p.nblk; b0 += 32) {
-    const int b = b0 + lane;
-    const int32_t c = b < p.nblk ? cnt[b] : 0;
-    int32_t incl = c;
+  constexpr int kBatch = 8;  // 32-block chunks whose counts are loaded before any is scanned
+  for (int c0 = 0; c0 < p.nblk; c0 += 32 * kBatch) {
+    int32_t cs[kBatch];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += u;
+    for (int i = 0; i < kBatch; ++i) {
+      const int b = c0 + 32 * i + lane;
+      cs[i] = b < p.nblk ? cnt[b] : 0;
     }
-    const int64_t excl = run + incl - c;
-    if (b < p.nblk) base[b] = static_cast<int32_t>(excl < p.cap ? excl : p.cap);
-    run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int b = c0 + 32 * i + lane;
+      const int32_t c = cs[i];
+      int32_t incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += u;
+      }
+      const int64_t excl = run + incl - c;
+      if (b < p.nblk) base[b] = static_cast<int32_t>(excl < p.cap ? excl : p.cap);
+      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
   }
   if (lane == 0) {
     p.token_nums[e] = static_cast<int32_t>(run < p.cap ? run : p.cap);
