@@ -51,7 +51,11 @@ struct PermuteParams {
   uint32_t* status;
 };
 
+// The scan and the scatter are launched as programmatic dependents of the
+// pass before them: each lets its dependent start launching at once and the
+// dependent waits (griddepcontrol.wait) for its results before reading them.
 __global__ void __launch_bounds__(kThreads) permute_count(const PermuteParams p) {
+  pdl_launch_dependents();
   __shared__ int32_t hist[kMaxExperts];
   for (int i = threadIdx.x; i < p.E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
@@ -70,6 +74,8 @@ __global__ void __launch_bounds__(kThreads) permute_count(const PermuteParams p)
 
 // One warp per expert (32 experts per CTA of 1024 threads).
 __global__ void __launch_bounds__(1024) permute_scan(const PermuteParams p) {
+  pdl_launch_dependents();
+  pdl_wait();  // the block counts
   const int lane = threadIdx.x & 31;
   const int e = blockIdx.x * 32 + (threadIdx.x >> 5);
   if (e >= p.E) return;
@@ -112,6 +118,7 @@ __global__ void __launch_bounds__(kThreads) permute_scatter(const PermuteParams 
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTok;
   const int64_t ntok = p.T - t0 < kTok ? p.T - t0 : kTok;
   const int entries = static_cast<int>(ntok) * p.topk;
+  pdl_wait();  // the block bases
   for (int i = threadIdx.x; i < p.E; i += blockDim.x)
     running[i] = p.base[static_cast<int64_t>(i) * p.nblk + blockIdx.x];
   __syncthreads();
@@ -264,12 +271,11 @@ int hq_prefill_permute(const void* x, int elem_bytes, const void* scale, int sca
     hq::permute_count<<<p.nblk, hq::kThreads, 0, st>>>(p);
     if (cudaGetLastError() != cudaSuccess) return HQ_ERR_CUDA;
   }
-  hq::permute_scan<<<(num_experts + 31) / 32, 1024, 0, st>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return HQ_ERR_CUDA;
-  if (p.nblk > 0) {
-    hq::permute_scatter<<<p.nblk, hq::kThreads, 0, st>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return HQ_ERR_CUDA;
-  }
+  if (hq::launch(hq::permute_scan, dim3((num_experts + 31) / 32), dim3(1024), 0, st, p.nblk > 0, p) != cudaSuccess)
+    return HQ_ERR_CUDA;
+  if (p.nblk > 0 &&
+      hq::launch(hq::permute_scatter, dim3(p.nblk), dim3(hq::kThreads), 0, st, true, p) != cudaSuccess)
+    return HQ_ERR_CUDA;
   return HQ_OK;
 }
 
