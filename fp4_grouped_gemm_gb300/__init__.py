@@ -59,12 +59,13 @@ def group_size(mode):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # a plain int (or None): the c_void_p argument types convert it
+    return None if t is None else t.data_ptr()
 
 
 def _stream(stream):
     s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    return s.cuda_stream
 
 
 def sf_bytes(rows, k, mode):
