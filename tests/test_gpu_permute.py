@@ -73,6 +73,12 @@ def test_permute_one_token_many_slots_and_ragged_block(cuda_dev):
     run_case(129, 8, 3, 512, 512, 2, "broadcast", seed=4, ids=ids)
 
 
+def test_permute_max_topk_and_many_experts(cuda_dev):
+    # topk 32 (the largest accepted) over 1000 experts: each block ranks 32
+    # slots per token, the prefix runs over 32 CTAs of expert warps
+    run_case(40, 32, 1000, 512, 128, 1, "direct", seed=9)
+
+
 def test_permute_overflow_and_bad_ids_are_dropped(cuda_dev):
     ids = np.zeros((300, 1), np.int64)
     ids[7, 0] = 40                               # out of range
