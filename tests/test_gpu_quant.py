@@ -196,3 +196,41 @@ def test_quant_masked_many_experts(cuda_dev):
     assert np.array_equal(q_gpu[rows], q_ref), "valid rows' codes"
     assert np.array_equal(sf_gpu[rows], sf_ref.reshape(len(rows), S)), "valid rows' scale bytes"
     assert (q_gpu[~valid] == 0xAA).all() and (sf_gpu[~valid] == 0xAA).all(), "rows past masked_m written"
+
+
+def test_quant_masked_full_size_sampled(cuda_dev):
+    """hq_quant_masked on the grouped-masked MoE workload (E = 32 experts of
+    512 rows, K = 7168, counts ~ U{0..512}): sampled valid rows (each
+    expert's first and last valid row and a random one) match the oracle bit
+    for bit, and the first row past each expert's count is untouched."""
+    cfg = synth.moe_masked(device="cuda")
+    E, max_m, k = cfg["E"], cfg["max_m"], cfg["k"]
+    counts = cfg["masked_m"]
+    a = cfg["a"]
+    q = torch.full((E * max_m, k // 2), 0xAA, dtype=torch.uint8, device="cuda")
+    sf = torch.full((hq.sf_bytes(E * max_m, k, "nvfp4"),), 0xAA, dtype=torch.uint8, device="cuda")
+    mm = torch.from_numpy(counts).to("cuda")
+    hq.get_device_status(clear=True)
+    hq.hq_quant_masked(a, mm, max_m, "nvfp4", q_out=q, sf_out=sf)
+    torch.cuda.synchronize()
+    status, _ = hq.get_device_status(clear=True)
+    assert status == 0
+    rng = np.random.default_rng(11)
+    valid, past = [], []
+    for e, c in enumerate(counts):
+        c = int(c)
+        if c > 0:
+            valid += sorted({e * max_m, e * max_m + c - 1, e * max_m + int(rng.integers(0, c))})
+        if c < max_m:
+            past.append(e * max_m + c)
+    valid, past = np.asarray(valid), np.asarray(past)
+    x_rows = a[torch.from_numpy(valid).to("cuda")].cpu()
+    q_ref, sf_ref = oquant.quantize(np_f32(x_rows), "nvfp4", None)
+    assert np.array_equal(q[torch.from_numpy(valid).to("cuda")].cpu().numpy(), q_ref)
+    S = k // 16
+    sf_gpu = sf.cpu().numpy()
+    rr, ss = np.meshgrid(valid, np.arange(S), indexing="ij")
+    assert np.array_equal(sf_gpu[oquant.sfatom_offset(rr, ss, S)], sf_ref)
+    assert (q[torch.from_numpy(past).to("cuda")].cpu().numpy() == 0xAA).all()
+    rp, sp = np.meshgrid(past, np.arange(S), indexing="ij")
+    assert (sf_gpu[oquant.sfatom_offset(rp, sp, S)] == 0xAA).all()
