@@ -134,7 +134,10 @@ size_t hq_sf_bytes(int64_t rows, int64_t k, hq_mode mode);
 int hq_get_device_status(uint32_t *out, int clear, hq_stream_t s);
 
 /* Limit of every bounded pipeline wait inside the kernels, in nanoseconds
- * (default 1e9).  Applies to launches made after the call. */
+ * (default 1e9).  Applies to launches made after the call.  After a wait
+ * expires the kernel still waits for its copies in flight, each such drain
+ * wait bounded by the same limit, so an aborted launch can take several times
+ * the limit before it returns. */
 int hq_set_wait_limit_ns(uint64_t ns);
 
 /* Self-test of the bounded wait: launches one CTA that waits on a pipeline
